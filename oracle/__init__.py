@@ -1,0 +1,139 @@
+"""fp64 CPU oracle for the DeltaNet delta-rule recurrence -- TEST INFRASTRUCTURE.
+
+This package is not part of the product.  Only the tests, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import it.
+The product library never calls it, and it shares no code with the CUDA path.
+
+The arithmetic lives in ``deltanet_oracle.c`` (plain C, fp64, OpenMP over the
+independent (batch, head) pairs).  This module only compiles it with gcc and
+passes numpy arrays to it.  The recurrence, per (b, h), token by token:
+
+    p_t = S_{t-1} k_t;  u_t = beta_t (v_t - p_t);  S_t = S_{t-1} + u_t k_t^T;
+    o_t = S_t q_t
+
+is the error-correcting delta rule of "DeltaNet 引入 Delta Rule"
+(garden.houmin.site/infra/delta-net) and of "DeltaNet : écrire l'erreur de
+prédiction plutôt que la valeur" (fr.news.hada.io/topic?id=31925), reading
+after writing as "Calcul de toutes les sorties internes au chunk" on the same
+page states.
+
+Layouts follow the library's: q, k ``[B, H, T, dk]``; v, o ``[B, H, T, dv]``;
+beta ``[B, H, T]``; state ``[B, H, dk, dv]`` (the pages' dv x dk state stored
+transposed, value channel contiguous).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` to closed
+forms, invariants and brute force that do not reuse this code.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from pathlib import Path
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+_SRC = _HERE / "deltanet_oracle.c"
+_BUILD_DIR = _HERE / "_build"
+_LIB_PATH = _BUILD_DIR / "libdn_oracle.so"
+
+_lib = None
+
+
+def build(force: bool = False) -> Path:
+    """Compiles the C oracle with gcc (fp64, no FMA contraction, OpenMP)."""
+    if (not force and _LIB_PATH.exists()
+            and _LIB_PATH.stat().st_mtime >= _SRC.stat().st_mtime):
+        return _LIB_PATH
+    _BUILD_DIR.mkdir(exist_ok=True)
+    tmp = _BUILD_DIR / f"libdn_oracle.{os.getpid()}.so"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", str(_SRC), "-o", str(tmp)]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(str(_LIB_PATH))
+        dp = ctypes.POINTER(ctypes.c_double)
+        lib.dn_oracle_forward.argtypes = [dp, dp, dp, dp, dp, dp,
+                                          ctypes.c_long, ctypes.c_long,
+                                          ctypes.c_long, ctypes.c_long,
+                                          ctypes.c_int]
+        lib.dn_oracle_forward.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def host_cores() -> int:
+    """Cores this process may run on (the count the oracle uses by default)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover - non-Linux
+        return os.cpu_count() or 1
+
+
+def _f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # a torch tensor
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def forward(q, k, v, beta, S0=None, nthreads: int | None = None):
+    """Runs the recurrence over a whole sequence.
+
+    Args:
+      q, k: ``[B, H, T, dk]``; v: ``[B, H, T, dv]``; beta: ``[B, H, T]``.
+      S0: ``[B, H, dk, dv]`` initial state, or None for zeros.
+      nthreads: OpenMP threads (default: every core this process may use).
+
+    Returns ``(o, S_T)`` as fp64 numpy arrays, ``o`` ``[B, H, T, dv]`` and
+    ``S_T`` ``[B, H, dk, dv]``.  Inputs of any float dtype are widened to fp64
+    exactly, so bf16 inputs reach the oracle with the values the GPU sees.
+    """
+    q, k, v, beta = _f64(q), _f64(k), _f64(v), _f64(beta)
+    if q.ndim != 4 or k.shape != q.shape or v.ndim != 4:
+        raise ValueError("q, k must be [B,H,T,dk] and v [B,H,T,dv]")
+    B, H, T, dk = q.shape
+    dv = v.shape[3]
+    if v.shape[:3] != (B, H, T) or beta.shape != (B, H, T):
+        raise ValueError("v must be [B,H,T,dv] and beta [B,H,T]")
+    if S0 is None:
+        S = np.zeros((B, H, dk, dv), dtype=np.float64)
+    else:
+        S = _f64(S0).copy()
+        if S.shape != (B, H, dk, dv):
+            raise ValueError("S0 must be [B,H,dk,dv]")
+    o = np.zeros((B, H, T, dv), dtype=np.float64)
+    if B * H == 0 or T == 0:
+        return o, S
+    n = host_cores() if nthreads is None else int(nthreads)
+    rc = _load().dn_oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                   _ptr(S), _ptr(o), B * H, T, dk, dv, n)
+    if rc != 0:
+        raise MemoryError("oracle could not allocate its scratch vector")
+    return o, S
+
+
+def recurrent_step(q, k, v, beta, S, nthreads: int | None = None):
+    """One decoding step: the recurrence applied to a single token.
+
+    Args:
+      q, k: ``[B, H, dk]``; v: ``[B, H, dv]``; beta: ``[B, H]``;
+      S: ``[B, H, dk, dv]`` state before the step.
+
+    Returns ``(o, S_new)``: ``o`` ``[B, H, dv]`` and the state after the step.
+    """
+    q, k, v, beta = _f64(q), _f64(k), _f64(v), _f64(beta)
+    o, S_new = forward(q[:, :, None, :], k[:, :, None, :], v[:, :, None, :],
+                       beta[:, :, None], S, nthreads=nthreads)
+    return o[:, :, 0, :], S_new

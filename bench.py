@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Benchmark of the DeltaNet delta-rule operator on one GB300 (per rank).
+
+Headline (``value``): chunkwise forward tokens/s on the 1.3B-layer shape
+(B8 H16 T2048 dk=dv=128, C=64, bf16 I/O, fp32 state, zero initial state).
+One step = one ``dn_chunk_fwd`` over that batch.  Beside it, in the same
+run: the fused decoding step (B256 H16 dk=dv=128, fp32 state, bf16 inputs,
+beta in (0,2)) over 1024 chained steps with fresh inputs, reported as
+tokens/s and achieved HBM GB/s; the headline measured end to end through the
+public API from pinned host buffers; and the fp64 oracle on a bounded sample
+of the headline workload on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs the same per-GPU workload on its own GPU (the
+operator shards over independent (batch, head) pairs, no collective): weak
+scaling, ``value`` = all ranks' tokens / the slowest rank's time.  The
+reference arm (``--impl reference``) times the fp64 CPU oracle, rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "delta-rule chunk fwd tokens/s on 1 GB300 + % roofline; decode step HBM GB/s"
+HEADLINE = "layer1p3b_bf16"
+DECODE = "decode_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 2**20
+
+
+def chunk_flops_per_token_head(C, dk, dv):
+    """Algorithmic FLOPs of the chunkwise WY form per token and head, with the
+    triangular halves skipped: C(3dk + 2dv) + 6 dk dv + C^2/3."""
+    return C * (3 * dk + 2 * dv) + 6 * dk * dv + C * C / 3.0
+
+
+def chunk_bytes(B, H, T, dk, dv, esize, with_s0, with_st):
+    """Algorithmic HBM bytes of one chunk forward: q, k, v, beta read, o
+    written, plus the fp32 states read / written once per head."""
+    b = B * H * T * (2 * dk + 2 * dv + 1) * esize
+    b += B * H * dk * dv * 4 * (int(with_s0) + int(with_st))
+    return b
+
+
+def decode_bytes(B, H, dk, dv, esize):
+    """Algorithmic HBM bytes of one decoding step: the fp32 state read and
+    written once, q, k, v, beta read and o written."""
+    return B * H * (2 * dk * dv * 4 + (2 * dk + 2 * dv + 1) * esize)
+
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_traffic(name: str, source: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since it was captured."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None
+    entry = json.loads(p.read_text()).get(name)
+    if not entry:
+        return None
+    src = ROOT / "delta_rule_recurrent_gb300" / "csrc" / source
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    return entry["bytes_per_launch"] if entry.get("source_sha") == sha else None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in Path(self.path).read_text().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [r for r in rows if r[2] > 200.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        seen = sorted({names[i] for r in busy for i, flag in enumerate(r[3]) if flag == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": seen, "samples": len(busy)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def timed_loop(fn, steps, stream, world):
+    """Runs fn `steps` times between a barrier + synchronize on both sides;
+    returns (wall seconds of the whole region, per-launch event ms list)."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        starts[i].record(stream)
+        fn(i)
+        ends[i].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    region_s = e0.elapsed_time(e1) / 1e3
+    return region_s, [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def cpu_oracle_sample(inp, budget_s=12.0, min_heads=None):
+    """Times the fp64 oracle on whole batch elements of the workload (all H
+    heads, all T tokens each) until `budget_s` has passed; returns tokens/s
+    of the workload, the batch elements done and the cores used."""
+    import oracle
+    cores = oracle.host_cores()
+    B, H, T, _, _ = inp.shape
+    done, t0 = 0, time.perf_counter()
+    while done < B:
+        sl = slice(done, done + 1)
+        oracle.forward(inp.q[sl], inp.k[sl], inp.v[sl], inp.beta[sl],
+                       None if inp.S0 is None else inp.S0[sl], nthreads=cores)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return done * T / el, done, cores, el
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle on the headline workload."""
+    if rank != 0:
+        return
+    import workloads
+    w = workloads.WORKLOADS[HEADLINE]
+    inp = workloads.workload_inputs(HEADLINE)
+    B, H, T, dk, dv = inp.shape
+    import oracle
+    cores = oracle.host_cores()
+    def one(i):
+        b = i % B
+        sl = slice(b, b + 1)
+        oracle.forward(inp.q[sl], inp.k[sl], inp.v[sl], inp.beta[sl], None, nthreads=cores)
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(args.warmup + i)
+    el = time.perf_counter() - t0
+    value = args.steps * T / el
+    sample = f"per step one batch element of {HEADLINE} (H={H} heads x T={T} tokens), fp64"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": HEADLINE, "B": B, "H": H, "T": T, "dk": dk, "dv": dv,
+                   "C": w["C"], "io_dtype": w["dtype"]},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import delta_rule_recurrent_gb300 as dn
+    import workloads
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
+
+    # ---------------- headline: chunk forward, 1.3B-layer shape -------------
+    w = workloads.WORKLOADS[HEADLINE]
+    inp = workloads.workload_inputs(HEADLINE)
+    B, H, T, dk, dv = inp.shape
+    C = w["C"]
+    q, k, v, beta = (x.to(dev) for x in (inp.q, inp.k, inp.v, inp.beta))
+    o = torch.empty(B, H, T, dv, dtype=q.dtype, device=dev)
+    S_T = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+    algo = args.algo
+    lib = dn.load()
+    tc = algo in ("auto", "tcgen05") and _tc_used(lib, dk, dv, q.dtype)
+
+    def chunk_step(_i):
+        dn.chunk_fwd(q, k, v, beta, out=o, final_state=S_T, algo=algo)
+
+    for i in range(args.warmup):
+        chunk_step(i)
+    torch.cuda.synchronize()
+
+    gpu_index = _physical_gpu_index(local)
+    with ClockSampler(gpu_index) as clocks:
+        region_s, per_launch = timed_loop(chunk_step, args.steps, stream, world)
+        region_s = max_over_ranks(region_s, world)
+
+        # ---------------- decode: fused recurrent step ----------------------
+        wd = workloads.WORKLOADS[DECODE]
+        Bd, Hd, dkd, dvd = wd["B"], wd["H"], wd["dk"], wd["dv"]
+        nsteps = args.decode_steps
+        dq, dkk, dvv, db = workloads.decode_inputs_on_device(
+            Bd, Hd, dkd, dvd, nsteps + args.warmup, dtype=wd["dtype"], seed=wd["seed"],
+            beta_scale=wd["beta_scale"], device=dev)
+        Sd = (torch.randn(Bd, Hd, dkd, dvd, device=dev,
+                          generator=torch.Generator(device=dev).manual_seed(wd["seed"]))
+              * wd["s0_std"])
+        od = torch.empty(Bd, Hd, dvd, dtype=dq.dtype, device=dev)
+
+        def decode_step(i):
+            dn.recurrent_step(dq[i], dkk[i], dvv[i], db[i], Sd, out=od)
+
+        for i in range(args.warmup):
+            decode_step(nsteps + i)
+        torch.cuda.synchronize()
+        dec_region_s, dec_launch = timed_loop(decode_step, nsteps, stream, world)
+        dec_region_s = max_over_ranks(dec_region_s, world)
+    clk = clocks.summary()
+    del dq, dkk, dvv, db
+
+    # ---------------- e2e: public API from pinned host buffers --------------
+    hq, hk, hv, hb = (x.pin_memory() for x in (inp.q, inp.k, inp.v, inp.beta))
+    ho = torch.empty(B, H, T, dv, dtype=q.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hb))
+    d2h = ho.numel() * ho.element_size()
+
+    def e2e_step(_i):
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        beta.copy_(hb, non_blocking=True)
+        dn.chunk_fwd(q, k, v, beta, out=o, final_state=S_T, algo=algo)
+        ho.copy_(o, non_blocking=True)
+
+    for i in range(min(args.warmup, 3)):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 50))
+    e2e_s, _ = timed_loop(e2e_step, e2e_steps, stream, world)
+    e2e_s = max_over_ranks(e2e_s, world)
+
+    # ---------------- numbers ----------------------------------------------
+    tokens = B * T
+    value = world * tokens * args.steps / region_s
+    launch_s = statistics.mean(per_launch) / 1e3
+    flops = chunk_flops_per_token_head(C, dk, dv) * B * H * T
+    cbytes = chunk_bytes(B, H, T, dk, dv, q.element_size(), False, True)
+    tflops = flops / launch_s / 1e12
+    kname = "chunk_tc" if tc else "chunk_simt"
+    roofline = {
+        "bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+        "frac": tflops / peaks["bf16_tflops"],
+        "traffic": kernel_traffic(kname, "chunk_tc.cu" if tc else "chunk_simt.cu"),
+        "peak_source": f"{peak_src} (bf16 dense burst)", "kernel": kname,
+        "flops_per_launch": flops, "launch_us": launch_s * 1e6,
+        "hbm": {"achieved": cbytes / launch_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": cbytes / launch_s / 1e9 / peaks["hbm_gbs"], "bytes_per_launch": cbytes},
+    }
+    dbytes = decode_bytes(Bd, Hd, dkd, dvd, 2)
+    dec_launch_s = statistics.mean(dec_launch) / 1e3
+    dec_gbs = dbytes / dec_launch_s / 1e9
+    decode = {
+        "workload": DECODE, "steps": nsteps, "value": world * Bd * nsteps / dec_region_s,
+        "unit": "tokens/s", "ms_per_step": 1e3 * dec_region_s / nsteps,
+        "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
+                     "traffic": kernel_traffic("recurrent_step", "decode.cu"),
+                     "peak_source": f"{peak_src} (copy bandwidth)", "bytes_per_launch": dbytes,
+                     "launch_us": dec_launch_s * 1e6},
+        "config": {"B": Bd, "H": Hd, "dk": dkd, "dv": dvd, "state": "fp32",
+                   "io_dtype": wd["dtype"], "beta": "2*sigmoid(N(0,1))",
+                   "l2": "state 537 MB per step > L2"},
+    }
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * region_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if tc else "f32", "data": "synthetic (seeded)",
+        "config": {"workload": HEADLINE, "B": B, "H": H, "T": T, "dk": dk, "dv": dv, "C": C,
+                   "io_dtype": w["dtype"], "state": "fp32", "algo": kname,
+                   "l2": f"inputs {(3 * B * H * T * dk * 2) >> 20} MB > L2 (129 MB), no flush",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "decode": decode,
+        "e2e": {"value": world * tokens * e2e_steps / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": 1e3 * e2e_s / e2e_steps},
+        "gpu_launches": args.steps + nsteps + e2e_steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        val, done, cores, el = cpu_oracle_sample(inp, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {
+            "value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {B} batch elements of {HEADLINE} (all {H} heads x {T} "
+                      f"tokens each), fp64, {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _tc_used(lib, dk, dv, dtype):
+    import torch
+    # the AUTO policy: tensor cores whenever the tcgen05 path covers the case
+    code = 1 if dtype == torch.bfloat16 else 0
+    return lib.dn_chunk_fwd_algo(None, None, None, None, None, None, None, 0, 0, 0, dk, dv, 64,
+                                 code, None, 0, None, 2) == 0
+
+
+def _physical_gpu_index(local: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local < len(ids) and ids[local].isdigit():
+            return int(ids[local])
+    return local
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--algo", choices=["auto", "simt", "tcgen05"], default="auto")
+    ap.add_argument("--decode-steps", type=int, default=1024)
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle time for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,131 @@
+"""GB300-native DeltaNet delta-rule operator.
+
+Thin Python binding over the C ABI in ``include/deltanet.h``: these functions
+only check tensors, allocate outputs with PyTorch and pass raw device
+pointers plus the current CUDA stream to ``libdeltanet.so``.  Every step of
+the computation runs in the library's sm_103a kernels.
+
+    chunk_fwd(q, k, v, beta, initial_state=None, output_final_state=True)
+        -> (o, final_state)          # training / prefill, chunkwise form
+    recurrent_step(q, k, v, beta, state) -> o   # decoding, state in place
+
+Shapes: q, k ``[B, H, T, dk]``; v ``[B, H, T, dv]``; beta ``[B, H, T]``;
+state ``[B, H, dk, dv]`` fp32 (the pages' dv x dk state, transposed).  For a
+decoding step the T axis is absent.  q and k must already be L2-normalised.
+"""
+from __future__ import annotations
+
+import torch
+
+from ._lib import (DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05, DN_BF16, DN_F32,
+                   DeltaNetError, check, header_symbols, lib_path, load)
+
+__all__ = ["chunk_fwd", "recurrent_step", "DeltaNetError", "load", "lib_path",
+           "header_symbols", "ALGOS"]
+
+ALGOS = {"auto": DN_ALGO_AUTO, "simt": DN_ALGO_SIMT, "tcgen05": DN_ALGO_TCGEN05}
+_DT = {torch.float32: DN_F32, torch.bfloat16: DN_BF16}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+    return _DT[t.dtype]
+
+
+def _check_cuda(name: str, t: torch.Tensor, device) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda" or (device is not None and t.device != device):
+        raise ValueError(f"{name} must live on {device or 'a CUDA device'}, not {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_handle(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+              initial_state: torch.Tensor | None = None, output_final_state: bool = True,
+              chunk_size: int = 64, algo: str = "auto", out: torch.Tensor | None = None,
+              final_state: torch.Tensor | None = None):
+    """Chunkwise delta-rule forward (``dn_chunk_fwd``).
+
+    Returns ``(o, S_T)``; ``S_T`` is None when ``output_final_state`` is
+    False.  ``final_state`` may be ``initial_state`` itself to update it in
+    place; ``out`` may supply the output buffer.
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
+        _check_cuda(name, t, dev)
+    dt = _dtype_code(q)
+    if not (k.dtype == v.dtype == beta.dtype == q.dtype):
+        raise TypeError("q, k, v and beta must share one dtype")
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4:
+        raise ValueError("q, k must be [B,H,T,dk] and v [B,H,T,dv]")
+    B, H, T, dk = q.shape
+    dv = v.shape[3]
+    if tuple(v.shape[:3]) != (B, H, T) or tuple(beta.shape) != (B, H, T):
+        raise ValueError("v must be [B,H,T,dv] and beta [B,H,T]")
+    if initial_state is not None:
+        _check_cuda("initial_state", initial_state, dev)
+        if initial_state.dtype != torch.float32 or tuple(initial_state.shape) != (B, H, dk, dv):
+            raise ValueError("initial_state must be float32 [B,H,dk,dv]")
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev)
+    else:
+        _check_cuda("out", out, dev)
+        if out.dtype != q.dtype or tuple(out.shape) != (B, H, T, dv):
+            raise ValueError("out must match v's shape and dtype")
+    S_T = None
+    if output_final_state:
+        S_T = final_state if final_state is not None else torch.empty(
+            (B, H, dk, dv), dtype=torch.float32, device=dev)
+        _check_cuda("final_state", S_T, dev)
+        if S_T.dtype != torch.float32 or tuple(S_T.shape) != (B, H, dk, dv):
+            raise ValueError("final_state must be float32 [B,H,dk,dv]")
+    lib = load()
+    ws_bytes = lib.dn_chunk_fwd_workspace_bytes(B, H, T, dk, dv, chunk_size, dt)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    with torch.cuda.device(dev):
+        check(lib.dn_chunk_fwd_algo(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(),
+            initial_state.data_ptr() if initial_state is not None else None,
+            out.data_ptr(), S_T.data_ptr() if S_T is not None else None,
+            B, H, T, dk, dv, chunk_size, dt,
+            ws.data_ptr() if ws is not None else None, ws_bytes,
+            _stream_handle(dev), ALGOS[algo]))
+    return out, S_T
+
+
+def recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                   state: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """One fused decoding step (``dn_recurrent_step``); ``state`` is updated
+    in place and the step's output ``o`` ``[B, H, dv]`` is returned."""
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("state", state)):
+        _check_cuda(name, t, dev)
+    dt = _dtype_code(q)
+    if not (k.dtype == v.dtype == beta.dtype == q.dtype):
+        raise TypeError("q, k, v and beta must share one dtype")
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3:
+        raise ValueError("q, k must be [B,H,dk] and v [B,H,dv]")
+    B, H, dk = q.shape
+    dv = v.shape[2]
+    if tuple(v.shape[:2]) != (B, H) or tuple(beta.shape) != (B, H):
+        raise ValueError("v must be [B,H,dv] and beta [B,H]")
+    if state.dtype != torch.float32 or tuple(state.shape) != (B, H, dk, dv):
+        raise ValueError("state must be float32 [B,H,dk,dv]")
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=q.dtype, device=dev)
+    else:
+        _check_cuda("out", out, dev)
+        if out.dtype != q.dtype or tuple(out.shape) != (B, H, dv):
+            raise ValueError("out must be [B,H,dv] in q's dtype")
+    lib = load()
+    with torch.cuda.device(dev):
+        check(lib.dn_recurrent_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(),
+                                    state.data_ptr(), out.data_ptr(), B, H, dk, dv, dt,
+                                    _stream_handle(dev)))
+    return out

@@ -1,0 +1,202 @@
+// api.cu -- the C ABI declared in include/deltanet.h: argument checks and
+// dispatch.  Every check runs on the host before anything is enqueued.
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include "../../include/deltanet.h"
+#include "dn_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int ok() {
+    g_last_error[0] = '\0';
+    return DN_OK;
+}
+
+struct Span {
+    const char* name;
+    const void* p;
+    size_t bytes;
+};
+
+bool overlaps(const Span& a, const Span& b) {
+    if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = (uintptr_t)a.p, b0 = (uintptr_t)b.p;
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// The pointer must be device (or managed) memory of the current device and
+// aligned to `align` bytes.
+int check_device_ptr(const Span& s, size_t align, int device) {
+    if (!s.p) return fail(DN_ERR_INVALID_ARG, "%s is NULL", s.name);
+    if ((uintptr_t)s.p % align != 0)
+        return fail(DN_ERR_INVALID_ARG, "%s is not %zu-byte aligned", s.name, align);
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, s.p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(DN_ERR_INVALID_ARG, "%s: cudaPointerGetAttributes failed (%s)", s.name,
+                    cudaGetErrorString(e));
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return fail(DN_ERR_INVALID_ARG, "%s is not device memory", s.name);
+    if (attr.type == cudaMemoryTypeDevice && attr.device != device)
+        return fail(DN_ERR_INVALID_ARG, "%s lives on device %d, current device is %d", s.name,
+                    attr.device, device);
+    return DN_OK;
+}
+
+int current_device(int* dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(DN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    }
+    return DN_OK;
+}
+
+int cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return ok();
+    return fail(DN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool supported_dim(int d) { return d == 64 || d == 128; }
+
+size_t elem_size(int dt) { return dt == DN_F32 ? 4 : 2; }
+
+}  // namespace
+
+extern "C" {
+
+const char* dn_status_string(int status) {
+    switch (status) {
+        case DN_OK: return "DN_OK";
+        case DN_ERR_INVALID_ARG: return "DN_ERR_INVALID_ARG";
+        case DN_ERR_UNSUPPORTED: return "DN_ERR_UNSUPPORTED";
+        case DN_ERR_CUDA: return "DN_ERR_CUDA";
+        default: return "DN_UNKNOWN_STATUS";
+    }
+}
+
+const char* dn_last_error(void) { return g_last_error; }
+
+int dn_abi_version(void) { return DN_ABI_VERSION; }
+
+size_t dn_chunk_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt) {
+    (void)B; (void)H; (void)T; (void)dk; (void)dv; (void)C; (void)dt;
+    return 0;
+}
+
+int dn_chunk_fwd_algo(const void* q, const void* k, const void* v, const void* beta,
+                      const float* S0, void* o, float* S_T, int B, int H, int T, int dk,
+                      int dv, int C, int dt, void* workspace, size_t workspace_bytes,
+                      void* stream, int algo) {
+    (void)workspace;
+    if (B < 0 || H < 0 || T < 0)
+        return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d T=%d)", B, H, T);
+    if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
+    if (algo != DN_ALGO_AUTO && algo != DN_ALGO_SIMT && algo != DN_ALGO_TCGEN05)
+        return fail(DN_ERR_INVALID_ARG, "unknown algo %d", algo);
+    if (dk <= 0 || dv <= 0 || C <= 0)
+        return fail(DN_ERR_INVALID_ARG, "dk, dv and C must be positive");
+    if (!supported_dim(dk) || !supported_dim(dv))
+        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this build supports 64 and 128", dk, dv);
+    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this build supports 64", C);
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
+    const size_t need_ws = dn_chunk_fwd_workspace_bytes(B, H, T, dk, dv, C, dt);
+    if (workspace_bytes < need_ws)
+        return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes, need_ws);
+    if (algo == DN_ALGO_TCGEN05 && !dn::chunk_tc_supports(dk, dv, dt))
+        return fail(DN_ERR_UNSUPPORTED, "tcgen05 path does not cover dk=%d dv=%d dtype=%d", dk,
+                    dv, dt);
+    if (BH == 0) return ok();
+
+    const size_t es = elem_size(dt);
+    const size_t ntok = (size_t)BH * (size_t)T;
+    const size_t state_bytes = (size_t)BH * dk * dv * sizeof(float);
+    const Span sq{"q", q, ntok * dk * es}, sk{"k", k, ntok * dk * es}, sv{"v", v, ntok * dv * es},
+        sb{"beta", beta, ntok * es}, so{"o", o, ntok * dv * es}, s0{"S0", S0, state_bytes},
+        sT{"S_T", S_T, state_bytes};
+    int dev = 0;
+    if (int st = current_device(&dev)) return st;
+    if (T > 0) {
+        for (const Span* s : {&sq, &sk, &sv, &so})
+            if (int st = check_device_ptr(*s, 16, dev)) return st;
+        if (int st = check_device_ptr(sb, es, dev)) return st;
+    }
+    if (S0)
+        if (int st = check_device_ptr(s0, 16, dev)) return st;
+    if (S_T)
+        if (int st = check_device_ptr(sT, 16, dev)) return st;
+    if (T > 0)
+        for (const Span* s : {&sq, &sk, &sv, &sb, &s0, &sT})
+            if (overlaps(so, *s)) return fail(DN_ERR_INVALID_ARG, "o overlaps %s", s->name);
+    for (const Span* s : {&sq, &sk, &sv, &sb})
+        if (T > 0 && overlaps(sT, *s)) return fail(DN_ERR_INVALID_ARG, "S_T overlaps %s", s->name);
+    if (S_T && S0 && S_T != S0 && overlaps(sT, s0))
+        return fail(DN_ERR_INVALID_ARG, "S_T partly overlaps S0");
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        if (!S_T || S_T == S0) return ok();
+        if (S0)
+            return cuda_status(cudaMemcpyAsync(S_T, S0, state_bytes, cudaMemcpyDeviceToDevice, st),
+                               "cudaMemcpyAsync(S_T <- S0)");
+        return cuda_status(cudaMemsetAsync(S_T, 0, state_bytes, st), "cudaMemsetAsync(S_T)");
+    }
+    const bool use_tc = algo == DN_ALGO_TCGEN05 ||
+                        (algo == DN_ALGO_AUTO && dn::chunk_tc_supports(dk, dv, dt));
+    cudaError_t e = use_tc
+        ? dn::launch_chunk_tc(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, st)
+        : dn::launch_chunk_simt(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, st);
+    return cuda_status(e, use_tc ? "chunk forward (tcgen05) launch" : "chunk forward (SIMT) launch");
+}
+
+int dn_chunk_fwd(const void* q, const void* k, const void* v, const void* beta, const float* S0,
+                 void* o, float* S_T, int B, int H, int T, int dk, int dv, int C, int dt,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+    return dn_chunk_fwd_algo(q, k, v, beta, S0, o, S_T, B, H, T, dk, dv, C, dt, workspace,
+                             workspace_bytes, stream, DN_ALGO_AUTO);
+}
+
+int dn_recurrent_step(const void* q, const void* k, const void* v, const void* beta, float* S,
+                      void* o, int B, int H, int dk, int dv, int dt, void* stream) {
+    if (B < 0 || H < 0) return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d)", B, H);
+    if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
+    if (dk <= 0 || dv <= 0) return fail(DN_ERR_INVALID_ARG, "dk and dv must be positive");
+    if (!supported_dim(dk) || !supported_dim(dv))
+        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this build supports 64 and 128", dk, dv);
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
+    if (BH == 0) return ok();
+    const size_t es = elem_size(dt);
+    const Span sq{"q", q, (size_t)BH * dk * es}, sk{"k", k, (size_t)BH * dk * es},
+        sv{"v", v, (size_t)BH * dv * es}, sb{"beta", beta, (size_t)BH * es},
+        so{"o", o, (size_t)BH * dv * es}, sS{"S", S, (size_t)BH * dk * dv * sizeof(float)};
+    int dev = 0;
+    if (int st = current_device(&dev)) return st;
+    for (const Span* s : {&sq, &sk, &sv, &so, &sS})
+        if (int st = check_device_ptr(*s, 16, dev)) return st;
+    if (int st = check_device_ptr(sb, es, dev)) return st;
+    for (const Span* s : {&sq, &sk, &sv, &sb, &sS})
+        if (overlaps(so, *s)) return fail(DN_ERR_INVALID_ARG, "o overlaps %s", s->name);
+    for (const Span* s : {&sq, &sk, &sv, &sb})
+        if (overlaps(sS, *s)) return fail(DN_ERR_INVALID_ARG, "S overlaps %s", s->name);
+    return cuda_status(dn::launch_recurrent_step(q, k, v, beta, S, o, (int)BH, dk, dv, dt,
+                                                 static_cast<cudaStream_t>(stream)),
+                       "recurrent step launch");
+}
+
+}  // extern "C"

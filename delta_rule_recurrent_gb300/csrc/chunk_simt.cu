@@ -1,0 +1,321 @@
+// chunk_simt.cu -- chunkwise delta-rule forward on CUDA cores, fp32 throughout.
+//
+// This is the full-precision path (fp32 I/O is held to 1e-4 relative L2,
+// which bf16 or tf32 tensor-core operands cannot meet) and the fallback for
+// shapes the tensor-core kernel does not cover.
+//
+// Chunk algebra ("Chunkwise KDA : réorganiser la récurrence en
+// multiplications matricielles", fr.news.hada.io/topic?id=31925, with the
+// decay D = I; appendix B.2 "UT transform" of paperlayer.ai/abs/2406.06484v6).
+// For a chunk of C tokens (rows of K, Q, V) and incoming state S ([dk][dv]):
+//     A   = tril(diag(beta) K K^T, -1)            (strictly lower)
+//     X   = (I + A)^{-1}                          (blocked forward substitution)
+//     R'  = diag(beta) (V - K S)
+//     U'  = X R'                                  (the true per-token errors)
+//     O   = Q S + (Q K^T . M) U'                  (M: causal incl. diagonal)
+//     S  <- S + K^T U'
+// A CTA owns one (batch, head) and a slice of NV value channels; it walks the
+// chunks in order with its slice of S resident in shared memory.  Value
+// channels are independent in every step above, so slices never exchange
+// data; the key-side work (A, X, Q K^T) is recomputed per slice.
+#include "dn_common.cuh"
+#include "dn_internal.h"
+
+namespace dn {
+namespace {
+
+constexpr int kC = 64;         // chunk length
+constexpr int kThreads = 256;  // 16 x 16 thread grid for the register-tiled products
+constexpr int kLC = kC + 1;    // odd row pitches keep shared-memory reads conflict-free
+
+// acc[i][j] += sum_kk a(ty + 16 i, kk) * b(kk, tx + 16 j) for a 256-thread CTA.
+template <int M, int N, int K, typename FA, typename FB>
+__device__ __forceinline__ void mm_acc(float (&acc)[M / 16][N / 16], FA a, FB b) {
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll 4
+    for (int kk = 0; kk < K; ++kk) {
+        float av[M / 16], bv[N / 16];
+#pragma unroll
+        for (int i = 0; i < M / 16; ++i) av[i] = a(ty + 16 * i, kk);
+#pragma unroll
+        for (int j = 0; j < N / 16; ++j) bv[j] = b(kk, tx + 16 * j);
+#pragma unroll
+        for (int i = 0; i < M / 16; ++i)
+#pragma unroll
+            for (int j = 0; j < N / 16; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+}
+
+template <int M, int N>
+__device__ __forceinline__ void zero(float (&acc)[M / 16][N / 16]) {
+#pragma unroll
+    for (int i = 0; i < M / 16; ++i)
+#pragma unroll
+        for (int j = 0; j < N / 16; ++j) acc[i][j] = 0.f;
+}
+
+// X = (I + A)^{-1} for a strictly lower-triangular 64 x 64 A (row pitch kLC),
+// by blocks of 16: the four diagonal blocks by column-wise substitution,
+// then X_ij = -X_ii sum_{l=j}^{i-1} A_il X_lj one block diagonal at a time.
+// Ys is 3 x 16 x 17 floats of scratch.  Ends with a barrier.
+__device__ void unit_lower_inverse64(const float* __restrict__ Am,
+                                     float* __restrict__ Xm, float* __restrict__ Ys) {
+    const int tid = threadIdx.x;
+    if (tid < 64) {
+        const int base = (tid >> 4) * 16, c = tid & 15;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = (r == c) ? 1.f : 0.f;
+#pragma unroll
+            for (int l = 0; l < r; ++l) acc = fmaf(-Am[(base + r) * kLC + base + l], x[l], acc);
+            x[r] = (r < c) ? 0.f : acc;
+            Xm[(base + r) * kLC + base + c] = x[r];
+        }
+    }
+    // Blocks above the diagonal are zero.
+    for (int e = tid; e < 6 * 256; e += kThreads) {
+        const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
+        // (i, j) pairs with j > i: (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        Xm[(16 * bi + r) * kLC + 16 * bj + c] = 0.f;
+    }
+    __syncthreads();
+    for (int d = 1; d < 4; ++d) {
+        const int nb = 4 - d;
+        for (int e = tid; e < nb * 256; e += kThreads) {
+            const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
+            float acc = 0.f;
+            for (int kk = 16 * j; kk < 16 * i; ++kk)
+                acc = fmaf(Am[(16 * i + r) * kLC + kk], Xm[kk * kLC + 16 * j + c], acc);
+            Ys[j * 272 + r * 17 + c] = acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < nb * 256; e += kThreads) {
+            const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
+            float acc = 0.f;
+            for (int m = 0; m <= r; ++m)
+                acc = fmaf(Xm[(16 * i + r) * kLC + 16 * i + m], Ys[j * 272 + m * 17 + c], acc);
+            Xm[(16 * i + r) * kLC + 16 * j + c] = -acc;
+        }
+        __syncthreads();
+    }
+}
+
+template <int DK, int NV>
+struct SimtSmem {
+    static constexpr int LK = DK + 1, LV = NV + 1;
+    static constexpr int kK = 0;                       // C x LK   keys
+    static constexpr int kQ = kK + kC * LK;            // C x LK   queries
+    static constexpr int kR = kQ + kC * LK;            // C x LV   values, then R'
+    static constexpr int kU = kR + kC * LV;            // C x LV   U'
+    static constexpr int kS = kU + kC * LV;            // DK x LV  state slice
+    static constexpr int kA = kS + DK * LV;            // C x kLC  A
+    static constexpr int kX = kA + kC * kLC;           // C x kLC  (I + A)^{-1}
+    static constexpr int kP = kX + kC * kLC;           // C x kLC  Q K^T . M
+    static constexpr int kY = kP + kC * kLC;           // 3 x 16 x 17 solve scratch
+    static constexpr int kB = kY + 3 * 16 * 17;        // C        beta
+    static constexpr int kFloats = kB + kC;
+    static constexpr size_t kBytes = sizeof(float) * kFloats;
+};
+
+template <typename T, int DK, int DV, int NV>
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
+                  const T* __restrict__ v, const T* __restrict__ beta,
+                  const float* __restrict__ S0, T* __restrict__ o,
+                  float* __restrict__ S_T, int Tlen) {
+    using L = SimtSmem<DK, NV>;
+    constexpr int LK = L::LK, LV = L::LV;
+    constexpr int NSLICE = DV / NV;
+    extern __shared__ float smem[];
+    float* Ks = smem + L::kK;
+    float* Qs = smem + L::kQ;
+    float* Rs = smem + L::kR;
+    float* Us = smem + L::kU;
+    float* Ss = smem + L::kS;
+    float* Am = smem + L::kA;
+    float* Xm = smem + L::kX;
+    float* Pm = smem + L::kP;
+    float* Ys = smem + L::kY;
+    float* bs = smem + L::kB;
+
+    const int tid = threadIdx.x;
+    const int tx = tid & 15, ty = tid >> 4;
+    const int bh = blockIdx.x / NSLICE;
+    const int j0 = (blockIdx.x % NSLICE) * NV;
+    const size_t tok0 = (size_t)bh * Tlen;
+
+    for (int e = tid; e < DK * NV; e += kThreads) {
+        const int i = e / NV, jj = e % NV;
+        Ss[i * LV + jj] = S0 ? S0[((size_t)bh * DK + i) * DV + j0 + jj] : 0.f;
+    }
+
+    const int nchunks = (Tlen + kC - 1) / kC;
+    for (int c = 0; c < nchunks; ++c) {
+        const int t0 = c * kC;
+        const int n = min(kC, Tlen - t0);
+        // ---- load the chunk (padding rows: k = q = v = 0, beta = 0) ----
+        for (int e = tid; e < kC * DK; e += kThreads) {
+            const int t = e / DK, i = e % DK;
+            const size_t g = (tok0 + t0 + t) * DK + i;
+            Ks[t * LK + i] = t < n ? to_f32(k[g]) : 0.f;
+            Qs[t * LK + i] = t < n ? to_f32(q[g]) : 0.f;
+        }
+        for (int e = tid; e < kC * NV; e += kThreads) {
+            const int t = e / NV, jj = e % NV;
+            Rs[t * LV + jj] = t < n ? to_f32(v[(tok0 + t0 + t) * DV + j0 + jj]) : 0.f;
+        }
+        if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
+        __syncthreads();
+
+        // ---- A = tril(diag(beta) K K^T, -1) and P = tril(Q K^T) ----
+        {
+            float aa[4][4], ap[4][4];
+            zero<64, 64>(aa);
+            zero<64, 64>(ap);
+#pragma unroll 2
+            for (int kk = 0; kk < DK; ++kk) {
+                float ak[4], aq[4], bk[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    ak[i] = Ks[(ty + 16 * i) * LK + kk];
+                    aq[i] = Qs[(ty + 16 * i) * LK + kk];
+                    bk[i] = Ks[(tx + 16 * i) * LK + kk];
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        aa[i][j] = fmaf(ak[i], bk[j], aa[i][j]);
+                        ap[i][j] = fmaf(aq[i], bk[j], ap[i][j]);
+                    }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int m = ty + 16 * i, nn = tx + 16 * j;
+                    Am[m * kLC + nn] = nn < m ? bs[m] * aa[i][j] : 0.f;
+                    Pm[m * kLC + nn] = nn <= m ? ap[i][j] : 0.f;
+                }
+        }
+        __syncthreads();
+
+        // ---- R' = diag(beta) (V - K S), in place over V ----
+        {
+            float acc[4][NV / 16];
+            zero<64, NV>(acc);
+            mm_acc<64, NV, DK>(acc, [&](int m, int kk) { return Ks[m * LK + kk]; },
+                               [&](int kk, int nn) { return Ss[kk * LV + nn]; });
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < NV / 16; ++j) {
+                    const int m = ty + 16 * i, nn = tx + 16 * j;
+                    Rs[m * LV + nn] = bs[m] * (Rs[m * LV + nn] - acc[i][j]);
+                }
+        }
+        // ---- X = (I + A)^{-1} (touches only Am, Xm, Ys; ends with a barrier) ----
+        unit_lower_inverse64(Am, Xm, Ys);
+
+        // ---- U' = X R' ----
+        {
+            float acc[4][NV / 16];
+            zero<64, NV>(acc);
+            mm_acc<64, NV, kC>(acc, [&](int m, int kk) { return Xm[m * kLC + kk]; },
+                               [&](int kk, int nn) { return Rs[kk * LV + nn]; });
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < NV / 16; ++j)
+                    Us[(ty + 16 * i) * LV + tx + 16 * j] = acc[i][j];
+        }
+        __syncthreads();
+
+        // ---- O = Q S + P U' ----
+        {
+            float acc[4][NV / 16];
+            zero<64, NV>(acc);
+            mm_acc<64, NV, DK>(acc, [&](int m, int kk) { return Qs[m * LK + kk]; },
+                               [&](int kk, int nn) { return Ss[kk * LV + nn]; });
+            mm_acc<64, NV, kC>(acc, [&](int m, int kk) { return Pm[m * kLC + kk]; },
+                               [&](int kk, int nn) { return Us[kk * LV + nn]; });
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int m = ty + 16 * i;
+                if (m < n) {
+#pragma unroll
+                    for (int j = 0; j < NV / 16; ++j)
+                        o[(tok0 + t0 + m) * DV + j0 + tx + 16 * j] = from_f32<T>(acc[i][j]);
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- S <- S + K^T U' ----
+        {
+            float acc[DK / 16][NV / 16];
+            zero<DK, NV>(acc);
+            mm_acc<DK, NV, kC>(acc, [&](int m, int kk) { return Ks[kk * LK + m]; },
+                               [&](int kk, int nn) { return Us[kk * LV + nn]; });
+#pragma unroll
+            for (int i = 0; i < DK / 16; ++i)
+#pragma unroll
+                for (int j = 0; j < NV / 16; ++j)
+                    Ss[(ty + 16 * i) * LV + tx + 16 * j] += acc[i][j];
+        }
+        __syncthreads();
+    }
+
+    if (S_T) {
+        for (int e = tid; e < DK * NV; e += kThreads) {
+            const int i = e / NV, jj = e % NV;
+            S_T[((size_t)bh * DK + i) * DV + j0 + jj] = Ss[i * LV + jj];
+        }
+    }
+}
+
+template <typename T, int DK, int DV>
+cudaError_t launch_typed(const void* q, const void* k, const void* v,
+                         const void* beta, const float* S0, void* o, float* S_T,
+                         int BH, int Tlen, cudaStream_t stream) {
+    constexpr int NV = DV < 64 ? DV : 64;
+    using L = SimtSmem<DK, NV>;
+    auto kern = chunk_simt_kernel<T, DK, DV, NV>;
+    cudaError_t err = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
+    if (err != cudaSuccess) return err;
+    const long long grid = (long long)BH * (DV / NV);
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)grid, kThreads, L::kBytes, stream>>>(
+        static_cast<const T*>(q), static_cast<const T*>(k),
+        static_cast<const T*>(v), static_cast<const T*>(beta), S0,
+        static_cast<T*>(o), S_T, Tlen);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_dims(const void* q, const void* k, const void* v,
+                        const void* beta, const float* S0, void* o, float* S_T,
+                        int BH, int Tlen, int dk, int dv, cudaStream_t st) {
+    if (dk == 128 && dv == 128) return launch_typed<T, 128, 128>(q, k, v, beta, S0, o, S_T, BH, Tlen, st);
+    if (dk == 128 && dv == 64) return launch_typed<T, 128, 64>(q, k, v, beta, S0, o, S_T, BH, Tlen, st);
+    if (dk == 64 && dv == 128) return launch_typed<T, 64, 128>(q, k, v, beta, S0, o, S_T, BH, Tlen, st);
+    if (dk == 64 && dv == 64) return launch_typed<T, 64, 64>(q, k, v, beta, S0, o, S_T, BH, Tlen, st);
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v,
+                              const void* beta, const float* S0, void* o,
+                              float* S_T, int BH, int T, int dk, int dv, int dt,
+                              cudaStream_t stream) {
+    if (BH <= 0 || T <= 0) return cudaSuccess;
+    if (dt == 0) return launch_dims<float>(q, k, v, beta, S0, o, S_T, BH, T, dk, dv, stream);
+    return launch_dims<__nv_bfloat16>(q, k, v, beta, S0, o, S_T, BH, T, dk, dv, stream);
+}
+
+}  // namespace dn

@@ -1,0 +1,31 @@
+// dn_internal.h -- launchers behind the C ABI (host side, no validation).
+//
+// Each launcher assumes the ABI layer has already checked pointers, sizes and
+// the (dtype, dk, dv) combination, and returns the cudaError_t of its launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace dn {
+
+// One decoding step over B*H heads (see dn_recurrent_step).
+cudaError_t launch_recurrent_step(const void* q, const void* k, const void* v,
+                                  const void* beta, float* S, void* o, int BH,
+                                  int dk, int dv, int dt, cudaStream_t stream);
+
+// Chunkwise forward with fp32 CUDA-core arithmetic (any T >= 1).
+cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v,
+                              const void* beta, const float* S0, void* o,
+                              float* S_T, int BH, int T, int dk, int dv, int dt,
+                              cudaStream_t stream);
+
+// Chunkwise forward on tcgen05 tensor cores.  Returns cudaErrorNotSupported
+// (without launching) for shapes or dtypes it does not cover.
+bool chunk_tc_supports(int dk, int dv, int dt);
+cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v,
+                            const void* beta, const float* S0, void* o,
+                            float* S_T, int BH, int T, int dk, int dv, int dt,
+                            cudaStream_t stream);
+
+}  // namespace dn

@@ -1,0 +1,155 @@
+/*
+ * deltanet.h -- C ABI of the GB300 (sm_103a) DeltaNet delta-rule operator.
+ *
+ * The operator is the delta-rule recurrence of "DeltaNet 引入 Delta Rule"
+ * (garden.houmin.site/infra/delta-net) and of "DeltaNet : écrire l'erreur de
+ * prédiction plutôt que la valeur" / "Transition d'état structurée"
+ * (fr.news.hada.io/topic?id=31925), per batch b and head h:
+ *
+ *     S_t = S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   o_t = S_t q_t
+ *
+ * i.e. u_t = beta_t (v_t - S_{t-1} k_t), S_t = S_{t-1} + u_t k_t^T, and the
+ * output is read after the token's own write.  The pages' state S is
+ * dv x dk (key space -> value space); this library stores it transposed,
+ * as [dk][dv] fp32 with the value channel contiguous.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers (cudaMalloc, or managed
+ *     memory), contiguous, row-major, 16-byte aligned (beta: aligned to its
+ *     element).  Host pointers are rejected with DN_ERR_INVALID_ARG.
+ *   - The caller owns all memory.  The library allocates nothing, never
+ *     synchronises, and enqueues its kernels on `stream` (a cudaStream_t;
+ *     NULL means the legacy default stream).  Results are ready when the
+ *     stream reaches them.
+ *   - q and k are used as given (the caller L2-normalises them); there is no
+ *     query scale; beta is used as given (0..1, or 0..2 for the
+ *     negative-eigenvalue variant), with no clamping.
+ *   - Arguments are checked on the host before anything is enqueued; a
+ *     rejected call enqueues nothing.  Kernels have no device traps and no
+ *     unbounded waits.  Launch failures are reported as DN_ERR_CUDA.
+ *   - The library keeps no mutable global state apart from a thread-local
+ *     error message, so calls from several threads are safe.
+ */
+#ifndef DELTANET_H
+#define DELTANET_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define DN_API __attribute__((visibility("default")))
+#else
+#define DN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+typedef enum {
+    DN_OK = 0,
+    DN_ERR_INVALID_ARG = 1, /* NULL / host / misaligned / aliasing pointer, bad size */
+    DN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement     */
+    DN_ERR_CUDA = 3         /* the CUDA runtime reported an error              */
+} dn_status;
+
+/* Element type of q, k, v, beta and o.  The state is always fp32. */
+typedef enum { DN_F32 = 0, DN_BF16 = 1 } dn_dtype;
+
+/* Which kernel evaluates the chunkwise forward. */
+typedef enum {
+    DN_ALGO_AUTO = 0,  /* tensor cores when the shape and dtype allow, else SIMT  */
+    DN_ALGO_SIMT = 1,  /* fp32 CUDA-core arithmetic throughout                    */
+    DN_ALGO_TCGEN05 = 2 /* tcgen05 tensor cores (bf16 operands, fp32 accumulate)  */
+} dn_algo;
+
+/*
+ * dn_chunk_fwd -- chunkwise-parallel forward over whole sequences (training
+ * and prefill).
+ *
+ * Computes, for every (b, h), the recurrence above over t = 0..T-1 starting
+ * from S0, evaluated chunk by chunk in the UT / WY form ("Chunkwise KDA :
+ * réorganiser la récurrence en multiplications matricielles",
+ * fr.news.hada.io/topic?id=31925, with no decay; "Chunkwise parallelization"
+ * and appendix B.2 of paperlayer.ai/abs/2406.06484v6).  Per chunk of C
+ * tokens with incoming state S:
+ *     A = tril(diag(beta) K K^T, -1),  T = (I + A)^{-1} diag(beta),
+ *     U' = T (V - K S),  O = Q S + (Q K^T . M) U',  S <- S + K^T U'
+ * where M is the causal mask including the diagonal.  The result equals the
+ * token-by-token recurrence up to rounding.
+ *
+ * Arguments:
+ *   q, k    [B, H, T, dk]   dtype `dt`
+ *   v       [B, H, T, dv]   dtype `dt`
+ *   beta    [B, H, T]       dtype `dt`
+ *   S0      [B, H, dk, dv]  fp32 initial state, or NULL for zeros
+ *   o       [B, H, T, dv]   dtype `dt`, written; must not overlap any input
+ *   S_T     [B, H, dk, dv]  fp32 final state, or NULL to skip; may equal S0
+ *                           (updated in place) but must not partly overlap it
+ *   B, H, T >= 0 (T = 0 only copies S0, or zeros, to S_T)
+ *   dk, dv  64 or 128;  C (chunk length) 64
+ *   dt      DN_F32 or DN_BF16
+ *   workspace, workspace_bytes: scratch of at least
+ *           dn_chunk_fwd_workspace_bytes(...) bytes (NULL/0 when that is 0)
+ *   stream  cudaStream_t
+ * A last chunk shorter than C is handled exactly (as if padded with beta = 0
+ * and k = 0 tokens, whose outputs are dropped).
+ * Errors: DN_ERR_INVALID_ARG, DN_ERR_UNSUPPORTED (other dk, dv, C), DN_ERR_CUDA.
+ */
+DN_API int dn_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
+                 const float *S0, void *o, float *S_T,
+                 int B, int H, int T, int dk, int dv, int C,
+                 int dt, void *workspace, size_t workspace_bytes,
+                 void *stream);
+
+/* As dn_chunk_fwd, choosing the kernel explicitly.  DN_ALGO_TCGEN05 returns
+ * DN_ERR_UNSUPPORTED for shapes or dtypes it does not cover. */
+DN_API int dn_chunk_fwd_algo(const void *q, const void *k, const void *v,
+                      const void *beta, const float *S0, void *o, float *S_T,
+                      int B, int H, int T, int dk, int dv, int C,
+                      int dt, void *workspace, size_t workspace_bytes,
+                      void *stream, int algo);
+
+/* Scratch bytes dn_chunk_fwd needs for this problem (0 means none). */
+DN_API size_t dn_chunk_fwd_workspace_bytes(int B, int H, int T, int dk, int dv,
+                                    int C, int dt);
+
+/*
+ * dn_recurrent_step -- one decoding step, fused: for every (b, h) it reads
+ * the state once, forms p = S k and r = S q (reductions over dk), sets
+ * u = beta (v - p), writes S <- S + u k^T back in place and returns
+ * o = S_new q = r + (k . q) u.  This is the error-correcting update of
+ * "DeltaNet : écrire l'erreur de prédiction plutôt que la valeur" followed
+ * by the read, as the fused recurrent kernel of "Kernel Triton récurrent
+ * fusionné pour le décodage" (fr.news.hada.io/topic?id=31925) performs it.
+ *
+ * Arguments:
+ *   q, k  [B, H, dk]      dtype `dt`
+ *   v     [B, H, dv]      dtype `dt`
+ *   beta  [B, H]          dtype `dt`
+ *   S     [B, H, dk, dv]  fp32 state, updated in place
+ *   o     [B, H, dv]      dtype `dt`, written; must not overlap any input
+ *   B, H >= 0; dk, dv 64 or 128; dt DN_F32 or DN_BF16; stream cudaStream_t.
+ * Errors: DN_ERR_INVALID_ARG, DN_ERR_UNSUPPORTED (other dk, dv), DN_ERR_CUDA.
+ */
+DN_API int dn_recurrent_step(const void *q, const void *k, const void *v,
+                      const void *beta, float *S, void *o,
+                      int B, int H, int dk, int dv, int dt, void *stream);
+
+/* Static text for a dn_status value. */
+DN_API const char *dn_status_string(int status);
+
+/* Detail of the last non-OK return on the calling thread ("" if none).  The
+ * pointer stays valid until the next call into the library on this thread. */
+DN_API const char *dn_last_error(void);
+
+/* ABI version of this header (bumped on incompatible changes). */
+DN_API int dn_abi_version(void);
+
+#define DN_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DELTANET_H */

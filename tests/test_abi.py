@@ -1,0 +1,111 @@
+"""The C-ABI library loads and exports what include/deltanet.h declares.
+
+CPU only: nothing here launches a kernel.  The argument checks exercised
+return before the library makes any CUDA call.
+"""
+import ctypes
+import subprocess
+
+import pytest
+
+import delta_rule_recurrent_gb300 as dn
+from delta_rule_recurrent_gb300 import _lib, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def test_header_declares_the_boundary():
+    names = _lib.header_symbols()
+    for required in ("dn_chunk_fwd", "dn_recurrent_step", "dn_status_string",
+                     "dn_last_error"):
+        assert required in names
+    assert set(names) == set(_lib.SIGNATURES), "binding signatures drift from the header"
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", str(_lib.lib_path())],
+                         check=True, capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in _lib.header_symbols():
+        assert name in exported, f"{name} declared but not exported"
+        assert getattr(lib, name) is not None
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.dn_abi_version() == 1
+    assert lib.dn_status_string(0) == b"DN_OK"
+    assert lib.dn_status_string(1) == b"DN_ERR_INVALID_ARG"
+    assert lib.dn_status_string(2) == b"DN_ERR_UNSUPPORTED"
+    assert lib.dn_status_string(3) == b"DN_ERR_CUDA"
+    assert lib.dn_status_string(99) == b"DN_UNKNOWN_STATUS"
+
+
+def test_workspace_is_zero(lib):
+    assert lib.dn_chunk_fwd_workspace_bytes(8, 16, 2048, 128, 128, 64, 1) == 0
+
+
+def _chunk(lib, B=1, H=1, T=64, dk=64, dv=64, C=64, dt=1, algo=0):
+    return lib.dn_chunk_fwd_algo(None, None, None, None, None, None, None, B, H, T, dk, dv,
+                                 C, dt, None, 0, None, algo)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=-1), _lib.DN_ERR_INVALID_ARG),
+    (dict(T=-5), _lib.DN_ERR_INVALID_ARG),
+    (dict(dt=7), _lib.DN_ERR_INVALID_ARG),
+    (dict(algo=9), _lib.DN_ERR_INVALID_ARG),
+    (dict(dk=0), _lib.DN_ERR_INVALID_ARG),
+    (dict(dk=96), _lib.DN_ERR_UNSUPPORTED),
+    (dict(dv=256), _lib.DN_ERR_UNSUPPORTED),
+    (dict(C=32), _lib.DN_ERR_UNSUPPORTED),
+    (dict(B=0), _lib.DN_OK),
+    (dict(H=0, T=100), _lib.DN_OK),
+])
+def test_chunk_argument_checks_before_cuda(lib, kw, status):
+    assert _chunk(lib, **kw) == status
+    if status != _lib.DN_OK:
+        assert lib.dn_last_error()  # a detail message is set
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=-1), _lib.DN_ERR_INVALID_ARG),
+    (dict(dt=3), _lib.DN_ERR_INVALID_ARG),
+    (dict(dk=32), _lib.DN_ERR_UNSUPPORTED),
+    (dict(B=0), _lib.DN_OK),
+])
+def test_decode_argument_checks_before_cuda(lib, kw, status):
+    a = dict(B=2, H=2, dk=128, dv=128, dt=1)
+    a.update(kw)
+    assert lib.dn_recurrent_step(None, None, None, None, None, None, a["B"], a["H"], a["dk"],
+                                 a["dv"], a["dt"], None) == status
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 1, 4, 64)
+    with pytest.raises(ValueError):
+        dn.chunk_fwd(q, q, q, torch.zeros(1, 1, 4))
+
+
+def test_check_raises_with_detail(lib):
+    _chunk(lib, dk=96)
+    with pytest.raises(dn.DeltaNetError, match="UNSUPPORTED"):
+        _lib.check(_lib.DN_ERR_UNSUPPORTED)
+
+
+def test_last_error_is_per_thread(lib):
+    import threading
+    _chunk(lib, dk=96)
+    seen = {}
+
+    def other():
+        seen["msg"] = lib.dn_last_error()
+    th = threading.Thread(target=other)
+    th.start()
+    th.join()
+    assert seen["msg"] == b""
+    assert lib.dn_last_error() != b""

@@ -1,0 +1,171 @@
+"""Chunkwise forward on the GPU against the fp64 oracle (through the C ABI).
+
+Bars: relative L2 <= 1e-4 for fp32 I/O and <= 1e-2 for bf16 I/O, separately
+on o and on the final state.  Full-size workloads are checked on sampled
+(batch, head) pairs, each of which the oracle recomputes in full; every
+head is independent, so a sample is an exact sub-problem.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.conftest import rel_l2
+from tests.gpu_util import TOL, dev, run_chunk, sample_heads, take_heads
+
+pytestmark = pytest.mark.gpu
+
+ALGOS_BF16 = ["simt", "auto"]
+
+
+def _check(o, S, o_ref, S_ref, dtype, what=""):
+    eo, eS = rel_l2(o, o_ref), rel_l2(S, S_ref)
+    assert eo <= TOL[dtype], f"{what} o rel L2 {eo:.3e}"
+    assert eS <= TOL[dtype], f"{what} S_T rel L2 {eS:.3e}"
+    return eo, eS
+
+
+def test_tiny_fp32_workload():
+    """B1 H2 T256 d64, fp32 I/O: the whole output and state."""
+    inp = workloads.workload_inputs("tiny_fp32")
+    o, S = run_chunk(inp)
+    o_ref, S_ref = oracle.forward(inp.q, inp.k, inp.v, inp.beta, inp.S0)
+    _check(o, S, o_ref, S_ref, torch.float32, "tiny")
+
+
+@pytest.mark.parametrize("algo", ALGOS_BF16)
+def test_recall_workload(algo):
+    """B4 H4 T1024 d64 bf16 associative recall: oracle parity and the closed
+    form (each re-queried key returns its stored value)."""
+    inp, expect = workloads.workload_inputs("recall_bf16")
+    o, S = run_chunk(inp, algo)
+    o_ref, S_ref = oracle.forward(inp.q, inp.k, inp.v, inp.beta, inp.S0)
+    _check(o, S, o_ref, S_ref, torch.bfloat16, "recall")
+    assert rel_l2(o, expect) <= 1e-2
+
+
+@pytest.mark.parametrize("algo", ALGOS_BF16)
+def test_layer_1p3b_workload_sampled_heads(algo):
+    """B8 H16 T2048 d128 bf16 (the 1.3B-layer shape), full launch; 12 sampled
+    heads recomputed by the oracle."""
+    inp = workloads.workload_inputs("layer1p3b_bf16")
+    o, S = run_chunk(inp, algo)
+    B, H = inp.q.shape[:2]
+    bi, hi = sample_heads(B, H, 12, seed=5)
+    o_ref, S_ref = oracle.forward(*(take_heads(x, bi, hi) for x in (inp.q, inp.k, inp.v, inp.beta)),
+                                  take_heads(inp.S0, bi, hi))
+    _check(o[bi, hi][None], S[bi, hi][None], o_ref, S_ref, torch.bfloat16, "1.3B layer")
+    assert np.isfinite(o).all() and np.isfinite(S).all()
+
+
+@pytest.mark.parametrize("algo", ALGOS_BF16)
+def test_long_prefill_workload_sampled_heads(algo):
+    """B1 H16 T32768 d128 bf16 with an fp32 initial state; 2 heads checked."""
+    inp = workloads.workload_inputs("long_prefill_bf16")
+    o, S = run_chunk(inp, algo)
+    bi, hi = np.array([0, 0]), np.array([0, 15])
+    o_ref, S_ref = oracle.forward(*(take_heads(x, bi, hi) for x in (inp.q, inp.k, inp.v, inp.beta)),
+                                  take_heads(inp.S0, bi, hi))
+    _check(o[bi, hi][None], S[bi, hi][None], o_ref, S_ref, torch.bfloat16, "long prefill")
+    assert np.isfinite(o).all() and np.isfinite(S).all()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64), (128, 128)])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
+def test_shapes_and_ragged_tails(dtype, dk, dv, T):
+    """Every supported (dk, dv), both dtypes, sequences shorter than, equal
+    to and not a multiple of the 64-token chunk, with a carried state."""
+    inp = workloads.chunk_inputs(2, 3, T, dk, dv, dtype=dtype, seed=T * 7 + dk + dv,
+                                 s0_std=0.3)
+    o, S = run_chunk(inp)
+    o_ref, S_ref = oracle.forward(inp.q, inp.k, inp.v, inp.beta, inp.S0)
+    _check(o, S, o_ref, S_ref, inp.q.dtype, f"{dtype} dk{dk} dv{dv} T{T}")
+
+
+def test_negative_eigenvalue_beta():
+    """beta in (0, 2) through the chunk path."""
+    inp = workloads.chunk_inputs(2, 2, 300, 128, 128, dtype="bf16", seed=77, beta_scale=2.0,
+                                 s0_std=0.1)
+    o, S = run_chunk(inp)
+    o_ref, S_ref = oracle.forward(inp.q, inp.k, inp.v, inp.beta, inp.S0)
+    _check(o, S, o_ref, S_ref, torch.bfloat16, "beta in (0,2)")
+
+
+def test_beta_zero_keeps_state_fp32():
+    inp = workloads.chunk_inputs(1, 2, 130, 64, 64, dtype="f32", seed=3, s0_std=0.5)
+    inp.beta.zero_()
+    o, S = run_chunk(inp)
+    assert rel_l2(S, inp.S0.double().numpy()) <= 1e-6
+    o_ref = np.einsum("bhij,bhti->bhtj", inp.S0.double().numpy(), inp.q.double().numpy())
+    assert rel_l2(o, o_ref) <= 1e-5
+
+
+def test_zero_length_sequence_copies_state():
+    import delta_rule_recurrent_gb300 as dn
+    S0 = torch.randn(2, 3, 64, 64, device="cuda:0")
+    q = torch.zeros(2, 3, 0, 64, device="cuda:0")
+    beta = torch.zeros(2, 3, 0, device="cuda:0")
+    o, S = dn.chunk_fwd(q, q, q, beta, initial_state=S0)
+    torch.cuda.synchronize()
+    assert o.shape == (2, 3, 0, 64) and torch.equal(S, S0)
+    _, Sz = dn.chunk_fwd(q, q, q, beta)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(Sz) == 0
+
+
+def test_state_updated_in_place_and_optional():
+    import delta_rule_recurrent_gb300 as dn
+    inp = workloads.chunk_inputs(1, 2, 100, 128, 128, dtype="bf16", seed=9, s0_std=0.2)
+    o_ref, S_ref = oracle.forward(inp.q, inp.k, inp.v, inp.beta, inp.S0)
+    S = dev(inp.S0)
+    o, S_out = dn.chunk_fwd(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta),
+                            initial_state=S, final_state=S)
+    torch.cuda.synchronize()
+    assert S_out.data_ptr() == S.data_ptr()
+    _check(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref, torch.bfloat16)
+    o2, none = dn.chunk_fwd(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta),
+                            initial_state=dev(inp.S0), output_final_state=False)
+    torch.cuda.synchronize()
+    assert none is None
+    assert rel_l2(o2.double().cpu().numpy(), o_ref) <= 1e-2
+
+
+def test_prefill_then_decode_handoff():
+    """Chunk forward over a prefix, then decoding steps from its final state,
+    equals the oracle over the whole sequence."""
+    import delta_rule_recurrent_gb300 as dn
+    full = workloads.chunk_inputs(2, 4, 150, 128, 128, dtype="bf16", seed=12)
+    o_ref, S_ref = oracle.forward(full.q, full.k, full.v, full.beta, None)
+    P = 140
+    o_pre, S = dn.chunk_fwd(dev(full.q[:, :, :P].contiguous()), dev(full.k[:, :, :P].contiguous()),
+                            dev(full.v[:, :, :P].contiguous()),
+                            dev(full.beta[:, :, :P].contiguous()))
+    outs = [o_pre]
+    for t in range(P, 150):
+        outs.append(dn.recurrent_step(dev(full.q[:, :, t].contiguous()),
+                                      dev(full.k[:, :, t].contiguous()),
+                                      dev(full.v[:, :, t].contiguous()),
+                                      dev(full.beta[:, :, t].contiguous()), S)[:, :, None])
+    torch.cuda.synchronize()
+    o = torch.cat(outs, dim=2).double().cpu().numpy()
+    _check(o, S.double().cpu().numpy(), o_ref, S_ref, torch.bfloat16, "handoff")
+
+
+def test_rejects_bad_pointers_without_launching():
+    from delta_rule_recurrent_gb300 import _lib
+    lib = _lib.load()
+    B, H, T, d = 1, 2, 64, 64
+    q = torch.zeros(B, H, T, d, dtype=torch.bfloat16, device="cuda:0")
+    beta = torch.zeros(B, H, T, dtype=torch.bfloat16, device="cuda:0")
+    o = torch.zeros_like(q)
+    host = torch.zeros_like(q, device="cpu")
+    call = lambda qp, op: lib.dn_chunk_fwd(qp, q.data_ptr(), q.data_ptr(), beta.data_ptr(),
+                                           None, op, None, B, H, T, d, d, 64, 1, None, 0, None)
+    assert call(host.data_ptr(), o.data_ptr()) == _lib.DN_ERR_INVALID_ARG      # host memory
+    assert call(q.data_ptr() + 2, o.data_ptr()) == _lib.DN_ERR_INVALID_ARG     # misaligned
+    assert call(q.data_ptr(), q.data_ptr()) == _lib.DN_ERR_INVALID_ARG         # o aliases q
+    assert call(None, o.data_ptr()) == _lib.DN_ERR_INVALID_ARG                 # NULL
+    assert call(q.data_ptr(), o.data_ptr()) == _lib.DN_OK
+    torch.cuda.synchronize()

@@ -32,6 +32,7 @@ SIGNATURES = {
     "dn_status_string": (ctypes.c_char_p, [_int]),
     "dn_last_error": (ctypes.c_char_p, []),
     "dn_abi_version": (_int, []),
+    "dn_device_error": (_int, []),
 }
 
 _lib = None

@@ -93,6 +93,15 @@ const char* dn_last_error(void) { return g_last_error; }
 
 int dn_abi_version(void) { return DN_ABI_VERSION; }
 
+int dn_device_error(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    const unsigned int e = dn::chunk_tc_take_device_error();
+    return e == ~0u ? -1 : (int)e;
+}
+
 size_t dn_chunk_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt) {
     (void)B; (void)H; (void)T; (void)dk; (void)dv; (void)C; (void)dt;
     return 0;

@@ -20,6 +20,7 @@
 // data; the key-side work (A, X, Q K^T) is recomputed per slice.
 #include "dn_common.cuh"
 #include "dn_internal.h"
+#include "tri_inverse.cuh"
 
 namespace dn {
 namespace {
@@ -52,55 +53,6 @@ __device__ __forceinline__ void zero(float (&acc)[M / 16][N / 16]) {
     for (int i = 0; i < M / 16; ++i)
 #pragma unroll
         for (int j = 0; j < N / 16; ++j) acc[i][j] = 0.f;
-}
-
-// X = (I + A)^{-1} for a strictly lower-triangular 64 x 64 A (row pitch kLC),
-// by blocks of 16: the four diagonal blocks by column-wise substitution,
-// then X_ij = -X_ii sum_{l=j}^{i-1} A_il X_lj one block diagonal at a time.
-// Ys is 3 x 16 x 17 floats of scratch.  Ends with a barrier.
-__device__ void unit_lower_inverse64(const float* __restrict__ Am,
-                                     float* __restrict__ Xm, float* __restrict__ Ys) {
-    const int tid = threadIdx.x;
-    if (tid < 64) {
-        const int base = (tid >> 4) * 16, c = tid & 15;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = (r == c) ? 1.f : 0.f;
-#pragma unroll
-            for (int l = 0; l < r; ++l) acc = fmaf(-Am[(base + r) * kLC + base + l], x[l], acc);
-            x[r] = (r < c) ? 0.f : acc;
-            Xm[(base + r) * kLC + base + c] = x[r];
-        }
-    }
-    // Blocks above the diagonal are zero.
-    for (int e = tid; e < 6 * 256; e += kThreads) {
-        const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
-        // (i, j) pairs with j > i: (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
-        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-        Xm[(16 * bi + r) * kLC + 16 * bj + c] = 0.f;
-    }
-    __syncthreads();
-    for (int d = 1; d < 4; ++d) {
-        const int nb = 4 - d;
-        for (int e = tid; e < nb * 256; e += kThreads) {
-            const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
-            float acc = 0.f;
-            for (int kk = 16 * j; kk < 16 * i; ++kk)
-                acc = fmaf(Am[(16 * i + r) * kLC + kk], Xm[kk * kLC + 16 * j + c], acc);
-            Ys[j * 272 + r * 17 + c] = acc;
-        }
-        __syncthreads();
-        for (int e = tid; e < nb * 256; e += kThreads) {
-            const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
-            float acc = 0.f;
-            for (int m = 0; m <= r; ++m)
-                acc = fmaf(Xm[(16 * i + r) * kLC + 16 * i + m], Ys[j * 272 + m * 17 + c], acc);
-            Xm[(16 * i + r) * kLC + 16 * j + c] = -acc;
-        }
-        __syncthreads();
-    }
 }
 
 template <int DK, int NV>
@@ -218,7 +170,7 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
                 }
         }
         // ---- X = (I + A)^{-1} (touches only Am, Xm, Ys; ends with a barrier) ----
-        unit_lower_inverse64(Am, Xm, Ys);
+        unit_lower_inverse64<kThreads>(Am, Xm, Ys);
 
         // ---- U' = X R' ----
         {

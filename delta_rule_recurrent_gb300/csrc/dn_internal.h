@@ -28,4 +28,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v,
                             float* S_T, int BH, int T, int dk, int dv, int dt,
                             cudaStream_t stream);
 
+// Returns and clears the error word the tensor-core kernel sets when one of
+// its bounded waits runs out (0 = none, ~0u = could not read it).  Synchronous.
+unsigned int chunk_tc_take_device_error();
+
 }  // namespace dn

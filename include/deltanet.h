@@ -136,6 +136,16 @@ DN_API int dn_recurrent_step(const void *q, const void *k, const void *v,
                       const void *beta, float *S, void *o,
                       int B, int H, int dk, int dv, int dt, void *stream);
 
+/*
+ * dn_device_error -- returns the first error code a kernel recorded on the
+ * device since the previous call (0 if none) and clears it.  Kernels whose
+ * internal waits are bounded record a code instead of hanging when a wait
+ * runs out (1: a TMA load never completed, 2: a tensor-core operation never
+ * completed); the outputs of such a call are then undefined.  This call
+ * synchronises the current device.  Returns -1 if the word could not be read.
+ */
+DN_API int dn_device_error(void);
+
 /* Static text for a dn_status value. */
 DN_API const char *dn_status_string(int status);
 

@@ -16,7 +16,17 @@ from tests.gpu_util import TOL, dev, run_chunk, sample_heads, take_heads
 
 pytestmark = pytest.mark.gpu
 
-ALGOS_BF16 = ["simt", "auto"]
+ALGOS_BF16 = ["simt", "tcgen05"]
+
+
+@pytest.fixture(autouse=True)
+def no_device_error():
+    """Every test must leave no device-side error recorded by a kernel."""
+    from delta_rule_recurrent_gb300 import _lib
+    lib = _lib.load()
+    assert lib.dn_device_error() == 0
+    yield
+    assert lib.dn_device_error() == 0
 
 
 def _check(o, S, o_ref, S_ref, dtype, what=""):
@@ -34,7 +44,7 @@ def test_tiny_fp32_workload():
     _check(o, S, o_ref, S_ref, torch.float32, "tiny")
 
 
-@pytest.mark.parametrize("algo", ALGOS_BF16)
+@pytest.mark.parametrize("algo", ["simt", "auto"])
 def test_recall_workload(algo):
     """B4 H4 T1024 d64 bf16 associative recall: oracle parity and the closed
     form (each re-queried key returns its stored value)."""
@@ -82,6 +92,25 @@ def test_shapes_and_ragged_tails(dtype, dk, dv, T):
     o, S = run_chunk(inp)
     o_ref, S_ref = oracle.forward(inp.q, inp.k, inp.v, inp.beta, inp.S0)
     _check(o, S, o_ref, S_ref, inp.q.dtype, f"{dtype} dk{dk} dv{dv} T{T}")
+
+
+@pytest.mark.parametrize("T", [1, 37, 64, 65, 200, 1000])
+@pytest.mark.parametrize("with_s0", [False, True])
+def test_tensor_core_path_ragged(T, with_s0):
+    """The tcgen05 kernel on sequences shorter than, equal to and not a
+    multiple of the chunk, with and without a carried state."""
+    inp = workloads.chunk_inputs(3, 2, T, 128, 128, dtype="bf16", seed=100 + T,
+                                 feature_map="silu", s0_std=0.1 if with_s0 else None)
+    o, S = run_chunk(inp, "tcgen05")
+    o_ref, S_ref = oracle.forward(inp.q, inp.k, inp.v, inp.beta, inp.S0)
+    _check(o, S, o_ref, S_ref, torch.bfloat16, f"tcgen05 T{T}")
+
+
+def test_tensor_core_rejects_other_shapes():
+    from delta_rule_recurrent_gb300 import _lib
+    inp = workloads.chunk_inputs(1, 1, 64, 64, 64, dtype="bf16", seed=1)
+    with pytest.raises(_lib.DeltaNetError, match="UNSUPPORTED"):
+        run_chunk(inp, "tcgen05")
 
 
 def test_negative_eigenvalue_beta():

@@ -40,6 +40,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of the same condition (for loops that poll several barriers).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase with the given parity to complete; gives up (returns
 // false) after timeout_ns of wall time instead of spinning forever.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
@@ -72,6 +84,12 @@ __device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int 
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::
                      "l"(map),
                  "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+// Asks the TMA unit to pull one box of a tensor into L2 ahead of its load.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(map),
+                 "r"(x), "r"(y), "r"(z)
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() {

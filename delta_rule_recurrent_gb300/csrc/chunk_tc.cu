@@ -85,15 +85,18 @@ enum : int {
     B_G_EMPTY = 18,   // [2] chunk group finished with its G / PT columns
     B_V_FULL = 20,    // v tile landed
     B_V_EMPTY = 21,   // D1 = [PT;Tm] V done (v tile free)
-    B_DW_FULL = 22,   // DW = [PT;Tm] K done
-    B_DW_EMPTY = 23,  // chunk group finished reading DW
-    B_SB_FULL = 24,   // S bf16 operand written
-    B_D1_FULL = 25,   // D1 += [Q';-W] S done
-    B_U_FULL = 26,    // U' written
-    B_D1_EMPTY = 27,  // state group finished reading D1
-    B_S_READY = 28,   // S += K^T U' done
-    B_DRAIN = 29,     // final drain of the MMA pipe
+    B_DW_FULL = 22,   // [2] DW = [PT;Tm] K done (one per chunk group)
+    B_DW_EMPTY = 24,  // chunk group finished reading DW
+    B_SB_FULL = 25,   // S bf16 operand written
+    B_D1_FULL = 26,   // D1 += [Q';-W] S done
+    B_U_FULL = 27,    // U' written
+    B_D1_EMPTY = 28,  // state group finished reading D1
+    B_S_READY = 29,   // S += K^T U' done
+    B_DRAIN = 30,     // final drain of the MMA pipe
 };
+// Parity waits are only unambiguous when a barrier cannot run two phases
+// ahead of its waiter, so every barrier has exactly one waiting role, which
+// consumes its phases in order.
 
 // TMEM columns (512 allocated): S | D1 (O, U') | DW (PT K, W) | G/PT even | G/PT odd
 constexpr uint32_t COL_S = 0, COL_D1 = 128, COL_DW = 256, COL_G = 384;
@@ -389,7 +392,7 @@ __device__ void mma_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int nchu
             for (int kk = 0; kk < 4; ++kk)
                 mma_bf16_ss(tmem + COL_DW, sw128_desc(tp + 32u * kk, 16, 1024),
                             sw128_desc(kqw + 2048u * kk, kRegKQW, 1024), IDESC_KB, kk > 0);
-            mma_commit(ctl.bar(B_DW_FULL));
+            mma_commit(ctl.bar(B_DW_FULL + (nDW & 1)));
             ++nDW;
             issued = true;
         } else if (nPT < nG && ready(B_TP_READY + (nPT & 1), nPT >> 1)) {
@@ -604,7 +607,7 @@ __device__ void chunk_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
             mbar_arrive(ctl.bar(B_G_EMPTY + g));
         }
 
-        ok = ctl.wait(B_DW_FULL, (uint32_t)c);
+        ok = ctl.wait(B_DW_FULL + g, (uint32_t)it);
         if (wg_sync_or(barid, !ok)) return;
         tc_fence_after_sync();
         // rows 0-63: Q' = Q - PT K over the Q rows; rows 64-127: -W into the W rows.

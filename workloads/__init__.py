@@ -206,22 +206,24 @@ def workload_inputs(name: str, **overrides):
 
 def decode_inputs_on_device(B: int, H: int, dk: int, dv: int, steps: int, *,
                             dtype="bf16", seed: int = 0, beta_scale: float = 2.0,
-                            device="cuda"):
-    """All ``steps`` decoding steps' inputs drawn at once on the device (for
-    timing runs, where CPU generation of gigabytes would dominate): same
-    recipe as ``decode_step_inputs``, drawn from a seeded device generator.
-    Returns q, k ``[steps, B, H, dk]``, v ``[steps, B, H, dv]``, beta
-    ``[steps, B, H]`` in the I/O dtype."""
+                            device="cuda", block: int = 64):
+    """All ``steps`` decoding steps' inputs drawn on the device (for timing
+    runs, where CPU generation of gigabytes would dominate): same recipe as
+    ``decode_step_inputs``, drawn from a seeded device generator ``block``
+    steps at a time.  Returns q, k ``[steps, B, H, dk]``, v
+    ``[steps, B, H, dv]``, beta ``[steps, B, H]`` in the I/O dtype."""
     g = torch.Generator(device=device).manual_seed(int(seed))
     dt = torch_dtype(dtype)
     q = torch.empty(steps, B, H, dk, dtype=dt, device=device)
     k = torch.empty_like(q)
     v = torch.empty(steps, B, H, dv, dtype=dt, device=device)
     beta = torch.empty(steps, B, H, dtype=dt, device=device)
-    for s in range(steps):  # one step at a time keeps the fp32 temporaries small
-        q[s] = l2norm(torch.randn(B, H, dk, generator=g, device=device)).to(dt)
-        k[s] = l2norm(torch.randn(B, H, dk, generator=g, device=device)).to(dt)
-        v[s] = torch.randn(B, H, dv, generator=g, device=device).to(dt)
-        beta[s] = (torch.sigmoid(torch.randn(B, H, generator=g, device=device))
-                   * float(beta_scale)).to(dt)
+    for s0 in range(0, steps, block):
+        n = min(block, steps - s0)
+        sl = slice(s0, s0 + n)
+        q[sl] = l2norm(torch.randn(n, B, H, dk, generator=g, device=device)).to(dt)
+        k[sl] = l2norm(torch.randn(n, B, H, dk, generator=g, device=device)).to(dt)
+        v[sl] = torch.randn(n, B, H, dv, generator=g, device=device).to(dt)
+        beta[sl] = (torch.sigmoid(torch.randn(n, B, H, generator=g, device=device))
+                    * float(beta_scale)).to(dt)
     return q, k, v, beta

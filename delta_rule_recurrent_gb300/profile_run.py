@@ -1,0 +1,54 @@
+"""Runs one workload a few times through the public API, for profiler captures.
+
+    python -m delta_rule_recurrent_gb300.profile_run chunk [--B 8] [--T 2048] [--algo auto] [--reps 3]
+    python -m delta_rule_recurrent_gb300.profile_run decode [--B 256] [--steps 4]
+
+`chunk` runs the chunkwise forward on the 1.3B-layer shape (B8 H16 T2048
+dk=dv=128, bf16; B and T can be reduced); `decode` runs consecutive decoding
+steps on the decode workload's shape (B256 H16 dk=dv=128, fp32 state).  Inputs
+come from the seeded generators in `workloads`.
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+from pathlib import Path
+
+sys.path.insert(0, str(Path(__file__).resolve().parent.parent))
+
+
+def main(argv=None):
+    import torch
+
+    import delta_rule_recurrent_gb300 as dn
+    import workloads
+
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("what", choices=["chunk", "decode"])
+    ap.add_argument("--B", type=int, default=None)
+    ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--algo", default="auto", choices=list(dn.ALGOS))
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=4)
+    a = ap.parse_args(argv)
+    dev = torch.device("cuda:0")
+    if a.what == "chunk":
+        over = {k: v for k, v in (("B", a.B), ("T", a.T)) if v is not None}
+        inp = workloads.workload_inputs("layer1p3b_bf16", **over)
+        q, k, v, b = (x.to(dev) for x in (inp.q, inp.k, inp.v, inp.beta))
+        for _ in range(a.reps):
+            o, _ = dn.chunk_fwd(q, k, v, b, algo=a.algo)
+    else:
+        w = workloads.WORKLOADS["decode_bf16"]
+        B = a.B or w["B"]
+        q, k, v, b = workloads.decode_inputs_on_device(B, w["H"], w["dk"], w["dv"], a.steps,
+                                                       seed=3, device=dev)
+        S = torch.randn(B, w["H"], w["dk"], w["dv"], device=dev) * w["s0_std"]
+        for i in range(a.steps):
+            o = dn.recurrent_step(q[i], k[i], v[i], b[i], S)
+    torch.cuda.synchronize()
+    print("ok", float(o.float().abs().mean()))
+
+
+if __name__ == "__main__":
+    main()

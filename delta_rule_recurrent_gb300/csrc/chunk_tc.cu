@@ -17,18 +17,20 @@
 // dk -> U' -> bf16 -> S += K^T U'.
 //
 // One CTA owns one (batch, head) and keeps S in TMEM for the whole sequence.
-// Its 16 warps have fixed roles so the serial chain of chunk c overlaps the
-// state-independent work of chunks c+1 and c+2:
-//   warp 0      TMA producer (q, k, v tiles; 3-D maps, rows past the end read 0)
-//   warp 1      TMEM owner and the single MMA-issuing thread; it polls the
-//               readiness of every pending MMA and issues the state chain first
+// Its 16 warps have fixed roles so the state chain of chunk c overlaps the
+// state-independent work of the following chunks:
+//   warp 0      TMA producer: [K; Q] tiles into a 3-stage ring, v tiles
+//               (3-D maps, so rows past the end of a sequence read as zeros)
+//   warp 1      TMEM owner and the single MMA-issuing thread; it issues every
+//               MMA group whose inputs are ready, the state chain first
 //   warp 2      TMA store of o tiles (rows past the end are not written)
 //   warps 4-7   state group: S -> bf16 operand, O and U' epilogues, final state
-//   warps 8-11, 12-15   chunk groups for even and odd chunks: A, P, the
-//               triangular solve, Tm, PT, and the Q' / -W operands
-// Operand tiles use the 128-byte swizzled shared-memory layout that TMA
-// writes.  Every wait is bounded: on a timeout the CTA records an error code
-// (read back with dn_device_error), drains what it started and exits.
+//   warps 8-11, 12-15   chunk groups for even and odd chunks: A and P, the
+//               triangular solve, Tm, PT, and the [Q'; -W] operand
+// Operand tiles in shared memory use the 128-byte swizzled layout TMA writes;
+// [Q'; -W], the A operand of the state-dependent MMA, lives in TMEM.
+// Every wait is bounded: on a timeout the CTA records an error code (read
+// back with dn_device_error), drains what it started and exits.
 #include <cudaTypedefs.h>
 #include <cuda.h>
 
@@ -47,63 +49,72 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kC = 64;          // chunk length
-constexpr int kD = 128;         // dk = dv
-constexpr int kThreads = 512;   // 16 warps
+constexpr int kC = 64;         // chunk length
+constexpr int kD = 128;        // dk = dv
+constexpr int kThreads = 512;  // 16 warps
+constexpr int kStages = 3;     // [K; Q] ring depth
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s without progress
-constexpr int kP = 65;          // row pitch (floats) of the fp32 solve array
+// The polling roles count SM cycles (clock64 is cheap to read); at the
+// GB300's clocks 4e9 cycles is 2 s or more.
+constexpr long long kTimeoutCycles = 4000000000ll;
+constexpr int kP = 68;   // row pitch (floats) of the fp32 solve array: 16-byte rows,
+                         // and 8 consecutive rows of a 128-bit access hit 8 distinct bank groups
+constexpr int kYP = 36;  // row pitch of the 32 x 32 solve scratch
 
 // ---------------------------------------------------------------- smem map
-constexpr uint32_t kRegKQW = 192 * 128;              // one dk half of [K; Q'; -W]
-constexpr uint32_t kStageKQW = 2 * kRegKQW;
-constexpr uint32_t OFF_KQW = 0;                      // 2 stages
-constexpr uint32_t OFF_V = OFF_KQW + 2 * kStageKQW;  // V, 2 dv halves x 64 rows
-constexpr uint32_t OFF_TP = OFF_V + 16384;           // 2 stages of [PT; Tm]; then the O tile
+constexpr uint32_t kRegKQ = 128 * 128;               // one dk half of [K; Q]: 128 rows x 128 B
+constexpr uint32_t kStageKQ = 2 * kRegKQ;            // 32 KB
+constexpr uint32_t OFF_KQ = 0;                       // kStages stages
+constexpr uint32_t OFF_V = OFF_KQ + kStages * kStageKQ;  // V, 2 dv halves x 64 rows
+constexpr uint32_t OFF_TP = OFF_V + 16384;           // 2 x [PT; Tm] (per chunk group); then o tile
 constexpr uint32_t OFF_SB = OFF_TP + 2 * 16384;      // S as bf16 (2 x 128 rows); then U'
 constexpr uint32_t OFF_X = OFF_SB + 32768;           // 2 x fp32 64 x kP: A, overwritten by X
 constexpr uint32_t kXBytes = 64 * kP * 4;
-constexpr uint32_t OFF_Y = OFF_X + 2 * kXBytes;      // 2 x 3 x 16 x 16 fp32 solve scratch
-constexpr uint32_t OFF_BETA = OFF_Y + 2 * 3072;      // 2 x 64 fp32
+constexpr uint32_t OFF_Y = OFF_X + 2 * kXBytes;      // 2 x fp32 32 x kYP solve scratch
+constexpr uint32_t kYBytes = 32 * kYP * 4;
+constexpr uint32_t OFF_BETA = OFF_Y + 2 * kYBytes;   // 2 x 64 fp32
 constexpr uint32_t OFF_BAR = OFF_BETA + 512;         // mbarriers, 8 bytes each
-constexpr int kNumBars = 32;
+constexpr int kNumBars = 36;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * kNumBars;  // abort flag, TMEM address
 constexpr uint32_t kSmemBytes = OFF_MISC + 16 + 1024;  // + 1024-byte alignment slack
 static_assert(OFF_V % 1024 == 0 && OFF_TP % 1024 == 0 && OFF_SB % 1024 == 0, "tile alignment");
+static_assert(OFF_X % 16 == 0 && OFF_Y % 16 == 0 && OFF_BETA % 16 == 0, "vector alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-// mbarrier indices ([2] = one per chunk parity)
+// mbarrier indices.  Every barrier has exactly one waiting role, which
+// consumes its phases in order, so a parity test can never see a phase two
+// ahead of the one it asks for.
 enum : int {
-    B_KQ_FULL = 0,    // [2] q, k tiles landed
-    B_KQ_EMPTY = 2,   // [2] stage's last reader (S += K^T U') completed
-    B_TP_READY = 4,   // [2] P and Tm written (chunk group)
-    B_TP_FULL = 6,    // [2] PT written over P (chunk group)
-    B_QW_READY = 8,   // [2] Q' and -W written (chunk group)
-    B_O_FULL = 10,    // [2] O tile written (state group)
-    B_O_FREE = 12,    // [2] O tile stored (store warp)
-    B_G_FULL = 14,    // [2] G = [K;Q] K^T done
-    B_PT_FULL = 16,   // [2] PT = P Tm done
-    B_G_EMPTY = 18,   // [2] chunk group finished with its G / PT columns
-    B_V_FULL = 20,    // v tile landed
-    B_V_EMPTY = 21,   // D1 = [PT;Tm] V done (v tile free)
-    B_DW_FULL = 22,   // [2] DW = [PT;Tm] K done (one per chunk group)
-    B_DW_EMPTY = 24,  // chunk group finished reading DW
-    B_SB_FULL = 25,   // S bf16 operand written
-    B_D1_FULL = 26,   // D1 += [Q';-W] S done
-    B_U_FULL = 27,    // U' written
-    B_D1_EMPTY = 28,  // state group finished reading D1
-    B_S_READY = 29,   // S += K^T U' done
-    B_DRAIN = 30,     // final drain of the MMA pipe
+    B_KQ_FULL = 0,    // [3] q, k tiles of a stage landed
+    B_KQ_EMPTY = 3,   // [3] the stage's last reader (S += K^T U') completed
+    B_TP_READY = 6,   // [2] P and Tm written (chunk group)
+    B_TP_FULL = 8,    // [2] PT written over P (chunk group)
+    B_QW_READY = 10,  // [2] [Q'; -W] written to TMEM (chunk group)
+    B_O_FULL = 12,    // [2] o tile written (state group)
+    B_O_FREE = 14,    // [2] o tile stored (store warp)
+    B_G_FULL = 16,    // [2] G = [K;Q] K^T done
+    B_PT_FULL = 18,   // [2] PT = P Tm done
+    B_G_EMPTY = 20,   // [2] chunk group finished with its TMEM columns
+    B_DW_FULL = 22,   // [2] DW = [PT;Tm] K done
+    B_QW_FREE = 24,   // [2] the previous chunk's D1 += [Q';-W] S has read [Q'; -W]
+    B_V_FULL = 26,    // v tile landed
+    B_V_EMPTY = 27,   // D1 = [PT;Tm] V done (v tile free)
+    B_DW_EMPTY = 28,  // chunk group finished reading DW (shared upper half)
+    B_SB_FULL = 29,   // S bf16 operand written
+    B_D1_FULL = 30,   // D1 += [Q';-W] S done
+    B_U_FULL = 31,    // U' written
+    B_D1_EMPTY = 32,  // state group finished reading D1
+    B_S_READY = 33,   // S += K^T U' done
+    B_DRAIN = 34,     // final drain of the MMA pipe
 };
-// Parity waits are only unambiguous when a barrier cannot run two phases
-// ahead of its waiter, so every barrier has exactly one waiting role, which
-// consumes its phases in order.
 
-// TMEM columns (512 allocated): S | D1 (O, U') | DW (PT K, W) | G/PT even | G/PT odd
-constexpr uint32_t COL_S = 0, COL_D1 = 128, COL_DW = 256, COL_G = 384;
+// TMEM columns (512 allocated):
+//   S | D1 (O, U') | [Q'; -W] bf16 | G, PT, DW[:, 0:64] per chunk group x 2 | DW[:, 64:128]
+constexpr uint32_t COL_S = 0, COL_D1 = 128, COL_QW = 256, COL_G = 320, COL_DWX = 448;
 
 constexpr uint32_t IDESC_G = idesc_bf16_f32(128, 64, 0, 0);    // [K;Q] K^T
-constexpr uint32_t IDESC_PT = idesc_bf16_f32(128, 64, 0, 1);   // [P;Tm] Tm
-constexpr uint32_t IDESC_KB = idesc_bf16_f32(128, 128, 0, 1);  // A K-major, B MN-major
+constexpr uint32_t IDESC_N64 = idesc_bf16_f32(128, 64, 0, 1);  // A K-major, B MN-major, N = 64
+constexpr uint32_t IDESC_KB = idesc_bf16_f32(128, 128, 0, 1);  // A K-major (smem or TMEM), B MN-major
 constexpr uint32_t IDESC_MM = idesc_bf16_f32(128, 128, 1, 1);  // both MN-major
 
 enum : unsigned { kErrTimeout = 1 };
@@ -135,6 +146,21 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                  : "memory");
     return v;
 }
+__device__ __forceinline__ void tmem_ld64f(uint32_t taddr, float (&x)[64]) {
+    uint32_t r[64];
+    tmem_ld64(taddr, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(r[i]);
+}
+// 64 fp32 values -> bf16 into the 8 chunks of row r of a swizzled region.
+__device__ __forceinline__ void store_row64_bf16(uint32_t region, int r, const float (&x)[64]) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        st_shared_v4(region + sw128(r, c), pack_bf16(x[8 * c + 0], x[8 * c + 1]),
+                     pack_bf16(x[8 * c + 2], x[8 * c + 3]), pack_bf16(x[8 * c + 4], x[8 * c + 5]),
+                     pack_bf16(x[8 * c + 6], x[8 * c + 7]));
+}
 // 32 fp32 values -> bf16 into 4 consecutive chunks (from ch0) of row r.
 __device__ __forceinline__ void store_row32_bf16(uint32_t region, int r, int ch0,
                                                  const float (&x)[32]) {
@@ -144,13 +170,15 @@ __device__ __forceinline__ void store_row32_bf16(uint32_t region, int r, int ch0
                      pack_bf16(x[8 * c + 2], x[8 * c + 3]), pack_bf16(x[8 * c + 4], x[8 * c + 5]),
                      pack_bf16(x[8 * c + 6], x[8 * c + 7]));
 }
-__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&x)[32]) {
-    uint32_t r[32];
-    tmem_ld32(taddr, r);
-    tmem_wait_ld();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+__device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void sts4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void fma4(float4& acc, float a, const float4& b) {
+    acc.x = fmaf(a, b.x, acc.x);
+    acc.y = fmaf(a, b.y, acc.y);
+    acc.z = fmaf(a, b.z, acc.z);
+    acc.w = fmaf(a, b.w, acc.w);
 }
+__device__ __forceinline__ float4 neg4(float4 v) { return make_float4(-v.x, -v.y, -v.z, -v.w); }
 // Named barrier over one 128-thread warpgroup.
 __device__ __forceinline__ void wg_sync(int id) {
     asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
@@ -201,21 +229,30 @@ struct Ctl {
     }
 };
 
+// Group wait: thread 0 of the warpgroup polls the barrier, the others sleep
+// in the named barrier.  True for the whole group, or false for the whole
+// group if the wait gave up.
+__device__ __forceinline__ bool wg_wait(const Ctl& ctl, int b, uint32_t parity, int t, int barid) {
+    bool ok = true;
+    if (t == 0) ok = ctl.wait(b, parity);
+    return !wg_sync_or(barid, !ok);
+}
+
 struct Smem {
     uint32_t base;   // shared address of the 1024-aligned base
     uint8_t* gbase;  // generic pointer to it
-    __device__ uint32_t kqw(int s) const { return base + OFF_KQW + (uint32_t)s * kStageKQW; }
-    __device__ uint32_t tp(int s) const { return base + OFF_TP + (uint32_t)s * 16384u; }
+    __device__ uint32_t kq(int s) const { return base + OFF_KQ + (uint32_t)s * kStageKQ; }
+    __device__ uint32_t tp(int g) const { return base + OFF_TP + (uint32_t)g * 16384u; }
     __device__ uint32_t v() const { return base + OFF_V; }
     __device__ uint32_t sb() const { return base + OFF_SB; }
-    __device__ float* x(int s) const {
-        return reinterpret_cast<float*>(gbase + OFF_X + (uint32_t)s * kXBytes);
+    __device__ float* x(int g) const {
+        return reinterpret_cast<float*>(gbase + OFF_X + (uint32_t)g * kXBytes);
     }
-    __device__ float* y(int s) const {
-        return reinterpret_cast<float*>(gbase + OFF_Y + (uint32_t)s * 3072u);
+    __device__ float* y(int g) const {
+        return reinterpret_cast<float*>(gbase + OFF_Y + (uint32_t)g * kYBytes);
     }
-    __device__ float* beta(int s) const {
-        return reinterpret_cast<float*>(gbase + OFF_BETA + (uint32_t)s * 256u);
+    __device__ float* beta(int g) const {
+        return reinterpret_cast<float*>(gbase + OFF_BETA + (uint32_t)g * 256u);
     }
 };
 
@@ -225,21 +262,26 @@ struct Smem {
 // The pages compute this inverse by forward substitution, in blocks of 16
 // tokens ("Hardware-efficient implementation", section 3 of
 // paperlayer.ai/abs/2406.06484v6; "Pipeline Triton Chunkwise",
-// fr.news.hada.io/topic?id=31925).  Diagonal 16 x 16 blocks: right-looking
-// column substitution in registers.  Block rows i = 1..3 then follow from
-// X_ij = -X_ii sum_{k=j}^{i-1} A_ik X_kj; block row i of A is only read
-// while forming block row i of X, so X overwrites it in place.
+// fr.news.hada.io/topic?id=31925).  Here:
+//   - the four 16 x 16 diagonal blocks by right-looking column substitution;
+//   - 16 -> 32: inside each 32-row half, X_10 = -X_11 A_10 X_00;
+//   - 32 -> 64: X_[10] = -X_[11] A_[10] X_[00] with 32 x 32 blocks, skipping
+//     the known zero quarter of X_[00] and of X_[11].
+// A block of A is only read while forming the block of X at its position, so
+// X overwrites A in place.  Ys (32 x kYP floats) holds the intermediate
+// products.  Shared-memory bandwidth bounds this routine, so every thread
+// keeps a small register tile and reads with 128-bit loads.
 __device__ __forceinline__ void solve_unit_lower64(float* X, float* Ys, int t, int barid) {
     if (t < 64) {
         const int base = (t >> 4) * 16, c = t & 15;
+        const float* blk = X + base * (kP + 1);  // &X[base][base]
         float x[16];
 #pragma unroll
         for (int l = 0; l < 16; ++l) x[l] = (l == c) ? 1.f : 0.f;
 #pragma unroll
         for (int r = 0; r < 15; ++r)
 #pragma unroll
-            for (int l = r + 1; l < 16; ++l)
-                x[l] = fmaf(-X[(base + l) * kP + base + r], x[r], x[l]);
+            for (int l = r + 1; l < 16; ++l) x[l] = fmaf(-blk[l * kP + r], x[r], x[l]);
         wg_sync(barid);
 #pragma unroll
         for (int l = 0; l < 16; ++l) X[(base + l) * kP + base + c] = x[l];
@@ -247,34 +289,77 @@ __device__ __forceinline__ void solve_unit_lower64(float* X, float* Ys, int t, i
         wg_sync(barid);
     }
     wg_sync(barid);
-    const int r0 = t >> 4, c = t & 15;
+    {   // 16 -> 32 in both halves: thread (half h, row r, 4 columns c4)
+        const int h = t >> 6, r = (t >> 2) & 15, c4 = (t & 3) * 4;
+        const int o = 32 * h;
+        const float* arow = X + (o + 16 + r) * kP + o;
+        float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int i = 1; i < 4; ++i) {
-#pragma unroll
-        for (int m = 0; m < 2 * i; ++m) {
-            const int j = m >> 1, r = r0 + 8 * (m & 1);
-            const float* arow = X + (16 * i + r) * kP;
-            float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-            for (int k = 16 * j; k < 16 * i; k += 2) {
-                y0 = fmaf(arow[k], X[k * kP + 16 * j + c], y0);
-                y1 = fmaf(arow[k + 1], X[(k + 1) * kP + 16 * j + c], y1);
-            }
-            Ys[(j * 16 + r) * 16 + c] = y0 + y1;
+        for (int k = 0; k < 16; k += 4) {
+            const float4 a = lds4(arow + k);
+            fma4(y, a.x, lds4(X + (o + k + 0) * kP + o + c4));
+            fma4(y, a.y, lds4(X + (o + k + 1) * kP + o + c4));
+            fma4(y, a.z, lds4(X + (o + k + 2) * kP + o + c4));
+            fma4(y, a.w, lds4(X + (o + k + 3) * kP + o + c4));
         }
+        sts4(Ys + (16 * h + r) * kYP + c4, y);
         wg_sync(barid);
+        const float* xrow = X + (o + 16 + r) * kP + o + 16;
+        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int m = 0; m < 2 * i; ++m) {
-            const int j = m >> 1, r = r0 + 8 * (m & 1);
-            const float* xrow = X + (16 * i + r) * kP + 16 * i;
-            float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-            for (int mm = 0; mm < 16; mm += 2) {
-                x0 = fmaf(xrow[mm], Ys[(j * 16 + mm) * 16 + c], x0);
-                x1 = fmaf(xrow[mm + 1], Ys[(j * 16 + mm + 1) * 16 + c], x1);
-            }
-            X[(16 * i + r) * kP + 16 * j + c] = -(x0 + x1);
+        for (int m = 0; m < 16; m += 4) {
+            const float4 a = lds4(xrow + m);
+            fma4(z, a.x, lds4(Ys + (16 * h + m + 0) * kYP + c4));
+            fma4(z, a.y, lds4(Ys + (16 * h + m + 1) * kYP + c4));
+            fma4(z, a.z, lds4(Ys + (16 * h + m + 2) * kYP + c4));
+            fma4(z, a.w, lds4(Ys + (16 * h + m + 3) * kYP + c4));
         }
+        sts4(X + (o + 16 + r) * kP + o + c4, neg4(z));
+        wg_sync(barid);
+    }
+    {   // 32 -> 64: thread (rows r and r + 16, 4 columns c); c is warp-uniform
+        const int r = t & 15, c = (t >> 4) * 4;
+        const float* a0 = X + (32 + r) * kP;
+        const float* a1 = X + (48 + r) * kP;
+        float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
+        auto ystep = [&](int k) {
+            const float4 p = lds4(a0 + k), q = lds4(a1 + k);
+            const float4 x0 = lds4(X + (k + 0) * kP + c), x1 = lds4(X + (k + 1) * kP + c);
+            const float4 x2 = lds4(X + (k + 2) * kP + c), x3 = lds4(X + (k + 3) * kP + c);
+            fma4(y0, p.x, x0); fma4(y0, p.y, x1); fma4(y0, p.z, x2); fma4(y0, p.w, x3);
+            fma4(y1, q.x, x0); fma4(y1, q.y, x1); fma4(y1, q.z, x2); fma4(y1, q.w, x3);
+        };
+        if (c < 16) {
+#pragma unroll
+            for (int k = 0; k < 32; k += 4) ystep(k);
+        } else {  // rows 0-15 of X_[00] are zero in columns 16-31
+#pragma unroll
+            for (int k = 16; k < 32; k += 4) ystep(k);
+        }
+        sts4(Ys + r * kYP + c, y0);
+        sts4(Ys + (16 + r) * kYP + c, y1);
+        wg_sync(barid);
+        const float* x0r = X + (32 + r) * kP + 32;
+        const float* x1r = X + (48 + r) * kP + 32;
+        float4 z0 = make_float4(0.f, 0.f, 0.f, 0.f), z1 = z0;
+#pragma unroll
+        for (int m = 0; m < 16; m += 4) {  // row r of X_[11] is zero past column 15
+            const float4 p = lds4(x0r + m), q = lds4(x1r + m);
+            const float4 y_0 = lds4(Ys + (m + 0) * kYP + c), y_1 = lds4(Ys + (m + 1) * kYP + c);
+            const float4 y_2 = lds4(Ys + (m + 2) * kYP + c), y_3 = lds4(Ys + (m + 3) * kYP + c);
+            fma4(z0, p.x, y_0); fma4(z0, p.y, y_1); fma4(z0, p.z, y_2); fma4(z0, p.w, y_3);
+            fma4(z1, q.x, y_0); fma4(z1, q.y, y_1); fma4(z1, q.z, y_2); fma4(z1, q.w, y_3);
+        }
+#pragma unroll
+        for (int m = 16; m < 32; m += 4) {
+            const float4 q = lds4(x1r + m);
+            fma4(z1, q.x, lds4(Ys + (m + 0) * kYP + c));
+            fma4(z1, q.y, lds4(Ys + (m + 1) * kYP + c));
+            fma4(z1, q.z, lds4(Ys + (m + 2) * kYP + c));
+            fma4(z1, q.w, lds4(Ys + (m + 3) * kYP + c));
+        }
+        sts4(X + (32 + r) * kP + c, neg4(z0));
+        sts4(X + (48 + r) * kP + c, neg4(z1));
         wg_sync(barid);
     }
 }
@@ -284,33 +369,35 @@ __device__ void producer_role(const Ctl& ctl, const Smem& sm, const CUtensorMap*
                               const CUtensorMap* tm_k, const CUtensorMap* tm_v, int bh,
                               int nchunks) {
     int nkq = 0, nv = 0;
-    uint64_t t0 = globaltimer_ns();
+    long long t0 = clock64();
     while ((nkq < nchunks || nv < nchunks) && !ctl.aborted()) {
         bool progressed = false;
+        const int s = nkq % kStages;
         if (nkq < nchunks &&
-            (nkq < 2 || mbar_test_wait(ctl.bar(B_KQ_EMPTY + (nkq & 1)), ((nkq >> 1) - 1) & 1))) {
-            const int s = nkq & 1;
-            const uint32_t st = sm.kqw(s), bar = ctl.bar(B_KQ_FULL + s);
+            (nkq < kStages ||
+             mbar_test_wait(ctl.bar(B_KQ_EMPTY + s), (uint32_t)(nkq / kStages - 1) & 1u))) {
+            const uint32_t st = sm.kq(s), bar = ctl.bar(B_KQ_FULL + s);
             mbar_arrive_expect_tx(bar, 4 * 8192);
             tma_load_3d(st, tm_k, bar, 0, nkq * kC, bh);
-            tma_load_3d(st + kRegKQW, tm_k, bar, 64, nkq * kC, bh);
+            tma_load_3d(st + kRegKQ, tm_k, bar, 64, nkq * kC, bh);
             tma_load_3d(st + 8192, tm_q, bar, 0, nkq * kC, bh);
-            tma_load_3d(st + kRegKQW + 8192, tm_q, bar, 64, nkq * kC, bh);
-            if (nkq + 2 < nchunks) {  // warm L2 for the load after next
-                tma_prefetch_l2_3d(tm_k, 0, (nkq + 2) * kC, bh);
-                tma_prefetch_l2_3d(tm_k, 64, (nkq + 2) * kC, bh);
-                tma_prefetch_l2_3d(tm_q, 0, (nkq + 2) * kC, bh);
-                tma_prefetch_l2_3d(tm_q, 64, (nkq + 2) * kC, bh);
+            tma_load_3d(st + kRegKQ + 8192, tm_q, bar, 64, nkq * kC, bh);
+            if (nkq + kStages < nchunks) {  // warm L2 for this stage's next tiles
+                const int y = (nkq + kStages) * kC;
+                tma_prefetch_l2_3d(tm_k, 0, y, bh);
+                tma_prefetch_l2_3d(tm_k, 64, y, bh);
+                tma_prefetch_l2_3d(tm_q, 0, y, bh);
+                tma_prefetch_l2_3d(tm_q, 64, y, bh);
             }
             ++nkq;
             progressed = true;
         }
-        if (nv < nchunks && (nv < 1 || mbar_test_wait(ctl.bar(B_V_EMPTY), (nv - 1) & 1))) {
+        if (nv < nchunks && (nv < 1 || mbar_test_wait(ctl.bar(B_V_EMPTY), (uint32_t)(nv - 1) & 1u))) {
             const uint32_t bar = ctl.bar(B_V_FULL);
             mbar_arrive_expect_tx(bar, 2 * 8192);
             tma_load_3d(sm.v(), tm_v, bar, 0, nv * kC, bh);
             tma_load_3d(sm.v() + 8192, tm_v, bar, 64, nv * kC, bh);
-            if (nv + 1 < nchunks) {  // v tile is single-buffered: warm L2 for the next one
+            if (nv + 1 < nchunks) {  // the v tile is single-buffered: warm L2 for the next one
                 tma_prefetch_l2_3d(tm_v, 0, (nv + 1) * kC, bh);
                 tma_prefetch_l2_3d(tm_v, 64, (nv + 1) * kC, bh);
             }
@@ -318,27 +405,27 @@ __device__ void producer_role(const Ctl& ctl, const Smem& sm, const CUtensorMap*
             progressed = true;
         }
         if (progressed) {
-            t0 = globaltimer_ns();
-        } else if (globaltimer_ns() - t0 > kTimeoutNs) {
-            ctl.raise();
+            t0 = clock64();
+        } else {
+            __nanosleep(64);  // loads run well ahead; stay off the issue slots
+            if (clock64() - t0 > kTimeoutCycles) ctl.raise();
         }
     }
     // Leave nothing in flight: wait (bounded) for the last load on each barrier.
-    for (int s = 0; s < 2; ++s) {
-        const int n_s = (nkq - s + 1) / 2;  // loads issued into stage s
+    for (int s = 0; s < kStages; ++s) {
+        const int n_s = (nkq - s + kStages - 1) / kStages;  // loads issued into stage s
         if (n_s > 0) mbar_wait(ctl.bar(B_KQ_FULL + s), (uint32_t)(n_s - 1) & 1u, kTimeoutNs);
     }
     if (nv > 0) mbar_wait(ctl.bar(B_V_FULL), (uint32_t)(nv - 1) & 1u, kTimeoutNs);
 }
 
-// The single MMA-issuing thread.  Each pending MMA group becomes issuable
-// when the barriers it depends on have completed; the state chain
-// (S += K^T U', then D1 += [Q';-W] S) has priority over chunk-local work.
-// Every barrier checked here can complete at most once between two checks
-// of the same phase, so parity tests are unambiguous.
+// The single MMA-issuing thread.  A pending MMA group becomes issuable when
+// the barriers it depends on have completed; the state chain
+// (S += K^T U', then D1 += [Q';-W] S) has priority.  With nothing issuable
+// the thread sleeps on the next state-chain barrier for a bounded time.
 __device__ void mma_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int nchunks) {
     int nG = 0, nPT = 0, nDW = 0, nD1 = 0, nM2 = 0, nM3 = 0;
-    uint64_t t0 = globaltimer_ns();
+    long long t0 = clock64();
     auto ready = [&](int b, int phase) {
         return mbar_test_wait(ctl.bar(b), (uint32_t)phase & 1u);
     };
@@ -346,29 +433,26 @@ __device__ void mma_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int nchu
         bool issued = false;
         if (nM3 < nM2 && ready(B_U_FULL, nM3)) {
             // S += K^T U'
-            const uint32_t kqw = sm.kqw(nM3 & 1);
+            const uint32_t kq = sm.kq(nM3 % kStages);
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + COL_S, sw128_desc(kqw + 2048u * kk, kRegKQW, 1024),
+                mma_bf16_ss(tmem + COL_S, sw128_desc(kq + 2048u * kk, kRegKQ, 1024),
                             sw128_desc(sm.sb() + 2048u * kk, 8192, 1024), IDESC_MM, 1);
             mma_commit(ctl.bar(B_S_READY));
-            mma_commit(ctl.bar(B_KQ_EMPTY + (nM3 & 1)));
+            mma_commit(ctl.bar(B_KQ_EMPTY + nM3 % kStages));
             ++nM3;
             issued = true;
         } else if (nM2 < nD1 && ready(B_QW_READY + (nM2 & 1), nM2 >> 1) &&
                    ready(B_SB_FULL, nM2)) {
-            // D1 += [Q'; -W] S
-            const uint32_t kqw = sm.kqw(nM2 & 1);
+            // D1 += [Q'; -W] S, A from TMEM
             tc_fence_after_sync();
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t a =
-                    kqw + (uint32_t)(kk >> 2) * kRegKQW + 8192u + (uint32_t)(kk & 3) * 32u;
-                mma_bf16_ss(tmem + COL_D1, sw128_desc(a, 16, 1024),
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ts(tmem + COL_D1, tmem + COL_QW + 8u * kk,
                             sw128_desc(sm.sb() + 2048u * kk, 16384, 1024), IDESC_KB, 1);
-            }
             mma_commit(ctl.bar(B_D1_FULL));
+            mma_commit(ctl.bar(B_QW_FREE + ((nM2 + 1) & 1)));
             ++nM2;
             issued = true;
         } else if (nD1 < nDW && nD1 == nM2 && ready(B_V_FULL, nD1) &&
@@ -385,35 +469,40 @@ __device__ void mma_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int nchu
             issued = true;
         } else if (nDW < nPT && ready(B_TP_FULL + (nDW & 1), nDW >> 1) &&
                    (nDW == 0 || ready(B_DW_EMPTY, nDW - 1))) {
-            // DW = [PT; Tm] K
-            const uint32_t tp = sm.tp(nDW & 1), kqw = sm.kqw(nDW & 1);
+            // DW = [PT; Tm] K as two N = 64 halves: dk 0-63 into the chunk
+            // group's columns, dk 64-127 into the shared columns.
+            const uint32_t tp = sm.tp(nDW & 1), kq = sm.kq(nDW % kStages);
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + COL_DW, sw128_desc(tp + 32u * kk, 16, 1024),
-                            sw128_desc(kqw + 2048u * kk, kRegKQW, 1024), IDESC_KB, kk > 0);
+                mma_bf16_ss(tmem + COL_G + 64u * (nDW & 1), sw128_desc(tp + 32u * kk, 16, 1024),
+                            sw128_desc(kq + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + COL_DWX, sw128_desc(tp + 32u * kk, 16, 1024),
+                            sw128_desc(kq + kRegKQ + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
             mma_commit(ctl.bar(B_DW_FULL + (nDW & 1)));
             ++nDW;
             issued = true;
         } else if (nPT < nG && ready(B_TP_READY + (nPT & 1), nPT >> 1)) {
-            // PT = P Tm into the chunk group's G columns
+            // PT = P Tm into the chunk group's columns
             const uint32_t tp = sm.tp(nPT & 1);
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 mma_bf16_ss(tmem + COL_G + 64u * (nPT & 1), sw128_desc(tp + 32u * kk, 16, 1024),
-                            sw128_desc(tp + 8192u + 2048u * kk, 8192, 1024), IDESC_PT, kk > 0);
+                            sw128_desc(tp + 8192u + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
             mma_commit(ctl.bar(B_PT_FULL + (nPT & 1)));
             ++nPT;
             issued = true;
-        } else if (nG < nchunks && ready(B_KQ_FULL + (nG & 1), nG >> 1) &&
+        } else if (nG < nchunks && ready(B_KQ_FULL + nG % kStages, nG / kStages) &&
                    (nG < 2 || ready(B_G_EMPTY + (nG & 1), (nG >> 1) - 1))) {
             // G = [K; Q] K^T
-            const uint32_t kqw = sm.kqw(nG & 1);
+            const uint32_t kq = sm.kq(nG % kStages);
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t a = kqw + (uint32_t)(kk >> 2) * kRegKQW + (uint32_t)(kk & 3) * 32u;
+                const uint32_t a = kq + (uint32_t)(kk >> 2) * kRegKQ + (uint32_t)(kk & 3) * 32u;
                 mma_bf16_ss(tmem + COL_G + 64u * (nG & 1), sw128_desc(a, 16, 1024),
                             sw128_desc(a, 16, 1024), IDESC_G, kk > 0);
             }
@@ -422,9 +511,17 @@ __device__ void mma_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int nchu
             issued = true;
         }
         if (issued) {
-            t0 = globaltimer_ns();
-        } else if (globaltimer_ns() - t0 > kTimeoutNs) {
-            ctl.raise();
+            t0 = clock64();
+        } else {
+            // Sleep on the state chain's next event (woken as soon as it
+            // completes), or briefly when the chain is waiting on MMA results.
+            if (nM3 < nM2)
+                mbar_try_wait_hint(ctl.bar(B_U_FULL), (uint32_t)nM3 & 1u, 300);
+            else if (nM2 < nD1)
+                mbar_try_wait_hint(ctl.bar(B_SB_FULL), (uint32_t)nM2 & 1u, 300);
+            else
+                __nanosleep(32);
+            if (clock64() - t0 > kTimeoutCycles) ctl.raise();
         }
     }
     // Drain the MMA pipe before anyone releases TMEM or shared memory.
@@ -476,34 +573,30 @@ __device__ void state_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
     tmem_wait_st();
 
     for (int c = 0; c < nchunks; ++c) {
-        if (c > 0) {
-            const bool ok = ctl.wait(B_S_READY, (uint32_t)(c - 1));
-            if (wg_sync_or(kBar, !ok)) return;
-        }
+        if (c > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(c - 1), t, kBar)) return;
         tc_fence_after_sync();
         // S (fp32) -> bf16 operand tile: dv halves as regions, row t.
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-            float x[32];
-            tmem_ld32f(tmem + lane_base + COL_S + 32u * part, x);
-            store_row32_bf16(sm.sb() + (uint32_t)(part >> 1) * 16384u, t, 4 * (part & 1), x);
+        for (int half = 0; half < 2; ++half) {
+            float x[64];
+            tmem_ld64f(tmem + lane_base + COL_S + 64u * half, x);
+            store_row64_bf16(sm.sb() + (uint32_t)half * 16384u, t, x);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
         wg_sync(kBar);
         if (t == 0) mbar_arrive(ctl.bar(B_SB_FULL));
 
-        const bool ok = ctl.wait(B_D1_FULL, (uint32_t)c);
-        if (wg_sync_or(kBar, !ok)) return;
+        if (!wg_wait(ctl, B_D1_FULL, (uint32_t)c, t, kBar)) return;
         tc_fence_after_sync();
         // rows 0-63: O into the chunk's o tile; rows 64-127: U' over the S operand.
         const int row = t & 63;
         const uint32_t dst = (t < 64) ? sm.tp(c & 1) : sm.sb();
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-            float x[32];
-            tmem_ld32f(tmem + lane_base + COL_D1 + 32u * part, x);
-            store_row32_bf16(dst + (uint32_t)(part >> 1) * 8192u, row, 4 * (part & 1), x);
+        for (int half = 0; half < 2; ++half) {
+            float x[64];
+            tmem_ld64f(tmem + lane_base + COL_D1 + 64u * half, x);
+            store_row64_bf16(dst + (uint32_t)half * 8192u, row, x);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
@@ -514,19 +607,16 @@ __device__ void state_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
             mbar_arrive(ctl.bar(B_O_FULL + (c & 1)));
         }
     }
-    if (nchunks > 0) {
-        const bool ok = ctl.wait(B_S_READY, (uint32_t)(nchunks - 1));
-        if (wg_sync_or(kBar, !ok)) return;
-    }
+    if (nchunks > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(nchunks - 1), t, kBar)) return;
     tc_fence_after_sync();
     if (S_T) {
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-            float x[32];
-            tmem_ld32f(tmem + lane_base + COL_S + 32u * part, x);
-            float4* dst = reinterpret_cast<float4*>(S_T + ((size_t)bh * kD + t) * kD + 32 * part);
+        for (int half = 0; half < 2; ++half) {
+            float x[64];
+            tmem_ld64f(tmem + lane_base + COL_S + 64u * half, x);
+            float4* dst = reinterpret_cast<float4*>(S_T + ((size_t)bh * kD + t) * kD + 64 * half);
 #pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
+            for (int v4 = 0; v4 < 16; ++v4)
                 dst[v4] = make_float4(x[4 * v4], x[4 * v4 + 1], x[4 * v4 + 2], x[4 * v4 + 3]);
         }
     }
@@ -541,36 +631,38 @@ __device__ void chunk_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
     float* const X = sm.x(g);
     float* const Ys = sm.y(g);
     float* const betas = sm.beta(g);
-    const uint32_t tp = sm.tp(g), kqw = sm.kqw(g);
+    const uint32_t tp = sm.tp(g);
     const int row = t & 63;
 
     for (int c = g, it = 0; c < nchunks; c += 2, ++it) {
         const int t0 = c * kC;
         const int n = min(kC, T - t0);
+        const uint32_t kq = sm.kq(c % kStages);
         if (t < kC) betas[t] = t < n ? __bfloat162float(beta[(size_t)bh * T + t0 + t]) : 0.f;
         bool ok = true;
-        if (it > 0) ok = ctl.wait(B_O_FREE + g, (uint32_t)(it - 1));  // o tile of c-2 stored
-        ok = ok && ctl.wait(B_G_FULL + g, (uint32_t)it);
+        if (t == 0) {
+            if (it > 0) ok = ctl.wait(B_O_FREE + g, (uint32_t)(it - 1));  // o tile of c-2 stored
+            ok = ok && ctl.wait(B_G_FULL + g, (uint32_t)it);
+        }
         if (wg_sync_or(barid, !ok)) return;
         tc_fence_after_sync();
         // A = beta_i (k_i . k_j) for j < i (TMEM rows 0-63) as fp32;
         // P = q_t . k_j for j <= t (rows 64-127) as bf16 over rows 0-63 of [PT; Tm].
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            float x[32];
-            tmem_ld32f(tmem + lane_base + colG + 32u * part, x);
+        {
+            float x[64];
+            tmem_ld64f(tmem + lane_base + colG, x);
             if (t < 64) {
                 const float bi = betas[row];
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = 32 * part + jj;
-                    X[row * kP + j] = j < row ? bi * x[jj] : 0.f;
-                }
+                for (int j = 0; j < 64; j += 4)
+                    sts4(X + row * kP + j,
+                         make_float4(j + 0 < row ? bi * x[j + 0] : 0.f, j + 1 < row ? bi * x[j + 1] : 0.f,
+                                     j + 2 < row ? bi * x[j + 2] : 0.f, j + 3 < row ? bi * x[j + 3] : 0.f));
             } else {
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj)
-                    if (32 * part + jj > row) x[jj] = 0.f;
-                store_row32_bf16(tp, row, 4 * part, x);
+                for (int j = 0; j < 64; ++j)
+                    if (j > row) x[j] = 0.f;
+                store_row64_bf16(tp, row, x);
             }
         }
         tc_fence_before_sync();
@@ -581,66 +673,72 @@ __device__ void chunk_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
             const int i = t >> 1, c0 = 32 * (t & 1);
             float x[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = X[i * kP + c0 + e] * betas[c0 + e];
+            for (int e = 0; e < 32; e += 4) {
+                const float4 xv = lds4(X + i * kP + c0 + e), bv = lds4(betas + c0 + e);
+                x[e] = xv.x * bv.x;
+                x[e + 1] = xv.y * bv.y;
+                x[e + 2] = xv.z * bv.z;
+                x[e + 3] = xv.w * bv.w;
+            }
             store_row32_bf16(tp, 64 + i, c0 / 8, x);
         }
         fence_proxy_async_smem();
         wg_sync(barid);
         if (t == 0) mbar_arrive(ctl.bar(B_TP_READY + g));
 
-        ok = ctl.wait(B_PT_FULL + g, (uint32_t)it);
-        if (wg_sync_or(barid, !ok)) return;
+        if (!wg_wait(ctl, B_PT_FULL + g, (uint32_t)it, t, barid)) return;
         tc_fence_after_sync();
         if (t < 64) {  // PT -> bf16 over P
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                float x[32];
-                tmem_ld32f(tmem + lane_base + colG + 32u * part, x);
-                store_row32_bf16(tp, t, 4 * part, x);
-            }
+            float x[64];
+            tmem_ld64f(tmem + lane_base + colG, x);
+            store_row64_bf16(tp, t, x);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
         wg_sync(barid);
-        if (t == 0) {
-            mbar_arrive(ctl.bar(B_TP_FULL + g));
-            mbar_arrive(ctl.bar(B_G_EMPTY + g));
-        }
+        if (t == 0) mbar_arrive(ctl.bar(B_TP_FULL + g));
 
-        ok = ctl.wait(B_DW_FULL + g, (uint32_t)it);
+        // DW done, and the previous chunk's state MMA has read [Q'; -W].
+        ok = true;
+        if (t == 0) {
+            ok = ctl.wait(B_DW_FULL + g, (uint32_t)it);
+            if (g == 1 || it > 0) ok = ok && ctl.wait(B_QW_FREE + g, (uint32_t)(g == 1 ? it : it - 1));
+        }
         if (wg_sync_or(barid, !ok)) return;
         tc_fence_after_sync();
-        // rows 0-63: Q' = Q - PT K over the Q rows; rows 64-127: -W into the W rows.
+        // rows 0-63: Q' = Q - PT K; rows 64-127: -W.  Written as bf16 pairs to TMEM.
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-            float x[32];
-            tmem_ld32f(tmem + lane_base + COL_DW + 32u * part, x);
-            const uint32_t region = kqw + (uint32_t)(part >> 1) * kRegKQW;
-            const int ch0 = 4 * (part & 1);
+        for (int half = 0; half < 2; ++half) {
+            float x[64];
+            tmem_ld64f(tmem + lane_base + (half == 0 ? colG : COL_DWX), x);
+            uint32_t packed[32];
             if (t < 64) {
+                const uint32_t region = kq + (uint32_t)half * kRegKQ;
+                uint4 qv[8];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const uint32_t addr = region + sw128(64 + row, ch0 + cc);
-                    const uint4 qv = ld_shared_v4(addr);
-                    const float2 a0 = unpack_bf16(qv.x), a1 = unpack_bf16(qv.y),
-                                 a2 = unpack_bf16(qv.z), a3 = unpack_bf16(qv.w);
+                for (int cc = 0; cc < 8; ++cc) qv[cc] = ld_shared_v4(region + sw128(64 + row, cc));
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const float2 a0 = unpack_bf16(qv[cc].x), a1 = unpack_bf16(qv[cc].y),
+                                 a2 = unpack_bf16(qv[cc].z), a3 = unpack_bf16(qv[cc].w);
                     const float* d = x + 8 * cc;
-                    st_shared_v4(addr, pack_bf16(a0.x - d[0], a0.y - d[1]),
-                                 pack_bf16(a1.x - d[2], a1.y - d[3]),
-                                 pack_bf16(a2.x - d[4], a2.y - d[5]),
-                                 pack_bf16(a3.x - d[6], a3.y - d[7]));
+                    packed[4 * cc + 0] = pack_bf16(a0.x - d[0], a0.y - d[1]);
+                    packed[4 * cc + 1] = pack_bf16(a1.x - d[2], a1.y - d[3]);
+                    packed[4 * cc + 2] = pack_bf16(a2.x - d[4], a2.y - d[5]);
+                    packed[4 * cc + 3] = pack_bf16(a3.x - d[6], a3.y - d[7]);
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) x[e] = -x[e];
-                store_row32_bf16(region, 128 + row, ch0, x);
+                for (int e = 0; e < 32; ++e) packed[e] = pack_bf16(-x[2 * e], -x[2 * e + 1]);
             }
+            tmem_st32(tmem + lane_base + COL_QW + 32u * half, packed);
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before_sync();
         wg_sync(barid);
         if (t == 0) {
             mbar_arrive(ctl.bar(B_DW_EMPTY));
+            mbar_arrive(ctl.bar(B_G_EMPTY + g));
             mbar_arrive(ctl.bar(B_QW_READY + g));
         }
     }

@@ -21,12 +21,15 @@
 // state-independent work of the following chunks:
 //   warp 0      TMA producer: [K; Q] tiles into a 3-stage ring, v tiles
 //               (3-D maps, so rows past the end of a sequence read as zeros)
-//   warp 1      TMEM owner and the single MMA-issuing thread; it issues every
-//               MMA group whose inputs are ready, the state chain first
+//   warp 1      TMEM owner
 //   warp 2      TMA store of o tiles (rows past the end are not written)
-//   warps 4-7   state group: S -> bf16 operand, O and U' epilogues, final state
-//   warps 8-11, 12-15   chunk groups for even and odd chunks: A and P, the
-//               triangular solve, Tm, PT, and the [Q'; -W] operand
+//   warps 4-7   state group: S -> bf16 operand, the state MMAs, O and U'
+//               epilogues, final state
+//   warps 8-11, 12-15   chunk groups for even and odd chunks: the G, PT, DW
+//               and D1 MMAs, A and P, the triangular solve, Tm, PT, and the
+//               [Q'; -W] operand
+// Each group's elected thread issues its own MMAs and waits on its own
+// commits, so no MMA waits for another role to notice that it is ready.
 // Operand tiles in shared memory use the 128-byte swizzled layout TMA writes;
 // [Q'; -W], the A operand of the state-dependent MMA, lives in TMEM.
 // Every wait is bounded: on a timeout the CTA records an error code (read
@@ -74,7 +77,7 @@ constexpr uint32_t OFF_Y = OFF_X + 2 * kXBytes;      // 2 x fp32 32 x kYP solve 
 constexpr uint32_t kYBytes = 32 * kYP * 4;
 constexpr uint32_t OFF_BETA = OFF_Y + 2 * kYBytes;   // 2 x 64 fp32
 constexpr uint32_t OFF_BAR = OFF_BETA + 512;         // mbarriers, 8 bytes each
-constexpr int kNumBars = 36;
+constexpr int kNumBars = 40;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * kNumBars;  // abort flag, TMEM address
 constexpr uint32_t kSmemBytes = OFF_MISC + 16 + 1024;  // + 1024-byte alignment slack
 static_assert(OFF_V % 1024 == 0 && OFF_TP % 1024 == 0 && OFF_SB % 1024 == 0, "tile alignment");
@@ -83,29 +86,26 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // mbarrier indices.  Every barrier has exactly one waiting role, which
 // consumes its phases in order, so a parity test can never see a phase two
-// ahead of the one it asks for.
+// ahead of the one it asks for.  Barriers indexed [2] belong to the chunk
+// group of that parity; [6] is (stage, group): chunk c uses c % 6.
 enum : int {
-    B_KQ_FULL = 0,    // [3] q, k tiles of a stage landed
-    B_KQ_EMPTY = 3,   // [3] the stage's last reader (S += K^T U') completed
-    B_TP_READY = 6,   // [2] P and Tm written (chunk group)
-    B_TP_FULL = 8,    // [2] PT written over P (chunk group)
-    B_QW_READY = 10,  // [2] [Q'; -W] written to TMEM (chunk group)
-    B_O_FULL = 12,    // [2] o tile written (state group)
-    B_O_FREE = 14,    // [2] o tile stored (store warp)
-    B_G_FULL = 16,    // [2] G = [K;Q] K^T done
-    B_PT_FULL = 18,   // [2] PT = P Tm done
-    B_G_EMPTY = 20,   // [2] chunk group finished with its TMEM columns
-    B_DW_FULL = 22,   // [2] DW = [PT;Tm] K done
-    B_QW_FREE = 24,   // [2] the previous chunk's D1 += [Q';-W] S has read [Q'; -W]
-    B_V_FULL = 26,    // v tile landed
-    B_V_EMPTY = 27,   // D1 = [PT;Tm] V done (v tile free)
-    B_DW_EMPTY = 28,  // chunk group finished reading DW (shared upper half)
-    B_SB_FULL = 29,   // S bf16 operand written
-    B_D1_FULL = 30,   // D1 += [Q';-W] S done
-    B_U_FULL = 31,    // U' written
-    B_D1_EMPTY = 32,  // state group finished reading D1
-    B_S_READY = 33,   // S += K^T U' done
-    B_DRAIN = 34,     // final drain of the MMA pipe
+    B_KQ_FULL = 0,     // [6] q, k tiles landed               (producer -> chunk group)
+    B_KQ_EMPTY = 6,    // [3] stage's last reader done         (state MMA -> producer)
+    B_V_FULL = 9,      // [2] v tile landed                    (producer -> chunk group)
+    B_V_EMPTY = 11,    // D1 = [PT;Tm] V done, v tile free     (chunk MMA -> producer)
+    B_G_FULL = 12,     // [2] G = [K;Q] K^T done               (own commit)
+    B_PT_FULL = 14,    // [2] PT = P Tm done                   (own commit)
+    B_DW_FULL = 16,    // [2] DW = [PT;Tm] K done              (own commit)
+    B_D1I_FULL = 18,   // [2] D1 = [PT;Tm] V done              (chunk MMA -> state group)
+    B_QW_READY = 20,   // [2] [Q'; -W] written to TMEM         (chunk group -> state group)
+    B_QW_FREE = 22,    // [2] previous D1 += [Q';-W] S done    (state MMA -> chunk group)
+    B_D1_EMPTY = 24,   // [2] previous D1 read out             (state group -> chunk group)
+    B_DWX_FREE = 26,   // [2] previous DW upper half read out  (chunk group -> other group)
+    B_O_FULL = 28,     // [2] o tile written                   (state group -> store warp)
+    B_O_FREE = 30,     // [2] o tile stored                    (store warp -> chunk group)
+    B_D1_FULL = 32,    // D1 += [Q';-W] S done                 (own commit, state group)
+    B_S_READY = 33,    // S += K^T U' done                     (own commit, state group)
+    B_DRAIN = 34,      // [3] final drain of each issuer's MMAs (state, group 0, group 1)
 };
 
 // TMEM columns (512 allocated):
@@ -376,7 +376,7 @@ __device__ void producer_role(const Ctl& ctl, const Smem& sm, const CUtensorMap*
         if (nkq < nchunks &&
             (nkq < kStages ||
              mbar_test_wait(ctl.bar(B_KQ_EMPTY + s), (uint32_t)(nkq / kStages - 1) & 1u))) {
-            const uint32_t st = sm.kq(s), bar = ctl.bar(B_KQ_FULL + s);
+            const uint32_t st = sm.kq(s), bar = ctl.bar(B_KQ_FULL + nkq % 6);
             mbar_arrive_expect_tx(bar, 4 * 8192);
             tma_load_3d(st, tm_k, bar, 0, nkq * kC, bh);
             tma_load_3d(st + kRegKQ, tm_k, bar, 64, nkq * kC, bh);
@@ -393,7 +393,7 @@ __device__ void producer_role(const Ctl& ctl, const Smem& sm, const CUtensorMap*
             progressed = true;
         }
         if (nv < nchunks && (nv < 1 || mbar_test_wait(ctl.bar(B_V_EMPTY), (uint32_t)(nv - 1) & 1u))) {
-            const uint32_t bar = ctl.bar(B_V_FULL);
+            const uint32_t bar = ctl.bar(B_V_FULL + (nv & 1));
             mbar_arrive_expect_tx(bar, 2 * 8192);
             tma_load_3d(sm.v(), tm_v, bar, 0, nv * kC, bh);
             tma_load_3d(sm.v() + 8192, tm_v, bar, 64, nv * kC, bh);
@@ -412,121 +412,21 @@ __device__ void producer_role(const Ctl& ctl, const Smem& sm, const CUtensorMap*
         }
     }
     // Leave nothing in flight: wait (bounded) for the last load on each barrier.
-    for (int s = 0; s < kStages; ++s) {
-        const int n_s = (nkq - s + kStages - 1) / kStages;  // loads issued into stage s
-        if (n_s > 0) mbar_wait(ctl.bar(B_KQ_FULL + s), (uint32_t)(n_s - 1) & 1u, kTimeoutNs);
+    for (int b = 0; b < 6; ++b) {
+        const int n_b = (nkq - b + 5) / 6;  // loads that completed on barrier b
+        if (n_b > 0) mbar_wait(ctl.bar(B_KQ_FULL + b), (uint32_t)(n_b - 1) & 1u, kTimeoutNs);
     }
-    if (nv > 0) mbar_wait(ctl.bar(B_V_FULL), (uint32_t)(nv - 1) & 1u, kTimeoutNs);
+    for (int b = 0; b < 2; ++b) {
+        const int n_b = (nv - b + 1) / 2;
+        if (n_b > 0) mbar_wait(ctl.bar(B_V_FULL + b), (uint32_t)(n_b - 1) & 1u, kTimeoutNs);
+    }
 }
 
-// The single MMA-issuing thread.  A pending MMA group becomes issuable when
-// the barriers it depends on have completed; the state chain
-// (S += K^T U', then D1 += [Q';-W] S) has priority.  With nothing issuable
-// the thread sleeps on the next state-chain barrier for a bounded time.
-__device__ void mma_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int nchunks) {
-    int nG = 0, nPT = 0, nDW = 0, nD1 = 0, nM2 = 0, nM3 = 0;
-    long long t0 = clock64();
-    auto ready = [&](int b, int phase) {
-        return mbar_test_wait(ctl.bar(b), (uint32_t)phase & 1u);
-    };
-    while (nM3 < nchunks && !ctl.aborted()) {
-        bool issued = false;
-        if (nM3 < nM2 && ready(B_U_FULL, nM3)) {
-            // S += K^T U'
-            const uint32_t kq = sm.kq(nM3 % kStages);
-            tc_fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + COL_S, sw128_desc(kq + 2048u * kk, kRegKQ, 1024),
-                            sw128_desc(sm.sb() + 2048u * kk, 8192, 1024), IDESC_MM, 1);
-            mma_commit(ctl.bar(B_S_READY));
-            mma_commit(ctl.bar(B_KQ_EMPTY + nM3 % kStages));
-            ++nM3;
-            issued = true;
-        } else if (nM2 < nD1 && ready(B_QW_READY + (nM2 & 1), nM2 >> 1) &&
-                   ready(B_SB_FULL, nM2)) {
-            // D1 += [Q'; -W] S, A from TMEM
-            tc_fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_ts(tmem + COL_D1, tmem + COL_QW + 8u * kk,
-                            sw128_desc(sm.sb() + 2048u * kk, 16384, 1024), IDESC_KB, 1);
-            mma_commit(ctl.bar(B_D1_FULL));
-            mma_commit(ctl.bar(B_QW_FREE + ((nM2 + 1) & 1)));
-            ++nM2;
-            issued = true;
-        } else if (nD1 < nDW && nD1 == nM2 && ready(B_V_FULL, nD1) &&
-                   (nD1 == 0 || ready(B_D1_EMPTY, nD1 - 1))) {
-            // D1 = [PT; Tm] V   (the chunk's TP_FULL was seen when its DW was issued)
-            const uint32_t tp = sm.tp(nD1 & 1);
-            tc_fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + COL_D1, sw128_desc(tp + 32u * kk, 16, 1024),
-                            sw128_desc(sm.v() + 2048u * kk, 8192, 1024), IDESC_KB, kk > 0);
-            mma_commit(ctl.bar(B_V_EMPTY));
-            ++nD1;
-            issued = true;
-        } else if (nDW < nPT && ready(B_TP_FULL + (nDW & 1), nDW >> 1) &&
-                   (nDW == 0 || ready(B_DW_EMPTY, nDW - 1))) {
-            // DW = [PT; Tm] K as two N = 64 halves: dk 0-63 into the chunk
-            // group's columns, dk 64-127 into the shared columns.
-            const uint32_t tp = sm.tp(nDW & 1), kq = sm.kq(nDW % kStages);
-            tc_fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + COL_G + 64u * (nDW & 1), sw128_desc(tp + 32u * kk, 16, 1024),
-                            sw128_desc(kq + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + COL_DWX, sw128_desc(tp + 32u * kk, 16, 1024),
-                            sw128_desc(kq + kRegKQ + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
-            mma_commit(ctl.bar(B_DW_FULL + (nDW & 1)));
-            ++nDW;
-            issued = true;
-        } else if (nPT < nG && ready(B_TP_READY + (nPT & 1), nPT >> 1)) {
-            // PT = P Tm into the chunk group's columns
-            const uint32_t tp = sm.tp(nPT & 1);
-            tc_fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + COL_G + 64u * (nPT & 1), sw128_desc(tp + 32u * kk, 16, 1024),
-                            sw128_desc(tp + 8192u + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
-            mma_commit(ctl.bar(B_PT_FULL + (nPT & 1)));
-            ++nPT;
-            issued = true;
-        } else if (nG < nchunks && ready(B_KQ_FULL + nG % kStages, nG / kStages) &&
-                   (nG < 2 || ready(B_G_EMPTY + (nG & 1), (nG >> 1) - 1))) {
-            // G = [K; Q] K^T
-            const uint32_t kq = sm.kq(nG % kStages);
-            tc_fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t a = kq + (uint32_t)(kk >> 2) * kRegKQ + (uint32_t)(kk & 3) * 32u;
-                mma_bf16_ss(tmem + COL_G + 64u * (nG & 1), sw128_desc(a, 16, 1024),
-                            sw128_desc(a, 16, 1024), IDESC_G, kk > 0);
-            }
-            mma_commit(ctl.bar(B_G_FULL + (nG & 1)));
-            ++nG;
-            issued = true;
-        }
-        if (issued) {
-            t0 = clock64();
-        } else {
-            // Sleep on the state chain's next event (woken as soon as it
-            // completes), or briefly when the chain is waiting on MMA results.
-            if (nM3 < nM2)
-                mbar_try_wait_hint(ctl.bar(B_U_FULL), (uint32_t)nM3 & 1u, 300);
-            else if (nM2 < nD1)
-                mbar_try_wait_hint(ctl.bar(B_SB_FULL), (uint32_t)nM2 & 1u, 300);
-            else
-                __nanosleep(32);
-            if (clock64() - t0 > kTimeoutCycles) ctl.raise();
-        }
-    }
-    // Drain the MMA pipe before anyone releases TMEM or shared memory.
-    mma_commit(ctl.bar(B_DRAIN));
-    mbar_wait(ctl.bar(B_DRAIN), 0, kTimeoutNs);
+// Lets everything a thread issued to the tensor core finish (bounded), so
+// TMEM and shared memory can be released safely.
+__device__ __forceinline__ void drain_mmas(const Ctl& ctl, int b) {
+    mma_commit(ctl.bar(b));
+    mbar_wait(ctl.bar(b), 0, kTimeoutNs);
 }
 
 __device__ void store_role(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_o, int bh,
@@ -543,10 +443,11 @@ __device__ void store_role(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm
     bulk_wait_group0();
 }
 
-// State group (warps 4-7): thread t owns state row t = TMEM lane t.
-__device__ void state_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
-                           const float* __restrict__ S0, float* __restrict__ S_T, int bh,
-                           int nchunks) {
+// State group (warps 4-7): thread t owns state row t = TMEM lane t; thread 0
+// issues the two state-dependent MMAs of every chunk.
+__device__ void state_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
+                                const float* __restrict__ S0, float* __restrict__ S_T, int bh,
+                                int nchunks) {
     constexpr int kBar = 1;
     const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
     // S0 (or zeros) into TMEM.
@@ -573,6 +474,7 @@ __device__ void state_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
     tmem_wait_st();
 
     for (int c = 0; c < nchunks; ++c) {
+        const int g = c & 1;
         if (c > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(c - 1), t, kBar)) return;
         tc_fence_after_sync();
         // S (fp32) -> bf16 operand tile: dv halves as regions, row t.
@@ -585,13 +487,27 @@ __device__ void state_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         fence_proxy_async_smem();
         tc_fence_before_sync();
         wg_sync(kBar);
-        if (t == 0) mbar_arrive(ctl.bar(B_SB_FULL));
-
-        if (!wg_wait(ctl, B_D1_FULL, (uint32_t)c, t, kBar)) return;
+        // D1 += [Q'; -W] S, once the chunk group has [Q'; -W] in TMEM and D1 initialised.
+        bool ok = true;
+        if (t == 0) {
+            ok = ctl.wait(B_QW_READY + g, (uint32_t)(c >> 1)) &&
+                 ctl.wait(B_D1I_FULL + g, (uint32_t)(c >> 1));
+            if (ok) {
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16_ts(tmem + COL_D1, tmem + COL_QW + 8u * kk,
+                                sw128_desc(sm.sb() + 2048u * kk, 16384, 1024), IDESC_KB, 1);
+                mma_commit(ctl.bar(B_D1_FULL));
+                mma_commit(ctl.bar(B_QW_FREE + (g ^ 1)));
+                ok = ctl.wait(B_D1_FULL, (uint32_t)c);
+            }
+        }
+        if (wg_sync_or(kBar, !ok)) return;
         tc_fence_after_sync();
         // rows 0-63: O into the chunk's o tile; rows 64-127: U' over the S operand.
         const int row = t & 63;
-        const uint32_t dst = (t < 64) ? sm.tp(c & 1) : sm.sb();
+        const uint32_t dst = (t < 64) ? sm.tp(g) : sm.sb();
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             float x[64];
@@ -602,9 +518,17 @@ __device__ void state_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         tc_fence_before_sync();
         wg_sync(kBar);
         if (t == 0) {
-            mbar_arrive(ctl.bar(B_U_FULL));
-            mbar_arrive(ctl.bar(B_D1_EMPTY));
-            mbar_arrive(ctl.bar(B_O_FULL + (c & 1)));
+            mbar_arrive(ctl.bar(B_D1_EMPTY + (g ^ 1)));
+            mbar_arrive(ctl.bar(B_O_FULL + g));
+            // S += K^T U'
+            const uint32_t kq = sm.kq(c % kStages);
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + COL_S, sw128_desc(kq + 2048u * kk, kRegKQ, 1024),
+                            sw128_desc(sm.sb() + 2048u * kk, 8192, 1024), IDESC_MM, 1);
+            mma_commit(ctl.bar(B_S_READY));
+            mma_commit(ctl.bar(B_KQ_EMPTY + c % kStages));
         }
     }
     if (nchunks > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(nchunks - 1), t, kBar)) return;
@@ -622,9 +546,20 @@ __device__ void state_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
     }
 }
 
-// Chunk group g (0: even chunks, warps 8-11; 1: odd chunks, warps 12-15).
-__device__ void chunk_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int g,
-                           const __nv_bfloat16* __restrict__ beta, int bh, int T, int nchunks) {
+__device__ void state_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
+                           const float* __restrict__ S0, float* __restrict__ S_T, int bh,
+                           int nchunks) {
+    state_role_body(ctl, sm, tmem, t, S0, S_T, bh, nchunks);
+    if (t == 0) drain_mmas(ctl, B_DRAIN + 0);
+}
+
+// Chunk group g (0: even chunks, warps 8-11; 1: odd chunks, warps 12-15);
+// thread 0 issues the group's MMAs.  For the handoffs between the two
+// groups and the state group, "previous chunk" phases are: group 1 waits
+// phase it, group 0 phase it - 1 (and chunk 0 waits for nothing).
+__device__ void chunk_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int g,
+                                const __nv_bfloat16* __restrict__ beta, int bh, int T,
+                                int nchunks) {
     const int barid = 2 + g;
     const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
     const uint32_t colG = COL_G + 64u * (uint32_t)g;
@@ -638,11 +573,25 @@ __device__ void chunk_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         const int t0 = c * kC;
         const int n = min(kC, T - t0);
         const uint32_t kq = sm.kq(c % kStages);
+        const bool has_prev = c > 0;                               // a chunk c - 1 exists
+        const uint32_t prev_phase = (uint32_t)(g == 1 ? it : it - 1);  // its handoff phase
         if (t < kC) betas[t] = t < n ? __bfloat162float(beta[(size_t)bh * T + t0 + t]) : 0.f;
+        // G = [K; Q] K^T
         bool ok = true;
         if (t == 0) {
             if (it > 0) ok = ctl.wait(B_O_FREE + g, (uint32_t)(it - 1));  // o tile of c-2 stored
-            ok = ok && ctl.wait(B_G_FULL + g, (uint32_t)it);
+            ok = ok && ctl.wait(B_KQ_FULL + c % 6, (uint32_t)(c / 6));
+            if (ok) {
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t a = kq + (uint32_t)(kk >> 2) * kRegKQ + (uint32_t)(kk & 3) * 32u;
+                    mma_bf16_ss(tmem + colG, sw128_desc(a, 16, 1024), sw128_desc(a, 16, 1024),
+                                IDESC_G, kk > 0);
+                }
+                mma_commit(ctl.bar(B_G_FULL + g));
+                ok = ctl.wait(B_G_FULL + g, (uint32_t)it);
+            }
         }
         if (wg_sync_or(barid, !ok)) return;
         tc_fence_after_sync();
@@ -684,9 +633,18 @@ __device__ void chunk_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         }
         fence_proxy_async_smem();
         wg_sync(barid);
-        if (t == 0) mbar_arrive(ctl.bar(B_TP_READY + g));
-
-        if (!wg_wait(ctl, B_PT_FULL + g, (uint32_t)it, t, barid)) return;
+        // PT = P Tm into the group's columns
+        ok = true;
+        if (t == 0) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + colG, sw128_desc(tp + 32u * kk, 16, 1024),
+                            sw128_desc(tp + 8192u + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
+            mma_commit(ctl.bar(B_PT_FULL + g));
+            ok = ctl.wait(B_PT_FULL + g, (uint32_t)it);
+        }
+        if (wg_sync_or(barid, !ok)) return;
         tc_fence_after_sync();
         if (t < 64) {  // PT -> bf16 over P
             float x[64];
@@ -696,13 +654,26 @@ __device__ void chunk_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         fence_proxy_async_smem();
         tc_fence_before_sync();
         wg_sync(barid);
-        if (t == 0) mbar_arrive(ctl.bar(B_TP_FULL + g));
-
-        // DW done, and the previous chunk's state MMA has read [Q'; -W].
+        // DW = [PT; Tm] K as two N = 64 halves: dk 0-63 into the group's columns,
+        // dk 64-127 into the shared columns (once the other group has read them).
         ok = true;
         if (t == 0) {
-            ok = ctl.wait(B_DW_FULL + g, (uint32_t)it);
-            if (g == 1 || it > 0) ok = ok && ctl.wait(B_QW_FREE + g, (uint32_t)(g == 1 ? it : it - 1));
+            if (has_prev) ok = ctl.wait(B_DWX_FREE + g, prev_phase);
+            if (ok) {
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss(tmem + colG, sw128_desc(tp + 32u * kk, 16, 1024),
+                                sw128_desc(kq + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss(tmem + COL_DWX, sw128_desc(tp + 32u * kk, 16, 1024),
+                                sw128_desc(kq + kRegKQ + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
+                mma_commit(ctl.bar(B_DW_FULL + g));
+                ok = ctl.wait(B_DW_FULL + g, (uint32_t)it);
+                // [Q'; -W] may be overwritten once the previous chunk's state MMA read it.
+                if (ok && has_prev) ok = ctl.wait(B_QW_FREE + g, prev_phase);
+            }
         }
         if (wg_sync_or(barid, !ok)) return;
         tc_fence_after_sync();
@@ -736,12 +707,31 @@ __device__ void chunk_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         tmem_wait_st();
         tc_fence_before_sync();
         wg_sync(barid);
+        // D1 = [PT; Tm] V once v has landed and the previous chunk's D1 was read out.
+        ok = true;
         if (t == 0) {
-            mbar_arrive(ctl.bar(B_DW_EMPTY));
-            mbar_arrive(ctl.bar(B_G_EMPTY + g));
+            mbar_arrive(ctl.bar(B_DWX_FREE + (g ^ 1)));
             mbar_arrive(ctl.bar(B_QW_READY + g));
+            ok = ctl.wait(B_V_FULL + g, (uint32_t)it);
+            if (ok && has_prev) ok = ctl.wait(B_D1_EMPTY + g, prev_phase);
+            if (ok) {
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss(tmem + COL_D1, sw128_desc(tp + 32u * kk, 16, 1024),
+                                sw128_desc(sm.v() + 2048u * kk, 8192, 1024), IDESC_KB, kk > 0);
+                mma_commit(ctl.bar(B_V_EMPTY));
+                mma_commit(ctl.bar(B_D1I_FULL + g));
+            }
         }
+        if (wg_sync_or(barid, !ok)) return;
     }
+}
+
+__device__ void chunk_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int g,
+                           const __nv_bfloat16* __restrict__ beta, int bh, int T, int nchunks) {
+    chunk_role_body(ctl, sm, tmem, t, g, beta, bh, T, nchunks);
+    if (t == 0) drain_mmas(ctl, B_DRAIN + 1 + g);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -781,8 +771,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     if (warp == 0) {
         if (lane == 0) producer_role(ctl, sm, &tm_q, &tm_k, &tm_v, bh, nchunks);
-    } else if (warp == 1) {
-        if (lane == 0) mma_role(ctl, sm, tmem, nchunks);
     } else if (warp == 2) {
         if (lane == 0) store_role(ctl, sm, &tm_o, bh, nchunks);
     } else if (warp >= 4 && warp < 8) {

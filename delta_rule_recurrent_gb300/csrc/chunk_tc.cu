@@ -11,27 +11,28 @@
 //     U'   = U - W S                        (true per-token errors)
 //     O    = Q S + P U'                     S <- S + K^T U'
 // The kernel regroups the output as O = (Q - PT K) S + PT V with PT = P Tm,
-// which equals Q S + P U' exactly and lets one MMA produce O and U' together:
+// which equals Q S + P U' exactly and lets one accumulator produce O and U':
 //     D1 = [PT; Tm] V  (+)  [Q - PT K; -W] S    ->  rows 0-63: O, rows 64-127: U'
-// so the state-dependent chain per chunk is only: S -> bf16 -> one MMA over
-// dk -> U' -> bf16 -> S += K^T U'.
+// Everything left of the (+) depends only on the chunk's own inputs, so the
+// state-dependent chain per chunk is: S -> bf16 -> the D1 MMAs -> U' -> bf16
+// -> S += K^T U'.
 //
 // One CTA owns one (batch, head) and keeps S in TMEM for the whole sequence.
-// Its 16 warps have fixed roles so the state chain of chunk c overlaps the
-// state-independent work of the following chunks:
+// Its warps have fixed roles:
 //   warp 0      TMA producer: [K; Q] tiles into a 3-stage ring, v tiles
 //               (3-D maps, so rows past the end of a sequence read as zeros)
 //   warp 1      TMEM owner
-//   warp 2      TMA store of o tiles (rows past the end are not written)
-//   warps 4-7   state group: S -> bf16 operand, the state MMAs, O and U'
-//               epilogues, final state
-//   warps 8-11, 12-15   chunk groups for even and odd chunks: the G, PT, DW
-//               and D1 MMAs, A and P, the triangular solve, Tm, PT, and the
-//               [Q'; -W] operand
-// Each group's elected thread issues its own MMAs and waits on its own
-// commits, so no MMA waits for another role to notice that it is ready.
-// Operand tiles in shared memory use the 128-byte swizzled layout TMA writes;
-// [Q'; -W], the A operand of the state-dependent MMA, lives in TMEM.
+//   warps 4-7   state group: S -> bf16 operand, the D1 MMAs, the o tile
+//               (TMA store from the spent half of the S operand), U',
+//               S += K^T U', final state
+//   warps 8-11, 12-15   chunk groups for even and odd chunks: G = [K; Q] K^T,
+//               A and P, the triangular solve, Tm, PT and the [Q'; -W]
+//               operand, which each group leaves in a TMEM buffer of its own
+// A chunk group meets the state group only at the hand-over of its chunk and
+// when it reuses its buffers two chunks later, so the groups run ahead of the
+// state chain by up to a chunk each.  Each elected thread issues its role's
+// MMAs and waits on its own commits.  Operand tiles in shared memory use the
+// 128-byte swizzled layout TMA writes.
 // Every wait is bounded: on a timeout the CTA records an error code (read
 // back with dn_device_error), drains what it started and exits.
 #include <cudaTypedefs.h>
@@ -69,15 +70,15 @@ constexpr uint32_t kRegKQ = 128 * 128;               // one dk half of [K; Q]: 1
 constexpr uint32_t kStageKQ = 2 * kRegKQ;            // 32 KB
 constexpr uint32_t OFF_KQ = 0;                       // kStages stages
 constexpr uint32_t OFF_V = OFF_KQ + kStages * kStageKQ;  // V, 2 dv halves x 64 rows
-constexpr uint32_t OFF_TP = OFF_V + 16384;           // 2 x [PT; Tm] (per chunk group); then o tile
-constexpr uint32_t OFF_SB = OFF_TP + 2 * 16384;      // S as bf16 (2 x 128 rows); then U'
+constexpr uint32_t OFF_TP = OFF_V + 16384;           // 2 x [PT; Tm] (one per chunk group)
+constexpr uint32_t OFF_SB = OFF_TP + 2 * 16384;      // S as bf16 (2 x 128 rows); then U', o tile
 constexpr uint32_t OFF_X = OFF_SB + 32768;           // 2 x fp32 64 x kP: A, overwritten by X
 constexpr uint32_t kXBytes = 64 * kP * 4;
 constexpr uint32_t OFF_Y = OFF_X + 2 * kXBytes;      // 2 x fp32 32 x kYP solve scratch
 constexpr uint32_t kYBytes = 32 * kYP * 4;
 constexpr uint32_t OFF_BETA = OFF_Y + 2 * kYBytes;   // 2 x 64 fp32
 constexpr uint32_t OFF_BAR = OFF_BETA + 512;         // mbarriers, 8 bytes each
-constexpr int kNumBars = 40;
+constexpr int kNumBars = 26;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * kNumBars;  // abort flag, TMEM address
 constexpr uint32_t kSmemBytes = OFF_MISC + 16 + 1024;  // + 1024-byte alignment slack
 static_assert(OFF_V % 1024 == 0 && OFF_TP % 1024 == 0 && OFF_SB % 1024 == 0, "tile alignment");
@@ -91,26 +92,23 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 enum : int {
     B_KQ_FULL = 0,     // [6] q, k tiles landed               (producer -> chunk group)
     B_KQ_EMPTY = 6,    // [3] stage's last reader done         (state MMA -> producer)
-    B_V_FULL = 9,      // [2] v tile landed                    (producer -> chunk group)
-    B_V_EMPTY = 11,    // D1 = [PT;Tm] V done, v tile free     (chunk MMA -> producer)
-    B_G_FULL = 12,     // [2] G = [K;Q] K^T done               (own commit)
-    B_PT_FULL = 14,    // [2] PT = P Tm done                   (own commit)
-    B_DW_FULL = 16,    // [2] DW = [PT;Tm] K done              (own commit)
-    B_D1I_FULL = 18,   // [2] D1 = [PT;Tm] V done              (chunk MMA -> state group)
-    B_QW_READY = 20,   // [2] [Q'; -W] written to TMEM         (chunk group -> state group)
-    B_QW_FREE = 22,    // [2] previous D1 += [Q';-W] S done    (state MMA -> chunk group)
-    B_D1_EMPTY = 24,   // [2] previous D1 read out             (state group -> chunk group)
-    B_DWX_FREE = 26,   // [2] previous DW upper half read out  (chunk group -> other group)
-    B_O_FULL = 28,     // [2] o tile written                   (state group -> store warp)
-    B_O_FREE = 30,     // [2] o tile stored                    (store warp -> chunk group)
-    B_D1_FULL = 32,    // D1 += [Q';-W] S done                 (own commit, state group)
-    B_S_READY = 33,    // S += K^T U' done                     (own commit, state group)
-    B_DRAIN = 34,      // [3] final drain of each issuer's MMAs (state, group 0, group 1)
+    B_V_FULL = 9,      // v tile landed                        (producer -> state group)
+    B_V_EMPTY = 10,    // D1 MMAs done, v tile free            (state MMA -> producer)
+    B_G_FULL = 11,     // [2] G = [K;Q] K^T done               (own commit)
+    B_PT_FULL = 13,    // [2] PT = P Tm done                   (own commit)
+    B_DW_FULL = 15,    // [2] DW = [PT;Tm] K done              (own commit)
+    B_QW_READY = 17,   // [2] [PT; Tm] and [Q'; -W] ready      (chunk group -> state group)
+    B_FREE = 19,       // [2] D1 MMAs read them; both free     (state MMA -> chunk group)
+    B_D1_FULL = 21,    // D1 done                              (own commit, state group)
+    B_S_READY = 22,    // S += K^T U' done                     (own commit, state group)
+    B_DRAIN = 23,      // [3] final drain of each issuer's MMAs (state, group 0, group 1)
 };
 
 // TMEM columns (512 allocated):
-//   S | D1 (O, U') | [Q'; -W] bf16 | G, PT, DW[:, 0:64] per chunk group x 2 | DW[:, 64:128]
-constexpr uint32_t COL_S = 0, COL_D1 = 128, COL_QW = 256, COL_G = 320, COL_DWX = 448;
+//   S | D1 (O, U') | per chunk group g: [Q'; -W] bf16 (64), then G / PT (64)
+// DW = [PT; Tm] K spans a group's 128 columns (dk 0-63 in the [Q'; -W]
+// columns, dk 64-127 in the G columns) before being packed into the first 64.
+constexpr uint32_t COL_S = 0, COL_D1 = 128, COL_GRP = 256;
 
 constexpr uint32_t IDESC_G = idesc_bf16_f32(128, 64, 0, 0);    // [K;Q] K^T
 constexpr uint32_t IDESC_N64 = idesc_bf16_f32(128, 64, 0, 1);  // A K-major, B MN-major, N = 64
@@ -161,15 +159,6 @@ __device__ __forceinline__ void store_row64_bf16(uint32_t region, int r, const f
                      pack_bf16(x[8 * c + 2], x[8 * c + 3]), pack_bf16(x[8 * c + 4], x[8 * c + 5]),
                      pack_bf16(x[8 * c + 6], x[8 * c + 7]));
 }
-// 32 fp32 values -> bf16 into 4 consecutive chunks (from ch0) of row r.
-__device__ __forceinline__ void store_row32_bf16(uint32_t region, int r, int ch0,
-                                                 const float (&x)[32]) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-        st_shared_v4(region + sw128(r, ch0 + c), pack_bf16(x[8 * c + 0], x[8 * c + 1]),
-                     pack_bf16(x[8 * c + 2], x[8 * c + 3]), pack_bf16(x[8 * c + 4], x[8 * c + 5]),
-                     pack_bf16(x[8 * c + 6], x[8 * c + 7]));
-}
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void sts4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 __device__ __forceinline__ void fma4(float4& acc, float a, const float4& b) {
@@ -196,6 +185,12 @@ __device__ __forceinline__ bool wg_sync_or(int id, bool v) {
         : "r"((uint32_t)v), "r"(id)
         : "memory");
     return r != 0;
+}
+// 16-bit read-only global load that the compiler keeps in program order.
+__device__ __forceinline__ uint16_t ld_nc_u16(const void* p) {
+    uint16_t v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -364,6 +359,7 @@ __device__ __forceinline__ void solve_unit_lower64(float* X, float* Ys, int t, i
     }
 }
 
+
 // ----------------------------------------------------------------- roles
 __device__ void producer_role(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q,
                               const CUtensorMap* tm_k, const CUtensorMap* tm_v, int bh,
@@ -393,7 +389,7 @@ __device__ void producer_role(const Ctl& ctl, const Smem& sm, const CUtensorMap*
             progressed = true;
         }
         if (nv < nchunks && (nv < 1 || mbar_test_wait(ctl.bar(B_V_EMPTY), (uint32_t)(nv - 1) & 1u))) {
-            const uint32_t bar = ctl.bar(B_V_FULL + (nv & 1));
+            const uint32_t bar = ctl.bar(B_V_FULL);
             mbar_arrive_expect_tx(bar, 2 * 8192);
             tma_load_3d(sm.v(), tm_v, bar, 0, nv * kC, bh);
             tma_load_3d(sm.v() + 8192, tm_v, bar, 64, nv * kC, bh);
@@ -416,10 +412,7 @@ __device__ void producer_role(const Ctl& ctl, const Smem& sm, const CUtensorMap*
         const int n_b = (nkq - b + 5) / 6;  // loads that completed on barrier b
         if (n_b > 0) mbar_wait(ctl.bar(B_KQ_FULL + b), (uint32_t)(n_b - 1) & 1u, kTimeoutNs);
     }
-    for (int b = 0; b < 2; ++b) {
-        const int n_b = (nv - b + 1) / 2;
-        if (n_b > 0) mbar_wait(ctl.bar(B_V_FULL + b), (uint32_t)(n_b - 1) & 1u, kTimeoutNs);
-    }
+    if (nv > 0) mbar_wait(ctl.bar(B_V_FULL), (uint32_t)(nv - 1) & 1u, kTimeoutNs);
 }
 
 // Lets everything a thread issued to the tensor core finish (bounded), so
@@ -429,25 +422,11 @@ __device__ __forceinline__ void drain_mmas(const Ctl& ctl, int b) {
     mbar_wait(ctl.bar(b), 0, kTimeoutNs);
 }
 
-__device__ void store_role(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_o, int bh,
-                           int nchunks) {
-    for (int c = 0; c < nchunks; ++c) {
-        if (!ctl.wait(B_O_FULL + (c & 1), (uint32_t)(c >> 1))) break;
-        const uint32_t tile = sm.tp(c & 1);
-        tma_store_3d(tm_o, tile, 0, c * kC, bh);
-        tma_store_3d(tm_o, tile + 8192u, 64, c * kC, bh);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-        mbar_arrive(ctl.bar(B_O_FREE + (c & 1)));
-    }
-    bulk_wait_group0();
-}
-
 // State group (warps 4-7): thread t owns state row t = TMEM lane t; thread 0
-// issues the two state-dependent MMAs of every chunk.
+// issues the state group's MMAs.
 __device__ void state_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
-                                const float* __restrict__ S0, float* __restrict__ S_T, int bh,
-                                int nchunks) {
+                                const float* __restrict__ S0, float* __restrict__ S_T,
+                                const CUtensorMap* tm_o, int bh, int nchunks) {
     constexpr int kBar = 1;
     const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
     // S0 (or zeros) into TMEM.
@@ -475,7 +454,15 @@ __device__ void state_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, i
 
     for (int c = 0; c < nchunks; ++c) {
         const int g = c & 1;
-        if (c > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(c - 1), t, kBar)) return;
+        // S += K^T U' of the previous chunk done, and its o tile read out by TMA.
+        if (c > 0) {
+            bool ok0 = true;
+            if (t == 0) {
+                ok0 = ctl.wait(B_S_READY, (uint32_t)(c - 1));
+                bulk_wait_group_read0();
+            }
+            if (wg_sync_or(kBar, !ok0)) return;
+        }
         tc_fence_after_sync();
         // S (fp32) -> bf16 operand tile: dv halves as regions, row t.
 #pragma unroll
@@ -487,39 +474,48 @@ __device__ void state_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, i
         fence_proxy_async_smem();
         tc_fence_before_sync();
         wg_sync(kBar);
-        // D1 += [Q'; -W] S, once the chunk group has [Q'; -W] in TMEM and D1 initialised.
+        // D1 = [PT; Tm] V + [Q'; -W] S once the chunk group has handed its chunk over.
         bool ok = true;
         if (t == 0) {
-            ok = ctl.wait(B_QW_READY + g, (uint32_t)(c >> 1)) &&
-                 ctl.wait(B_D1I_FULL + g, (uint32_t)(c >> 1));
+            ok = ctl.wait(B_QW_READY + g, (uint32_t)(c >> 1)) && ctl.wait(B_V_FULL, (uint32_t)c);
             if (ok) {
                 tc_fence_after_sync();
+                const uint32_t tp = sm.tp(g), qw = tmem + COL_GRP + 128u * (uint32_t)g;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss(tmem + COL_D1, sw128_desc(tp + 32u * kk, 16, 1024),
+                                sw128_desc(sm.v() + 2048u * kk, 8192, 1024), IDESC_KB, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ts(tmem + COL_D1, tmem + COL_QW + 8u * kk,
+                    mma_bf16_ts(tmem + COL_D1, qw + 8u * kk,
                                 sw128_desc(sm.sb() + 2048u * kk, 16384, 1024), IDESC_KB, 1);
                 mma_commit(ctl.bar(B_D1_FULL));
-                mma_commit(ctl.bar(B_QW_FREE + (g ^ 1)));
+                mma_commit(ctl.bar(B_V_EMPTY));
+                mma_commit(ctl.bar(B_FREE + g));
                 ok = ctl.wait(B_D1_FULL, (uint32_t)c);
             }
         }
         if (wg_sync_or(kBar, !ok)) return;
         tc_fence_after_sync();
-        // rows 0-63: O into the chunk's o tile; rows 64-127: U' over the S operand.
-        const int row = t & 63;
-        const uint32_t dst = (t < 64) ? sm.tp(g) : sm.sb();
+        // The S operand is spent: rows 0-63 (o) into its upper 16 KB as the o
+        // tile, rows 64-127 (U') into its lower 16 KB.
+        {
+            const uint32_t dst = sm.sb() + (t < 64 ? 16384u : 0u);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float x[64];
-            tmem_ld64f(tmem + lane_base + COL_D1 + 64u * half, x);
-            store_row64_bf16(dst + (uint32_t)half * 8192u, row, x);
+            for (int half = 0; half < 2; ++half) {
+                float x[64];
+                tmem_ld64f(tmem + lane_base + COL_D1 + 64u * half, x);
+                store_row64_bf16(dst + (uint32_t)half * 8192u, t & 63, x);
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
         wg_sync(kBar);
         if (t == 0) {
-            mbar_arrive(ctl.bar(B_D1_EMPTY + (g ^ 1)));
-            mbar_arrive(ctl.bar(B_O_FULL + g));
+            // o tile out (rows past the end of the sequence are clipped)
+            tma_store_3d(tm_o, sm.sb() + 16384u, 0, c * kC, bh);
+            tma_store_3d(tm_o, sm.sb() + 24576u, 64, c * kC, bh);
+            bulk_commit_group();
             // S += K^T U'
             const uint32_t kq = sm.kq(c % kStages);
             tc_fence_after_sync();
@@ -547,40 +543,68 @@ __device__ void state_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, i
 }
 
 __device__ void state_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
-                           const float* __restrict__ S0, float* __restrict__ S_T, int bh,
-                           int nchunks) {
-    state_role_body(ctl, sm, tmem, t, S0, S_T, bh, nchunks);
-    if (t == 0) drain_mmas(ctl, B_DRAIN + 0);
+                           const float* __restrict__ S0, float* __restrict__ S_T,
+                           const CUtensorMap* tm_o, int bh, int nchunks) {
+    state_role_body(ctl, sm, tmem, t, S0, S_T, tm_o, bh, nchunks);
+    if (t == 0) {
+        drain_mmas(ctl, B_DRAIN + 0);
+        bulk_wait_group0();  // o tiles written
+    }
+}
+
+// One quarter (32 dk columns) of the [Q'; -W] operand, packed to bf16 pairs:
+// rows 0-63 (t < 64) take Q - PT K with Q from the chunk's q tile, rows 64-127
+// take -W.  `x` holds the fp32 DW values of the quarter for this row.
+__device__ __forceinline__ void qw_quarter(const float (&x)[32], bool is_q, uint32_t q_region,
+                                           int row, int ch0, uint32_t* pk) {
+    if (is_q) {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const uint4 qv = ld_shared_v4(q_region + sw128(64 + row, ch0 + cc));
+            const float2 a0 = unpack_bf16(qv.x), a1 = unpack_bf16(qv.y), a2 = unpack_bf16(qv.z),
+                         a3 = unpack_bf16(qv.w);
+            const float* d = x + 8 * cc;
+            pk[4 * cc + 0] = pack_bf16(a0.x - d[0], a0.y - d[1]);
+            pk[4 * cc + 1] = pack_bf16(a1.x - d[2], a1.y - d[3]);
+            pk[4 * cc + 2] = pack_bf16(a2.x - d[4], a2.y - d[5]);
+            pk[4 * cc + 3] = pack_bf16(a3.x - d[6], a3.y - d[7]);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(-x[2 * e], -x[2 * e + 1]);
+    }
 }
 
 // Chunk group g (0: even chunks, warps 8-11; 1: odd chunks, warps 12-15);
-// thread 0 issues the group's MMAs.  For the handoffs between the two
-// groups and the state group, "previous chunk" phases are: group 1 waits
-// phase it, group 0 phase it - 1 (and chunk 0 waits for nothing).
+// thread 0 issues the group's MMAs.  Iteration `it` handles chunk c = g + 2 it.
 __device__ void chunk_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int g,
                                 const __nv_bfloat16* __restrict__ beta, int bh, int T,
                                 int nchunks) {
     const int barid = 2 + g;
     const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
-    const uint32_t colG = COL_G + 64u * (uint32_t)g;
+    const uint32_t colQW = COL_GRP + 128u * (uint32_t)g, colG = colQW + 64u;
     float* const X = sm.x(g);
     float* const Ys = sm.y(g);
     float* const betas = sm.beta(g);
     const uint32_t tp = sm.tp(g);
     const int row = t & 63;
+    const __nv_bfloat16* const beta_bh = beta + (size_t)bh * T;
+    // Strengths of the group's next chunk, loaded one iteration ahead (0 past
+    // T); the load is issued as volatile PTX so it stays where it is written.
+    uint16_t bnext = 0;
+    if (t < kC && g * kC + t < T) bnext = ld_nc_u16(beta_bh + g * kC + t);
 
     for (int c = g, it = 0; c < nchunks; c += 2, ++it) {
-        const int t0 = c * kC;
-        const int n = min(kC, T - t0);
         const uint32_t kq = sm.kq(c % kStages);
-        const bool has_prev = c > 0;                               // a chunk c - 1 exists
-        const uint32_t prev_phase = (uint32_t)(g == 1 ? it : it - 1);  // its handoff phase
-        if (t < kC) betas[t] = t < n ? __bfloat162float(beta[(size_t)bh * T + t0 + t]) : 0.f;
+        if (t < kC) {
+            betas[t] = __bfloat162float(__ushort_as_bfloat16(bnext));
+            const int nx = (c + 2) * kC + t;
+            bnext = nx < T ? ld_nc_u16(beta_bh + nx) : (uint16_t)0;
+        }
         // G = [K; Q] K^T
         bool ok = true;
         if (t == 0) {
-            if (it > 0) ok = ctl.wait(B_O_FREE + g, (uint32_t)(it - 1));  // o tile of c-2 stored
-            ok = ok && ctl.wait(B_KQ_FULL + c % 6, (uint32_t)(c / 6));
+            ok = ctl.wait(B_KQ_FULL + c % 6, (uint32_t)(c / 6));
             if (ok) {
                 tc_fence_after_sync();
 #pragma unroll
@@ -595,43 +619,46 @@ __device__ void chunk_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, i
         }
         if (wg_sync_or(barid, !ok)) return;
         tc_fence_after_sync();
-        // A = beta_i (k_i . k_j) for j < i (TMEM rows 0-63) as fp32;
-        // P = q_t . k_j for j <= t (rows 64-127) as bf16 over rows 0-63 of [PT; Tm].
-        {
+        // A = beta_i (k_i . k_j) for j < i (TMEM rows 0-63) into the fp32 solve
+        // array.  P (rows 64-127) stays in TMEM until the solve is done.
+        if (t < 64) {
             float x[64];
             tmem_ld64f(tmem + lane_base + colG, x);
-            if (t < 64) {
-                const float bi = betas[row];
+            const float bi = betas[row];
 #pragma unroll
-                for (int j = 0; j < 64; j += 4)
-                    sts4(X + row * kP + j,
-                         make_float4(j + 0 < row ? bi * x[j + 0] : 0.f, j + 1 < row ? bi * x[j + 1] : 0.f,
-                                     j + 2 < row ? bi * x[j + 2] : 0.f, j + 3 < row ? bi * x[j + 3] : 0.f));
-            } else {
+            for (int j = 0; j < 64; j += 4)
+                sts4(X + row * kP + j,
+                     make_float4(j + 0 < row ? bi * x[j + 0] : 0.f, j + 1 < row ? bi * x[j + 1] : 0.f,
+                                 j + 2 < row ? bi * x[j + 2] : 0.f, j + 3 < row ? bi * x[j + 3] : 0.f));
+        }
+        tc_fence_before_sync();
+        wg_sync(barid);
+        solve_unit_lower64(X, Ys, t, barid);
+        // [PT; Tm] and [Q'; -W] of chunk c - 2 must have been read by the state group.
+        if (it > 0 && !wg_wait(ctl, B_FREE + g, (uint32_t)(it - 1), t, barid)) return;
+        tc_fence_after_sync();
+        {
+            float x[64];
+            if (t < 64) {  // Tm row t = X row t diag(beta) -> bf16 row 64 + t of [PT; Tm]
+#pragma unroll
+                for (int e = 0; e < 64; e += 4) {
+                    const float4 xv = lds4(X + t * kP + e), bv = lds4(betas + e);
+                    x[e] = xv.x * bv.x;
+                    x[e + 1] = xv.y * bv.y;
+                    x[e + 2] = xv.z * bv.z;
+                    x[e + 3] = xv.w * bv.w;
+                }
+                store_row64_bf16(tp, 64 + t, x);
+            } else {  // P row: q_t . k_j for j <= t -> bf16 row t of [PT; Tm]
+                tmem_ld64f(tmem + lane_base + colG, x);
 #pragma unroll
                 for (int j = 0; j < 64; ++j)
                     if (j > row) x[j] = 0.f;
                 store_row64_bf16(tp, row, x);
             }
         }
-        tc_fence_before_sync();
-        wg_sync(barid);
-        solve_unit_lower64(X, Ys, t, barid);
-        // Tm = X diag(beta) -> bf16 rows 64-127 of [PT; Tm]
-        {
-            const int i = t >> 1, c0 = 32 * (t & 1);
-            float x[32];
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-                const float4 xv = lds4(X + i * kP + c0 + e), bv = lds4(betas + c0 + e);
-                x[e] = xv.x * bv.x;
-                x[e + 1] = xv.y * bv.y;
-                x[e + 2] = xv.z * bv.z;
-                x[e + 3] = xv.w * bv.w;
-            }
-            store_row32_bf16(tp, 64 + i, c0 / 8, x);
-        }
         fence_proxy_async_smem();
+        tc_fence_before_sync();
         wg_sync(barid);
         // PT = P Tm into the group's columns
         ok = true;
@@ -654,77 +681,42 @@ __device__ void chunk_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, i
         fence_proxy_async_smem();
         tc_fence_before_sync();
         wg_sync(barid);
-        // DW = [PT; Tm] K as two N = 64 halves: dk 0-63 into the group's columns,
-        // dk 64-127 into the shared columns (once the other group has read them).
+        // DW = [PT; Tm] K over the group's 128 columns
         ok = true;
         if (t == 0) {
-            if (has_prev) ok = ctl.wait(B_DWX_FREE + g, prev_phase);
-            if (ok) {
-                tc_fence_after_sync();
+            tc_fence_after_sync();
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(tmem + colG, sw128_desc(tp + 32u * kk, 16, 1024),
-                                sw128_desc(kq + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(tmem + COL_DWX, sw128_desc(tp + 32u * kk, 16, 1024),
-                                sw128_desc(kq + kRegKQ + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
-                mma_commit(ctl.bar(B_DW_FULL + g));
-                ok = ctl.wait(B_DW_FULL + g, (uint32_t)it);
-                // [Q'; -W] may be overwritten once the previous chunk's state MMA read it.
-                if (ok && has_prev) ok = ctl.wait(B_QW_FREE + g, prev_phase);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + colQW, sw128_desc(tp + 32u * kk, 16, 1024),
+                            sw128_desc(kq + 2048u * kk, kRegKQ, 1024), IDESC_KB, kk > 0);
+            mma_commit(ctl.bar(B_DW_FULL + g));
+            ok = ctl.wait(B_DW_FULL + g, (uint32_t)it);
         }
         if (wg_sync_or(barid, !ok)) return;
         tc_fence_after_sync();
-        // rows 0-63: Q' = Q - PT K; rows 64-127: -W.  Written as bf16 pairs to TMEM.
+        // [Q'; -W] as bf16 pairs into the group's first 64 columns; all of DW
+        // is read before the packed operand overwrites its dk 0-63 half.
+        {
+            const bool is_q = t < 64;
+            uint32_t hi[32], lo[32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float x[64];
-            tmem_ld64f(tmem + lane_base + (half == 0 ? colG : COL_DWX), x);
-            uint32_t packed[32];
-            if (t < 64) {
-                const uint32_t region = kq + (uint32_t)half * kRegKQ;
-                uint4 qv[8];
+            for (int qd = 0; qd < 4; ++qd) {  // dk quarter qd sits in columns colQW + 32 qd
+                float x[32];
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + colQW + 32u * (uint32_t)qd, r);
+                tmem_wait_ld();
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) qv[cc] = ld_shared_v4(region + sw128(64 + row, cc));
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const float2 a0 = unpack_bf16(qv[cc].x), a1 = unpack_bf16(qv[cc].y),
-                                 a2 = unpack_bf16(qv[cc].z), a3 = unpack_bf16(qv[cc].w);
-                    const float* d = x + 8 * cc;
-                    packed[4 * cc + 0] = pack_bf16(a0.x - d[0], a0.y - d[1]);
-                    packed[4 * cc + 1] = pack_bf16(a1.x - d[2], a1.y - d[3]);
-                    packed[4 * cc + 2] = pack_bf16(a2.x - d[4], a2.y - d[5]);
-                    packed[4 * cc + 3] = pack_bf16(a3.x - d[6], a3.y - d[7]);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) packed[e] = pack_bf16(-x[2 * e], -x[2 * e + 1]);
+                for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
+                qw_quarter(x, is_q, kq + (uint32_t)(qd >> 1) * kRegKQ, row, (qd & 1) * 4,
+                           (qd < 2 ? lo : hi) + 16 * (qd & 1));
             }
-            tmem_st32(tmem + lane_base + COL_QW + 32u * half, packed);
+            tmem_st32(tmem + lane_base + colQW, lo);
+            tmem_st32(tmem + lane_base + colQW + 32u, hi);
         }
         tmem_wait_st();
         tc_fence_before_sync();
         wg_sync(barid);
-        // D1 = [PT; Tm] V once v has landed and the previous chunk's D1 was read out.
-        ok = true;
-        if (t == 0) {
-            mbar_arrive(ctl.bar(B_DWX_FREE + (g ^ 1)));
-            mbar_arrive(ctl.bar(B_QW_READY + g));
-            ok = ctl.wait(B_V_FULL + g, (uint32_t)it);
-            if (ok && has_prev) ok = ctl.wait(B_D1_EMPTY + g, prev_phase);
-            if (ok) {
-                tc_fence_after_sync();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(tmem + COL_D1, sw128_desc(tp + 32u * kk, 16, 1024),
-                                sw128_desc(sm.v() + 2048u * kk, 8192, 1024), IDESC_KB, kk > 0);
-                mma_commit(ctl.bar(B_V_EMPTY));
-                mma_commit(ctl.bar(B_D1I_FULL + g));
-            }
-        }
-        if (wg_sync_or(barid, !ok)) return;
+        if (t == 0) mbar_arrive(ctl.bar(B_QW_READY + g));
     }
 }
 
@@ -771,10 +763,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     if (warp == 0) {
         if (lane == 0) producer_role(ctl, sm, &tm_q, &tm_k, &tm_v, bh, nchunks);
-    } else if (warp == 2) {
-        if (lane == 0) store_role(ctl, sm, &tm_o, bh, nchunks);
     } else if (warp >= 4 && warp < 8) {
-        state_role(ctl, sm, tmem, tid - 128, S0, S_T, bh, nchunks);
+        state_role(ctl, sm, tmem, tid - 128, S0, S_T, &tm_o, bh, nchunks);
     } else if (warp >= 8) {
         const int g = (warp - 8) >> 2;
         chunk_role(ctl, sm, tmem, tid - 256 - 128 * g, g, beta, bh, T, nchunks);

@@ -49,12 +49,15 @@ def _stream_handle(device) -> int:
 def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
               initial_state: torch.Tensor | None = None, output_final_state: bool = True,
               chunk_size: int = 64, algo: str = "auto", out: torch.Tensor | None = None,
-              final_state: torch.Tensor | None = None):
+              final_state: torch.Tensor | None = None, workspace="auto"):
     """Chunkwise delta-rule forward (``dn_chunk_fwd``).
 
     Returns ``(o, S_T)``; ``S_T`` is None when ``output_final_state`` is
     False.  ``final_state`` may be ``initial_state`` itself to update it in
-    place; ``out`` may supply the output buffer.
+    place; ``out`` may supply the output buffer.  ``workspace``: "auto"
+    allocates the scratch ``dn_chunk_fwd_workspace_bytes`` asks for (the
+    two-pass tensor-core path), None runs without scratch (one fused kernel),
+    and a uint8 CUDA tensor of at least that many bytes is used as given.
     """
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
@@ -87,7 +90,15 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Ten
             raise ValueError("final_state must be float32 [B,H,dk,dv]")
     lib = load()
     ws_bytes = lib.dn_chunk_fwd_workspace_bytes(B, H, T, dk, dv, chunk_size, dt)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be 'auto', None or a uint8 CUDA tensor")
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    elif workspace is None:
+        ws, ws_bytes = None, 0
+    else:
+        _check_cuda("workspace", workspace, dev)
+        ws, ws_bytes = workspace, workspace.numel() * workspace.element_size()
     with torch.cuda.device(dev):
         check(lib.dn_chunk_fwd_algo(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(),

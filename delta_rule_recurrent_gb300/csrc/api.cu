@@ -103,15 +103,16 @@ int dn_device_error(void) {
 }
 
 size_t dn_chunk_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt) {
-    (void)B; (void)H; (void)T; (void)dk; (void)dv; (void)C; (void)dt;
-    return 0;
+    if (B <= 0 || H <= 0 || T <= 0 || C != 64 || !dn::chunk_tc_supports(dk, dv, dt)) return 0;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return 0;
+    return dn::chunk_tc_workspace_bytes((int)BH, T);
 }
 
 int dn_chunk_fwd_algo(const void* q, const void* k, const void* v, const void* beta,
                       const float* S0, void* o, float* S_T, int B, int H, int T, int dk,
                       int dv, int C, int dt, void* workspace, size_t workspace_bytes,
                       void* stream, int algo) {
-    (void)workspace;
     if (B < 0 || H < 0 || T < 0)
         return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d T=%d)", B, H, T);
     if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
@@ -125,8 +126,9 @@ int dn_chunk_fwd_algo(const void* q, const void* k, const void* v, const void* b
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
     const size_t need_ws = dn_chunk_fwd_workspace_bytes(B, H, T, dk, dv, C, dt);
-    if (workspace_bytes < need_ws)
-        return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes, need_ws);
+    if (workspace && workspace_bytes < need_ws)
+        return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed (or pass NULL)",
+                    workspace_bytes, need_ws);
     if (algo == DN_ALGO_TCGEN05 && !dn::chunk_tc_supports(dk, dv, dt))
         return fail(DN_ERR_UNSUPPORTED, "tcgen05 path does not cover dk=%d dv=%d dtype=%d", dk,
                     dv, dt);
@@ -167,8 +169,15 @@ int dn_chunk_fwd_algo(const void* q, const void* k, const void* v, const void* b
     }
     const bool use_tc = algo == DN_ALGO_TCGEN05 ||
                         (algo == DN_ALGO_AUTO && dn::chunk_tc_supports(dk, dv, dt));
+    void* const ws = (use_tc && workspace && need_ws > 0) ? workspace : nullptr;
+    if (ws) {
+        const Span sw{"workspace", ws, need_ws};
+        if (int st2 = check_device_ptr(sw, 16, dev)) return st2;
+        for (const Span* s : {&sq, &sk, &sv, &sb, &so, &s0, &sT})
+            if (overlaps(sw, *s)) return fail(DN_ERR_INVALID_ARG, "workspace overlaps %s", s->name);
+    }
     cudaError_t e = use_tc
-        ? dn::launch_chunk_tc(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, st)
+        ? dn::launch_chunk_tc(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, ws, st)
         : dn::launch_chunk_simt(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, st);
     return cuda_status(e, use_tc ? "chunk forward (tcgen05) launch" : "chunk forward (SIMT) launch");
 }

@@ -38,6 +38,8 @@
 #include <cudaTypedefs.h>
 #include <cuda.h>
 
+#include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "dn_common.cuh"
@@ -55,8 +57,6 @@ using namespace ptx;
 
 constexpr int kC = 64;         // chunk length
 constexpr int kD = 128;        // dk = dv
-constexpr int kThreads = 512;  // 16 warps
-constexpr int kStages = 3;     // [K; Q] ring depth
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s without progress
 // The polling roles count SM cycles (clock64 is cheap to read); at the
 // GB300's clocks 4e9 cycles is 2 s or more.
@@ -68,41 +68,59 @@ constexpr int kYP = 36;  // row pitch of the 32 x 32 solve scratch
 // ---------------------------------------------------------------- smem map
 constexpr uint32_t kRegKQ = 128 * 128;               // one dk half of [K; Q]: 128 rows x 128 B
 constexpr uint32_t kStageKQ = 2 * kRegKQ;            // 32 KB
-constexpr uint32_t OFF_KQ = 0;                       // kStages stages
-constexpr uint32_t OFF_V = OFF_KQ + kStages * kStageKQ;  // V, 2 dv halves x 64 rows
-constexpr uint32_t OFF_TP = OFF_V + 16384;           // 2 x [PT; Tm] (one per chunk group)
-constexpr uint32_t OFF_SB = OFF_TP + 2 * 16384;      // S as bf16 (2 x 128 rows); then U', o tile
-constexpr uint32_t OFF_X = OFF_SB + 32768;           // 2 x fp32 64 x kP: A, overwritten by X
-constexpr uint32_t kXBytes = 64 * kP * 4;
-constexpr uint32_t OFF_Y = OFF_X + 2 * kXBytes;      // 2 x fp32 32 x kYP solve scratch
-constexpr uint32_t kYBytes = 32 * kYP * 4;
-constexpr uint32_t OFF_BETA = OFF_Y + 2 * kYBytes;   // 2 x 64 fp32
-constexpr uint32_t OFF_BAR = OFF_BETA + 512;         // mbarriers, 8 bytes each
-constexpr int kNumBars = 26;
-constexpr uint32_t OFF_MISC = OFF_BAR + 8 * kNumBars;  // abort flag, TMEM address
-constexpr uint32_t kSmemBytes = OFF_MISC + 16 + 1024;  // + 1024-byte alignment slack
-static_assert(OFF_V % 1024 == 0 && OFF_TP % 1024 == 0 && OFF_SB % 1024 == 0, "tile alignment");
-static_assert(OFF_X % 16 == 0 && OFF_Y % 16 == 0 && OFF_BETA % 16 == 0, "vector alignment");
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kTile = 16384;                    // a 128 x 64 or 64 x 128 bf16 tile
+constexpr uint32_t kXBytes = 64 * kP * 4;            // fp32 64 x kP solve array
+constexpr uint32_t kYBytes = 32 * kYP * 4;           // fp32 32 x kYP solve scratch
+constexpr int kNumBars = 34;
+// Shared memory of the sequence kernel.  The fused form (kSplit false) also
+// holds the chunk groups' solve arrays; the split form, whose [PT; Tm] tiles
+// come from the prepare kernel, spends that space on a second v buffer and a
+// constant operand tile.
+template <bool kSplit>
+struct Layout {
+    static constexpr int kStages = 3;                          // [K; Q] ring depth
+    static constexpr int kVBufs = kSplit ? 2 : 1;              // v tiles in flight
+    static constexpr uint32_t OFF_KQ = 0;                      // kStages stages
+    static constexpr uint32_t OFF_V = OFF_KQ + kStages * kStageKQ;  // v: 2 dv halves x 64 rows each
+    static constexpr uint32_t OFF_TP = OFF_V + kVBufs * kTile; // 2 x [PT; Tm] (one per chunk group)
+    static constexpr uint32_t OFF_SB = OFF_TP + 2 * kTile;     // S as bf16 (2 x 128 rows); then U', o tile
+    static constexpr uint32_t OFF_I = OFF_SB + 2 * kTile;      // split: constant [-I; 0] operand
+    static constexpr uint32_t OFF_X = OFF_I + (kSplit ? kTile : 0);  // fused: 2 x A, overwritten by X
+    static constexpr uint32_t OFF_Y = OFF_X + (kSplit ? 0 : 2 * kXBytes);     // fused: 2 x scratch
+    static constexpr uint32_t OFF_BETA = OFF_Y + (kSplit ? 0 : 2 * kYBytes);  // fused: 2 x 64 fp32
+    static constexpr uint32_t OFF_BAR = OFF_BETA + (kSplit ? 0 : 512);        // mbarriers
+    static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * kNumBars;  // abort flag, TMEM address
+    static constexpr uint32_t kSmemBytes = OFF_MISC + 16 + 1024;  // + 1024-byte alignment slack
+    static_assert(OFF_V % 1024 == 0 && OFF_TP % 1024 == 0 && OFF_SB % 1024 == 0, "tile alignment");
+    static_assert(OFF_X % 16 == 0 && OFF_Y % 16 == 0 && OFF_BETA % 16 == 0, "vector alignment");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
 
 // mbarrier indices.  Every barrier has exactly one waiting role, which
 // consumes its phases in order, so a parity test can never see a phase two
-// ahead of the one it asks for.  Barriers indexed [2] belong to the chunk
+// ahead of the one it asks for.  B_FREE is waited on by the chunk group in
+// the fused form and by the producer (before it reloads [PT; Tm]) in the
+// split form.  Barriers indexed [2] belong to the chunk
 // group of that parity; [6] is (stage, group): chunk c uses c % 6.
 enum : int {
     B_KQ_FULL = 0,     // [6] q, k tiles landed               (producer -> chunk group)
-    B_KQ_EMPTY = 6,    // [3] stage's last reader done         (state MMA -> producer)
-    B_V_FULL = 9,      // v tile landed                        (producer -> state group)
-    B_V_EMPTY = 10,    // D1 MMAs done, v tile free            (state MMA -> producer)
-    B_G_FULL = 11,     // [2] G = [K;Q] K^T done               (own commit)
-    B_PT_FULL = 13,    // [2] PT = P Tm done                   (own commit)
-    B_DW_FULL = 15,    // [2] DW = [PT;Tm] K done              (own commit)
-    B_QW_READY = 17,   // [2] [PT; Tm] and [Q'; -W] ready      (chunk group -> state group)
-    B_FREE = 19,       // [2] D1 MMAs read them; both free     (state MMA -> chunk group)
-    B_D1_FULL = 21,    // D1 done                              (own commit, state group)
-    B_S_READY = 22,    // S += K^T U' done                     (own commit, state group)
-    B_DRAIN = 23,      // [3] final drain of each issuer's MMAs (state, group 0, group 1)
+    B_KQ_EMPTY = 6,    // [4] stage's last reader done         (state MMA -> producer)
+    B_V_FULL = 10,     // [2] v tile landed (per v buffer)     (producer -> state group)
+    B_V_EMPTY = 12,    // [2] D1 MMAs done, v buffer free      (state MMA -> producer)
+    B_G_FULL = 14,     // [2] G = [K;Q] K^T done               (own commit)
+    B_PT_FULL = 16,    // [2] PT = P Tm done                   (own commit)
+    B_DW_FULL = 18,    // [2] DW = [PT;Tm] K done              (own commit)
+    B_QW_READY = 20,   // [2] [PT; Tm] and [Q'; -W] ready      (chunk group -> state group)
+    B_FREE = 22,       // [2] D1 MMAs read them; both free     (state MMA -> group or producer)
+    B_D1_FULL = 24,    // [2] D1 done (per state half)         (own commit, state group)
+    B_S_READY = 26,    // [2] S += K^T U' done (per state half) (own commit, state group)
+    B_DRAIN = 28,      // [4] final drain of each MMA issuer
+    B_TP_FULL = 32,    // [2] split form: [PT; Tm] tile landed (producer -> chunk group)
 };
+static_assert(B_TP_FULL + 2 <= kNumBars, "barrier count");
+// Chunk c waits on [K; Q] barrier c % kKQBars: one barrier per (stage, group) pair.
+template <bool kSplit>
+constexpr int kKQBars = Layout<kSplit>::kStages % 2 ? 2 * Layout<kSplit>::kStages : Layout<kSplit>::kStages;
 
 // TMEM columns (512 allocated):
 //   S | D1 (O, U') | per chunk group g: [Q'; -W] bf16 (64), then G / PT (64)
@@ -114,6 +132,7 @@ constexpr uint32_t IDESC_G = idesc_bf16_f32(128, 64, 0, 0);    // [K;Q] K^T
 constexpr uint32_t IDESC_N64 = idesc_bf16_f32(128, 64, 0, 1);  // A K-major, B MN-major, N = 64
 constexpr uint32_t IDESC_KB = idesc_bf16_f32(128, 128, 0, 1);  // A K-major (smem or TMEM), B MN-major
 constexpr uint32_t IDESC_MM = idesc_bf16_f32(128, 128, 1, 1);  // both MN-major
+constexpr uint32_t IDESC_MM64 = idesc_bf16_f32(128, 64, 1, 1);  // both MN-major, N = 64
 
 enum : unsigned { kErrTimeout = 1 };
 
@@ -168,21 +187,21 @@ __device__ __forceinline__ void fma4(float4& acc, float a, const float4& b) {
     acc.w = fmaf(a, b.w, acc.w);
 }
 __device__ __forceinline__ float4 neg4(float4 v) { return make_float4(-v.x, -v.y, -v.z, -v.w); }
-// Named barrier over one 128-thread warpgroup.
-__device__ __forceinline__ void wg_sync(int id) {
-    asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+// Named barrier over one 128-thread warpgroup (or n threads).
+__device__ __forceinline__ void wg_sync(int id, int n = 128) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 // Named barrier over one warpgroup that also ORs a flag across it, so every
 // thread of the group takes the same branch after a bounded wait.
-__device__ __forceinline__ bool wg_sync_or(int id, bool v) {
+__device__ __forceinline__ bool wg_sync_or(int id, bool v, int n = 128) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, 128, p;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)v), "r"(id)
+        : "r"((uint32_t)v), "r"(id), "r"(n)
         : "memory");
     return r != 0;
 }
@@ -227,27 +246,31 @@ struct Ctl {
 // Group wait: thread 0 of the warpgroup polls the barrier, the others sleep
 // in the named barrier.  True for the whole group, or false for the whole
 // group if the wait gave up.
-__device__ __forceinline__ bool wg_wait(const Ctl& ctl, int b, uint32_t parity, int t, int barid) {
+__device__ __forceinline__ bool wg_wait(const Ctl& ctl, int b, uint32_t parity, int t, int barid,
+                                        int n = 128) {
     bool ok = true;
     if (t == 0) ok = ctl.wait(b, parity);
-    return !wg_sync_or(barid, !ok);
+    return !wg_sync_or(barid, !ok, n);
 }
 
+template <bool kSplit>
 struct Smem {
+    using L = Layout<kSplit>;
     uint32_t base;   // shared address of the 1024-aligned base
     uint8_t* gbase;  // generic pointer to it
-    __device__ uint32_t kq(int s) const { return base + OFF_KQ + (uint32_t)s * kStageKQ; }
-    __device__ uint32_t tp(int g) const { return base + OFF_TP + (uint32_t)g * 16384u; }
-    __device__ uint32_t v() const { return base + OFF_V; }
-    __device__ uint32_t sb() const { return base + OFF_SB; }
+    __device__ uint32_t kq(int c) const { return base + L::OFF_KQ + (uint32_t)(c % L::kStages) * kStageKQ; }
+    __device__ uint32_t tp(int g) const { return base + L::OFF_TP + (uint32_t)g * kTile; }
+    __device__ uint32_t v(int c) const { return base + L::OFF_V + (uint32_t)(c % L::kVBufs) * kTile; }
+    __device__ uint32_t sb() const { return base + L::OFF_SB; }
+    __device__ uint32_t itile() const { return base + L::OFF_I; }
     __device__ float* x(int g) const {
-        return reinterpret_cast<float*>(gbase + OFF_X + (uint32_t)g * kXBytes);
+        return reinterpret_cast<float*>(gbase + L::OFF_X + (uint32_t)g * kXBytes);
     }
     __device__ float* y(int g) const {
-        return reinterpret_cast<float*>(gbase + OFF_Y + (uint32_t)g * kYBytes);
+        return reinterpret_cast<float*>(gbase + L::OFF_Y + (uint32_t)g * kYBytes);
     }
     __device__ float* beta(int g) const {
-        return reinterpret_cast<float*>(gbase + OFF_BETA + (uint32_t)g * 256u);
+        return reinterpret_cast<float*>(gbase + L::OFF_BETA + (uint32_t)g * 256u);
     }
 };
 
@@ -360,26 +383,128 @@ __device__ __forceinline__ void solve_unit_lower64(float* X, float* Ys, int t, i
 }
 
 
+// Variant of the solve above for the prepare kernel, where many chunks share
+// an SM and shared-memory bandwidth, not latency, sets the pace.  The 16 x 16
+// diagonal blocks are solved the same way (fp32); the two block-merge levels
+// (16 -> 32 and 32 -> 64, the same products as above) run on warp-level
+// m16n8k8 tensor-core MMAs with tf32 operands and fp32 accumulation, which
+// read each operand element once per 16 x 8 tile instead of once per thread.
+// X then holds (I + A)^{-1} to about 1e-4 (tf32 products), well below the
+// bf16 rounding its use as an MMA operand applies afterwards.
+__device__ __forceinline__ uint32_t f2tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4],
+                                                const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// acc (16 x 8) += L (16 x k) R (k x 8) over k in [kb, ke), multiples of 8.  L and
+// R point at the tiles' first elements, with row pitches LP and RP (floats).
+// Fragment layout of m16n8k8: lane = 4 g + q holds A rows g, g + 8 at columns
+// q, q + 4; B rows q, q + 4 at column g; C rows g, g + 8 at columns 2q, 2q + 1.
+template <int LP, int RP>
+__device__ __forceinline__ void tile16x8_tf32(float (&acc)[4], const float* L, const float* R,
+                                              int kb, int ke, int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll 4
+    for (int k = kb; k < ke; k += 8) {
+        const uint32_t a[4] = {f2tf32(L[g * LP + k + q]), f2tf32(L[(g + 8) * LP + k + q]),
+                               f2tf32(L[g * LP + k + q + 4]), f2tf32(L[(g + 8) * LP + k + q + 4])};
+        const uint32_t b[2] = {f2tf32(R[(k + q) * RP + g]), f2tf32(R[(k + q + 4) * RP + g])};
+        mma_tf32_16x8x8(acc, a, b);
+    }
+}
+template <int P>
+__device__ __forceinline__ void store16x8(float* D, const float (&acc)[4], int lane, float s) {
+    const int g = lane >> 2, q = lane & 3;
+    *reinterpret_cast<float2*>(D + g * P + 2 * q) = make_float2(s * acc[0], s * acc[1]);
+    *reinterpret_cast<float2*>(D + (g + 8) * P + 2 * q) = make_float2(s * acc[2], s * acc[3]);
+}
+__device__ __forceinline__ void solve_unit_lower64_mma(float* X, float* Ys, int t, int barid) {
+    if (t < 64) {  // the four 16 x 16 diagonal blocks, one column per thread
+        const int base = (t >> 4) * 16, c = t & 15;
+        const float* blk = X + base * (kP + 1);
+        float x[16];
+#pragma unroll
+        for (int l = 0; l < 16; ++l) x[l] = (l == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 0; r < 15; ++r)
+#pragma unroll
+            for (int l = r + 1; l < 16; ++l) x[l] = fmaf(-blk[l * kP + r], x[r], x[l]);
+        wg_sync(barid);
+#pragma unroll
+        for (int l = 0; l < 16; ++l) X[(base + l) * kP + base + c] = x[l];
+    } else {
+        wg_sync(barid);
+    }
+    wg_sync(barid);
+    const int w = t >> 5, lane = t & 31;
+    {   // 16 -> 32 in both halves: Y = A10 X00, X10 = -X11 Y; warp: half h, columns 8 nt
+        const int h = w >> 1, nt = w & 1, o = 32 * h;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        // X00 is lower triangular: rows k < 8 nt are zero in these columns
+        tile16x8_tf32<kP, kP>(acc, X + (o + 16) * kP + o, X + o * kP + o + 8 * nt, 8 * nt, 16, lane);
+        store16x8<kYP>(Ys + (16 * h) * kYP + 8 * nt, acc, lane, 1.f);
+        wg_sync(barid);
+        float z[4] = {0.f, 0.f, 0.f, 0.f};
+        tile16x8_tf32<kP, kYP>(z, X + (o + 16) * kP + o + 16, Ys + (16 * h) * kYP + 8 * nt, 0, 16,
+                               lane);
+        store16x8<kP>(X + (o + 16) * kP + o + 8 * nt, z, lane, -1.f);
+        wg_sync(barid);
+    }
+    {   // 32 -> 64: Y = A[10] X[00], X[10] = -X[11] Y; warp: rows 16 mt, columns 16 nh .. + 15
+        const int mt = w >> 1, nh = w & 1;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int nt = 2 * nh + j;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            tile16x8_tf32<kP, kP>(acc, X + (32 + 16 * mt) * kP, X + 8 * nt, 8 * nt, 32, lane);
+            store16x8<kYP>(Ys + (16 * mt) * kYP + 8 * nt, acc, lane, 1.f);
+        }
+        wg_sync(barid);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int nt = 2 * nh + j;
+            float z[4] = {0.f, 0.f, 0.f, 0.f};
+            // X[11] is lower triangular: columns past row 16 mt + 15 are zero
+            tile16x8_tf32<kP, kYP>(z, X + (32 + 16 * mt) * kP + 32, Ys + 8 * nt, 0, 16 * mt + 16,
+                                   lane);
+            store16x8<kP>(X + (32 + 16 * mt) * kP + 8 * nt, z, lane, -1.f);
+        }
+        wg_sync(barid);
+    }
+}
+
 // ----------------------------------------------------------------- roles
-__device__ void producer_role(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q,
-                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, int bh,
-                              int nchunks) {
-    int nkq = 0, nv = 0;
+// TMA producer (one thread).  Streams [K; Q] into the stage ring, v into its
+// single buffer and, in the split form, each chunk's [PT; Tm] tile from the
+// workspace into its chunk group's buffer once the state group has released it.
+template <bool kSplit>
+__device__ void producer_role(const Ctl& ctl, const Smem<kSplit>& sm, const CUtensorMap* tm_q,
+                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                              const CUtensorMap* tm_ws, int bh, int nchunks) {
+    constexpr int kS = Layout<kSplit>::kStages, kF = kKQBars<kSplit>, kVB = Layout<kSplit>::kVBufs;
+    int nkq = 0, nv = 0, ntp = kSplit ? 0 : nchunks;
     long long t0 = clock64();
-    while ((nkq < nchunks || nv < nchunks) && !ctl.aborted()) {
+    while ((nkq < nchunks || nv < nchunks || ntp < nchunks) && !ctl.aborted()) {
         bool progressed = false;
-        const int s = nkq % kStages;
         if (nkq < nchunks &&
-            (nkq < kStages ||
-             mbar_test_wait(ctl.bar(B_KQ_EMPTY + s), (uint32_t)(nkq / kStages - 1) & 1u))) {
-            const uint32_t st = sm.kq(s), bar = ctl.bar(B_KQ_FULL + nkq % 6);
+            (nkq < kS ||
+             mbar_test_wait(ctl.bar(B_KQ_EMPTY + nkq % kS), (uint32_t)(nkq / kS - 1) & 1u))) {
+            const uint32_t st = sm.kq(nkq), bar = ctl.bar(B_KQ_FULL + nkq % kF);
             mbar_arrive_expect_tx(bar, 4 * 8192);
             tma_load_3d(st, tm_k, bar, 0, nkq * kC, bh);
             tma_load_3d(st + kRegKQ, tm_k, bar, 64, nkq * kC, bh);
             tma_load_3d(st + 8192, tm_q, bar, 0, nkq * kC, bh);
             tma_load_3d(st + kRegKQ + 8192, tm_q, bar, 64, nkq * kC, bh);
-            if (nkq + kStages < nchunks) {  // warm L2 for this stage's next tiles
-                const int y = (nkq + kStages) * kC;
+            if (nkq + kS < nchunks) {  // warm L2 for this stage's next tiles
+                const int y = (nkq + kS) * kC;
                 tma_prefetch_l2_3d(tm_k, 0, y, bh);
                 tma_prefetch_l2_3d(tm_k, 64, y, bh);
                 tma_prefetch_l2_3d(tm_q, 0, y, bh);
@@ -388,17 +513,30 @@ __device__ void producer_role(const Ctl& ctl, const Smem& sm, const CUtensorMap*
             ++nkq;
             progressed = true;
         }
-        if (nv < nchunks && (nv < 1 || mbar_test_wait(ctl.bar(B_V_EMPTY), (uint32_t)(nv - 1) & 1u))) {
-            const uint32_t bar = ctl.bar(B_V_FULL);
+        if (nv < nchunks &&
+            (nv < kVB ||
+             mbar_test_wait(ctl.bar(B_V_EMPTY + nv % kVB), (uint32_t)(nv / kVB - 1) & 1u))) {
+            const uint32_t bar = ctl.bar(B_V_FULL + nv % kVB);
             mbar_arrive_expect_tx(bar, 2 * 8192);
-            tma_load_3d(sm.v(), tm_v, bar, 0, nv * kC, bh);
-            tma_load_3d(sm.v() + 8192, tm_v, bar, 64, nv * kC, bh);
-            if (nv + 1 < nchunks) {  // the v tile is single-buffered: warm L2 for the next one
-                tma_prefetch_l2_3d(tm_v, 0, (nv + 1) * kC, bh);
-                tma_prefetch_l2_3d(tm_v, 64, (nv + 1) * kC, bh);
+            tma_load_3d(sm.v(nv), tm_v, bar, 0, nv * kC, bh);
+            tma_load_3d(sm.v(nv) + 8192, tm_v, bar, 64, nv * kC, bh);
+            if (nv + kVB < nchunks) {  // warm L2 for this buffer's next tile
+                tma_prefetch_l2_3d(tm_v, 0, (nv + kVB) * kC, bh);
+                tma_prefetch_l2_3d(tm_v, 64, (nv + kVB) * kC, bh);
             }
             ++nv;
             progressed = true;
+        }
+        if (kSplit && ntp < nchunks) {
+            const int g = ntp & 1, it = ntp >> 1;
+            if (it == 0 || mbar_test_wait(ctl.bar(B_FREE + g), (uint32_t)(it - 1) & 1u)) {
+                const uint32_t bar = ctl.bar(B_TP_FULL + g);
+                mbar_arrive_expect_tx(bar, kTile);
+                tma_load_3d(sm.tp(g), tm_ws, bar, 0, ntp * 128, bh);
+                if (ntp + 2 < nchunks) tma_prefetch_l2_3d(tm_ws, 0, (ntp + 2) * 128, bh);
+                ++ntp;
+                progressed = true;
+            }
         }
         if (progressed) {
             t0 = clock64();
@@ -408,11 +546,19 @@ __device__ void producer_role(const Ctl& ctl, const Smem& sm, const CUtensorMap*
         }
     }
     // Leave nothing in flight: wait (bounded) for the last load on each barrier.
-    for (int b = 0; b < 6; ++b) {
-        const int n_b = (nkq - b + 5) / 6;  // loads that completed on barrier b
+    for (int b = 0; b < kF; ++b) {
+        const int n_b = (nkq - b + kF - 1) / kF;  // loads that completed on barrier b
         if (n_b > 0) mbar_wait(ctl.bar(B_KQ_FULL + b), (uint32_t)(n_b - 1) & 1u, kTimeoutNs);
     }
-    if (nv > 0) mbar_wait(ctl.bar(B_V_FULL), (uint32_t)(nv - 1) & 1u, kTimeoutNs);
+    for (int b = 0; b < kVB; ++b) {
+        const int n_b = (nv - b + kVB - 1) / kVB;
+        if (n_b > 0) mbar_wait(ctl.bar(B_V_FULL + b), (uint32_t)(n_b - 1) & 1u, kTimeoutNs);
+    }
+    if (kSplit)
+        for (int g = 0; g < 2; ++g) {
+            const int n_g = (ntp - g + 1) / 2;
+            if (n_g > 0) mbar_wait(ctl.bar(B_TP_FULL + g), (uint32_t)(n_g - 1) & 1u, kTimeoutNs);
+        }
 }
 
 // Lets everything a thread issued to the tensor core finish (bounded), so
@@ -422,20 +568,182 @@ __device__ __forceinline__ void drain_mmas(const Ctl& ctl, int b) {
     mbar_wait(ctl.bar(b), 0, kTimeoutNs);
 }
 
-// State group (warps 4-7): thread t owns state row t = TMEM lane t; thread 0
-// issues the state group's MMAs.
-__device__ void state_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
+// State role: thread ts owns state row t = ts % 128 (TMEM lane t).  In the
+// fused form one warpgroup (warps 4-7) converts all 128 columns; in the split
+// form a second warpgroup (warps 0-3, ts >= 128) takes the dv 64-127 half of
+// every conversion.  Thread ts = 0 issues the state MMAs.
+template <bool kSplit>
+__device__ void state_role_body(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t tmem, int ts,
                                 const float* __restrict__ S0, float* __restrict__ S_T,
                                 const CUtensorMap* tm_o, int bh, int nchunks) {
-    constexpr int kBar = 1;
+    constexpr int kBar = 1, kN = kSplit ? 256 : 128, kHalves = kSplit ? 1 : 2;
+    constexpr int kVB = Layout<kSplit>::kVBufs;
+    const int t = ts & 127, h0 = kSplit ? (ts >> 7) : 0;  // row; first dv half handled
     const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
     // S0 (or zeros) into TMEM.
 #pragma unroll
-    for (int part = 0; part < 4; ++part) {
+    for (int hh = 0; hh < kHalves; ++hh) {
+        const int h = h0 + hh;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            uint32_t r[32];
+            if (S0) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    S0 + ((size_t)bh * kD + t) * kD + 64 * h + 32 * part);
+#pragma unroll
+                for (int v4 = 0; v4 < 8; ++v4) {
+                    const float4 f = src[v4];
+                    r[4 * v4 + 0] = __float_as_uint(f.x);
+                    r[4 * v4 + 1] = __float_as_uint(f.y);
+                    r[4 * v4 + 2] = __float_as_uint(f.z);
+                    r[4 * v4 + 3] = __float_as_uint(f.w);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = 0u;
+            }
+            tmem_st32(tmem + lane_base + COL_S + 64u * h + 32u * part, r);
+        }
+    }
+    tmem_wait_st();
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int g = c & 1;
+        const uint32_t tp = sm.tp(g), qw = tmem + COL_GRP + 128u * (uint32_t)g;
+        // S += K^T U' of the previous chunk done, and its o tile read out by TMA.
+        if (c > 0) {
+            bool ok0 = true;
+            if (ts == 0) {
+                ok0 = ctl.wait(B_S_READY, (uint32_t)(c - 1));
+                bulk_wait_group_read0();
+            }
+            if (wg_sync_or(kBar, !ok0, kN)) return;
+        }
+        tc_fence_after_sync();
+        // D1 = [PT; Tm] V needs no S: issue it now if the chunk is already
+        // handed over, so it runs while S is converted.
+        bool vpart = false;
+        if (ts == 0 && mbar_test_wait(ctl.bar(B_QW_READY + g), (uint32_t)(c >> 1) & 1u) &&
+            mbar_test_wait(ctl.bar(B_V_FULL + c % kVB), (uint32_t)(c / kVB) & 1u)) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + COL_D1, sw128_desc(tp + 32u * kk, 16, 1024),
+                            sw128_desc(sm.v(c) + 2048u * kk, 8192, 1024), IDESC_KB, kk > 0);
+            vpart = true;
+        }
+        // S (fp32) -> bf16 operand tile: dv halves as regions, row t.
+#pragma unroll
+        for (int hh = 0; hh < kHalves; ++hh) {
+            const int h = h0 + hh;
+            float x[64];
+            tmem_ld64f(tmem + lane_base + COL_S + 64u * h, x);
+            store_row64_bf16(sm.sb() + (uint32_t)h * 16384u, t, x);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        wg_sync(kBar, kN);
+        // D1 (+)= [PT; Tm] V, D1 += [Q'; -W] S once the chunk group has handed its chunk over.
+        bool ok = true;
+        if (ts == 0) {
+            ok = ctl.wait(B_QW_READY + g, (uint32_t)(c >> 1)) &&
+                 ctl.wait(B_V_FULL + c % kVB, (uint32_t)(c / kVB));
+            if (ok) {
+                tc_fence_after_sync();
+                if (!vpart)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss(tmem + COL_D1, sw128_desc(tp + 32u * kk, 16, 1024),
+                                    sw128_desc(sm.v(c) + 2048u * kk, 8192, 1024), IDESC_KB, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16_ts(tmem + COL_D1, qw + 8u * kk,
+                                sw128_desc(sm.sb() + 2048u * kk, 16384, 1024), IDESC_KB, 1);
+                mma_commit(ctl.bar(B_D1_FULL));
+                mma_commit(ctl.bar(B_V_EMPTY + c % kVB));
+                mma_commit(ctl.bar(B_FREE + g));
+                ok = ctl.wait(B_D1_FULL, (uint32_t)c);
+            }
+        }
+        if (wg_sync_or(kBar, !ok, kN)) return;
+        tc_fence_after_sync();
+        // The S operand is spent: rows 0-63 (o) into its upper 16 KB as the o
+        // tile, rows 64-127 (U') into its lower 16 KB.
+        {
+            const uint32_t dst = sm.sb() + (t < 64 ? 16384u : 0u);
+#pragma unroll
+            for (int hh = 0; hh < kHalves; ++hh) {
+                const int h = h0 + hh;
+                float x[64];
+                tmem_ld64f(tmem + lane_base + COL_D1 + 64u * h, x);
+                store_row64_bf16(dst + (uint32_t)h * 8192u, t & 63, x);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        wg_sync(kBar, kN);
+        if (ts == 0) {
+            // S += K^T U'
+            const uint32_t kq = sm.kq(c);
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + COL_S, sw128_desc(kq + 2048u * kk, kRegKQ, 1024),
+                            sw128_desc(sm.sb() + 2048u * kk, 8192, 1024), IDESC_MM, 1);
+            mma_commit(ctl.bar(B_S_READY));
+            mma_commit(ctl.bar(B_KQ_EMPTY + c % Layout<kSplit>::kStages));
+            // o tile out (rows past the end of the sequence are clipped)
+            tma_store_3d(tm_o, sm.sb() + 16384u, 0, c * kC, bh);
+            tma_store_3d(tm_o, sm.sb() + 24576u, 64, c * kC, bh);
+            bulk_commit_group();
+        }
+    }
+    if (nchunks > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(nchunks - 1), ts, kBar, kN)) return;
+    tc_fence_after_sync();
+    if (S_T) {
+#pragma unroll
+        for (int hh = 0; hh < kHalves; ++hh) {
+            const int h = h0 + hh;
+            float x[64];
+            tmem_ld64f(tmem + lane_base + COL_S + 64u * h, x);
+            float4* dst = reinterpret_cast<float4*>(S_T + ((size_t)bh * kD + t) * kD + 64 * h);
+#pragma unroll
+            for (int v4 = 0; v4 < 16; ++v4)
+                dst[v4] = make_float4(x[4 * v4], x[4 * v4 + 1], x[4 * v4 + 2], x[4 * v4 + 3]);
+        }
+    }
+}
+
+template <bool kSplit>
+__device__ void state_role(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t tmem, int ts,
+                           const float* __restrict__ S0, float* __restrict__ S_T,
+                           const CUtensorMap* tm_o, int bh, int nchunks) {
+    state_role_body<kSplit>(ctl, sm, tmem, ts, S0, S_T, tm_o, bh, nchunks);
+    if (ts == 0) {
+        drain_mmas(ctl, B_DRAIN + 0);
+        bulk_wait_group0();  // o tiles written
+    }
+}
+
+// Split form state: the recurrence acts on every dv column of S on its own,
+// so the state runs as two independent chains, one per dv half.  Half h
+// (0: warps 4-7, 1: warps 0-3) owns S[:, 64h .. 64h + 63] and the same D1
+// columns; its 16 KB region of the S operand buffer holds S[:, half] as bf16,
+// then U' (rows 0-63 of the region) and the o half tile (rows 64-127).
+// Thread t owns TMEM lane t; t == 0 issues the half's MMAs.
+__device__ void state_half_body(const Ctl& ctl, const Smem<true>& sm, uint32_t tmem, int t, int h,
+                                const float* __restrict__ S0, float* __restrict__ S_T,
+                                const CUtensorMap* tm_o, int bh, int nchunks) {
+    constexpr int kVB = Layout<true>::kVBufs, kS = Layout<true>::kStages;
+    const int barid = h == 0 ? 1 : 3;
+    const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
+    const uint32_t colS = COL_S + 64u * (uint32_t)h, colD = COL_D1 + 64u * (uint32_t)h;
+    const uint32_t sbh = sm.sb() + 16384u * (uint32_t)h;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {  // S0[:, half] (or zeros) into TMEM
         uint32_t r[32];
         if (S0) {
-            const float4* src =
-                reinterpret_cast<const float4*>(S0 + ((size_t)bh * kD + t) * kD + 32 * part);
+            const float4* src = reinterpret_cast<const float4*>(
+                S0 + ((size_t)bh * kD + t) * kD + 64 * h + 32 * part);
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4) {
                 const float4 f = src[v4];
@@ -448,106 +756,107 @@ __device__ void state_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, i
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = 0u;
         }
-        tmem_st32(tmem + lane_base + COL_S + 32u * part, r);
+        tmem_st32(tmem + lane_base + colS + 32u * part, r);
     }
     tmem_wait_st();
 
     for (int c = 0; c < nchunks; ++c) {
         const int g = c & 1;
-        // S += K^T U' of the previous chunk done, and its o tile read out by TMA.
+        const uint32_t tp = sm.tp(g), qw = tmem + COL_GRP + 128u * (uint32_t)g;
+        const uint32_t vh = sm.v(c) + 8192u * (uint32_t)h;
+        // This half's S += K^T U' of the previous chunk done, its o tile read out.
         if (c > 0) {
             bool ok0 = true;
             if (t == 0) {
-                ok0 = ctl.wait(B_S_READY, (uint32_t)(c - 1));
+                ok0 = ctl.wait(B_S_READY + h, (uint32_t)(c - 1));
                 bulk_wait_group_read0();
             }
-            if (wg_sync_or(kBar, !ok0)) return;
+            if (wg_sync_or(barid, !ok0)) return;
         }
         tc_fence_after_sync();
-        // S (fp32) -> bf16 operand tile: dv halves as regions, row t.
+        // D1[:, half] = [PT; Tm] V[:, half] needs no S: issue it now if the chunk
+        // is already handed over, so it runs while S is converted.
+        bool vpart = false;
+        if (t == 0 && mbar_test_wait(ctl.bar(B_QW_READY + g), (uint32_t)(c >> 1) & 1u) &&
+            mbar_test_wait(ctl.bar(B_V_FULL + c % kVB), (uint32_t)(c / kVB) & 1u)) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + colD, sw128_desc(tp + 32u * kk, 16, 1024),
+                            sw128_desc(vh + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
+            vpart = true;
+        }
+        {   // S[:, half] (fp32) -> bf16 operand, row t
             float x[64];
-            tmem_ld64f(tmem + lane_base + COL_S + 64u * half, x);
-            store_row64_bf16(sm.sb() + (uint32_t)half * 16384u, t, x);
+            tmem_ld64f(tmem + lane_base + colS, x);
+            store_row64_bf16(sbh, t, x);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
-        wg_sync(kBar);
-        // D1 = [PT; Tm] V + [Q'; -W] S once the chunk group has handed its chunk over.
+        wg_sync(barid);
         bool ok = true;
         if (t == 0) {
-            ok = ctl.wait(B_QW_READY + g, (uint32_t)(c >> 1)) && ctl.wait(B_V_FULL, (uint32_t)c);
+            ok = ctl.wait(B_QW_READY + g, (uint32_t)(c >> 1)) &&
+                 ctl.wait(B_V_FULL + c % kVB, (uint32_t)(c / kVB));
             if (ok) {
                 tc_fence_after_sync();
-                const uint32_t tp = sm.tp(g), qw = tmem + COL_GRP + 128u * (uint32_t)g;
+                if (!vpart)
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(tmem + COL_D1, sw128_desc(tp + 32u * kk, 16, 1024),
-                                sw128_desc(sm.v() + 2048u * kk, 8192, 1024), IDESC_KB, kk > 0);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss(tmem + colD, sw128_desc(tp + 32u * kk, 16, 1024),
+                                    sw128_desc(vh + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ts(tmem + COL_D1, qw + 8u * kk,
-                                sw128_desc(sm.sb() + 2048u * kk, 16384, 1024), IDESC_KB, 1);
-                mma_commit(ctl.bar(B_D1_FULL));
-                mma_commit(ctl.bar(B_V_EMPTY));
+                for (int kk = 0; kk < 8; ++kk)  // D1[:, half] += [Q'; -W] S[:, half]
+                    mma_bf16_ts(tmem + colD, qw + 8u * kk, sw128_desc(sbh + 2048u * kk, 8192, 1024),
+                                IDESC_N64, 1);
+                mma_commit(ctl.bar(B_D1_FULL + h));
+                mma_commit(ctl.bar(B_V_EMPTY + c % kVB));
                 mma_commit(ctl.bar(B_FREE + g));
-                ok = ctl.wait(B_D1_FULL, (uint32_t)c);
+                ok = ctl.wait(B_D1_FULL + h, (uint32_t)c);
             }
         }
-        if (wg_sync_or(kBar, !ok)) return;
+        if (wg_sync_or(barid, !ok)) return;
         tc_fence_after_sync();
-        // The S operand is spent: rows 0-63 (o) into its upper 16 KB as the o
-        // tile, rows 64-127 (U') into its lower 16 KB.
-        {
-            const uint32_t dst = sm.sb() + (t < 64 ? 16384u : 0u);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float x[64];
-                tmem_ld64f(tmem + lane_base + COL_D1 + 64u * half, x);
-                store_row64_bf16(dst + (uint32_t)half * 8192u, t & 63, x);
-            }
+        {   // rows 0-63 (o) -> the o half tile, rows 64-127 (U') -> the U' half
+            float x[64];
+            tmem_ld64f(tmem + lane_base + colD, x);
+            store_row64_bf16(sbh + (t < 64 ? 8192u : 0u), t & 63, x);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
-        wg_sync(kBar);
+        wg_sync(barid);
         if (t == 0) {
-            // o tile out (rows past the end of the sequence are clipped)
-            tma_store_3d(tm_o, sm.sb() + 16384u, 0, c * kC, bh);
-            tma_store_3d(tm_o, sm.sb() + 24576u, 64, c * kC, bh);
-            bulk_commit_group();
-            // S += K^T U'
-            const uint32_t kq = sm.kq(c % kStages);
+            // S[:, half] += K^T U'[:, half]
+            const uint32_t kq = sm.kq(c);
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + COL_S, sw128_desc(kq + 2048u * kk, kRegKQ, 1024),
-                            sw128_desc(sm.sb() + 2048u * kk, 8192, 1024), IDESC_MM, 1);
-            mma_commit(ctl.bar(B_S_READY));
-            mma_commit(ctl.bar(B_KQ_EMPTY + c % kStages));
+                mma_bf16_ss(tmem + colS, sw128_desc(kq + 2048u * kk, kRegKQ, 1024),
+                            sw128_desc(sbh + 2048u * kk, 8192, 1024), IDESC_MM64, 1);
+            mma_commit(ctl.bar(B_S_READY + h));
+            mma_commit(ctl.bar(B_KQ_EMPTY + c % kS));
+            // o half tile out (rows past the end of the sequence are clipped)
+            tma_store_3d(tm_o, sbh + 8192u, 64 * h, c * kC, bh);
+            bulk_commit_group();
         }
     }
-    if (nchunks > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(nchunks - 1), t, kBar)) return;
+    if (nchunks > 0 && !wg_wait(ctl, B_S_READY + h, (uint32_t)(nchunks - 1), t, barid)) return;
     tc_fence_after_sync();
     if (S_T) {
+        float x[64];
+        tmem_ld64f(tmem + lane_base + colS, x);
+        float4* dst = reinterpret_cast<float4*>(S_T + ((size_t)bh * kD + t) * kD + 64 * h);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float x[64];
-            tmem_ld64f(tmem + lane_base + COL_S + 64u * half, x);
-            float4* dst = reinterpret_cast<float4*>(S_T + ((size_t)bh * kD + t) * kD + 64 * half);
-#pragma unroll
-            for (int v4 = 0; v4 < 16; ++v4)
-                dst[v4] = make_float4(x[4 * v4], x[4 * v4 + 1], x[4 * v4 + 2], x[4 * v4 + 3]);
-        }
+        for (int v4 = 0; v4 < 16; ++v4)
+            dst[v4] = make_float4(x[4 * v4], x[4 * v4 + 1], x[4 * v4 + 2], x[4 * v4 + 3]);
     }
 }
 
-__device__ void state_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
-                           const float* __restrict__ S0, float* __restrict__ S_T,
-                           const CUtensorMap* tm_o, int bh, int nchunks) {
-    state_role_body(ctl, sm, tmem, t, S0, S_T, tm_o, bh, nchunks);
+__device__ void state_half_role(const Ctl& ctl, const Smem<true>& sm, uint32_t tmem, int t, int h,
+                                const float* __restrict__ S0, float* __restrict__ S_T,
+                                const CUtensorMap* tm_o, int bh, int nchunks) {
+    state_half_body(ctl, sm, tmem, t, h, S0, S_T, tm_o, bh, nchunks);
     if (t == 0) {
-        drain_mmas(ctl, B_DRAIN + 0);
+        drain_mmas(ctl, B_DRAIN + h);
         bulk_wait_group0();  // o tiles written
     }
 }
@@ -575,11 +884,45 @@ __device__ __forceinline__ void qw_quarter(const float (&x)[32], bool is_q, uint
     }
 }
 
-// Chunk group g (0: even chunks, warps 8-11; 1: odd chunks, warps 12-15);
-// thread 0 issues the group's MMAs.  Iteration `it` handles chunk c = g + 2 it.
-__device__ void chunk_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int g,
-                                const __nv_bfloat16* __restrict__ beta, int bh, int T,
+// DW = [PT; Tm] K (TMEM columns colQW .. colQW + 127, fp32) -> [Q'; -W] as
+// bf16 pairs in colQW .. colQW + 63.  All of DW is read before the packed
+// operand overwrites its dk 0-63 half.  Thread t owns TMEM lane t.
+__device__ __forceinline__ void qw_epilogue(uint32_t tmem, uint32_t lane_base, uint32_t colQW,
+                                            uint32_t kq, int t) {
+    const bool is_q = t < 64;
+    const int row = t & 63;
+    uint32_t hi[32], lo[32];
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {  // dk quarter qd sits in columns colQW + 32 qd
+        float x[32];
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + colQW + 32u * (uint32_t)qd, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
+        qw_quarter(x, is_q, kq + (uint32_t)(qd >> 1) * kRegKQ, row, (qd & 1) * 4,
+                   (qd < 2 ? lo : hi) + 16 * (qd & 1));
+    }
+    tmem_st32(tmem + lane_base + colQW, lo);
+    tmem_st32(tmem + lane_base + colQW + 32u, hi);
+    tmem_wait_st();
+}
+
+// DW = [PT; Tm] K into a chunk group's 128 columns (issued by one thread).
+__device__ __forceinline__ void issue_dw(uint32_t tmem, uint32_t colQW, uint32_t tp, uint32_t kq) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        mma_bf16_ss(tmem + colQW, sw128_desc(tp + 32u * kk, 16, 1024),
+                    sw128_desc(kq + 2048u * kk, kRegKQ, 1024), IDESC_KB, kk > 0);
+}
+
+// Fused form, chunk group g (0: even chunks, warps 8-11; 1: odd chunks,
+// warps 12-15); thread 0 issues the group's MMAs.  Iteration `it` handles
+// chunk c = g + 2 it.
+__device__ void chunk_role_body(const Ctl& ctl, const Smem<false>& sm, uint32_t tmem, int t,
+                                int g, const __nv_bfloat16* __restrict__ beta, int bh, int T,
                                 int nchunks) {
+    constexpr int kF = kKQBars<false>;
     const int barid = 2 + g;
     const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
     const uint32_t colQW = COL_GRP + 128u * (uint32_t)g, colG = colQW + 64u;
@@ -595,7 +938,7 @@ __device__ void chunk_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, i
     if (t < kC && g * kC + t < T) bnext = ld_nc_u16(beta_bh + g * kC + t);
 
     for (int c = g, it = 0; c < nchunks; c += 2, ++it) {
-        const uint32_t kq = sm.kq(c % kStages);
+        const uint32_t kq = sm.kq(c);
         if (t < kC) {
             betas[t] = __bfloat162float(__ushort_as_bfloat16(bnext));
             const int nx = (c + 2) * kC + t;
@@ -604,7 +947,7 @@ __device__ void chunk_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, i
         // G = [K; Q] K^T
         bool ok = true;
         if (t == 0) {
-            ok = ctl.wait(B_KQ_FULL + c % 6, (uint32_t)(c / 6));
+            ok = ctl.wait(B_KQ_FULL + c % kF, (uint32_t)(c / kF));
             if (ok) {
                 tc_fence_after_sync();
 #pragma unroll
@@ -660,7 +1003,7 @@ __device__ void chunk_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, i
         fence_proxy_async_smem();
         tc_fence_before_sync();
         wg_sync(barid);
-        // PT = P Tm into the group's columns
+        // PT = P Tm into the group's scratch columns
         ok = true;
         if (t == 0) {
             tc_fence_after_sync();
@@ -685,58 +1028,113 @@ __device__ void chunk_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, i
         ok = true;
         if (t == 0) {
             tc_fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + colQW, sw128_desc(tp + 32u * kk, 16, 1024),
-                            sw128_desc(kq + 2048u * kk, kRegKQ, 1024), IDESC_KB, kk > 0);
+            issue_dw(tmem, colQW, tp, kq);
             mma_commit(ctl.bar(B_DW_FULL + g));
             ok = ctl.wait(B_DW_FULL + g, (uint32_t)it);
         }
         if (wg_sync_or(barid, !ok)) return;
         tc_fence_after_sync();
-        // [Q'; -W] as bf16 pairs into the group's first 64 columns; all of DW
-        // is read before the packed operand overwrites its dk 0-63 half.
-        {
-            const bool is_q = t < 64;
-            uint32_t hi[32], lo[32];
-#pragma unroll
-            for (int qd = 0; qd < 4; ++qd) {  // dk quarter qd sits in columns colQW + 32 qd
-                float x[32];
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + colQW + 32u * (uint32_t)qd, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
-                qw_quarter(x, is_q, kq + (uint32_t)(qd >> 1) * kRegKQ, row, (qd & 1) * 4,
-                           (qd < 2 ? lo : hi) + 16 * (qd & 1));
-            }
-            tmem_st32(tmem + lane_base + colQW, lo);
-            tmem_st32(tmem + lane_base + colQW + 32u, hi);
-        }
-        tmem_wait_st();
+        qw_epilogue(tmem, lane_base, colQW, kq, t);
         tc_fence_before_sync();
         wg_sync(barid);
         if (t == 0) mbar_arrive(ctl.bar(B_QW_READY + g));
     }
 }
 
-__device__ void chunk_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int g,
-                           const __nv_bfloat16* __restrict__ beta, int bh, int T, int nchunks) {
-    chunk_role_body(ctl, sm, tmem, t, g, beta, bh, T, nchunks);
-    if (t == 0) drain_mmas(ctl, B_DRAIN + 1 + g);
+// Split form: [PT; Tm] arrives from the workspace, so one chunk group
+// (warps 8-11) forms the [Q'; -W] operand of every chunk, alternating between
+// the two buffer sets by chunk parity.  One MMA over the whole [K; Q] tile
+//     DW' = [PT  -I; Tm  0] [K; Q] = [PT K - Q; W] = -[Q'; -W]
+// (the right half of the A operand is a constant tile) leaves only a negate
+// and pack for the epilogue.
+__device__ void chunk_role_split_body(const Ctl& ctl, const Smem<true>& sm, uint32_t tmem, int t,
+                                      int nchunks) {
+    constexpr int kF = kKQBars<true>;
+    const int barid = 2;
+    const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
+    {   // constant [-I; 0] (128 x 64 bf16), row t
+        float x[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) x[j] = (j == t) ? -1.f : 0.f;
+        store_row64_bf16(sm.itile(), t, x);
+        fence_proxy_async_smem();
+        wg_sync(barid);
+    }
+    for (int c = 0; c < nchunks; ++c) {
+        const int g = c & 1, it = c >> 1;
+        const uint32_t kq = sm.kq(c), colQW = COL_GRP + 128u * (uint32_t)g;
+        bool ok = true;
+        if (t == 0) {
+            // The [PT; Tm] tile is loaded only after both state halves released
+            // this buffer set, so its [Q'; -W] columns are free as well.
+            ok = ctl.wait(B_KQ_FULL + c % kF, (uint32_t)(c / kF)) &&
+                 ctl.wait(B_TP_FULL + g, (uint32_t)it);
+            if (ok) {
+                tc_fence_after_sync();
+                const uint32_t tp = sm.tp(g);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t a = kk < 4 ? tp + 32u * kk : sm.itile() + 32u * (kk - 4);
+                    mma_bf16_ss(tmem + colQW, sw128_desc(a, 16, 1024),
+                                sw128_desc(kq + 2048u * kk, kRegKQ, 1024), IDESC_KB, kk > 0);
+                }
+                mma_commit(ctl.bar(B_DW_FULL));
+                ok = ctl.wait(B_DW_FULL, (uint32_t)c);
+            }
+        }
+        if (wg_sync_or(barid, !ok)) return;
+        tc_fence_after_sync();
+        {   // -DW' as bf16 pairs into the set's first 64 columns (all of DW' read first)
+            uint32_t hi[32], lo[32];
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + colQW + 32u * (uint32_t)qd, r);
+                tmem_wait_ld();
+                uint32_t* pk = (qd < 2 ? lo : hi) + 16 * (qd & 1);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16(-__uint_as_float(r[2 * e]), -__uint_as_float(r[2 * e + 1]));
+            }
+            tmem_st32(tmem + lane_base + colQW, lo);
+            tmem_st32(tmem + lane_base + colQW + 32u, hi);
+            tmem_wait_st();
+        }
+        tc_fence_before_sync();
+        wg_sync(barid);
+        if (t == 0) mbar_arrive(ctl.bar(B_QW_READY + g));
+    }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kSplit>
+__device__ void chunk_role(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t tmem, int t, int g,
+                           const __nv_bfloat16* __restrict__ beta, int bh, int T, int nchunks) {
+    if constexpr (kSplit)
+        chunk_role_split_body(ctl, sm, tmem, t, nchunks);
+    else
+        chunk_role_body(ctl, sm, tmem, t, g, beta, bh, T, nchunks);
+    if (t == 0) drain_mmas(ctl, B_DRAIN + 2 + g);
+}
+
+// Sequence kernel: one CTA per (batch, head), the whole sequence in order,
+// 16 warps.  Fused form: producer 0, TMEM owner 1, state 4-7, chunk groups
+// 8-11 and 12-15.  Split form: state halves 4-7 (dv 0-63) and 0-3
+// (dv 64-127), chunk group 8-11, producer 12, TMEM owner 13.
+template <bool kSplit>
+constexpr int kSeqThreads = 512;
+template <bool kSplit>
+__global__ void __launch_bounds__(kSeqThreads<kSplit>, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                const __nv_bfloat16* __restrict__ beta, const float* __restrict__ S0,
-                float* __restrict__ S_T, int T) {
+                const __grid_constant__ CUtensorMap tm_ws, const __nv_bfloat16* __restrict__ beta,
+                const float* __restrict__ S0, float* __restrict__ S_T, int T) {
+    using L = Layout<kSplit>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
-    const Smem sm{base, smem_raw + (base - raw_addr)};
-    int* const misc = reinterpret_cast<int*>(sm.gbase + OFF_MISC);
-    const Ctl ctl{base + OFF_BAR, reinterpret_cast<volatile int*>(misc)};
+    const Smem<kSplit> sm{base, smem_raw + (base - raw_addr)};
+    int* const misc = reinterpret_cast<int*>(sm.gbase + L::OFF_MISC);
+    const Ctl ctl{base + L::OFF_BAR, reinterpret_cast<volatile int*>(misc)};
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -745,14 +1143,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     if (tid == 0) {
         misc[0] = 0;
-        for (int b = 0; b < kNumBars; ++b) mbar_init(ctl.bar(b), 1);
+        // In the split form both state halves release [K; Q] stages, v buffers
+        // and [PT; Tm] / [Q'; -W] sets, so those barriers take two arrivals.
+        for (int b = 0; b < kNumBars; ++b) {
+            const bool two = kSplit && ((b >= B_KQ_EMPTY && b < B_KQ_EMPTY + 4) ||
+                                        (b >= B_V_EMPTY && b < B_V_EMPTY + 2) ||
+                                        (b >= B_FREE && b < B_FREE + 2));
+            mbar_init(ctl.bar(b), two ? 2 : 1);
+        }
         fence_mbar_init();
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_o);
+        if (kSplit) prefetch_tensormap(&tm_ws);
     }
-    if (warp == 1) {
+    constexpr int kProdWarp = kSplit ? 12 : 0, kTmemWarp = kSplit ? 13 : 1;
+    if (warp == kTmemWarp) {
         tmem_alloc(smem_addr(tmem_holder), 512);
         tmem_relinquish();
     }
@@ -761,19 +1168,188 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 0) {
-        if (lane == 0) producer_role(ctl, sm, &tm_q, &tm_k, &tm_v, bh, nchunks);
-    } else if (warp >= 4 && warp < 8) {
-        state_role(ctl, sm, tmem, tid - 128, S0, S_T, &tm_o, bh, nchunks);
-    } else if (warp >= 8) {
+    if (warp == kProdWarp) {
+        if (lane == 0) producer_role<kSplit>(ctl, sm, &tm_q, &tm_k, &tm_v, &tm_ws, bh, nchunks);
+    } else if (warp < 8 && (kSplit || warp >= 4)) {
+        if constexpr (kSplit)
+            state_half_role(ctl, sm, tmem, tid & 127, warp < 4 ? 1 : 0, S0, S_T, &tm_o, bh, nchunks);
+        else
+            state_role<false>(ctl, sm, tmem, tid - 128, S0, S_T, &tm_o, bh, nchunks);
+    } else if (warp >= 8 && warp < (kSplit ? 12 : 16)) {
         const int g = (warp - 8) >> 2;
-        chunk_role(ctl, sm, tmem, tid - 256 - 128 * g, g, beta, bh, T, nchunks);
+        chunk_role<kSplit>(ctl, sm, tmem, tid - 256 - 128 * g, g, beta, bh, T, nchunks);
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kTmemWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------ prepare kernel
+// Split form, first pass: [PT; Tm] of every (batch, head, chunk).  It depends
+// only on the chunk's own k, q and beta, so all chunks of all heads run in
+// parallel.  A CTA is one warpgroup that walks the work items blockIdx.x,
+// blockIdx.x + gridDim.x, ...; several CTAs share an SM, so the loads, MMAs
+// and solves of different chunks overlap.  The tile goes to the workspace,
+// laid out [BH][chunk][128 rows][64] bf16, rows 0-63 PT and 64-127 Tm.
+constexpr int kPrepThreads = 128;
+constexpr int kPrepCtasPerSm = 4;
+constexpr uint32_t P_OFF_KQ = 0;                   // [K; Q] tile; [PT; Tm] reuses its first 16 KB
+constexpr uint32_t P_OFF_X = P_OFF_KQ + kStageKQ;  // fp32 A, overwritten by X
+constexpr uint32_t P_OFF_Y = P_OFF_X + kXBytes;    // solve scratch
+constexpr uint32_t P_OFF_BETA = P_OFF_Y + kYBytes; // 64 fp32
+constexpr uint32_t P_OFF_BAR = P_OFF_BETA + 256;   // mbarriers: tiles landed, MMA done, drain
+constexpr uint32_t P_OFF_MISC = P_OFF_BAR + 24;    // abort flag, TMEM address
+constexpr uint32_t kPrepSmemBytes = P_OFF_MISC + 16 + 1024;
+static_assert(kPrepCtasPerSm * (kPrepSmemBytes + 1024) <= 233472, "prepare kernel occupancy");
+
+__global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
+chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_ws, const __nv_bfloat16* __restrict__ beta,
+                  int T, int nchunks, int items) {
+    constexpr int kBar = 1, B_TILES = 0, B_MMA = 1, B_END = 2;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* const gbase = smem_raw + (base - raw_addr);
+    float* const X = reinterpret_cast<float*>(gbase + P_OFF_X);
+    float* const Ys = reinterpret_cast<float*>(gbase + P_OFF_Y);
+    float* const betas = reinterpret_cast<float*>(gbase + P_OFF_BETA);
+    int* const misc = reinterpret_cast<int*>(gbase + P_OFF_MISC);
+    const Ctl ctl{base + P_OFF_BAR, reinterpret_cast<volatile int*>(misc)};
+    uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
+    const int t = threadIdx.x, row = t & 63;
+    const uint32_t kq = base + P_OFF_KQ, tp = kq;
+    const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
+
+    if (t == 0) {
+        misc[0] = 0;
+        for (int b = 0; b < 3; ++b) mbar_init(ctl.bar(b), 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_ws);
+    }
+    if (t < 32) {
+        tmem_alloc(smem_addr(tmem_holder), 64);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    int n = 0, loads = 0;  // items finished, tile loads issued (thread 0)
+    for (int w = blockIdx.x; w < items; w += gridDim.x, ++n) {
+        const int bh = w / nchunks, c = w % nchunks;
+        if (t == 0) {
+            bulk_wait_group_read0();  // the previous tile's store has read the area
+            const uint32_t bar = ctl.bar(B_TILES);
+            mbar_arrive_expect_tx(bar, 4 * 8192);
+            tma_load_3d(kq, &tm_k, bar, 0, c * kC, bh);
+            tma_load_3d(kq + kRegKQ, &tm_k, bar, 64, c * kC, bh);
+            tma_load_3d(kq + 8192, &tm_q, bar, 0, c * kC, bh);
+            tma_load_3d(kq + kRegKQ + 8192, &tm_q, bar, 64, c * kC, bh);
+            ++loads;
+        }
+        if (t < kC) {
+            const int tok = c * kC + t;
+            betas[t] = tok < T ? __bfloat162float(beta[(size_t)bh * T + tok]) : 0.f;
+        }
+        // G = [K; Q] K^T
+        bool ok = true;
+        if (t == 0) {
+            ok = ctl.wait(B_TILES, (uint32_t)n);
+            if (ok) {
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t a = kq + (uint32_t)(kk >> 2) * kRegKQ + (uint32_t)(kk & 3) * 32u;
+                    mma_bf16_ss(tmem, sw128_desc(a, 16, 1024), sw128_desc(a, 16, 1024), IDESC_G,
+                                kk > 0);
+                }
+                mma_commit(ctl.bar(B_MMA));
+                ok = ctl.wait(B_MMA, (uint32_t)(2 * n));
+            }
+        }
+        if (wg_sync_or(kBar, !ok)) break;
+        tc_fence_after_sync();
+        // A (TMEM rows 0-63) into the solve array; P (rows 64-127) stays in TMEM.
+        if (t < 64) {
+            float x[64];
+            tmem_ld64f(tmem + lane_base, x);
+            const float bi = betas[row];
+#pragma unroll
+            for (int j = 0; j < 64; j += 4)
+                sts4(X + row * kP + j,
+                     make_float4(j + 0 < row ? bi * x[j + 0] : 0.f, j + 1 < row ? bi * x[j + 1] : 0.f,
+                                 j + 2 < row ? bi * x[j + 2] : 0.f, j + 3 < row ? bi * x[j + 3] : 0.f));
+        }
+        tc_fence_before_sync();
+        wg_sync(kBar);
+        solve_unit_lower64_mma(X, Ys, t, kBar);
+        // [K; Q] is spent: Tm and P into the [PT; Tm] tile over its first 16 KB.
+        {
+            float x[64];
+            if (t < 64) {
+#pragma unroll
+                for (int e = 0; e < 64; e += 4) {
+                    const float4 xv = lds4(X + t * kP + e), bv = lds4(betas + e);
+                    x[e] = xv.x * bv.x;
+                    x[e + 1] = xv.y * bv.y;
+                    x[e + 2] = xv.z * bv.z;
+                    x[e + 3] = xv.w * bv.w;
+                }
+                store_row64_bf16(tp, 64 + t, x);
+            } else {
+                tmem_ld64f(tmem + lane_base, x);
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                    if (j > row) x[j] = 0.f;
+                store_row64_bf16(tp, row, x);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        wg_sync(kBar);
+        // PT = P Tm
+        ok = true;
+        if (t == 0) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem, sw128_desc(tp + 32u * kk, 16, 1024),
+                            sw128_desc(tp + 8192u + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
+            mma_commit(ctl.bar(B_MMA));
+            ok = ctl.wait(B_MMA, (uint32_t)(2 * n + 1));
+        }
+        if (wg_sync_or(kBar, !ok)) break;
+        tc_fence_after_sync();
+        if (t < 64) {
+            float x[64];
+            tmem_ld64f(tmem + lane_base, x);
+            store_row64_bf16(tp, t, x);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        wg_sync(kBar);
+        if (t == 0) {
+            tma_store_3d(&tm_ws, tp, 0, c * 128, bh);
+            bulk_commit_group();
+        }
+    }
+    if (t == 0) {
+        drain_mmas(ctl, B_END);
+        if (loads > n) mbar_wait(ctl.bar(B_TILES), (uint32_t)(loads - 1) & 1u, kTimeoutNs);
+        bulk_wait_group0();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (t < 32) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 64);
     }
 }
 
@@ -805,24 +1381,72 @@ bool make_map(CUtensorMap* map, const void* ptr, int BH, int T) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over the workspace [BH][nchunks * 128][64] bf16, one [PT; Tm] tile per box.
+bool make_ws_map(CUtensorMap* map, void* ptr, int BH, int nchunks) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, (cuuint64_t)nchunks * 128, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {128, (cuuint64_t)nchunks * kTile};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 1;
+    return n;
+}
+
 }  // namespace
 
 bool chunk_tc_supports(int dk, int dv, int dt) { return dk == kD && dv == kD && dt == 1; }
 
+size_t chunk_tc_workspace_bytes(int BH, int T) {
+    if (BH <= 0 || T <= 0) return 0;
+    return (size_t)BH * (size_t)((T + kC - 1) / kC) * kTile;
+}
+
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const void* beta,
                             const float* S0, void* o, float* S_T, int BH, int T, int dk, int dv,
-                            int dt, cudaStream_t stream) {
+                            int dt, void* workspace, cudaStream_t stream) {
     if (!chunk_tc_supports(dk, dv, dt)) return cudaErrorNotSupported;
     if (BH <= 0 || T <= 0) return cudaSuccess;
-    CUtensorMap mq, mk, mv, mo;
+    const int nchunks = (T + kC - 1) / kC;
+    CUtensorMap mq, mk, mv, mo, mws;
+    memset(&mws, 0, sizeof(mws));
     if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mv, v, BH, T) ||
-        !make_map(&mo, o, BH, T))
+        !make_map(&mo, o, BH, T) || (workspace && !make_ws_map(&mws, workspace, BH, nchunks)))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(chunk_tc_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (err != cudaSuccess) return err;
-    chunk_tc_kernel<<<BH, kThreads, kSmemBytes, stream>>>(
-        mq, mk, mv, mo, static_cast<const __nv_bfloat16*>(beta), S0, S_T, T);
+    const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(beta);
+    cudaError_t err;
+    if (workspace) {
+        const long long items = (long long)BH * nchunks;
+        if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+        if ((err = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kPrepSmemBytes)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(chunk_tc_kernel<true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        Layout<true>::kSmemBytes)) != cudaSuccess)
+            return err;
+        const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
+        chunk_prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(mq, mk, mws, b, T, nchunks,
+                                                                          (int)items);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        chunk_tc_kernel<true><<<BH, kSeqThreads<true>, Layout<true>::kSmemBytes, stream>>>(
+            mq, mk, mv, mo, mws, b, S0, S_T, T);
+        return cudaGetLastError();
+    }
+    if ((err = cudaFuncSetAttribute(chunk_tc_kernel<false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Layout<false>::kSmemBytes)) != cudaSuccess)
+        return err;
+    chunk_tc_kernel<false><<<BH, kSeqThreads<false>, Layout<false>::kSmemBytes, stream>>>(
+        mq, mk, mv, mo, mws, b, S0, S_T, T);
     return cudaGetLastError();
 }
 

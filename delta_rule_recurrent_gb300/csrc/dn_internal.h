@@ -21,12 +21,16 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v,
                               cudaStream_t stream);
 
 // Chunkwise forward on tcgen05 tensor cores.  Returns cudaErrorNotSupported
-// (without launching) for shapes or dtypes it does not cover.
+// (without launching) for shapes or dtypes it does not cover.  With a
+// workspace of chunk_tc_workspace_bytes(BH, T) bytes (16-byte aligned) it runs
+// in two passes: every chunk's [PT; Tm] in parallel, then the sequences;
+// with workspace == nullptr one fused kernel does both.
 bool chunk_tc_supports(int dk, int dv, int dt);
+size_t chunk_tc_workspace_bytes(int BH, int T);
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v,
                             const void* beta, const float* S0, void* o,
                             float* S_T, int BH, int T, int dk, int dv, int dt,
-                            cudaStream_t stream);
+                            void* workspace, cudaStream_t stream);
 
 // Returns and clears the error word the tensor-core kernel sets when one of
 // its bounded waits runs out (0 = none, ~0u = could not read it).  Synchronous.

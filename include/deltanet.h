@@ -89,12 +89,19 @@ typedef enum {
  *   B, H, T >= 0 (T = 0 only copies S0, or zeros, to S_T)
  *   dk, dv  64 or 128;  C (chunk length) 64
  *   dt      DN_F32 or DN_BF16
- *   workspace, workspace_bytes: scratch of at least
- *           dn_chunk_fwd_workspace_bytes(...) bytes (NULL/0 when that is 0)
+ *   workspace, workspace_bytes: device scratch, 16-byte aligned, of at least
+ *           dn_chunk_fwd_workspace_bytes(...) bytes, not overlapping any other
+ *           argument; or NULL.  With it the tensor-core path runs in two
+ *           passes (every chunk's [PT; Tm] = [P T; T] with P = (Q K^T . M),
+ *           in parallel over all chunks, then the sequential scan); with NULL
+ *           one fused kernel does both (slower).  Other paths ignore it.  The
+ *           contents need no initialisation and are undefined afterwards.
  *   stream  cudaStream_t
  * A last chunk shorter than C is handled exactly (as if padded with beta = 0
  * and k = 0 tokens, whose outputs are dropped).
- * Errors: DN_ERR_INVALID_ARG, DN_ERR_UNSUPPORTED (other dk, dv, C), DN_ERR_CUDA.
+ * Errors: DN_ERR_INVALID_ARG (including a non-NULL workspace that is too
+ * small, misaligned, not device memory or overlapping), DN_ERR_UNSUPPORTED
+ * (other dk, dv, C), DN_ERR_CUDA.
  */
 DN_API int dn_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
                  const float *S0, void *o, float *S_T,
@@ -110,7 +117,9 @@ DN_API int dn_chunk_fwd_algo(const void *q, const void *k, const void *v,
                       int dt, void *workspace, size_t workspace_bytes,
                       void *stream, int algo);
 
-/* Scratch bytes dn_chunk_fwd needs for this problem (0 means none). */
+/* Scratch bytes the fastest dn_chunk_fwd path uses for this problem: one
+ * 16 KB bf16 [PT; T] tile (128 x 64) per (batch, head, chunk) on the
+ * tensor-core path (bf16, dk = dv = 128, C = 64), else 0.  Host-only. */
 DN_API size_t dn_chunk_fwd_workspace_bytes(int B, int H, int T, int dk, int dv,
                                     int C, int dt);
 

@@ -16,9 +16,15 @@ def dev(t):
 
 
 def run_chunk(inp, algo="auto", want_state=True):
-    """Runs the library on ChunkInputs; returns (o, S_T) as fp64 numpy."""
+    """Runs the library on ChunkInputs; returns (o, S_T) as fp64 numpy.
+    algo "tcgen05-fused" is the tensor-core path without a workspace (one
+    fused kernel); "tcgen05" and "auto" get the workspace (two passes)."""
+    ws = "auto"
+    if algo.endswith("-fused"):
+        algo, ws = algo[: -len("-fused")], None
     o, S = dn.chunk_fwd(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta),
-                        initial_state=dev(inp.S0), output_final_state=want_state, algo=algo)
+                        initial_state=dev(inp.S0), output_final_state=want_state, algo=algo,
+                        workspace=ws)
     torch.cuda.synchronize()
     o = o.double().cpu().numpy()
     return o, (S.double().cpu().numpy() if S is not None else None)

@@ -44,8 +44,19 @@ def test_abi_version_and_status_strings(lib):
     assert lib.dn_status_string(99) == b"DN_UNKNOWN_STATUS"
 
 
-def test_workspace_is_zero(lib):
-    assert lib.dn_chunk_fwd_workspace_bytes(8, 16, 2048, 128, 128, 64, 1) == 0
+def test_workspace_bytes(lib):
+    """The tensor-core path (bf16, dk = dv = 128, C = 64) asks for one 16 KB
+    [PT; Tm] tile per (batch, head, chunk); every other case needs none."""
+    f = lib.dn_chunk_fwd_workspace_bytes
+    assert f(8, 16, 2048, 128, 128, 64, 1) == 8 * 16 * 32 * 16384
+    assert f(1, 2, 130, 128, 128, 64, 1) == 2 * 3 * 16384
+    assert f(1, 1, 1, 128, 128, 64, 1) == 16384
+    assert f(1, 1, 0, 128, 128, 64, 1) == 0
+    assert f(0, 4, 64, 128, 128, 64, 1) == 0
+    assert f(8, 16, 2048, 128, 128, 64, 0) == 0  # fp32 I/O
+    assert f(8, 16, 2048, 64, 64, 64, 1) == 0    # d = 64
+    assert f(8, 16, 2048, 128, 64, 64, 1) == 0
+    assert f(8, 16, 2048, 128, 128, 32, 1) == 0  # other chunk length
 
 
 def _chunk(lib, B=1, H=1, T=64, dk=64, dv=64, C=64, dt=1, algo=0):

@@ -16,7 +16,7 @@ from tests.gpu_util import TOL, dev, run_chunk, sample_heads, take_heads
 
 pytestmark = pytest.mark.gpu
 
-ALGOS_BF16 = ["simt", "tcgen05"]
+ALGOS_BF16 = ["simt", "tcgen05", "tcgen05-fused"]
 
 
 @pytest.fixture(autouse=True)
@@ -96,14 +96,57 @@ def test_shapes_and_ragged_tails(dtype, dk, dv, T):
 
 @pytest.mark.parametrize("T", [1, 37, 64, 65, 200, 1000])
 @pytest.mark.parametrize("with_s0", [False, True])
-def test_tensor_core_path_ragged(T, with_s0):
-    """The tcgen05 kernel on sequences shorter than, equal to and not a
-    multiple of the chunk, with and without a carried state."""
+@pytest.mark.parametrize("algo", ["tcgen05", "tcgen05-fused"])
+def test_tensor_core_path_ragged(T, with_s0, algo):
+    """The tcgen05 kernels (two-pass and fused) on sequences shorter than,
+    equal to and not a multiple of the chunk, with and without a carried
+    state."""
     inp = workloads.chunk_inputs(3, 2, T, 128, 128, dtype="bf16", seed=100 + T,
                                  feature_map="silu", s0_std=0.1 if with_s0 else None)
-    o, S = run_chunk(inp, "tcgen05")
+    o, S = run_chunk(inp, algo)
     o_ref, S_ref = oracle.forward(inp.q, inp.k, inp.v, inp.beta, inp.S0)
-    _check(o, S, o_ref, S_ref, torch.bfloat16, f"tcgen05 T{T}")
+    _check(o, S, o_ref, S_ref, torch.bfloat16, f"{algo} T{T}")
+
+
+def test_split_and_fused_agree():
+    """The two tensor-core forms differ only in how the triangular inverse is
+    rounded (tf32 block merges in the prepare kernel, fp32 in the fused one)
+    before both round it to bf16, so they agree with each other to the bf16
+    bar and each meets it against the oracle."""
+    inp = workloads.chunk_inputs(2, 4, 700, 128, 128, dtype="bf16", seed=404,
+                                 feature_map="silu", s0_std=0.1)
+    o1, S1 = run_chunk(inp, "tcgen05")
+    o2, S2 = run_chunk(inp, "tcgen05-fused")
+    o_ref, S_ref = oracle.forward(inp.q, inp.k, inp.v, inp.beta, inp.S0)
+    _check(o1, S1, o_ref, S_ref, torch.bfloat16, "split")
+    _check(o2, S2, o_ref, S_ref, torch.bfloat16, "fused")
+    assert rel_l2(o1, o2) <= TOL[torch.bfloat16] and rel_l2(S1, S2) <= TOL[torch.bfloat16]
+
+
+def test_workspace_checks():
+    """A short, misaligned or overlapping workspace is refused before any
+    launch; NULL selects the fused kernel."""
+    from delta_rule_recurrent_gb300 import _lib
+    import delta_rule_recurrent_gb300 as dn
+    inp = workloads.chunk_inputs(1, 2, 130, 128, 128, dtype="bf16", seed=9, feature_map="silu")
+    q, k, v, b = (dev(x) for x in (inp.q, inp.k, inp.v, inp.beta))
+    lib = _lib.load()
+    need = lib.dn_chunk_fwd_workspace_bytes(1, 2, 130, 128, 128, 64, 1)
+    assert need == 2 * 3 * 16384
+    short = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(_lib.DeltaNetError, match="INVALID_ARG"):
+        dn.chunk_fwd(q, k, v, b, workspace=short)
+    big = torch.empty(need + 64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(_lib.DeltaNetError, match="INVALID_ARG"):
+        dn.chunk_fwd(q, k, v, b, workspace=big[8:])
+    buf = torch.empty(need // 2 + 2 * 130 * 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(_lib.DeltaNetError, match="INVALID_ARG"):  # workspace covers o
+        dn.chunk_fwd(q, k, v, b, out=buf[: 2 * 130 * 128].view(1, 2, 130, 128),
+                     workspace=buf.view(torch.uint8))
+    o, S = dn.chunk_fwd(q, k, v, b, workspace=None)
+    o_ref, S_ref = oracle.forward(inp.q, inp.k, inp.v, inp.beta, inp.S0)
+    torch.cuda.synchronize()
+    _check(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref, torch.bfloat16)
 
 
 def test_tensor_core_rejects_other_shapes():

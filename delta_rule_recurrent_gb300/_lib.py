@@ -27,6 +27,8 @@ SIGNATURES = {
     "dn_chunk_fwd_algo": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _fp, _int, _int, _int, _int,
                                  _int, _int, _int, _vp, _size, _vp, _int]),
     "dn_chunk_fwd_workspace_bytes": (_size, [_int] * 7),
+    "dn_chunk_fwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _fp, _int, _int, _int, _int,
+                                    _int, _int, _int, _vp]),
     "dn_recurrent_step": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _int, _int, _int, _int, _int,
                                  _vp]),
     "dn_status_string": (ctypes.c_char_p, [_int]),

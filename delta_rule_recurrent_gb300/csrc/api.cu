@@ -189,6 +189,63 @@ int dn_chunk_fwd(const void* q, const void* k, const void* v, const void* beta, 
                              workspace_bytes, stream, DN_ALGO_AUTO);
 }
 
+int dn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const void* beta,
+                         const float* S0, void* o, float* S_T, int B, int H, int T, int dk,
+                         int dv, int C, int dt, void* stream) {
+    if (B < 0 || H < 0 || T < 0)
+        return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d T=%d)", B, H, T);
+    if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
+    if (C != 64 || !dn::chunk_tc_supports(dk, dv, dt))
+        return fail(DN_ERR_UNSUPPORTED,
+                    "the no-alloc entry point covers bf16, dk = dv = 128, C = 64 (got dk=%d dv=%d "
+                    "C=%d dtype=%d)", dk, dv, C, dt);
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
+    const long long tiles = BH * (((long long)T + 63) / 64);
+    if (tiles > (long long)dn::noalloc_max_tiles())
+        return fail(DN_ERR_INVALID_ARG,
+                    "B*H*ceil(T/64) = %lld chunk tiles; the no-alloc entry point holds %zu",
+                    tiles, dn::noalloc_max_tiles());
+    if (BH == 0) return ok();
+
+    const size_t es = elem_size(dt);
+    const size_t ntok = (size_t)BH * (size_t)T;
+    const size_t state_bytes = (size_t)BH * dk * dv * sizeof(float);
+    const Span sq{"q", q, ntok * dk * es}, sk{"k", k, ntok * dk * es}, sv{"v", v, ntok * dv * es},
+        sb{"beta", beta, ntok * es}, so{"o", o, ntok * dv * es}, s0{"S0", S0, state_bytes},
+        sT{"S_T", S_T, state_bytes};
+    int dev = 0;
+    if (int st = current_device(&dev)) return st;
+    if (T > 0) {
+        for (const Span* s : {&sq, &sk, &sv, &so})
+            if (int st = check_device_ptr(*s, 16, dev)) return st;
+        if (int st = check_device_ptr(sb, es, dev)) return st;
+    }
+    if (S0)
+        if (int st = check_device_ptr(s0, 16, dev)) return st;
+    if (S_T)
+        if (int st = check_device_ptr(sT, 16, dev)) return st;
+    if (T > 0)
+        for (const Span* s : {&sq, &sk, &sv, &sb, &s0, &sT})
+            if (overlaps(so, *s)) return fail(DN_ERR_INVALID_ARG, "o overlaps %s", s->name);
+    for (const Span* s : {&sq, &sk, &sv, &sb})
+        if (T > 0 && overlaps(sT, *s)) return fail(DN_ERR_INVALID_ARG, "S_T overlaps %s", s->name);
+    if (S_T && S0 && S_T != S0 && overlaps(sT, s0))
+        return fail(DN_ERR_INVALID_ARG, "S_T partly overlaps S0");
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        if (!S_T || S_T == S0) return ok();
+        if (S0)
+            return cuda_status(cudaMemcpyAsync(S_T, S0, state_bytes, cudaMemcpyDeviceToDevice, st),
+                               "cudaMemcpyAsync(S_T <- S0)");
+        return cuda_status(cudaMemsetAsync(S_T, 0, state_bytes, st), "cudaMemsetAsync(S_T)");
+    }
+    return cuda_status(
+        dn::launch_chunk_tc_noalloc(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, st),
+        "chunk forward (tcgen05, static scratch) launch");
+}
+
 int dn_recurrent_step(const void* q, const void* k, const void* v, const void* beta, float* S,
                       void* o, int B, int H, int dk, int dv, int dt, void* stream) {
     if (B < 0 || H < 0) return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d)", B, H);

@@ -1450,6 +1450,37 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
     return cudaGetLastError();
 }
 
+// Scratch of dn_chunk_fwd_noalloc: a fixed number of [PT; Tm] tiles, shared
+// by every call on a device.
+constexpr size_t kNoAllocTiles = 512;
+static __device__ __align__(256) uint8_t g_noalloc_ws[kNoAllocTiles * kTile];
+
+size_t noalloc_max_tiles() { return kNoAllocTiles; }
+
+cudaError_t launch_chunk_tc_noalloc(const void* q, const void* k, const void* v,
+                                    const void* beta, const float* S0, void* o, float* S_T,
+                                    int BH, int T, int dk, int dv, int dt, cudaStream_t stream) {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!addr[dev]) {  // first call on this device: look the array up once
+            void* p = nullptr;
+            if ((e = cudaGetSymbolAddress(&p, g_noalloc_ws)) != cudaSuccess) return e;
+            addr[dev] = p;
+        }
+        ws = addr[dev];
+    }
+    if (chunk_tc_workspace_bytes(BH, T) > kNoAllocTiles * kTile) return cudaErrorInvalidValue;
+    return launch_chunk_tc(q, k, v, beta, S0, o, S_T, BH, T, dk, dv, dt, ws, stream);
+}
+
 unsigned int chunk_tc_take_device_error() {
     unsigned int h = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&h, g_chunk_tc_error, sizeof(h)) != cudaSuccess) return ~0u;

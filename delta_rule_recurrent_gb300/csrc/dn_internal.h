@@ -32,6 +32,16 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v,
                             float* S_T, int BH, int T, int dk, int dv, int dt,
                             void* workspace, cudaStream_t stream);
 
+// As launch_chunk_tc with the workspace in a static device array of
+// noalloc_max_tiles tiles (the caller has checked the size).  The array's
+// address is looked up once per device, on the first call with that device
+// current; no memory is allocated.
+size_t noalloc_max_tiles();
+cudaError_t launch_chunk_tc_noalloc(const void* q, const void* k, const void* v,
+                                    const void* beta, const float* S0, void* o,
+                                    float* S_T, int BH, int T, int dk, int dv,
+                                    int dt, cudaStream_t stream);
+
 // Returns and clears the error word the tensor-core kernel sets when one of
 // its bounded waits runs out (0 = none, ~0u = could not read it).  Synchronous.
 unsigned int chunk_tc_take_device_error();

@@ -162,6 +162,33 @@ DN_API const char *dn_status_string(int status);
  * pointer stays valid until the next call into the library on this thread. */
 DN_API const char *dn_last_error(void);
 
+/*
+ * dn_chunk_fwd_noalloc -- dn_chunk_fwd on the two-pass tensor-core path,
+ * using no memory the caller provides and allocating none.  The paper has no
+ * counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc.  The per-chunk [PT; T] tiles go to a static device array inside
+ * the library that holds DN_NOALLOC_MAX_TILES tiles of 16 KB (8 MiB).
+ *
+ *   - Covers bf16 with dk = dv = 128 and C = 64 only; other shapes and dtypes
+ *     return DN_ERR_UNSUPPORTED.
+ *   - Needs B * H * ceil(T / 64) <= DN_NOALLOC_MAX_TILES; larger problems
+ *     return DN_ERR_INVALID_ARG before anything is launched.
+ *   - Nothing in the array has to start at zero: within a call every tile is
+ *     written before it is read.
+ *   - Every call on a device shares the array, so calls whose kernels overlap
+ *     on the GPU (on different streams, say) race; serialise them.
+ *   - The first call on each device looks the array's address up
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ * Arguments, layouts and the remaining errors are those of dn_chunk_fwd.
+ */
+#define DN_NOALLOC_MAX_TILES 512
+DN_API int dn_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
+                         const void *beta, const float *S0, void *o, float *S_T,
+                         int B, int H, int T, int dk, int dv, int C, int dt,
+                         void *stream);
+
 /* ABI version of this header (bumped on incompatible changes). */
 DN_API int dn_abi_version(void);
 

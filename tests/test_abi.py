@@ -120,3 +120,23 @@ def test_last_error_is_per_thread(lib):
     th.join()
     assert seen["msg"] == b""
     assert lib.dn_last_error() != b""
+
+
+def test_noalloc_entry_point_rejects_before_any_cuda_call(lib):
+    """dn_chunk_fwd_noalloc refuses shapes it does not cover and problems
+    larger than its static scratch (DN_NOALLOC_MAX_TILES chunk tiles) from
+    the sizes alone, before touching a pointer or the device."""
+    f = lib.dn_chunk_fwd_noalloc
+    null = [None] * 7
+
+    def call(B, H, T, dk=128, dv=128, C=64, dt=1):
+        return f(*null, B, H, T, dk, dv, C, dt, None)
+
+    assert call(1, 8, 64 * 65) == _lib.DN_ERR_INVALID_ARG  # 520 tiles > 512
+    assert b"512" in lib.dn_last_error()
+    assert call(1, 8, 64 * 64 + 1) == _lib.DN_ERR_INVALID_ARG  # a ragged tail counts as a tile
+    assert call(1, 1, 64, dt=0) == _lib.DN_ERR_UNSUPPORTED
+    assert call(1, 1, 64, dk=64, dv=64) == _lib.DN_ERR_UNSUPPORTED
+    assert call(1, 1, 64, C=32) == _lib.DN_ERR_UNSUPPORTED
+    assert call(-1, 1, 64) == _lib.DN_ERR_INVALID_ARG
+    assert call(0, 4, 64) == _lib.DN_OK  # nothing to do, nothing touched

@@ -74,8 +74,8 @@ constexpr uint32_t kYBytes = 32 * kYP * 4;           // fp32 32 x kYP solve scra
 constexpr int kNumBars = 34;
 // Shared memory of the sequence kernel.  The fused form (kSplit false) also
 // holds the chunk groups' solve arrays; the split form, whose [PT; Tm] tiles
-// come from the prepare kernel, spends that space on a second v buffer and a
-// constant operand tile.
+// come from the prepare kernel, spends that space on a second v buffer and an
+// o tile of its own.
 template <bool kSplit>
 struct Layout {
     static constexpr int kStages = 3;                          // [K; Q] ring depth
@@ -84,8 +84,8 @@ struct Layout {
     static constexpr uint32_t OFF_V = OFF_KQ + kStages * kStageKQ;  // v: 2 dv halves x 64 rows each
     static constexpr uint32_t OFF_TP = OFF_V + kVBufs * kTile; // 2 x [PT; Tm] (one per chunk group)
     static constexpr uint32_t OFF_SB = OFF_TP + 2 * kTile;     // S as bf16 (2 x 128 rows); then U', o tile
-    static constexpr uint32_t OFF_I = OFF_SB + 2 * kTile;      // split: constant [-I; 0] operand
-    static constexpr uint32_t OFF_X = OFF_I + (kSplit ? kTile : 0);  // fused: 2 x A, overwritten by X
+    static constexpr uint32_t OFF_O = OFF_SB + 2 * kTile;      // split: o tile of its own
+    static constexpr uint32_t OFF_X = OFF_O + (kSplit ? kTile : 0);  // fused: 2 x A, overwritten by X
     static constexpr uint32_t OFF_Y = OFF_X + (kSplit ? 0 : 2 * kXBytes);     // fused: 2 x scratch
     static constexpr uint32_t OFF_BETA = OFF_Y + (kSplit ? 0 : 2 * kYBytes);  // fused: 2 x 64 fp32
     static constexpr uint32_t OFF_BAR = OFF_BETA + (kSplit ? 0 : 512);        // mbarriers
@@ -112,8 +112,8 @@ enum : int {
     B_DW_FULL = 18,    // [2] DW = [PT;Tm] K done              (own commit)
     B_QW_READY = 20,   // [2] [PT; Tm] and [Q'; -W] ready      (chunk group -> state group)
     B_FREE = 22,       // [2] D1 MMAs read them; both free     (state MMA -> group or producer)
-    B_D1_FULL = 24,    // [2] D1 done (per state half)         (own commit, state group)
-    B_S_READY = 26,    // [2] S += K^T U' done (per state half) (own commit, state group)
+    B_D1_FULL = 24,    // D1 done                              (own commit, state group)
+    B_S_READY = 26,    // S += K^T U' done                     (own commit, state group)
     B_DRAIN = 28,      // [4] final drain of each MMA issuer
     B_TP_FULL = 32,    // [2] split form: [PT; Tm] tile landed (producer -> chunk group)
 };
@@ -132,7 +132,6 @@ constexpr uint32_t IDESC_G = idesc_bf16_f32(128, 64, 0, 0);    // [K;Q] K^T
 constexpr uint32_t IDESC_N64 = idesc_bf16_f32(128, 64, 0, 1);  // A K-major, B MN-major, N = 64
 constexpr uint32_t IDESC_KB = idesc_bf16_f32(128, 128, 0, 1);  // A K-major (smem or TMEM), B MN-major
 constexpr uint32_t IDESC_MM = idesc_bf16_f32(128, 128, 1, 1);  // both MN-major
-constexpr uint32_t IDESC_MM64 = idesc_bf16_f32(128, 64, 1, 1);  // both MN-major, N = 64
 
 enum : unsigned { kErrTimeout = 1 };
 
@@ -262,7 +261,8 @@ struct Smem {
     __device__ uint32_t tp(int g) const { return base + L::OFF_TP + (uint32_t)g * kTile; }
     __device__ uint32_t v(int c) const { return base + L::OFF_V + (uint32_t)(c % L::kVBufs) * kTile; }
     __device__ uint32_t sb() const { return base + L::OFF_SB; }
-    __device__ uint32_t itile() const { return base + L::OFF_I; }
+    // o tile: its own buffer in the split form, the spent S operand's upper half otherwise
+    __device__ uint32_t otile() const { return base + (kSplit ? L::OFF_O : L::OFF_SB + 16384u); }
     __device__ float* x(int g) const {
         return reinterpret_cast<float*>(gbase + L::OFF_X + (uint32_t)g * kXBytes);
     }
@@ -568,6 +568,14 @@ __device__ __forceinline__ void drain_mmas(const Ctl& ctl, int b) {
     mbar_wait(ctl.bar(b), 0, kTimeoutNs);
 }
 
+// D1 = [PT; Tm] V (overwrites D1), issued by one thread.
+__device__ __forceinline__ void issue_vpart(uint32_t tmem, uint32_t tp, uint32_t v) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        mma_bf16_ss(tmem + COL_D1, sw128_desc(tp + 32u * kk, 16, 1024),
+                    sw128_desc(v + 2048u * kk, 8192, 1024), IDESC_KB, kk > 0);
+}
+
 // State role: thread ts owns state row t = ts % 128 (TMEM lane t).  In the
 // fused form one warpgroup (warps 4-7) converts all 128 columns; in the split
 // form a second warpgroup (warps 0-3, ts >= 128) takes the dv 64-127 half of
@@ -607,30 +615,21 @@ __device__ void state_role_body(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t
     }
     tmem_wait_st();
 
+    bool vnext = false;  // (thread 0) the [PT; Tm] V part of chunk c is already issued
     for (int c = 0; c < nchunks; ++c) {
         const int g = c & 1;
         const uint32_t tp = sm.tp(g), qw = tmem + COL_GRP + 128u * (uint32_t)g;
-        // S += K^T U' of the previous chunk done, and its o tile read out by TMA.
+        // S += K^T U' of the previous chunk done (and, where the o tile shares
+        // the S operand's buffer, that tile read out by TMA).
         if (c > 0) {
             bool ok0 = true;
             if (ts == 0) {
                 ok0 = ctl.wait(B_S_READY, (uint32_t)(c - 1));
-                bulk_wait_group_read0();
+                if (!kSplit) bulk_wait_group_read0();
             }
             if (wg_sync_or(kBar, !ok0, kN)) return;
         }
         tc_fence_after_sync();
-        // D1 = [PT; Tm] V needs no S: issue it now if the chunk is already
-        // handed over, so it runs while S is converted.
-        bool vpart = false;
-        if (ts == 0 && mbar_test_wait(ctl.bar(B_QW_READY + g), (uint32_t)(c >> 1) & 1u) &&
-            mbar_test_wait(ctl.bar(B_V_FULL + c % kVB), (uint32_t)(c / kVB) & 1u)) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + COL_D1, sw128_desc(tp + 32u * kk, 16, 1024),
-                            sw128_desc(sm.v(c) + 2048u * kk, 8192, 1024), IDESC_KB, kk > 0);
-            vpart = true;
-        }
         // S (fp32) -> bf16 operand tile: dv halves as regions, row t.
 #pragma unroll
         for (int hh = 0; hh < kHalves; ++hh) {
@@ -649,11 +648,7 @@ __device__ void state_role_body(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t
                  ctl.wait(B_V_FULL + c % kVB, (uint32_t)(c / kVB));
             if (ok) {
                 tc_fence_after_sync();
-                if (!vpart)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ss(tmem + COL_D1, sw128_desc(tp + 32u * kk, 16, 1024),
-                                    sw128_desc(sm.v(c) + 2048u * kk, 8192, 1024), IDESC_KB, kk > 0);
+                if (!vnext) issue_vpart(tmem, tp, sm.v(c));
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16_ts(tmem + COL_D1, qw + 8u * kk,
@@ -662,14 +657,16 @@ __device__ void state_role_body(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t
                 mma_commit(ctl.bar(B_V_EMPTY + c % kVB));
                 mma_commit(ctl.bar(B_FREE + g));
                 ok = ctl.wait(B_D1_FULL, (uint32_t)c);
+                // a separate o tile may still be read by the previous chunk's store
+                if (kSplit) bulk_wait_group_read0();
             }
         }
         if (wg_sync_or(kBar, !ok, kN)) return;
         tc_fence_after_sync();
-        // The S operand is spent: rows 0-63 (o) into its upper 16 KB as the o
-        // tile, rows 64-127 (U') into its lower 16 KB.
+        // The S operand is spent: rows 64-127 (U') into its lower 16 KB, rows
+        // 0-63 (o) into the o tile.
         {
-            const uint32_t dst = sm.sb() + (t < 64 ? 16384u : 0u);
+            const uint32_t dst = t < 64 ? sm.otile() : sm.sb();
 #pragma unroll
             for (int hh = 0; hh < kHalves; ++hh) {
                 const int h = h0 + hh;
@@ -692,9 +689,17 @@ __device__ void state_role_body(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t
             mma_commit(ctl.bar(B_S_READY));
             mma_commit(ctl.bar(B_KQ_EMPTY + c % Layout<kSplit>::kStages));
             // o tile out (rows past the end of the sequence are clipped)
-            tma_store_3d(tm_o, sm.sb() + 16384u, 0, c * kC, bh);
-            tma_store_3d(tm_o, sm.sb() + 24576u, 64, c * kC, bh);
+            tma_store_3d(tm_o, sm.otile(), 0, c * kC, bh);
+            tma_store_3d(tm_o, sm.otile() + 8192u, 64, c * kC, bh);
             bulk_commit_group();
+            // D1 is read out: its [PT; Tm] V part for the next chunk needs no S,
+            // so start it now if that chunk is handed over; it then runs while
+            // S is converted.
+            const int cn = c + 1;
+            vnext = cn < nchunks &&
+                    mbar_test_wait(ctl.bar(B_QW_READY + (cn & 1)), (uint32_t)(cn >> 1) & 1u) &&
+                    mbar_test_wait(ctl.bar(B_V_FULL + cn % kVB), (uint32_t)(cn / kVB) & 1u);
+            if (vnext) issue_vpart(tmem, sm.tp(cn & 1), sm.v(cn));
         }
     }
     if (nchunks > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(nchunks - 1), ts, kBar, kN)) return;
@@ -720,143 +725,6 @@ __device__ void state_role(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t tmem
     state_role_body<kSplit>(ctl, sm, tmem, ts, S0, S_T, tm_o, bh, nchunks);
     if (ts == 0) {
         drain_mmas(ctl, B_DRAIN + 0);
-        bulk_wait_group0();  // o tiles written
-    }
-}
-
-// Split form state: the recurrence acts on every dv column of S on its own,
-// so the state runs as two independent chains, one per dv half.  Half h
-// (0: warps 4-7, 1: warps 0-3) owns S[:, 64h .. 64h + 63] and the same D1
-// columns; its 16 KB region of the S operand buffer holds S[:, half] as bf16,
-// then U' (rows 0-63 of the region) and the o half tile (rows 64-127).
-// Thread t owns TMEM lane t; t == 0 issues the half's MMAs.
-__device__ void state_half_body(const Ctl& ctl, const Smem<true>& sm, uint32_t tmem, int t, int h,
-                                const float* __restrict__ S0, float* __restrict__ S_T,
-                                const CUtensorMap* tm_o, int bh, int nchunks) {
-    constexpr int kVB = Layout<true>::kVBufs, kS = Layout<true>::kStages;
-    const int barid = h == 0 ? 1 : 3;
-    const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
-    const uint32_t colS = COL_S + 64u * (uint32_t)h, colD = COL_D1 + 64u * (uint32_t)h;
-    const uint32_t sbh = sm.sb() + 16384u * (uint32_t)h;
-#pragma unroll
-    for (int part = 0; part < 2; ++part) {  // S0[:, half] (or zeros) into TMEM
-        uint32_t r[32];
-        if (S0) {
-            const float4* src = reinterpret_cast<const float4*>(
-                S0 + ((size_t)bh * kD + t) * kD + 64 * h + 32 * part);
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4) {
-                const float4 f = src[v4];
-                r[4 * v4 + 0] = __float_as_uint(f.x);
-                r[4 * v4 + 1] = __float_as_uint(f.y);
-                r[4 * v4 + 2] = __float_as_uint(f.z);
-                r[4 * v4 + 3] = __float_as_uint(f.w);
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = 0u;
-        }
-        tmem_st32(tmem + lane_base + colS + 32u * part, r);
-    }
-    tmem_wait_st();
-
-    for (int c = 0; c < nchunks; ++c) {
-        const int g = c & 1;
-        const uint32_t tp = sm.tp(g), qw = tmem + COL_GRP + 128u * (uint32_t)g;
-        const uint32_t vh = sm.v(c) + 8192u * (uint32_t)h;
-        // This half's S += K^T U' of the previous chunk done, its o tile read out.
-        if (c > 0) {
-            bool ok0 = true;
-            if (t == 0) {
-                ok0 = ctl.wait(B_S_READY + h, (uint32_t)(c - 1));
-                bulk_wait_group_read0();
-            }
-            if (wg_sync_or(barid, !ok0)) return;
-        }
-        tc_fence_after_sync();
-        // D1[:, half] = [PT; Tm] V[:, half] needs no S: issue it now if the chunk
-        // is already handed over, so it runs while S is converted.
-        bool vpart = false;
-        if (t == 0 && mbar_test_wait(ctl.bar(B_QW_READY + g), (uint32_t)(c >> 1) & 1u) &&
-            mbar_test_wait(ctl.bar(B_V_FULL + c % kVB), (uint32_t)(c / kVB) & 1u)) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + colD, sw128_desc(tp + 32u * kk, 16, 1024),
-                            sw128_desc(vh + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
-            vpart = true;
-        }
-        {   // S[:, half] (fp32) -> bf16 operand, row t
-            float x[64];
-            tmem_ld64f(tmem + lane_base + colS, x);
-            store_row64_bf16(sbh, t, x);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        wg_sync(barid);
-        bool ok = true;
-        if (t == 0) {
-            ok = ctl.wait(B_QW_READY + g, (uint32_t)(c >> 1)) &&
-                 ctl.wait(B_V_FULL + c % kVB, (uint32_t)(c / kVB));
-            if (ok) {
-                tc_fence_after_sync();
-                if (!vpart)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ss(tmem + colD, sw128_desc(tp + 32u * kk, 16, 1024),
-                                    sw128_desc(vh + 2048u * kk, 8192, 1024), IDESC_N64, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // D1[:, half] += [Q'; -W] S[:, half]
-                    mma_bf16_ts(tmem + colD, qw + 8u * kk, sw128_desc(sbh + 2048u * kk, 8192, 1024),
-                                IDESC_N64, 1);
-                mma_commit(ctl.bar(B_D1_FULL + h));
-                mma_commit(ctl.bar(B_V_EMPTY + c % kVB));
-                mma_commit(ctl.bar(B_FREE + g));
-                ok = ctl.wait(B_D1_FULL + h, (uint32_t)c);
-            }
-        }
-        if (wg_sync_or(barid, !ok)) return;
-        tc_fence_after_sync();
-        {   // rows 0-63 (o) -> the o half tile, rows 64-127 (U') -> the U' half
-            float x[64];
-            tmem_ld64f(tmem + lane_base + colD, x);
-            store_row64_bf16(sbh + (t < 64 ? 8192u : 0u), t & 63, x);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        wg_sync(barid);
-        if (t == 0) {
-            // S[:, half] += K^T U'[:, half]
-            const uint32_t kq = sm.kq(c);
-            tc_fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + colS, sw128_desc(kq + 2048u * kk, kRegKQ, 1024),
-                            sw128_desc(sbh + 2048u * kk, 8192, 1024), IDESC_MM64, 1);
-            mma_commit(ctl.bar(B_S_READY + h));
-            mma_commit(ctl.bar(B_KQ_EMPTY + c % kS));
-            // o half tile out (rows past the end of the sequence are clipped)
-            tma_store_3d(tm_o, sbh + 8192u, 64 * h, c * kC, bh);
-            bulk_commit_group();
-        }
-    }
-    if (nchunks > 0 && !wg_wait(ctl, B_S_READY + h, (uint32_t)(nchunks - 1), t, barid)) return;
-    tc_fence_after_sync();
-    if (S_T) {
-        float x[64];
-        tmem_ld64f(tmem + lane_base + colS, x);
-        float4* dst = reinterpret_cast<float4*>(S_T + ((size_t)bh * kD + t) * kD + 64 * h);
-#pragma unroll
-        for (int v4 = 0; v4 < 16; ++v4)
-            dst[v4] = make_float4(x[4 * v4], x[4 * v4 + 1], x[4 * v4 + 2], x[4 * v4 + 3]);
-    }
-}
-
-__device__ void state_half_role(const Ctl& ctl, const Smem<true>& sm, uint32_t tmem, int t, int h,
-                                const float* __restrict__ S0, float* __restrict__ S_T,
-                                const CUtensorMap* tm_o, int bh, int nchunks) {
-    state_half_body(ctl, sm, tmem, t, h, S0, S_T, tm_o, bh, nchunks);
-    if (t == 0) {
-        drain_mmas(ctl, B_DRAIN + h);
         bulk_wait_group0();  // o tiles written
     }
 }
@@ -1043,44 +911,64 @@ __device__ void chunk_role_body(const Ctl& ctl, const Smem<false>& sm, uint32_t 
 
 // Split form: [PT; Tm] arrives from the workspace, so one chunk group
 // (warps 8-11) forms the [Q'; -W] operand of every chunk, alternating between
-// the two buffer sets by chunk parity.  One MMA over the whole [K; Q] tile
-//     DW' = [PT  -I; Tm  0] [K; Q] = [PT K - Q; W] = -[Q'; -W]
-// (the right half of the A operand is a constant tile) leaves only a negate
-// and pack for the epilogue.
+// the two buffer sets by chunk parity.  The group writes [-Q; 0] into the
+// set's 128 accumulator columns and adds [PT; Tm] K on the tensor cores:
+//     DW' = [-Q; 0] + [PT; Tm] K = [PT K - Q; W] = -[Q'; -W],
+// which the epilogue negates and packs.
 __device__ void chunk_role_split_body(const Ctl& ctl, const Smem<true>& sm, uint32_t tmem, int t,
                                       int nchunks) {
     constexpr int kF = kKQBars<true>;
-    const int barid = 2;
+    const int barid = 2, row = t & 63;
     const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
-    {   // constant [-I; 0] (128 x 64 bf16), row t
-        float x[64];
-#pragma unroll
-        for (int j = 0; j < 64; ++j) x[j] = (j == t) ? -1.f : 0.f;
-        store_row64_bf16(sm.itile(), t, x);
-        fence_proxy_async_smem();
-        wg_sync(barid);
-    }
     for (int c = 0; c < nchunks; ++c) {
         const int g = c & 1, it = c >> 1;
         const uint32_t kq = sm.kq(c), colQW = COL_GRP + 128u * (uint32_t)g;
         bool ok = true;
         if (t == 0) {
-            // The [PT; Tm] tile is loaded only after both state halves released
+            // The [PT; Tm] tile is loaded only after the state group released
             // this buffer set, so its [Q'; -W] columns are free as well.
             ok = ctl.wait(B_KQ_FULL + c % kF, (uint32_t)(c / kF)) &&
                  ctl.wait(B_TP_FULL + g, (uint32_t)it);
-            if (ok) {
-                tc_fence_after_sync();
-                const uint32_t tp = sm.tp(g);
+        }
+        if (wg_sync_or(barid, !ok)) return;
+        tc_fence_after_sync();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t a = kk < 4 ? tp + 32u * kk : sm.itile() + 32u * (kk - 4);
-                    mma_bf16_ss(tmem + colQW, sw128_desc(a, 16, 1024),
-                                sw128_desc(kq + 2048u * kk, kRegKQ, 1024), IDESC_KB, kk > 0);
+        for (int qd = 0; qd < 4; ++qd) {  // -Q (rows 0-63) or 0 (rows 64-127), dk quarter qd
+            uint32_t r[32];
+            if (t < 64) {
+                const uint32_t region = kq + (uint32_t)(qd >> 1) * kRegKQ;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const uint4 qv = ld_shared_v4(region + sw128(64 + row, (qd & 1) * 4 + cc));
+                    const float2 a0 = unpack_bf16(qv.x), a1 = unpack_bf16(qv.y),
+                                 a2 = unpack_bf16(qv.z), a3 = unpack_bf16(qv.w);
+                    r[8 * cc + 0] = __float_as_uint(-a0.x);
+                    r[8 * cc + 1] = __float_as_uint(-a0.y);
+                    r[8 * cc + 2] = __float_as_uint(-a1.x);
+                    r[8 * cc + 3] = __float_as_uint(-a1.y);
+                    r[8 * cc + 4] = __float_as_uint(-a2.x);
+                    r[8 * cc + 5] = __float_as_uint(-a2.y);
+                    r[8 * cc + 6] = __float_as_uint(-a3.x);
+                    r[8 * cc + 7] = __float_as_uint(-a3.y);
                 }
-                mma_commit(ctl.bar(B_DW_FULL));
-                ok = ctl.wait(B_DW_FULL, (uint32_t)c);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = 0u;
             }
+            tmem_st32(tmem + lane_base + colQW + 32u * (uint32_t)qd, r);
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        wg_sync(barid);
+        if (t == 0) {
+            tc_fence_after_sync();
+            const uint32_t tp = sm.tp(g);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + colQW, sw128_desc(tp + 32u * kk, 16, 1024),
+                            sw128_desc(kq + 2048u * kk, kRegKQ, 1024), IDESC_KB, 1);
+            mma_commit(ctl.bar(B_DW_FULL));
+            ok = ctl.wait(B_DW_FULL, (uint32_t)c);
         }
         if (wg_sync_or(barid, !ok)) return;
         tc_fence_after_sync();
@@ -1118,8 +1006,8 @@ __device__ void chunk_role(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t tmem
 
 // Sequence kernel: one CTA per (batch, head), the whole sequence in order,
 // 16 warps.  Fused form: producer 0, TMEM owner 1, state 4-7, chunk groups
-// 8-11 and 12-15.  Split form: state halves 4-7 (dv 0-63) and 0-3
-// (dv 64-127), chunk group 8-11, producer 12, TMEM owner 13.
+// 8-11 and 12-15.  Split form: state 4-7 and 0-3 (which share its
+// conversions by dv halves), chunk group 8-11, producer 12, TMEM owner 13.
 template <bool kSplit>
 constexpr int kSeqThreads = 512;
 template <bool kSplit>
@@ -1143,14 +1031,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     if (tid == 0) {
         misc[0] = 0;
-        // In the split form both state halves release [K; Q] stages, v buffers
-        // and [PT; Tm] / [Q'; -W] sets, so those barriers take two arrivals.
-        for (int b = 0; b < kNumBars; ++b) {
-            const bool two = kSplit && ((b >= B_KQ_EMPTY && b < B_KQ_EMPTY + 4) ||
-                                        (b >= B_V_EMPTY && b < B_V_EMPTY + 2) ||
-                                        (b >= B_FREE && b < B_FREE + 2));
-            mbar_init(ctl.bar(b), two ? 2 : 1);
-        }
+        for (int b = 0; b < kNumBars; ++b) mbar_init(ctl.bar(b), 1);
         fence_mbar_init();
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
@@ -1171,10 +1052,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (warp == kProdWarp) {
         if (lane == 0) producer_role<kSplit>(ctl, sm, &tm_q, &tm_k, &tm_v, &tm_ws, bh, nchunks);
     } else if (warp < 8 && (kSplit || warp >= 4)) {
-        if constexpr (kSplit)
-            state_half_role(ctl, sm, tmem, tid & 127, warp < 4 ? 1 : 0, S0, S_T, &tm_o, bh, nchunks);
-        else
-            state_role<false>(ctl, sm, tmem, tid - 128, S0, S_T, &tm_o, bh, nchunks);
+        // split form: warps 4-7 convert dv 0-63, warps 0-3 dv 64-127
+        state_role<kSplit>(ctl, sm, tmem, warp >= 4 ? tid - 128 : tid + 128, S0, S_T, &tm_o, bh,
+                           nchunks);
     } else if (warp >= 8 && warp < (kSplit ? 12 : 16)) {
         const int g = (warp - 8) >> 2;
         chunk_role<kSplit>(ctl, sm, tmem, tid - 256 - 128 * g, g, beta, bh, T, nchunks);

@@ -68,18 +68,22 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_traffic(name: str, source: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since it was captured."""
+def kernel_traffic(names, source: str):
+    """DRAM bytes per call (summed over the named kernels) from the committed
+    ncu summary, or None when the kernel source changed since the capture."""
     p = ROOT / "profiles" / "traffic.json"
     if not p.exists():
         return None
-    entry = json.loads(p.read_text()).get(name)
-    if not entry:
-        return None
+    table = json.loads(p.read_text())
     src = ROOT / "delta_rule_recurrent_gb300" / "csrc" / source
     sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
-    return entry["bytes_per_launch"] if entry.get("source_sha") == sha else None
+    total = 0.0
+    for name in ([names] if isinstance(names, str) else names):
+        entry = table.get(name)
+        if not entry or entry.get("source_sha") != sha:
+            return None
+        total += entry["bytes_per_launch"]
+    return total
 
 
 class ClockSampler:
@@ -260,9 +264,16 @@ def run_ours(args, rank, world, local):
     algo = args.algo
     lib = dn.load()
     tc = algo in ("auto", "tcgen05") and _tc_used(lib, dk, dv, q.dtype)
+    # The two-pass tensor-core path takes a workspace (one [PT; T] tile per
+    # chunk), allocated once here, outside the timed region.
+    ws_bytes = 0 if args.no_workspace else lib.dn_chunk_fwd_workspace_bytes(
+        B, H, T, dk, dv, C, 1 if q.dtype == torch.bfloat16 else 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    split = tc and ws is not None
+    launches_per_call = 2 if split else 1
 
     def chunk_step(_i):
-        dn.chunk_fwd(q, k, v, beta, out=o, final_state=S_T, algo=algo)
+        dn.chunk_fwd(q, k, v, beta, out=o, final_state=S_T, algo=algo, workspace=ws)
 
     for i in range(args.warmup):
         chunk_step(i)
@@ -307,7 +318,7 @@ def run_ours(args, rank, world, local):
         k.copy_(hk, non_blocking=True)
         v.copy_(hv, non_blocking=True)
         beta.copy_(hb, non_blocking=True)
-        dn.chunk_fwd(q, k, v, beta, out=o, final_state=S_T, algo=algo)
+        dn.chunk_fwd(q, k, v, beta, out=o, final_state=S_T, algo=algo, workspace=ws)
         ho.copy_(o, non_blocking=True)
 
     for i in range(min(args.warmup, 3)):
@@ -324,12 +335,20 @@ def run_ours(args, rank, world, local):
     flops = chunk_flops_per_token_head(C, dk, dv) * B * H * T
     cbytes = chunk_bytes(B, H, T, dk, dv, q.element_size(), False, True)
     tflops = flops / launch_s / 1e12
-    kname = "chunk_tc" if tc else "chunk_simt"
+    # A "launch" here is one dn_chunk_fwd call; on the two-pass path that is
+    # the prepare kernel and the sequence kernel back to back.
+    if split:
+        kname, knames = "chunk_prep + chunk_tc (split)", ["chunk_prep", "chunk_tc_split"]
+    elif tc:
+        kname, knames = "chunk_tc (fused)", ["chunk_tc_fused"]
+    else:
+        kname, knames = "chunk_simt", ["chunk_simt"]
     roofline = {
         "bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
         "frac": tflops / peaks["bf16_tflops"],
-        "traffic": kernel_traffic(kname, "chunk_tc.cu" if tc else "chunk_simt.cu"),
+        "traffic": kernel_traffic(knames, "chunk_tc.cu" if tc else "chunk_simt.cu"),
         "peak_source": f"{peak_src} (bf16 dense burst)", "kernel": kname,
+        "launches_per_call": launches_per_call,
         "flops_per_launch": flops, "launch_us": launch_s * 1e6,
         "hbm": {"achieved": cbytes / launch_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": cbytes / launch_s / 1e9 / peaks["hbm_gbs"], "bytes_per_launch": cbytes},
@@ -356,6 +375,7 @@ def run_ours(args, rank, world, local):
         "dtype": "bf16" if tc else "f32", "data": "synthetic (seeded)",
         "config": {"workload": HEADLINE, "B": B, "H": H, "T": T, "dk": dk, "dv": dv, "C": C,
                    "io_dtype": w["dtype"], "state": "fp32", "algo": kname,
+                   "workspace_bytes": ws_bytes,
                    "l2": f"inputs {(3 * B * H * T * dk * 2) >> 20} MB > L2 (129 MB), no flush",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
@@ -363,7 +383,7 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": world * tokens * e2e_steps / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": 1e3 * e2e_s / e2e_steps},
-        "gpu_launches": args.steps + nsteps + e2e_steps,
+        "gpu_launches": launches_per_call * (args.steps + e2e_steps) + nsteps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -404,6 +424,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="tensor-core path without a workspace (the fused kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -1,10 +1,11 @@
 """Runs one workload a few times through the public API, for profiler captures.
 
-    python -m delta_rule_recurrent_gb300.profile_run chunk [--B 8] [--T 2048] [--algo auto] [--reps 3]
+    python -m delta_rule_recurrent_gb300.profile_run chunk [--B 8] [--T 2048] [--algo auto] [--reps 3] [--no-workspace]
     python -m delta_rule_recurrent_gb300.profile_run decode [--B 256] [--steps 4]
 
 `chunk` runs the chunkwise forward on the 1.3B-layer shape (B8 H16 T2048
-dk=dv=128, bf16; B and T can be reduced); `decode` runs consecutive decoding
+dk=dv=128, bf16; B and T can be reduced; the tensor-core path runs in two
+passes unless --no-workspace selects its fused kernel); `decode` runs consecutive decoding
 steps on the decode workload's shape (B256 H16 dk=dv=128, fp32 state).  Inputs
 come from the seeded generators in `workloads`.
 """
@@ -30,6 +31,7 @@ def main(argv=None):
     ap.add_argument("--algo", default="auto", choices=list(dn.ALGOS))
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--steps", type=int, default=4)
+    ap.add_argument("--no-workspace", action="store_true")
     a = ap.parse_args(argv)
     dev = torch.device("cuda:0")
     if a.what == "chunk":
@@ -37,7 +39,8 @@ def main(argv=None):
         inp = workloads.workload_inputs("layer1p3b_bf16", **over)
         q, k, v, b = (x.to(dev) for x in (inp.q, inp.k, inp.v, inp.beta))
         for _ in range(a.reps):
-            o, _ = dn.chunk_fwd(q, k, v, b, algo=a.algo)
+            o, _ = dn.chunk_fwd(q, k, v, b, algo=a.algo,
+                                workspace=None if a.no_workspace else "auto")
     else:
         w = workloads.WORKLOADS["decode_bf16"]
         B = a.B or w["B"]

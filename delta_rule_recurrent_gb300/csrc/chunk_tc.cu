@@ -1074,16 +1074,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // blockIdx.x + gridDim.x, ...; several CTAs share an SM, so the loads, MMAs
 // and solves of different chunks overlap.  The tile goes to the workspace,
 // laid out [BH][chunk][128 rows][64] bf16, rows 0-63 PT and 64-127 Tm.
+// [K; Q] is spent once G is formed, so the next item's tiles (and strengths)
+// are fetched while this item is solved; [PT; Tm] is built over the fp32
+// solve array, which is spent once Tm has been read from it.
 constexpr int kPrepThreads = 128;
 constexpr int kPrepCtasPerSm = 4;
-constexpr uint32_t P_OFF_KQ = 0;                   // [K; Q] tile; [PT; Tm] reuses its first 16 KB
-constexpr uint32_t P_OFF_X = P_OFF_KQ + kStageKQ;  // fp32 A, overwritten by X
+constexpr uint32_t P_OFF_KQ = 0;                   // [K; Q] tile
+constexpr uint32_t P_OFF_X = P_OFF_KQ + kStageKQ;  // fp32 A, overwritten by X; then [PT; Tm]
 constexpr uint32_t P_OFF_Y = P_OFF_X + kXBytes;    // solve scratch
 constexpr uint32_t P_OFF_BETA = P_OFF_Y + kYBytes; // 64 fp32
 constexpr uint32_t P_OFF_BAR = P_OFF_BETA + 256;   // mbarriers: tiles landed, MMA done, drain
 constexpr uint32_t P_OFF_MISC = P_OFF_BAR + 24;    // abort flag, TMEM address
 constexpr uint32_t kPrepSmemBytes = P_OFF_MISC + 16 + 1024;
 static_assert(kPrepCtasPerSm * (kPrepSmemBytes + 1024) <= 233472, "prepare kernel occupancy");
+static_assert(P_OFF_X % 1024 == 0 && kXBytes >= kTile, "[PT; Tm] over the solve array");
 
 __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -1101,7 +1105,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const Ctl ctl{base + P_OFF_BAR, reinterpret_cast<volatile int*>(misc)};
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
     const int t = threadIdx.x, row = t & 63;
-    const uint32_t kq = base + P_OFF_KQ, tp = kq;
+    const uint32_t kq = base + P_OFF_KQ, tp = base + P_OFF_X;
     const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
 
     if (t == 0) {
@@ -1121,23 +1125,31 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_holder;
 
-    int n = 0, loads = 0;  // items finished, tile loads issued (thread 0)
-    for (int w = blockIdx.x; w < items; w += gridDim.x, ++n) {
+    // [K; Q] tiles of item w into the tile area (thread 0).
+    auto load_tiles = [&](int w) {
         const int bh = w / nchunks, c = w % nchunks;
-        if (t == 0) {
-            bulk_wait_group_read0();  // the previous tile's store has read the area
-            const uint32_t bar = ctl.bar(B_TILES);
-            mbar_arrive_expect_tx(bar, 4 * 8192);
-            tma_load_3d(kq, &tm_k, bar, 0, c * kC, bh);
-            tma_load_3d(kq + kRegKQ, &tm_k, bar, 64, c * kC, bh);
-            tma_load_3d(kq + 8192, &tm_q, bar, 0, c * kC, bh);
-            tma_load_3d(kq + kRegKQ + 8192, &tm_q, bar, 64, c * kC, bh);
-            ++loads;
-        }
-        if (t < kC) {
-            const int tok = c * kC + t;
-            betas[t] = tok < T ? __bfloat162float(beta[(size_t)bh * T + tok]) : 0.f;
-        }
+        const uint32_t bar = ctl.bar(B_TILES);
+        mbar_arrive_expect_tx(bar, 4 * 8192);
+        tma_load_3d(kq, &tm_k, bar, 0, c * kC, bh);
+        tma_load_3d(kq + kRegKQ, &tm_k, bar, 64, c * kC, bh);
+        tma_load_3d(kq + 8192, &tm_q, bar, 0, c * kC, bh);
+        tma_load_3d(kq + kRegKQ + 8192, &tm_q, bar, 64, c * kC, bh);
+    };
+    // Strength of token t of item w (0 past T), as volatile loads kept in place.
+    auto load_beta = [&](int w) -> uint16_t {
+        const int bh = w / nchunks, tok = (w % nchunks) * kC + t;
+        return tok < T ? ld_nc_u16(beta + (size_t)bh * T + tok) : (uint16_t)0;
+    };
+
+    int n = 0, loads = 0;  // items finished, tile loads issued (thread 0)
+    if (t == 0 && (int)blockIdx.x < items) {
+        load_tiles(blockIdx.x);
+        ++loads;
+    }
+    uint16_t bnext = (t < kC && (int)blockIdx.x < items) ? load_beta(blockIdx.x) : (uint16_t)0;
+    for (int w = blockIdx.x; w < items; w += gridDim.x, ++n) {
+        const int bh = w / nchunks, c = w % nchunks, wn = w + (int)gridDim.x;
+        if (t < kC) betas[t] = __bfloat162float(__ushort_as_bfloat16(bnext));
         // G = [K; Q] K^T
         bool ok = true;
         if (t == 0) {
@@ -1153,7 +1165,17 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 mma_commit(ctl.bar(B_MMA));
                 ok = ctl.wait(B_MMA, (uint32_t)(2 * n));
             }
+            if (ok) {
+                // [K; Q] is spent: fetch the next item's tiles now.  The previous
+                // [PT; Tm] store must have read the solve array before A goes in.
+                if (wn < items) {
+                    load_tiles(wn);
+                    ++loads;
+                }
+                bulk_wait_group_read0();
+            }
         }
+        if (t < kC && wn < items) bnext = load_beta(wn);
         if (wg_sync_or(kBar, !ok)) break;
         tc_fence_after_sync();
         // A (TMEM rows 0-63) into the solve array; P (rows 64-127) stays in TMEM.
@@ -1170,7 +1192,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tc_fence_before_sync();
         wg_sync(kBar);
         solve_unit_lower64_mma(X, Ys, t, kBar);
-        // [K; Q] is spent: Tm and P into the [PT; Tm] tile over its first 16 KB.
+        // Tm = X diag(beta) (rows 64-127) and P (rows 0-63) as bf16 over the
+        // spent solve array: everything is read before anything is written.
         {
             float x[64];
             if (t < 64) {
@@ -1182,14 +1205,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     x[e + 2] = xv.z * bv.z;
                     x[e + 3] = xv.w * bv.w;
                 }
-                store_row64_bf16(tp, 64 + t, x);
             } else {
                 tmem_ld64f(tmem + lane_base, x);
 #pragma unroll
                 for (int j = 0; j < 64; ++j)
                     if (j > row) x[j] = 0.f;
-                store_row64_bf16(tp, row, x);
             }
+            tc_fence_before_sync();
+            wg_sync(kBar);
+            store_row64_bf16(tp, t < 64 ? 64 + t : row, x);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();

@@ -1257,6 +1257,388 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 }
 
+// --------------------------------------------------------------- scan kernel
+// Split form, second pass: one CTA of 16 warps per (batch, head) walks the
+// chunks in order with S resident in TMEM.  It computes the transpose of the
+// chunk algebra, so the state's bf16 operand and U' stay in TMEM as A operands
+// and never pass through shared memory:
+//     D1^T = V^T [PT; Tm]^T + S^T [Q'; -W]^T     (lanes: dv; columns: o, U' rows)
+//     S^T += U'^T K
+// where S^T[j][i] = S[i][j] with S the [dk][dv] state.  [Q'; -W] is the B
+// operand, built in shared memory by the chunk group.
+//   warp 0      TMA producer: [K; Q] ring (3), v (2), [PT; Tm] from the workspace (2)
+//   warp 1      TMEM owner
+//   warps 4-7   state: thread t owns dv column t (TMEM lane t); thread 0 issues
+//               D1^T += S^T [Q'; -W]^T and S^T += U'^T K
+//   warps 8-11  chunk group: DW = [PT; Tm] K, then the chunk's [Q'; -W] tile
+//               from DW and the q rows
+//   warps 12-15 o writer: reads the o rows of D1^T, stores them (coalesced
+//               global stores), and starts the next chunk's D1^T = V^T [PT; Tm]^T
+namespace scan {
+constexpr int kStages = 3, kVBufs = 2, kKQ = 6;       // [K; Q] barriers: one per (stage, parity)
+constexpr uint32_t OFF_KQ = 0;                         // kStages x [K; Q]
+constexpr uint32_t OFF_V = OFF_KQ + kStages * kStageKQ;   // kVBufs x v (2 dv-half regions)
+constexpr uint32_t OFF_TP = OFF_V + kVBufs * kTile;    // 2 x [PT; Tm]
+constexpr uint32_t OFF_QW = OFF_TP + 2 * kTile;        // 2 x [Q'; -W] (2 dk-half regions of 128 rows)
+constexpr uint32_t OFF_BAR = OFF_QW + 4 * kTile;
+enum : int {
+    B_KQ_FULL = 0,    // [6] q, k tiles landed                 (producer -> chunk group)
+    B_KQ_EMPTY = 6,   // [3] S^T += U'^T K done with the stage  (state MMA -> producer)
+    B_V_FULL = 9,     // [2] v tile landed                      (producer -> o writer)
+    B_V_EMPTY = 11,   // [2] v part done with the v buffer      (o writer MMA -> producer)
+    B_TP_FULL = 13,   // [2] [PT; Tm] landed                    (producer -> chunk group, o writer)
+    B_QW_READY = 15,  // [2] [Q'; -W] written                   (chunk group -> state)
+    B_FREE = 17,      // [2] D1 MMAs done with [PT; Tm], [Q'; -W] (state MMA -> producer)
+    B_D1_FULL = 19,   // D1^T done                              (own commit, state)
+    B_S_READY = 20,   // S^T += U'^T K done                     (own commit, state)
+    B_DW_FULL = 21,   // DW done                                (own commit, chunk group)
+    B_O_READY = 22,   // D1^T final                             (state -> o writer)
+    B_U_READ = 23,    // U' rows of D1^T read                   (state -> o writer)
+    B_VP_DONE = 24,   // v part of D1^T done                    (o writer MMA -> state)
+    B_DRAIN = 25,     // [3] final drain per MMA issuer         (state, chunk group, o writer)
+};
+constexpr int kBars = 28;
+constexpr uint32_t OFF_MISC = OFF_BAR + 8 * kBars;     // abort flag, TMEM address
+constexpr uint32_t kSmemBytes = OFF_MISC + 16 + 1024;
+static_assert(kSmemBytes <= 232448, "scan kernel shared memory");
+// TMEM columns: S^T fp32 | D1^T fp32 (o rows 0-63, U' rows 64-127) | S^T bf16 |
+// U'^T bf16 | the chunk group's 128 DW accumulator columns.
+constexpr uint32_t C_ST = 0, C_D1 = 128, C_SB = 256, C_UB = 320, C_GRP = 352;
+constexpr uint32_t ID_VP = idesc_bf16_f32(128, 128, 1, 0);  // A v^T (MN-major), B [PT;Tm] (K-major)
+constexpr uint32_t ID_SP = idesc_bf16_f32(128, 128, 0, 0);  // A S^T (TMEM), B [Q';-W] (K-major)
+constexpr uint32_t ID_KB = idesc_bf16_f32(128, 128, 0, 1);  // A U'^T (TMEM) or [PT;Tm], B K (MN-major)
+
+struct Smem {
+    uint32_t base;
+    __device__ uint32_t kq(int c) const { return base + OFF_KQ + (uint32_t)(c % kStages) * kStageKQ; }
+    __device__ uint32_t v(int c) const { return base + OFF_V + (uint32_t)(c % kVBufs) * kTile; }
+    __device__ uint32_t tp(int g) const { return base + OFF_TP + (uint32_t)g * kTile; }
+    __device__ uint32_t qw(int g) const { return base + OFF_QW + (uint32_t)g * 2u * kTile; }
+};
+
+__device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q,
+                         const CUtensorMap* tm_k, const CUtensorMap* tm_v, const CUtensorMap* tm_ws,
+                         int bh, int nchunks) {
+    int nkq = 0, nv = 0, ntp = 0;
+    long long t0 = clock64();
+    while ((nkq < nchunks || nv < nchunks || ntp < nchunks) && !ctl.aborted()) {
+        bool progressed = false;
+        if (nkq < nchunks &&
+            (nkq < kStages ||
+             mbar_test_wait(ctl.bar(B_KQ_EMPTY + nkq % kStages), (uint32_t)(nkq / kStages - 1) & 1u))) {
+            const uint32_t st = sm.kq(nkq), bar = ctl.bar(B_KQ_FULL + nkq % kKQ);
+            mbar_arrive_expect_tx(bar, 4 * 8192);
+            tma_load_3d(st, tm_k, bar, 0, nkq * kC, bh);
+            tma_load_3d(st + kRegKQ, tm_k, bar, 64, nkq * kC, bh);
+            tma_load_3d(st + 8192, tm_q, bar, 0, nkq * kC, bh);
+            tma_load_3d(st + kRegKQ + 8192, tm_q, bar, 64, nkq * kC, bh);
+            if (nkq + kStages < nchunks) {  // warm L2 for this stage's next tiles
+                const int y = (nkq + kStages) * kC;
+                tma_prefetch_l2_3d(tm_k, 0, y, bh);
+                tma_prefetch_l2_3d(tm_k, 64, y, bh);
+                tma_prefetch_l2_3d(tm_q, 0, y, bh);
+                tma_prefetch_l2_3d(tm_q, 64, y, bh);
+            }
+            ++nkq;
+            progressed = true;
+        }
+        if (nv < nchunks &&
+            (nv < kVBufs ||
+             mbar_test_wait(ctl.bar(B_V_EMPTY + nv % kVBufs), (uint32_t)(nv / kVBufs - 1) & 1u))) {
+            const uint32_t bar = ctl.bar(B_V_FULL + nv % kVBufs);
+            mbar_arrive_expect_tx(bar, 2 * 8192);
+            tma_load_3d(sm.v(nv), tm_v, bar, 0, nv * kC, bh);
+            tma_load_3d(sm.v(nv) + 8192, tm_v, bar, 64, nv * kC, bh);
+            if (nv + kVBufs < nchunks) {
+                tma_prefetch_l2_3d(tm_v, 0, (nv + kVBufs) * kC, bh);
+                tma_prefetch_l2_3d(tm_v, 64, (nv + kVBufs) * kC, bh);
+            }
+            ++nv;
+            progressed = true;
+        }
+        if (ntp < nchunks) {
+            const int g = ntp & 1, it = ntp >> 1;
+            if (it == 0 || mbar_test_wait(ctl.bar(B_FREE + g), (uint32_t)(it - 1) & 1u)) {
+                const uint32_t bar = ctl.bar(B_TP_FULL + g);
+                mbar_arrive_expect_tx(bar, kTile);
+                tma_load_3d(sm.tp(g), tm_ws, bar, 0, ntp * 128, bh);
+                if (ntp + 2 < nchunks) tma_prefetch_l2_3d(tm_ws, 0, (ntp + 2) * 128, bh);
+                ++ntp;
+                progressed = true;
+            }
+        }
+        if (progressed) {
+            t0 = clock64();
+        } else {
+            __nanosleep(64);
+            if (clock64() - t0 > kTimeoutCycles) ctl.raise();
+        }
+    }
+    for (int b = 0; b < kKQ; ++b) {  // leave nothing in flight (bounded waits)
+        const int n_b = (nkq - b + kKQ - 1) / kKQ;
+        if (n_b > 0) mbar_wait(ctl.bar(B_KQ_FULL + b), (uint32_t)(n_b - 1) & 1u, kTimeoutNs);
+    }
+    for (int b = 0; b < kVBufs; ++b) {
+        const int n_b = (nv - b + kVBufs - 1) / kVBufs;
+        if (n_b > 0) mbar_wait(ctl.bar(B_V_FULL + b), (uint32_t)(n_b - 1) & 1u, kTimeoutNs);
+    }
+    for (int g = 0; g < 2; ++g) {
+        const int n_g = (ntp - g + 1) / 2;
+        if (n_g > 0) mbar_wait(ctl.bar(B_TP_FULL + g), (uint32_t)(n_g - 1) & 1u, kTimeoutNs);
+    }
+}
+
+// 64 fp32 TMEM columns (lane of the calling thread) -> 32 bf16-pair columns.
+__device__ __forceinline__ void tmem_pack64(uint32_t src, uint32_t dst) {
+    float x[64];
+    tmem_ld64f(src, x);
+    uint32_t p[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) p[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+    tmem_st32(dst, p);
+}
+
+__device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
+                           const float* __restrict__ S0, float* __restrict__ S_T, int bh,
+                           int nchunks) {
+    constexpr int kBar = 1;
+    const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
+    // S0^T into TMEM: lane t holds dv column t of S0 (zeros without S0).
+#pragma unroll
+    for (int part = 0; part < 4; ++part) {
+        uint32_t r[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            r[e] = S0 ? __float_as_uint(S0[((size_t)bh * kD + 32 * part + e) * kD + t]) : 0u;
+        tmem_st32(lane + C_ST + 32u * part, r);
+    }
+    tmem_wait_st();
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int g = c & 1;
+        if (c > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(c - 1), t, kBar)) return;
+        tc_fence_after_sync();
+        tmem_pack64(lane + C_ST, lane + C_SB);             // S^T -> bf16, dk 0-63
+        tmem_pack64(lane + C_ST + 64u, lane + C_SB + 32u);  // dk 64-127
+        tmem_wait_st();
+        tc_fence_before_sync();
+        wg_sync(kBar);
+        bool ok = true;
+        if (t == 0) {
+            // the o writer started D1^T with its v part once D1^T was free
+            ok = ctl.wait(B_QW_READY + g, (uint32_t)(c >> 1)) && ctl.wait(B_VP_DONE, (uint32_t)c);
+            if (ok) {
+                tc_fence_after_sync();
+                const uint32_t qw = sm.qw(g);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // D1^T += S^T [Q'; -W]^T over dk
+                    mma_bf16_ts(tmem + C_D1, tmem + C_SB + 8u * kk,
+                                sw128_desc(qw + (uint32_t)(kk >> 2) * kTile + 32u * (kk & 3), 16, 1024),
+                                ID_SP, 1);
+                mma_commit(ctl.bar(B_D1_FULL));
+                mma_commit(ctl.bar(B_FREE + g));
+                ok = ctl.wait(B_D1_FULL, (uint32_t)c);
+                if (ok) mbar_arrive(ctl.bar(B_O_READY));
+            }
+        }
+        if (wg_sync_or(kBar, !ok)) return;
+        tc_fence_after_sync();
+        tmem_pack64(lane + C_D1 + 64u, lane + C_UB);  // U'^T -> bf16 (tokens)
+        tmem_wait_st();
+        tc_fence_before_sync();
+        wg_sync(kBar);
+        if (t == 0) {
+            mbar_arrive(ctl.bar(B_U_READ));
+            tc_fence_after_sync();
+            const uint32_t kq = sm.kq(c);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // S^T += U'^T K over the chunk's tokens
+                mma_bf16_ts(tmem + C_ST, tmem + C_UB + 8u * kk,
+                            sw128_desc(kq + 2048u * kk, kRegKQ, 1024), ID_KB, 1);
+            mma_commit(ctl.bar(B_S_READY));
+            mma_commit(ctl.bar(B_KQ_EMPTY + c % kStages));
+        }
+    }
+    if (nchunks > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(nchunks - 1), t, kBar)) return;
+    tc_fence_after_sync();
+    if (S_T) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float x[64];
+            tmem_ld64f(lane + C_ST + 64u * half, x);
+#pragma unroll
+            for (int i = 0; i < 64; ++i) S_T[((size_t)bh * kD + 64 * half + i) * kD + t] = x[i];
+        }
+    }
+}
+
+// Chunk group: [Q'; -W] of every chunk as the B operand tile of the state MMA
+// (2 dk-half regions of 128 rows x 64 bf16): DW = [PT; Tm] K into its 128
+// accumulator columns, then row t of [Q - PT K; -W] from DW and the chunk's q
+// rows.  Thread t owns TMEM lane t; thread 0 issues.
+__device__ void group_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int nchunks) {
+    constexpr int kBar = 2;
+    const int row = t & 63;
+    const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
+    for (int c = 0; c < nchunks; ++c) {
+        const int g = c & 1;
+        const uint32_t kq = sm.kq(c), tp = sm.tp(g), qw = sm.qw(g);
+        bool ok = true;
+        // [PT; Tm] is loaded only after the state released this buffer set,
+        // so the [Q'; -W] tile is free as well.
+        if (t == 0) {
+            ok = ctl.wait(B_KQ_FULL + c % kKQ, (uint32_t)(c / kKQ)) &&
+                 ctl.wait(B_TP_FULL + g, (uint32_t)(c >> 1));
+            if (ok) {
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss(tmem + C_GRP, sw128_desc(tp + 32u * kk, 16, 1024),
+                                sw128_desc(kq + 2048u * kk, kRegKQ, 1024), ID_KB, kk > 0);
+                mma_commit(ctl.bar(B_DW_FULL));
+                ok = ctl.wait(B_DW_FULL, (uint32_t)c);
+            }
+        }
+        if (wg_sync_or(kBar, !ok)) return;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // row t of [Q'; -W], dk half h
+            float x[64];
+            tmem_ld64f(lane + C_GRP + 64u * h, x);
+            if (t < 64) {
+                const uint32_t region = kq + (uint32_t)h * kRegKQ;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint4 qv = ld_shared_v4(region + sw128(64 + row, cc));
+                    const float2 a0 = unpack_bf16(qv.x), a1 = unpack_bf16(qv.y),
+                                 a2 = unpack_bf16(qv.z), a3 = unpack_bf16(qv.w);
+                    float* d = x + 8 * cc;
+                    d[0] = a0.x - d[0];
+                    d[1] = a0.y - d[1];
+                    d[2] = a1.x - d[2];
+                    d[3] = a1.y - d[3];
+                    d[4] = a2.x - d[4];
+                    d[5] = a2.y - d[5];
+                    d[6] = a3.x - d[6];
+                    d[7] = a3.y - d[7];
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 64; ++e) x[e] = -x[e];
+            }
+            store_row64_bf16(qw + (uint32_t)h * kTile, t, x);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        wg_sync(kBar);
+        if (t == 0) mbar_arrive(ctl.bar(B_QW_READY + g));
+    }
+}
+
+// D1^T = v^T [PT; Tm]^T (overwrites D1^T), issued by one thread.
+__device__ __forceinline__ void issue_vpart(uint32_t tmem, uint32_t v, uint32_t tp) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        mma_bf16_ss(tmem + C_D1, sw128_desc(v + 2048u * kk, 8192, 1024),
+                    sw128_desc(tp + 32u * kk, 16, 1024), ID_VP, kk > 0);
+}
+
+// o writer: thread t owns dv column t (TMEM lane t); thread 0 issues the v part.
+__device__ void writer_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
+                            __nv_bfloat16* __restrict__ o, int bh, int T, int nchunks) {
+    constexpr int kBar = 3;
+    const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
+    // v part of chunk cn, once its v tile and [PT; Tm] are in (thread 0).
+    auto start = [&](int cn) -> bool {
+        if (!ctl.wait(B_TP_FULL + (cn & 1), (uint32_t)(cn >> 1)) ||
+            !ctl.wait(B_V_FULL + cn % kVBufs, (uint32_t)(cn / kVBufs)))
+            return false;
+        tc_fence_after_sync();
+        issue_vpart(tmem, sm.v(cn), sm.tp(cn & 1));
+        mma_commit(ctl.bar(B_VP_DONE));
+        mma_commit(ctl.bar(B_V_EMPTY + cn % kVBufs));
+        return true;
+    };
+    bool ok = t != 0 || nchunks == 0 || start(0);
+    if (wg_sync_or(kBar, !ok)) return;
+    for (int c = 0; c < nchunks; ++c) {
+        ok = true;
+        if (t == 0) ok = ctl.wait(B_O_READY, (uint32_t)c);
+        if (wg_sync_or(kBar, !ok)) return;
+        tc_fence_after_sync();
+        float ov[64];  // o^T: dv t, the chunk's 64 tokens
+        tmem_ld64f(lane + C_D1, ov);
+        tc_fence_before_sync();
+        wg_sync(kBar);
+        // D1^T is free once the state has read the U' rows as well.
+        if (t == 0) ok = ctl.wait(B_U_READ, (uint32_t)c) && (c + 1 >= nchunks || start(c + 1));
+        const int tok0 = c * kC;
+        __nv_bfloat16* const ob = o + ((size_t)bh * T + tok0) * kD + t;
+#pragma unroll
+        for (int r = 0; r < 64; ++r)
+            if (tok0 + r < T) ob[(size_t)r * kD] = __float2bfloat16_rn(ov[r]);
+        if (wg_sync_or(kBar, !ok)) return;
+    }
+}
+}  // namespace scan
+
+__global__ void __launch_bounds__(512, 1)
+chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ws,
+                  const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
+                  float* __restrict__ S_T, int T) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    const scan::Smem sm{base};
+    int* const misc = reinterpret_cast<int*>(smem_raw + (base - raw_addr) + scan::OFF_MISC);
+    const Ctl ctl{base + scan::OFF_BAR, reinterpret_cast<volatile int*>(misc)};
+    uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.x;
+    const int nchunks = (T + kC - 1) / kC;
+
+    if (tid == 0) {
+        misc[0] = 0;
+        for (int b = 0; b < scan::kBars; ++b) mbar_init(ctl.bar(b), 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_ws);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_holder), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) scan::producer(ctl, sm, &tm_q, &tm_k, &tm_v, &tm_ws, bh, nchunks);
+    } else if (warp >= 4 && warp < 8) {
+        const int t = tid - 128;
+        scan::state_body(ctl, sm, tmem, t, S0, S_T, bh, nchunks);
+        if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 0);
+    } else if (warp >= 8 && warp < 12) {
+        const int t = tid - 256;
+        scan::group_body(ctl, sm, tmem, t, nchunks);
+        if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 1);
+    } else if (warp >= 12) {
+        const int t = tid - 384;
+        scan::writer_body(ctl, sm, tmem, t, o, bh, T, nchunks);
+        if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 2);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1333,16 +1715,16 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
         if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
         if ((err = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kPrepSmemBytes)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(chunk_tc_kernel<true>,
+            (err = cudaFuncSetAttribute(chunk_scan_kernel,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        Layout<true>::kSmemBytes)) != cudaSuccess)
+                                        scan::kSmemBytes)) != cudaSuccess)
             return err;
         const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
         chunk_prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(mq, mk, mws, b, T, nchunks,
                                                                           (int)items);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
-        chunk_tc_kernel<true><<<BH, kSeqThreads<true>, Layout<true>::kSmemBytes, stream>>>(
-            mq, mk, mv, mo, mws, b, S0, S_T, T);
+        chunk_scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(
+            mq, mk, mv, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, T);
         return cudaGetLastError();
     }
     if ((err = cudaFuncSetAttribute(chunk_tc_kernel<false>,

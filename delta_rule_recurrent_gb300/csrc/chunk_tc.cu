@@ -10,29 +10,23 @@
 //     Tm   = (I + A)^{-1} diag(beta)        W = Tm K,  U = Tm V
 //     U'   = U - W S                        (true per-token errors)
 //     O    = Q S + P U'                     S <- S + K^T U'
-// The kernel regroups the output as O = (Q - PT K) S + PT V with PT = P Tm,
+// The kernels regroup the output as O = (Q - PT K) S + PT V with PT = P Tm,
 // which equals Q S + P U' exactly and lets one accumulator produce O and U':
 //     D1 = [PT; Tm] V  (+)  [Q - PT K; -W] S    ->  rows 0-63: O, rows 64-127: U'
 // Everything left of the (+) depends only on the chunk's own inputs, so the
 // state-dependent chain per chunk is: S -> bf16 -> the D1 MMAs -> U' -> bf16
 // -> S += K^T U'.
 //
-// One CTA owns one (batch, head) and keeps S in TMEM for the whole sequence.
-// Its warps have fixed roles:
-//   warp 0      TMA producer: [K; Q] tiles into a 3-stage ring, v tiles
-//               (3-D maps, so rows past the end of a sequence read as zeros)
-//   warp 1      TMEM owner
-//   warps 4-7   state group: S -> bf16 operand, the D1 MMAs, the o tile
-//               (TMA store from the spent half of the S operand), U',
-//               S += K^T U', final state
-//   warps 8-11, 12-15   chunk groups for even and odd chunks: G = [K; Q] K^T,
-//               A and P, the triangular solve, Tm, PT and the [Q'; -W]
-//               operand, which each group leaves in a TMEM buffer of its own
-// A chunk group meets the state group only at the hand-over of its chunk and
-// when it reuses its buffers two chunks later, so the groups run ahead of the
-// state chain by up to a chunk each.  Each elected thread issues its role's
-// MMAs and waits on its own commits.  Operand tiles in shared memory use the
-// 128-byte swizzled layout TMA writes.
+// Two forms share this algebra:
+//   - two passes (with a workspace): chunk_prep_kernel forms [PT; Tm] of
+//     every chunk of every head in parallel; chunk_scan_kernel then walks
+//     each (batch, head) in order, computing the transposed products so the
+//     state's operands stay in TMEM (see the scan kernel's own comment);
+//   - fused (without a workspace): chunk_tc_kernel does both in one CTA per
+//     (batch, head), with two chunk groups forming [PT; Tm] and [Q'; -W] for
+//     alternate chunks next to the state group.
+// Each role's elected thread issues its MMAs and waits on its own commits.
+// Operand tiles in shared memory use the 128-byte swizzled layout TMA writes.
 // Every wait is bounded: on a timeout the CTA records an error code (read
 // back with dn_device_error), drains what it started and exits.
 #include <cudaTypedefs.h>
@@ -71,24 +65,20 @@ constexpr uint32_t kStageKQ = 2 * kRegKQ;            // 32 KB
 constexpr uint32_t kTile = 16384;                    // a 128 x 64 or 64 x 128 bf16 tile
 constexpr uint32_t kXBytes = 64 * kP * 4;            // fp32 64 x kP solve array
 constexpr uint32_t kYBytes = 32 * kYP * 4;           // fp32 32 x kYP solve scratch
-constexpr int kNumBars = 34;
-// Shared memory of the sequence kernel.  The fused form (kSplit false) also
-// holds the chunk groups' solve arrays; the split form, whose [PT; Tm] tiles
-// come from the prepare kernel, spends that space on a second v buffer and an
-// o tile of its own.
-template <bool kSplit>
+// Shared memory of the fused kernel: the [K; Q] ring, v, the chunk groups'
+// [PT; Tm] tiles, the S operand (then U' and the o tile) and the groups'
+// solve arrays.
 struct Layout {
     static constexpr int kStages = 3;                          // [K; Q] ring depth
-    static constexpr int kVBufs = kSplit ? 2 : 1;              // v tiles in flight
     static constexpr uint32_t OFF_KQ = 0;                      // kStages stages
     static constexpr uint32_t OFF_V = OFF_KQ + kStages * kStageKQ;  // v: 2 dv halves x 64 rows each
-    static constexpr uint32_t OFF_TP = OFF_V + kVBufs * kTile; // 2 x [PT; Tm] (one per chunk group)
+    static constexpr uint32_t OFF_TP = OFF_V + kTile;          // 2 x [PT; Tm] (one per chunk group)
     static constexpr uint32_t OFF_SB = OFF_TP + 2 * kTile;     // S as bf16 (2 x 128 rows); then U', o tile
-    static constexpr uint32_t OFF_O = OFF_SB + 2 * kTile;      // split: o tile of its own
-    static constexpr uint32_t OFF_X = OFF_O + (kSplit ? kTile : 0);  // fused: 2 x A, overwritten by X
-    static constexpr uint32_t OFF_Y = OFF_X + (kSplit ? 0 : 2 * kXBytes);     // fused: 2 x scratch
-    static constexpr uint32_t OFF_BETA = OFF_Y + (kSplit ? 0 : 2 * kYBytes);  // fused: 2 x 64 fp32
-    static constexpr uint32_t OFF_BAR = OFF_BETA + (kSplit ? 0 : 512);        // mbarriers
+    static constexpr uint32_t OFF_X = OFF_SB + 2 * kTile;      // 2 x A, overwritten by X
+    static constexpr uint32_t OFF_Y = OFF_X + 2 * kXBytes;     // 2 x solve scratch
+    static constexpr uint32_t OFF_BETA = OFF_Y + 2 * kYBytes;  // 2 x 64 fp32
+    static constexpr uint32_t OFF_BAR = OFF_BETA + 512;        // mbarriers
+    static constexpr int kNumBars = 26;
     static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * kNumBars;  // abort flag, TMEM address
     static constexpr uint32_t kSmemBytes = OFF_MISC + 16 + 1024;  // + 1024-byte alignment slack
     static_assert(OFF_V % 1024 == 0 && OFF_TP % 1024 == 0 && OFF_SB % 1024 == 0, "tile alignment");
@@ -98,29 +88,24 @@ struct Layout {
 
 // mbarrier indices.  Every barrier has exactly one waiting role, which
 // consumes its phases in order, so a parity test can never see a phase two
-// ahead of the one it asks for.  B_FREE is waited on by the chunk group in
-// the fused form and by the producer (before it reloads [PT; Tm]) in the
-// split form.  Barriers indexed [2] belong to the chunk
+// ahead of the one it asks for.  Barriers indexed [2] belong to the chunk
 // group of that parity; [6] is (stage, group): chunk c uses c % 6.
 enum : int {
     B_KQ_FULL = 0,     // [6] q, k tiles landed               (producer -> chunk group)
-    B_KQ_EMPTY = 6,    // [4] stage's last reader done         (state MMA -> producer)
-    B_V_FULL = 10,     // [2] v tile landed (per v buffer)     (producer -> state group)
-    B_V_EMPTY = 12,    // [2] D1 MMAs done, v buffer free      (state MMA -> producer)
-    B_G_FULL = 14,     // [2] G = [K;Q] K^T done               (own commit)
-    B_PT_FULL = 16,    // [2] PT = P Tm done                   (own commit)
-    B_DW_FULL = 18,    // [2] DW = [PT;Tm] K done              (own commit)
-    B_QW_READY = 20,   // [2] [PT; Tm] and [Q'; -W] ready      (chunk group -> state group)
-    B_FREE = 22,       // [2] D1 MMAs read them; both free     (state MMA -> group or producer)
-    B_D1_FULL = 24,    // D1 done                              (own commit, state group)
-    B_S_READY = 26,    // S += K^T U' done                     (own commit, state group)
-    B_DRAIN = 28,      // [4] final drain of each MMA issuer
-    B_TP_FULL = 32,    // [2] split form: [PT; Tm] tile landed (producer -> chunk group)
+    B_KQ_EMPTY = 6,    // [3] stage's last reader done         (state MMA -> producer)
+    B_V_FULL = 9,      // v tile landed                        (producer -> state group)
+    B_V_EMPTY = 10,    // D1 MMAs done, v tile free            (state MMA -> producer)
+    B_G_FULL = 11,     // [2] G = [K;Q] K^T done               (own commit)
+    B_PT_FULL = 13,    // [2] PT = P Tm done                   (own commit)
+    B_DW_FULL = 15,    // [2] DW = [PT;Tm] K done              (own commit)
+    B_QW_READY = 17,   // [2] [PT; Tm] and [Q'; -W] ready      (chunk group -> state group)
+    B_FREE = 19,       // [2] D1 MMAs read them; both free     (state MMA -> chunk group)
+    B_D1_FULL = 21,    // D1 done                              (own commit, state group)
+    B_S_READY = 22,    // S += K^T U' done                     (own commit, state group)
+    B_DRAIN = 23,      // [3] final drain of each MMA issuer (state, group 0, group 1)
 };
-static_assert(B_TP_FULL + 2 <= kNumBars, "barrier count");
-// Chunk c waits on [K; Q] barrier c % kKQBars: one barrier per (stage, group) pair.
-template <bool kSplit>
-constexpr int kKQBars = Layout<kSplit>::kStages % 2 ? 2 * Layout<kSplit>::kStages : Layout<kSplit>::kStages;
+static_assert(B_DRAIN + 3 <= Layout::kNumBars, "barrier count");
+constexpr int kKQBars = 6;  // chunk c waits on [K; Q] barrier c % 6: one per (stage, group)
 
 // TMEM columns (512 allocated):
 //   S | D1 (O, U') | per chunk group g: [Q'; -W] bf16 (64), then G / PT (64)
@@ -252,17 +237,15 @@ __device__ __forceinline__ bool wg_wait(const Ctl& ctl, int b, uint32_t parity, 
     return !wg_sync_or(barid, !ok, n);
 }
 
-template <bool kSplit>
 struct Smem {
-    using L = Layout<kSplit>;
+    using L = Layout;
     uint32_t base;   // shared address of the 1024-aligned base
     uint8_t* gbase;  // generic pointer to it
     __device__ uint32_t kq(int c) const { return base + L::OFF_KQ + (uint32_t)(c % L::kStages) * kStageKQ; }
     __device__ uint32_t tp(int g) const { return base + L::OFF_TP + (uint32_t)g * kTile; }
-    __device__ uint32_t v(int c) const { return base + L::OFF_V + (uint32_t)(c % L::kVBufs) * kTile; }
+    __device__ uint32_t v() const { return base + L::OFF_V; }
     __device__ uint32_t sb() const { return base + L::OFF_SB; }
-    // o tile: its own buffer in the split form, the spent S operand's upper half otherwise
-    __device__ uint32_t otile() const { return base + (kSplit ? L::OFF_O : L::OFF_SB + 16384u); }
+    __device__ uint32_t otile() const { return base + L::OFF_SB + 16384u; }  // the spent S operand's upper half
     __device__ float* x(int g) const {
         return reinterpret_cast<float*>(gbase + L::OFF_X + (uint32_t)g * kXBytes);
     }
@@ -482,17 +465,14 @@ __device__ __forceinline__ void solve_unit_lower64_mma(float* X, float* Ys, int 
 }
 
 // ----------------------------------------------------------------- roles
-// TMA producer (one thread).  Streams [K; Q] into the stage ring, v into its
-// single buffer and, in the split form, each chunk's [PT; Tm] tile from the
-// workspace into its chunk group's buffer once the state group has released it.
-template <bool kSplit>
-__device__ void producer_role(const Ctl& ctl, const Smem<kSplit>& sm, const CUtensorMap* tm_q,
-                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                              const CUtensorMap* tm_ws, int bh, int nchunks) {
-    constexpr int kS = Layout<kSplit>::kStages, kF = kKQBars<kSplit>, kVB = Layout<kSplit>::kVBufs;
-    int nkq = 0, nv = 0, ntp = kSplit ? 0 : nchunks;
+// TMA producer (one thread): [K; Q] into the stage ring and v into its buffer.
+__device__ void producer_role(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q,
+                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, int bh,
+                              int nchunks) {
+    constexpr int kS = Layout::kStages, kF = kKQBars;
+    int nkq = 0, nv = 0;
     long long t0 = clock64();
-    while ((nkq < nchunks || nv < nchunks || ntp < nchunks) && !ctl.aborted()) {
+    while ((nkq < nchunks || nv < nchunks) && !ctl.aborted()) {
         bool progressed = false;
         if (nkq < nchunks &&
             (nkq < kS ||
@@ -513,30 +493,17 @@ __device__ void producer_role(const Ctl& ctl, const Smem<kSplit>& sm, const CUte
             ++nkq;
             progressed = true;
         }
-        if (nv < nchunks &&
-            (nv < kVB ||
-             mbar_test_wait(ctl.bar(B_V_EMPTY + nv % kVB), (uint32_t)(nv / kVB - 1) & 1u))) {
-            const uint32_t bar = ctl.bar(B_V_FULL + nv % kVB);
+        if (nv < nchunks && (nv < 1 || mbar_test_wait(ctl.bar(B_V_EMPTY), (uint32_t)(nv - 1) & 1u))) {
+            const uint32_t bar = ctl.bar(B_V_FULL);
             mbar_arrive_expect_tx(bar, 2 * 8192);
-            tma_load_3d(sm.v(nv), tm_v, bar, 0, nv * kC, bh);
-            tma_load_3d(sm.v(nv) + 8192, tm_v, bar, 64, nv * kC, bh);
-            if (nv + kVB < nchunks) {  // warm L2 for this buffer's next tile
-                tma_prefetch_l2_3d(tm_v, 0, (nv + kVB) * kC, bh);
-                tma_prefetch_l2_3d(tm_v, 64, (nv + kVB) * kC, bh);
+            tma_load_3d(sm.v(), tm_v, bar, 0, nv * kC, bh);
+            tma_load_3d(sm.v() + 8192, tm_v, bar, 64, nv * kC, bh);
+            if (nv + 1 < nchunks) {  // the v tile is single-buffered: warm L2 for the next one
+                tma_prefetch_l2_3d(tm_v, 0, (nv + 1) * kC, bh);
+                tma_prefetch_l2_3d(tm_v, 64, (nv + 1) * kC, bh);
             }
             ++nv;
             progressed = true;
-        }
-        if (kSplit && ntp < nchunks) {
-            const int g = ntp & 1, it = ntp >> 1;
-            if (it == 0 || mbar_test_wait(ctl.bar(B_FREE + g), (uint32_t)(it - 1) & 1u)) {
-                const uint32_t bar = ctl.bar(B_TP_FULL + g);
-                mbar_arrive_expect_tx(bar, kTile);
-                tma_load_3d(sm.tp(g), tm_ws, bar, 0, ntp * 128, bh);
-                if (ntp + 2 < nchunks) tma_prefetch_l2_3d(tm_ws, 0, (ntp + 2) * 128, bh);
-                ++ntp;
-                progressed = true;
-            }
         }
         if (progressed) {
             t0 = clock64();
@@ -550,15 +517,7 @@ __device__ void producer_role(const Ctl& ctl, const Smem<kSplit>& sm, const CUte
         const int n_b = (nkq - b + kF - 1) / kF;  // loads that completed on barrier b
         if (n_b > 0) mbar_wait(ctl.bar(B_KQ_FULL + b), (uint32_t)(n_b - 1) & 1u, kTimeoutNs);
     }
-    for (int b = 0; b < kVB; ++b) {
-        const int n_b = (nv - b + kVB - 1) / kVB;
-        if (n_b > 0) mbar_wait(ctl.bar(B_V_FULL + b), (uint32_t)(n_b - 1) & 1u, kTimeoutNs);
-    }
-    if (kSplit)
-        for (int g = 0; g < 2; ++g) {
-            const int n_g = (ntp - g + 1) / 2;
-            if (n_g > 0) mbar_wait(ctl.bar(B_TP_FULL + g), (uint32_t)(n_g - 1) & 1u, kTimeoutNs);
-        }
+    if (nv > 0) mbar_wait(ctl.bar(B_V_FULL), (uint32_t)(nv - 1) & 1u, kTimeoutNs);
 }
 
 // Lets everything a thread issued to the tensor core finish (bounded), so
@@ -576,22 +535,16 @@ __device__ __forceinline__ void issue_vpart(uint32_t tmem, uint32_t tp, uint32_t
                     sw128_desc(v + 2048u * kk, 8192, 1024), IDESC_KB, kk > 0);
 }
 
-// State role: thread ts owns state row t = ts % 128 (TMEM lane t).  In the
-// fused form one warpgroup (warps 4-7) converts all 128 columns; in the split
-// form a second warpgroup (warps 0-3, ts >= 128) takes the dv 64-127 half of
-// every conversion.  Thread ts = 0 issues the state MMAs.
-template <bool kSplit>
-__device__ void state_role_body(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t tmem, int ts,
+// State group (warps 4-7): thread t owns state row t (TMEM lane t); thread 0
+// issues the state MMAs.
+__device__ void state_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                                 const float* __restrict__ S0, float* __restrict__ S_T,
                                 const CUtensorMap* tm_o, int bh, int nchunks) {
-    constexpr int kBar = 1, kN = kSplit ? 256 : 128, kHalves = kSplit ? 1 : 2;
-    constexpr int kVB = Layout<kSplit>::kVBufs;
-    const int t = ts & 127, h0 = kSplit ? (ts >> 7) : 0;  // row; first dv half handled
+    constexpr int kBar = 1;
     const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
     // S0 (or zeros) into TMEM.
 #pragma unroll
-    for (int hh = 0; hh < kHalves; ++hh) {
-        const int h = h0 + hh;
+    for (int h = 0; h < 2; ++h) {
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
             uint32_t r[32];
@@ -619,57 +572,52 @@ __device__ void state_role_body(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t
     for (int c = 0; c < nchunks; ++c) {
         const int g = c & 1;
         const uint32_t tp = sm.tp(g), qw = tmem + COL_GRP + 128u * (uint32_t)g;
-        // S += K^T U' of the previous chunk done (and, where the o tile shares
-        // the S operand's buffer, that tile read out by TMA).
+        // S += K^T U' of the previous chunk done, and its o tile (in the S
+        // operand's buffer) read out by TMA.
         if (c > 0) {
             bool ok0 = true;
-            if (ts == 0) {
+            if (t == 0) {
                 ok0 = ctl.wait(B_S_READY, (uint32_t)(c - 1));
-                if (!kSplit) bulk_wait_group_read0();
+                bulk_wait_group_read0();
             }
-            if (wg_sync_or(kBar, !ok0, kN)) return;
+            if (wg_sync_or(kBar, !ok0)) return;
         }
         tc_fence_after_sync();
         // S (fp32) -> bf16 operand tile: dv halves as regions, row t.
 #pragma unroll
-        for (int hh = 0; hh < kHalves; ++hh) {
-            const int h = h0 + hh;
+        for (int h = 0; h < 2; ++h) {
             float x[64];
             tmem_ld64f(tmem + lane_base + COL_S + 64u * h, x);
             store_row64_bf16(sm.sb() + (uint32_t)h * 16384u, t, x);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
-        wg_sync(kBar, kN);
+        wg_sync(kBar);
         // D1 (+)= [PT; Tm] V, D1 += [Q'; -W] S once the chunk group has handed its chunk over.
         bool ok = true;
-        if (ts == 0) {
-            ok = ctl.wait(B_QW_READY + g, (uint32_t)(c >> 1)) &&
-                 ctl.wait(B_V_FULL + c % kVB, (uint32_t)(c / kVB));
+        if (t == 0) {
+            ok = ctl.wait(B_QW_READY + g, (uint32_t)(c >> 1)) && ctl.wait(B_V_FULL, (uint32_t)c);
             if (ok) {
                 tc_fence_after_sync();
-                if (!vnext) issue_vpart(tmem, tp, sm.v(c));
+                if (!vnext) issue_vpart(tmem, tp, sm.v());
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16_ts(tmem + COL_D1, qw + 8u * kk,
                                 sw128_desc(sm.sb() + 2048u * kk, 16384, 1024), IDESC_KB, 1);
                 mma_commit(ctl.bar(B_D1_FULL));
-                mma_commit(ctl.bar(B_V_EMPTY + c % kVB));
+                mma_commit(ctl.bar(B_V_EMPTY));
                 mma_commit(ctl.bar(B_FREE + g));
                 ok = ctl.wait(B_D1_FULL, (uint32_t)c);
-                // a separate o tile may still be read by the previous chunk's store
-                if (kSplit) bulk_wait_group_read0();
             }
         }
-        if (wg_sync_or(kBar, !ok, kN)) return;
+        if (wg_sync_or(kBar, !ok)) return;
         tc_fence_after_sync();
         // The S operand is spent: rows 64-127 (U') into its lower 16 KB, rows
         // 0-63 (o) into the o tile.
         {
             const uint32_t dst = t < 64 ? sm.otile() : sm.sb();
 #pragma unroll
-            for (int hh = 0; hh < kHalves; ++hh) {
-                const int h = h0 + hh;
+            for (int h = 0; h < 2; ++h) {
                 float x[64];
                 tmem_ld64f(tmem + lane_base + COL_D1 + 64u * h, x);
                 store_row64_bf16(dst + (uint32_t)h * 8192u, t & 63, x);
@@ -677,8 +625,8 @@ __device__ void state_role_body(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
-        wg_sync(kBar, kN);
-        if (ts == 0) {
+        wg_sync(kBar);
+        if (t == 0) {
             // S += K^T U'
             const uint32_t kq = sm.kq(c);
             tc_fence_after_sync();
@@ -687,7 +635,7 @@ __device__ void state_role_body(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t
                 mma_bf16_ss(tmem + COL_S, sw128_desc(kq + 2048u * kk, kRegKQ, 1024),
                             sw128_desc(sm.sb() + 2048u * kk, 8192, 1024), IDESC_MM, 1);
             mma_commit(ctl.bar(B_S_READY));
-            mma_commit(ctl.bar(B_KQ_EMPTY + c % Layout<kSplit>::kStages));
+            mma_commit(ctl.bar(B_KQ_EMPTY + c % Layout::kStages));
             // o tile out (rows past the end of the sequence are clipped)
             tma_store_3d(tm_o, sm.otile(), 0, c * kC, bh);
             tma_store_3d(tm_o, sm.otile() + 8192u, 64, c * kC, bh);
@@ -698,16 +646,15 @@ __device__ void state_role_body(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t
             const int cn = c + 1;
             vnext = cn < nchunks &&
                     mbar_test_wait(ctl.bar(B_QW_READY + (cn & 1)), (uint32_t)(cn >> 1) & 1u) &&
-                    mbar_test_wait(ctl.bar(B_V_FULL + cn % kVB), (uint32_t)(cn / kVB) & 1u);
-            if (vnext) issue_vpart(tmem, sm.tp(cn & 1), sm.v(cn));
+                    mbar_test_wait(ctl.bar(B_V_FULL), (uint32_t)cn & 1u);
+            if (vnext) issue_vpart(tmem, sm.tp(cn & 1), sm.v());
         }
     }
-    if (nchunks > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(nchunks - 1), ts, kBar, kN)) return;
+    if (nchunks > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(nchunks - 1), t, kBar)) return;
     tc_fence_after_sync();
     if (S_T) {
 #pragma unroll
-        for (int hh = 0; hh < kHalves; ++hh) {
-            const int h = h0 + hh;
+        for (int h = 0; h < 2; ++h) {
             float x[64];
             tmem_ld64f(tmem + lane_base + COL_S + 64u * h, x);
             float4* dst = reinterpret_cast<float4*>(S_T + ((size_t)bh * kD + t) * kD + 64 * h);
@@ -718,12 +665,11 @@ __device__ void state_role_body(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t
     }
 }
 
-template <bool kSplit>
-__device__ void state_role(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t tmem, int ts,
+__device__ void state_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                            const float* __restrict__ S0, float* __restrict__ S_T,
                            const CUtensorMap* tm_o, int bh, int nchunks) {
-    state_role_body<kSplit>(ctl, sm, tmem, ts, S0, S_T, tm_o, bh, nchunks);
-    if (ts == 0) {
+    state_role_body(ctl, sm, tmem, t, S0, S_T, tm_o, bh, nchunks);
+    if (t == 0) {
         drain_mmas(ctl, B_DRAIN + 0);
         bulk_wait_group0();  // o tiles written
     }
@@ -787,10 +733,10 @@ __device__ __forceinline__ void issue_dw(uint32_t tmem, uint32_t colQW, uint32_t
 // Fused form, chunk group g (0: even chunks, warps 8-11; 1: odd chunks,
 // warps 12-15); thread 0 issues the group's MMAs.  Iteration `it` handles
 // chunk c = g + 2 it.
-__device__ void chunk_role_body(const Ctl& ctl, const Smem<false>& sm, uint32_t tmem, int t,
+__device__ void chunk_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                                 int g, const __nv_bfloat16* __restrict__ beta, int bh, int T,
                                 int nchunks) {
-    constexpr int kF = kKQBars<false>;
+    constexpr int kF = kKQBars;
     const int barid = 2 + g;
     const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
     const uint32_t colQW = COL_GRP + 128u * (uint32_t)g, colG = colQW + 64u;
@@ -909,118 +855,24 @@ __device__ void chunk_role_body(const Ctl& ctl, const Smem<false>& sm, uint32_t 
     }
 }
 
-// Split form: [PT; Tm] arrives from the workspace, so one chunk group
-// (warps 8-11) forms the [Q'; -W] operand of every chunk, alternating between
-// the two buffer sets by chunk parity.  The group writes [-Q; 0] into the
-// set's 128 accumulator columns and adds [PT; Tm] K on the tensor cores:
-//     DW' = [-Q; 0] + [PT; Tm] K = [PT K - Q; W] = -[Q'; -W],
-// which the epilogue negates and packs.
-__device__ void chunk_role_split_body(const Ctl& ctl, const Smem<true>& sm, uint32_t tmem, int t,
-                                      int nchunks) {
-    constexpr int kF = kKQBars<true>;
-    const int barid = 2, row = t & 63;
-    const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
-    for (int c = 0; c < nchunks; ++c) {
-        const int g = c & 1, it = c >> 1;
-        const uint32_t kq = sm.kq(c), colQW = COL_GRP + 128u * (uint32_t)g;
-        bool ok = true;
-        if (t == 0) {
-            // The [PT; Tm] tile is loaded only after the state group released
-            // this buffer set, so its [Q'; -W] columns are free as well.
-            ok = ctl.wait(B_KQ_FULL + c % kF, (uint32_t)(c / kF)) &&
-                 ctl.wait(B_TP_FULL + g, (uint32_t)it);
-        }
-        if (wg_sync_or(barid, !ok)) return;
-        tc_fence_after_sync();
-#pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {  // -Q (rows 0-63) or 0 (rows 64-127), dk quarter qd
-            uint32_t r[32];
-            if (t < 64) {
-                const uint32_t region = kq + (uint32_t)(qd >> 1) * kRegKQ;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const uint4 qv = ld_shared_v4(region + sw128(64 + row, (qd & 1) * 4 + cc));
-                    const float2 a0 = unpack_bf16(qv.x), a1 = unpack_bf16(qv.y),
-                                 a2 = unpack_bf16(qv.z), a3 = unpack_bf16(qv.w);
-                    r[8 * cc + 0] = __float_as_uint(-a0.x);
-                    r[8 * cc + 1] = __float_as_uint(-a0.y);
-                    r[8 * cc + 2] = __float_as_uint(-a1.x);
-                    r[8 * cc + 3] = __float_as_uint(-a1.y);
-                    r[8 * cc + 4] = __float_as_uint(-a2.x);
-                    r[8 * cc + 5] = __float_as_uint(-a2.y);
-                    r[8 * cc + 6] = __float_as_uint(-a3.x);
-                    r[8 * cc + 7] = __float_as_uint(-a3.y);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = 0u;
-            }
-            tmem_st32(tmem + lane_base + colQW + 32u * (uint32_t)qd, r);
-        }
-        tmem_wait_st();
-        tc_fence_before_sync();
-        wg_sync(barid);
-        if (t == 0) {
-            tc_fence_after_sync();
-            const uint32_t tp = sm.tp(g);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + colQW, sw128_desc(tp + 32u * kk, 16, 1024),
-                            sw128_desc(kq + 2048u * kk, kRegKQ, 1024), IDESC_KB, 1);
-            mma_commit(ctl.bar(B_DW_FULL));
-            ok = ctl.wait(B_DW_FULL, (uint32_t)c);
-        }
-        if (wg_sync_or(barid, !ok)) return;
-        tc_fence_after_sync();
-        {   // -DW' as bf16 pairs into the set's first 64 columns (all of DW' read first)
-            uint32_t hi[32], lo[32];
-#pragma unroll
-            for (int qd = 0; qd < 4; ++qd) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + colQW + 32u * (uint32_t)qd, r);
-                tmem_wait_ld();
-                uint32_t* pk = (qd < 2 ? lo : hi) + 16 * (qd & 1);
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16(-__uint_as_float(r[2 * e]), -__uint_as_float(r[2 * e + 1]));
-            }
-            tmem_st32(tmem + lane_base + colQW, lo);
-            tmem_st32(tmem + lane_base + colQW + 32u, hi);
-            tmem_wait_st();
-        }
-        tc_fence_before_sync();
-        wg_sync(barid);
-        if (t == 0) mbar_arrive(ctl.bar(B_QW_READY + g));
-    }
-}
-
-template <bool kSplit>
-__device__ void chunk_role(const Ctl& ctl, const Smem<kSplit>& sm, uint32_t tmem, int t, int g,
+__device__ void chunk_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int g,
                            const __nv_bfloat16* __restrict__ beta, int bh, int T, int nchunks) {
-    if constexpr (kSplit)
-        chunk_role_split_body(ctl, sm, tmem, t, nchunks);
-    else
-        chunk_role_body(ctl, sm, tmem, t, g, beta, bh, T, nchunks);
-    if (t == 0) drain_mmas(ctl, B_DRAIN + 2 + g);
+    chunk_role_body(ctl, sm, tmem, t, g, beta, bh, T, nchunks);
+    if (t == 0) drain_mmas(ctl, B_DRAIN + 1 + g);
 }
 
-// Sequence kernel: one CTA per (batch, head), the whole sequence in order,
-// 16 warps.  Fused form: producer 0, TMEM owner 1, state 4-7, chunk groups
-// 8-11 and 12-15.  Split form: state 4-7 and 0-3 (which share its
-// conversions by dv halves), chunk group 8-11, producer 12, TMEM owner 13.
-template <bool kSplit>
-constexpr int kSeqThreads = 512;
-template <bool kSplit>
-__global__ void __launch_bounds__(kSeqThreads<kSplit>, 1)
+// Fused kernel: one CTA of 16 warps per (batch, head), the whole sequence in
+// order: producer 0, TMEM owner 1, state 4-7, chunk groups 8-11 and 12-15.
+__global__ void __launch_bounds__(512, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                const __grid_constant__ CUtensorMap tm_ws, const __nv_bfloat16* __restrict__ beta,
-                const float* __restrict__ S0, float* __restrict__ S_T, int T) {
-    using L = Layout<kSplit>;
+                const __nv_bfloat16* __restrict__ beta, const float* __restrict__ S0,
+                float* __restrict__ S_T, int T) {
+    using L = Layout;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
-    const Smem<kSplit> sm{base, smem_raw + (base - raw_addr)};
+    const Smem sm{base, smem_raw + (base - raw_addr)};
     int* const misc = reinterpret_cast<int*>(sm.gbase + L::OFF_MISC);
     const Ctl ctl{base + L::OFF_BAR, reinterpret_cast<volatile int*>(misc)};
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
@@ -1031,16 +883,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     if (tid == 0) {
         misc[0] = 0;
-        for (int b = 0; b < kNumBars; ++b) mbar_init(ctl.bar(b), 1);
+        for (int b = 0; b < L::kNumBars; ++b) mbar_init(ctl.bar(b), 1);
         fence_mbar_init();
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_o);
-        if (kSplit) prefetch_tensormap(&tm_ws);
     }
-    constexpr int kProdWarp = kSplit ? 12 : 0, kTmemWarp = kSplit ? 13 : 1;
-    if (warp == kTmemWarp) {
+    if (warp == 1) {
         tmem_alloc(smem_addr(tmem_holder), 512);
         tmem_relinquish();
     }
@@ -1049,19 +899,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == kProdWarp) {
-        if (lane == 0) producer_role<kSplit>(ctl, sm, &tm_q, &tm_k, &tm_v, &tm_ws, bh, nchunks);
-    } else if (warp < 8 && (kSplit || warp >= 4)) {
-        // split form: warps 4-7 convert dv 0-63, warps 0-3 dv 64-127
-        state_role<kSplit>(ctl, sm, tmem, warp >= 4 ? tid - 128 : tid + 128, S0, S_T, &tm_o, bh,
-                           nchunks);
-    } else if (warp >= 8 && warp < (kSplit ? 12 : 16)) {
+    if (warp == 0) {
+        if (lane == 0) producer_role(ctl, sm, &tm_q, &tm_k, &tm_v, bh, nchunks);
+    } else if (warp >= 4 && warp < 8) {
+        state_role(ctl, sm, tmem, tid - 128, S0, S_T, &tm_o, bh, nchunks);
+    } else if (warp >= 8) {
         const int g = (warp - 8) >> 2;
-        chunk_role<kSplit>(ctl, sm, tmem, tid - 256 - 128 * g, g, beta, bh, T, nchunks);
+        chunk_role(ctl, sm, tmem, tid - 256 - 128 * g, g, beta, bh, T, nchunks);
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == kTmemWarp) {
+    if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, 512);
     }
@@ -1727,12 +1575,10 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
             mq, mk, mv, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, T);
         return cudaGetLastError();
     }
-    if ((err = cudaFuncSetAttribute(chunk_tc_kernel<false>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Layout<false>::kSmemBytes)) != cudaSuccess)
+    if ((err = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Layout::kSmemBytes)) != cudaSuccess)
         return err;
-    chunk_tc_kernel<false><<<BH, kSeqThreads<false>, Layout<false>::kSmemBytes, stream>>>(
-        mq, mk, mv, mo, mws, b, S0, S_T, T);
+    chunk_tc_kernel<<<BH, 512, Layout::kSmemBytes, stream>>>(mq, mk, mv, mo, b, S0, S_T, T);
     return cudaGetLastError();
 }
 

@@ -338,7 +338,7 @@ def run_ours(args, rank, world, local):
     # A "launch" here is one dn_chunk_fwd call; on the two-pass path that is
     # the prepare kernel and the sequence kernel back to back.
     if split:
-        kname, knames = "chunk_prep + chunk_tc (split)", ["chunk_prep", "chunk_tc_split"]
+        kname, knames = "chunk_prep + chunk_scan (two passes)", ["chunk_prep", "chunk_scan"]
     elif tc:
         kname, knames = "chunk_tc (fused)", ["chunk_tc_fused"]
     else:

@@ -66,6 +66,8 @@ def _load():
                                           ctypes.c_long, ctypes.c_long,
                                           ctypes.c_int]
         lib.dn_oracle_forward.restype = ctypes.c_int
+        lib.dn_oracle_backward.argtypes = [dp] * 12 + [ctypes.c_long] * 4 + [ctypes.c_int]
+        lib.dn_oracle_backward.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -137,3 +139,54 @@ def recurrent_step(q, k, v, beta, S, nthreads: int | None = None):
     o, S_new = forward(q[:, :, None, :], k[:, :, None, :], v[:, :, None, :],
                        beta[:, :, None], S, nthreads=nthreads)
     return o[:, :, 0, :], S_new
+
+
+def backward(q, k, v, beta, dO, S0=None, dS_T=None, nthreads: int | None = None,
+             max_bytes: int = 4 << 30):
+    """Gradients of L = <dO, o> + <dS_T, S_T> for the recurrence run by
+    ``forward`` (its exact vector-Jacobian product, fp64).
+
+    Args:
+      q, k, v, beta, S0: as for ``forward``.
+      dO: ``[B, H, T, dv]`` gradient of the outputs.
+      dS_T: ``[B, H, dk, dv]`` gradient of the final state, or None (zeros).
+      nthreads: OpenMP threads; lowered so that the per-thread copies of the
+        T + 1 states of one head stay within ``max_bytes`` in total.
+
+    Returns ``(dq, dk, dv, dbeta, dS0)`` as fp64 numpy arrays shaped like
+    ``q, k, v, beta`` and the state.
+    """
+    q, k, v, beta, dO = _f64(q), _f64(k), _f64(v), _f64(beta), _f64(dO)
+    B, H, T, dk = q.shape
+    dv = v.shape[3]
+    if k.shape != q.shape or v.shape[:3] != (B, H, T) or beta.shape != (B, H, T):
+        raise ValueError("q, k must be [B,H,T,dk], v [B,H,T,dv] and beta [B,H,T]")
+    if dO.shape != v.shape:
+        raise ValueError("dO must be shaped like v")
+    S0a = None if S0 is None else _f64(S0)
+    dSa = None if dS_T is None else _f64(dS_T)
+    for name, a in (("S0", S0a), ("dS_T", dSa)):
+        if a is not None and a.shape != (B, H, dk, dv):
+            raise ValueError(f"{name} must be [B,H,dk,dv]")
+    dq = np.zeros_like(q)
+    dkk = np.zeros_like(k)
+    dvv = np.zeros_like(v)
+    db = np.zeros_like(beta)
+    dS0 = np.zeros((B, H, dk, dv), dtype=np.float64)
+    if B * H == 0:
+        return dq, dkk, dvv, db, dS0
+    if T == 0:
+        if dSa is not None:
+            dS0[...] = dSa
+        return dq, dkk, dvv, db, dS0
+    n = host_cores() if nthreads is None else int(nthreads)
+    per_thread = 8 * dk * dv * (T + 2)
+    n = max(1, min(n, max_bytes // max(per_thread, 1)))
+    null = ctypes.POINTER(ctypes.c_double)()
+    rc = _load().dn_oracle_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(S0a) if S0a is not None else null,
+        _ptr(dO), _ptr(dSa) if dSa is not None else null, _ptr(dq), _ptr(dkk), _ptr(dvv),
+        _ptr(db), _ptr(dS0), B * H, T, dk, dv, n)
+    if rc != 0:
+        raise MemoryError("oracle could not allocate its state history")
+    return dq, dkk, dvv, db, dS0

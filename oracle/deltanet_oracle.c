@@ -104,3 +104,130 @@ int dn_oracle_forward(const double *q, const double *k, const double *v,
     }
     return failed ? -1 : 0;
 }
+
+/*
+ * Gradient of the recurrence (its exact vector-Jacobian product), for the
+ * training backward pass that "Hardware-efficient implementation" (section 3
+ * of paperlayer.ai/abs/2406.06484v6) runs after the forward: given the
+ * upstream gradients dO of o and dS_T of S_T, it returns dq, dk, dv, dbeta
+ * and dS_0 of L = <dO, o> + <dS_T, S_T>.
+ *
+ * Reverse mode through each token, with G = dL/dS_t (pages' orientation):
+ *   o_t = S_t q_t                 G += dO_t q_t^T,   dq_t = S_t^T dO_t
+ *   S_t = S_{t-1} + u_t k_t^T     du_t = G k_t,      dk_t (part) = G^T u_t
+ *   u_t = beta_t e_t,             e_t = v_t - S_{t-1} k_t
+ *                                 dv_t = beta_t du_t
+ *                                 dbeta_t = <du_t, e_t>
+ *                                 dk_t -= beta_t S_{t-1}^T du_t
+ *                                 G  -= beta_t du_t k_t^T   (then G = dL/dS_{t-1})
+ * Every state S_0 .. S_T of the head is kept (states[t] = S_t).
+ */
+static void grad_one_head(const double *q, const double *k, const double *v,
+                          const double *beta, const double *S0, const double *dO,
+                          const double *dST, double *dq, double *dk, double *dvv,
+                          double *dbeta, double *dS0, long T, long dk_, long dv,
+                          double *states, double *G, double *e, double *du)
+{
+    const size_t n = (size_t)dk_ * (size_t)dv;
+    for (size_t x = 0; x < n; ++x)
+        states[x] = S0 ? S0[x] : 0.0;
+    for (long t = 0; t < T; ++t) {  /* forward, keeping S_t */
+        const double *Sp = states + (size_t)t * n;
+        double *St = states + (size_t)(t + 1) * n;
+        const double *kt = k + t * dk_;
+        for (long j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (long i = 0; i < dk_; ++i)
+                acc += S_AT(Sp, dv, j, i) * kt[i];
+            e[j] = v[t * dv + j] - acc;
+        }
+        for (long j = 0; j < dv; ++j)
+            for (long i = 0; i < dk_; ++i)
+                S_AT(St, dv, j, i) = S_AT(Sp, dv, j, i) + beta[t] * e[j] * kt[i];
+    }
+    for (size_t x = 0; x < n; ++x)
+        G[x] = dST ? dST[x] : 0.0;
+    for (long t = T - 1; t >= 0; --t) {
+        const double *Sp = states + (size_t)t * n;
+        const double *St = states + (size_t)(t + 1) * n;
+        const double *kt = k + t * dk_, *qt = q + t * dk_, *dOt = dO + t * dv;
+        const double bt = beta[t];
+        /* read: o_t = S_t q_t */
+        for (long j = 0; j < dv; ++j)
+            for (long i = 0; i < dk_; ++i)
+                S_AT(G, dv, j, i) += dOt[j] * qt[i];
+        for (long i = 0; i < dk_; ++i) {
+            double acc = 0.0;
+            for (long j = 0; j < dv; ++j)
+                acc += S_AT(St, dv, j, i) * dOt[j];
+            dq[t * dk_ + i] = acc;
+        }
+        /* write: S_t = S_{t-1} + beta_t e_t k_t^T */
+        for (long j = 0; j < dv; ++j) {
+            double a = 0.0, p = 0.0;
+            for (long i = 0; i < dk_; ++i) {
+                a += S_AT(G, dv, j, i) * kt[i];
+                p += S_AT(Sp, dv, j, i) * kt[i];
+            }
+            du[j] = a;
+            e[j] = v[t * dv + j] - p;
+        }
+        double db = 0.0;
+        for (long j = 0; j < dv; ++j) {
+            dvv[t * dv + j] = bt * du[j];
+            db += du[j] * e[j];
+        }
+        dbeta[t] = db;
+        for (long i = 0; i < dk_; ++i) {
+            double acc = 0.0;
+            for (long j = 0; j < dv; ++j)
+                acc += S_AT(G, dv, j, i) * bt * e[j] - bt * S_AT(Sp, dv, j, i) * du[j];
+            dk[t * dk_ + i] = acc;
+        }
+        for (long j = 0; j < dv; ++j)
+            for (long i = 0; i < dk_; ++i)
+                S_AT(G, dv, j, i) -= bt * du[j] * kt[i];
+    }
+    for (size_t x = 0; x < n; ++x)
+        dS0[x] = G[x];
+}
+
+/*
+ * Gradients for all BH (batch, head) pairs, on nthreads OpenMP threads.
+ * S0 and dST may be NULL (zeros).  Layouts as for dn_oracle_forward; dO is
+ * [BH][T][dv], the outputs dq, dk [BH][T][dk], dv [BH][T][dv], dbeta
+ * [BH][T], dS0 [BH][dk][dv].  Returns 0, or -1 if scratch memory could not
+ * be had.
+ */
+int dn_oracle_backward(const double *q, const double *k, const double *v,
+                       const double *beta, const double *S0, const double *dO,
+                       const double *dST, double *dq, double *dk, double *dvv,
+                       double *dbeta, double *dS0, long BH, long T, long dk_,
+                       long dv, int nthreads)
+{
+    int failed = 0;
+    const size_t n = (size_t)dk_ * (size_t)dv;
+    if (nthreads < 1)
+        nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+    {
+        double *states = (double *)malloc(sizeof(double) * (n * (size_t)(T + 1) + n + 2 * (size_t)dv + 2));
+        if (!states) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long h = 0; h < BH; ++h) {
+            if (!states)
+                continue;
+            double *G = states + n * (size_t)(T + 1);
+            double *e = G + n, *du = e + dv + 1;
+            grad_one_head(q + h * T * dk_, k + h * T * dk_, v + h * T * dv, beta + h * T,
+                          S0 ? S0 + h * n : NULL, dO + h * T * dv, dST ? dST + h * n : NULL,
+                          dq + h * T * dk_, dk + h * T * dk_, dvv + h * T * dv, dbeta + h * T,
+                          dS0 + h * n, T, dk_, dv, states, G, e, du);
+        }
+        free(states);
+    }
+    return failed ? -1 : 0;
+}

@@ -8,6 +8,9 @@ the computation runs in the library's sm_103a kernels.
     chunk_fwd(q, k, v, beta, initial_state=None, output_final_state=True)
         -> (o, final_state)          # training / prefill, chunkwise form
     recurrent_step(q, k, v, beta, state) -> o   # decoding, state in place
+    chunk_bwd(q, k, v, beta, d_o, initial_state=None, d_final_state=None)
+        -> (d_q, d_k, d_v, d_beta, d_initial_state)   # training backward
+    DeltaRule.apply(q, k, v, beta, initial_state)     # autograd: (o, final_state)
 
 Shapes: q, k ``[B, H, T, dk]``; v ``[B, H, T, dv]``; beta ``[B, H, T]``;
 state ``[B, H, dk, dv]`` fp32 (the pages' dv x dk state, transposed).  For a
@@ -20,8 +23,8 @@ import torch
 from ._lib import (DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05, DN_BF16, DN_F32,
                    DeltaNetError, check, header_symbols, lib_path, load)
 
-__all__ = ["chunk_fwd", "recurrent_step", "DeltaNetError", "load", "lib_path",
-           "header_symbols", "ALGOS"]
+__all__ = ["chunk_fwd", "chunk_bwd", "recurrent_step", "DeltaRule", "DeltaNetError", "load",
+           "lib_path", "header_symbols", "ALGOS"]
 
 ALGOS = {"auto": DN_ALGO_AUTO, "simt": DN_ALGO_SIMT, "tcgen05": DN_ALGO_TCGEN05}
 _DT = {torch.float32: DN_F32, torch.bfloat16: DN_BF16}
@@ -140,3 +143,75 @@ def recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torc
                                     state.data_ptr(), out.data_ptr(), B, H, dk, dv, dt,
                                     _stream_handle(dev)))
     return out
+
+
+def chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+              d_o: torch.Tensor, initial_state: torch.Tensor | None = None,
+              d_final_state: torch.Tensor | None = None, chunk_size: int = 64,
+              workspace: torch.Tensor | None = None):
+    """Gradients of the chunkwise forward (``dn_chunk_bwd``).
+
+    Returns ``(d_q, d_k, d_v, d_beta, d_initial_state)`` for
+    L = <d_o, o> + <d_final_state, final_state>; ``d_initial_state`` is fp32
+    ``[B, H, dk, dv]`` (zeros-based even when ``initial_state`` is None).
+    ``workspace``: a uint8 CUDA tensor of at least
+    ``dn_chunk_bwd_workspace_bytes`` bytes, or None to allocate one.
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("d_o", d_o)):
+        _check_cuda(name, t, dev)
+    dt = _dtype_code(q)
+    if not (k.dtype == v.dtype == beta.dtype == d_o.dtype == q.dtype):
+        raise TypeError("q, k, v, beta and d_o must share one dtype")
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or d_o.shape != v.shape:
+        raise ValueError("q, k must be [B,H,T,dk]; v and d_o [B,H,T,dv]")
+    B, H, T, dk = q.shape
+    dv = v.shape[3]
+    if tuple(v.shape[:3]) != (B, H, T) or tuple(beta.shape) != (B, H, T):
+        raise ValueError("v must be [B,H,T,dv] and beta [B,H,T]")
+    for name, t in (("initial_state", initial_state), ("d_final_state", d_final_state)):
+        if t is not None:
+            _check_cuda(name, t, dev)
+            if t.dtype != torch.float32 or tuple(t.shape) != (B, H, dk, dv):
+                raise ValueError(f"{name} must be float32 [B,H,dk,dv]")
+    lib = load()
+    need = lib.dn_chunk_bwd_workspace_bytes(B, H, T, dk, dv, chunk_size, dt)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    else:
+        _check_cuda("workspace", workspace, dev)
+    d_q, d_k = torch.empty_like(q), torch.empty_like(k)
+    d_v, d_beta = torch.empty_like(v), torch.empty_like(beta)
+    d_S0 = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        check(lib.dn_chunk_bwd(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(),
+            initial_state.data_ptr() if initial_state is not None else None, d_o.data_ptr(),
+            d_final_state.data_ptr() if d_final_state is not None else None,
+            d_q.data_ptr(), d_k.data_ptr(), d_v.data_ptr(), d_beta.data_ptr(), d_S0.data_ptr(),
+            B, H, T, dk, dv, chunk_size, dt, workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_handle(dev)))
+    return d_q, d_k, d_v, d_beta, d_S0
+
+
+class DeltaRule(torch.autograd.Function):
+    """Autograd wrapper: ``DeltaRule.apply(q, k, v, beta, initial_state)``
+    returns ``(o, final_state)`` from ``chunk_fwd``; the backward pass calls
+    ``chunk_bwd`` (the chunk states are recomputed there, not stored)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, beta, initial_state=None):
+        q, k, v, beta = (t.contiguous() for t in (q, k, v, beta))
+        if initial_state is not None:
+            initial_state = initial_state.contiguous()
+        o, S_T = chunk_fwd(q, k, v, beta, initial_state=initial_state, output_final_state=True)
+        ctx.save_for_backward(q, k, v, beta, initial_state)
+        return o, S_T
+
+    @staticmethod
+    def backward(ctx, d_o, d_S_T):
+        q, k, v, beta, S0 = ctx.saved_tensors
+        d_o = torch.zeros_like(v) if d_o is None else d_o.contiguous()
+        d_S_T = None if d_S_T is None else d_S_T.contiguous().float()
+        d_q, d_k, d_v, d_beta, d_S0 = chunk_bwd(q, k, v, beta, d_o.to(v.dtype), S0, d_S_T)
+        return d_q, d_k, d_v, d_beta, (d_S0 if S0 is not None else None)

@@ -31,6 +31,9 @@ SIGNATURES = {
                                     _int, _int, _int, _vp]),
     "dn_recurrent_step": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _int, _int, _int, _int, _int,
                                  _vp]),
+    "dn_chunk_bwd": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _fp, _vp, _vp, _vp, _vp, _fp]
+                     + [_int] * 7 + [_vp, _size, _vp]),
+    "dn_chunk_bwd_workspace_bytes": (_size, [_int] * 7),
     "dn_status_string": (ctypes.c_char_p, [_int]),
     "dn_last_error": (ctypes.c_char_p, []),
     "dn_abi_version": (_int, []),

@@ -274,4 +274,80 @@ int dn_recurrent_step(const void* q, const void* k, const void* v, const void* b
                        "recurrent step launch");
 }
 
+size_t dn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt) {
+    if (B <= 0 || H <= 0 || T <= 0 || C != 64 || (dt != DN_F32 && dt != DN_BF16) ||
+        !supported_dim(dk) || !supported_dim(dv))
+        return 0;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return 0;
+    return dn::chunk_bwd_workspace_bytes((int)BH, T, dk, dv);
+}
+
+int dn_chunk_bwd(const void* q, const void* k, const void* v, const void* beta, const float* S0,
+                 const void* d_o, const float* d_S_T, void* d_q, void* d_k, void* d_v,
+                 void* d_beta, float* d_S0, int B, int H, int T, int dk, int dv, int C, int dt,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+    if (B < 0 || H < 0 || T < 0)
+        return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d T=%d)", B, H, T);
+    if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
+    if (dk <= 0 || dv <= 0 || C <= 0)
+        return fail(DN_ERR_INVALID_ARG, "dk, dv and C must be positive");
+    if (!supported_dim(dk) || !supported_dim(dv))
+        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this build supports 64 and 128", dk, dv);
+    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this build supports 64", C);
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
+    const size_t need_ws = dn_chunk_bwd_workspace_bytes(B, H, T, dk, dv, C, dt);
+    if (workspace_bytes < need_ws || (need_ws > 0 && !workspace))
+        return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                    need_ws);
+    if (BH == 0) return ok();
+
+    const size_t es = elem_size(dt);
+    const size_t ntok = (size_t)BH * (size_t)T;
+    const size_t state_bytes = (size_t)BH * dk * dv * sizeof(float);
+    const Span sq{"q", q, ntok * dk * es}, sk{"k", k, ntok * dk * es}, sv{"v", v, ntok * dv * es},
+        sb{"beta", beta, ntok * es}, s0{"S0", S0, state_bytes}, sdo{"d_o", d_o, ntok * dv * es},
+        sdT{"d_S_T", d_S_T, state_bytes}, sdq{"d_q", d_q, ntok * dk * es},
+        sdk{"d_k", d_k, ntok * dk * es}, sdv{"d_v", d_v, ntok * dv * es},
+        sdb{"d_beta", d_beta, ntok * es}, sd0{"d_S0", d_S0, state_bytes},
+        sw{"workspace", workspace, need_ws};
+    int dev = 0;
+    if (int st = current_device(&dev)) return st;
+    if (T > 0) {
+        for (const Span* s : {&sq, &sk, &sv, &sdo, &sdq, &sdk, &sdv, &sw})
+            if (int st = check_device_ptr(*s, 16, dev)) return st;
+        for (const Span* s : {&sb, &sdb})
+            if (int st = check_device_ptr(*s, es, dev)) return st;
+    }
+    for (const Span* s : {&s0, &sdT, &sd0})
+        if (s->p)
+            if (int st = check_device_ptr(*s, 16, dev)) return st;
+    // Outputs (and the workspace) overlap no input and no other output.
+    const Span* ins[] = {&sq, &sk, &sv, &sb, &s0, &sdo, &sdT};
+    const Span* outs[] = {&sdq, &sdk, &sdv, &sdb, &sd0, &sw};
+    for (const Span* o : outs) {
+        if (T == 0 && o != &sd0) continue;
+        for (const Span* i : ins)
+            if ((T > 0 || i == &sdT) && overlaps(*o, *i))
+                return fail(DN_ERR_INVALID_ARG, "%s overlaps %s", o->name, i->name);
+        for (const Span* o2 : outs)
+            if (o2 != o && (T > 0 || o2 == &sd0) && overlaps(*o, *o2))
+                return fail(DN_ERR_INVALID_ARG, "%s overlaps %s", o->name, o2->name);
+    }
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {  // the state passes through unchanged
+        if (!d_S0) return ok();
+        if (d_S_T)
+            return cuda_status(
+                cudaMemcpyAsync(d_S0, d_S_T, state_bytes, cudaMemcpyDeviceToDevice, st),
+                "cudaMemcpyAsync(d_S0 <- d_S_T)");
+        return cuda_status(cudaMemsetAsync(d_S0, 0, state_bytes, st), "cudaMemsetAsync(d_S0)");
+    }
+    return cuda_status(dn::launch_chunk_bwd(q, k, v, beta, S0, d_o, d_S_T, d_q, d_k, d_v, d_beta,
+                                            d_S0, (int)BH, T, dk, dv, dt, workspace, st),
+                       "chunk backward (SIMT) launch");
+}
+
 }  // extern "C"

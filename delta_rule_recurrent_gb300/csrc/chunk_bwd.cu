@@ -1,0 +1,441 @@
+// chunk_bwd.cu -- chunkwise delta-rule backward on CUDA cores, fp32 throughout.
+//
+// The training pass that follows the chunkwise forward ("Hardware-efficient
+// implementation", section 3 of paperlayer.ai/abs/2406.06484v6, which
+// recomputes the chunk states during backpropagation instead of storing
+// them).  It returns the gradients of L = <d_o, o> + <d_S_T, S_T>.
+//
+// Forward per chunk (rows K, Q, V, strengths beta, incoming state S, stored
+// [dk][dv]; the algebra of chunk_simt.cu):
+//     A = tril(diag(beta) K K^T, -1),  X = (I + A)^{-1},  Tm = X diag(beta)
+//     R = V - K S,  U' = Tm R,  P = tril(Q K^T),  O = Q S + P U',
+//     S_next = S + K^T U'
+// Backward per chunk, last to first, with G = dL/dS_next:
+//     dU' = P^T dO + K G,   dV = Tm^T dU',   dL/dS = G + Q^T dO - K^T dV
+//     dP = tril(dO U'^T),   dTm = dU' R^T
+//     dQ = dO S^T + dP K
+//     dK = dP^T Q + U' G^T - dV S^T + Z K
+//     dA = strict_tril(-X^T (dTm diag(beta)) X^T),   Z = diag(beta) dA + (diag(beta) dA)^T
+//     dbeta_j = sum_i X_ij dTm_ij + sum_l dA_jl (K K^T)_jl
+// Value channels are independent in the chain (dU', dV and dL/dS column by
+// column), so it runs per (batch, head, value slice); dQ, dK and dbeta sum
+// over all value channels, and every chunk's share needs only S and G at its
+// ends, so they run in parallel over all chunks.  Three launches:
+//   1. the CUDA-core forward without outputs, recording S at every chunk start;
+//   2. chunk_bwd_chain_kernel: per (b, h, value slice), chunks last to first:
+//      G at every chunk end, d_v, d_S0;
+//   3. chunk_bwd_grads_kernel: one CTA per (b, h, chunk): d_q, d_k, d_beta.
+#include "dn_common.cuh"
+#include "dn_internal.h"
+#include "simt_mm.cuh"
+#include "tri_inverse.cuh"
+
+namespace dn {
+namespace {
+
+using simt::for_each;
+using simt::kThreads;
+using simt::mm_acc;
+using simt::zero;
+constexpr int kC = 64;       // chunk length
+constexpr int kLC = kC + 1;  // odd row pitches keep shared-memory reads conflict-free
+static_assert(kLC == kTriPitch, "the solve's operand pitch");
+
+// Chunk rows [t0, t0 + 64) of a [T][D] tensor of head bh into shared memory
+// (row pitch LD, columns c0 .. c0 + W - 1), zeros past the end of the sequence.
+template <int W, int LD, int D, typename T>
+__device__ __forceinline__ void load_rows(float* dst, const T* __restrict__ src, size_t tok0,
+                                          int t0, int n, int c0) {
+    for (int e = threadIdx.x; e < kC * W; e += kThreads) {
+        const int t = e / W, i = e % W;
+        dst[t * LD + i] = t < n ? to_f32(src[(tok0 + t0 + t) * D + c0 + i]) : 0.f;
+    }
+}
+
+// A = tril(diag(beta) K K^T, -1) and P = tril(Q K^T) (diagonal included);
+// K K^T itself too when KK is given.
+template <int DK>
+__device__ __forceinline__ void form_a_p(const float* Ks, const float* Qs, const float* bs,
+                                         float* Am, float* Pm, float* KK) {
+    constexpr int LK = DK + 1;
+    float aa[4][4], ap[4][4];
+    zero<64, 64>(aa);
+    zero<64, 64>(ap);
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll 2
+    for (int kk = 0; kk < DK; ++kk) {
+        float ak[4], aq[4], bk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ak[i] = Ks[(ty + 16 * i) * LK + kk];
+            aq[i] = Qs[(ty + 16 * i) * LK + kk];
+            bk[i] = Ks[(tx + 16 * i) * LK + kk];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                aa[i][j] = fmaf(ak[i], bk[j], aa[i][j]);
+                ap[i][j] = fmaf(aq[i], bk[j], ap[i][j]);
+            }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int m = ty + 16 * i, nn = tx + 16 * j;
+            Am[m * kLC + nn] = nn < m ? bs[m] * aa[i][j] : 0.f;
+            Pm[m * kLC + nn] = nn <= m ? ap[i][j] : 0.f;
+            if (KK) KK[m * kLC + nn] = aa[i][j];
+        }
+}
+
+// ------------------------------------------------------------------ chain
+template <int DK, int NV>
+struct ChainSmem {
+    static constexpr int LK = DK + 1, LV = NV + 1;
+    static constexpr int kK = 0;                  // C x LK   keys
+    static constexpr int kQ = kK + kC * LK;       // C x LK   queries
+    static constexpr int kD = kQ + kC * LK;       // C x LV   output gradient slice
+    static constexpr int kU = kD + kC * LV;       // C x LV   dU'
+    static constexpr int kV = kU + kC * LV;       // C x LV   dV
+    static constexpr int kG = kV + kC * LV;       // DK x LV  state gradient slice
+    static constexpr int kA = kG + DK * LV;       // C x kLC  A
+    static constexpr int kX = kA + kC * kLC;      // C x kLC  (I + A)^{-1}
+    static constexpr int kP = kX + kC * kLC;      // C x kLC  tril(Q K^T)
+    static constexpr int kY = kP + kC * kLC;      // solve scratch
+    static constexpr int kB = kY + 3 * 16 * 17;   // C        beta
+    static constexpr int kFloats = kB + kC;
+    static constexpr size_t kBytes = sizeof(float) * kFloats;
+};
+
+// One CTA per (batch, head, slice of NV value channels): G = dL/dS from the
+// last chunk to the first.  Writes G at the end of every chunk (G_chunks,
+// [BH][chunk][dk][dv] fp32), d_v, and d_S0 (if given).
+template <typename T, int DK, int DV, int NV>
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
+                       const T* __restrict__ beta, const T* __restrict__ d_o,
+                       const float* __restrict__ d_S_T, T* __restrict__ d_v,
+                       float* __restrict__ d_S0, float* __restrict__ G_chunks, int Tlen) {
+    using L = ChainSmem<DK, NV>;
+    constexpr int LK = L::LK, LV = L::LV, NSLICE = DV / NV;
+    extern __shared__ float smem[];
+    float* Ks = smem + L::kK;
+    float* Qs = smem + L::kQ;
+    float* Ds = smem + L::kD;
+    float* Us = smem + L::kU;
+    float* Vs = smem + L::kV;
+    float* Gs = smem + L::kG;
+    float* Am = smem + L::kA;
+    float* Xm = smem + L::kX;
+    float* Pm = smem + L::kP;
+    float* Ys = smem + L::kY;
+    float* bs = smem + L::kB;
+    const int tid = threadIdx.x;
+    const int bh = blockIdx.x / NSLICE, j0 = (blockIdx.x % NSLICE) * NV;
+    const size_t tok0 = (size_t)bh * Tlen;
+    const int nchunks = (Tlen + kC - 1) / kC;
+
+    for (int e = tid; e < DK * NV; e += kThreads) {
+        const int i = e / NV, jj = e % NV;
+        Gs[i * LV + jj] = d_S_T ? d_S_T[((size_t)bh * DK + i) * DV + j0 + jj] : 0.f;
+    }
+    for (int c = nchunks - 1; c >= 0; --c) {
+        const int t0 = c * kC, n = min(kC, Tlen - t0);
+        for (int e = tid; e < DK * NV; e += kThreads) {  // G at the end of chunk c
+            const int i = e / NV, jj = e % NV;
+            G_chunks[(((size_t)bh * nchunks + c) * DK + i) * DV + j0 + jj] = Gs[i * LV + jj];
+        }
+        load_rows<DK, LK, DK>(Ks, k, tok0, t0, n, 0);
+        load_rows<DK, LK, DK>(Qs, q, tok0, t0, n, 0);
+        load_rows<NV, LV, DV>(Ds, d_o, tok0, t0, n, j0);
+        if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
+        __syncthreads();
+        form_a_p<DK>(Ks, Qs, bs, Am, Pm, nullptr);
+        __syncthreads();
+        {   // dU' = P^T dO + K G
+            float acc[4][NV / 16];
+            zero<64, NV>(acc);
+            mm_acc<64, NV, kC>(acc, [&](int m, int s) { return Pm[s * kLC + m]; },
+                               [&](int s, int nn) { return Ds[s * LV + nn]; });
+            mm_acc<64, NV, DK>(acc, [&](int m, int i) { return Ks[m * LK + i]; },
+                               [&](int i, int nn) { return Gs[i * LV + nn]; });
+            for_each<64, NV>(acc, [&](int m, int nn, float x) { Us[m * LV + nn] = x; });
+        }
+        unit_lower_inverse64<kThreads>(Am, Xm, Ys);  // ends with a barrier
+        {   // dV = Tm^T dU' = diag(beta) X^T dU'
+            float acc[4][NV / 16];
+            zero<64, NV>(acc);
+            mm_acc<64, NV, kC>(acc, [&](int m, int s) { return Xm[s * kLC + m]; },
+                               [&](int s, int nn) { return Us[s * LV + nn]; });
+            for_each<64, NV>(acc, [&](int m, int nn, float x) {
+                const float y = bs[m] * x;
+                Vs[m * LV + nn] = y;
+                if (m < n) d_v[(tok0 + t0 + m) * DV + j0 + nn] = from_f32<T>(y);
+            });
+        }
+        __syncthreads();
+        {   // G <- G + Q^T dO - K^T dV  (the gradient of the state chunk c starts from)
+            float acc[DK / 16][NV / 16];
+            zero<DK, NV>(acc);
+            mm_acc<DK, NV, kC>(acc, [&](int i, int s) { return Qs[s * LK + i]; },
+                               [&](int s, int nn) { return Ds[s * LV + nn]; });
+            mm_acc<DK, NV, kC>(acc, [&](int i, int s) { return -Ks[s * LK + i]; },
+                               [&](int s, int nn) { return Vs[s * LV + nn]; });
+            for_each<DK, NV>(acc, [&](int i, int nn, float x) { Gs[i * LV + nn] += x; });
+        }
+        __syncthreads();
+    }
+    if (d_S0) {
+        for (int e = tid; e < DK * NV; e += kThreads) {
+            const int i = e / NV, jj = e % NV;
+            d_S0[((size_t)bh * DK + i) * DV + j0 + jj] = Gs[i * LV + jj];
+        }
+    }
+}
+
+// ------------------------------------------------------------------ grads
+template <int DK, int NS>
+struct GradSmem {
+    static constexpr int LK = DK + 1, LS = NS + 1;
+    static constexpr int kK = 0;                  // C x LK   keys
+    static constexpr int kQ = kK + kC * LK;       // C x LK   queries
+    static constexpr int kA = kQ + kC * LK;       // C x kLC  A
+    static constexpr int kX = kA + kC * kLC;      // C x kLC  (I + A)^{-1}
+    static constexpr int kP = kX + kC * kLC;      // C x kLC  tril(Q K^T)
+    static constexpr int kKK = kP + kC * kLC;     // C x kLC  K K^T
+    static constexpr int kY = kKK + kC * kLC;     // solve scratch
+    static constexpr int kB = kY + 3 * 16 * 17;   // C        beta
+    // value-slice operands, reused as C x kLC matrices once the slices are done
+    static constexpr int kV = kB + kC;            // C x LS   V
+    static constexpr int kD = kV + kC * LS;       // C x LS   dO
+    static constexpr int kR = kD + kC * LS;       // C x LS   R = V - K S
+    static constexpr int kU = kR + kC * LS;       // C x LS   U'
+    static constexpr int kE = kU + kC * LS;       // C x LS   dU'
+    static constexpr int kF = kE + kC * LS;       // C x LS   dV
+    static constexpr int kS = kF + kC * LS;       // DK x LS  S slice
+    static constexpr int kG = kS + DK * LS;       // DK x LS  G slice
+    static constexpr int kFloats = kG + DK * LS;
+    static constexpr size_t kBytes = sizeof(float) * kFloats;
+    static_assert(kFloats - kV >= 4 * kC * kLC, "room for dP, dTm, M1, dA");
+};
+
+// One CTA per (batch, head, chunk): the chunk's d_q, d_k and d_beta from S at
+// its start (S_chunks) and G at its end (G_chunks), over all value channels
+// in slices of NS.
+template <typename T, int DK, int DV>
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
+                       const T* __restrict__ v, const T* __restrict__ beta,
+                       const T* __restrict__ d_o, const float* __restrict__ S_chunks,
+                       const float* __restrict__ G_chunks, T* __restrict__ d_q,
+                       T* __restrict__ d_k, T* __restrict__ d_beta, int Tlen, int nchunks) {
+    constexpr int NS = 32;
+    using L = GradSmem<DK, NS>;
+    constexpr int LK = L::LK, LS = L::LS;
+    extern __shared__ float smem[];
+    float* Ks = smem + L::kK;
+    float* Qs = smem + L::kQ;
+    float* Am = smem + L::kA;
+    float* Xm = smem + L::kX;
+    float* Pm = smem + L::kP;
+    float* KK = smem + L::kKK;
+    float* Ys = smem + L::kY;
+    float* bs = smem + L::kB;
+    float* Vs = smem + L::kV;
+    float* Ds = smem + L::kD;
+    float* Rs = smem + L::kR;
+    float* Us = smem + L::kU;
+    float* Es = smem + L::kE;
+    float* Fs = smem + L::kF;
+    float* Ss = smem + L::kS;
+    float* Gs = smem + L::kG;
+    const int tid = threadIdx.x;
+    const int bh = blockIdx.x / nchunks, c = blockIdx.x % nchunks;
+    const int t0 = c * kC, n = min(kC, Tlen - t0);
+    const size_t tok0 = (size_t)bh * Tlen;
+    const size_t st0 = ((size_t)bh * nchunks + c) * DK * DV;
+
+    load_rows<DK, LK, DK>(Ks, k, tok0, t0, n, 0);
+    load_rows<DK, LK, DK>(Qs, q, tok0, t0, n, 0);
+    if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
+    __syncthreads();
+    form_a_p<DK>(Ks, Qs, bs, Am, Pm, KK);
+    __syncthreads();
+    unit_lower_inverse64<kThreads>(Am, Xm, Ys);  // ends with a barrier
+
+    float aQ[4][DK / 16], aK[4][DK / 16], aP[4][4], aT[4][4];
+    zero<64, DK>(aQ);
+    zero<64, DK>(aK);
+    zero<64, 64>(aP);
+    zero<64, 64>(aT);
+    for (int js = 0; js < DV; js += NS) {
+        load_rows<NS, LS, DV>(Vs, v, tok0, t0, n, js);
+        load_rows<NS, LS, DV>(Ds, d_o, tok0, t0, n, js);
+        for (int e = tid; e < DK * NS; e += kThreads) {
+            const int i = e / NS, jj = e % NS;
+            Ss[i * LS + jj] = S_chunks[st0 + (size_t)i * DV + js + jj];
+            Gs[i * LS + jj] = G_chunks[st0 + (size_t)i * DV + js + jj];
+        }
+        __syncthreads();
+        {   // R = V - K S and dU' = P^T dO + K G
+            float r[4][NS / 16], e[4][NS / 16];
+            zero<64, NS>(r);
+            zero<64, NS>(e);
+            mm_acc<64, NS, DK>(r, [&](int m, int i) { return Ks[m * LK + i]; },
+                               [&](int i, int nn) { return Ss[i * LS + nn]; });
+            mm_acc<64, NS, kC>(e, [&](int m, int s) { return Pm[s * kLC + m]; },
+                               [&](int s, int nn) { return Ds[s * LS + nn]; });
+            mm_acc<64, NS, DK>(e, [&](int m, int i) { return Ks[m * LK + i]; },
+                               [&](int i, int nn) { return Gs[i * LS + nn]; });
+            for_each<64, NS>(r, [&](int m, int nn, float x) { Rs[m * LS + nn] = Vs[m * LS + nn] - x; });
+            for_each<64, NS>(e, [&](int m, int nn, float x) { Es[m * LS + nn] = x; });
+        }
+        __syncthreads();
+        {   // U' = X diag(beta) R and dV = diag(beta) X^T dU'
+            float u[4][NS / 16], f[4][NS / 16];
+            zero<64, NS>(u);
+            zero<64, NS>(f);
+            mm_acc<64, NS, kC>(u, [&](int m, int s) { return Xm[m * kLC + s] * bs[s]; },
+                               [&](int s, int nn) { return Rs[s * LS + nn]; });
+            mm_acc<64, NS, kC>(f, [&](int m, int s) { return Xm[s * kLC + m]; },
+                               [&](int s, int nn) { return Es[s * LS + nn]; });
+            for_each<64, NS>(u, [&](int m, int nn, float x) { Us[m * LS + nn] = x; });
+            for_each<64, NS>(f, [&](int m, int nn, float x) { Fs[m * LS + nn] = bs[m] * x; });
+        }
+        __syncthreads();
+        // dP += dO U'^T, dTm += dU' R^T, dQ += dO S^T, dK += U' G^T - dV S^T
+        mm_acc<64, 64, NS>(aP, [&](int m, int j) { return Ds[m * LS + j]; },
+                           [&](int j, int nn) { return Us[nn * LS + j]; });
+        mm_acc<64, 64, NS>(aT, [&](int m, int j) { return Es[m * LS + j]; },
+                           [&](int j, int nn) { return Rs[nn * LS + j]; });
+        mm_acc<64, DK, NS>(aQ, [&](int m, int j) { return Ds[m * LS + j]; },
+                           [&](int j, int i) { return Ss[i * LS + j]; });
+        mm_acc<64, DK, NS>(aK, [&](int m, int j) { return Us[m * LS + j]; },
+                           [&](int j, int i) { return Gs[i * LS + j]; });
+        mm_acc<64, DK, NS>(aK, [&](int m, int j) { return -Fs[m * LS + j]; },
+                           [&](int j, int i) { return Ss[i * LS + j]; });
+        __syncthreads();
+    }
+
+    // The slice area now holds C x C matrices.
+    float* dPm = smem + L::kV;
+    float* dTs = dPm + kC * kLC;
+    float* M1 = dTs + kC * kLC;
+    float* dAm = M1 + kC * kLC;
+    for_each<64, 64>(aP, [&](int m, int nn, float x) { dPm[m * kLC + nn] = nn <= m ? x : 0.f; });
+    for_each<64, 64>(aT, [&](int m, int nn, float x) { dTs[m * kLC + nn] = x; });
+    __syncthreads();
+    // dQ += dP K, dK += dP^T Q
+    mm_acc<64, DK, kC>(aQ, [&](int m, int s) { return dPm[m * kLC + s]; },
+                       [&](int s, int i) { return Ks[s * LK + i]; });
+    mm_acc<64, DK, kC>(aK, [&](int m, int s) { return dPm[s * kLC + m]; },
+                       [&](int s, int i) { return Qs[s * LK + i]; });
+    {   // M1 = (dTm diag(beta)) X^T
+        float acc[4][4];
+        zero<64, 64>(acc);
+        mm_acc<64, 64, kC>(acc, [&](int m, int s) { return dTs[m * kLC + s] * bs[s]; },
+                           [&](int s, int nn) { return Xm[nn * kLC + s]; });
+        for_each<64, 64>(acc, [&](int m, int nn, float x) { M1[m * kLC + nn] = x; });
+    }
+    float db = 0.f;  // thread j < 64: dbeta_j
+    if (tid < kC)
+        for (int i = 0; i < kC; ++i) db = fmaf(Xm[i * kLC + tid], dTs[i * kLC + tid], db);
+    __syncthreads();
+    {   // dA = strict_tril(-X^T M1)
+        float acc[4][4];
+        zero<64, 64>(acc);
+        mm_acc<64, 64, kC>(acc, [&](int m, int s) { return Xm[s * kLC + m]; },
+                           [&](int s, int nn) { return M1[s * kLC + nn]; });
+        for_each<64, 64>(acc, [&](int m, int nn, float x) { dAm[m * kLC + nn] = nn < m ? -x : 0.f; });
+    }
+    __syncthreads();
+    if (tid < kC)
+        for (int l = 0; l < kC; ++l) db = fmaf(dAm[tid * kLC + l], KK[tid * kLC + l], db);
+    // dK += Z K with Z = diag(beta) dA + (diag(beta) dA)^T
+    mm_acc<64, DK, kC>(aK, [&](int m, int s) {
+        return bs[m] * dAm[m * kLC + s] + bs[s] * dAm[s * kLC + m];
+    }, [&](int s, int i) { return Ks[s * LK + i]; });
+
+    for_each<64, DK>(aQ, [&](int m, int i, float x) {
+        if (m < n) d_q[(tok0 + t0 + m) * DK + i] = from_f32<T>(x);
+    });
+    for_each<64, DK>(aK, [&](int m, int i, float x) {
+        if (m < n) d_k[(tok0 + t0 + m) * DK + i] = from_f32<T>(x);
+    });
+    if (tid < n) d_beta[tok0 + t0 + tid] = from_f32<T>(db);
+}
+
+template <typename T, int DK, int DV>
+cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const void* beta,
+                             const void* d_o, const float* d_S_T, void* d_q, void* d_k, void* d_v,
+                             void* d_beta, float* d_S0, float* Sc, float* Gc, int BH, int Tlen,
+                             cudaStream_t stream) {
+    constexpr int NV = DV < 64 ? DV : 64;
+    using LC = ChainSmem<DK, NV>;
+    using LG = GradSmem<DK, 32>;
+    const int nchunks = (Tlen + kC - 1) / kC;
+    auto chain = chunk_bwd_chain_kernel<T, DK, DV, NV>;
+    auto grads = chunk_bwd_grads_kernel<T, DK, DV>;
+    cudaError_t err;
+    if ((err = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)LC::kBytes)) != cudaSuccess ||
+        (err = cudaFuncSetAttribute(grads, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)LG::kBytes)) != cudaSuccess)
+        return err;
+    const long long g_chain = (long long)BH * (DV / NV), g_grads = (long long)BH * nchunks;
+    if (g_chain > 0x7fffffffLL || g_grads > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    chain<<<(unsigned)g_chain, kThreads, LC::kBytes, stream>>>(
+        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(beta),
+        static_cast<const T*>(d_o), d_S_T, static_cast<T*>(d_v), d_S0, Gc, Tlen);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    grads<<<(unsigned)g_grads, kThreads, LG::kBytes, stream>>>(
+        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
+        static_cast<const T*>(beta), static_cast<const T*>(d_o), Sc, Gc, static_cast<T*>(d_q),
+        static_cast<T*>(d_k), static_cast<T*>(d_beta), Tlen, nchunks);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_bwd_dims(const void* q, const void* k, const void* v, const void* beta,
+                            const void* d_o, const float* d_S_T, void* d_q, void* d_k, void* d_v,
+                            void* d_beta, float* d_S0, float* Sc, float* Gc, int BH, int Tlen,
+                            int dk, int dv, cudaStream_t st) {
+#define DN_BWD_CASE(DK_, DV_)                                                                   \
+    if (dk == DK_ && dv == DV_)                                                                 \
+        return launch_bwd_typed<T, DK_, DV_>(q, k, v, beta, d_o, d_S_T, d_q, d_k, d_v, d_beta,  \
+                                             d_S0, Sc, Gc, BH, Tlen, st);
+    DN_BWD_CASE(128, 128)
+    DN_BWD_CASE(128, 64)
+    DN_BWD_CASE(64, 128)
+    DN_BWD_CASE(64, 64)
+#undef DN_BWD_CASE
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+size_t chunk_bwd_workspace_bytes(int BH, int T, int dk, int dv) {
+    if (BH <= 0 || T <= 0) return 0;
+    return 2 * (size_t)BH * (size_t)((T + kC - 1) / kC) * (size_t)dk * (size_t)dv * sizeof(float);
+}
+
+cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const void* beta,
+                             const float* S0, const void* d_o, const float* d_S_T, void* d_q,
+                             void* d_k, void* d_v, void* d_beta, float* d_S0, int BH, int T,
+                             int dk, int dv, int dt, void* workspace, cudaStream_t stream) {
+    if (BH <= 0 || T <= 0) return cudaSuccess;
+    float* const Sc = static_cast<float*>(workspace);
+    float* const Gc = Sc + (size_t)BH * ((T + kC - 1) / kC) * (size_t)dk * dv;
+    cudaError_t err = launch_chunk_simt(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt,
+                                        stream, Sc);
+    if (err != cudaSuccess) return err;
+    if (dt == 0)
+        return launch_bwd_dims<float>(q, k, v, beta, d_o, d_S_T, d_q, d_k, d_v, d_beta, d_S0, Sc,
+                                      Gc, BH, T, dk, dv, stream);
+    return launch_bwd_dims<__nv_bfloat16>(q, k, v, beta, d_o, d_S_T, d_q, d_k, d_v, d_beta, d_S0,
+                                          Sc, Gc, BH, T, dk, dv, stream);
+}
+
+}  // namespace dn

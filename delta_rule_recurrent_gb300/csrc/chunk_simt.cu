@@ -15,45 +15,24 @@
 //     O   = Q S + (Q K^T . M) U'                  (M: causal incl. diagonal)
 //     S  <- S + K^T U'
 // A CTA owns one (batch, head) and a slice of NV value channels; it walks the
-// chunks in order with its slice of S resident in shared memory.  Value
+// chunks in order with its slice of S resident in shared memory.  For the
+// backward pass it can also record the state at the start of every chunk
+// (S_chunks, [BH][chunk][dk][dv] fp32) and skip the outputs (o == nullptr).  Value
 // channels are independent in every step above, so slices never exchange
 // data; the key-side work (A, X, Q K^T) is recomputed per slice.
 #include "dn_common.cuh"
 #include "dn_internal.h"
+#include "simt_mm.cuh"
 #include "tri_inverse.cuh"
 
 namespace dn {
 namespace {
 
+using simt::kThreads;
+using simt::mm_acc;
+using simt::zero;
 constexpr int kC = 64;         // chunk length
-constexpr int kThreads = 256;  // 16 x 16 thread grid for the register-tiled products
 constexpr int kLC = kC + 1;    // odd row pitches keep shared-memory reads conflict-free
-
-// acc[i][j] += sum_kk a(ty + 16 i, kk) * b(kk, tx + 16 j) for a 256-thread CTA.
-template <int M, int N, int K, typename FA, typename FB>
-__device__ __forceinline__ void mm_acc(float (&acc)[M / 16][N / 16], FA a, FB b) {
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-#pragma unroll 4
-    for (int kk = 0; kk < K; ++kk) {
-        float av[M / 16], bv[N / 16];
-#pragma unroll
-        for (int i = 0; i < M / 16; ++i) av[i] = a(ty + 16 * i, kk);
-#pragma unroll
-        for (int j = 0; j < N / 16; ++j) bv[j] = b(kk, tx + 16 * j);
-#pragma unroll
-        for (int i = 0; i < M / 16; ++i)
-#pragma unroll
-            for (int j = 0; j < N / 16; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-}
-
-template <int M, int N>
-__device__ __forceinline__ void zero(float (&acc)[M / 16][N / 16]) {
-#pragma unroll
-    for (int i = 0; i < M / 16; ++i)
-#pragma unroll
-        for (int j = 0; j < N / 16; ++j) acc[i][j] = 0.f;
-}
 
 template <int DK, int NV>
 struct SimtSmem {
@@ -77,7 +56,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
                   const T* __restrict__ v, const T* __restrict__ beta,
                   const float* __restrict__ S0, T* __restrict__ o,
-                  float* __restrict__ S_T, int Tlen) {
+                  float* __restrict__ S_T, float* __restrict__ S_chunks, int Tlen) {
     using L = SimtSmem<DK, NV>;
     constexpr int LK = L::LK, LV = L::LV;
     constexpr int NSLICE = DV / NV;
@@ -108,6 +87,12 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kC;
         const int n = min(kC, Tlen - t0);
+        if (S_chunks) {  // the state this chunk starts from
+            for (int e = tid; e < DK * NV; e += kThreads) {
+                const int i = e / NV, jj = e % NV;
+                S_chunks[(((size_t)bh * nchunks + c) * DK + i) * DV + j0 + jj] = Ss[i * LV + jj];
+            }
+        }
         // ---- load the chunk (padding rows: k = q = v = 0, beta = 0) ----
         for (int e = tid; e < kC * DK; e += kThreads) {
             const int t = e / DK, i = e % DK;
@@ -187,7 +172,7 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
         __syncthreads();
 
         // ---- O = Q S + P U' ----
-        {
+        if (o) {
             float acc[4][NV / 16];
             zero<64, NV>(acc);
             mm_acc<64, NV, DK>(acc, [&](int m, int kk) { return Qs[m * LK + kk]; },
@@ -232,7 +217,7 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
 template <typename T, int DK, int DV>
 cudaError_t launch_typed(const void* q, const void* k, const void* v,
                          const void* beta, const float* S0, void* o, float* S_T,
-                         int BH, int Tlen, cudaStream_t stream) {
+                         float* S_chunks, int BH, int Tlen, cudaStream_t stream) {
     constexpr int NV = DV < 64 ? DV : 64;
     using L = SimtSmem<DK, NV>;
     auto kern = chunk_simt_kernel<T, DK, DV, NV>;
@@ -244,18 +229,18 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
     kern<<<(unsigned)grid, kThreads, L::kBytes, stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k),
         static_cast<const T*>(v), static_cast<const T*>(beta), S0,
-        static_cast<T*>(o), S_T, Tlen);
+        static_cast<T*>(o), S_T, S_chunks, Tlen);
     return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_dims(const void* q, const void* k, const void* v,
                         const void* beta, const float* S0, void* o, float* S_T,
-                        int BH, int Tlen, int dk, int dv, cudaStream_t st) {
-    if (dk == 128 && dv == 128) return launch_typed<T, 128, 128>(q, k, v, beta, S0, o, S_T, BH, Tlen, st);
-    if (dk == 128 && dv == 64) return launch_typed<T, 128, 64>(q, k, v, beta, S0, o, S_T, BH, Tlen, st);
-    if (dk == 64 && dv == 128) return launch_typed<T, 64, 128>(q, k, v, beta, S0, o, S_T, BH, Tlen, st);
-    if (dk == 64 && dv == 64) return launch_typed<T, 64, 64>(q, k, v, beta, S0, o, S_T, BH, Tlen, st);
+                        float* Sc, int BH, int Tlen, int dk, int dv, cudaStream_t st) {
+    if (dk == 128 && dv == 128) return launch_typed<T, 128, 128>(q, k, v, beta, S0, o, S_T, Sc, BH, Tlen, st);
+    if (dk == 128 && dv == 64) return launch_typed<T, 128, 64>(q, k, v, beta, S0, o, S_T, Sc, BH, Tlen, st);
+    if (dk == 64 && dv == 128) return launch_typed<T, 64, 128>(q, k, v, beta, S0, o, S_T, Sc, BH, Tlen, st);
+    if (dk == 64 && dv == 64) return launch_typed<T, 64, 64>(q, k, v, beta, S0, o, S_T, Sc, BH, Tlen, st);
     return cudaErrorNotSupported;
 }
 
@@ -264,10 +249,10 @@ cudaError_t launch_dims(const void* q, const void* k, const void* v,
 cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v,
                               const void* beta, const float* S0, void* o,
                               float* S_T, int BH, int T, int dk, int dv, int dt,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, float* S_chunks) {
     if (BH <= 0 || T <= 0) return cudaSuccess;
-    if (dt == 0) return launch_dims<float>(q, k, v, beta, S0, o, S_T, BH, T, dk, dv, stream);
-    return launch_dims<__nv_bfloat16>(q, k, v, beta, S0, o, S_T, BH, T, dk, dv, stream);
+    if (dt == 0) return launch_dims<float>(q, k, v, beta, S0, o, S_T, S_chunks, BH, T, dk, dv, stream);
+    return launch_dims<__nv_bfloat16>(q, k, v, beta, S0, o, S_T, S_chunks, BH, T, dk, dv, stream);
 }
 
 }  // namespace dn

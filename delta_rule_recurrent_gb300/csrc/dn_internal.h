@@ -14,11 +14,24 @@ cudaError_t launch_recurrent_step(const void* q, const void* k, const void* v,
                                   const void* beta, float* S, void* o, int BH,
                                   int dk, int dv, int dt, cudaStream_t stream);
 
-// Chunkwise forward with fp32 CUDA-core arithmetic (any T >= 1).
+// Chunkwise forward with fp32 CUDA-core arithmetic (any T >= 1).  o may be
+// nullptr (no outputs); S_chunks, if given, receives the state at the start
+// of every chunk ([BH][ceil(T/64)][dk][dv] fp32), for the backward pass.
 cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v,
                               const void* beta, const float* S0, void* o,
                               float* S_T, int BH, int T, int dk, int dv, int dt,
-                              cudaStream_t stream);
+                              cudaStream_t stream, float* S_chunks = nullptr);
+
+// Chunkwise backward (fp32 CUDA-core arithmetic): the gradients of
+// L = <d_o, o> + <d_S_T, S_T> for dn_chunk_fwd's outputs.  The workspace
+// holds chunk_bwd_workspace_bytes(BH, T, dk, dv) bytes: the state at the start
+// of every chunk and the gradient of the state at its end.  d_S_T, S0 and
+// d_S0 may be nullptr.
+size_t chunk_bwd_workspace_bytes(int BH, int T, int dk, int dv);
+cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const void* beta,
+                             const float* S0, const void* d_o, const float* d_S_T, void* d_q,
+                             void* d_k, void* d_v, void* d_beta, float* d_S0, int BH, int T,
+                             int dk, int dv, int dt, void* workspace, cudaStream_t stream);
 
 // Chunkwise forward on tcgen05 tensor cores.  Returns cudaErrorNotSupported
 // (without launching) for shapes or dtypes it does not cover.  With a

@@ -189,6 +189,46 @@ DN_API int dn_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                          int B, int H, int T, int dk, int dv, int C, int dt,
                          void *stream);
 
+/*
+ * dn_chunk_bwd -- gradients of the chunkwise forward, for training: given
+ * the gradient d_o of the outputs and d_S_T of the final state, returns the
+ * gradients of L = <d_o, o> + <d_S_T, S_T> with respect to q, k, v, beta and
+ * S0.  The pages run this pass after the forward and recompute the chunk
+ * states instead of storing them ("Hardware-efficient implementation",
+ * section 3 of paperlayer.ai/abs/2406.06484v6); the result is the exact
+ * gradient of the recurrence up to rounding.  The arithmetic is fp32 on
+ * CUDA cores for both I/O types.
+ *
+ * Arguments:
+ *   q, k, v, beta, S0   as for dn_chunk_fwd (S0 may be NULL: zeros)
+ *   d_o     [B, H, T, dv]   dtype `dt`
+ *   d_S_T   [B, H, dk, dv]  fp32, or NULL (zeros)
+ *   d_q, d_k [B, H, T, dk], d_v [B, H, T, dv], d_beta [B, H, T]   dtype `dt`,
+ *           written
+ *   d_S0    [B, H, dk, dv]  fp32, written, or NULL to skip
+ *   B, H, T, dk, dv, C, dt  as for dn_chunk_fwd
+ *   workspace, workspace_bytes: device scratch, 16-byte aligned, of at least
+ *           dn_chunk_bwd_workspace_bytes(...) bytes (required when
+ *           B * H * T > 0); the contents need no initialisation and are
+ *           undefined afterwards.
+ *   stream  cudaStream_t
+ * No output may overlap an input, another output or the workspace.  With
+ * T = 0 only d_S0 is written (a copy of d_S_T, or zeros).
+ * Errors: DN_ERR_INVALID_ARG (including a missing or short workspace),
+ * DN_ERR_UNSUPPORTED (other dk, dv, C), DN_ERR_CUDA.
+ */
+DN_API int dn_chunk_bwd(const void *q, const void *k, const void *v, const void *beta,
+                 const float *S0, const void *d_o, const float *d_S_T,
+                 void *d_q, void *d_k, void *d_v, void *d_beta, float *d_S0,
+                 int B, int H, int T, int dk, int dv, int C, int dt,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* Scratch bytes dn_chunk_bwd needs: the fp32 state at the start of every
+ * chunk and the gradient of the state at its end, 2 * B * H * ceil(T / 64) *
+ * dk * dv * 4 bytes (0 for unsupported arguments).  Host-only. */
+DN_API size_t dn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv,
+                                    int C, int dt);
+
 /* ABI version of this header (bumped on incompatible changes). */
 DN_API int dn_abi_version(void);
 

@@ -4,6 +4,7 @@ CPU only: nothing here launches a kernel.  The argument checks exercised
 return before the library makes any CUDA call.
 """
 import ctypes
+import re
 import subprocess
 
 import pytest
@@ -24,6 +25,17 @@ def test_header_declares_the_boundary():
                      "dn_last_error"):
         assert required in names
     assert set(names) == set(_lib.SIGNATURES), "binding signatures drift from the header"
+
+
+def test_binding_argument_counts_match_the_header():
+    """Each ctypes signature has as many parameters as the header's
+    declaration (a miscount would shift every later argument)."""
+    text = _lib.HEADER.read_text()
+    for name, (_res, args) in _lib.SIGNATURES.items():
+        m = re.search(r"DN_API\s+[\w\s\*]*?\b" + name + r"\s*\(([^)]*)\)", text)
+        assert m, name
+        params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
+        assert len(params) == len(args), f"{name}: header {len(params)}, binding {len(args)}"
 
 
 def test_library_exports_every_declared_symbol(lib):

@@ -227,3 +227,17 @@ def decode_inputs_on_device(B: int, H: int, dk: int, dv: int, steps: int, *,
         beta[sl] = (torch.sigmoid(torch.randn(n, B, H, generator=g, device=device))
                     * float(beta_scale)).to(dt)
     return q, k, v, beta
+
+
+def grad_inputs(B: int, H: int, T: int, dv: int, dk: int | None = None, *, dtype="bf16",
+                seed: int = 0, ds_std: float | None = 0.1):
+    """Upstream gradients for a backward pass: d_o ``[B, H, T, dv]`` ~ N(0, 1)
+    in the I/O dtype, and d_S_T ``[B, H, dk, dv]`` ~ N(0, ds_std^2) fp32 (None
+    when ds_std is None).  Seeded by (seed, "grad")."""
+    g = torch.Generator().manual_seed(int(seed) * 7907 + 104729)
+    d_o = torch.randn(B, H, T, dv, generator=g).to(torch_dtype(dtype)).contiguous()
+    d_S = None
+    if ds_std is not None:
+        d_S = (torch.randn(B, H, dk if dk is not None else dv, dv, generator=g)
+               * float(ds_std)).float().contiguous()
+    return d_o, d_S

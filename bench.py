@@ -46,6 +46,19 @@ def chunk_flops_per_token_head(C, dk, dv):
     return C * (3 * dk + 2 * dv) + 6 * dk * dv + C * C / 3.0
 
 
+def bwd_flops_per_chunk(C, dk, dv):
+    """FLOPs the chunkwise backward executes per (batch, head, chunk), dense
+    tiles as the three kernels form them (the forward recompute of the chunk
+    states included, as the method recomputes by design):
+    2 (9 C^2 dk + 10 C dk dv + 8 C^2 dv + 2.5 C^3)."""
+    return 2.0 * (9 * C * C * dk + 10 * C * dk * dv + 8 * C * C * dv + 2.5 * C ** 3)
+
+
+def fp32_alu_tflops(sm_mhz, sms=152, lanes=128):
+    """FP32 CUDA-core peak: SMs x FP32 lanes per SM x 2 FLOP (FMA) x clock."""
+    return sms * lanes * 2 * sm_mhz * 1e6 / 1e12
+
+
 def chunk_bytes(B, H, T, dk, dv, esize, with_s0, with_st):
     """Algorithmic HBM bytes of one chunk forward: q, k, v, beta read, o
     written, plus the fp32 states read / written once per head."""
@@ -185,6 +198,30 @@ def timed_loop(fn, steps, stream, world):
     return region_s, [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def graph_decode(step, nsteps, stream, world):
+    """Captures step(0..nsteps-1) into one CUDA graph, replays it once to
+    warm up, then times one replay; returns (seconds, None) or (None, error)."""
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            for i in range(nsteps):
+                step(i)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(torch.cuda.current_stream())
+        g.replay()
+        e1.record(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1) / 1e3, world), None
+    except Exception as exc:  # reported in the JSON line, the eager numbers stand
+        return None, f"{type(exc).__name__}: {exc}"
+
+
 def cpu_oracle_sample(inp, budget_s=10.0, max_passes=50):
     """Times the fp64 oracle on whole batch elements of the workload (all H
     heads, all T tokens each), pass after pass, until `budget_s` has passed;
@@ -304,6 +341,28 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         dec_region_s, dec_launch = timed_loop(decode_step, nsteps, stream, world)
         dec_region_s = max_over_ranks(dec_region_s, world)
+
+        # The same steps captured once into a CUDA graph and replayed as one
+        # launch (no per-step host overhead); the state keeps evolving.
+        dec_graph = graph_decode(decode_step, nsteps, stream, world)
+
+        # ---------------- backward: gradients of the chunk forward ----------
+        d_o, d_S = workloads.grad_inputs(B, H, T, dv, dk, dtype=w["dtype"], seed=w["seed"],
+                                         ds_std=0.1)
+        d_o, d_S = d_o.to(dev), d_S.to(dev)
+        bws = torch.empty(lib.dn_chunk_bwd_workspace_bytes(B, H, T, dk, dv, C, 1 if tc else 0),
+                          dtype=torch.uint8, device=dev)
+
+        def bwd_step(_i):
+            dn.chunk_bwd(q, k, v, beta, d_o, d_final_state=d_S, workspace=bws)
+
+        bwd_steps = max(1, min(args.steps, 10))
+        for i in range(min(args.warmup, 3)):
+            bwd_step(i)
+        torch.cuda.synchronize()
+        bwd_region_s, bwd_launch = timed_loop(bwd_step, bwd_steps, stream, world)
+        bwd_region_s = max_over_ranks(bwd_region_s, world)
+        del d_o, d_S, bws
     clk = clocks.summary()
     del dq, dkk, dvv, db
 
@@ -364,9 +423,30 @@ def run_ours(args, rank, world, local):
                      "traffic": kernel_traffic("recurrent_step", "decode.cu"),
                      "peak_source": f"{peak_src} (copy bandwidth)", "bytes_per_launch": dbytes,
                      "launch_us": dec_launch_s * 1e6},
+        "graph": ({"value": world * Bd * nsteps / dec_graph[0], "unit": "tokens/s",
+                   "ms_per_step": 1e3 * dec_graph[0] / nsteps,
+                   "hbm_gbs": dbytes * nsteps / dec_graph[0] / 1e9,
+                   "frac": dbytes * nsteps / dec_graph[0] / 1e9 / peaks["hbm_gbs"],
+                   "launches": nsteps, "note": "all steps in one CUDA graph, one replay"}
+                  if dec_graph[0] else {"unavailable": dec_graph[1]}),
         "config": {"B": Bd, "H": Hd, "dk": dkd, "dv": dvd, "state": "fp32",
                    "io_dtype": wd["dtype"], "beta": "2*sigmoid(N(0,1))",
                    "l2": "state 537 MB per step > L2"},
+    }
+    nchunks = -(-T // C)
+    bflops = bwd_flops_per_chunk(C, dk, dv) * B * H * nchunks
+    bwd_launch_s = statistics.mean(bwd_launch) / 1e3
+    alu_peak = fp32_alu_tflops(2070.0)
+    backward = {
+        "workload": HEADLINE, "steps": bwd_steps, "value": world * tokens * bwd_steps / bwd_region_s,
+        "unit": "tokens/s", "ms_per_step": 1e3 * bwd_region_s / bwd_steps,
+        "arith": "fp32 CUDA cores", "launches_per_call": 3,
+        "roofline": {"bound": "alu", "achieved": bflops / bwd_launch_s / 1e12, "peak": alu_peak,
+                     "unit": "TFLOP/s", "frac": bflops / bwd_launch_s / 1e12 / alu_peak,
+                     "traffic": None,
+                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz",
+                     "flops_per_launch": bflops, "launch_us": bwd_launch_s * 1e6},
+        "config": {"d_o": "N(0,1)", "d_S_T": "N(0,0.1^2)", "S0": "none"},
     }
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -380,10 +460,12 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
         "decode": decode,
+        "backward": backward,
         "e2e": {"value": world * tokens * e2e_steps / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": 1e3 * e2e_s / e2e_steps},
-        "gpu_launches": launches_per_call * (args.steps + e2e_steps) + nsteps,
+        "gpu_launches": launches_per_call * (args.steps + e2e_steps) + nsteps
+                        + (nsteps if dec_graph[0] else 0) + 3 * bwd_steps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -57,11 +57,16 @@ int check_device_ptr(const Span& s, size_t align, int device) {
     return DN_OK;
 }
 
+// The calling thread's device, with its primary context made current: the
+// tensor maps are encoded through the driver, which needs a current context,
+// and a thread that has made no runtime call yet (an autograd worker, say)
+// has none.
 int current_device(int* dev) {
     cudaError_t e = cudaGetDevice(dev);
+    if (e == cudaSuccess) e = cudaSetDevice(*dev);
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return fail(DN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+        return fail(DN_ERR_CUDA, "cudaGetDevice/cudaSetDevice: %s", cudaGetErrorString(e));
     }
     return DN_OK;
 }
@@ -280,7 +285,7 @@ size_t dn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, 
         return 0;
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return 0;
-    return dn::chunk_bwd_workspace_bytes((int)BH, T, dk, dv);
+    return dn::chunk_bwd_workspace_bytes((int)BH, T, dk, dv, dt);
 }
 
 int dn_chunk_bwd(const void* q, const void* k, const void* v, const void* beta, const float* S0,
@@ -345,9 +350,12 @@ int dn_chunk_bwd(const void* q, const void* k, const void* v, const void* beta, 
                 "cudaMemcpyAsync(d_S0 <- d_S_T)");
         return cuda_status(cudaMemsetAsync(d_S0, 0, state_bytes, st), "cudaMemsetAsync(d_S0)");
     }
-    return cuda_status(dn::launch_chunk_bwd(q, k, v, beta, S0, d_o, d_S_T, d_q, d_k, d_v, d_beta,
-                                            d_S0, (int)BH, T, dk, dv, dt, workspace, st),
-                       "chunk backward (SIMT) launch");
+    const char* stage = "launch";
+    const cudaError_t e = dn::launch_chunk_bwd(q, k, v, beta, S0, d_o, d_S_T, d_q, d_k, d_v,
+                                               d_beta, d_S0, (int)BH, T, dk, dv, dt, workspace,
+                                               st, &stage);
+    if (e == cudaSuccess) return ok();
+    return fail(DN_ERR_CUDA, "chunk backward (%s): %s", stage, cudaGetErrorString(e));
 }
 
 }  // extern "C"

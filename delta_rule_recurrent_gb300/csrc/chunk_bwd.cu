@@ -21,7 +21,9 @@
 // column), so it runs per (batch, head, value slice); dQ, dK and dbeta sum
 // over all value channels, and every chunk's share needs only S and G at its
 // ends, so they run in parallel over all chunks.  Three launches:
-//   1. the CUDA-core forward without outputs, recording S at every chunk start;
+//   1. the forward without outputs, recording S at every chunk start (the
+//      tensor-core two-pass forward where it covers the shape, else the
+//      CUDA-core one);
 //   2. chunk_bwd_chain_kernel: per (b, h, value slice), chunks last to first:
 //      G at every chunk end, d_v, d_S0;
 //   3. chunk_bwd_grads_kernel: one CTA per (b, h, chunk): d_q, d_k, d_beta.
@@ -416,21 +418,31 @@ cudaError_t launch_bwd_dims(const void* q, const void* k, const void* v, const v
 
 }  // namespace
 
-size_t chunk_bwd_workspace_bytes(int BH, int T, int dk, int dv) {
+// Workspace: S at every chunk start, G at every chunk end (fp32), then the
+// tensor-core forward's own scratch where that path records the states.
+size_t chunk_bwd_workspace_bytes(int BH, int T, int dk, int dv, int dt) {
     if (BH <= 0 || T <= 0) return 0;
-    return 2 * (size_t)BH * (size_t)((T + kC - 1) / kC) * (size_t)dk * (size_t)dv * sizeof(float);
+    const size_t states =
+        2 * (size_t)BH * (size_t)((T + kC - 1) / kC) * (size_t)dk * (size_t)dv * sizeof(float);
+    return states + (chunk_tc_supports(dk, dv, dt) ? chunk_tc_workspace_bytes(BH, T) : 0);
 }
 
 cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const void* beta,
                              const float* S0, const void* d_o, const float* d_S_T, void* d_q,
                              void* d_k, void* d_v, void* d_beta, float* d_S0, int BH, int T,
-                             int dk, int dv, int dt, void* workspace, cudaStream_t stream) {
+                             int dk, int dv, int dt, void* workspace, cudaStream_t stream,
+                             const char** stage) {
     if (BH <= 0 || T <= 0) return cudaSuccess;
+    *stage = "state recompute";
+    const size_t per = (size_t)BH * ((T + kC - 1) / kC) * (size_t)dk * dv;
     float* const Sc = static_cast<float*>(workspace);
-    float* const Gc = Sc + (size_t)BH * ((T + kC - 1) / kC) * (size_t)dk * dv;
-    cudaError_t err = launch_chunk_simt(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt,
-                                        stream, Sc);
+    float* const Gc = Sc + per;
+    cudaError_t err = chunk_tc_supports(dk, dv, dt)
+        ? launch_chunk_tc(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt, Gc + per, stream,
+                          Sc)
+        : launch_chunk_simt(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt, stream, Sc);
     if (err != cudaSuccess) return err;
+    *stage = "gradient kernels";
     if (dt == 0)
         return launch_bwd_dims<float>(q, k, v, beta, d_o, d_S_T, d_q, d_k, d_v, d_beta, d_S0, Sc,
                                       Gc, BH, T, dk, dv, stream);

@@ -1236,10 +1236,15 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
     }
 }
 
-// 64 fp32 TMEM columns (lane of the calling thread) -> 32 bf16-pair columns.
-__device__ __forceinline__ void tmem_pack64(uint32_t src, uint32_t dst) {
+// 64 fp32 TMEM columns (lane of the calling thread) -> 32 bf16-pair columns;
+// with `rec`, the fp32 values also go to rec[e * kD], e = 0..63.
+__device__ __forceinline__ void tmem_pack64(uint32_t src, uint32_t dst, float* rec = nullptr) {
     float x[64];
     tmem_ld64f(src, x);
+    if (rec) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) rec[(size_t)e * kD] = x[e];
+    }
     uint32_t p[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) p[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
@@ -1247,8 +1252,8 @@ __device__ __forceinline__ void tmem_pack64(uint32_t src, uint32_t dst) {
 }
 
 __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
-                           const float* __restrict__ S0, float* __restrict__ S_T, int bh,
-                           int nchunks) {
+                           const float* __restrict__ S0, float* __restrict__ S_T,
+                           float* __restrict__ S_chunks, int bh, int nchunks) {
     constexpr int kBar = 1;
     const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
     // S0^T into TMEM: lane t holds dv column t of S0 (zeros without S0).
@@ -1266,8 +1271,10 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         const int g = c & 1;
         if (c > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(c - 1), t, kBar)) return;
         tc_fence_after_sync();
-        tmem_pack64(lane + C_ST, lane + C_SB);             // S^T -> bf16, dk 0-63
-        tmem_pack64(lane + C_ST + 64u, lane + C_SB + 32u);  // dk 64-127
+        // S^T -> bf16 (dk 0-63, then 64-127); S itself recorded when asked
+        float* const rec = S_chunks ? S_chunks + ((size_t)bh * nchunks + c) * kD * kD + t : nullptr;
+        tmem_pack64(lane + C_ST, lane + C_SB, rec);
+        tmem_pack64(lane + C_ST + 64u, lane + C_SB + 32u, rec ? rec + 64 * kD : nullptr);
         tmem_wait_st();
         tc_fence_before_sync();
         wg_sync(kBar);
@@ -1421,10 +1428,12 @@ __device__ void writer_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t
         // D1^T is free once the state has read the U' rows as well.
         if (t == 0) ok = ctl.wait(B_U_READ, (uint32_t)c) && (c + 1 >= nchunks || start(c + 1));
         const int tok0 = c * kC;
-        __nv_bfloat16* const ob = o + ((size_t)bh * T + tok0) * kD + t;
+        if (o) {  // (no outputs when only the chunk states are wanted)
+            __nv_bfloat16* const ob = o + ((size_t)bh * T + tok0) * kD + t;
 #pragma unroll
-        for (int r = 0; r < 64; ++r)
-            if (tok0 + r < T) ob[(size_t)r * kD] = __float2bfloat16_rn(ov[r]);
+            for (int r = 0; r < 64; ++r)
+                if (tok0 + r < T) ob[(size_t)r * kD] = __float2bfloat16_rn(ov[r]);
+        }
         if (wg_sync_or(kBar, !ok)) return;
     }
 }
@@ -1434,7 +1443,7 @@ __global__ void __launch_bounds__(512, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ws,
                   const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
-                  float* __restrict__ S_T, int T) {
+                  float* __restrict__ S_T, float* __restrict__ S_chunks, int T) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -1468,7 +1477,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (lane == 0) scan::producer(ctl, sm, &tm_q, &tm_k, &tm_v, &tm_ws, bh, nchunks);
     } else if (warp >= 4 && warp < 8) {
         const int t = tid - 128;
-        scan::state_body(ctl, sm, tmem, t, S0, S_T, bh, nchunks);
+        scan::state_body(ctl, sm, tmem, t, S0, S_T, S_chunks, bh, nchunks);
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 0);
     } else if (warp >= 8 && warp < 12) {
         const int t = tid - 256;
@@ -1547,14 +1556,18 @@ size_t chunk_tc_workspace_bytes(int BH, int T) {
 
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const void* beta,
                             const float* S0, void* o, float* S_T, int BH, int T, int dk, int dv,
-                            int dt, void* workspace, cudaStream_t stream) {
+                            int dt, void* workspace, cudaStream_t stream, float* S_chunks) {
     if (!chunk_tc_supports(dk, dv, dt)) return cudaErrorNotSupported;
     if (BH <= 0 || T <= 0) return cudaSuccess;
+    // Outputs may be skipped (o == nullptr) only on the two-pass path.
+    if (!workspace && (!o || S_chunks)) return cudaErrorInvalidValue;
     const int nchunks = (T + kC - 1) / kC;
     CUtensorMap mq, mk, mv, mo, mws;
+    memset(&mo, 0, sizeof(mo));
     memset(&mws, 0, sizeof(mws));
     if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mv, v, BH, T) ||
-        !make_map(&mo, o, BH, T) || (workspace && !make_ws_map(&mws, workspace, BH, nchunks)))
+        (!workspace && !make_map(&mo, o, BH, T)) ||
+        (workspace && !make_ws_map(&mws, workspace, BH, nchunks)))
         return cudaErrorInvalidValue;
     const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(beta);
     cudaError_t err;
@@ -1572,7 +1585,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
                                                                           (int)items);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
         chunk_scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(
-            mq, mk, mv, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, T);
+            mq, mk, mv, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, S_chunks, T);
         return cudaGetLastError();
     }
     if ((err = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

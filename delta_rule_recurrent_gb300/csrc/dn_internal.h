@@ -24,26 +24,30 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v,
 
 // Chunkwise backward (fp32 CUDA-core arithmetic): the gradients of
 // L = <d_o, o> + <d_S_T, S_T> for dn_chunk_fwd's outputs.  The workspace
-// holds chunk_bwd_workspace_bytes(BH, T, dk, dv) bytes: the state at the start
-// of every chunk and the gradient of the state at its end.  d_S_T, S0 and
+// holds chunk_bwd_workspace_bytes(BH, T, dk, dv, dt) bytes: the state at the
+// start of every chunk, the gradient of the state at its end, and the
+// tensor-core forward's scratch when that path recomputes the states.  d_S_T, S0 and
 // d_S0 may be nullptr.
-size_t chunk_bwd_workspace_bytes(int BH, int T, int dk, int dv);
+size_t chunk_bwd_workspace_bytes(int BH, int T, int dk, int dv, int dt);
 cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const void* beta,
                              const float* S0, const void* d_o, const float* d_S_T, void* d_q,
                              void* d_k, void* d_v, void* d_beta, float* d_S0, int BH, int T,
-                             int dk, int dv, int dt, void* workspace, cudaStream_t stream);
+                             int dk, int dv, int dt, void* workspace, cudaStream_t stream,
+                             const char** stage);
 
 // Chunkwise forward on tcgen05 tensor cores.  Returns cudaErrorNotSupported
 // (without launching) for shapes or dtypes it does not cover.  With a
 // workspace of chunk_tc_workspace_bytes(BH, T) bytes (16-byte aligned) it runs
 // in two passes: every chunk's [PT; Tm] in parallel, then the sequences;
-// with workspace == nullptr one fused kernel does both.
+// with workspace == nullptr one fused kernel does both.  On the two-pass path
+// o may be nullptr (no outputs) and S_chunks, if given, receives the fp32
+// state at the start of every chunk ([BH][ceil(T/64)][dk][dv]).
 bool chunk_tc_supports(int dk, int dv, int dt);
 size_t chunk_tc_workspace_bytes(int BH, int T);
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v,
                             const void* beta, const float* S0, void* o,
                             float* S_T, int BH, int T, int dk, int dv, int dt,
-                            void* workspace, cudaStream_t stream);
+                            void* workspace, cudaStream_t stream, float* S_chunks = nullptr);
 
 // As launch_chunk_tc with the workspace in a static device array of
 // noalloc_max_tiles tiles (the caller has checked the size).  The array's

@@ -196,8 +196,9 @@ DN_API int dn_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
  * S0.  The pages run this pass after the forward and recompute the chunk
  * states instead of storing them ("Hardware-efficient implementation",
  * section 3 of paperlayer.ai/abs/2406.06484v6); the result is the exact
- * gradient of the recurrence up to rounding.  The arithmetic is fp32 on
- * CUDA cores for both I/O types.
+ * gradient of the recurrence up to rounding.  The gradient arithmetic is
+ * fp32 on CUDA cores for both I/O types; the states are recomputed by the
+ * tensor-core forward where it covers the shape (bf16, dk = dv = 128).
  *
  * Arguments:
  *   q, k, v, beta, S0   as for dn_chunk_fwd (S0 may be NULL: zeros)
@@ -225,7 +226,9 @@ DN_API int dn_chunk_bwd(const void *q, const void *k, const void *v, const void 
 
 /* Scratch bytes dn_chunk_bwd needs: the fp32 state at the start of every
  * chunk and the gradient of the state at its end, 2 * B * H * ceil(T / 64) *
- * dk * dv * 4 bytes (0 for unsupported arguments).  Host-only. */
+ * dk * dv * 4 bytes, plus dn_chunk_fwd_workspace_bytes(...) where the
+ * tensor-core forward recomputes the states (0 for unsupported arguments).
+ * Host-only. */
 DN_API size_t dn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv,
                                     int C, int dt);
 

@@ -241,3 +241,34 @@ def test_rejects_bad_pointers_without_launching():
     assert call(None, o.data_ptr()) == _lib.DN_ERR_INVALID_ARG                 # NULL
     assert call(q.data_ptr(), o.data_ptr()) == _lib.DN_OK
     torch.cuda.synchronize()
+
+
+def test_tensor_core_path_from_a_fresh_thread():
+    """A thread that has made no CUDA runtime call has no current context;
+    the library makes the device's primary context current before it
+    encodes its tensor maps (through the driver), so the call works there."""
+    import threading
+    inp = workloads.chunk_inputs(1, 2, 130, 128, 128, dtype="bf16", seed=12, feature_map="silu")
+    q, k, v, b = (dev(x) for x in (inp.q, inp.k, inp.v, inp.beta))
+    o_main, S_main = dn_chunk(q, k, v, b)
+    out = {}
+
+    def worker():
+        try:
+            out["res"] = dn_chunk(q, k, v, b)
+        except Exception as exc:  # reported below
+            out["err"] = exc
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join()
+    assert "err" not in out, out.get("err")
+    torch.cuda.synchronize()
+    assert torch.equal(out["res"][0], o_main) and torch.equal(out["res"][1], S_main)
+
+
+def dn_chunk(q, k, v, b):
+    import delta_rule_recurrent_gb300 as dn
+    o, S = dn.chunk_fwd(q, k, v, b, algo="tcgen05")
+    torch.cuda.current_stream().synchronize()
+    return o, S

@@ -1,4 +1,4 @@
-// chunk_bwd.cu -- chunkwise delta-rule backward on CUDA cores, fp32 throughout.
+// chunk_bwd.cu -- chunkwise delta-rule backward (fp32 accumulation throughout).
 //
 // The training pass that follows the chunkwise forward ("Hardware-efficient
 // implementation", section 3 of paperlayer.ai/abs/2406.06484v6, which
@@ -27,6 +27,11 @@
 //   2. chunk_bwd_chain_kernel: per (b, h, value slice), chunks last to first:
 //      G at every chunk end, d_v, d_S0;
 //   3. chunk_bwd_grads_kernel: one CTA per (b, h, chunk): d_q, d_k, d_beta.
+// The products run as fp32 FMA for fp32 I/O (held to 1e-4) and as warp-level
+// tf32 tensor-core MMAs for bf16 I/O (simt_mm.cuh); the triangular solve is
+// fp32 on CUDA cores in both.
+#include <type_traits>
+
 #include "dn_common.cuh"
 #include "dn_internal.h"
 #include "simt_mm.cuh"
@@ -35,10 +40,7 @@
 namespace dn {
 namespace {
 
-using simt::for_each;
 using simt::kThreads;
-using simt::mm_acc;
-using simt::zero;
 constexpr int kC = 64;       // chunk length
 constexpr int kLC = kC + 1;  // odd row pitches keep shared-memory reads conflict-free
 static_assert(kLC == kTriPitch, "the solve's operand pitch");
@@ -56,40 +58,22 @@ __device__ __forceinline__ void load_rows(float* dst, const T* __restrict__ src,
 
 // A = tril(diag(beta) K K^T, -1) and P = tril(Q K^T) (diagonal included);
 // K K^T itself too when KK is given.
-template <int DK>
+template <class Ops, int DK>
 __device__ __forceinline__ void form_a_p(const float* Ks, const float* Qs, const float* bs,
                                          float* Am, float* Pm, float* KK) {
     constexpr int LK = DK + 1;
-    float aa[4][4], ap[4][4];
-    zero<64, 64>(aa);
-    zero<64, 64>(ap);
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-#pragma unroll 2
-    for (int kk = 0; kk < DK; ++kk) {
-        float ak[4], aq[4], bk[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            ak[i] = Ks[(ty + 16 * i) * LK + kk];
-            aq[i] = Qs[(ty + 16 * i) * LK + kk];
-            bk[i] = Ks[(tx + 16 * i) * LK + kk];
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                aa[i][j] = fmaf(ak[i], bk[j], aa[i][j]);
-                ap[i][j] = fmaf(aq[i], bk[j], ap[i][j]);
-            }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int m = ty + 16 * i, nn = tx + 16 * j;
-            Am[m * kLC + nn] = nn < m ? bs[m] * aa[i][j] : 0.f;
-            Pm[m * kLC + nn] = nn <= m ? ap[i][j] : 0.f;
-            if (KK) KK[m * kLC + nn] = aa[i][j];
-        }
+    typename Ops::template Acc<64, 64> aa, ap;
+    Ops::zero(aa);
+    Ops::zero(ap);
+    Ops::template mm<64, 64, DK>(aa, [&](int m, int i) { return Ks[m * LK + i]; },
+                                 [&](int i, int nn) { return Ks[nn * LK + i]; });
+    Ops::template mm<64, 64, DK>(ap, [&](int m, int i) { return Qs[m * LK + i]; },
+                                 [&](int i, int nn) { return Ks[nn * LK + i]; });
+    Ops::for_each(aa, [&](int m, int nn, float x) {
+        Am[m * kLC + nn] = nn < m ? bs[m] * x : 0.f;
+        if (KK) KK[m * kLC + nn] = x;
+    });
+    Ops::for_each(ap, [&](int m, int nn, float x) { Pm[m * kLC + nn] = nn <= m ? x : 0.f; });
 }
 
 // ------------------------------------------------------------------ chain
@@ -114,7 +98,7 @@ struct ChainSmem {
 // One CTA per (batch, head, slice of NV value channels): G = dL/dS from the
 // last chunk to the first.  Writes G at the end of every chunk (G_chunks,
 // [BH][chunk][dk][dv] fp32), d_v, and d_S0 (if given).
-template <typename T, int DK, int DV, int NV>
+template <class Ops, typename T, int DK, int DV, int NV>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
                        const T* __restrict__ beta, const T* __restrict__ d_o,
@@ -154,24 +138,24 @@ chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
         load_rows<NV, LV, DV>(Ds, d_o, tok0, t0, n, j0);
         if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
         __syncthreads();
-        form_a_p<DK>(Ks, Qs, bs, Am, Pm, nullptr);
+        form_a_p<Ops, DK>(Ks, Qs, bs, Am, Pm, nullptr);
         __syncthreads();
         {   // dU' = P^T dO + K G
-            float acc[4][NV / 16];
-            zero<64, NV>(acc);
-            mm_acc<64, NV, kC>(acc, [&](int m, int s) { return Pm[s * kLC + m]; },
+            typename Ops::template Acc<64, NV> acc;
+            Ops::zero(acc);
+            Ops::template mm<64, NV, kC>(acc, [&](int m, int s) { return Pm[s * kLC + m]; },
                                [&](int s, int nn) { return Ds[s * LV + nn]; });
-            mm_acc<64, NV, DK>(acc, [&](int m, int i) { return Ks[m * LK + i]; },
+            Ops::template mm<64, NV, DK>(acc, [&](int m, int i) { return Ks[m * LK + i]; },
                                [&](int i, int nn) { return Gs[i * LV + nn]; });
-            for_each<64, NV>(acc, [&](int m, int nn, float x) { Us[m * LV + nn] = x; });
+            Ops::for_each(acc, [&](int m, int nn, float x) { Us[m * LV + nn] = x; });
         }
         unit_lower_inverse64<kThreads>(Am, Xm, Ys);  // ends with a barrier
         {   // dV = Tm^T dU' = diag(beta) X^T dU'
-            float acc[4][NV / 16];
-            zero<64, NV>(acc);
-            mm_acc<64, NV, kC>(acc, [&](int m, int s) { return Xm[s * kLC + m]; },
+            typename Ops::template Acc<64, NV> acc;
+            Ops::zero(acc);
+            Ops::template mm<64, NV, kC>(acc, [&](int m, int s) { return Xm[s * kLC + m]; },
                                [&](int s, int nn) { return Us[s * LV + nn]; });
-            for_each<64, NV>(acc, [&](int m, int nn, float x) {
+            Ops::for_each(acc, [&](int m, int nn, float x) {
                 const float y = bs[m] * x;
                 Vs[m * LV + nn] = y;
                 if (m < n) d_v[(tok0 + t0 + m) * DV + j0 + nn] = from_f32<T>(y);
@@ -179,13 +163,13 @@ chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
         }
         __syncthreads();
         {   // G <- G + Q^T dO - K^T dV  (the gradient of the state chunk c starts from)
-            float acc[DK / 16][NV / 16];
-            zero<DK, NV>(acc);
-            mm_acc<DK, NV, kC>(acc, [&](int i, int s) { return Qs[s * LK + i]; },
+            typename Ops::template Acc<DK, NV> acc;
+            Ops::zero(acc);
+            Ops::template mm<DK, NV, kC>(acc, [&](int i, int s) { return Qs[s * LK + i]; },
                                [&](int s, int nn) { return Ds[s * LV + nn]; });
-            mm_acc<DK, NV, kC>(acc, [&](int i, int s) { return -Ks[s * LK + i]; },
+            Ops::template mm<DK, NV, kC>(acc, [&](int i, int s) { return -Ks[s * LK + i]; },
                                [&](int s, int nn) { return Vs[s * LV + nn]; });
-            for_each<DK, NV>(acc, [&](int i, int nn, float x) { Gs[i * LV + nn] += x; });
+            Ops::for_each(acc, [&](int i, int nn, float x) { Gs[i * LV + nn] += x; });
         }
         __syncthreads();
     }
@@ -226,7 +210,7 @@ struct GradSmem {
 // One CTA per (batch, head, chunk): the chunk's d_q, d_k and d_beta from S at
 // its start (S_chunks) and G at its end (G_chunks), over all value channels
 // in slices of NS.
-template <typename T, int DK, int DV>
+template <class Ops, typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
                        const T* __restrict__ v, const T* __restrict__ beta,
@@ -263,15 +247,16 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
     load_rows<DK, LK, DK>(Qs, q, tok0, t0, n, 0);
     if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
     __syncthreads();
-    form_a_p<DK>(Ks, Qs, bs, Am, Pm, KK);
+    form_a_p<Ops, DK>(Ks, Qs, bs, Am, Pm, KK);
     __syncthreads();
     unit_lower_inverse64<kThreads>(Am, Xm, Ys);  // ends with a barrier
 
-    float aQ[4][DK / 16], aK[4][DK / 16], aP[4][4], aT[4][4];
-    zero<64, DK>(aQ);
-    zero<64, DK>(aK);
-    zero<64, 64>(aP);
-    zero<64, 64>(aT);
+    typename Ops::template Acc<64, DK> aQ, aK;
+    typename Ops::template Acc<64, 64> aP, aT;
+    Ops::zero(aQ);
+    Ops::zero(aK);
+    Ops::zero(aP);
+    Ops::zero(aT);
     for (int js = 0; js < DV; js += NS) {
         load_rows<NS, LS, DV>(Vs, v, tok0, t0, n, js);
         load_rows<NS, LS, DV>(Ds, d_o, tok0, t0, n, js);
@@ -282,41 +267,41 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
         }
         __syncthreads();
         {   // R = V - K S and dU' = P^T dO + K G
-            float r[4][NS / 16], e[4][NS / 16];
-            zero<64, NS>(r);
-            zero<64, NS>(e);
-            mm_acc<64, NS, DK>(r, [&](int m, int i) { return Ks[m * LK + i]; },
+            typename Ops::template Acc<64, NS> r, e;
+            Ops::zero(r);
+            Ops::zero(e);
+            Ops::template mm<64, NS, DK>(r, [&](int m, int i) { return Ks[m * LK + i]; },
                                [&](int i, int nn) { return Ss[i * LS + nn]; });
-            mm_acc<64, NS, kC>(e, [&](int m, int s) { return Pm[s * kLC + m]; },
+            Ops::template mm<64, NS, kC>(e, [&](int m, int s) { return Pm[s * kLC + m]; },
                                [&](int s, int nn) { return Ds[s * LS + nn]; });
-            mm_acc<64, NS, DK>(e, [&](int m, int i) { return Ks[m * LK + i]; },
+            Ops::template mm<64, NS, DK>(e, [&](int m, int i) { return Ks[m * LK + i]; },
                                [&](int i, int nn) { return Gs[i * LS + nn]; });
-            for_each<64, NS>(r, [&](int m, int nn, float x) { Rs[m * LS + nn] = Vs[m * LS + nn] - x; });
-            for_each<64, NS>(e, [&](int m, int nn, float x) { Es[m * LS + nn] = x; });
+            Ops::for_each(r, [&](int m, int nn, float x) { Rs[m * LS + nn] = Vs[m * LS + nn] - x; });
+            Ops::for_each(e, [&](int m, int nn, float x) { Es[m * LS + nn] = x; });
         }
         __syncthreads();
         {   // U' = X diag(beta) R and dV = diag(beta) X^T dU'
-            float u[4][NS / 16], f[4][NS / 16];
-            zero<64, NS>(u);
-            zero<64, NS>(f);
-            mm_acc<64, NS, kC>(u, [&](int m, int s) { return Xm[m * kLC + s] * bs[s]; },
+            typename Ops::template Acc<64, NS> u, f;
+            Ops::zero(u);
+            Ops::zero(f);
+            Ops::template mm<64, NS, kC>(u, [&](int m, int s) { return Xm[m * kLC + s] * bs[s]; },
                                [&](int s, int nn) { return Rs[s * LS + nn]; });
-            mm_acc<64, NS, kC>(f, [&](int m, int s) { return Xm[s * kLC + m]; },
+            Ops::template mm<64, NS, kC>(f, [&](int m, int s) { return Xm[s * kLC + m]; },
                                [&](int s, int nn) { return Es[s * LS + nn]; });
-            for_each<64, NS>(u, [&](int m, int nn, float x) { Us[m * LS + nn] = x; });
-            for_each<64, NS>(f, [&](int m, int nn, float x) { Fs[m * LS + nn] = bs[m] * x; });
+            Ops::for_each(u, [&](int m, int nn, float x) { Us[m * LS + nn] = x; });
+            Ops::for_each(f, [&](int m, int nn, float x) { Fs[m * LS + nn] = bs[m] * x; });
         }
         __syncthreads();
         // dP += dO U'^T, dTm += dU' R^T, dQ += dO S^T, dK += U' G^T - dV S^T
-        mm_acc<64, 64, NS>(aP, [&](int m, int j) { return Ds[m * LS + j]; },
+        Ops::template mm<64, 64, NS>(aP, [&](int m, int j) { return Ds[m * LS + j]; },
                            [&](int j, int nn) { return Us[nn * LS + j]; });
-        mm_acc<64, 64, NS>(aT, [&](int m, int j) { return Es[m * LS + j]; },
+        Ops::template mm<64, 64, NS>(aT, [&](int m, int j) { return Es[m * LS + j]; },
                            [&](int j, int nn) { return Rs[nn * LS + j]; });
-        mm_acc<64, DK, NS>(aQ, [&](int m, int j) { return Ds[m * LS + j]; },
+        Ops::template mm<64, DK, NS>(aQ, [&](int m, int j) { return Ds[m * LS + j]; },
                            [&](int j, int i) { return Ss[i * LS + j]; });
-        mm_acc<64, DK, NS>(aK, [&](int m, int j) { return Us[m * LS + j]; },
+        Ops::template mm<64, DK, NS>(aK, [&](int m, int j) { return Us[m * LS + j]; },
                            [&](int j, int i) { return Gs[i * LS + j]; });
-        mm_acc<64, DK, NS>(aK, [&](int m, int j) { return -Fs[m * LS + j]; },
+        Ops::template mm<64, DK, NS>(aK, [&](int m, int j) { return -Fs[m * LS + j]; },
                            [&](int j, int i) { return Ss[i * LS + j]; });
         __syncthreads();
     }
@@ -326,44 +311,44 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
     float* dTs = dPm + kC * kLC;
     float* M1 = dTs + kC * kLC;
     float* dAm = M1 + kC * kLC;
-    for_each<64, 64>(aP, [&](int m, int nn, float x) { dPm[m * kLC + nn] = nn <= m ? x : 0.f; });
-    for_each<64, 64>(aT, [&](int m, int nn, float x) { dTs[m * kLC + nn] = x; });
+    Ops::for_each(aP, [&](int m, int nn, float x) { dPm[m * kLC + nn] = nn <= m ? x : 0.f; });
+    Ops::for_each(aT, [&](int m, int nn, float x) { dTs[m * kLC + nn] = x; });
     __syncthreads();
     // dQ += dP K, dK += dP^T Q
-    mm_acc<64, DK, kC>(aQ, [&](int m, int s) { return dPm[m * kLC + s]; },
+    Ops::template mm<64, DK, kC>(aQ, [&](int m, int s) { return dPm[m * kLC + s]; },
                        [&](int s, int i) { return Ks[s * LK + i]; });
-    mm_acc<64, DK, kC>(aK, [&](int m, int s) { return dPm[s * kLC + m]; },
+    Ops::template mm<64, DK, kC>(aK, [&](int m, int s) { return dPm[s * kLC + m]; },
                        [&](int s, int i) { return Qs[s * LK + i]; });
     {   // M1 = (dTm diag(beta)) X^T
-        float acc[4][4];
-        zero<64, 64>(acc);
-        mm_acc<64, 64, kC>(acc, [&](int m, int s) { return dTs[m * kLC + s] * bs[s]; },
+        typename Ops::template Acc<64, 64> acc;
+        Ops::zero(acc);
+        Ops::template mm<64, 64, kC>(acc, [&](int m, int s) { return dTs[m * kLC + s] * bs[s]; },
                            [&](int s, int nn) { return Xm[nn * kLC + s]; });
-        for_each<64, 64>(acc, [&](int m, int nn, float x) { M1[m * kLC + nn] = x; });
+        Ops::for_each(acc, [&](int m, int nn, float x) { M1[m * kLC + nn] = x; });
     }
     float db = 0.f;  // thread j < 64: dbeta_j
     if (tid < kC)
         for (int i = 0; i < kC; ++i) db = fmaf(Xm[i * kLC + tid], dTs[i * kLC + tid], db);
     __syncthreads();
     {   // dA = strict_tril(-X^T M1)
-        float acc[4][4];
-        zero<64, 64>(acc);
-        mm_acc<64, 64, kC>(acc, [&](int m, int s) { return Xm[s * kLC + m]; },
+        typename Ops::template Acc<64, 64> acc;
+        Ops::zero(acc);
+        Ops::template mm<64, 64, kC>(acc, [&](int m, int s) { return Xm[s * kLC + m]; },
                            [&](int s, int nn) { return M1[s * kLC + nn]; });
-        for_each<64, 64>(acc, [&](int m, int nn, float x) { dAm[m * kLC + nn] = nn < m ? -x : 0.f; });
+        Ops::for_each(acc, [&](int m, int nn, float x) { dAm[m * kLC + nn] = nn < m ? -x : 0.f; });
     }
     __syncthreads();
     if (tid < kC)
         for (int l = 0; l < kC; ++l) db = fmaf(dAm[tid * kLC + l], KK[tid * kLC + l], db);
     // dK += Z K with Z = diag(beta) dA + (diag(beta) dA)^T
-    mm_acc<64, DK, kC>(aK, [&](int m, int s) {
+    Ops::template mm<64, DK, kC>(aK, [&](int m, int s) {
         return bs[m] * dAm[m * kLC + s] + bs[s] * dAm[s * kLC + m];
     }, [&](int s, int i) { return Ks[s * LK + i]; });
 
-    for_each<64, DK>(aQ, [&](int m, int i, float x) {
+    Ops::for_each(aQ, [&](int m, int i, float x) {
         if (m < n) d_q[(tok0 + t0 + m) * DK + i] = from_f32<T>(x);
     });
-    for_each<64, DK>(aK, [&](int m, int i, float x) {
+    Ops::for_each(aK, [&](int m, int i, float x) {
         if (m < n) d_k[(tok0 + t0 + m) * DK + i] = from_f32<T>(x);
     });
     if (tid < n) d_beta[tok0 + t0 + tid] = from_f32<T>(db);
@@ -378,8 +363,10 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
     using LC = ChainSmem<DK, NV>;
     using LG = GradSmem<DK, 32>;
     const int nchunks = (Tlen + kC - 1) / kC;
-    auto chain = chunk_bwd_chain_kernel<T, DK, DV, NV>;
-    auto grads = chunk_bwd_grads_kernel<T, DK, DV>;
+    // fp32 I/O keeps fp32 products; bf16 I/O runs them on tf32 tensor cores.
+    using Ops = std::conditional_t<std::is_same_v<T, float>, simt::Fp32Ops, simt::Tf32Ops>;
+    auto chain = chunk_bwd_chain_kernel<Ops, T, DK, DV, NV>;
+    auto grads = chunk_bwd_grads_kernel<Ops, T, DK, DV>;
     cudaError_t err;
     if ((err = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)LC::kBytes)) != cudaSuccess ||

@@ -1,17 +1,141 @@
-// simt_mm.cuh -- register-tiled fp32 products for the CUDA-core chunk kernels.
+// simt_mm.cuh -- register-tiled products for the CUDA-core chunk kernels.
 //
-// A CTA of 256 threads is viewed as a 16 x 16 grid (tx = tid % 16,
-// ty = tid / 16); thread (ty, tx) owns the elements (ty + 16 i, tx + 16 j) of
-// an M x N result.  Operands are read through accessors, so the same loop
-// serves plain, transposed and masked operands in shared memory.
+// A CTA of 256 threads forms M x N products (M, N multiples of 64 and 16)
+// from operands in shared memory, read through accessors a(m, k) and
+// b(k, n), so the same loop serves plain, transposed and masked operands.
+// Two interchangeable policies with the same interface:
+//   Fp32Ops  fp32 FMA on CUDA cores: thread (ty, tx) = (tid / 16, tid % 16)
+//            owns the elements (ty + 16 i, tx + 16 j);
+//   Tf32Ops  warp-level m16n8k8 tensor-core MMAs with tf32 operands and fp32
+//            accumulation: warp w owns row blocks (w % 4) + 4 i of 16 rows
+//            and the half (w / 4) of the columns, in the m16n8 accumulator
+//            layout (lane 4g + q holds rows g, g + 8 at columns 2q, 2q + 1).
+// Both hold M N / 256 floats per thread; an accumulator is only ever read
+// through the for_each of the policy that filled it.
 #pragma once
+
+#include <stdint.h>
 
 namespace dn {
 namespace simt {
 
 constexpr int kThreads = 256;
 
-// acc[i][j] += sum_kk a(ty + 16 i, kk) * b(kk, tx + 16 j).
+struct Fp32Ops {
+    template <int M, int N>
+    struct Acc {
+        float v[M / 16][N / 16];
+    };
+
+    template <int M, int N>
+    static __device__ __forceinline__ void zero(Acc<M, N>& acc) {
+#pragma unroll
+        for (int i = 0; i < M / 16; ++i)
+#pragma unroll
+            for (int j = 0; j < N / 16; ++j) acc.v[i][j] = 0.f;
+    }
+
+    // acc += sum_kk a(m, kk) * b(kk, n)
+    template <int M, int N, int K, typename FA, typename FB>
+    static __device__ __forceinline__ void mm(Acc<M, N>& acc, FA a, FB b) {
+        const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll 4
+        for (int kk = 0; kk < K; ++kk) {
+            float av[M / 16], bv[N / 16];
+#pragma unroll
+            for (int i = 0; i < M / 16; ++i) av[i] = a(ty + 16 * i, kk);
+#pragma unroll
+            for (int j = 0; j < N / 16; ++j) bv[j] = b(kk, tx + 16 * j);
+#pragma unroll
+            for (int i = 0; i < M / 16; ++i)
+#pragma unroll
+                for (int j = 0; j < N / 16; ++j) acc.v[i][j] = fmaf(av[i], bv[j], acc.v[i][j]);
+        }
+    }
+
+    // f(m, n, value) for every element the calling thread owns
+    template <int M, int N, typename F>
+    static __device__ __forceinline__ void for_each(const Acc<M, N>& acc, F f) {
+        const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll
+        for (int i = 0; i < M / 16; ++i)
+#pragma unroll
+            for (int j = 0; j < N / 16; ++j) f(ty + 16 * i, tx + 16 * j, acc.v[i][j]);
+    }
+};
+
+struct Tf32Ops {
+    template <int M, int N>
+    struct Acc {
+        float v[M / 64][N / 16][4];
+    };
+
+    static __device__ __forceinline__ uint32_t tf32(float x) {
+        uint32_t r;
+        asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+        return r;
+    }
+
+    template <int M, int N>
+    static __device__ __forceinline__ void zero(Acc<M, N>& acc) {
+#pragma unroll
+        for (int i = 0; i < M / 64; ++i)
+#pragma unroll
+            for (int j = 0; j < N / 16; ++j)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc.v[i][j][r] = 0.f;
+    }
+
+    template <int M, int N, int K, typename FA, typename FB>
+    static __device__ __forceinline__ void mm(Acc<M, N>& acc, FA a, FB b) {
+        static_assert(K % 8 == 0, "K in steps of 8");
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+        const int m0 = 16 * (w & 3), n0 = (w >> 2) * (N / 2);
+#pragma unroll 2
+        for (int k = 0; k < K; k += 8) {
+            uint32_t af[M / 64][4], bf[N / 16][2];
+#pragma unroll
+            for (int i = 0; i < M / 64; ++i) {
+                const int r = m0 + 64 * i + g;
+                af[i][0] = tf32(a(r, k + q));
+                af[i][1] = tf32(a(r + 8, k + q));
+                af[i][2] = tf32(a(r, k + q + 4));
+                af[i][3] = tf32(a(r + 8, k + q + 4));
+            }
+#pragma unroll
+            for (int j = 0; j < N / 16; ++j) {
+                bf[j][0] = tf32(b(k + q, n0 + 8 * j + g));
+                bf[j][1] = tf32(b(k + q + 4, n0 + 8 * j + g));
+            }
+#pragma unroll
+            for (int i = 0; i < M / 64; ++i)
+#pragma unroll
+                for (int j = 0; j < N / 16; ++j)
+                    asm volatile(
+                        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, "
+                        "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                        : "+f"(acc.v[i][j][0]), "+f"(acc.v[i][j][1]), "+f"(acc.v[i][j][2]),
+                          "+f"(acc.v[i][j][3])
+                        : "r"(af[i][0]), "r"(af[i][1]), "r"(af[i][2]), "r"(af[i][3]),
+                          "r"(bf[j][0]), "r"(bf[j][1]));
+        }
+    }
+
+    template <int M, int N, typename F>
+    static __device__ __forceinline__ void for_each(const Acc<M, N>& acc, F f) {
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+        const int m0 = 16 * (w & 3), n0 = (w >> 2) * (N / 2);
+#pragma unroll
+        for (int i = 0; i < M / 64; ++i)
+#pragma unroll
+            for (int j = 0; j < N / 16; ++j)
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    f(m0 + 64 * i + g + 8 * (r >> 1), n0 + 8 * j + 2 * q + (r & 1), acc.v[i][j][r]);
+    }
+};
+
+// The CUDA-core forward's helpers (fp32 FMA, plain arrays).
 template <int M, int N, int K, typename FA, typename FB>
 __device__ __forceinline__ void mm_acc(float (&acc)[M / 16][N / 16], FA a, FB b) {
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -35,16 +159,6 @@ __device__ __forceinline__ void zero(float (&acc)[M / 16][N / 16]) {
     for (int i = 0; i < M / 16; ++i)
 #pragma unroll
         for (int j = 0; j < N / 16; ++j) acc[i][j] = 0.f;
-}
-
-// f(m, n, acc[i][j]) for every element the calling thread owns.
-template <int M, int N, typename F>
-__device__ __forceinline__ void for_each(const float (&acc)[M / 16][N / 16], F f) {
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-#pragma unroll
-    for (int i = 0; i < M / 16; ++i)
-#pragma unroll
-        for (int j = 0; j < N / 16; ++j) f(ty + 16 * i, tx + 16 * j, acc[i][j]);
 }
 
 }  // namespace simt

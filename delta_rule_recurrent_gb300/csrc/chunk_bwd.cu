@@ -41,9 +41,8 @@ namespace dn {
 namespace {
 
 using simt::kThreads;
-constexpr int kC = 64;       // chunk length
-constexpr int kLC = kC + 1;  // odd row pitches keep shared-memory reads conflict-free
-static_assert(kLC == kTriPitch, "the solve's operand pitch");
+constexpr int kC = 64;  // chunk length
+// Row pitches are the operand width plus the policy's padding (Ops::kPad).
 
 // Chunk rows [t0, t0 + 64) of a [T][D] tensor of head bh into shared memory
 // (row pitch LD, columns c0 .. c0 + W - 1), zeros past the end of the sequence.
@@ -61,7 +60,7 @@ __device__ __forceinline__ void load_rows(float* dst, const T* __restrict__ src,
 template <class Ops, int DK>
 __device__ __forceinline__ void form_a_p(const float* Ks, const float* Qs, const float* bs,
                                          float* Am, float* Pm, float* KK) {
-    constexpr int LK = DK + 1;
+    constexpr int LK = DK + Ops::kPad, kLC = kC + Ops::kPad;
     typename Ops::template Acc<64, 64> aa, ap;
     Ops::zero(aa);
     Ops::zero(ap);
@@ -77,9 +76,9 @@ __device__ __forceinline__ void form_a_p(const float* Ks, const float* Qs, const
 }
 
 // ------------------------------------------------------------------ chain
-template <int DK, int NV>
+template <int DK, int NV, int PAD>
 struct ChainSmem {
-    static constexpr int LK = DK + 1, LV = NV + 1;
+    static constexpr int LK = DK + PAD, LV = NV + PAD, kLC = kC + PAD;
     static constexpr int kK = 0;                  // C x LK   keys
     static constexpr int kQ = kK + kC * LK;       // C x LK   queries
     static constexpr int kD = kQ + kC * LK;       // C x LV   output gradient slice
@@ -93,6 +92,7 @@ struct ChainSmem {
     static constexpr int kB = kY + 3 * 16 * 17;   // C        beta
     static constexpr int kFloats = kB + kC;
     static constexpr size_t kBytes = sizeof(float) * kFloats;
+    static_assert(kBytes <= 232448, "one CTA's shared memory");
 };
 
 // One CTA per (batch, head, slice of NV value channels): G = dL/dS from the
@@ -104,8 +104,8 @@ chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
                        const T* __restrict__ beta, const T* __restrict__ d_o,
                        const float* __restrict__ d_S_T, T* __restrict__ d_v,
                        float* __restrict__ d_S0, float* __restrict__ G_chunks, int Tlen) {
-    using L = ChainSmem<DK, NV>;
-    constexpr int LK = L::LK, LV = L::LV, NSLICE = DV / NV;
+    using L = ChainSmem<DK, NV, Ops::kPad>;
+    constexpr int LK = L::LK, LV = L::LV, kLC = L::kLC, NSLICE = DV / NV;
     extern __shared__ float smem[];
     float* Ks = smem + L::kK;
     float* Qs = smem + L::kQ;
@@ -149,7 +149,7 @@ chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
                                [&](int i, int nn) { return Gs[i * LV + nn]; });
             Ops::for_each(acc, [&](int m, int nn, float x) { Us[m * LV + nn] = x; });
         }
-        unit_lower_inverse64<kThreads>(Am, Xm, Ys);  // ends with a barrier
+        unit_lower_inverse64<kThreads, kLC>(Am, Xm, Ys);  // ends with a barrier
         {   // dV = Tm^T dU' = diag(beta) X^T dU'
             typename Ops::template Acc<64, NV> acc;
             Ops::zero(acc);
@@ -182,19 +182,21 @@ chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
 }
 
 // ------------------------------------------------------------------ grads
-template <int DK, int NS>
+template <int DK, int NS, int PAD>
 struct GradSmem {
-    static constexpr int LK = DK + 1, LS = NS + 1;
+    static constexpr int LK = DK + PAD, LS = NS + PAD, kLC = kC + PAD;
     static constexpr int kK = 0;                  // C x LK   keys
     static constexpr int kQ = kK + kC * LK;       // C x LK   queries
-    static constexpr int kA = kQ + kC * LK;       // C x kLC  A
-    static constexpr int kX = kA + kC * kLC;      // C x kLC  (I + A)^{-1}
+    static constexpr int kX = kQ + kC * LK;       // C x kLC  (I + A)^{-1}
     static constexpr int kP = kX + kC * kLC;      // C x kLC  tril(Q K^T)
     static constexpr int kKK = kP + kC * kLC;     // C x kLC  K K^T
-    static constexpr int kY = kKK + kC * kLC;     // solve scratch
-    static constexpr int kB = kY + 3 * 16 * 17;   // C        beta
-    // value-slice operands, reused as C x kLC matrices once the slices are done
-    static constexpr int kV = kB + kC;            // C x LS   V
+    static constexpr int kB = kKK + kC * kLC;     // C        beta
+    // The work area: A and the solve scratch until X is formed, then the
+    // value-slice operands, then C x C matrices once the slices are done.
+    static constexpr int kW = kB + kC;
+    static constexpr int kA = kW;                 // C x kLC  A
+    static constexpr int kY = kA + kC * kLC;      // solve scratch
+    static constexpr int kV = kW;                 // C x LS   V
     static constexpr int kD = kV + kC * LS;       // C x LS   dO
     static constexpr int kR = kD + kC * LS;       // C x LS   R = V - K S
     static constexpr int kU = kR + kC * LS;       // C x LS   U'
@@ -204,7 +206,9 @@ struct GradSmem {
     static constexpr int kG = kS + DK * LS;       // DK x LS  G slice
     static constexpr int kFloats = kG + DK * LS;
     static constexpr size_t kBytes = sizeof(float) * kFloats;
-    static_assert(kFloats - kV >= 4 * kC * kLC, "room for dP, dTm, M1, dA");
+    static_assert(kFloats - kW >= 4 * kC * kLC, "room for dP, dTm, M1, dA");
+    static_assert(kFloats - kW >= kC * kLC + 3 * 16 * 17, "room for A and the solve scratch");
+    static_assert(kBytes <= 232448, "one CTA's shared memory");
 };
 
 // One CTA per (batch, head, chunk): the chunk's d_q, d_k and d_beta from S at
@@ -218,8 +222,8 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
                        const float* __restrict__ G_chunks, T* __restrict__ d_q,
                        T* __restrict__ d_k, T* __restrict__ d_beta, int Tlen, int nchunks) {
     constexpr int NS = 32;
-    using L = GradSmem<DK, NS>;
-    constexpr int LK = L::LK, LS = L::LS;
+    using L = GradSmem<DK, NS, Ops::kPad>;
+    constexpr int LK = L::LK, LS = L::LS, kLC = L::kLC;
     extern __shared__ float smem[];
     float* Ks = smem + L::kK;
     float* Qs = smem + L::kQ;
@@ -249,7 +253,7 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
     __syncthreads();
     form_a_p<Ops, DK>(Ks, Qs, bs, Am, Pm, KK);
     __syncthreads();
-    unit_lower_inverse64<kThreads>(Am, Xm, Ys);  // ends with a barrier
+    unit_lower_inverse64<kThreads, kLC>(Am, Xm, Ys);  // ends with a barrier
 
     typename Ops::template Acc<64, DK> aQ, aK;
     typename Ops::template Acc<64, 64> aP, aT;
@@ -306,8 +310,8 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
         __syncthreads();
     }
 
-    // The slice area now holds C x C matrices.
-    float* dPm = smem + L::kV;
+    // The work area now holds C x C matrices.
+    float* dPm = smem + L::kW;
     float* dTs = dPm + kC * kLC;
     float* M1 = dTs + kC * kLC;
     float* dAm = M1 + kC * kLC;
@@ -360,11 +364,11 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
                              void* d_beta, float* d_S0, float* Sc, float* Gc, int BH, int Tlen,
                              cudaStream_t stream) {
     constexpr int NV = DV < 64 ? DV : 64;
-    using LC = ChainSmem<DK, NV>;
-    using LG = GradSmem<DK, 32>;
-    const int nchunks = (Tlen + kC - 1) / kC;
     // fp32 I/O keeps fp32 products; bf16 I/O runs them on tf32 tensor cores.
     using Ops = std::conditional_t<std::is_same_v<T, float>, simt::Fp32Ops, simt::Tf32Ops>;
+    using LC = ChainSmem<DK, NV, Ops::kPad>;
+    using LG = GradSmem<DK, 32, Ops::kPad>;
+    const int nchunks = (Tlen + kC - 1) / kC;
     auto chain = chunk_bwd_chain_kernel<Ops, T, DK, DV, NV>;
     auto grads = chunk_bwd_grads_kernel<Ops, T, DK, DV>;
     cudaError_t err;

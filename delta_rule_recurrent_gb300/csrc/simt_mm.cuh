@@ -11,7 +11,10 @@
 //            and the half (w / 4) of the columns, in the m16n8 accumulator
 //            layout (lane 4g + q holds rows g, g + 8 at columns 2q, 2q + 1).
 // Both hold M N / 256 floats per thread; an accumulator is only ever read
-// through the for_each of the policy that filled it.
+// through the for_each of the policy that filled it.  kPad is the row padding
+// (floats) that keeps the policy's shared-memory operand reads free of bank
+// conflicts: an odd pitch for the per-thread FMA pattern, a pitch of 4 mod 32
+// for the fragment pattern (rows g = 0..7 by columns q = 0..3).
 #pragma once
 
 #include <stdint.h>
@@ -22,6 +25,8 @@ namespace simt {
 constexpr int kThreads = 256;
 
 struct Fp32Ops {
+    static constexpr int kPad = 1;
+
     template <int M, int N>
     struct Acc {
         float v[M / 16][N / 16];
@@ -65,6 +70,8 @@ struct Fp32Ops {
 };
 
 struct Tf32Ops {
+    static constexpr int kPad = 4;
+
     template <int M, int N>
     struct Acc {
         float v[M / 64][N / 16][4];

@@ -10,17 +10,16 @@
 
 namespace dn {
 
-constexpr int kTriPitch = 65;  // row pitch (floats) of the 64 x 64 operands
+constexpr int kTriPitch = 65;  // default row pitch (floats) of the 64 x 64 operands
 
-// A and X are 64 x 64 fp32 in shared memory with row pitch kTriPitch; Ys is
+// A and X are 64 x 64 fp32 in shared memory with row pitch L; Ys is
 // 3 x 16 x 17 floats of scratch.  The four 16 x 16 diagonal blocks are
 // inverted by column-wise substitution, then the block diagonals below them
 // follow from X_ij = -X_ii * sum_{l=j}^{i-1} A_il X_lj.  All NT threads of the
 // block must call it; it ends with a barrier.
-template <int NT>
+template <int NT, int L = kTriPitch>
 __device__ void unit_lower_inverse64(const float* __restrict__ Am, float* __restrict__ Xm,
                                      float* __restrict__ Ys) {
-    constexpr int L = kTriPitch;
     const int tid = threadIdx.x;
     if (tid < 64) {
         const int base = (tid >> 4) * 16, c = tid & 15;

@@ -40,16 +40,15 @@
 namespace dn {
 namespace {
 
-using simt::kThreads;
 constexpr int kC = 64;  // chunk length
 // Row pitches are the operand width plus the policy's padding (Ops::kPad).
 
 // Chunk rows [t0, t0 + 64) of a [T][D] tensor of head bh into shared memory
 // (row pitch LD, columns c0 .. c0 + W - 1), zeros past the end of the sequence.
-template <int W, int LD, int D, typename T>
+template <int NT, int W, int LD, int D, typename T>
 __device__ __forceinline__ void load_rows(float* dst, const T* __restrict__ src, size_t tok0,
                                           int t0, int n, int c0) {
-    for (int e = threadIdx.x; e < kC * W; e += kThreads) {
+    for (int e = threadIdx.x; e < kC * W; e += NT) {
         const int t = e / W, i = e % W;
         dst[t * LD + i] = t < n ? to_f32(src[(tok0 + t0 + t) * D + c0 + i]) : 0.f;
     }
@@ -99,13 +98,13 @@ struct ChainSmem {
 // last chunk to the first.  Writes G at the end of every chunk (G_chunks,
 // [BH][chunk][dk][dv] fp32), d_v, and d_S0 (if given).
 template <class Ops, typename T, int DK, int DV, int NV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Ops::kThreads, 1)
 chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
                        const T* __restrict__ beta, const T* __restrict__ d_o,
                        const float* __restrict__ d_S_T, T* __restrict__ d_v,
                        float* __restrict__ d_S0, float* __restrict__ G_chunks, int Tlen) {
     using L = ChainSmem<DK, NV, Ops::kPad>;
-    constexpr int LK = L::LK, LV = L::LV, kLC = L::kLC, NSLICE = DV / NV;
+    constexpr int LK = L::LK, LV = L::LV, kLC = L::kLC, NSLICE = DV / NV, NT = Ops::kThreads;
     extern __shared__ float smem[];
     float* Ks = smem + L::kK;
     float* Qs = smem + L::kQ;
@@ -123,19 +122,19 @@ chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
     const size_t tok0 = (size_t)bh * Tlen;
     const int nchunks = (Tlen + kC - 1) / kC;
 
-    for (int e = tid; e < DK * NV; e += kThreads) {
+    for (int e = tid; e < DK * NV; e += NT) {
         const int i = e / NV, jj = e % NV;
         Gs[i * LV + jj] = d_S_T ? d_S_T[((size_t)bh * DK + i) * DV + j0 + jj] : 0.f;
     }
     for (int c = nchunks - 1; c >= 0; --c) {
         const int t0 = c * kC, n = min(kC, Tlen - t0);
-        for (int e = tid; e < DK * NV; e += kThreads) {  // G at the end of chunk c
+        for (int e = tid; e < DK * NV; e += NT) {  // G at the end of chunk c
             const int i = e / NV, jj = e % NV;
             G_chunks[(((size_t)bh * nchunks + c) * DK + i) * DV + j0 + jj] = Gs[i * LV + jj];
         }
-        load_rows<DK, LK, DK>(Ks, k, tok0, t0, n, 0);
-        load_rows<DK, LK, DK>(Qs, q, tok0, t0, n, 0);
-        load_rows<NV, LV, DV>(Ds, d_o, tok0, t0, n, j0);
+        load_rows<NT, DK, LK, DK>(Ks, k, tok0, t0, n, 0);
+        load_rows<NT, DK, LK, DK>(Qs, q, tok0, t0, n, 0);
+        load_rows<NT, NV, LV, DV>(Ds, d_o, tok0, t0, n, j0);
         if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
         __syncthreads();
         form_a_p<Ops, DK>(Ks, Qs, bs, Am, Pm, nullptr);
@@ -149,7 +148,7 @@ chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
                                [&](int i, int nn) { return Gs[i * LV + nn]; });
             Ops::for_each(acc, [&](int m, int nn, float x) { Us[m * LV + nn] = x; });
         }
-        unit_lower_inverse64<kThreads, kLC>(Am, Xm, Ys);  // ends with a barrier
+        unit_lower_inverse64<NT, kLC>(Am, Xm, Ys);  // ends with a barrier
         {   // dV = Tm^T dU' = diag(beta) X^T dU'
             typename Ops::template Acc<64, NV> acc;
             Ops::zero(acc);
@@ -174,7 +173,7 @@ chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
         __syncthreads();
     }
     if (d_S0) {
-        for (int e = tid; e < DK * NV; e += kThreads) {
+        for (int e = tid; e < DK * NV; e += NT) {
             const int i = e / NV, jj = e % NV;
             d_S0[((size_t)bh * DK + i) * DV + j0 + jj] = Gs[i * LV + jj];
         }
@@ -215,7 +214,7 @@ struct GradSmem {
 // its start (S_chunks) and G at its end (G_chunks), over all value channels
 // in slices of NS.
 template <class Ops, typename T, int DK, int DV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Ops::kThreads, 1)
 chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
                        const T* __restrict__ v, const T* __restrict__ beta,
                        const T* __restrict__ d_o, const float* __restrict__ S_chunks,
@@ -223,7 +222,7 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
                        T* __restrict__ d_k, T* __restrict__ d_beta, int Tlen, int nchunks) {
     constexpr int NS = 32;
     using L = GradSmem<DK, NS, Ops::kPad>;
-    constexpr int LK = L::LK, LS = L::LS, kLC = L::kLC;
+    constexpr int LK = L::LK, LS = L::LS, kLC = L::kLC, NT = Ops::kThreads;
     extern __shared__ float smem[];
     float* Ks = smem + L::kK;
     float* Qs = smem + L::kQ;
@@ -247,13 +246,13 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
     const size_t tok0 = (size_t)bh * Tlen;
     const size_t st0 = ((size_t)bh * nchunks + c) * DK * DV;
 
-    load_rows<DK, LK, DK>(Ks, k, tok0, t0, n, 0);
-    load_rows<DK, LK, DK>(Qs, q, tok0, t0, n, 0);
+    load_rows<NT, DK, LK, DK>(Ks, k, tok0, t0, n, 0);
+    load_rows<NT, DK, LK, DK>(Qs, q, tok0, t0, n, 0);
     if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
     __syncthreads();
     form_a_p<Ops, DK>(Ks, Qs, bs, Am, Pm, KK);
     __syncthreads();
-    unit_lower_inverse64<kThreads, kLC>(Am, Xm, Ys);  // ends with a barrier
+    unit_lower_inverse64<NT, kLC>(Am, Xm, Ys);  // ends with a barrier
 
     typename Ops::template Acc<64, DK> aQ, aK;
     typename Ops::template Acc<64, 64> aP, aT;
@@ -262,9 +261,9 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
     Ops::zero(aP);
     Ops::zero(aT);
     for (int js = 0; js < DV; js += NS) {
-        load_rows<NS, LS, DV>(Vs, v, tok0, t0, n, js);
-        load_rows<NS, LS, DV>(Ds, d_o, tok0, t0, n, js);
-        for (int e = tid; e < DK * NS; e += kThreads) {
+        load_rows<NT, NS, LS, DV>(Vs, v, tok0, t0, n, js);
+        load_rows<NT, NS, LS, DV>(Ds, d_o, tok0, t0, n, js);
+        for (int e = tid; e < DK * NS; e += NT) {
             const int i = e / NS, jj = e % NS;
             Ss[i * LS + jj] = S_chunks[st0 + (size_t)i * DV + js + jj];
             Gs[i * LS + jj] = G_chunks[st0 + (size_t)i * DV + js + jj];
@@ -365,7 +364,7 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
                              cudaStream_t stream) {
     constexpr int NV = DV < 64 ? DV : 64;
     // fp32 I/O keeps fp32 products; bf16 I/O runs them on tf32 tensor cores.
-    using Ops = std::conditional_t<std::is_same_v<T, float>, simt::Fp32Ops, simt::Tf32Ops>;
+    using Ops = std::conditional_t<std::is_same_v<T, float>, simt::Fp32Ops, simt::Tf32Ops<8>>;
     using LC = ChainSmem<DK, NV, Ops::kPad>;
     using LG = GradSmem<DK, 32, Ops::kPad>;
     const int nchunks = (Tlen + kC - 1) / kC;
@@ -379,11 +378,11 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
         return err;
     const long long g_chain = (long long)BH * (DV / NV), g_grads = (long long)BH * nchunks;
     if (g_chain > 0x7fffffffLL || g_grads > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    chain<<<(unsigned)g_chain, kThreads, LC::kBytes, stream>>>(
+    chain<<<(unsigned)g_chain, Ops::kThreads, LC::kBytes, stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(beta),
         static_cast<const T*>(d_o), d_S_T, static_cast<T*>(d_v), d_S0, Gc, Tlen);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    grads<<<(unsigned)g_grads, kThreads, LG::kBytes, stream>>>(
+    grads<<<(unsigned)g_grads, Ops::kThreads, LG::kBytes, stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
         static_cast<const T*>(beta), static_cast<const T*>(d_o), Sc, Gc, static_cast<T*>(d_q),
         static_cast<T*>(d_k), static_cast<T*>(d_beta), Tlen, nchunks);

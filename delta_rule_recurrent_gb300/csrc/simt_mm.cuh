@@ -1,17 +1,18 @@
 // simt_mm.cuh -- register-tiled products for the CUDA-core chunk kernels.
 //
-// A CTA of 256 threads forms M x N products (M, N multiples of 64 and 16)
-// from operands in shared memory, read through accessors a(m, k) and
-// b(k, n), so the same loop serves plain, transposed and masked operands.
+// A CTA of kThreads threads forms M x N products (M a multiple of 64, N of
+// 16 or 32) from operands in shared memory, read through accessors a(m, k)
+// and b(k, n), so the same loop serves plain, transposed and masked operands.
 // Two interchangeable policies with the same interface:
-//   Fp32Ops  fp32 FMA on CUDA cores: thread (ty, tx) = (tid / 16, tid % 16)
-//            owns the elements (ty + 16 i, tx + 16 j);
-//   Tf32Ops  warp-level m16n8k8 tensor-core MMAs with tf32 operands and fp32
-//            accumulation: warp w owns row blocks (w % 4) + 4 i of 16 rows
-//            and the half (w / 4) of the columns, in the m16n8 accumulator
-//            layout (lane 4g + q holds rows g, g + 8 at columns 2q, 2q + 1).
-// Both hold M N / 256 floats per thread; an accumulator is only ever read
-// through the for_each of the policy that filled it.  kPad is the row padding
+//   Fp32Ops      fp32 FMA on CUDA cores, 256 threads: thread (ty, tx) =
+//                (tid / 16, tid % 16) owns the elements (ty + 16 i, tx + 16 j);
+//   Tf32Ops<NW>  warp-level m16n8k8 tensor-core MMAs with tf32 operands and
+//                fp32 accumulation, NW warps: warp w owns row blocks
+//                (w % 4) + 4 i of 16 rows and column part w / 4 of NW / 4,
+//                in the m16n8 accumulator layout (lane 4g + q holds rows g,
+//                g + 8 at columns 2q, 2q + 1).
+// Each holds M N / kThreads floats per thread; an accumulator is only ever
+// read through the for_each of the policy that filled it.  kPad is the row padding
 // (floats) that keeps the policy's shared-memory operand reads free of bank
 // conflicts: an odd pitch for the per-thread FMA pattern, a pitch of 4 mod 32
 // for the fragment pattern (rows g = 0..7 by columns q = 0..3).
@@ -26,6 +27,7 @@ constexpr int kThreads = 256;
 
 struct Fp32Ops {
     static constexpr int kPad = 1;
+    static constexpr int kThreads = 256;
 
     template <int M, int N>
     struct Acc {
@@ -69,26 +71,28 @@ struct Fp32Ops {
     }
 };
 
+template <int NW>
 struct Tf32Ops {
     static constexpr int kPad = 4;
+    static constexpr int kThreads = 32 * NW;
+    static constexpr int kParts = NW / 4;  // column parts
 
     template <int M, int N>
     struct Acc {
-        float v[M / 64][N / 16][4];
+        static_assert(N % (8 * kParts) == 0, "whole n8 tiles per warp");
+        float v[M / 64][N / (8 * kParts)][4];
     };
 
-    static __device__ __forceinline__ uint32_t tf32(float x) {
-        uint32_t r;
-        asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-        return r;
-    }
+    // The fp32 bit pattern as a tf32 operand: the MMA reads its upper 19
+    // bits, i.e. the value truncated to tf32 (no separate rounding step).
+    static __device__ __forceinline__ uint32_t tf32(float x) { return __float_as_uint(x); }
 
     template <int M, int N>
     static __device__ __forceinline__ void zero(Acc<M, N>& acc) {
 #pragma unroll
         for (int i = 0; i < M / 64; ++i)
 #pragma unroll
-            for (int j = 0; j < N / 16; ++j)
+            for (int j = 0; j < N / (8 * kParts); ++j)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) acc.v[i][j][r] = 0.f;
     }
@@ -96,11 +100,12 @@ struct Tf32Ops {
     template <int M, int N, int K, typename FA, typename FB>
     static __device__ __forceinline__ void mm(Acc<M, N>& acc, FA a, FB b) {
         static_assert(K % 8 == 0, "K in steps of 8");
+        constexpr int NJ = N / (8 * kParts);
         const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-        const int m0 = 16 * (w & 3), n0 = (w >> 2) * (N / 2);
+        const int m0 = 16 * (w & 3), n0 = (w >> 2) * (N / kParts);
 #pragma unroll 2
         for (int k = 0; k < K; k += 8) {
-            uint32_t af[M / 64][4], bf[N / 16][2];
+            uint32_t af[M / 64][4], bf[NJ][2];
 #pragma unroll
             for (int i = 0; i < M / 64; ++i) {
                 const int r = m0 + 64 * i + g;
@@ -110,14 +115,14 @@ struct Tf32Ops {
                 af[i][3] = tf32(a(r + 8, k + q + 4));
             }
 #pragma unroll
-            for (int j = 0; j < N / 16; ++j) {
+            for (int j = 0; j < NJ; ++j) {
                 bf[j][0] = tf32(b(k + q, n0 + 8 * j + g));
                 bf[j][1] = tf32(b(k + q + 4, n0 + 8 * j + g));
             }
 #pragma unroll
             for (int i = 0; i < M / 64; ++i)
 #pragma unroll
-                for (int j = 0; j < N / 16; ++j)
+                for (int j = 0; j < NJ; ++j)
                     asm volatile(
                         "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, "
                         "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
@@ -131,11 +136,11 @@ struct Tf32Ops {
     template <int M, int N, typename F>
     static __device__ __forceinline__ void for_each(const Acc<M, N>& acc, F f) {
         const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-        const int m0 = 16 * (w & 3), n0 = (w >> 2) * (N / 2);
+        const int m0 = 16 * (w & 3), n0 = (w >> 2) * (N / kParts);
 #pragma unroll
         for (int i = 0; i < M / 64; ++i)
 #pragma unroll
-            for (int j = 0; j < N / 16; ++j)
+            for (int j = 0; j < N / (8 * kParts); ++j)
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
                     f(m0 + 64 * i + g + 8 * (r >> 1), n0 + 8 * j + 2 * q + (r & 1), acc.v[i][j][r]);

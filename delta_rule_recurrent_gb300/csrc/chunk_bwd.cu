@@ -43,15 +43,51 @@ namespace {
 constexpr int kC = 64;  // chunk length
 // Row pitches are the operand width plus the policy's padding (Ops::kPad).
 
-// Chunk rows [t0, t0 + 64) of a [T][D] tensor of head bh into shared memory
-// (row pitch LD, columns c0 .. c0 + W - 1), zeros past the end of the sequence.
+// 16 bytes of T from global memory (16-byte aligned) as floats.
+__device__ __forceinline__ void load16(const float* p, float (&x)[4]) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+}
+__device__ __forceinline__ void load16(const __nv_bfloat16* p, float (&x)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        x[2 * j] = __uint_as_float(w[j] << 16);
+        x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+}
+
+// Rows [r0, r0 + R) of a row-major tensor with row length D, columns
+// c0 .. c0 + W - 1, into shared memory with row pitch LD; rows at or past
+// n (relative to r0) read as zeros.  16-byte loads, several in flight per
+// thread (row starts and c0 are multiples of 16 bytes).
+template <int NT, int R, int W, int LD, int D, typename T>
+__device__ __forceinline__ void load_tile(float* dst, const T* __restrict__ src, size_t r0,
+                                          int n, int c0) {
+    constexpr int V = 16 / sizeof(T), PER = W / V;
+    static_assert(W % V == 0, "whole 16-byte groups");
+#pragma unroll 4
+    for (int e = threadIdx.x; e < R * PER; e += NT) {
+        const int t = e / PER, i = (e % PER) * V;
+        float x[V];
+        if (t < n) {
+            load16(src + (r0 + t) * D + c0 + i, x);
+        } else {
+#pragma unroll
+            for (int j = 0; j < V; ++j) x[j] = 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < V; ++j) dst[t * LD + i + j] = x[j];
+    }
+}
+
+// Chunk rows [t0, t0 + 64) of a [T][D] tensor of head bh (tok0 = bh * T),
+// zeros past the end of the sequence.
 template <int NT, int W, int LD, int D, typename T>
 __device__ __forceinline__ void load_rows(float* dst, const T* __restrict__ src, size_t tok0,
                                           int t0, int n, int c0) {
-    for (int e = threadIdx.x; e < kC * W; e += NT) {
-        const int t = e / W, i = e % W;
-        dst[t * LD + i] = t < n ? to_f32(src[(tok0 + t0 + t) * D + c0 + i]) : 0.f;
-    }
+    load_tile<NT, kC, W, LD, D>(dst, src, tok0 + t0, n, c0);
 }
 
 // A = tril(diag(beta) K K^T, -1) and P = tril(Q K^T) (diagonal included);
@@ -263,11 +299,8 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
     for (int js = 0; js < DV; js += NS) {
         load_rows<NT, NS, LS, DV>(Vs, v, tok0, t0, n, js);
         load_rows<NT, NS, LS, DV>(Ds, d_o, tok0, t0, n, js);
-        for (int e = tid; e < DK * NS; e += NT) {
-            const int i = e / NS, jj = e % NS;
-            Ss[i * LS + jj] = S_chunks[st0 + (size_t)i * DV + js + jj];
-            Gs[i * LS + jj] = G_chunks[st0 + (size_t)i * DV + js + jj];
-        }
+        load_tile<NT, DK, NS, LS, DV>(Ss, S_chunks + st0, 0, DK, js);
+        load_tile<NT, DK, NS, LS, DV>(Gs, G_chunks + st0, 0, DK, js);
         __syncthreads();
         {   // R = V - K S and dU' = P^T dO + K G
             typename Ops::template Acc<64, NS> r, e;

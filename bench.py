@@ -59,6 +59,10 @@ def fp32_alu_tflops(sm_mhz, sms=152, lanes=128):
     return sms * lanes * 2 * sm_mhz * 1e6 / 1e12
 
 
+# Nominal dense tensor rates per GB300 (PFLOP/s): tf32 against bf16.
+TF32_PER_BF16 = 1.1 / 2.25
+
+
 def chunk_bytes(B, H, T, dk, dv, esize, with_s0, with_st):
     """Algorithmic HBM bytes of one chunk forward: q, k, v, beta read, o
     written, plus the fp32 states read / written once per head."""
@@ -436,15 +440,20 @@ def run_ours(args, rank, world, local):
     nchunks = -(-T // C)
     bflops = bwd_flops_per_chunk(C, dk, dv) * B * H * nchunks
     bwd_launch_s = statistics.mean(bwd_launch) / 1e3
-    alu_peak = fp32_alu_tflops(2070.0)
+    if tc:  # bf16 I/O: the products run as tf32 MMAs (the solve and the rest on CUDA cores)
+        bpeak = peaks["bf16_tflops"] * TF32_PER_BF16
+        bbound, barith = "tensor", "tf32 mma.sync products, fp32 accumulation"
+        bsrc = f"{peak_src} bf16 burst x nominal tf32/bf16 ratio (1.1/2.25)"
+    else:
+        bpeak, bbound, barith = fp32_alu_tflops(2070.0), "alu", "fp32 CUDA cores"
+        bsrc = "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz"
     backward = {
         "workload": HEADLINE, "steps": bwd_steps, "value": world * tokens * bwd_steps / bwd_region_s,
         "unit": "tokens/s", "ms_per_step": 1e3 * bwd_region_s / bwd_steps,
-        "arith": "fp32 CUDA cores", "launches_per_call": 3,
-        "roofline": {"bound": "alu", "achieved": bflops / bwd_launch_s / 1e12, "peak": alu_peak,
-                     "unit": "TFLOP/s", "frac": bflops / bwd_launch_s / 1e12 / alu_peak,
-                     "traffic": None,
-                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz",
+        "arith": barith, "launches_per_call": 3,
+        "roofline": {"bound": bbound, "achieved": bflops / bwd_launch_s / 1e12, "peak": bpeak,
+                     "unit": "TFLOP/s", "frac": bflops / bwd_launch_s / 1e12 / bpeak,
+                     "traffic": None, "peak_source": bsrc,
                      "flops_per_launch": bflops, "launch_us": bwd_launch_s * 1e6},
         "config": {"d_o": "N(0,1)", "d_S_T": "N(0,0.1^2)", "S0": "none"},
     }

@@ -23,6 +23,7 @@
 #include "dn_common.cuh"
 #include "dn_internal.h"
 #include "simt_mm.cuh"
+#include "tile_load.cuh"
 #include "tri_inverse.cuh"
 
 namespace dn {
@@ -94,16 +95,9 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
             }
         }
         // ---- load the chunk (padding rows: k = q = v = 0, beta = 0) ----
-        for (int e = tid; e < kC * DK; e += kThreads) {
-            const int t = e / DK, i = e % DK;
-            const size_t g = (tok0 + t0 + t) * DK + i;
-            Ks[t * LK + i] = t < n ? to_f32(k[g]) : 0.f;
-            Qs[t * LK + i] = t < n ? to_f32(q[g]) : 0.f;
-        }
-        for (int e = tid; e < kC * NV; e += kThreads) {
-            const int t = e / NV, jj = e % NV;
-            Rs[t * LV + jj] = t < n ? to_f32(v[(tok0 + t0 + t) * DV + j0 + jj]) : 0.f;
-        }
+        load_tile<kThreads, kC, DK, LK, DK>(Ks, k, tok0 + t0, n, 0);
+        load_tile<kThreads, kC, DK, LK, DK>(Qs, q, tok0 + t0, n, 0);
+        load_tile<kThreads, kC, NV, LV, DV>(Rs, v, tok0 + t0, n, j0);
         if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
         __syncthreads();
 

@@ -1251,6 +1251,9 @@ __device__ __forceinline__ void tmem_pack64(uint32_t src, uint32_t dst, float* r
     tmem_st32(dst, p);
 }
 
+// kRec: also record S at every chunk start (the backward's recompute); the
+// forward proper is compiled without it, so its state chain carries no test.
+template <bool kRec>
 __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                            const float* __restrict__ S0, float* __restrict__ S_T,
                            float* __restrict__ S_chunks, int bh, int nchunks) {
@@ -1272,9 +1275,14 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         if (c > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(c - 1), t, kBar)) return;
         tc_fence_after_sync();
         // S^T -> bf16 (dk 0-63, then 64-127); S itself recorded when asked
-        float* const rec = S_chunks ? S_chunks + ((size_t)bh * nchunks + c) * kD * kD + t : nullptr;
-        tmem_pack64(lane + C_ST, lane + C_SB, rec);
-        tmem_pack64(lane + C_ST + 64u, lane + C_SB + 32u, rec ? rec + 64 * kD : nullptr);
+        if constexpr (kRec) {
+            float* const rec = S_chunks + ((size_t)bh * nchunks + c) * kD * kD + t;
+            tmem_pack64(lane + C_ST, lane + C_SB, rec);
+            tmem_pack64(lane + C_ST + 64u, lane + C_SB + 32u, rec + 64 * kD);
+        } else {
+            tmem_pack64(lane + C_ST, lane + C_SB);
+            tmem_pack64(lane + C_ST + 64u, lane + C_SB + 32u);
+        }
         tmem_wait_st();
         tc_fence_before_sync();
         wg_sync(kBar);
@@ -1439,6 +1447,7 @@ __device__ void writer_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t
 }
 }  // namespace scan
 
+template <bool kRec>
 __global__ void __launch_bounds__(512, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ws,
@@ -1477,7 +1486,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (lane == 0) scan::producer(ctl, sm, &tm_q, &tm_k, &tm_v, &tm_ws, bh, nchunks);
     } else if (warp >= 4 && warp < 8) {
         const int t = tid - 128;
-        scan::state_body(ctl, sm, tmem, t, S0, S_T, S_chunks, bh, nchunks);
+        scan::state_body<kRec>(ctl, sm, tmem, t, S0, S_T, S_chunks, bh, nchunks);
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 0);
     } else if (warp >= 8 && warp < 12) {
         const int t = tid - 256;
@@ -1574,17 +1583,17 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
     if (workspace) {
         const long long items = (long long)BH * nchunks;
         if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+        auto scan_kernel = S_chunks ? chunk_scan_kernel<true> : chunk_scan_kernel<false>;
         if ((err = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kPrepSmemBytes)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(chunk_scan_kernel,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+            (err = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         scan::kSmemBytes)) != cudaSuccess)
             return err;
         const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
         chunk_prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(mq, mk, mws, b, T, nchunks,
                                                                           (int)items);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
-        chunk_scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(
+        scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(
             mq, mk, mv, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, S_chunks, T);
         return cudaGetLastError();
     }

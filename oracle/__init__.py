@@ -49,7 +49,7 @@ def build(force: bool = False) -> Path:
     _BUILD_DIR.mkdir(exist_ok=True)
     tmp = _BUILD_DIR / f"libdn_oracle.{os.getpid()}.so"
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
-           "-ffp-contract=off", "-fno-fast-math", str(_SRC), "-o", str(tmp)]
+           "-ffp-contract=off", "-fno-fast-math", str(_SRC), "-o", str(tmp), "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -68,6 +68,8 @@ def _load():
         lib.dn_oracle_forward.restype = ctypes.c_int
         lib.dn_oracle_backward.argtypes = [dp] * 12 + [ctypes.c_long] * 4 + [ctypes.c_int]
         lib.dn_oracle_backward.restype = ctypes.c_int
+        lib.dn_oracle_forward_gated.argtypes = [dp] * 7 + [ctypes.c_long] * 4 + [ctypes.c_int]
+        lib.dn_oracle_forward_gated.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -190,3 +192,34 @@ def backward(q, k, v, beta, dO, S0=None, dS_T=None, nthreads: int | None = None,
     if rc != 0:
         raise MemoryError("oracle could not allocate its state history")
     return dq, dkk, dvv, db, dS0
+
+
+def forward_gated(q, k, v, beta, g, S0=None, nthreads: int | None = None):
+    """Gated DeltaNet over a whole sequence: the keep rate exp(g_t) decays the
+    state before each delta-rule update (forget, predict, correct, write,
+    read).  ``g``: ``[B, H, T]`` log keep rates.  Other arguments and the
+    result ``(o, S_T)`` as for ``forward``."""
+    q, k, v, beta, g = _f64(q), _f64(k), _f64(v), _f64(beta), _f64(g)
+    B, H, T, dk = q.shape
+    dv = v.shape[3]
+    if (k.shape != q.shape or v.shape[:3] != (B, H, T) or beta.shape != (B, H, T)
+            or g.shape != (B, H, T)):
+        raise ValueError("q, k [B,H,T,dk]; v [B,H,T,dv]; beta and g [B,H,T]")
+    S = np.zeros((B, H, dk, dv)) if S0 is None else _f64(S0).copy()
+    o = np.zeros((B, H, T, dv))
+    if B * H == 0 or T == 0:
+        return o, S
+    n = host_cores() if nthreads is None else int(nthreads)
+    rc = _load().dn_oracle_forward_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                                         _ptr(S), _ptr(o), B * H, T, dk, dv, n)
+    if rc != 0:
+        raise MemoryError("oracle could not allocate its scratch vector")
+    return o, S
+
+
+def recurrent_step_gated(q, k, v, beta, g, S, nthreads: int | None = None):
+    """One gated decoding step (``g``: ``[B, H]``); returns ``(o, S_new)``."""
+    q, k, v, beta, g = _f64(q), _f64(k), _f64(v), _f64(beta), _f64(g)
+    o, S_new = forward_gated(q[:, :, None, :], k[:, :, None, :], v[:, :, None, :],
+                             beta[:, :, None], g[:, :, None], S, nthreads=nthreads)
+    return o[:, :, 0, :], S_new

@@ -34,6 +34,7 @@
  *   S      [BH][dk][dv]     holds S_0 on entry and S_T on return.
  * BH is the number of independent (batch, head) pairs.
  */
+#include <math.h>
 #include <stdlib.h>
 
 /* The pages' S(j,i) for a state stored as [dk][dv]. */
@@ -228,6 +229,78 @@ int dn_oracle_backward(const double *q, const double *k, const double *v,
                           dS0 + h * n, T, dk_, dv, states, G, e, du);
         }
         free(states);
+    }
+    return failed ? -1 : 0;
+}
+
+/*
+ * Gated DeltaNet ("Gated DeltaNet", garden.houmin.site/infra/delta-net;
+ * "Gated DeltaNet : oublier d'abord l'état entier", fr.news.hada.io/topic?id=31925):
+ * a scalar keep rate alpha_t = exp(g_t) per token decays the whole state
+ * before the delta rule, in the order the second page fixes:
+ *   forget       S~ = alpha_t S_{t-1}
+ *   predict      p = S~ k_t
+ *   correct      u = beta_t (v_t - p)
+ *   write        S_t = S~ + u k_t^T
+ *   read         o_t = S_t q_t
+ * i.e. S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T.
+ * g is the log keep rate ([BH][T], fp64), as implementations store it.
+ */
+static void run_one_head_gated(const double *q, const double *k, const double *v,
+                               const double *beta, const double *g, double *S, double *o,
+                               long T, long dk, long dv, double *p)
+{
+    for (long t = 0; t < T; ++t) {
+        const double *kt = k + t * dk;
+        const double *qt = q + t * dk;
+        const double *vt = v + t * dv;
+        double *ot = o + t * dv;
+        const double alpha = exp(g[t]);
+        for (long j = 0; j < dv; ++j)           /* forget */
+            for (long i = 0; i < dk; ++i)
+                S_AT(S, dv, j, i) *= alpha;
+        for (long j = 0; j < dv; ++j) {         /* predict */
+            double acc = 0.0;
+            for (long i = 0; i < dk; ++i)
+                acc += S_AT(S, dv, j, i) * kt[i];
+            p[j] = acc;
+        }
+        for (long j = 0; j < dv; ++j) {         /* correct and write */
+            const double u = beta[t] * (vt[j] - p[j]);
+            for (long i = 0; i < dk; ++i)
+                S_AT(S, dv, j, i) += u * kt[i];
+        }
+        for (long j = 0; j < dv; ++j) {         /* read */
+            double acc = 0.0;
+            for (long i = 0; i < dk; ++i)
+                acc += S_AT(S, dv, j, i) * qt[i];
+            ot[j] = acc;
+        }
+    }
+}
+
+int dn_oracle_forward_gated(const double *q, const double *k, const double *v,
+                            const double *beta, const double *g, double *S, double *o,
+                            long BH, long T, long dk, long dv, int nthreads)
+{
+    int failed = 0;
+    if (nthreads < 1)
+        nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)(dv > 0 ? dv : 1));
+        if (!p) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long n = 0; n < BH; ++n) {
+            if (!p)
+                continue;
+            run_one_head_gated(q + n * T * dk, k + n * T * dk, v + n * T * dv, beta + n * T,
+                               g + n * T, S + n * dk * dv, o + n * T * dv, T, dk, dv, p);
+        }
+        free(p);
     }
     return failed ? -1 : 0;
 }

@@ -11,6 +11,8 @@ the computation runs in the library's sm_103a kernels.
     chunk_bwd(q, k, v, beta, d_o, initial_state=None, d_final_state=None)
         -> (d_q, d_k, d_v, d_beta, d_initial_state)   # training backward
     DeltaRule.apply(q, k, v, beta, initial_state)     # autograd: (o, final_state)
+    chunk_fwd_gated(q, k, v, beta, g, ...), recurrent_step_gated(q, k, v, beta, g, state)
+        # Gated DeltaNet: log keep rate g per token (per head for a step)
 
 Shapes: q, k ``[B, H, T, dk]``; v ``[B, H, T, dv]``; beta ``[B, H, T]``;
 state ``[B, H, dk, dv]`` fp32 (the pages' dv x dk state, transposed).  For a
@@ -23,8 +25,9 @@ import torch
 from ._lib import (DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05, DN_BF16, DN_F32,
                    DeltaNetError, check, header_symbols, lib_path, load)
 
-__all__ = ["chunk_fwd", "chunk_bwd", "recurrent_step", "DeltaRule", "DeltaNetError", "load",
-           "lib_path", "header_symbols", "ALGOS"]
+__all__ = ["chunk_fwd", "chunk_bwd", "recurrent_step", "chunk_fwd_gated",
+           "recurrent_step_gated", "DeltaRule", "DeltaNetError", "load", "lib_path",
+           "header_symbols", "ALGOS"]
 
 ALGOS = {"auto": DN_ALGO_AUTO, "simt": DN_ALGO_SIMT, "tcgen05": DN_ALGO_TCGEN05}
 _DT = {torch.float32: DN_F32, torch.bfloat16: DN_BF16}
@@ -215,3 +218,72 @@ class DeltaRule(torch.autograd.Function):
         d_S_T = None if d_S_T is None else d_S_T.contiguous().float()
         d_q, d_k, d_v, d_beta, d_S0 = chunk_bwd(q, k, v, beta, d_o.to(v.dtype), S0, d_S_T)
         return d_q, d_k, d_v, d_beta, (d_S0 if S0 is not None else None)
+
+
+def _check_gate(g: torch.Tensor, shape, dev) -> None:
+    _check_cuda("g", g, dev)
+    if g.dtype != torch.float32 or tuple(g.shape) != tuple(shape):
+        raise ValueError(f"g must be float32 {list(shape)}")
+
+
+def chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                    g: torch.Tensor, initial_state: torch.Tensor | None = None,
+                    output_final_state: bool = True, chunk_size: int = 64,
+                    out: torch.Tensor | None = None, final_state: torch.Tensor | None = None):
+    """Gated DeltaNet, chunkwise (``dn_chunk_fwd_gated``): ``g`` is the fp32
+    ``[B, H, T]`` log keep rate.  Returns ``(o, S_T)`` as ``chunk_fwd``."""
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
+        _check_cuda(name, t, dev)
+    dt = _dtype_code(q)
+    if not (k.dtype == v.dtype == beta.dtype == q.dtype):
+        raise TypeError("q, k, v and beta must share one dtype")
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4:
+        raise ValueError("q, k must be [B,H,T,dk] and v [B,H,T,dv]")
+    B, H, T, dk = q.shape
+    dv = v.shape[3]
+    if tuple(v.shape[:3]) != (B, H, T) or tuple(beta.shape) != (B, H, T):
+        raise ValueError("v must be [B,H,T,dv] and beta [B,H,T]")
+    _check_gate(g, (B, H, T), dev)
+    if initial_state is not None:
+        _check_cuda("initial_state", initial_state, dev)
+        if initial_state.dtype != torch.float32 or tuple(initial_state.shape) != (B, H, dk, dv):
+            raise ValueError("initial_state must be float32 [B,H,dk,dv]")
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev)
+    S_T = None
+    if output_final_state:
+        S_T = final_state if final_state is not None else torch.empty(
+            (B, H, dk, dv), dtype=torch.float32, device=dev)
+    lib = load()
+    with torch.cuda.device(dev):
+        check(lib.dn_chunk_fwd_gated(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(), g.data_ptr(),
+            initial_state.data_ptr() if initial_state is not None else None, out.data_ptr(),
+            S_T.data_ptr() if S_T is not None else None, B, H, T, dk, dv, chunk_size, dt,
+            _stream_handle(dev)))
+    return out, S_T
+
+
+def recurrent_step_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                         g: torch.Tensor, state: torch.Tensor,
+                         out: torch.Tensor | None = None) -> torch.Tensor:
+    """One Gated DeltaNet decoding step (``dn_recurrent_step_gated``); ``g``
+    is the fp32 ``[B, H]`` log keep rate; ``state`` is updated in place."""
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("state", state)):
+        _check_cuda(name, t, dev)
+    dt = _dtype_code(q)
+    B, H, dk = q.shape
+    dv = v.shape[2]
+    _check_gate(g, (B, H), dev)
+    if state.dtype != torch.float32 or tuple(state.shape) != (B, H, dk, dv):
+        raise ValueError("state must be float32 [B,H,dk,dv]")
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=q.dtype, device=dev)
+    lib = load()
+    with torch.cuda.device(dev):
+        check(lib.dn_recurrent_step_gated(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                          beta.data_ptr(), g.data_ptr(), state.data_ptr(),
+                                          out.data_ptr(), B, H, dk, dv, dt, _stream_handle(dev)))
+    return out

@@ -34,6 +34,8 @@ SIGNATURES = {
     "dn_chunk_bwd": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _fp, _vp, _vp, _vp, _vp, _fp]
                      + [_int] * 7 + [_vp, _size, _vp]),
     "dn_chunk_bwd_workspace_bytes": (_size, [_int] * 7),
+    "dn_chunk_fwd_gated": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp] + [_int] * 7 + [_vp]),
+    "dn_recurrent_step_gated": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp] + [_int] * 5 + [_vp]),
     "dn_status_string": (ctypes.c_char_p, [_int]),
     "dn_last_error": (ctypes.c_char_p, []),
     "dn_abi_version": (_int, []),

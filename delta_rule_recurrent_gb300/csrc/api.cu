@@ -251,6 +251,89 @@ int dn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const void
         "chunk forward (tcgen05, static scratch) launch");
 }
 
+int dn_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* beta,
+                       const float* g, const float* S0, void* o, float* S_T, int B, int H,
+                       int T, int dk, int dv, int C, int dt, void* stream) {
+    if (B < 0 || H < 0 || T < 0)
+        return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d T=%d)", B, H, T);
+    if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
+    if (dk <= 0 || dv <= 0 || C <= 0)
+        return fail(DN_ERR_INVALID_ARG, "dk, dv and C must be positive");
+    if (!supported_dim(dk) || !supported_dim(dv))
+        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this build supports 64 and 128", dk, dv);
+    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this build supports 64", C);
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
+    if (BH == 0) return ok();
+    const size_t es = elem_size(dt);
+    const size_t ntok = (size_t)BH * (size_t)T;
+    const size_t state_bytes = (size_t)BH * dk * dv * sizeof(float);
+    const Span sq{"q", q, ntok * dk * es}, sk{"k", k, ntok * dk * es}, sv{"v", v, ntok * dv * es},
+        sb{"beta", beta, ntok * es}, sg{"g", g, ntok * sizeof(float)}, so{"o", o, ntok * dv * es},
+        s0{"S0", S0, state_bytes}, sT{"S_T", S_T, state_bytes};
+    int dev = 0;
+    if (int st = current_device(&dev)) return st;
+    if (T > 0) {
+        for (const Span* s : {&sq, &sk, &sv, &so})
+            if (int st = check_device_ptr(*s, 16, dev)) return st;
+        if (int st = check_device_ptr(sb, es, dev)) return st;
+        if (int st = check_device_ptr(sg, sizeof(float), dev)) return st;
+    }
+    if (S0)
+        if (int st = check_device_ptr(s0, 16, dev)) return st;
+    if (S_T)
+        if (int st = check_device_ptr(sT, 16, dev)) return st;
+    if (T > 0)
+        for (const Span* s : {&sq, &sk, &sv, &sb, &sg, &s0, &sT})
+            if (overlaps(so, *s)) return fail(DN_ERR_INVALID_ARG, "o overlaps %s", s->name);
+    for (const Span* s : {&sq, &sk, &sv, &sb, &sg})
+        if (T > 0 && overlaps(sT, *s)) return fail(DN_ERR_INVALID_ARG, "S_T overlaps %s", s->name);
+    if (S_T && S0 && S_T != S0 && overlaps(sT, s0))
+        return fail(DN_ERR_INVALID_ARG, "S_T partly overlaps S0");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        if (!S_T || S_T == S0) return ok();
+        if (S0)
+            return cuda_status(cudaMemcpyAsync(S_T, S0, state_bytes, cudaMemcpyDeviceToDevice, st),
+                               "cudaMemcpyAsync(S_T <- S0)");
+        return cuda_status(cudaMemsetAsync(S_T, 0, state_bytes, st), "cudaMemsetAsync(S_T)");
+    }
+    return cuda_status(dn::launch_chunk_simt(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, st,
+                                             nullptr, g),
+                       "gated chunk forward launch");
+}
+
+int dn_recurrent_step_gated(const void* q, const void* k, const void* v, const void* beta,
+                            const float* g, float* S, void* o, int B, int H, int dk, int dv,
+                            int dt, void* stream) {
+    if (B < 0 || H < 0) return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d)", B, H);
+    if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
+    if (dk <= 0 || dv <= 0) return fail(DN_ERR_INVALID_ARG, "dk and dv must be positive");
+    if (!supported_dim(dk) || !supported_dim(dv))
+        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this build supports 64 and 128", dk, dv);
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
+    if (BH == 0) return ok();
+    const size_t es = elem_size(dt);
+    const Span sq{"q", q, (size_t)BH * dk * es}, sk{"k", k, (size_t)BH * dk * es},
+        sv{"v", v, (size_t)BH * dv * es}, sb{"beta", beta, (size_t)BH * es},
+        sg{"g", g, (size_t)BH * sizeof(float)}, so{"o", o, (size_t)BH * dv * es},
+        sS{"S", S, (size_t)BH * dk * dv * sizeof(float)};
+    int dev = 0;
+    if (int st = current_device(&dev)) return st;
+    for (const Span* s : {&sq, &sk, &sv, &so, &sS})
+        if (int st = check_device_ptr(*s, 16, dev)) return st;
+    if (int st = check_device_ptr(sb, es, dev)) return st;
+    if (int st = check_device_ptr(sg, sizeof(float), dev)) return st;
+    for (const Span* s : {&sq, &sk, &sv, &sb, &sg, &sS})
+        if (overlaps(so, *s)) return fail(DN_ERR_INVALID_ARG, "o overlaps %s", s->name);
+    for (const Span* s : {&sq, &sk, &sv, &sb, &sg})
+        if (overlaps(sS, *s)) return fail(DN_ERR_INVALID_ARG, "S overlaps %s", s->name);
+    return cuda_status(dn::launch_recurrent_step(q, k, v, beta, S, o, (int)BH, dk, dv, dt,
+                                                 static_cast<cudaStream_t>(stream), g),
+                       "gated recurrent step launch");
+}
+
 int dn_recurrent_step(const void* q, const void* k, const void* v, const void* beta, float* S,
                       void* o, int B, int H, int dk, int dv, int dt, void* stream) {
     if (B < 0 || H < 0) return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d)", B, H);

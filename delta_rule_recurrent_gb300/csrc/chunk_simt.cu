@@ -20,6 +20,18 @@
 // (S_chunks, [BH][chunk][dk][dv] fp32) and skip the outputs (o == nullptr).  Value
 // channels are independent in every step above, so slices never exchange
 // data; the key-side work (A, X, Q K^T) is recomputed per slice.
+//
+// Gated DeltaNet (a log keep rate g_t per token, alpha_t = exp(g_t); "Gated
+// DeltaNet : oublier d'abord l'état entier", fr.news.hada.io/topic?id=31925,
+// and "Gated DeltaNet", garden.houmin.site/infra/delta-net) runs through the
+// same kernel.  With G_t the cumulative log decay from the chunk start
+// (G = 0 without g, which makes every factor below exactly 1):
+//     A   = tril(diag(beta) (K K^T . exp(G_i - G_j)), -1)
+//     R'  = diag(beta) (V - diag(exp G) K S)
+//     O   = diag(exp G) Q S + (Q K^T . M . exp(G_i - G_j)) U'
+//     S  <- exp(G_C) S + K^T diag(exp(G_C - G_s)) U'
+// (the state S / Gamma_t follows the plain rule on values v_t / Gamma_t; the
+// ratios of Gamma within a chunk are at most 1).
 #include "dn_common.cuh"
 #include "dn_internal.h"
 #include "simt_mm.cuh"
@@ -48,7 +60,8 @@ struct SimtSmem {
     static constexpr int kP = kX + kC * kLC;           // C x kLC  Q K^T . M
     static constexpr int kY = kP + kC * kLC;           // 3 x 16 x 17 solve scratch
     static constexpr int kB = kY + 3 * 16 * 17;        // C        beta
-    static constexpr int kFloats = kB + kC;
+    static constexpr int kG = kB + kC;                 // 3 x C    G, exp(G), exp(G_C - G)
+    static constexpr int kFloats = kG + 3 * kC;
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
 
@@ -57,7 +70,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
                   const T* __restrict__ v, const T* __restrict__ beta,
                   const float* __restrict__ S0, T* __restrict__ o,
-                  float* __restrict__ S_T, float* __restrict__ S_chunks, int Tlen) {
+                  float* __restrict__ S_T, float* __restrict__ S_chunks,
+                  const float* __restrict__ g, int Tlen) {
     using L = SimtSmem<DK, NV>;
     constexpr int LK = L::LK, LV = L::LV;
     constexpr int NSLICE = DV / NV;
@@ -72,6 +86,9 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
     float* Pm = smem + L::kP;
     float* Ys = smem + L::kY;
     float* bs = smem + L::kB;
+    float* Gc = smem + L::kG;          // cumulative log decay within the chunk
+    float* eG = Gc + kC;               // exp(G_t)
+    float* dec = eG + kC;              // exp(G_C - G_t)
 
     const int tid = threadIdx.x;
     const int tx = tid & 15, ty = tid >> 4;
@@ -99,6 +116,25 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
         load_tile<kThreads, kC, DK, LK, DK>(Qs, q, tok0 + t0, n, 0);
         load_tile<kThreads, kC, NV, LV, DV>(Rs, v, tok0 + t0, n, j0);
         if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
+        if (tid < 32) {  // prefix sums of the log keep rates (padding tokens keep everything)
+            const int t = 2 * tid;
+            const float a = (g && t < n) ? g[tok0 + t0 + t] : 0.f;
+            const float b = (g && t + 1 < n) ? g[tok0 + t0 + t + 1] : 0.f;
+            float incl = a + b;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (tid >= off) incl += y;
+            }
+            const float last = __shfl_sync(0xffffffffu, incl, 31);
+            const float g0 = incl - b;
+            Gc[t] = g0;
+            Gc[t + 1] = incl;
+            eG[t] = expf(g0);
+            eG[t + 1] = expf(incl);
+            dec[t] = expf(last - g0);
+            dec[t + 1] = expf(last - incl);
+        }
         __syncthreads();
 
         // ---- A = tril(diag(beta) K K^T, -1) and P = tril(Q K^T) ----
@@ -128,13 +164,14 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int m = ty + 16 * i, nn = tx + 16 * j;
-                    Am[m * kLC + nn] = nn < m ? bs[m] * aa[i][j] : 0.f;
-                    Pm[m * kLC + nn] = nn <= m ? ap[i][j] : 0.f;
+                    const float r = nn <= m ? expf(Gc[m] - Gc[nn]) : 0.f;
+                    Am[m * kLC + nn] = nn < m ? bs[m] * (aa[i][j] * r) : 0.f;
+                    Pm[m * kLC + nn] = nn <= m ? ap[i][j] * r : 0.f;
                 }
         }
         __syncthreads();
 
-        // ---- R' = diag(beta) (V - K S), in place over V ----
+        // ---- R' = diag(beta) (V - diag(exp G) K S), in place over V ----
         {
             float acc[4][NV / 16];
             zero<64, NV>(acc);
@@ -145,7 +182,7 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
 #pragma unroll
                 for (int j = 0; j < NV / 16; ++j) {
                     const int m = ty + 16 * i, nn = tx + 16 * j;
-                    Rs[m * LV + nn] = bs[m] * (Rs[m * LV + nn] - acc[i][j]);
+                    Rs[m * LV + nn] = bs[m] * (Rs[m * LV + nn] - eG[m] * acc[i][j]);
                 }
         }
         // ---- X = (I + A)^{-1} (touches only Am, Xm, Ys; ends with a barrier) ----
@@ -165,12 +202,16 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
         }
         __syncthreads();
 
-        // ---- O = Q S + P U' ----
+        // ---- O = diag(exp G) Q S + P U' ----
         if (o) {
             float acc[4][NV / 16];
             zero<64, NV>(acc);
             mm_acc<64, NV, DK>(acc, [&](int m, int kk) { return Qs[m * LK + kk]; },
                                [&](int kk, int nn) { return Ss[kk * LV + nn]; });
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < NV / 16; ++j) acc[i][j] *= eG[ty + 16 * i];
             mm_acc<64, NV, kC>(acc, [&](int m, int kk) { return Pm[m * kLC + kk]; },
                                [&](int kk, int nn) { return Us[kk * LV + nn]; });
 #pragma unroll
@@ -185,17 +226,20 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
         }
         __syncthreads();
 
-        // ---- S <- S + K^T U' ----
+        // ---- S <- exp(G_C) S + K^T diag(exp(G_C - G)) U' ----
         {
             float acc[DK / 16][NV / 16];
             zero<DK, NV>(acc);
-            mm_acc<DK, NV, kC>(acc, [&](int m, int kk) { return Ks[kk * LK + m]; },
+            mm_acc<DK, NV, kC>(acc, [&](int m, int kk) { return Ks[kk * LK + m] * dec[kk]; },
                                [&](int kk, int nn) { return Us[kk * LV + nn]; });
+            const float keep = eG[kC - 1];
 #pragma unroll
             for (int i = 0; i < DK / 16; ++i)
 #pragma unroll
-                for (int j = 0; j < NV / 16; ++j)
-                    Ss[(ty + 16 * i) * LV + tx + 16 * j] += acc[i][j];
+                for (int j = 0; j < NV / 16; ++j) {
+                    float* const sp = Ss + (ty + 16 * i) * LV + tx + 16 * j;
+                    *sp = fmaf(keep, *sp, acc[i][j]);
+                }
         }
         __syncthreads();
     }
@@ -211,7 +255,7 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
 template <typename T, int DK, int DV>
 cudaError_t launch_typed(const void* q, const void* k, const void* v,
                          const void* beta, const float* S0, void* o, float* S_T,
-                         float* S_chunks, int BH, int Tlen, cudaStream_t stream) {
+                         float* S_chunks, const float* g, int BH, int Tlen, cudaStream_t stream) {
     constexpr int NV = DV < 64 ? DV : 64;
     using L = SimtSmem<DK, NV>;
     auto kern = chunk_simt_kernel<T, DK, DV, NV>;
@@ -223,18 +267,23 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
     kern<<<(unsigned)grid, kThreads, L::kBytes, stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k),
         static_cast<const T*>(v), static_cast<const T*>(beta), S0,
-        static_cast<T*>(o), S_T, S_chunks, Tlen);
+        static_cast<T*>(o), S_T, S_chunks, g, Tlen);
     return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_dims(const void* q, const void* k, const void* v,
                         const void* beta, const float* S0, void* o, float* S_T,
-                        float* Sc, int BH, int Tlen, int dk, int dv, cudaStream_t st) {
-    if (dk == 128 && dv == 128) return launch_typed<T, 128, 128>(q, k, v, beta, S0, o, S_T, Sc, BH, Tlen, st);
-    if (dk == 128 && dv == 64) return launch_typed<T, 128, 64>(q, k, v, beta, S0, o, S_T, Sc, BH, Tlen, st);
-    if (dk == 64 && dv == 128) return launch_typed<T, 64, 128>(q, k, v, beta, S0, o, S_T, Sc, BH, Tlen, st);
-    if (dk == 64 && dv == 64) return launch_typed<T, 64, 64>(q, k, v, beta, S0, o, S_T, Sc, BH, Tlen, st);
+                        float* Sc, const float* g, int BH, int Tlen, int dk, int dv,
+                        cudaStream_t st) {
+#define DN_SIMT_CASE(DK_, DV_)                                                             \
+    if (dk == DK_ && dv == DV_)                                                            \
+        return launch_typed<T, DK_, DV_>(q, k, v, beta, S0, o, S_T, Sc, g, BH, Tlen, st);
+    DN_SIMT_CASE(128, 128)
+    DN_SIMT_CASE(128, 64)
+    DN_SIMT_CASE(64, 128)
+    DN_SIMT_CASE(64, 64)
+#undef DN_SIMT_CASE
     return cudaErrorNotSupported;
 }
 
@@ -243,10 +292,12 @@ cudaError_t launch_dims(const void* q, const void* k, const void* v,
 cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v,
                               const void* beta, const float* S0, void* o,
                               float* S_T, int BH, int T, int dk, int dv, int dt,
-                              cudaStream_t stream, float* S_chunks) {
+                              cudaStream_t stream, float* S_chunks, const float* g) {
     if (BH <= 0 || T <= 0) return cudaSuccess;
-    if (dt == 0) return launch_dims<float>(q, k, v, beta, S0, o, S_T, S_chunks, BH, T, dk, dv, stream);
-    return launch_dims<__nv_bfloat16>(q, k, v, beta, S0, o, S_T, S_chunks, BH, T, dk, dv, stream);
+    if (dt == 0)
+        return launch_dims<float>(q, k, v, beta, S0, o, S_T, S_chunks, g, BH, T, dk, dv, stream);
+    return launch_dims<__nv_bfloat16>(q, k, v, beta, S0, o, S_T, S_chunks, g, BH, T, dk, dv,
+                                      stream);
 }
 
 }  // namespace dn

@@ -9,18 +9,22 @@
 
 namespace dn {
 
-// One decoding step over B*H heads (see dn_recurrent_step).
+// One decoding step over B*H heads (see dn_recurrent_step); with g (fp32
+// [BH] log keep rates) the gated step of dn_recurrent_step_gated.
 cudaError_t launch_recurrent_step(const void* q, const void* k, const void* v,
                                   const void* beta, float* S, void* o, int BH,
-                                  int dk, int dv, int dt, cudaStream_t stream);
+                                  int dk, int dv, int dt, cudaStream_t stream,
+                                  const float* g = nullptr);
 
 // Chunkwise forward with fp32 CUDA-core arithmetic (any T >= 1).  o may be
 // nullptr (no outputs); S_chunks, if given, receives the state at the start
-// of every chunk ([BH][ceil(T/64)][dk][dv] fp32), for the backward pass.
+// of every chunk ([BH][ceil(T/64)][dk][dv] fp32), for the backward pass; g,
+// if given, is the fp32 [BH][T] log keep rate of Gated DeltaNet.
 cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v,
                               const void* beta, const float* S0, void* o,
                               float* S_T, int BH, int T, int dk, int dv, int dt,
-                              cudaStream_t stream, float* S_chunks = nullptr);
+                              cudaStream_t stream, float* S_chunks = nullptr,
+                              const float* g = nullptr);
 
 // Chunkwise backward (fp32 CUDA-core arithmetic): the gradients of
 // L = <d_o, o> + <d_S_T, S_T> for dn_chunk_fwd's outputs.  The workspace

@@ -232,6 +232,33 @@ DN_API int dn_chunk_bwd(const void *q, const void *k, const void *v, const void 
 DN_API size_t dn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv,
                                     int C, int dt);
 
+/*
+ * dn_chunk_fwd_gated -- Gated DeltaNet, chunkwise: a scalar keep rate
+ * alpha_t = exp(g_t) per token decays the whole state before the delta rule
+ * ("Gated DeltaNet", garden.houmin.site/infra/delta-net; "Gated DeltaNet :
+ * oublier d'abord l'état entier", fr.news.hada.io/topic?id=31925):
+ *     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,  o_t = S_t q_t
+ * i.e. forget (alpha S), predict, correct, write, read, in that order.
+ *   g       [B, H, T] fp32 log keep rates (g <= 0 keeps the state bounded;
+ *           not enforced), 4-byte aligned device memory
+ * Every other argument, layout and error as for dn_chunk_fwd (no workspace).
+ * The arithmetic is fp32 on CUDA cores for both I/O types.
+ */
+DN_API int dn_chunk_fwd_gated(const void *q, const void *k, const void *v,
+                       const void *beta, const float *g, const float *S0, void *o,
+                       float *S_T, int B, int H, int T, int dk, int dv, int C, int dt,
+                       void *stream);
+
+/*
+ * dn_recurrent_step_gated -- one Gated DeltaNet decoding step: with
+ * alpha = exp(g) per (b, h), p = alpha S k, u = beta (v - p),
+ * S <- alpha S + u k^T (stored layout: S += k u^T after the decay) and
+ * o = S_new q.  g is [B, H] fp32; everything else as for dn_recurrent_step.
+ */
+DN_API int dn_recurrent_step_gated(const void *q, const void *k, const void *v,
+                            const void *beta, const float *g, float *S, void *o,
+                            int B, int H, int dk, int dv, int dt, void *stream);
+
 /* ABI version of this header (bumped on incompatible changes). */
 DN_API int dn_abi_version(void);
 

@@ -1,0 +1,112 @@
+"""Gated DeltaNet on the GPU (chunkwise forward and decoding step) against
+the fp64 gated oracle, through the C ABI.  Bars as for the plain forms:
+relative L2 <= 1e-4 (fp32 I/O) and <= 1e-2 (bf16 I/O) on o and the state.
+"""
+import numpy as np
+import pytest
+import torch
+
+import delta_rule_recurrent_gb300 as dn
+import oracle
+import workloads
+from tests.conftest import rel_l2
+from tests.gpu_util import TOL, dev, sample_heads, take_heads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def no_device_error():
+    lib = dn.load()
+    assert lib.dn_device_error() == 0
+    yield
+    assert lib.dn_device_error() == 0
+
+
+def _check(o, S, o_ref, S_ref, dtype, what):
+    eo, eS = rel_l2(o, o_ref), rel_l2(S, S_ref)
+    assert eo <= TOL[dtype], f"{what} o rel L2 {eo:.3e}"
+    assert eS <= TOL[dtype], f"{what} S_T rel L2 {eS:.3e}"
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gated_chunk_ragged(dk, dv, dtype):
+    B, H, T = 2, 2, 200
+    inp = workloads.chunk_inputs(B, H, T, dk, dv, dtype=dtype, seed=dk + 3 * dv,
+                                 feature_map="silu", s0_std=0.1)
+    g = workloads.gate_inputs(B, H, T, seed=dk + dv)
+    o, S = dn.chunk_fwd_gated(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g),
+                              initial_state=dev(inp.S0))
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.forward_gated(inp.q, inp.k, inp.v, inp.beta, g, inp.S0)
+    _check(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
+           workloads.torch_dtype(dtype), f"{dtype} {dk}x{dv}")
+
+
+def test_gated_zero_decay_matches_the_plain_kernel_exactly():
+    """g = 0 runs the CUDA-core kernel with every decay factor exactly 1."""
+    inp = workloads.chunk_inputs(1, 2, 130, 64, 64, dtype="f32", seed=2, s0_std=0.1)
+    q, k, v, b, S0 = (dev(x) for x in (inp.q, inp.k, inp.v, inp.beta, inp.S0))
+    o1, S1 = dn.chunk_fwd(q, k, v, b, initial_state=S0, algo="simt")
+    o2, S2 = dn.chunk_fwd_gated(q, k, v, b, torch.zeros(1, 2, 130, device="cuda"),
+                                initial_state=S0)
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)
+
+
+def test_gated_strong_decay_and_edge_lengths():
+    for T in (1, 64, 65):
+        inp = workloads.chunk_inputs(1, 3, T, 128, 128, dtype="f32", seed=T, s0_std=0.5)
+        g = workloads.gate_inputs(1, 3, T, seed=T, lo=0.05, hi=0.5)  # alpha far below 1
+        o, S = dn.chunk_fwd_gated(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g),
+                                  initial_state=dev(inp.S0))
+        torch.cuda.synchronize()
+        o_ref, S_ref = oracle.forward_gated(inp.q, inp.k, inp.v, inp.beta, g, inp.S0)
+        _check(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
+               torch.float32, f"T={T}")
+
+
+def test_gated_layer_1p3b_sampled_heads():
+    inp = workloads.workload_inputs("layer1p3b_bf16")
+    B, H, T, d = inp.q.shape
+    g = workloads.gate_inputs(B, H, T, seed=7)
+    o, S = dn.chunk_fwd_gated(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g))
+    torch.cuda.synchronize()
+    bi, hi = sample_heads(B, H, 4, seed=8)
+    o_ref, S_ref = oracle.forward_gated(*(take_heads(x, bi, hi) for x in
+                                          (inp.q, inp.k, inp.v, inp.beta, g)))
+    ib, ih = torch.as_tensor(bi).cuda(), torch.as_tensor(hi).cuda()
+    _check(o[ib, ih].double().cpu().numpy()[None], S[ib, ih].double().cpu().numpy()[None],
+           o_ref, S_ref, torch.bfloat16, "1.3B")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gated_decode_steps(dtype):
+    B, H, d, steps, seed = 4, 4, 128, 24, 11
+    S0 = workloads.decode_state(B, H, d, d, std=0.1, seed=seed)
+    S = dev(S0)
+    rec = {n: [] for n in ("q", "k", "v", "beta", "g", "o")}
+    for step in range(steps):
+        x = workloads.decode_step_inputs(B, H, d, d, step=step, dtype=dtype, seed=seed)
+        g = workloads.gate_inputs(B, H, seed=seed * 100 + step, lo=0.8)
+        o = dn.recurrent_step_gated(dev(x.q), dev(x.k), dev(x.v), dev(x.beta), dev(g), S)
+        for n in ("q", "k", "v", "beta"):
+            rec[n].append(getattr(x, n))
+        rec["g"].append(g)
+        rec["o"].append(o.cpu())
+    torch.cuda.synchronize()
+    st = {n: torch.stack(v_, dim=2) for n, v_ in rec.items()}  # [B, H, steps, ...]
+    o_ref, S_ref = oracle.forward_gated(st["q"], st["k"], st["v"], st["beta"], st["g"], S0)
+    _check(st["o"].double().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
+           workloads.torch_dtype(dtype), f"decode {dtype}")
+
+
+def test_gated_decode_zero_decay_matches_the_plain_step_exactly():
+    B, H, d = 8, 2, 128
+    S0 = dev(workloads.decode_state(B, H, d, d, std=0.1, seed=3))
+    x = workloads.decode_step_inputs(B, H, d, d, step=0, dtype="bf16", seed=3)
+    S1, S2 = S0.clone(), S0.clone()
+    o1 = dn.recurrent_step(dev(x.q), dev(x.k), dev(x.v), dev(x.beta), S1)
+    o2 = dn.recurrent_step_gated(dev(x.q), dev(x.k), dev(x.v), dev(x.beta),
+                                 torch.zeros(B, H, device="cuda"), S2)
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)

@@ -367,6 +367,35 @@ def run_ours(args, rank, world, local):
         bwd_region_s, bwd_launch = timed_loop(bwd_step, bwd_steps, stream, world)
         bwd_region_s = max_over_ranks(bwd_region_s, world)
         del d_o, d_S, bws
+
+        # ---------------- Gated DeltaNet: chunk forward and decode step -----
+        gate = workloads.gate_inputs(B, H, T, seed=w["seed"]).to(dev)
+        og = torch.empty_like(o)
+        Sg = torch.empty_like(S_T)
+
+        def gated_step(_i):
+            dn.chunk_fwd_gated(q, k, v, beta, gate, out=og, final_state=Sg)
+
+        gsteps = max(1, min(args.steps, 10))
+        for i in range(min(args.warmup, 3)):
+            gated_step(i)
+        torch.cuda.synchronize()
+        g_region_s, g_launch = timed_loop(gated_step, gsteps, stream, world)
+        g_region_s = max_over_ranks(g_region_s, world)
+        del gate, og, Sg
+
+        dgate = workloads.gate_inputs(Bd, Hd, seed=wd["seed"]).to(dev)
+        Sdg = Sd.clone()
+
+        def gated_decode_step(i):
+            dn.recurrent_step_gated(dq[i], dkk[i], dvv[i], db[i], dgate, Sdg, out=od)
+
+        for i in range(args.warmup):
+            gated_decode_step(nsteps + i)
+        torch.cuda.synchronize()
+        gd_region_s, gd_launch = timed_loop(gated_decode_step, nsteps, stream, world)
+        gd_region_s = max_over_ranks(gd_region_s, world)
+        del dgate, Sdg
     clk = clocks.summary()
     del dq, dkk, dvv, db
 
@@ -457,6 +486,30 @@ def run_ours(args, rank, world, local):
                      "flops_per_launch": bflops, "launch_us": bwd_launch_s * 1e6},
         "config": {"d_o": "N(0,1)", "d_S_T": "N(0,0.1^2)", "S0": "none"},
     }
+    g_launch_s = statistics.mean(g_launch) / 1e3
+    gflops = chunk_flops_per_token_head(C, dk, dv) * B * H * T
+    gd_launch_s = statistics.mean(gd_launch) / 1e3
+    gdbytes = dbytes + Bd * Hd * 4  # plus the fp32 log keep rate per head
+    gated = {
+        "chunk": {"workload": HEADLINE, "steps": gsteps,
+                  "value": world * tokens * gsteps / g_region_s, "unit": "tokens/s",
+                  "ms_per_step": 1e3 * g_region_s / gsteps, "arith": "fp32 CUDA cores",
+                  "gate": "alpha ~ U(0.9, 1)",
+                  "roofline": {"bound": "alu", "achieved": gflops / g_launch_s / 1e12,
+                               "peak": fp32_alu_tflops(2070.0), "unit": "TFLOP/s",
+                               "frac": gflops / g_launch_s / 1e12 / fp32_alu_tflops(2070.0),
+                               "traffic": None,
+                               "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz",
+                               "flops_per_launch": gflops, "launch_us": g_launch_s * 1e6}},
+        "decode": {"workload": DECODE, "steps": nsteps,
+                   "value": world * Bd * nsteps / gd_region_s, "unit": "tokens/s",
+                   "ms_per_step": 1e3 * gd_region_s / nsteps,
+                   "roofline": {"bound": "hbm", "achieved": gdbytes / gd_launch_s / 1e9,
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": gdbytes / gd_launch_s / 1e9 / peaks["hbm_gbs"],
+                                "traffic": None, "peak_source": f"{peak_src} (copy bandwidth)",
+                                "bytes_per_launch": gdbytes, "launch_us": gd_launch_s * 1e6}},
+    }
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * region_s / args.steps,
@@ -470,11 +523,12 @@ def run_ours(args, rank, world, local):
         "roofline": roofline,
         "decode": decode,
         "backward": backward,
+        "gated": gated,
         "e2e": {"value": world * tokens * e2e_steps / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": 1e3 * e2e_s / e2e_steps},
         "gpu_launches": launches_per_call * (args.steps + e2e_steps) + nsteps
-                        + (nsteps if dec_graph[0] else 0) + 3 * bwd_steps,
+                        + (nsteps if dec_graph[0] else 0) + 3 * bwd_steps + gsteps + nsteps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -223,3 +223,28 @@ def recurrent_step_gated(q, k, v, beta, g, S, nthreads: int | None = None):
     o, S_new = forward_gated(q[:, :, None, :], k[:, :, None, :], v[:, :, None, :],
                              beta[:, :, None], g[:, :, None], S, nthreads=nthreads)
     return o[:, :, 0, :], S_new
+
+
+def forward_varlen(q, k, v, beta, cu_seqlens, S0=None, nthreads: int | None = None):
+    """Packed variable-length sequences: q, k ``[H, T, dk]``, v ``[H, T, dv]``,
+    beta ``[H, T]`` hold N sequences back to back along T, sequence n being
+    tokens ``cu_seqlens[n] .. cu_seqlens[n+1]-1``.  Each sequence runs the
+    recurrence from its own initial state (``S0``: ``[N, H, dk, dv]`` or
+    None).  Returns ``(o [H, T, dv], S_T [N, H, dk, dv])``."""
+    q, k, v, beta = _f64(q), _f64(k), _f64(v), _f64(beta)
+    cu = [int(x) for x in cu_seqlens]
+    H, T, dk = q.shape
+    dv = v.shape[2]
+    N = len(cu) - 1
+    if cu[0] != 0 or cu[-1] != T or any(b < a for a, b in zip(cu, cu[1:])):
+        raise ValueError("cu_seqlens must rise from 0 to T")
+    o = np.zeros((H, T, dv))
+    S_T = np.zeros((N, H, dk, dv))
+    for n in range(N):
+        a, b = cu[n], cu[n + 1]
+        s0 = None if S0 is None else _f64(S0)[n][None]
+        o_n, S_n = forward(q[None, :, a:b], k[None, :, a:b], v[None, :, a:b], beta[None, :, a:b],
+                           s0, nthreads=nthreads)
+        o[:, a:b] = o_n[0]
+        S_T[n] = S_n[0]
+    return o, S_T

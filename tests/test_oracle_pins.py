@@ -80,3 +80,29 @@ def test_oracle_recall_workload_closed_form(oracle_lib):
     o, _ = oracle_lib.forward(inp.q, inp.k, inp.v, inp.beta, None)
     from tests.conftest import rel_l2
     assert rel_l2(o, expect) < 1e-2
+
+
+def test_oracle_varlen_is_independent_sequences(oracle_lib):
+    """Packed sequences equal the same sequences run as a padded batch (each
+    from its own state; padding tokens have beta = 0 and k = 0, which is
+    exactly neutral), which the pinned forward computes."""
+    r = np.random.default_rng(51)
+    lens = [0, 1, 17, 64, 65, 30]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    H, dk, dv, T = 2, 5, 7, int(cu[-1])
+    q = r.standard_normal((H, T, dk))
+    k = r.standard_normal((H, T, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = r.standard_normal((H, T, dv))
+    beta = r.uniform(0.1, 1.0, (H, T))
+    S0 = r.standard_normal((len(lens), H, dk, dv))
+    o, S_T = oracle_lib.forward_varlen(q, k, v, beta, cu, S0)
+    L = max(lens)
+    pad = lambda x, n, w: np.concatenate([x, np.zeros(x.shape[:1] + (L - n,) + x.shape[2:])], 1)
+    for n, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        ln = b - a
+        ob, Sb = oracle_lib.forward(pad(q[:, a:b], ln, dk)[None], pad(k[:, a:b], ln, dk)[None],
+                                    pad(v[:, a:b], ln, dv)[None], pad(beta[:, a:b], ln, 1)[None],
+                                    S0[n][None])
+        assert np.allclose(o[:, a:b], ob[0, :, :ln], rtol=0, atol=1e-12)
+        assert np.allclose(S_T[n], Sb[0], rtol=0, atol=1e-12)

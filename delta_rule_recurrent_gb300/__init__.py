@@ -11,6 +11,7 @@ the computation runs in the library's sm_103a kernels.
     chunk_bwd(q, k, v, beta, d_o, initial_state=None, d_final_state=None)
         -> (d_q, d_k, d_v, d_beta, d_initial_state)   # training backward
     DeltaRule.apply(q, k, v, beta, initial_state)     # autograd: (o, final_state)
+    chunk_fwd_varlen(q, k, v, beta, cu_seqlens, ...)  # packed sequences, [H, T, d]
     chunk_fwd_gated(q, k, v, beta, g, ...), recurrent_step_gated(q, k, v, beta, g, state)
         # Gated DeltaNet: log keep rate g per token (per head for a step)
 
@@ -25,7 +26,7 @@ import torch
 from ._lib import (DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05, DN_BF16, DN_F32,
                    DeltaNetError, check, header_symbols, lib_path, load)
 
-__all__ = ["chunk_fwd", "chunk_bwd", "recurrent_step", "chunk_fwd_gated",
+__all__ = ["chunk_fwd", "chunk_bwd", "recurrent_step", "chunk_fwd_varlen", "chunk_fwd_gated",
            "recurrent_step_gated", "DeltaRule", "DeltaNetError", "load", "lib_path",
            "header_symbols", "ALGOS"]
 
@@ -287,3 +288,56 @@ def recurrent_step_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta
                                           beta.data_ptr(), g.data_ptr(), state.data_ptr(),
                                           out.data_ptr(), B, H, dk, dv, dt, _stream_handle(dev)))
     return out
+
+
+def chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                     cu_seqlens, initial_state: torch.Tensor | None = None,
+                     output_final_state: bool = True, chunk_size: int = 64,
+                     workspace="auto"):
+    """Packed variable-length sequences (``dn_chunk_fwd_varlen``).
+
+    q, k ``[H, T, dk]``, v ``[H, T, dv]``, beta ``[H, T]`` hold N sequences
+    back to back; ``cu_seqlens`` (a host sequence of N + 1 ints) gives their
+    offsets.  Returns ``(o [H, T, dv], S_T [N, H, dk, dv] or None)``.
+    ``workspace``: "auto" (the two-pass tensor-core path where it applies),
+    None (the CUDA-core path) or a uint8 CUDA tensor.
+    """
+    import ctypes
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
+        _check_cuda(name, t, dev)
+    dt = _dtype_code(q)
+    if not (k.dtype == v.dtype == beta.dtype == q.dtype):
+        raise TypeError("q, k, v and beta must share one dtype")
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3:
+        raise ValueError("q, k must be [H,T,dk] and v [H,T,dv]")
+    H, T, dk = q.shape
+    dv = v.shape[2]
+    if tuple(v.shape[:2]) != (H, T) or tuple(beta.shape) != (H, T):
+        raise ValueError("v must be [H,T,dv] and beta [H,T]")
+    cu = [int(x) for x in cu_seqlens]
+    N = len(cu) - 1
+    cu_arr = (ctypes.c_int * len(cu))(*cu)
+    if initial_state is not None:
+        _check_cuda("initial_state", initial_state, dev)
+        if initial_state.dtype != torch.float32 or tuple(initial_state.shape) != (N, H, dk, dv):
+            raise ValueError("initial_state must be float32 [N,H,dk,dv]")
+    out = torch.empty((H, T, dv), dtype=q.dtype, device=dev)
+    S_T = (torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+           if output_final_state else None)
+    lib = load()
+    need = lib.dn_chunk_fwd_varlen_workspace_bytes(cu_arr, N, H, dk, dv, chunk_size, dt)
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be 'auto', None or a uint8 CUDA tensor")
+        ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
+    else:
+        ws = workspace
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    with torch.cuda.device(dev):
+        check(lib.dn_chunk_fwd_varlen(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(),
+            initial_state.data_ptr() if initial_state is not None else None, out.data_ptr(),
+            S_T.data_ptr() if S_T is not None else None, cu_arr, N, H, T, dk, dv, chunk_size, dt,
+            ws.data_ptr() if ws is not None else None, ws_bytes, _stream_handle(dev)))
+    return out, S_T

@@ -19,6 +19,7 @@ DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05 = 0, 1, 2
 
 _vp, _fp = ctypes.c_void_p, ctypes.c_void_p
 _int, _size = ctypes.c_int, ctypes.c_size_t
+_ip = ctypes.POINTER(ctypes.c_int)
 
 # Signatures of every entry point in include/deltanet.h.
 SIGNATURES = {
@@ -34,6 +35,9 @@ SIGNATURES = {
     "dn_chunk_bwd": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _fp, _vp, _vp, _vp, _vp, _fp]
                      + [_int] * 7 + [_vp, _size, _vp]),
     "dn_chunk_bwd_workspace_bytes": (_size, [_int] * 7),
+    "dn_chunk_fwd_varlen": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _fp, _ip] + [_int] * 7
+                            + [_vp, _size, _vp]),
+    "dn_chunk_fwd_varlen_workspace_bytes": (_size, [_ip] + [_int] * 6),
     "dn_chunk_fwd_gated": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp] + [_int] * 7 + [_vp]),
     "dn_recurrent_step_gated": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp] + [_int] * 5 + [_vp]),
     "dn_status_string": (ctypes.c_char_p, [_int]),

@@ -251,6 +251,105 @@ int dn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const void
         "chunk forward (tcgen05, static scratch) launch");
 }
 
+// Checks cu_seqlens (host) and fills the kernels' sequence table.
+static int varlen_table(const int* cu, int N, int T, dn::VarlenTable* tab) {
+    if (N < 0 || N > dn::kMaxVarlenSeqs)
+        return fail(DN_ERR_INVALID_ARG, "%d sequences; 0 to %d are supported", N,
+                    dn::kMaxVarlenSeqs);
+    if (!cu) return fail(DN_ERR_INVALID_ARG, "cu_seqlens is NULL");
+    if (cu[0] != 0 || cu[N] != T)
+        return fail(DN_ERR_INVALID_ARG, "cu_seqlens must run from 0 to T=%d (got %d .. %d)", T,
+                    cu[0], cu[N]);
+    tab->n = N;
+    tab->start[0] = 0;
+    tab->chunk[0] = 0;
+    for (int i = 0; i < N; ++i) {
+        if (cu[i + 1] < cu[i]) return fail(DN_ERR_INVALID_ARG, "cu_seqlens decreases at %d", i);
+        tab->start[i + 1] = cu[i + 1];
+        tab->chunk[i + 1] = tab->chunk[i] + (cu[i + 1] - cu[i] + 63) / 64;
+    }
+    return DN_OK;
+}
+
+size_t dn_chunk_fwd_varlen_workspace_bytes(const int* cu_seqlens, int N, int H, int dk, int dv,
+                                           int C, int dt) {
+    if (!cu_seqlens || N <= 0 || N > dn::kMaxVarlenSeqs || H <= 0 || C != 64 ||
+        !dn::chunk_tc_supports(dk, dv, dt))
+        return 0;
+    long long chunks = 0;
+    for (int i = 0; i < N; ++i) {
+        const long long len = (long long)cu_seqlens[i + 1] - cu_seqlens[i];
+        if (len < 0) return 0;
+        chunks += (len + 63) / 64;
+    }
+    return (size_t)H * (size_t)chunks * 16384;
+}
+
+int dn_chunk_fwd_varlen(const void* q, const void* k, const void* v, const void* beta,
+                        const float* S0, void* o, float* S_T, const int* cu_seqlens, int N, int H,
+                        int T, int dk, int dv, int C, int dt, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    if (N < 0 || H < 0 || T < 0)
+        return fail(DN_ERR_INVALID_ARG, "negative size (N=%d H=%d T=%d)", N, H, T);
+    if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
+    if (dk <= 0 || dv <= 0 || C <= 0)
+        return fail(DN_ERR_INVALID_ARG, "dk, dv and C must be positive");
+    if (!supported_dim(dk) || !supported_dim(dv))
+        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this build supports 64 and 128", dk, dv);
+    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this build supports 64", C);
+    static thread_local dn::VarlenTable tab;
+    if (int st = varlen_table(cu_seqlens, N, T, &tab)) return st;
+    const size_t need_ws = dn_chunk_fwd_varlen_workspace_bytes(cu_seqlens, N, H, dk, dv, C, dt);
+    if (workspace && workspace_bytes < need_ws)
+        return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed (or pass NULL)",
+                    workspace_bytes, need_ws);
+    if ((long long)N * H == 0) return ok();
+    const size_t es = elem_size(dt);
+    const size_t ntok = (size_t)H * (size_t)T;
+    const size_t state_bytes = (size_t)N * H * dk * dv * sizeof(float);
+    const Span sq{"q", q, ntok * dk * es}, sk{"k", k, ntok * dk * es}, sv{"v", v, ntok * dv * es},
+        sb{"beta", beta, ntok * es}, so{"o", o, ntok * dv * es}, s0{"S0", S0, state_bytes},
+        sT{"S_T", S_T, state_bytes};
+    int dev = 0;
+    if (int st = current_device(&dev)) return st;
+    if (T > 0) {
+        for (const Span* s : {&sq, &sk, &sv, &so})
+            if (int st = check_device_ptr(*s, 16, dev)) return st;
+        if (int st = check_device_ptr(sb, es, dev)) return st;
+    }
+    if (S0)
+        if (int st = check_device_ptr(s0, 16, dev)) return st;
+    if (S_T)
+        if (int st = check_device_ptr(sT, 16, dev)) return st;
+    if (T > 0)
+        for (const Span* s : {&sq, &sk, &sv, &sb, &s0, &sT})
+            if (overlaps(so, *s)) return fail(DN_ERR_INVALID_ARG, "o overlaps %s", s->name);
+    for (const Span* s : {&sq, &sk, &sv, &sb})
+        if (T > 0 && overlaps(sT, *s)) return fail(DN_ERR_INVALID_ARG, "S_T overlaps %s", s->name);
+    if (S_T && S0 && S_T != S0 && overlaps(sT, s0))
+        return fail(DN_ERR_INVALID_ARG, "S_T partly overlaps S0");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {  // every sequence is empty
+        if (!S_T || S_T == S0) return ok();
+        if (S0)
+            return cuda_status(cudaMemcpyAsync(S_T, S0, state_bytes, cudaMemcpyDeviceToDevice, st),
+                               "cudaMemcpyAsync(S_T <- S0)");
+        return cuda_status(cudaMemsetAsync(S_T, 0, state_bytes, st), "cudaMemsetAsync(S_T)");
+    }
+    const bool use_tc = workspace && need_ws > 0;
+    if (use_tc) {
+        const Span sw{"workspace", workspace, need_ws};
+        if (int st2 = check_device_ptr(sw, 16, dev)) return st2;
+        for (const Span* s : {&sq, &sk, &sv, &sb, &so, &s0, &sT})
+            if (overlaps(sw, *s)) return fail(DN_ERR_INVALID_ARG, "workspace overlaps %s", s->name);
+    }
+    const cudaError_t e = use_tc
+        ? dn::launch_chunk_tc_varlen(q, k, v, beta, S0, o, S_T, tab, H, T, workspace, st)
+        : dn::launch_chunk_simt_varlen(q, k, v, beta, S0, o, S_T, tab, H, T, dk, dv, dt, st);
+    return cuda_status(e, use_tc ? "varlen chunk forward (tcgen05) launch"
+                                 : "varlen chunk forward (SIMT) launch");
+}
+
 int dn_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* beta,
                        const float* g, const float* S0, void* o, float* S_T, int B, int H,
                        int T, int dk, int dv, int C, int dt, void* stream) {

@@ -65,13 +65,16 @@ struct SimtSmem {
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
 
-template <typename T, int DK, int DV, int NV>
+// NMAX > 1: packed variable-length sequences (the CTA's state index is
+// (sequence, head); tokens come from the packed [H][T] layout).
+template <typename T, int DK, int DV, int NV, int NMAX>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
                   const T* __restrict__ v, const T* __restrict__ beta,
                   const float* __restrict__ S0, T* __restrict__ o,
                   float* __restrict__ S_T, float* __restrict__ S_chunks,
-                  const float* __restrict__ g, int Tlen) {
+                  const float* __restrict__ g, int Ttot, int H,
+                  const __grid_constant__ SeqTable<NMAX> seqs) {
     using L = SimtSmem<DK, NV>;
     constexpr int LK = L::LK, LV = L::LV;
     constexpr int NSLICE = DV / NV;
@@ -92,9 +95,15 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
 
     const int tid = threadIdx.x;
     const int tx = tid & 15, ty = tid >> 4;
-    const int bh = blockIdx.x / NSLICE;
+    const int bh = blockIdx.x / NSLICE;  // the state's index
     const int j0 = (blockIdx.x % NSLICE) * NV;
-    const size_t tok0 = (size_t)bh * Tlen;
+    size_t tok0 = (size_t)bh * Ttot;
+    int Tlen = Ttot;
+    if constexpr (NMAX > 1) {
+        const int n = bh / H, h = bh % H;
+        tok0 = (size_t)h * Ttot + seqs.start[n];
+        Tlen = seqs.start[n + 1] - seqs.start[n];
+    }
 
     for (int e = tid; e < DK * NV; e += kThreads) {
         const int i = e / NV, jj = e % NV;
@@ -252,13 +261,14 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
     }
 }
 
-template <typename T, int DK, int DV>
+template <typename T, int DK, int DV, int NMAX = 1>
 cudaError_t launch_typed(const void* q, const void* k, const void* v,
                          const void* beta, const float* S0, void* o, float* S_T,
-                         float* S_chunks, const float* g, int BH, int Tlen, cudaStream_t stream) {
+                         float* S_chunks, const float* g, int BH, int Tlen, cudaStream_t stream,
+                         int H = 1, const SeqTable<NMAX>* seqs = nullptr) {
     constexpr int NV = DV < 64 ? DV : 64;
     using L = SimtSmem<DK, NV>;
-    auto kern = chunk_simt_kernel<T, DK, DV, NV>;
+    auto kern = chunk_simt_kernel<T, DK, DV, NV, NMAX>;
     cudaError_t err = cudaFuncSetAttribute(
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
     if (err != cudaSuccess) return err;
@@ -267,7 +277,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
     kern<<<(unsigned)grid, kThreads, L::kBytes, stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k),
         static_cast<const T*>(v), static_cast<const T*>(beta), S0,
-        static_cast<T*>(o), S_T, S_chunks, g, Tlen);
+        static_cast<T*>(o), S_T, S_chunks, g, Tlen, H, seqs ? *seqs : SeqTable<NMAX>{});
     return cudaGetLastError();
 }
 
@@ -298,6 +308,32 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v,
         return launch_dims<float>(q, k, v, beta, S0, o, S_T, S_chunks, g, BH, T, dk, dv, stream);
     return launch_dims<__nv_bfloat16>(q, k, v, beta, S0, o, S_T, S_chunks, g, BH, T, dk, dv,
                                       stream);
+}
+
+cudaError_t launch_chunk_simt_varlen(const void* q, const void* k, const void* v,
+                                     const void* beta, const float* S0, void* o, float* S_T,
+                                     const VarlenTable& seqs, int H, int T, int dk, int dv,
+                                     int dt, cudaStream_t st) {
+    const long long ctas = (long long)seqs.n * H;
+    if (ctas <= 0) return cudaSuccess;
+    if (ctas > 0x3fffffffLL) return cudaErrorInvalidValue;
+#define DN_SIMT_VARLEN(T_, DK_, DV_)                                                           \
+    if (dk == DK_ && dv == DV_)                                                                \
+        return launch_typed<T_, DK_, DV_, kMaxVarlenSeqs>(q, k, v, beta, S0, o, S_T, nullptr,  \
+                                                          nullptr, (int)ctas, T, st, H, &seqs);
+    if (dt == 0) {
+        DN_SIMT_VARLEN(float, 128, 128)
+        DN_SIMT_VARLEN(float, 128, 64)
+        DN_SIMT_VARLEN(float, 64, 128)
+        DN_SIMT_VARLEN(float, 64, 64)
+    } else {
+        DN_SIMT_VARLEN(__nv_bfloat16, 128, 128)
+        DN_SIMT_VARLEN(__nv_bfloat16, 128, 64)
+        DN_SIMT_VARLEN(__nv_bfloat16, 64, 128)
+        DN_SIMT_VARLEN(__nv_bfloat16, 64, 64)
+    }
+#undef DN_SIMT_VARLEN
+    return cudaErrorNotSupported;
 }
 
 }  // namespace dn

@@ -915,6 +915,52 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
+// ------------------------------------------------ sequences (batched or packed)
+// Where chunk work lives.  Batched: (batch, head) bh is TMA z coordinate bh,
+// its tokens are rows 0 .. T-1.  Packed (varlen): head h is z, a sequence is
+// rows start[n] .. start[n+1]-1 of the packed T, and its chunks' tiles follow
+// the earlier sequences' in the workspace.
+struct ChunkRef {
+    int z;       // TMA z coordinate (bh, or the head when packed)
+    int row0;    // first row of the chunk
+    int end;     // one past the sequence's last row
+    int wsrow;   // the chunk's first row in the workspace map
+};
+
+// Work item w of the prepare pass (items: BH * nchunks, or H * total chunks).
+template <int NMAX>
+__device__ __forceinline__ ChunkRef prep_item(const SeqTable<NMAX>& seqs, int w, int nchunks,
+                                              int T) {
+    if constexpr (NMAX == 1) {
+        const int bh = w / nchunks, c = w % nchunks;
+        return {bh, c * kC, T, c * 128};
+    } else {
+        const int total = seqs.chunk[seqs.n], h = w / total, gc = w % total;
+        int lo = 0, hi = seqs.n - 1;  // the last sequence whose chunks start at or before gc
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (seqs.chunk[mid] <= gc) lo = mid; else hi = mid - 1;
+        }
+        return {h, seqs.start[lo] + (gc - seqs.chunk[lo]) * kC, seqs.start[lo + 1], gc * 128};
+    }
+}
+
+// The sequence a scan CTA walks.
+struct SeqSpan {
+    int z, row0, len, wsbase;  // TMA z, first row, tokens, first workspace chunk
+    size_t obase;              // row of its first token in o ([BH][T] or [H][T])
+};
+template <int NMAX>
+__device__ __forceinline__ SeqSpan scan_span(const SeqTable<NMAX>& seqs, int bh, int H, int T) {
+    if constexpr (NMAX == 1) {
+        return {bh, 0, T, 0, (size_t)bh * T};
+    } else {
+        const int n = bh / H, h = bh % H;
+        const int a = seqs.start[n];
+        return {h, a, seqs.start[n + 1] - a, seqs.chunk[n], (size_t)h * T + a};
+    }
+}
+
 // ------------------------------------------------------------ prepare kernel
 // Split form, first pass: [PT; Tm] of every (batch, head, chunk).  It depends
 // only on the chunk's own k, q and beta, so all chunks of all heads run in
@@ -937,10 +983,11 @@ constexpr uint32_t kPrepSmemBytes = P_OFF_MISC + 16 + 1024;
 static_assert(kPrepCtasPerSm * (kPrepSmemBytes + 1024) <= 233472, "prepare kernel occupancy");
 static_assert(P_OFF_X % 1024 == 0 && kXBytes >= kTile, "[PT; Tm] over the solve array");
 
+template <int NMAX>
 __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_ws, const __nv_bfloat16* __restrict__ beta,
-                  int T, int nchunks, int items) {
+                  int T, int nchunks, int items, const __grid_constant__ SeqTable<NMAX> seqs) {
     constexpr int kBar = 1, B_TILES = 0, B_MMA = 1, B_END = 2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -975,18 +1022,19 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     // [K; Q] tiles of item w into the tile area (thread 0).
     auto load_tiles = [&](int w) {
-        const int bh = w / nchunks, c = w % nchunks;
+        const ChunkRef r = prep_item(seqs, w, nchunks, T);
         const uint32_t bar = ctl.bar(B_TILES);
         mbar_arrive_expect_tx(bar, 4 * 8192);
-        tma_load_3d(kq, &tm_k, bar, 0, c * kC, bh);
-        tma_load_3d(kq + kRegKQ, &tm_k, bar, 64, c * kC, bh);
-        tma_load_3d(kq + 8192, &tm_q, bar, 0, c * kC, bh);
-        tma_load_3d(kq + kRegKQ + 8192, &tm_q, bar, 64, c * kC, bh);
+        tma_load_3d(kq, &tm_k, bar, 0, r.row0, r.z);
+        tma_load_3d(kq + kRegKQ, &tm_k, bar, 64, r.row0, r.z);
+        tma_load_3d(kq + 8192, &tm_q, bar, 0, r.row0, r.z);
+        tma_load_3d(kq + kRegKQ + 8192, &tm_q, bar, 64, r.row0, r.z);
     };
     // Strength of token t of item w (0 past T), as volatile loads kept in place.
     auto load_beta = [&](int w) -> uint16_t {
-        const int bh = w / nchunks, tok = (w % nchunks) * kC + t;
-        return tok < T ? ld_nc_u16(beta + (size_t)bh * T + tok) : (uint16_t)0;
+        const ChunkRef r = prep_item(seqs, w, nchunks, T);
+        const int tok = r.row0 + t;
+        return tok < r.end ? ld_nc_u16(beta + (size_t)r.z * T + tok) : (uint16_t)0;
     };
 
     int n = 0, loads = 0;  // items finished, tile loads issued (thread 0)
@@ -996,7 +1044,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     uint16_t bnext = (t < kC && (int)blockIdx.x < items) ? load_beta(blockIdx.x) : (uint16_t)0;
     for (int w = blockIdx.x; w < items; w += gridDim.x, ++n) {
-        const int bh = w / nchunks, c = w % nchunks, wn = w + (int)gridDim.x;
+        const int wn = w + (int)gridDim.x;
         if (t < kC) betas[t] = __bfloat162float(__ushort_as_bfloat16(bnext));
         // G = [K; Q] K^T
         bool ok = true;
@@ -1088,7 +1136,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tc_fence_before_sync();
         wg_sync(kBar);
         if (t == 0) {
-            tma_store_3d(&tm_ws, tp, 0, c * 128, bh);
+            const ChunkRef r = prep_item(seqs, w, nchunks, T);
+            tma_store_3d(&tm_ws, tp, 0, r.wsrow, r.z);
             bulk_commit_group();
         }
     }
@@ -1166,7 +1215,8 @@ struct Smem {
 
 __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q,
                          const CUtensorMap* tm_k, const CUtensorMap* tm_v, const CUtensorMap* tm_ws,
-                         int bh, int nchunks) {
+                         const SeqSpan& sp, int nchunks) {
+    const int z = sp.z, r0 = sp.row0, w0 = sp.wsbase;
     int nkq = 0, nv = 0, ntp = 0;
     long long t0 = clock64();
     while ((nkq < nchunks || nv < nchunks || ntp < nchunks) && !ctl.aborted()) {
@@ -1176,16 +1226,16 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
              mbar_test_wait(ctl.bar(B_KQ_EMPTY + nkq % kStages), (uint32_t)(nkq / kStages - 1) & 1u))) {
             const uint32_t st = sm.kq(nkq), bar = ctl.bar(B_KQ_FULL + nkq % kKQ);
             mbar_arrive_expect_tx(bar, 4 * 8192);
-            tma_load_3d(st, tm_k, bar, 0, nkq * kC, bh);
-            tma_load_3d(st + kRegKQ, tm_k, bar, 64, nkq * kC, bh);
-            tma_load_3d(st + 8192, tm_q, bar, 0, nkq * kC, bh);
-            tma_load_3d(st + kRegKQ + 8192, tm_q, bar, 64, nkq * kC, bh);
+            tma_load_3d(st, tm_k, bar, 0, r0 + nkq * kC, z);
+            tma_load_3d(st + kRegKQ, tm_k, bar, 64, r0 + nkq * kC, z);
+            tma_load_3d(st + 8192, tm_q, bar, 0, r0 + nkq * kC, z);
+            tma_load_3d(st + kRegKQ + 8192, tm_q, bar, 64, r0 + nkq * kC, z);
             if (nkq + kStages < nchunks) {  // warm L2 for this stage's next tiles
-                const int y = (nkq + kStages) * kC;
-                tma_prefetch_l2_3d(tm_k, 0, y, bh);
-                tma_prefetch_l2_3d(tm_k, 64, y, bh);
-                tma_prefetch_l2_3d(tm_q, 0, y, bh);
-                tma_prefetch_l2_3d(tm_q, 64, y, bh);
+                const int y = r0 + (nkq + kStages) * kC;
+                tma_prefetch_l2_3d(tm_k, 0, y, z);
+                tma_prefetch_l2_3d(tm_k, 64, y, z);
+                tma_prefetch_l2_3d(tm_q, 0, y, z);
+                tma_prefetch_l2_3d(tm_q, 64, y, z);
             }
             ++nkq;
             progressed = true;
@@ -1195,11 +1245,11 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
              mbar_test_wait(ctl.bar(B_V_EMPTY + nv % kVBufs), (uint32_t)(nv / kVBufs - 1) & 1u))) {
             const uint32_t bar = ctl.bar(B_V_FULL + nv % kVBufs);
             mbar_arrive_expect_tx(bar, 2 * 8192);
-            tma_load_3d(sm.v(nv), tm_v, bar, 0, nv * kC, bh);
-            tma_load_3d(sm.v(nv) + 8192, tm_v, bar, 64, nv * kC, bh);
+            tma_load_3d(sm.v(nv), tm_v, bar, 0, r0 + nv * kC, z);
+            tma_load_3d(sm.v(nv) + 8192, tm_v, bar, 64, r0 + nv * kC, z);
             if (nv + kVBufs < nchunks) {
-                tma_prefetch_l2_3d(tm_v, 0, (nv + kVBufs) * kC, bh);
-                tma_prefetch_l2_3d(tm_v, 64, (nv + kVBufs) * kC, bh);
+                tma_prefetch_l2_3d(tm_v, 0, r0 + (nv + kVBufs) * kC, z);
+                tma_prefetch_l2_3d(tm_v, 64, r0 + (nv + kVBufs) * kC, z);
             }
             ++nv;
             progressed = true;
@@ -1209,8 +1259,8 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
             if (it == 0 || mbar_test_wait(ctl.bar(B_FREE + g), (uint32_t)(it - 1) & 1u)) {
                 const uint32_t bar = ctl.bar(B_TP_FULL + g);
                 mbar_arrive_expect_tx(bar, kTile);
-                tma_load_3d(sm.tp(g), tm_ws, bar, 0, ntp * 128, bh);
-                if (ntp + 2 < nchunks) tma_prefetch_l2_3d(tm_ws, 0, (ntp + 2) * 128, bh);
+                tma_load_3d(sm.tp(g), tm_ws, bar, 0, (w0 + ntp) * 128, z);
+                if (ntp + 2 < nchunks) tma_prefetch_l2_3d(tm_ws, 0, (w0 + ntp + 2) * 128, z);
                 ++ntp;
                 progressed = true;
             }
@@ -1408,7 +1458,7 @@ __device__ __forceinline__ void issue_vpart(uint32_t tmem, uint32_t v, uint32_t 
 
 // o writer: thread t owns dv column t (TMEM lane t); thread 0 issues the v part.
 __device__ void writer_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
-                            __nv_bfloat16* __restrict__ o, int bh, int T, int nchunks) {
+                            __nv_bfloat16* __restrict__ o, size_t obase, int len, int nchunks) {
     constexpr int kBar = 3;
     const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
     // v part of chunk cn, once its v tile and [PT; Tm] are in (thread 0).
@@ -1437,22 +1487,23 @@ __device__ void writer_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t
         if (t == 0) ok = ctl.wait(B_U_READ, (uint32_t)c) && (c + 1 >= nchunks || start(c + 1));
         const int tok0 = c * kC;
         if (o) {  // (no outputs when only the chunk states are wanted)
-            __nv_bfloat16* const ob = o + ((size_t)bh * T + tok0) * kD + t;
+            __nv_bfloat16* const ob = o + (obase + tok0) * kD + t;
 #pragma unroll
             for (int r = 0; r < 64; ++r)
-                if (tok0 + r < T) ob[(size_t)r * kD] = __float2bfloat16_rn(ov[r]);
+                if (tok0 + r < len) ob[(size_t)r * kD] = __float2bfloat16_rn(ov[r]);
         }
         if (wg_sync_or(kBar, !ok)) return;
     }
 }
 }  // namespace scan
 
-template <bool kRec>
+template <bool kRec, int NMAX>
 __global__ void __launch_bounds__(512, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ws,
                   const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
-                  float* __restrict__ S_T, float* __restrict__ S_chunks, int T) {
+                  float* __restrict__ S_T, float* __restrict__ S_chunks, int T, int H,
+                  const __grid_constant__ SeqTable<NMAX> seqs) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -1461,8 +1512,9 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const Ctl ctl{base + scan::OFF_BAR, reinterpret_cast<volatile int*>(misc)};
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x;
-    const int nchunks = (T + kC - 1) / kC;
+    const int bh = blockIdx.x;  // the state's index: (batch, head) or (sequence, head)
+    const SeqSpan sp = scan_span(seqs, bh, H, T);
+    const int nchunks = (sp.len + kC - 1) / kC;
 
     if (tid == 0) {
         misc[0] = 0;
@@ -1483,7 +1535,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t tmem = *tmem_holder;
 
     if (warp == 0) {
-        if (lane == 0) scan::producer(ctl, sm, &tm_q, &tm_k, &tm_v, &tm_ws, bh, nchunks);
+        if (lane == 0) scan::producer(ctl, sm, &tm_q, &tm_k, &tm_v, &tm_ws, sp, nchunks);
     } else if (warp >= 4 && warp < 8) {
         const int t = tid - 128;
         scan::state_body<kRec>(ctl, sm, tmem, t, S0, S_T, S_chunks, bh, nchunks);
@@ -1494,7 +1546,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 1);
     } else if (warp >= 12) {
         const int t = tid - 384;
-        scan::writer_body(ctl, sm, tmem, t, o, bh, T, nchunks);
+        scan::writer_body(ctl, sm, tmem, t, o, sp.obase, sp.len, nchunks);
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 2);
     }
     tc_fence_before_sync();
@@ -1583,24 +1635,58 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
     if (workspace) {
         const long long items = (long long)BH * nchunks;
         if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
-        auto scan_kernel = S_chunks ? chunk_scan_kernel<true> : chunk_scan_kernel<false>;
-        if ((err = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        auto prep_kernel = chunk_prep_kernel<1>;
+        auto scan_kernel = S_chunks ? chunk_scan_kernel<true, 1> : chunk_scan_kernel<false, 1>;
+        if ((err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kPrepSmemBytes)) != cudaSuccess ||
             (err = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         scan::kSmemBytes)) != cudaSuccess)
             return err;
+        const SeqTable<1> batched{};
         const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
-        chunk_prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(mq, mk, mws, b, T, nchunks,
-                                                                          (int)items);
+        prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(mq, mk, mws, b, T, nchunks,
+                                                                    (int)items, batched);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
         scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(
-            mq, mk, mv, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, S_chunks, T);
+            mq, mk, mv, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, S_chunks, T, 1, batched);
         return cudaGetLastError();
     }
     if ((err = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Layout::kSmemBytes)) != cudaSuccess)
         return err;
     chunk_tc_kernel<<<BH, 512, Layout::kSmemBytes, stream>>>(mq, mk, mv, mo, b, S0, S_T, T);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v, const void* beta,
+                                   const float* S0, void* o, float* S_T, const VarlenTable& seqs,
+                                   int H, int T, void* workspace, cudaStream_t stream) {
+    const int total = seqs.chunk[seqs.n];
+    const long long ctas = (long long)seqs.n * H, items = (long long)H * total;
+    if (ctas <= 0) return cudaSuccess;
+    if (!workspace || ctas > 0x7fffffffLL || items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    CUtensorMap mq, mk, mv, mws;
+    memset(&mws, 0, sizeof(mws));
+    const int Tmap = T > 0 ? T : 1, nmap = total > 0 ? total : 1;
+    if (!make_map(&mq, q, H, Tmap) || !make_map(&mk, k, H, Tmap) || !make_map(&mv, v, H, Tmap) ||
+        !make_ws_map(&mws, workspace, H, nmap))
+        return cudaErrorInvalidValue;
+    auto prep_kernel = chunk_prep_kernel<kMaxVarlenSeqs>;
+    auto scan_kernel = chunk_scan_kernel<false, kMaxVarlenSeqs>;
+    cudaError_t err;
+    if ((err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kPrepSmemBytes)) != cudaSuccess ||
+        (err = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    scan::kSmemBytes)) != cudaSuccess)
+        return err;
+    if (items > 0) {
+        const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
+        prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
+            mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, 0, (int)items, seqs);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    scan_kernel<<<(unsigned)ctas, 512, scan::kSmemBytes, stream>>>(
+        mq, mk, mv, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, nullptr, T, H, seqs);
     return cudaGetLastError();
 }
 

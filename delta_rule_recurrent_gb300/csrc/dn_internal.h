@@ -9,6 +9,19 @@
 
 namespace dn {
 
+// Packed variable-length sequences: sequence n is tokens start[n] ..
+// start[n+1] - 1 of an [H][T][d] tensor, and chunk[n] counts the 64-token
+// chunks of the sequences before it.  Kernels take the table by value (a
+// kernel parameter), so varlen calls need no device memory for it.
+constexpr int kMaxVarlenSeqs = 1024;
+template <int NMAX>
+struct SeqTable {
+    int n;
+    int start[NMAX + 1];
+    int chunk[NMAX + 1];
+};
+using VarlenTable = SeqTable<kMaxVarlenSeqs>;
+
 // One decoding step over B*H heads (see dn_recurrent_step); with g (fp32
 // [BH] log keep rates) the gated step of dn_recurrent_step_gated.
 cudaError_t launch_recurrent_step(const void* q, const void* k, const void* v,
@@ -52,6 +65,18 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v,
                             const void* beta, const float* S0, void* o,
                             float* S_T, int BH, int T, int dk, int dv, int dt,
                             void* workspace, cudaStream_t stream, float* S_chunks = nullptr);
+
+// Varlen forms: q, k, v, beta, o are [H][T][.] (T the packed length), the
+// states [seqs.n][H][dk][dv].  The tensor-core form runs in two passes and
+// needs H * seqs.chunk[seqs.n] tiles of workspace.
+cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v,
+                                   const void* beta, const float* S0, void* o, float* S_T,
+                                   const VarlenTable& seqs, int H, int T, void* workspace,
+                                   cudaStream_t stream);
+cudaError_t launch_chunk_simt_varlen(const void* q, const void* k, const void* v,
+                                     const void* beta, const float* S0, void* o, float* S_T,
+                                     const VarlenTable& seqs, int H, int T, int dk, int dv,
+                                     int dt, cudaStream_t stream);
 
 // As launch_chunk_tc with the workspace in a static device array of
 // noalloc_max_tiles tiles (the caller has checked the size).  The array's

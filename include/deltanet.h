@@ -259,6 +259,37 @@ DN_API int dn_recurrent_step_gated(const void *q, const void *k, const void *v,
                             const void *beta, const float *g, float *S, void *o,
                             int B, int H, int dk, int dv, int dt, void *stream);
 
+/*
+ * dn_chunk_fwd_varlen -- dn_chunk_fwd over packed variable-length sequences
+ * (no padding): N sequences of one batch element lie back to back along T,
+ * sequence n being tokens cu_seqlens[n] .. cu_seqlens[n+1] - 1.  Each runs
+ * the recurrence from its own initial state.  The pages' layer takes such
+ * cu_seqlens offsets for variable-length batches (fla/layers/delta_net.py,
+ * DeltaNet.forward); the result per sequence is that of dn_chunk_fwd on it.
+ *
+ *   q, k [H, T, dk], v, o [H, T, dv], beta [H, T]   dtype `dt` (T = packed length)
+ *   S0, S_T [N, H, dk, dv] fp32 (S0 may be NULL: zeros; S_T may be NULL)
+ *   cu_seqlens  HOST array of N + 1 ints, 0 = cu_seqlens[0] <= ... <=
+ *               cu_seqlens[N] = T (empty sequences allowed);
+ *               1 <= N <= DN_MAX_VARLEN_SEQS
+ *   workspace   as for dn_chunk_fwd, of dn_chunk_fwd_varlen_workspace_bytes
+ *               bytes (one tile per head and chunk of every sequence); with it
+ *               the two-pass tensor-core path runs (bf16, dk = dv = 128), with
+ *               NULL (or for other shapes) the fp32 CUDA-core path
+ * Errors: as for dn_chunk_fwd, plus DN_ERR_INVALID_ARG for a bad cu_seqlens.
+ */
+#define DN_MAX_VARLEN_SEQS 1024
+DN_API int dn_chunk_fwd_varlen(const void *q, const void *k, const void *v,
+                        const void *beta, const float *S0, void *o, float *S_T,
+                        const int *cu_seqlens, int N, int H, int T, int dk, int dv,
+                        int C, int dt, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+/* Scratch bytes for dn_chunk_fwd_varlen's tensor-core path (0 where it does
+ * not apply).  Host-only; reads cu_seqlens (host, N + 1 ints). */
+DN_API size_t dn_chunk_fwd_varlen_workspace_bytes(const int *cu_seqlens, int N, int H,
+                                           int dk, int dv, int C, int dt);
+
 /* ABI version of this header (bumped on incompatible changes). */
 DN_API int dn_abi_version(void);
 

@@ -152,3 +152,24 @@ def test_noalloc_entry_point_rejects_before_any_cuda_call(lib):
     assert call(1, 1, 64, C=32) == _lib.DN_ERR_UNSUPPORTED
     assert call(-1, 1, 64) == _lib.DN_ERR_INVALID_ARG
     assert call(0, 4, 64) == _lib.DN_OK  # nothing to do, nothing touched
+
+
+def test_varlen_rejects_bad_offsets_before_any_cuda_call(lib):
+    """cu_seqlens is checked on the host first: it must run from 0 to T
+    without decreasing, with 0 < N <= DN_MAX_VARLEN_SEQS."""
+    f = lib.dn_chunk_fwd_varlen
+    null = [None] * 7
+
+    def call(cu, N, T, H=2):
+        arr = (ctypes.c_int * len(cu))(*cu)
+        return f(*null, arr, N, H, T, 128, 128, 64, 1, None, 0, None)
+
+    assert call([0, 5, 3, 9], 3, 9) == _lib.DN_ERR_INVALID_ARG  # decreases
+    assert call([1, 5, 9], 2, 9) == _lib.DN_ERR_INVALID_ARG     # does not start at 0
+    assert call([0, 5, 8], 2, 9) == _lib.DN_ERR_INVALID_ARG     # does not end at T
+    assert call([0] * 1026, 1025, 0) == _lib.DN_ERR_INVALID_ARG  # too many sequences
+    assert b"1024" in lib.dn_last_error()
+    size = lib.dn_chunk_fwd_varlen_workspace_bytes
+    arr = (ctypes.c_int * 4)(0, 65, 65, 100)
+    assert size(arr, 3, 2, 128, 128, 64, 1) == 2 * (2 + 0 + 1) * 16384
+    assert size(arr, 3, 2, 64, 64, 64, 1) == 0

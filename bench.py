@@ -368,6 +368,31 @@ def run_ours(args, rank, world, local):
         bwd_region_s = max_over_ranks(bwd_region_s, world)
         del d_o, d_S, bws
 
+        # ---------------- varlen: the same tokens as 64 packed sequences ------
+        vl_lens = workloads.varlen_lengths(64, B * T, seed=w["seed"])
+        vl_cu = [0]
+        for ln in vl_lens:
+            vl_cu.append(vl_cu[-1] + ln)
+        # q, k, v, beta re-read as [H, B*T, d]: head-major packing of the same values
+        vq, vk, vv = (x.transpose(0, 1).reshape(H, B * T, -1).contiguous() for x in (q, k, v))
+        vb = beta.transpose(0, 1).reshape(H, B * T).contiguous()
+        vws = None
+
+        def varlen_step(_i):
+            dn.chunk_fwd_varlen(vq, vk, vv, vb, vl_cu, workspace=vws)
+
+        import ctypes
+        cu_arr = (ctypes.c_int * len(vl_cu))(*vl_cu)
+        vneed = lib.dn_chunk_fwd_varlen_workspace_bytes(cu_arr, 64, H, dk, dv, C, 1 if tc else 0)
+        vws = torch.empty(vneed, dtype=torch.uint8, device=dev) if vneed else None
+        vsteps = max(1, min(args.steps, 20))
+        for i in range(min(args.warmup, 3)):
+            varlen_step(i)
+        torch.cuda.synchronize()
+        vl_region_s, vl_launch = timed_loop(varlen_step, vsteps, stream, world)
+        vl_region_s = max_over_ranks(vl_region_s, world)
+        del vq, vk, vv, vb, vws
+
         # ---------------- Gated DeltaNet: chunk forward and decode step -----
         gate = workloads.gate_inputs(B, H, T, seed=w["seed"]).to(dev)
         og = torch.empty_like(o)
@@ -486,6 +511,16 @@ def run_ours(args, rank, world, local):
                      "flops_per_launch": bflops, "launch_us": bwd_launch_s * 1e6},
         "config": {"d_o": "N(0,1)", "d_S_T": "N(0,0.1^2)", "S0": "none"},
     }
+    vl_launch_s = statistics.mean(vl_launch) / 1e3
+    varlen = {
+        "workload": f"{HEADLINE} tokens as 64 packed sequences (lengths {min(vl_lens)}-{max(vl_lens)})",
+        "steps": vsteps, "value": world * tokens * vsteps / vl_region_s, "unit": "tokens/s",
+        "ms_per_step": 1e3 * vl_region_s / vsteps,
+        "roofline": {"bound": "tensor", "achieved": flops / vl_launch_s / 1e12,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": flops / vl_launch_s / 1e12 / peaks["bf16_tflops"], "traffic": None,
+                     "peak_source": f"{peak_src} (bf16 dense burst)", "launch_us": vl_launch_s * 1e6},
+    }
     g_launch_s = statistics.mean(g_launch) / 1e3
     gflops = chunk_flops_per_token_head(C, dk, dv) * B * H * T
     gd_launch_s = statistics.mean(gd_launch) / 1e3
@@ -523,12 +558,14 @@ def run_ours(args, rank, world, local):
         "roofline": roofline,
         "decode": decode,
         "backward": backward,
+        "varlen": varlen,
         "gated": gated,
         "e2e": {"value": world * tokens * e2e_steps / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": 1e3 * e2e_s / e2e_steps},
         "gpu_launches": launches_per_call * (args.steps + e2e_steps) + nsteps
-                        + (nsteps if dec_graph[0] else 0) + 3 * bwd_steps + gsteps + nsteps,
+                        + (nsteps if dec_graph[0] else 0) + 3 * bwd_steps + gsteps + nsteps
+                        + launches_per_call * vsteps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -251,3 +251,13 @@ def gate_inputs(B: int, H: int, T: int | None = None, *, seed: int = 0, lo: floa
     shape = (B, H) if T is None else (B, H, T)
     alpha = lo + (hi - lo) * torch.rand(shape, generator=gen)
     return torch.log(alpha).float().contiguous()
+
+
+def varlen_lengths(n: int, total: int, *, seed: int = 0) -> list[int]:
+    """n sequence lengths summing to ``total``: seeded U(0, 1) weights, scaled
+    and rounded (the remainder goes to the last sequence)."""
+    gen = torch.Generator().manual_seed(int(seed) * 4409 + 2281)
+    w = torch.rand(n, generator=gen) + 0.05
+    lens = [int(x) for x in (w / w.sum() * total).floor().tolist()]
+    lens[-1] += total - sum(lens)
+    return lens

@@ -70,6 +70,8 @@ def _load():
         lib.dn_oracle_backward.restype = ctypes.c_int
         lib.dn_oracle_forward_gated.argtypes = [dp] * 7 + [ctypes.c_long] * 4 + [ctypes.c_int]
         lib.dn_oracle_forward_gated.restype = ctypes.c_int
+        lib.dn_oracle_forward_kda.argtypes = [dp] * 7 + [ctypes.c_long] * 4 + [ctypes.c_int]
+        lib.dn_oracle_forward_kda.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -248,3 +250,33 @@ def forward_varlen(q, k, v, beta, cu_seqlens, S0=None, nthreads: int | None = No
         o[:, a:b] = o_n[0]
         S_T[n] = S_n[0]
     return o, S_T
+
+
+def forward_kda(q, k, v, beta, g, S0=None, nthreads: int | None = None):
+    """Kimi Delta Attention over a whole sequence: per-key-channel keep rates
+    exp(g_t) (``g``: ``[B, H, T, dk]``) decay the state's key channels before
+    each delta-rule update.  Other arguments and the result as ``forward``."""
+    q, k, v, beta, g = _f64(q), _f64(k), _f64(v), _f64(beta), _f64(g)
+    B, H, T, dk = q.shape
+    dv = v.shape[3]
+    if (k.shape != q.shape or v.shape[:3] != (B, H, T) or beta.shape != (B, H, T)
+            or g.shape != q.shape):
+        raise ValueError("q, k, g [B,H,T,dk]; v [B,H,T,dv]; beta [B,H,T]")
+    S = np.zeros((B, H, dk, dv)) if S0 is None else _f64(S0).copy()
+    o = np.zeros((B, H, T, dv))
+    if B * H == 0 or T == 0:
+        return o, S
+    n = host_cores() if nthreads is None else int(nthreads)
+    rc = _load().dn_oracle_forward_kda(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                                       _ptr(S), _ptr(o), B * H, T, dk, dv, n)
+    if rc != 0:
+        raise MemoryError("oracle could not allocate its scratch vector")
+    return o, S
+
+
+def recurrent_step_kda(q, k, v, beta, g, S, nthreads: int | None = None):
+    """One KDA decoding step (``g``: ``[B, H, dk]``); returns ``(o, S_new)``."""
+    q, k, v, beta, g = _f64(q), _f64(k), _f64(v), _f64(beta), _f64(g)
+    o, S_new = forward_kda(q[:, :, None, :], k[:, :, None, :], v[:, :, None, :],
+                           beta[:, :, None], g[:, :, None, :], S, nthreads=nthreads)
+    return o[:, :, 0, :], S_new

@@ -304,3 +304,72 @@ int dn_oracle_forward_gated(const double *q, const double *k, const double *v,
     }
     return failed ? -1 : 0;
 }
+
+/*
+ * Kimi Delta Attention (KDA; "Kimi Delta Attention : atténuation par canal"
+ * and "Transition diagonale-bas rang", fr.news.hada.io/topic?id=31925): the
+ * scalar keep rate becomes one rate per key channel, alpha_t = exp(g_t) in
+ * R^dk, D_t = Diag(alpha_t), in the order the page gives:
+ *   decay        S~ = S_{t-1} D_t        (key channel i of S scaled by alpha_t[i])
+ *   predict      p = S~ k_t
+ *   correct      u = beta_t (v_t - p)
+ *   write        S_t = S~ + u k_t^T
+ *   read         o_t = S_t q_t          (the caller applies any query scale)
+ * i.e. S_t = S_{t-1} D_t (I - beta_t k_t k_t^T) + beta_t v_t k_t^T.
+ * g is [BH][T][dk] fp64 log keep rates.
+ */
+static void run_one_head_kda(const double *q, const double *k, const double *v,
+                             const double *beta, const double *g, double *S, double *o,
+                             long T, long dk, long dv, double *p)
+{
+    for (long t = 0; t < T; ++t) {
+        const double *kt = k + t * dk, *qt = q + t * dk, *vt = v + t * dv, *gt = g + t * dk;
+        double *ot = o + t * dv;
+        for (long j = 0; j < dv; ++j)           /* decay, per key channel */
+            for (long i = 0; i < dk; ++i)
+                S_AT(S, dv, j, i) *= exp(gt[i]);
+        for (long j = 0; j < dv; ++j) {         /* predict */
+            double acc = 0.0;
+            for (long i = 0; i < dk; ++i)
+                acc += S_AT(S, dv, j, i) * kt[i];
+            p[j] = acc;
+        }
+        for (long j = 0; j < dv; ++j) {         /* correct and write */
+            const double u = beta[t] * (vt[j] - p[j]);
+            for (long i = 0; i < dk; ++i)
+                S_AT(S, dv, j, i) += u * kt[i];
+        }
+        for (long j = 0; j < dv; ++j) {         /* read */
+            double acc = 0.0;
+            for (long i = 0; i < dk; ++i)
+                acc += S_AT(S, dv, j, i) * qt[i];
+            ot[j] = acc;
+        }
+    }
+}
+
+int dn_oracle_forward_kda(const double *q, const double *k, const double *v,
+                          const double *beta, const double *g, double *S, double *o,
+                          long BH, long T, long dk, long dv, int nthreads)
+{
+    int failed = 0;
+    if (nthreads < 1)
+        nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)(dv > 0 ? dv : 1));
+        if (!p) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long n = 0; n < BH; ++n) {
+            if (!p)
+                continue;
+            run_one_head_kda(q + n * T * dk, k + n * T * dk, v + n * T * dv, beta + n * T,
+                             g + n * T * dk, S + n * dk * dv, o + n * T * dv, T, dk, dv, p);
+        }
+        free(p);
+    }
+    return failed ? -1 : 0;
+}

@@ -14,6 +14,8 @@ the computation runs in the library's sm_103a kernels.
     chunk_fwd_varlen(q, k, v, beta, cu_seqlens, ...)  # packed sequences, [H, T, d]
     chunk_fwd_gated(q, k, v, beta, g, ...), recurrent_step_gated(q, k, v, beta, g, state)
         # Gated DeltaNet: log keep rate g per token (per head for a step)
+    chunk_fwd_kda(q, k, v, beta, g, ...), recurrent_step_kda(q, k, v, beta, g, state)
+        # KDA: one log keep rate per key channel
 
 Shapes: q, k ``[B, H, T, dk]``; v ``[B, H, T, dv]``; beta ``[B, H, T]``;
 state ``[B, H, dk, dv]`` fp32 (the pages' dv x dk state, transposed).  For a
@@ -27,7 +29,7 @@ from ._lib import (DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05, DN_BF16, DN_F32,
                    DeltaNetError, check, header_symbols, lib_path, load)
 
 __all__ = ["chunk_fwd", "chunk_bwd", "recurrent_step", "chunk_fwd_varlen", "chunk_fwd_gated",
-           "recurrent_step_gated", "DeltaRule", "DeltaNetError", "load", "lib_path",
+           "recurrent_step_gated", "chunk_fwd_kda", "recurrent_step_kda", "DeltaRule", "DeltaNetError", "load", "lib_path",
            "header_symbols", "ALGOS"]
 
 ALGOS = {"auto": DN_ALGO_AUTO, "simt": DN_ALGO_SIMT, "tcgen05": DN_ALGO_TCGEN05}
@@ -233,6 +235,22 @@ def chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: tor
                     out: torch.Tensor | None = None, final_state: torch.Tensor | None = None):
     """Gated DeltaNet, chunkwise (``dn_chunk_fwd_gated``): ``g`` is the fp32
     ``[B, H, T]`` log keep rate.  Returns ``(o, S_T)`` as ``chunk_fwd``."""
+    return _chunk_decayed(q, k, v, beta, g, False, initial_state, output_final_state,
+                          chunk_size, out, final_state)
+
+
+def chunk_fwd_kda(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                  g: torch.Tensor, initial_state: torch.Tensor | None = None,
+                  output_final_state: bool = True, chunk_size: int = 64,
+                  out: torch.Tensor | None = None, final_state: torch.Tensor | None = None):
+    """Kimi Delta Attention, chunkwise (``dn_chunk_fwd_kda``): ``g`` is the
+    fp32 ``[B, H, T, dk]`` per-key-channel log keep rate."""
+    return _chunk_decayed(q, k, v, beta, g, True, initial_state, output_final_state,
+                          chunk_size, out, final_state)
+
+
+def _chunk_decayed(q, k, v, beta, g, per_channel, initial_state, output_final_state,
+                   chunk_size, out, final_state):
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
         _check_cuda(name, t, dev)
@@ -245,7 +263,7 @@ def chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: tor
     dv = v.shape[3]
     if tuple(v.shape[:3]) != (B, H, T) or tuple(beta.shape) != (B, H, T):
         raise ValueError("v must be [B,H,T,dv] and beta [B,H,T]")
-    _check_gate(g, (B, H, T), dev)
+    _check_gate(g, (B, H, T, dk) if per_channel else (B, H, T), dev)
     if initial_state is not None:
         _check_cuda("initial_state", initial_state, dev)
         if initial_state.dtype != torch.float32 or tuple(initial_state.shape) != (B, H, dk, dv):
@@ -258,7 +276,8 @@ def chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: tor
             (B, H, dk, dv), dtype=torch.float32, device=dev)
     lib = load()
     with torch.cuda.device(dev):
-        check(lib.dn_chunk_fwd_gated(
+        entry = lib.dn_chunk_fwd_kda if per_channel else lib.dn_chunk_fwd_gated
+        check(entry(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(), g.data_ptr(),
             initial_state.data_ptr() if initial_state is not None else None, out.data_ptr(),
             S_T.data_ptr() if S_T is not None else None, B, H, T, dk, dv, chunk_size, dt,
@@ -271,22 +290,34 @@ def recurrent_step_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta
                          out: torch.Tensor | None = None) -> torch.Tensor:
     """One Gated DeltaNet decoding step (``dn_recurrent_step_gated``); ``g``
     is the fp32 ``[B, H]`` log keep rate; ``state`` is updated in place."""
+    return _step_decayed(q, k, v, beta, g, False, state, out)
+
+
+def recurrent_step_kda(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                       g: torch.Tensor, state: torch.Tensor,
+                       out: torch.Tensor | None = None) -> torch.Tensor:
+    """One KDA decoding step (``dn_recurrent_step_kda``); ``g`` is the fp32
+    ``[B, H, dk]`` per-key-channel log keep rate; ``state`` updated in place."""
+    return _step_decayed(q, k, v, beta, g, True, state, out)
+
+
+def _step_decayed(q, k, v, beta, g, per_channel, state, out):
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("state", state)):
         _check_cuda(name, t, dev)
     dt = _dtype_code(q)
     B, H, dk = q.shape
     dv = v.shape[2]
-    _check_gate(g, (B, H), dev)
+    _check_gate(g, (B, H, dk) if per_channel else (B, H), dev)
     if state.dtype != torch.float32 or tuple(state.shape) != (B, H, dk, dv):
         raise ValueError("state must be float32 [B,H,dk,dv]")
     if out is None:
         out = torch.empty((B, H, dv), dtype=q.dtype, device=dev)
     lib = load()
     with torch.cuda.device(dev):
-        check(lib.dn_recurrent_step_gated(q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                          beta.data_ptr(), g.data_ptr(), state.data_ptr(),
-                                          out.data_ptr(), B, H, dk, dv, dt, _stream_handle(dev)))
+        entry = lib.dn_recurrent_step_kda if per_channel else lib.dn_recurrent_step_gated
+        check(entry(q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(), g.data_ptr(),
+                    state.data_ptr(), out.data_ptr(), B, H, dk, dv, dt, _stream_handle(dev)))
     return out
 
 

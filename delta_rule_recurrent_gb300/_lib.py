@@ -40,6 +40,8 @@ SIGNATURES = {
     "dn_chunk_fwd_varlen_workspace_bytes": (_size, [_ip] + [_int] * 6),
     "dn_chunk_fwd_gated": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp] + [_int] * 7 + [_vp]),
     "dn_recurrent_step_gated": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp] + [_int] * 5 + [_vp]),
+    "dn_chunk_fwd_kda": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp] + [_int] * 7 + [_vp]),
+    "dn_recurrent_step_kda": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp] + [_int] * 5 + [_vp]),
     "dn_status_string": (ctypes.c_char_p, [_int]),
     "dn_last_error": (ctypes.c_char_p, []),
     "dn_abi_version": (_int, []),

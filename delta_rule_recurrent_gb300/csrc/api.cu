@@ -350,9 +350,12 @@ int dn_chunk_fwd_varlen(const void* q, const void* k, const void* v, const void*
                                  : "varlen chunk forward (SIMT) launch");
 }
 
-int dn_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* beta,
-                       const float* g, const float* S0, void* o, float* S_T, int B, int H,
-                       int T, int dk, int dv, int C, int dt, void* stream) {
+// The decayed chunkwise forms: Gated DeltaNet (one log keep rate per token,
+// per_channel = 0) and KDA (one per token and key channel, per_channel = 1).
+static int chunk_fwd_decayed(const void* q, const void* k, const void* v, const void* beta,
+                             const float* g, int per_channel, const float* S0, void* o,
+                             float* S_T, int B, int H, int T, int dk, int dv, int C, int dt,
+                             void* stream) {
     if (B < 0 || H < 0 || T < 0)
         return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d T=%d)", B, H, T);
     if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
@@ -368,8 +371,8 @@ int dn_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* 
     const size_t ntok = (size_t)BH * (size_t)T;
     const size_t state_bytes = (size_t)BH * dk * dv * sizeof(float);
     const Span sq{"q", q, ntok * dk * es}, sk{"k", k, ntok * dk * es}, sv{"v", v, ntok * dv * es},
-        sb{"beta", beta, ntok * es}, sg{"g", g, ntok * sizeof(float)}, so{"o", o, ntok * dv * es},
-        s0{"S0", S0, state_bytes}, sT{"S_T", S_T, state_bytes};
+        sb{"beta", beta, ntok * es}, sg{"g", g, ntok * (per_channel ? dk : 1) * sizeof(float)},
+        so{"o", o, ntok * dv * es}, s0{"S0", S0, state_bytes}, sT{"S_T", S_T, state_bytes};
     int dev = 0;
     if (int st = current_device(&dev)) return st;
     if (T > 0) {
@@ -397,14 +400,30 @@ int dn_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* 
                                "cudaMemcpyAsync(S_T <- S0)");
         return cuda_status(cudaMemsetAsync(S_T, 0, state_bytes, st), "cudaMemsetAsync(S_T)");
     }
+    if (per_channel)
+        return cuda_status(
+            dn::launch_chunk_simt_kda(q, k, v, beta, g, S0, o, S_T, (int)BH, T, dk, dv, dt, st),
+            "KDA chunk forward launch");
     return cuda_status(dn::launch_chunk_simt(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, st,
                                              nullptr, g),
                        "gated chunk forward launch");
 }
 
-int dn_recurrent_step_gated(const void* q, const void* k, const void* v, const void* beta,
-                            const float* g, float* S, void* o, int B, int H, int dk, int dv,
-                            int dt, void* stream) {
+int dn_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* beta,
+                       const float* g, const float* S0, void* o, float* S_T, int B, int H,
+                       int T, int dk, int dv, int C, int dt, void* stream) {
+    return chunk_fwd_decayed(q, k, v, beta, g, 0, S0, o, S_T, B, H, T, dk, dv, C, dt, stream);
+}
+
+int dn_chunk_fwd_kda(const void* q, const void* k, const void* v, const void* beta,
+                     const float* g, const float* S0, void* o, float* S_T, int B, int H, int T,
+                     int dk, int dv, int C, int dt, void* stream) {
+    return chunk_fwd_decayed(q, k, v, beta, g, 1, S0, o, S_T, B, H, T, dk, dv, C, dt, stream);
+}
+
+static int recurrent_step_decayed(const void* q, const void* k, const void* v,
+                                  const void* beta, const float* g, int per_channel, float* S,
+                                  void* o, int B, int H, int dk, int dv, int dt, void* stream) {
     if (B < 0 || H < 0) return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d)", B, H);
     if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
     if (dk <= 0 || dv <= 0) return fail(DN_ERR_INVALID_ARG, "dk and dv must be positive");
@@ -416,7 +435,8 @@ int dn_recurrent_step_gated(const void* q, const void* k, const void* v, const v
     const size_t es = elem_size(dt);
     const Span sq{"q", q, (size_t)BH * dk * es}, sk{"k", k, (size_t)BH * dk * es},
         sv{"v", v, (size_t)BH * dv * es}, sb{"beta", beta, (size_t)BH * es},
-        sg{"g", g, (size_t)BH * sizeof(float)}, so{"o", o, (size_t)BH * dv * es},
+        sg{"g", g, (size_t)BH * (per_channel ? dk : 1) * sizeof(float)},
+        so{"o", o, (size_t)BH * dv * es},
         sS{"S", S, (size_t)BH * dk * dv * sizeof(float)};
     int dev = 0;
     if (int st = current_device(&dev)) return st;
@@ -429,8 +449,21 @@ int dn_recurrent_step_gated(const void* q, const void* k, const void* v, const v
     for (const Span* s : {&sq, &sk, &sv, &sb, &sg})
         if (overlaps(sS, *s)) return fail(DN_ERR_INVALID_ARG, "S overlaps %s", s->name);
     return cuda_status(dn::launch_recurrent_step(q, k, v, beta, S, o, (int)BH, dk, dv, dt,
-                                                 static_cast<cudaStream_t>(stream), g),
-                       "gated recurrent step launch");
+                                                 static_cast<cudaStream_t>(stream), g,
+                                                 per_channel),
+                       per_channel ? "KDA recurrent step launch" : "gated recurrent step launch");
+}
+
+int dn_recurrent_step_gated(const void* q, const void* k, const void* v, const void* beta,
+                            const float* g, float* S, void* o, int B, int H, int dk, int dv,
+                            int dt, void* stream) {
+    return recurrent_step_decayed(q, k, v, beta, g, 0, S, o, B, H, dk, dv, dt, stream);
+}
+
+int dn_recurrent_step_kda(const void* q, const void* k, const void* v, const void* beta,
+                          const float* g, float* S, void* o, int B, int H, int dk, int dv,
+                          int dt, void* stream) {
+    return recurrent_step_decayed(q, k, v, beta, g, 1, S, o, B, H, dk, dv, dt, stream);
 }
 
 int dn_recurrent_step(const void* q, const void* k, const void* v, const void* beta, float* S,

@@ -32,6 +32,15 @@
 //     S  <- exp(G_C) S + K^T diag(exp(G_C - G_s)) U'
 // (the state S / Gamma_t follows the plain rule on values v_t / Gamma_t; the
 // ratios of Gamma within a chunk are at most 1).
+//
+// KDA (one keep rate per key channel, "Kimi Delta Attention : atténuation
+// par canal", same page) is the kChan instance: G_t[d] per channel, and
+//     A[i][j] = beta_i sum_d k_i[d] k_j[d] exp(G_i[d] - G_j[d])          (j < i)
+//     P[i][j] = sum_d q_i[d] k_j[d] exp(G_i[d] - G_j[d])                 (j <= i)
+//     R'  = diag(beta) (V - (K . exp G) S),   O = (Q . exp G) S + P U'
+//     S  <- diag(exp G_C) S + (K . exp(G_C - G))^T U'
+// The ratios sit inside the sums, so every exponent is <= 0 however strong
+// the decay (no 1 / Gamma factors).
 #include "dn_common.cuh"
 #include "dn_internal.h"
 #include "simt_mm.cuh"
@@ -47,7 +56,7 @@ using simt::zero;
 constexpr int kC = 64;         // chunk length
 constexpr int kLC = kC + 1;    // odd row pitches keep shared-memory reads conflict-free
 
-template <int DK, int NV>
+template <int DK, int NV, bool kChan = false>
 struct SimtSmem {
     static constexpr int LK = DK + 1, LV = NV + 1;
     static constexpr int kK = 0;                       // C x LK   keys
@@ -61,13 +70,14 @@ struct SimtSmem {
     static constexpr int kY = kP + kC * kLC;           // 3 x 16 x 17 solve scratch
     static constexpr int kB = kY + 3 * 16 * 17;        // C        beta
     static constexpr int kG = kB + kC;                 // 3 x C    G, exp(G), exp(G_C - G)
-    static constexpr int kFloats = kG + 3 * kC;
+    static constexpr int kGk = kG + 3 * kC;            // C x LK   per-channel G (KDA)
+    static constexpr int kFloats = kGk + (kChan ? kC * LK : 0);
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
 
 // NMAX > 1: packed variable-length sequences (the CTA's state index is
 // (sequence, head); tokens come from the packed [H][T] layout).
-template <typename T, int DK, int DV, int NV, int NMAX>
+template <typename T, int DK, int DV, int NV, int NMAX, bool kChan = false>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
                   const T* __restrict__ v, const T* __restrict__ beta,
@@ -75,7 +85,7 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
                   float* __restrict__ S_T, float* __restrict__ S_chunks,
                   const float* __restrict__ g, int Ttot, int H,
                   const __grid_constant__ SeqTable<NMAX> seqs) {
-    using L = SimtSmem<DK, NV>;
+    using L = SimtSmem<DK, NV, kChan>;
     constexpr int LK = L::LK, LV = L::LV;
     constexpr int NSLICE = DV / NV;
     extern __shared__ float smem[];
@@ -92,6 +102,7 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
     float* Gc = smem + L::kG;          // cumulative log decay within the chunk
     float* eG = Gc + kC;               // exp(G_t)
     float* dec = eG + kC;              // exp(G_C - G_t)
+    float* Gk = smem + L::kGk;         // KDA: cumulative log decay per key channel
 
     const int tid = threadIdx.x;
     const int tx = tid & 15, ty = tid >> 4;
@@ -125,7 +136,12 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
         load_tile<kThreads, kC, DK, LK, DK>(Qs, q, tok0 + t0, n, 0);
         load_tile<kThreads, kC, NV, LV, DV>(Rs, v, tok0 + t0, n, j0);
         if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
-        if (tid < 32) {  // prefix sums of the log keep rates (padding tokens keep everything)
+        if constexpr (kChan) {  // per-channel rates, then prefix sums over the chunk
+            load_tile<kThreads, kC, DK, LK, DK>(Gk, g, tok0 + t0, n, 0);
+            __syncthreads();
+            if (tid < DK)
+                for (int t = 1; t < kC; ++t) Gk[t * LK + tid] += Gk[(t - 1) * LK + tid];
+        } else if (tid < 32) {  // prefix sums of the log keep rates (padding tokens keep everything)
             const int t = 2 * tid;
             const float a = (g && t < n) ? g[tok0 + t0 + t] : 0.f;
             const float b = (g && t + 1 < n) ? g[tok0 + t0 + t + 1] : 0.f;
@@ -160,20 +176,37 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
                     aq[i] = Qs[(ty + 16 * i) * LK + kk];
                     bk[i] = Ks[(tx + 16 * i) * LK + kk];
                 }
+                if constexpr (kChan) {  // the channel's decay ratio inside the sum
+                    float gi[4], gj[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        aa[i][j] = fmaf(ak[i], bk[j], aa[i][j]);
-                        ap[i][j] = fmaf(aq[i], bk[j], ap[i][j]);
+                    for (int i = 0; i < 4; ++i) {
+                        gi[i] = Gk[(ty + 16 * i) * LK + kk];
+                        gj[i] = Gk[(tx + 16 * i) * LK + kk];
                     }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {  // pairs past the diagonal are masked below
+                            const float e = __expf(fminf(gi[i] - gj[j], 0.f));
+                            aa[i][j] = fmaf(ak[i] * e, bk[j], aa[i][j]);
+                            ap[i][j] = fmaf(aq[i] * e, bk[j], ap[i][j]);
+                        }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            aa[i][j] = fmaf(ak[i], bk[j], aa[i][j]);
+                            ap[i][j] = fmaf(aq[i], bk[j], ap[i][j]);
+                        }
+                }
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int m = ty + 16 * i, nn = tx + 16 * j;
-                    const float r = nn <= m ? expf(Gc[m] - Gc[nn]) : 0.f;
+                    const float r = kChan ? 1.f : (nn <= m ? expf(Gc[m] - Gc[nn]) : 0.f);
                     Am[m * kLC + nn] = nn < m ? bs[m] * (aa[i][j] * r) : 0.f;
                     Pm[m * kLC + nn] = nn <= m ? ap[i][j] * r : 0.f;
                 }
@@ -184,14 +217,16 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
         {
             float acc[4][NV / 16];
             zero<64, NV>(acc);
-            mm_acc<64, NV, DK>(acc, [&](int m, int kk) { return Ks[m * LK + kk]; },
-                               [&](int kk, int nn) { return Ss[kk * LV + nn]; });
+            mm_acc<64, NV, DK>(acc, [&](int m, int kk) {
+                return kChan ? Ks[m * LK + kk] * __expf(Gk[m * LK + kk]) : Ks[m * LK + kk];
+            }, [&](int kk, int nn) { return Ss[kk * LV + nn]; });
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < NV / 16; ++j) {
                     const int m = ty + 16 * i, nn = tx + 16 * j;
-                    Rs[m * LV + nn] = bs[m] * (Rs[m * LV + nn] - eG[m] * acc[i][j]);
+                    const float sc = kChan ? 1.f : eG[m];
+                    Rs[m * LV + nn] = bs[m] * (Rs[m * LV + nn] - sc * acc[i][j]);
                 }
         }
         // ---- X = (I + A)^{-1} (touches only Am, Xm, Ys; ends with a barrier) ----
@@ -215,12 +250,15 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
         if (o) {
             float acc[4][NV / 16];
             zero<64, NV>(acc);
-            mm_acc<64, NV, DK>(acc, [&](int m, int kk) { return Qs[m * LK + kk]; },
-                               [&](int kk, int nn) { return Ss[kk * LV + nn]; });
+            mm_acc<64, NV, DK>(acc, [&](int m, int kk) {
+                return kChan ? Qs[m * LK + kk] * __expf(Gk[m * LK + kk]) : Qs[m * LK + kk];
+            }, [&](int kk, int nn) { return Ss[kk * LV + nn]; });
+            if constexpr (!kChan) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < NV / 16; ++j) acc[i][j] *= eG[ty + 16 * i];
+                    for (int j = 0; j < NV / 16; ++j) acc[i][j] *= eG[ty + 16 * i];
+            }
             mm_acc<64, NV, kC>(acc, [&](int m, int kk) { return Pm[m * kLC + kk]; },
                                [&](int kk, int nn) { return Us[kk * LV + nn]; });
 #pragma unroll
@@ -239,16 +277,20 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
         {
             float acc[DK / 16][NV / 16];
             zero<DK, NV>(acc);
-            mm_acc<DK, NV, kC>(acc, [&](int m, int kk) { return Ks[kk * LK + m] * dec[kk]; },
-                               [&](int kk, int nn) { return Us[kk * LV + nn]; });
-            const float keep = eG[kC - 1];
+            mm_acc<DK, NV, kC>(acc, [&](int m, int kk) {
+                return kChan ? Ks[kk * LK + m] * __expf(Gk[(kC - 1) * LK + m] - Gk[kk * LK + m])
+                             : Ks[kk * LK + m] * dec[kk];
+            }, [&](int kk, int nn) { return Us[kk * LV + nn]; });
 #pragma unroll
-            for (int i = 0; i < DK / 16; ++i)
+            for (int i = 0; i < DK / 16; ++i) {
+                const int row = ty + 16 * i;
+                const float keep = kChan ? __expf(Gk[(kC - 1) * LK + row]) : eG[kC - 1];
 #pragma unroll
                 for (int j = 0; j < NV / 16; ++j) {
-                    float* const sp = Ss + (ty + 16 * i) * LV + tx + 16 * j;
+                    float* const sp = Ss + row * LV + tx + 16 * j;
                     *sp = fmaf(keep, *sp, acc[i][j]);
                 }
+            }
         }
         __syncthreads();
     }
@@ -261,14 +303,14 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
     }
 }
 
-template <typename T, int DK, int DV, int NMAX = 1>
+template <typename T, int DK, int DV, int NMAX = 1, bool kChan = false>
 cudaError_t launch_typed(const void* q, const void* k, const void* v,
                          const void* beta, const float* S0, void* o, float* S_T,
                          float* S_chunks, const float* g, int BH, int Tlen, cudaStream_t stream,
                          int H = 1, const SeqTable<NMAX>* seqs = nullptr) {
     constexpr int NV = DV < 64 ? DV : 64;
-    using L = SimtSmem<DK, NV>;
-    auto kern = chunk_simt_kernel<T, DK, DV, NV, NMAX>;
+    using L = SimtSmem<DK, NV, kChan>;
+    auto kern = chunk_simt_kernel<T, DK, DV, NV, NMAX, kChan>;
     cudaError_t err = cudaFuncSetAttribute(
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
     if (err != cudaSuccess) return err;
@@ -333,6 +375,28 @@ cudaError_t launch_chunk_simt_varlen(const void* q, const void* k, const void* v
         DN_SIMT_VARLEN(__nv_bfloat16, 64, 64)
     }
 #undef DN_SIMT_VARLEN
+    return cudaErrorNotSupported;
+}
+
+cudaError_t launch_chunk_simt_kda(const void* q, const void* k, const void* v, const void* beta,
+                                  const float* g, const float* S0, void* o, float* S_T, int BH,
+                                  int T, int dk, int dv, int dt, cudaStream_t st) {
+    if (BH <= 0 || T <= 0) return cudaSuccess;
+#define DN_SIMT_KDA(T_, DK_, DV_)                                                              \
+    if (dk == DK_ && dv == DV_)                                                                \
+        return launch_typed<T_, DK_, DV_, 1, true>(q, k, v, beta, S0, o, S_T, nullptr, g, BH, T, st);
+    if (dt == 0) {
+        DN_SIMT_KDA(float, 128, 128)
+        DN_SIMT_KDA(float, 128, 64)
+        DN_SIMT_KDA(float, 64, 128)
+        DN_SIMT_KDA(float, 64, 64)
+    } else {
+        DN_SIMT_KDA(__nv_bfloat16, 128, 128)
+        DN_SIMT_KDA(__nv_bfloat16, 128, 64)
+        DN_SIMT_KDA(__nv_bfloat16, 64, 128)
+        DN_SIMT_KDA(__nv_bfloat16, 64, 64)
+    }
+#undef DN_SIMT_KDA
     return cudaErrorNotSupported;
 }
 

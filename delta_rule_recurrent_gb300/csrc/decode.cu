@@ -9,7 +9,9 @@
 //     S <- S + k u^T,  o = r + (k . q) u   (= S_new^T q, read after write)
 // With a log keep rate g (Gated DeltaNet, "Gated DeltaNet : oublier d'abord
 // l'état entier", same page) the state is first decayed by alpha = exp(g):
-// p and r are taken from alpha S and the write is S <- alpha S + k u^T.
+// p and r are taken from alpha S and the write is S <- alpha S + k u^T.  With
+// one rate per key channel (KDA, "Kimi Delta Attention : atténuation par
+// canal") row i of the stored state decays by alpha[i] instead.
 //
 // Work split: one CTA per head.  A thread owns one float4 column group of
 // the value channel and DK / RG rows of the key channel, so a warp's loads
@@ -27,7 +29,8 @@ template <typename T, int DK, int DV, int NT>
 __global__ void __launch_bounds__(NT)
 recurrent_step_kernel(const T* __restrict__ q, const T* __restrict__ k,
                       const T* __restrict__ v, const T* __restrict__ beta,
-                      const float* __restrict__ g, float* __restrict__ S, T* __restrict__ o) {
+                      const float* __restrict__ g, int g_per_channel, float* __restrict__ S,
+                      T* __restrict__ o) {
     constexpr int CG = DV / 4;    // float4 column groups per state row
     constexpr int RG = NT / CG;   // row groups (threads sharing a column group)
     constexpr int RPT = DK / RG;  // state rows per thread
@@ -62,10 +65,16 @@ recurrent_step_kernel(const T* __restrict__ q, const T* __restrict__ k,
         if (tid == 0) kq_s = a;
     }
 
+    // keep rate of each of this thread's state rows (1 without decay)
+    float a[RPT];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r)
+        a[r] = !g ? 1.f : expf(g_per_channel ? g[(size_t)head * DK + rg + r * RG] : g[head]);
+
     float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-        const float kr = ks[rg + r * RG], qr = qs[rg + r * RG];
+    for (int r = 0; r < RPT; ++r) {  // forget before predicting and reading
+        const float kr = a[r] * ks[rg + r * RG], qr = a[r] * qs[rg + r * RG];
         pk.x = fmaf(s[r].x, kr, pk.x); pk.y = fmaf(s[r].y, kr, pk.y);
         pk.z = fmaf(s[r].z, kr, pk.z); pk.w = fmaf(s[r].w, kr, pk.w);
         pq.x = fmaf(s[r].x, qr, pq.x); pq.y = fmaf(s[r].y, qr, pq.y);
@@ -83,9 +92,6 @@ recurrent_step_kernel(const T* __restrict__ q, const T* __restrict__ k,
         R.x += b.x; R.y += b.y; R.z += b.z; R.w += b.w;
     }
     const float bt = beta_s;
-    const float alpha = g ? expf(g[head]) : 1.f;  // forget before predicting
-    P.x *= alpha; P.y *= alpha; P.z *= alpha; P.w *= alpha;
-    R.x *= alpha; R.y *= alpha; R.z *= alpha; R.w *= alpha;
     const int j = cg * 4;
     float4 u;
     u.x = bt * (vs[j + 0] - P.x);
@@ -106,32 +112,32 @@ recurrent_step_kernel(const T* __restrict__ q, const T* __restrict__ k,
     for (int r = 0; r < RPT; ++r) {
         const float kr = ks[rg + r * RG];
         float4 x = s[r];
-        x.x = fmaf(kr, u.x, alpha * x.x); x.y = fmaf(kr, u.y, alpha * x.y);
-        x.z = fmaf(kr, u.z, alpha * x.z); x.w = fmaf(kr, u.w, alpha * x.w);
+        x.x = fmaf(kr, u.x, a[r] * x.x); x.y = fmaf(kr, u.y, a[r] * x.y);
+        x.z = fmaf(kr, u.z, a[r] * x.z); x.w = fmaf(kr, u.w, a[r] * x.w);
         Sh[(size_t)(rg + r * RG) * CG + cg] = x;
     }
 }
 
 template <typename T, int DK, int DV>
 cudaError_t launch_typed(const void* q, const void* k, const void* v,
-                         const void* beta, const float* g, float* S, void* o, int BH,
+                         const void* beta, const float* g, int gpc, float* S, void* o, int BH,
                          cudaStream_t stream) {
     constexpr int NT = 256;
     recurrent_step_kernel<T, DK, DV, NT><<<BH, NT, 0, stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k),
-        static_cast<const T*>(v), static_cast<const T*>(beta), g, S,
+        static_cast<const T*>(v), static_cast<const T*>(beta), g, gpc, S,
         static_cast<T*>(o));
     return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_dims(const void* q, const void* k, const void* v,
-                        const void* beta, const float* g, float* S, void* o, int BH, int dk,
-                        int dv, cudaStream_t st) {
-    if (dk == 128 && dv == 128) return launch_typed<T, 128, 128>(q, k, v, beta, g, S, o, BH, st);
-    if (dk == 128 && dv == 64) return launch_typed<T, 128, 64>(q, k, v, beta, g, S, o, BH, st);
-    if (dk == 64 && dv == 128) return launch_typed<T, 64, 128>(q, k, v, beta, g, S, o, BH, st);
-    if (dk == 64 && dv == 64) return launch_typed<T, 64, 64>(q, k, v, beta, g, S, o, BH, st);
+                        const void* beta, const float* g, int gpc, float* S, void* o, int BH,
+                        int dk, int dv, cudaStream_t st) {
+    if (dk == 128 && dv == 128) return launch_typed<T, 128, 128>(q, k, v, beta, g, gpc, S, o, BH, st);
+    if (dk == 128 && dv == 64) return launch_typed<T, 128, 64>(q, k, v, beta, g, gpc, S, o, BH, st);
+    if (dk == 64 && dv == 128) return launch_typed<T, 64, 128>(q, k, v, beta, g, gpc, S, o, BH, st);
+    if (dk == 64 && dv == 64) return launch_typed<T, 64, 64>(q, k, v, beta, g, gpc, S, o, BH, st);
     return cudaErrorNotSupported;
 }
 
@@ -139,10 +145,11 @@ cudaError_t launch_dims(const void* q, const void* k, const void* v,
 
 cudaError_t launch_recurrent_step(const void* q, const void* k, const void* v,
                                   const void* beta, float* S, void* o, int BH,
-                                  int dk, int dv, int dt, cudaStream_t stream, const float* g) {
+                                  int dk, int dv, int dt, cudaStream_t stream, const float* g,
+                                  int g_per_channel) {
     if (BH <= 0) return cudaSuccess;
-    if (dt == 0) return launch_dims<float>(q, k, v, beta, g, S, o, BH, dk, dv, stream);
-    return launch_dims<__nv_bfloat16>(q, k, v, beta, g, S, o, BH, dk, dv, stream);
+    if (dt == 0) return launch_dims<float>(q, k, v, beta, g, g_per_channel, S, o, BH, dk, dv, stream);
+    return launch_dims<__nv_bfloat16>(q, k, v, beta, g, g_per_channel, S, o, BH, dk, dv, stream);
 }
 
 }  // namespace dn

@@ -23,11 +23,11 @@ struct SeqTable {
 using VarlenTable = SeqTable<kMaxVarlenSeqs>;
 
 // One decoding step over B*H heads (see dn_recurrent_step); with g (fp32
-// [BH] log keep rates) the gated step of dn_recurrent_step_gated.
+// log keep rates, [BH], or [BH][dk] when g_per_channel) the gated or KDA step.
 cudaError_t launch_recurrent_step(const void* q, const void* k, const void* v,
                                   const void* beta, float* S, void* o, int BH,
                                   int dk, int dv, int dt, cudaStream_t stream,
-                                  const float* g = nullptr);
+                                  const float* g = nullptr, int g_per_channel = 0);
 
 // Chunkwise forward with fp32 CUDA-core arithmetic (any T >= 1).  o may be
 // nullptr (no outputs); S_chunks, if given, receives the state at the start
@@ -73,6 +73,10 @@ cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v,
                                    const void* beta, const float* S0, void* o, float* S_T,
                                    const VarlenTable& seqs, int H, int T, void* workspace,
                                    cudaStream_t stream);
+// KDA: g is the fp32 [BH][T][dk] per-key-channel log keep rate.
+cudaError_t launch_chunk_simt_kda(const void* q, const void* k, const void* v, const void* beta,
+                                  const float* g, const float* S0, void* o, float* S_T, int BH,
+                                  int T, int dk, int dv, int dt, cudaStream_t stream);
 cudaError_t launch_chunk_simt_varlen(const void* q, const void* k, const void* v,
                                      const void* beta, const float* S0, void* o, float* S_T,
                                      const VarlenTable& seqs, int H, int T, int dk, int dv,

@@ -290,6 +290,27 @@ DN_API int dn_chunk_fwd_varlen(const void *q, const void *k, const void *v,
 DN_API size_t dn_chunk_fwd_varlen_workspace_bytes(const int *cu_seqlens, int N, int H,
                                            int dk, int dv, int C, int dt);
 
+/*
+ * dn_chunk_fwd_kda / dn_recurrent_step_kda -- Kimi Delta Attention: one keep
+ * rate per key channel, D_t = Diag(exp(g_t)), decays the state's key
+ * channels before the delta rule ("Kimi Delta Attention : atténuation par
+ * canal" and "Transition diagonale-bas rang", fr.news.hada.io/topic?id=31925):
+ *     S_t = S_{t-1} D_t (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,  o_t = S_t q_t
+ * (in the stored [dk][dv] layout, row i of S is scaled by exp(g_t[i])).  The
+ * page's read uses d_k^{-1/2} q_t; as everywhere in this library the caller
+ * applies any query scale.
+ *   g   [B, H, T, dk] fp32 for the chunkwise form, [B, H, dk] for a step
+ * Every other argument, layout and error as for dn_chunk_fwd_gated /
+ * dn_recurrent_step_gated.  fp32 arithmetic on CUDA cores.
+ */
+DN_API int dn_chunk_fwd_kda(const void *q, const void *k, const void *v,
+                     const void *beta, const float *g, const float *S0, void *o,
+                     float *S_T, int B, int H, int T, int dk, int dv, int C, int dt,
+                     void *stream);
+DN_API int dn_recurrent_step_kda(const void *q, const void *k, const void *v,
+                          const void *beta, const float *g, float *S, void *o,
+                          int B, int H, int dk, int dv, int dt, void *stream);
+
 /* ABI version of this header (bumped on incompatible changes). */
 DN_API int dn_abi_version(void);
 

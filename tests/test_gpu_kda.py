@@ -1,0 +1,102 @@
+"""Kimi Delta Attention on the GPU (chunkwise forward and decoding step)
+against the fp64 KDA oracle, through the C ABI.  Bars: relative L2 <= 1e-4
+(fp32 I/O) and <= 1e-2 (bf16 I/O) on o and the state.
+"""
+import pytest
+import torch
+
+import delta_rule_recurrent_gb300 as dn
+import oracle
+import workloads
+from tests.conftest import rel_l2
+from tests.gpu_util import TOL, dev, sample_heads, take_heads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def no_device_error():
+    lib = dn.load()
+    assert lib.dn_device_error() == 0
+    yield
+    assert lib.dn_device_error() == 0
+
+
+def _check(o, S, o_ref, S_ref, dtype, what):
+    eo, eS = rel_l2(o, o_ref), rel_l2(S, S_ref)
+    assert eo <= TOL[dtype], f"{what} o rel L2 {eo:.3e}"
+    assert eS <= TOL[dtype], f"{what} S_T rel L2 {eS:.3e}"
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_kda_chunk_ragged(dk, dv, dtype):
+    B, H, T = 2, 2, 200
+    inp = workloads.chunk_inputs(B, H, T, dk, dv, dtype=dtype, seed=dk + 5 * dv,
+                                 feature_map="silu", s0_std=0.1)
+    g = workloads.gate_inputs(B, H, T, seed=dk * dv, channels=dk)
+    o, S = dn.chunk_fwd_kda(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g),
+                            initial_state=dev(inp.S0))
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.forward_kda(inp.q, inp.k, inp.v, inp.beta, g, inp.S0)
+    _check(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
+           workloads.torch_dtype(dtype), f"{dtype} {dk}x{dv}")
+
+
+def test_kda_equal_channels_match_the_gated_kernel():
+    B, H, T, d = 1, 2, 150, 64
+    inp = workloads.chunk_inputs(B, H, T, d, d, dtype="f32", seed=4, s0_std=0.1)
+    g = workloads.gate_inputs(B, H, T, seed=4)
+    args = [dev(x) for x in (inp.q, inp.k, inp.v, inp.beta)]
+    o1, S1 = dn.chunk_fwd_gated(*args, dev(g), initial_state=dev(inp.S0))
+    o2, S2 = dn.chunk_fwd_kda(*args, dev(g)[..., None].expand(B, H, T, d).contiguous(),
+                              initial_state=dev(inp.S0))
+    assert rel_l2(o2.double().cpu().numpy(), o1.double().cpu().numpy()) <= 1e-5
+    assert rel_l2(S2.double().cpu().numpy(), S1.double().cpu().numpy()) <= 1e-5
+
+
+def test_kda_strong_decay_and_edge_lengths():
+    for T in (1, 64, 65):
+        inp = workloads.chunk_inputs(1, 2, T, 128, 128, dtype="f32", seed=T + 1, s0_std=0.5)
+        g = workloads.gate_inputs(1, 2, T, seed=T, lo=0.05, hi=0.6, channels=128)
+        o, S = dn.chunk_fwd_kda(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g),
+                                initial_state=dev(inp.S0))
+        torch.cuda.synchronize()
+        o_ref, S_ref = oracle.forward_kda(inp.q, inp.k, inp.v, inp.beta, g, inp.S0)
+        _check(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
+               torch.float32, f"T={T}")
+
+
+def test_kda_layer_1p3b_sampled_heads():
+    inp = workloads.workload_inputs("layer1p3b_bf16")
+    B, H, T, d = inp.q.shape
+    g = workloads.gate_inputs(B, H, T, seed=9, channels=d)
+    o, S = dn.chunk_fwd_kda(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g))
+    torch.cuda.synchronize()
+    bi, hi = sample_heads(B, H, 3, seed=10)
+    o_ref, S_ref = oracle.forward_kda(*(take_heads(x, bi, hi) for x in
+                                        (inp.q, inp.k, inp.v, inp.beta, g)))
+    ib, ih = torch.as_tensor(bi).cuda(), torch.as_tensor(hi).cuda()
+    _check(o[ib, ih].double().cpu().numpy()[None], S[ib, ih].double().cpu().numpy()[None],
+           o_ref, S_ref, torch.bfloat16, "1.3B")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_kda_decode_steps(dtype):
+    B, H, d, steps, seed = 4, 4, 128, 24, 13
+    S0 = workloads.decode_state(B, H, d, d, std=0.1, seed=seed)
+    S = dev(S0)
+    rec = {n: [] for n in ("q", "k", "v", "beta", "g", "o")}
+    for step in range(steps):
+        x = workloads.decode_step_inputs(B, H, d, d, step=step, dtype=dtype, seed=seed)
+        g = workloads.gate_inputs(B, H, seed=seed * 100 + step, lo=0.7, channels=d)
+        o = dn.recurrent_step_kda(dev(x.q), dev(x.k), dev(x.v), dev(x.beta), dev(g), S)
+        for n in ("q", "k", "v", "beta"):
+            rec[n].append(getattr(x, n))
+        rec["g"].append(g)
+        rec["o"].append(o.cpu())
+    torch.cuda.synchronize()
+    st = {n: torch.stack(v_, dim=2) for n, v_ in rec.items()}
+    o_ref, S_ref = oracle.forward_kda(st["q"], st["k"], st["v"], st["beta"], st["g"], S0)
+    _check(st["o"].double().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
+           workloads.torch_dtype(dtype), f"decode {dtype}")

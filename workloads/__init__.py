@@ -244,11 +244,14 @@ def grad_inputs(B: int, H: int, T: int, dv: int, dk: int | None = None, *, dtype
 
 
 def gate_inputs(B: int, H: int, T: int | None = None, *, seed: int = 0, lo: float = 0.9,
-                hi: float = 1.0) -> torch.Tensor:
+                hi: float = 1.0, channels: int | None = None) -> torch.Tensor:
     """Log keep rates g = log(alpha), alpha ~ U(lo, hi) fp32, [B, H, T] (or
-    [B, H] when T is None); seeded by (seed, "gate")."""
+    [B, H] when T is None), with a trailing [channels] axis for per-channel
+    rates; seeded by (seed, "gate")."""
     gen = torch.Generator().manual_seed(int(seed) * 6151 + 3571)
     shape = (B, H) if T is None else (B, H, T)
+    if channels is not None:
+        shape = shape + (channels,)
     alpha = lo + (hi - lo) * torch.rand(shape, generator=gen)
     return torch.log(alpha).float().contiguous()
 

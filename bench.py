@@ -421,6 +421,33 @@ def run_ours(args, rank, world, local):
         gd_region_s, gd_launch = timed_loop(gated_decode_step, nsteps, stream, world)
         gd_region_s = max_over_ranks(gd_region_s, world)
         del dgate, Sdg
+
+        # ---------------- KDA: per-key-channel decay, chunk forward and step --
+        kgate = workloads.gate_inputs(B, H, T, seed=w["seed"], channels=dk).to(dev)
+        ok_, Sk_ = torch.empty_like(o), torch.empty_like(S_T)
+
+        def kda_step(_i):
+            dn.chunk_fwd_kda(q, k, v, beta, kgate, out=ok_, final_state=Sk_)
+
+        for i in range(min(args.warmup, 3)):
+            kda_step(i)
+        torch.cuda.synchronize()
+        k_region_s, k_launch = timed_loop(kda_step, gsteps, stream, world)
+        k_region_s = max_over_ranks(k_region_s, world)
+        del kgate, ok_, Sk_
+
+        dkgate = workloads.gate_inputs(Bd, Hd, seed=wd["seed"], channels=dkd).to(dev)
+        Sdk = Sd.clone()
+
+        def kda_decode_step(i):
+            dn.recurrent_step_kda(dq[i], dkk[i], dvv[i], db[i], dkgate, Sdk, out=od)
+
+        for i in range(args.warmup):
+            kda_decode_step(nsteps + i)
+        torch.cuda.synchronize()
+        kd_region_s, kd_launch = timed_loop(kda_decode_step, nsteps, stream, world)
+        kd_region_s = max_over_ranks(kd_region_s, world)
+        del dkgate, Sdk
     clk = clocks.summary()
     del dq, dkk, dvv, db
 
@@ -545,6 +572,29 @@ def run_ours(args, rank, world, local):
                                 "traffic": None, "peak_source": f"{peak_src} (copy bandwidth)",
                                 "bytes_per_launch": gdbytes, "launch_us": gd_launch_s * 1e6}},
     }
+    k_launch_s = statistics.mean(k_launch) / 1e3
+    kd_launch_s = statistics.mean(kd_launch) / 1e3
+    kdbytes = dbytes + Bd * Hd * dkd * 4  # plus the fp32 per-channel log keep rates
+    kda = {
+        "chunk": {"workload": HEADLINE, "steps": gsteps,
+                  "value": world * tokens * gsteps / k_region_s, "unit": "tokens/s",
+                  "ms_per_step": 1e3 * k_region_s / gsteps, "arith": "fp32 CUDA cores",
+                  "gate": "alpha ~ U(0.9, 1) per key channel",
+                  "roofline": {"bound": "alu", "achieved": gflops / k_launch_s / 1e12,
+                               "peak": fp32_alu_tflops(2070.0), "unit": "TFLOP/s",
+                               "frac": gflops / k_launch_s / 1e12 / fp32_alu_tflops(2070.0),
+                               "traffic": None,
+                               "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz",
+                               "flops_per_launch": gflops, "launch_us": k_launch_s * 1e6}},
+        "decode": {"workload": DECODE, "steps": nsteps,
+                   "value": world * Bd * nsteps / kd_region_s, "unit": "tokens/s",
+                   "ms_per_step": 1e3 * kd_region_s / nsteps,
+                   "roofline": {"bound": "hbm", "achieved": kdbytes / kd_launch_s / 1e9,
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": kdbytes / kd_launch_s / 1e9 / peaks["hbm_gbs"],
+                                "traffic": None, "peak_source": f"{peak_src} (copy bandwidth)",
+                                "bytes_per_launch": kdbytes, "launch_us": kd_launch_s * 1e6}},
+    }
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * region_s / args.steps,
@@ -560,12 +610,13 @@ def run_ours(args, rank, world, local):
         "backward": backward,
         "varlen": varlen,
         "gated": gated,
+        "kda": kda,
         "e2e": {"value": world * tokens * e2e_steps / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": 1e3 * e2e_s / e2e_steps},
         "gpu_launches": launches_per_call * (args.steps + e2e_steps) + nsteps
                         + (nsteps if dec_graph[0] else 0) + 3 * bwd_steps + gsteps + nsteps
-                        + launches_per_call * vsteps,
+                        + launches_per_call * vsteps + gsteps + nsteps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

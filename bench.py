@@ -397,9 +397,14 @@ def run_ours(args, rank, world, local):
         gate = workloads.gate_inputs(B, H, T, seed=w["seed"]).to(dev)
         og = torch.empty_like(o)
         Sg = torch.empty_like(S_T)
+        gneed = lib.dn_chunk_fwd_gated_workspace_bytes(B, H, T, dk, dv, C, 1 if tc else 0)
+        gws = torch.empty(gneed, dtype=torch.uint8, device=dev) if gneed else None
 
-        def gated_step(_i):
-            dn.chunk_fwd_gated(q, k, v, beta, gate, out=og, final_state=Sg)
+        def gated_step(_i):  # the tcgen05 form where it applies
+            dn.chunk_fwd_gated(q, k, v, beta, gate, out=og, final_state=Sg, workspace=gws)
+
+        def gated_simt_step(_i):
+            dn.chunk_fwd_gated(q, k, v, beta, gate, out=og, final_state=Sg, workspace=None)
 
         gsteps = max(1, min(args.steps, 10))
         for i in range(min(args.warmup, 3)):
@@ -407,7 +412,12 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         g_region_s, g_launch = timed_loop(gated_step, gsteps, stream, world)
         g_region_s = max_over_ranks(g_region_s, world)
-        del gate, og, Sg
+        for i in range(min(args.warmup, 3)):
+            gated_simt_step(i)
+        torch.cuda.synchronize()
+        gs_region_s, gs_launch = timed_loop(gated_simt_step, gsteps, stream, world)
+        gs_region_s = max_over_ranks(gs_region_s, world)
+        del gate, og, Sg, gws
 
         dgate = workloads.gate_inputs(Bd, Hd, seed=wd["seed"]).to(dev)
         Sdg = Sd.clone()
@@ -549,20 +559,39 @@ def run_ours(args, rank, world, local):
                      "peak_source": f"{peak_src} (bf16 dense burst)", "launch_us": vl_launch_s * 1e6},
     }
     g_launch_s = statistics.mean(g_launch) / 1e3
+    gs_launch_s = statistics.mean(gs_launch) / 1e3
     gflops = chunk_flops_per_token_head(C, dk, dv) * B * H * T
+    alu_peak = fp32_alu_tflops(2070.0)
+    alu_src = "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz"
+    if gneed:
+        g_arith, g_peak, g_bound = "tcgen05 bf16 MMAs, fp32 accumulation (two passes)", \
+            peaks["bf16_tflops"], "tensor"
+        g_src = f"{peak_src} (bf16 dense burst)"
+    else:
+        g_arith, g_peak, g_bound, g_src = "fp32 CUDA cores", alu_peak, "alu", alu_src
     gd_launch_s = statistics.mean(gd_launch) / 1e3
     gdbytes = dbytes + Bd * Hd * 4  # plus the fp32 log keep rate per head
     gated = {
         "chunk": {"workload": HEADLINE, "steps": gsteps,
                   "value": world * tokens * gsteps / g_region_s, "unit": "tokens/s",
-                  "ms_per_step": 1e3 * g_region_s / gsteps, "arith": "fp32 CUDA cores",
-                  "gate": "alpha ~ U(0.9, 1)",
-                  "roofline": {"bound": "alu", "achieved": gflops / g_launch_s / 1e12,
-                               "peak": fp32_alu_tflops(2070.0), "unit": "TFLOP/s",
-                               "frac": gflops / g_launch_s / 1e12 / fp32_alu_tflops(2070.0),
-                               "traffic": None,
-                               "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz",
+                  "ms_per_step": 1e3 * g_region_s / gsteps, "arith": g_arith,
+                  "gate": "alpha ~ U(0.9, 1)", "workspace_bytes": gneed,
+                  "launches_per_call": 2 if gneed else 1,
+                  "roofline": {"bound": g_bound, "achieved": gflops / g_launch_s / 1e12,
+                               "peak": g_peak, "unit": "TFLOP/s",
+                               "frac": gflops / g_launch_s / 1e12 / g_peak,
+                               "traffic": None, "peak_source": g_src,
                                "flops_per_launch": gflops, "launch_us": g_launch_s * 1e6}},
+        "chunk_cuda_cores": {"workload": HEADLINE, "steps": gsteps,
+                             "value": world * tokens * gsteps / gs_region_s, "unit": "tokens/s",
+                             "ms_per_step": 1e3 * gs_region_s / gsteps, "arith": "fp32 CUDA cores",
+                             "note": "the same call with no workspace",
+                             "roofline": {"bound": "alu", "achieved": gflops / gs_launch_s / 1e12,
+                                          "peak": alu_peak, "unit": "TFLOP/s",
+                                          "frac": gflops / gs_launch_s / 1e12 / alu_peak,
+                                          "traffic": None, "peak_source": alu_src,
+                                          "flops_per_launch": gflops,
+                                          "launch_us": gs_launch_s * 1e6}},
         "decode": {"workload": DECODE, "steps": nsteps,
                    "value": world * Bd * nsteps / gd_region_s, "unit": "tokens/s",
                    "ms_per_step": 1e3 * gd_region_s / nsteps,

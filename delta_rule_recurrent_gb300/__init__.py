@@ -232,11 +232,15 @@ def _check_gate(g: torch.Tensor, shape, dev) -> None:
 def chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
                     g: torch.Tensor, initial_state: torch.Tensor | None = None,
                     output_final_state: bool = True, chunk_size: int = 64,
-                    out: torch.Tensor | None = None, final_state: torch.Tensor | None = None):
+                    out: torch.Tensor | None = None, final_state: torch.Tensor | None = None,
+                    workspace="auto"):
     """Gated DeltaNet, chunkwise (``dn_chunk_fwd_gated``): ``g`` is the fp32
-    ``[B, H, T]`` log keep rate.  Returns ``(o, S_T)`` as ``chunk_fwd``."""
+    ``[B, H, T]`` log keep rate.  Returns ``(o, S_T)`` as ``chunk_fwd``.
+    ``workspace``: "auto" allocates the scratch of the two-pass tensor-core
+    form where it applies (``dn_chunk_fwd_gated_workspace_bytes``), None runs
+    the fp32 CUDA-core kernel, a uint8 CUDA tensor supplies the scratch."""
     return _chunk_decayed(q, k, v, beta, g, False, initial_state, output_final_state,
-                          chunk_size, out, final_state)
+                          chunk_size, out, final_state, workspace)
 
 
 def chunk_fwd_kda(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
@@ -246,11 +250,11 @@ def chunk_fwd_kda(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch
     """Kimi Delta Attention, chunkwise (``dn_chunk_fwd_kda``): ``g`` is the
     fp32 ``[B, H, T, dk]`` per-key-channel log keep rate."""
     return _chunk_decayed(q, k, v, beta, g, True, initial_state, output_final_state,
-                          chunk_size, out, final_state)
+                          chunk_size, out, final_state, None)
 
 
 def _chunk_decayed(q, k, v, beta, g, per_channel, initial_state, output_final_state,
-                   chunk_size, out, final_state):
+                   chunk_size, out, final_state, workspace):
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
         _check_cuda(name, t, dev)
@@ -275,13 +279,25 @@ def _chunk_decayed(q, k, v, beta, g, per_channel, initial_state, output_final_st
         S_T = final_state if final_state is not None else torch.empty(
             (B, H, dk, dv), dtype=torch.float32, device=dev)
     lib = load()
-    with torch.cuda.device(dev):
-        entry = lib.dn_chunk_fwd_kda if per_channel else lib.dn_chunk_fwd_gated
-        check(entry(
-            q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(), g.data_ptr(),
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(), g.data_ptr(),
             initial_state.data_ptr() if initial_state is not None else None, out.data_ptr(),
-            S_T.data_ptr() if S_T is not None else None, B, H, T, dk, dv, chunk_size, dt,
-            _stream_handle(dev)))
+            S_T.data_ptr() if S_T is not None else None, B, H, T, dk, dv, chunk_size, dt)
+    with torch.cuda.device(dev):
+        if per_channel:
+            check(lib.dn_chunk_fwd_kda(*args, _stream_handle(dev)))
+            return out, S_T
+        if isinstance(workspace, str):
+            if workspace != "auto":
+                raise ValueError("workspace must be 'auto', None or a uint8 CUDA tensor")
+            need = lib.dn_chunk_fwd_gated_workspace_bytes(B, H, T, dk, dv, chunk_size, dt)
+            ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
+        else:
+            ws = workspace
+            if ws is not None:
+                _check_cuda("workspace", ws, dev)
+        ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+        check(lib.dn_chunk_fwd_gated(*args, ws.data_ptr() if ws is not None else None, ws_bytes,
+                                     _stream_handle(dev)))
     return out, S_T
 
 

@@ -38,7 +38,9 @@ SIGNATURES = {
     "dn_chunk_fwd_varlen": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _fp, _ip] + [_int] * 7
                             + [_vp, _size, _vp]),
     "dn_chunk_fwd_varlen_workspace_bytes": (_size, [_ip] + [_int] * 6),
-    "dn_chunk_fwd_gated": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp] + [_int] * 7 + [_vp]),
+    "dn_chunk_fwd_gated": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp] + [_int] * 7
+                           + [_vp, _size, _vp]),
+    "dn_chunk_fwd_gated_workspace_bytes": (_size, [_int] * 7),
     "dn_recurrent_step_gated": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp] + [_int] * 5 + [_vp]),
     "dn_chunk_fwd_kda": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp] + [_int] * 7 + [_vp]),
     "dn_recurrent_step_kda": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp] + [_int] * 5 + [_vp]),
@@ -88,7 +90,7 @@ def load(path: Path | None = None):
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)
         fn.restype, fn.argtypes = res, args
-    if lib.dn_abi_version() != 1:
+    if lib.dn_abi_version() != 2:
         raise RuntimeError("libdeltanet ABI version mismatch")
     if path is None:
         _lib = lib

@@ -352,10 +352,12 @@ int dn_chunk_fwd_varlen(const void* q, const void* k, const void* v, const void*
 
 // The decayed chunkwise forms: Gated DeltaNet (one log keep rate per token,
 // per_channel = 0) and KDA (one per token and key channel, per_channel = 1).
+// Gated: a workspace of dn_chunk_fwd_gated_workspace_bytes bytes selects the
+// two-pass tensor-core form where it applies.
 static int chunk_fwd_decayed(const void* q, const void* k, const void* v, const void* beta,
                              const float* g, int per_channel, const float* S0, void* o,
                              float* S_T, int B, int H, int T, int dk, int dv, int C, int dt,
-                             void* stream) {
+                             void* workspace, size_t workspace_bytes, void* stream) {
     if (B < 0 || H < 0 || T < 0)
         return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d T=%d)", B, H, T);
     if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
@@ -366,6 +368,11 @@ static int chunk_fwd_decayed(const void* q, const void* k, const void* v, const 
     if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this build supports 64", C);
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
+    const size_t need_ws =
+        per_channel ? 0 : dn_chunk_fwd_gated_workspace_bytes(B, H, T, dk, dv, C, dt);
+    if (workspace && workspace_bytes < need_ws)
+        return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed (or pass NULL)",
+                    workspace_bytes, need_ws);
     if (BH == 0) return ok();
     const size_t es = elem_size(dt);
     const size_t ntok = (size_t)BH * (size_t)T;
@@ -404,21 +411,40 @@ static int chunk_fwd_decayed(const void* q, const void* k, const void* v, const 
         return cuda_status(
             dn::launch_chunk_simt_kda(q, k, v, beta, g, S0, o, S_T, (int)BH, T, dk, dv, dt, st),
             "KDA chunk forward launch");
+    if (workspace && need_ws > 0) {
+        const Span sw{"workspace", workspace, need_ws};
+        if (int st2 = check_device_ptr(sw, 16, dev)) return st2;
+        for (const Span* s : {&sq, &sk, &sv, &sb, &sg, &so, &s0, &sT})
+            if (overlaps(sw, *s)) return fail(DN_ERR_INVALID_ARG, "workspace overlaps %s", s->name);
+        return cuda_status(dn::launch_chunk_tc_gated(q, k, v, beta, g, S0, o, S_T, (int)BH, T, dk,
+                                                     dv, dt, workspace, st),
+                           "gated chunk forward (tcgen05) launch");
+    }
     return cuda_status(dn::launch_chunk_simt(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, st,
                                              nullptr, g),
                        "gated chunk forward launch");
 }
 
+size_t dn_chunk_fwd_gated_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt) {
+    if (B <= 0 || H <= 0 || T <= 0 || C != 64 || !dn::chunk_tc_supports(dk, dv, dt)) return 0;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return 0;
+    return dn::chunk_tc_gated_workspace_bytes((int)BH, T);
+}
+
 int dn_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* beta,
                        const float* g, const float* S0, void* o, float* S_T, int B, int H,
-                       int T, int dk, int dv, int C, int dt, void* stream) {
-    return chunk_fwd_decayed(q, k, v, beta, g, 0, S0, o, S_T, B, H, T, dk, dv, C, dt, stream);
+                       int T, int dk, int dv, int C, int dt, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    return chunk_fwd_decayed(q, k, v, beta, g, 0, S0, o, S_T, B, H, T, dk, dv, C, dt, workspace,
+                             workspace_bytes, stream);
 }
 
 int dn_chunk_fwd_kda(const void* q, const void* k, const void* v, const void* beta,
                      const float* g, const float* S0, void* o, float* S_T, int B, int H, int T,
                      int dk, int dv, int C, int dt, void* stream) {
-    return chunk_fwd_decayed(q, k, v, beta, g, 1, S0, o, S_T, B, H, T, dk, dv, C, dt, stream);
+    return chunk_fwd_decayed(q, k, v, beta, g, 1, S0, o, S_T, B, H, T, dk, dv, C, dt, nullptr, 0,
+                             stream);
 }
 
 static int recurrent_step_decayed(const void* q, const void* k, const void* v,

@@ -971,23 +971,33 @@ __device__ __forceinline__ SeqSpan scan_span(const SeqTable<NMAX>& seqs, int bh,
 // [K; Q] is spent once G is formed, so the next item's tiles (and strengths)
 // are fetched while this item is solved; [PT; Tm] is built over the fp32
 // solve array, which is spent once Tm has been read from it.
+//
+// Gated DeltaNet (kGate; a log keep rate g per token, "Gated DeltaNet :
+// oublier d'abord l'état entier", fr.news.hada.io/topic?id=31925): with G_t
+// the cumulative log decay from the chunk start, A and P carry the ratios
+// exp(G_i - G_j) <= 1, and the item also writes the chunk's decay vectors
+// for the scan (exp G_t, exp(G_C - G_t) and exp G_C; kSideFloats per chunk).
 constexpr int kPrepThreads = 128;
+constexpr int kSideFloats = 256;
 constexpr int kPrepCtasPerSm = 4;
 constexpr uint32_t P_OFF_KQ = 0;                   // [K; Q] tile
 constexpr uint32_t P_OFF_X = P_OFF_KQ + kStageKQ;  // fp32 A, overwritten by X; then [PT; Tm]
 constexpr uint32_t P_OFF_Y = P_OFF_X + kXBytes;    // solve scratch
 constexpr uint32_t P_OFF_BETA = P_OFF_Y + kYBytes; // 64 fp32
-constexpr uint32_t P_OFF_BAR = P_OFF_BETA + 256;   // mbarriers: tiles landed, MMA done, drain
+constexpr uint32_t P_OFF_G = P_OFF_BETA + 256;     // 64 fp32 cumulative log decay + 2 partials
+constexpr uint32_t P_OFF_BAR = P_OFF_G + 272;      // mbarriers: tiles landed, MMA done, drain
 constexpr uint32_t P_OFF_MISC = P_OFF_BAR + 24;    // abort flag, TMEM address
 constexpr uint32_t kPrepSmemBytes = P_OFF_MISC + 16 + 1024;
 static_assert(kPrepCtasPerSm * (kPrepSmemBytes + 1024) <= 233472, "prepare kernel occupancy");
 static_assert(P_OFF_X % 1024 == 0 && kXBytes >= kTile, "[PT; Tm] over the solve array");
 
-template <int NMAX>
+template <int NMAX, bool kGate>
 __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_ws, const __nv_bfloat16* __restrict__ beta,
-                  int T, int nchunks, int items, const __grid_constant__ SeqTable<NMAX> seqs) {
+                  int T, int nchunks, int items, const __grid_constant__ SeqTable<NMAX> seqs,
+                  const float* __restrict__ gate, float* __restrict__ side) {
+    static_assert(!kGate || NMAX == 1, "gating on the batched layout");
     constexpr int kBar = 1, B_TILES = 0, B_MMA = 1, B_END = 2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -996,6 +1006,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     float* const X = reinterpret_cast<float*>(gbase + P_OFF_X);
     float* const Ys = reinterpret_cast<float*>(gbase + P_OFF_Y);
     float* const betas = reinterpret_cast<float*>(gbase + P_OFF_BETA);
+    float* const Gs = reinterpret_cast<float*>(gbase + P_OFF_G);  // [64] then 2 warp partials
     int* const misc = reinterpret_cast<int*>(gbase + P_OFF_MISC);
     const Ctl ctl{base + P_OFF_BAR, reinterpret_cast<volatile int*>(misc)};
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
@@ -1036,6 +1047,16 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int tok = r.row0 + t;
         return tok < r.end ? ld_nc_u16(beta + (size_t)r.z * T + tok) : (uint16_t)0;
     };
+    // Log keep rate of token t of item w (0 past T: padding keeps everything).
+    auto load_gate = [&](int w) -> float {
+        if constexpr (kGate) {
+            const ChunkRef r = prep_item(seqs, w, nchunks, T);
+            const int tok = r.row0 + t;
+            return tok < r.end ? gate[(size_t)r.z * T + tok] : 0.f;
+        } else {
+            return 0.f;
+        }
+    };
 
     int n = 0, loads = 0;  // items finished, tile loads issued (thread 0)
     if (t == 0 && (int)blockIdx.x < items) {
@@ -1043,9 +1064,23 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ++loads;
     }
     uint16_t bnext = (t < kC && (int)blockIdx.x < items) ? load_beta(blockIdx.x) : (uint16_t)0;
+    float gnext = (kGate && t < kC && (int)blockIdx.x < items) ? load_gate(blockIdx.x) : 0.f;
     for (int w = blockIdx.x; w < items; w += gridDim.x, ++n) {
         const int wn = w + (int)gridDim.x;
         if (t < kC) betas[t] = __bfloat162float(__ushort_as_bfloat16(bnext));
+        if constexpr (kGate) {  // G_t: inclusive prefix sums over the chunk (warps 0 and 1)
+            if (t < kC) {
+                float x = gnext;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, off);
+                    if ((t & 31) >= off) x += y;
+                }
+                if ((t & 31) == 31) Gs[64 + (t >> 5)] = x;
+                wg_sync(2, 64);
+                Gs[t] = t >= 32 ? x + Gs[64] : x;
+            }
+        }
         // G = [K; Q] K^T
         bool ok = true;
         if (t == 0) {
@@ -1072,6 +1107,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
         }
         if (t < kC && wn < items) bnext = load_beta(wn);
+        if (kGate && t < kC && wn < items) gnext = load_gate(wn);
         if (wg_sync_or(kBar, !ok)) break;
         tc_fence_after_sync();
         // A (TMEM rows 0-63) into the solve array; P (rows 64-127) stays in TMEM.
@@ -1079,6 +1115,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             float x[64];
             tmem_ld64f(tmem + lane_base, x);
             const float bi = betas[row];
+            if constexpr (kGate) {  // decay ratios exp(G_i - G_j), j < i
+                const float gi = Gs[row];
+#pragma unroll
+                for (int j = 0; j < 64; ++j) x[j] *= __expf(fminf(gi - Gs[j], 0.f));
+            }
 #pragma unroll
             for (int j = 0; j < 64; j += 4)
                 sts4(X + row * kP + j,
@@ -1103,6 +1144,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             } else {
                 tmem_ld64f(tmem + lane_base, x);
+                if constexpr (kGate) {  // decay ratios exp(G_i - G_j), j <= i
+                    const float gi = Gs[row];
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) x[j] *= __expf(fminf(gi - Gs[j], 0.f));
+                }
 #pragma unroll
                 for (int j = 0; j < 64; ++j)
                     if (j > row) x[j] = 0.f;
@@ -1139,6 +1185,14 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const ChunkRef r = prep_item(seqs, w, nchunks, T);
             tma_store_3d(&tm_ws, tp, 0, r.wsrow, r.z);
             bulk_commit_group();
+        }
+        if constexpr (kGate) {  // the chunk's decay vectors for the scan
+            if (t < kC) {
+                float* const sd = side + (size_t)w * kSideFloats;  // w = bh * nchunks + c
+                sd[t] = __expf(Gs[t]);                   // exp G_t
+                sd[64 + t] = __expf(Gs[63] - Gs[t]);     // exp(G_C - G_t)
+                if (t == 0) sd[128] = __expf(Gs[63]);    // exp G_C
+            }
         }
     }
     if (t == 0) {
@@ -1196,11 +1250,13 @@ enum : int {
 };
 constexpr int kBars = 28;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * kBars;     // abort flag, TMEM address
-constexpr uint32_t kSmemBytes = OFF_MISC + 16 + 1024;
+constexpr uint32_t OFF_SIDE = OFF_MISC + 16;           // gated: exp G (chunk group), dec (state)
+constexpr uint32_t kSmemBytes = OFF_SIDE + 512 + 1024;
 static_assert(kSmemBytes <= 232448, "scan kernel shared memory");
 // TMEM columns: S^T fp32 | D1^T fp32 (o rows 0-63, U' rows 64-127) | S^T bf16 |
 // U'^T bf16 | the chunk group's 128 DW accumulator columns.
 constexpr uint32_t C_ST = 0, C_D1 = 128, C_SB = 256, C_UB = 320, C_GRP = 352;
+constexpr uint32_t C_GA = 480;  // gated: [PT; Tm] diag(exp G) as the group's A operand
 constexpr uint32_t ID_VP = idesc_bf16_f32(128, 128, 1, 0);  // A v^T (MN-major), B [PT;Tm] (K-major)
 constexpr uint32_t ID_SP = idesc_bf16_f32(128, 128, 0, 0);  // A S^T (TMEM), B [Q';-W] (K-major)
 constexpr uint32_t ID_KB = idesc_bf16_f32(128, 128, 0, 1);  // A U'^T (TMEM) or [PT;Tm], B K (MN-major)
@@ -1301,12 +1357,48 @@ __device__ __forceinline__ void tmem_pack64(uint32_t src, uint32_t dst, float* r
     tmem_st32(dst, p);
 }
 
+// Gated forms of the two packs.  S^T: packed, then scaled in place by the
+// chunk's keep factor exp G_C.  U'^T: token column e scaled by dec[e] =
+// exp(G_C - G_e) (shared memory) as it is packed.
+__device__ __forceinline__ void tmem_pack64_keep(uint32_t src, uint32_t dst, float keep) {
+    float x[64];
+    tmem_ld64f(src, x);
+    uint32_t p[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) p[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+    tmem_st32(dst, p);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(keep * x[32 * h + e]);
+        tmem_st32(src + 32u * h, r);
+    }
+}
+__device__ __forceinline__ void tmem_pack64_cols(uint32_t src, uint32_t dst,
+                                                 const float* __restrict__ dec) {
+    float x[64];
+    tmem_ld64f(src, x);
+    const float4* const d4 = reinterpret_cast<const float4*>(dec);
+    uint32_t p[32];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const float4 d = d4[e];
+        p[2 * e] = pack_bf16(x[4 * e] * d.x, x[4 * e + 1] * d.y);
+        p[2 * e + 1] = pack_bf16(x[4 * e + 2] * d.z, x[4 * e + 3] * d.w);
+    }
+    tmem_st32(dst, p);
+}
+
 // kRec: also record S at every chunk start (the backward's recompute); the
 // forward proper is compiled without it, so its state chain carries no test.
-template <bool kRec>
+// kGate: S <- exp(G_C) S + K^T diag(exp(G_C - G_s)) U' per chunk, with the
+// decay vectors read from side (global) and staged in sdec (shared memory).
+template <bool kRec, bool kGate>
 __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                            const float* __restrict__ S0, float* __restrict__ S_T,
-                           float* __restrict__ S_chunks, int bh, int nchunks) {
+                           float* __restrict__ S_chunks, int bh, int nchunks,
+                           const float* __restrict__ side, float* sdec) {
     constexpr int kBar = 1;
     const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
     // S0^T into TMEM: lane t holds dv column t of S0 (zeros without S0).
@@ -1322,10 +1414,22 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
 
     for (int c = 0; c < nchunks; ++c) {
         const int g = c & 1;
+        float keep = 1.f;
+        float4 dec4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (kGate) {  // issued before the wait; sdec is free (last read before a barrier)
+            const float* const sd = side + (size_t)c * kSideFloats;
+            keep = __ldg(sd + 128);
+            if (t < 16) dec4 = __ldg(reinterpret_cast<const float4*>(sd + 64) + t);
+        }
         if (c > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(c - 1), t, kBar)) return;
         tc_fence_after_sync();
         // S^T -> bf16 (dk 0-63, then 64-127); S itself recorded when asked
-        if constexpr (kRec) {
+        if constexpr (kGate) {
+            static_assert(!kRec, "no state recording on the gated form");
+            if (t < 16) reinterpret_cast<float4*>(sdec)[t] = dec4;
+            tmem_pack64_keep(lane + C_ST, lane + C_SB, keep);
+            tmem_pack64_keep(lane + C_ST + 64u, lane + C_SB + 32u, keep);
+        } else if constexpr (kRec) {
             float* const rec = S_chunks + ((size_t)bh * nchunks + c) * kD * kD + t;
             tmem_pack64(lane + C_ST, lane + C_SB, rec);
             tmem_pack64(lane + C_ST + 64u, lane + C_SB + 32u, rec + 64 * kD);
@@ -1356,7 +1460,10 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         }
         if (wg_sync_or(kBar, !ok)) return;
         tc_fence_after_sync();
-        tmem_pack64(lane + C_D1 + 64u, lane + C_UB);  // U'^T -> bf16 (tokens)
+        if constexpr (kGate)
+            tmem_pack64_cols(lane + C_D1 + 64u, lane + C_UB, sdec);
+        else
+            tmem_pack64(lane + C_D1 + 64u, lane + C_UB);  // U'^T -> bf16 (tokens)
         tmem_wait_st();
         tc_fence_before_sync();
         wg_sync(kBar);
@@ -1389,7 +1496,13 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
 // (2 dk-half regions of 128 rows x 64 bf16): DW = [PT; Tm] K into its 128
 // accumulator columns, then row t of [Q - PT K; -W] from DW and the chunk's q
 // rows.  Thread t owns TMEM lane t; thread 0 issues.
-__device__ void group_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int nchunks) {
+// Gated (kGate): the key term uses K scaled by exp G per token, i.e.
+// DW = [PT; Tm] diag(exp G) K: row t of [PT; Tm] is scaled by exp G column
+// by column into TMEM (C_GA) and the MMA reads it from there; Q' = exp(G_t) q_t
+// - (PT diag(exp G) K)_t.  side holds the chunk's decay vectors.
+template <bool kGate>
+__device__ void group_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int nchunks,
+                           const float* __restrict__ side, float* seg) {
     constexpr int kBar = 2;
     const int row = t & 63;
     const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
@@ -1397,20 +1510,50 @@ __device__ void group_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         const int g = c & 1;
         const uint32_t kq = sm.kq(c), tp = sm.tp(g), qw = sm.qw(g);
         bool ok = true;
+        float4 eg_in = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (kGate && t < 16)  // issued before the waits; seg was last read before a barrier
+            eg_in = __ldg(reinterpret_cast<const float4*>(side + (size_t)c * kSideFloats) + t);
         // [PT; Tm] is loaded only after the state released this buffer set,
         // so the [Q'; -W] tile is free as well.
-        if (t == 0) {
+        if (t == 0)
             ok = ctl.wait(B_KQ_FULL + c % kKQ, (uint32_t)(c / kKQ)) &&
                  ctl.wait(B_TP_FULL + g, (uint32_t)(c >> 1));
-            if (ok) {
-                tc_fence_after_sync();
+        float eg_row = 1.f;
+        if constexpr (kGate) {  // row t of [PT; Tm] diag(exp G) into TMEM
+            if (t < 16) reinterpret_cast<float4*>(seg)[t] = eg_in;
+            if (wg_sync_or(kBar, !ok)) return;
+            const float4* const eg4 = reinterpret_cast<const float4*>(seg);
+            uint32_t pk[32];
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
+            for (int cc = 0; cc < 8; ++cc) {
+                const uint4 tv = ld_shared_v4(tp + sw128(t, cc));
+                const float4 e0 = eg4[2 * cc], e1 = eg4[2 * cc + 1];
+                const float2 a0 = unpack_bf16(tv.x), a1 = unpack_bf16(tv.y),
+                             a2 = unpack_bf16(tv.z), a3 = unpack_bf16(tv.w);
+                pk[4 * cc + 0] = pack_bf16(a0.x * e0.x, a0.y * e0.y);
+                pk[4 * cc + 1] = pack_bf16(a1.x * e0.z, a1.y * e0.w);
+                pk[4 * cc + 2] = pack_bf16(a2.x * e1.x, a2.y * e1.y);
+                pk[4 * cc + 3] = pack_bf16(a3.x * e1.z, a3.y * e1.w);
+            }
+            eg_row = seg[row];
+            tmem_st32(lane + C_GA, pk);
+            tmem_wait_st();
+            tc_fence_before_sync();
+            wg_sync(kBar);
+        }
+        if (t == 0 && ok) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                if constexpr (kGate)
+                    mma_bf16_ts(tmem + C_GRP, tmem + C_GA + 8u * kk,
+                                sw128_desc(kq + 2048u * kk, kRegKQ, 1024), ID_KB, kk > 0);
+                else
                     mma_bf16_ss(tmem + C_GRP, sw128_desc(tp + 32u * kk, 16, 1024),
                                 sw128_desc(kq + 2048u * kk, kRegKQ, 1024), ID_KB, kk > 0);
-                mma_commit(ctl.bar(B_DW_FULL));
-                ok = ctl.wait(B_DW_FULL, (uint32_t)c);
             }
+            mma_commit(ctl.bar(B_DW_FULL));
+            ok = ctl.wait(B_DW_FULL, (uint32_t)c);
         }
         if (wg_sync_or(kBar, !ok)) return;
         tc_fence_after_sync();
@@ -1426,14 +1569,14 @@ __device__ void group_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                     const float2 a0 = unpack_bf16(qv.x), a1 = unpack_bf16(qv.y),
                                  a2 = unpack_bf16(qv.z), a3 = unpack_bf16(qv.w);
                     float* d = x + 8 * cc;
-                    d[0] = a0.x - d[0];
-                    d[1] = a0.y - d[1];
-                    d[2] = a1.x - d[2];
-                    d[3] = a1.y - d[3];
-                    d[4] = a2.x - d[4];
-                    d[5] = a2.y - d[5];
-                    d[6] = a3.x - d[6];
-                    d[7] = a3.y - d[7];
+                    d[0] = fmaf(eg_row, a0.x, -d[0]);
+                    d[1] = fmaf(eg_row, a0.y, -d[1]);
+                    d[2] = fmaf(eg_row, a1.x, -d[2]);
+                    d[3] = fmaf(eg_row, a1.y, -d[3]);
+                    d[4] = fmaf(eg_row, a2.x, -d[4]);
+                    d[5] = fmaf(eg_row, a2.y, -d[5]);
+                    d[6] = fmaf(eg_row, a3.x, -d[6]);
+                    d[7] = fmaf(eg_row, a3.y, -d[7]);
                 }
             } else {
 #pragma unroll
@@ -1497,13 +1640,15 @@ __device__ void writer_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t
 }
 }  // namespace scan
 
-template <bool kRec, int NMAX>
+// kGate: side holds every chunk's decay vectors (kSideFloats per chunk, in
+// workspace-tile order), written by the gated prepare kernel.
+template <bool kRec, int NMAX, bool kGate = false>
 __global__ void __launch_bounds__(512, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ws,
                   const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
                   float* __restrict__ S_T, float* __restrict__ S_chunks, int T, int H,
-                  const __grid_constant__ SeqTable<NMAX> seqs) {
+                  const __grid_constant__ SeqTable<NMAX> seqs, const float* __restrict__ side) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -1511,10 +1656,13 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     int* const misc = reinterpret_cast<int*>(smem_raw + (base - raw_addr) + scan::OFF_MISC);
     const Ctl ctl{base + scan::OFF_BAR, reinterpret_cast<volatile int*>(misc)};
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
+    float* const sside = reinterpret_cast<float*>(smem_raw + (base - raw_addr) + scan::OFF_SIDE);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x;  // the state's index: (batch, head) or (sequence, head)
     const SeqSpan sp = scan_span(seqs, bh, H, T);
     const int nchunks = (sp.len + kC - 1) / kC;
+    static_assert(!kGate || NMAX == 1, "gating on the batched layout");
+    const float* const cside = kGate ? side + (size_t)bh * nchunks * kSideFloats : nullptr;
 
     if (tid == 0) {
         misc[0] = 0;
@@ -1538,11 +1686,12 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (lane == 0) scan::producer(ctl, sm, &tm_q, &tm_k, &tm_v, &tm_ws, sp, nchunks);
     } else if (warp >= 4 && warp < 8) {
         const int t = tid - 128;
-        scan::state_body<kRec>(ctl, sm, tmem, t, S0, S_T, S_chunks, bh, nchunks);
+        scan::state_body<kRec, kGate>(ctl, sm, tmem, t, S0, S_T, S_chunks, bh, nchunks, cside,
+                                      sside + 64);
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 0);
     } else if (warp >= 8 && warp < 12) {
         const int t = tid - 256;
-        scan::group_body(ctl, sm, tmem, t, nchunks);
+        scan::group_body<kGate>(ctl, sm, tmem, t, nchunks, cside, sside);
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 1);
     } else if (warp >= 12) {
         const int t = tid - 384;
@@ -1635,7 +1784,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
     if (workspace) {
         const long long items = (long long)BH * nchunks;
         if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
-        auto prep_kernel = chunk_prep_kernel<1>;
+        auto prep_kernel = chunk_prep_kernel<1, false>;
         auto scan_kernel = S_chunks ? chunk_scan_kernel<true, 1> : chunk_scan_kernel<false, 1>;
         if ((err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kPrepSmemBytes)) != cudaSuccess ||
@@ -1644,11 +1793,12 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
             return err;
         const SeqTable<1> batched{};
         const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
-        prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(mq, mk, mws, b, T, nchunks,
-                                                                    (int)items, batched);
+        prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
+            mq, mk, mws, b, T, nchunks, (int)items, batched, nullptr, nullptr);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
-        scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(
-            mq, mk, mv, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, S_chunks, T, 1, batched);
+        scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, S0,
+                                                           static_cast<__nv_bfloat16*>(o), S_T,
+                                                           S_chunks, T, 1, batched, nullptr);
         return cudaGetLastError();
     }
     if ((err = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1671,7 +1821,7 @@ cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v, 
     if (!make_map(&mq, q, H, Tmap) || !make_map(&mk, k, H, Tmap) || !make_map(&mv, v, H, Tmap) ||
         !make_ws_map(&mws, workspace, H, nmap))
         return cudaErrorInvalidValue;
-    auto prep_kernel = chunk_prep_kernel<kMaxVarlenSeqs>;
+    auto prep_kernel = chunk_prep_kernel<kMaxVarlenSeqs, false>;
     auto scan_kernel = chunk_scan_kernel<false, kMaxVarlenSeqs>;
     cudaError_t err;
     if ((err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1682,11 +1832,54 @@ cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v, 
     if (items > 0) {
         const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
         prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
-            mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, 0, (int)items, seqs);
+            mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, 0, (int)items, seqs, nullptr,
+            nullptr);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     scan_kernel<<<(unsigned)ctas, 512, scan::kSmemBytes, stream>>>(
-        mq, mk, mv, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, nullptr, T, H, seqs);
+        mq, mk, mv, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, nullptr, T, H, seqs, nullptr);
+    return cudaGetLastError();
+}
+
+size_t chunk_tc_gated_workspace_bytes(int BH, int T) {
+    if (BH <= 0 || T <= 0) return 0;
+    const size_t chunks = (size_t)BH * (size_t)((T + kC - 1) / kC);
+    return chunks * kTile + chunks * kSideFloats * sizeof(float);
+}
+
+cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, const void* beta,
+                                  const float* g, const float* S0, void* o, float* S_T, int BH,
+                                  int T, int dk, int dv, int dt, void* workspace,
+                                  cudaStream_t stream) {
+    if (!chunk_tc_supports(dk, dv, dt)) return cudaErrorNotSupported;
+    if (BH <= 0 || T <= 0) return cudaSuccess;
+    if (!workspace || !o || !g) return cudaErrorInvalidValue;
+    const int nchunks = (T + kC - 1) / kC;
+    const long long items = (long long)BH * nchunks;
+    if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    CUtensorMap mq, mk, mv, mws;
+    if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mv, v, BH, T) ||
+        !make_ws_map(&mws, workspace, BH, nchunks))
+        return cudaErrorInvalidValue;
+    float* const side = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                 (size_t)items * kTile);
+    auto prep_kernel = chunk_prep_kernel<1, true>;
+    auto scan_kernel = chunk_scan_kernel<false, 1, true>;
+    cudaError_t err;
+    if ((err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kPrepSmemBytes)) != cudaSuccess ||
+        (err = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    scan::kSmemBytes)) != cudaSuccess)
+        return err;
+    const SeqTable<1> batched{};
+    const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
+    prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
+        mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, nchunks, (int)items, batched, g,
+        side);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, S0,
+                                                       static_cast<__nv_bfloat16*>(o), S_T, nullptr,
+                                                       T, 1, batched, side);
     return cudaGetLastError();
 }
 

@@ -73,6 +73,14 @@ cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v,
                                    const void* beta, const float* S0, void* o, float* S_T,
                                    const VarlenTable& seqs, int H, int T, void* workspace,
                                    cudaStream_t stream);
+// Gated DeltaNet on tensor cores (two passes; g the fp32 [BH][T] log keep
+// rate): the workspace holds the [PT; Tm] tiles and then kSideFloats fp32
+// decay values per chunk, chunk_tc_gated_workspace_bytes(BH, T) in all.
+size_t chunk_tc_gated_workspace_bytes(int BH, int T);
+cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, const void* beta,
+                                  const float* g, const float* S0, void* o, float* S_T, int BH,
+                                  int T, int dk, int dv, int dt, void* workspace,
+                                  cudaStream_t stream);
 // KDA: g is the fp32 [BH][T][dk] per-key-channel log keep rate.
 cudaError_t launch_chunk_simt_kda(const void* q, const void* k, const void* v, const void* beta,
                                   const float* g, const float* S0, void* o, float* S_T, int BH,

@@ -239,15 +239,35 @@ DN_API size_t dn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv,
  * oublier d'abord l'état entier", fr.news.hada.io/topic?id=31925):
  *     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,  o_t = S_t q_t
  * i.e. forget (alpha S), predict, correct, write, read, in that order.
- *   g       [B, H, T] fp32 log keep rates (g <= 0 keeps the state bounded;
- *           not enforced), 4-byte aligned device memory
- * Every other argument, layout and error as for dn_chunk_fwd (no workspace).
- * The arithmetic is fp32 on CUDA cores for both I/O types.
+ *   g       [B, H, T] fp32 log keep rates, g <= 0 (keep rates alpha in
+ *           (0, 1], as the method defines them); 4-byte aligned device
+ *           memory.  Not checked: the chunk kernels clamp every in-chunk
+ *           decay ratio exp(G_i - G_j) at 1, so a positive g gives results
+ *           the recurrence does not define.
+ *   workspace, workspace_bytes
+ *           NULL: one fp32 CUDA-core kernel (any supported shape and dtype).
+ *           Otherwise device scratch of at least
+ *           dn_chunk_fwd_gated_workspace_bytes(...) bytes, 16-byte aligned,
+ *           owned by the caller and disjoint from every other argument; where
+ *           that size is non-zero (dk = dv = 128, bf16) the call runs in two
+ *           tcgen05 passes like dn_chunk_fwd: per chunk, the decay ratios
+ *           exp(G_i - G_j) (G the in-chunk cumulative log keep rate) enter A
+ *           and P before the solve, and the state is carried as
+ *           S <- exp(G_C) S + K^T diag(exp(G_C - G_s)) U'.  Its contents on
+ *           return are unspecified.  A smaller workspace is DN_ERR_INVALID_ARG.
+ * Every other argument, layout and error as for dn_chunk_fwd.
  */
 DN_API int dn_chunk_fwd_gated(const void *q, const void *k, const void *v,
                        const void *beta, const float *g, const float *S0, void *o,
                        float *S_T, int B, int H, int T, int dk, int dv, int C, int dt,
-                       void *stream);
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* Scratch bytes of the tensor-core form of dn_chunk_fwd_gated: one 16 KB
+ * [PT; Tm] tile and 1 KB of fp32 decay factors per (batch, head, chunk),
+ * B * H * ceil(T / 64) * 17408 bytes; 0 where that form does not apply
+ * (dk or dv != 128, fp32 I/O, C != 64, an empty problem).  Host-only. */
+DN_API size_t dn_chunk_fwd_gated_workspace_bytes(int B, int H, int T, int dk, int dv,
+                                          int C, int dt);
 
 /*
  * dn_recurrent_step_gated -- one Gated DeltaNet decoding step: with
@@ -300,8 +320,8 @@ DN_API size_t dn_chunk_fwd_varlen_workspace_bytes(const int *cu_seqlens, int N, 
  * page's read uses d_k^{-1/2} q_t; as everywhere in this library the caller
  * applies any query scale.
  *   g   [B, H, T, dk] fp32 for the chunkwise form, [B, H, dk] for a step
- * Every other argument, layout and error as for dn_chunk_fwd_gated /
- * dn_recurrent_step_gated.  fp32 arithmetic on CUDA cores.
+ * Every other argument, layout and error as for dn_chunk_fwd_gated (with no
+ * workspace) / dn_recurrent_step_gated.  fp32 arithmetic on CUDA cores.
  */
 DN_API int dn_chunk_fwd_kda(const void *q, const void *k, const void *v,
                      const void *beta, const float *g, const float *S0, void *o,
@@ -314,7 +334,7 @@ DN_API int dn_recurrent_step_kda(const void *q, const void *k, const void *v,
 /* ABI version of this header (bumped on incompatible changes). */
 DN_API int dn_abi_version(void);
 
-#define DN_ABI_VERSION 1
+#define DN_ABI_VERSION 2
 
 #ifdef __cplusplus
 }

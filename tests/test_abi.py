@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dn_abi_version() == 1
+    assert lib.dn_abi_version() == 2
     assert lib.dn_status_string(0) == b"DN_OK"
     assert lib.dn_status_string(1) == b"DN_ERR_INVALID_ARG"
     assert lib.dn_status_string(2) == b"DN_ERR_UNSUPPORTED"
@@ -69,6 +69,26 @@ def test_workspace_bytes(lib):
     assert f(8, 16, 2048, 64, 64, 64, 1) == 0    # d = 64
     assert f(8, 16, 2048, 128, 64, 64, 1) == 0
     assert f(8, 16, 2048, 128, 128, 32, 1) == 0  # other chunk length
+
+
+def test_gated_workspace_bytes(lib):
+    """The gated tensor-core form adds 1 KB of fp32 decay factors per chunk
+    to the 16 KB tile; where that form does not apply it needs none."""
+    f = lib.dn_chunk_fwd_gated_workspace_bytes
+    assert f(8, 16, 2048, 128, 128, 64, 1) == 8 * 16 * 32 * (16384 + 1024)
+    assert f(1, 2, 130, 128, 128, 64, 1) == 2 * 3 * 17408
+    assert f(1, 1, 0, 128, 128, 64, 1) == 0
+    assert f(8, 16, 2048, 128, 128, 64, 0) == 0
+    assert f(8, 16, 2048, 64, 128, 64, 1) == 0
+    assert f(8, 16, 2048, 128, 128, 32, 1) == 0
+
+
+def test_gated_rejects_a_short_workspace_before_any_cuda_call(lib):
+    need = lib.dn_chunk_fwd_gated_workspace_bytes(1, 2, 130, 128, 128, 64, 1)
+    st = lib.dn_chunk_fwd_gated(None, None, None, None, None, None, None, None, 1, 2, 130,
+                                128, 128, 64, 1, ctypes.c_void_p(4096), need - 1, None)
+    assert st == _lib.DN_ERR_INVALID_ARG
+    assert b"workspace" in lib.dn_last_error()
 
 
 def _chunk(lib, B=1, H=1, T=64, dk=64, dv=64, C=64, dt=1, algo=0):

@@ -1,6 +1,8 @@
 """Gated DeltaNet on the GPU (chunkwise forward and decoding step) against
 the fp64 gated oracle, through the C ABI.  Bars as for the plain forms:
 relative L2 <= 1e-4 (fp32 I/O) and <= 1e-2 (bf16 I/O) on o and the state.
+The chunkwise form has two kernels: the fp32 CUDA-core one (workspace=None,
+every shape) and the two-pass tcgen05 one (a workspace, dk = dv = 128 bf16).
 """
 import numpy as np
 import pytest
@@ -37,7 +39,7 @@ def test_gated_chunk_ragged(dk, dv, dtype):
                                  feature_map="silu", s0_std=0.1)
     g = workloads.gate_inputs(B, H, T, seed=dk + dv)
     o, S = dn.chunk_fwd_gated(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g),
-                              initial_state=dev(inp.S0))
+                              initial_state=dev(inp.S0), workspace=None)
     torch.cuda.synchronize()
     o_ref, S_ref = oracle.forward_gated(inp.q, inp.k, inp.v, inp.beta, g, inp.S0)
     _check(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
@@ -66,11 +68,74 @@ def test_gated_strong_decay_and_edge_lengths():
                torch.float32, f"T={T}")
 
 
-def test_gated_layer_1p3b_sampled_heads():
+def _tc_workspace(B, H, T):
+    n = dn.load().dn_chunk_fwd_gated_workspace_bytes(B, H, T, 128, 128, 64, 1)
+    assert n == B * H * ((T + 63) // 64) * 17408
+    return torch.empty(n, dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 1000])
+@pytest.mark.parametrize("lo", [0.9, 0.3], ids=["mild", "strong"])
+def test_gated_tc_chunk_ragged(T, lo):
+    """The tcgen05 form over ragged lengths (one partial chunk to 16
+    chunks), with an initial state, mild and strong decay (alpha down to 0.3:
+    exp G underflows inside a chunk)."""
+    B, H = 2, 3
+    inp = workloads.chunk_inputs(B, H, T, 128, 128, dtype="bf16", seed=T + 7,
+                                 feature_map="silu", s0_std=0.5)
+    g = workloads.gate_inputs(B, H, T, seed=T, lo=lo)
+    o, S = dn.chunk_fwd_gated(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g),
+                              initial_state=dev(inp.S0), workspace=_tc_workspace(B, H, T))
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.forward_gated(inp.q, inp.k, inp.v, inp.beta, g, inp.S0)
+    _check(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
+           torch.bfloat16, f"tcgen05 T={T} lo={lo}")
+
+
+def test_gated_tc_zero_decay_matches_the_plain_tc_kernel():
+    """g = 0: every decay factor of the gated tcgen05 form is exactly 1, so it
+    computes what the plain two-pass kernel computes."""
+    B, H, T = 2, 4, 333
+    inp = workloads.chunk_inputs(B, H, T, 128, 128, dtype="bf16", seed=12, s0_std=0.1)
+    q, k, v, b, S0 = (dev(x) for x in (inp.q, inp.k, inp.v, inp.beta, inp.S0))
+    o1, S1 = dn.chunk_fwd(q, k, v, b, initial_state=S0, algo="tcgen05")
+    o2, S2 = dn.chunk_fwd_gated(q, k, v, b, torch.zeros(B, H, T, device="cuda"),
+                                initial_state=S0, workspace=_tc_workspace(B, H, T))
+    torch.cuda.synchronize()
+    assert rel_l2(o2.double().cpu().numpy(), o1.double().cpu().numpy()) <= 1e-6
+    assert rel_l2(S2.double().cpu().numpy(), S1.double().cpu().numpy()) <= 1e-6
+
+
+def test_gated_tc_matches_the_cuda_core_kernel():
+    """Both kernels of the gated form on one bf16 problem agree to the bf16 bar."""
+    B, H, T = 2, 4, 777
+    inp = workloads.chunk_inputs(B, H, T, 128, 128, dtype="bf16", seed=21, s0_std=0.2)
+    g = workloads.gate_inputs(B, H, T, seed=21, lo=0.7)
+    args = [dev(x) for x in (inp.q, inp.k, inp.v, inp.beta, g)]
+    o1, S1 = dn.chunk_fwd_gated(*args, initial_state=dev(inp.S0), workspace=None)
+    o2, S2 = dn.chunk_fwd_gated(*args, initial_state=dev(inp.S0), workspace="auto")
+    torch.cuda.synchronize()
+    _check(o2.double().cpu().numpy(), S2.double().cpu().numpy(), o1.double().cpu().numpy(),
+           S1.double().cpu().numpy(), torch.bfloat16, "tcgen05 vs CUDA cores")
+
+
+def test_gated_tc_workspace_too_small_is_rejected():
+    B, H, T = 1, 2, 100
+    inp = workloads.chunk_inputs(B, H, T, 128, 128, dtype="bf16", seed=1)
+    g = workloads.gate_inputs(B, H, T, seed=1)
+    ws = _tc_workspace(B, H, T)[:-16]
+    with pytest.raises(RuntimeError, match="workspace"):
+        dn.chunk_fwd_gated(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g),
+                           workspace=ws)
+
+
+@pytest.mark.parametrize("workspace", ["auto", None], ids=["tcgen05", "cuda-cores"])
+def test_gated_layer_1p3b_sampled_heads(workspace):
     inp = workloads.workload_inputs("layer1p3b_bf16")
     B, H, T, d = inp.q.shape
     g = workloads.gate_inputs(B, H, T, seed=7)
-    o, S = dn.chunk_fwd_gated(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g))
+    o, S = dn.chunk_fwd_gated(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g),
+                              workspace=workspace)
     torch.cuda.synchronize()
     bi, hi = sample_heads(B, H, 4, seed=8)
     o_ref, S_ref = oracle.forward_gated(*(take_heads(x, bi, hi) for x in

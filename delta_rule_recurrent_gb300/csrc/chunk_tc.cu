@@ -976,7 +976,9 @@ __device__ __forceinline__ SeqSpan scan_span(const SeqTable<NMAX>& seqs, int bh,
 // oublier d'abord l'état entier", fr.news.hada.io/topic?id=31925): with G_t
 // the cumulative log decay from the chunk start, A and P carry the ratios
 // exp(G_i - G_j) <= 1, and the item also writes the chunk's decay vectors
-// for the scan (exp G_t, exp(G_C - G_t) and exp G_C; kSideFloats per chunk).
+// for the scan (exp G_t, exp(G_C - G_t) and exp G_C; kSideFloats per chunk)
+// and the decay-scaled tile [PT; Tm] diag(exp G) (tile2, row-major bf16, one
+// per item), the A operand of the scan's key term.
 constexpr int kPrepThreads = 128;
 constexpr int kSideFloats = 256;
 constexpr int kPrepCtasPerSm = 4;
@@ -985,18 +987,70 @@ constexpr uint32_t P_OFF_X = P_OFF_KQ + kStageKQ;  // fp32 A, overwritten by X; 
 constexpr uint32_t P_OFF_Y = P_OFF_X + kXBytes;    // solve scratch
 constexpr uint32_t P_OFF_BETA = P_OFF_Y + kYBytes; // 64 fp32
 constexpr uint32_t P_OFF_G = P_OFF_BETA + 256;     // 64 fp32 cumulative log decay + 2 partials
-constexpr uint32_t P_OFF_BAR = P_OFF_G + 272;      // mbarriers: tiles landed, MMA done, drain
+constexpr uint32_t P_OFF_E = P_OFF_G + 272;        // exp G_t, then exp(-G_t) (64 fp32 each)
+constexpr uint32_t P_OFF_BAR = P_OFF_E + 512;      // mbarriers: tiles landed, MMA done, drain
 constexpr uint32_t P_OFF_MISC = P_OFF_BAR + 24;    // abort flag, TMEM address
 constexpr uint32_t kPrepSmemBytes = P_OFF_MISC + 16 + 1024;
 static_assert(kPrepCtasPerSm * (kPrepSmemBytes + 1024) <= 233472, "prepare kernel occupancy");
 static_assert(P_OFF_X % 1024 == 0 && kXBytes >= kTile, "[PT; Tm] over the solve array");
+
+// Row i of A or P times the decay ratios exp(G_i - G_j) (entries past the
+// diagonal are masked afterwards).  While the chunk's total decay stays
+// within exp(-80) (separable(), uniform over the block: G is non-increasing,
+// so G_63 is the chunk's lowest) the ratio is the product exp(G_i) exp(-G_j)
+// of two normal fp32 numbers, one multiply per entry on the row in
+// registers.  Beyond that, decay_row_tmem applies one exponential per entry,
+// clamped at 1 so the masked entries stay finite, to the row in TMEM 32
+// columns at a time before it is read out.
+__device__ __forceinline__ bool separable(const float* Gs) { return Gs[63] >= -80.f; }
+__device__ __forceinline__ void decay_row(float (&x)[64], const float* Es, int i) {
+    const float ei = Es[i];
+    const float4* const einv = reinterpret_cast<const float4*>(Es + 64);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const float4 e = einv[j];
+        x[4 * j] *= ei * e.x;
+        x[4 * j + 1] *= ei * e.y;
+        x[4 * j + 2] *= ei * e.z;
+        x[4 * j + 3] *= ei * e.w;
+    }
+}
+__device__ __forceinline__ void decay_row_tmem(uint32_t taddr, const float* Gs, int i) {
+    const float gi = Gs[i];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r[32];
+        tmem_ld32(taddr + 32u * h, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            r[e] = __float_as_uint(__uint_as_float(r[e]) * __expf(fminf(gi - Gs[32 * h + e], 0.f)));
+        tmem_st32(taddr + 32u * h, r);
+    }
+    tmem_wait_st();
+}
+
+// Row of the decay-scaled tile in global memory: x[e] exp(G_e), as bf16.
+__device__ __forceinline__ void store_row64_scaled(__nv_bfloat16* dst, const float (&x)[64],
+                                                   const float* Es) {
+    uint4* const d = reinterpret_cast<uint4*>(dst);
+    const float4* const e4 = reinterpret_cast<const float4*>(Es);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const float4 e0 = e4[2 * c], e1 = e4[2 * c + 1];
+        const float* const xs = x + 8 * c;
+        d[c] = make_uint4(pack_bf16(xs[0] * e0.x, xs[1] * e0.y), pack_bf16(xs[2] * e0.z, xs[3] * e0.w),
+                          pack_bf16(xs[4] * e1.x, xs[5] * e1.y), pack_bf16(xs[6] * e1.z, xs[7] * e1.w));
+    }
+}
 
 template <int NMAX, bool kGate>
 __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_ws, const __nv_bfloat16* __restrict__ beta,
                   int T, int nchunks, int items, const __grid_constant__ SeqTable<NMAX> seqs,
-                  const float* __restrict__ gate, float* __restrict__ side) {
+                  const float* __restrict__ gate, float* __restrict__ side,
+                  __nv_bfloat16* __restrict__ tile2) {
     static_assert(!kGate || NMAX == 1, "gating on the batched layout");
     constexpr int kBar = 1, B_TILES = 0, B_MMA = 1, B_END = 2;
     extern __shared__ uint8_t smem_raw[];
@@ -1007,6 +1061,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     float* const Ys = reinterpret_cast<float*>(gbase + P_OFF_Y);
     float* const betas = reinterpret_cast<float*>(gbase + P_OFF_BETA);
     float* const Gs = reinterpret_cast<float*>(gbase + P_OFF_G);  // [64] then 2 warp partials
+    float* const Es = reinterpret_cast<float*>(gbase + P_OFF_E);  // exp G_t [64], exp(-G_t) [64]
     int* const misc = reinterpret_cast<int*>(gbase + P_OFF_MISC);
     const Ctl ctl{base + P_OFF_BAR, reinterpret_cast<volatile int*>(misc)};
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
@@ -1078,7 +1133,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
                 if ((t & 31) == 31) Gs[64 + (t >> 5)] = x;
                 wg_sync(2, 64);
-                Gs[t] = t >= 32 ? x + Gs[64] : x;
+                const float G = t >= 32 ? x + Gs[64] : x;
+                Gs[t] = G;
+                Es[t] = __expf(G);
+                Es[64 + t] = __expf(-G);
             }
         }
         // G = [K; Q] K^T
@@ -1112,14 +1170,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tc_fence_after_sync();
         // A (TMEM rows 0-63) into the solve array; P (rows 64-127) stays in TMEM.
         if (t < 64) {
+            bool sep = true;
+            if constexpr (kGate) {
+                sep = separable(Gs);
+                if (!sep) decay_row_tmem(tmem + lane_base, Gs, row);
+            }
             float x[64];
             tmem_ld64f(tmem + lane_base, x);
             const float bi = betas[row];
-            if constexpr (kGate) {  // decay ratios exp(G_i - G_j), j < i
-                const float gi = Gs[row];
-#pragma unroll
-                for (int j = 0; j < 64; ++j) x[j] *= __expf(fminf(gi - Gs[j], 0.f));
-            }
+            if (kGate && sep) decay_row(x, Es, row);  // exp(G_i - G_j), j < i
 #pragma unroll
             for (int j = 0; j < 64; j += 4)
                 sts4(X + row * kP + j,
@@ -1143,16 +1202,19 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     x[e + 3] = xv.w * bv.w;
                 }
             } else {
-                tmem_ld64f(tmem + lane_base, x);
-                if constexpr (kGate) {  // decay ratios exp(G_i - G_j), j <= i
-                    const float gi = Gs[row];
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) x[j] *= __expf(fminf(gi - Gs[j], 0.f));
+                bool sep = true;
+                if constexpr (kGate) {
+                    sep = separable(Gs);
+                    if (!sep) decay_row_tmem(tmem + lane_base, Gs, row);
                 }
+                tmem_ld64f(tmem + lane_base, x);
+                if (kGate && sep) decay_row(x, Es, row);  // exp(G_i - G_j), j <= i
 #pragma unroll
                 for (int j = 0; j < 64; ++j)
                     if (j > row) x[j] = 0.f;
             }
+            if (kGate && t < 64)  // Tm diag(exp G), row t
+                store_row64_scaled(tile2 + ((size_t)w * 128 + 64 + t) * 64, x, Es);
             tc_fence_before_sync();
             wg_sync(kBar);
             store_row64_bf16(tp, t < 64 ? 64 + t : row, x);
@@ -1177,6 +1239,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             float x[64];
             tmem_ld64f(tmem + lane_base, x);
             store_row64_bf16(tp, t, x);
+            if constexpr (kGate)  // PT diag(exp G), row t
+                store_row64_scaled(tile2 + ((size_t)w * 128 + t) * 64, x, Es);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
@@ -1189,7 +1253,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if constexpr (kGate) {  // the chunk's decay vectors for the scan
             if (t < kC) {
                 float* const sd = side + (size_t)w * kSideFloats;  // w = bh * nchunks + c
-                sd[t] = __expf(Gs[t]);                   // exp G_t
+                sd[t] = Es[t];                           // exp G_t
                 sd[64 + t] = __expf(Gs[63] - Gs[t]);     // exp(G_C - G_t)
                 if (t == 0) sd[128] = __expf(Gs[63]);    // exp G_C
             }
@@ -1215,14 +1279,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 // and never pass through shared memory:
 //     D1^T = V^T [PT; Tm]^T + S^T [Q'; -W]^T     (lanes: dv; columns: o, U' rows)
 //     S^T += U'^T K
-// where S^T[j][i] = S[i][j] with S the [dk][dv] state.  [Q'; -W] is the B
-// operand, built in shared memory by the chunk group.
+// where S^T[j][i] = S[i][j] with S the [dk][dv] state.  The chunk group
+// leaves [-Q'; W] in shared memory and the D1 MMAs take it as a negated B
+// operand.
 //   warp 0      TMA producer: [K; Q] ring (3), v (2), [PT; Tm] from the workspace (2)
 //   warp 1      TMEM owner
 //   warps 4-7   state: thread t owns dv column t (TMEM lane t); thread 0 issues
 //               D1^T += S^T [Q'; -W]^T and S^T += U'^T K
-//   warps 8-11  chunk group: DW = [PT; Tm] K, then the chunk's [Q'; -W] tile
-//               from DW and the q rows
+//   warps 8-11  chunk group: [-Q'; W] = [[PT, -I]; [Tm, 0]] [K; Q] on the
+//               tensor core, converted to the bf16 tile
 //   warps 12-15 o writer: reads the o rows of D1^T, stores them (coalesced
 //               global stores), and starts the next chunk's D1^T = V^T [PT; Tm]^T
 namespace scan {
@@ -1230,7 +1295,7 @@ constexpr int kStages = 3, kVBufs = 2, kKQ = 6;       // [K; Q] barriers: one pe
 constexpr uint32_t OFF_KQ = 0;                         // kStages x [K; Q]
 constexpr uint32_t OFF_V = OFF_KQ + kStages * kStageKQ;   // kVBufs x v (2 dv-half regions)
 constexpr uint32_t OFF_TP = OFF_V + kVBufs * kTile;    // 2 x [PT; Tm]
-constexpr uint32_t OFF_QW = OFF_TP + 2 * kTile;        // 2 x [Q'; -W] (2 dk-half regions of 128 rows)
+constexpr uint32_t OFF_QW = OFF_TP + 2 * kTile;        // 2 x [-Q'; W] (2 dk-half regions of 128 rows)
 constexpr uint32_t OFF_BAR = OFF_QW + 4 * kTile;
 enum : int {
     B_KQ_FULL = 0,    // [6] q, k tiles landed                 (producer -> chunk group)
@@ -1250,15 +1315,19 @@ enum : int {
 };
 constexpr int kBars = 28;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * kBars;     // abort flag, TMEM address
-constexpr uint32_t OFF_SIDE = OFF_MISC + 16;           // gated: exp G (chunk group), dec (state)
-constexpr uint32_t kSmemBytes = OFF_SIDE + 512 + 1024;
+// Gated: 2 x the chunk's decay vectors (exp G_t [64], exp(G_C - G_t) [64],
+// exp G_C, padding), loaded with [PT; Tm]; then the state's copy of dec.
+constexpr uint32_t kSideCopyBytes = 528;
+constexpr uint32_t OFF_SIDE = OFF_MISC + 16;
+constexpr uint32_t OFF_DEC = OFF_SIDE + 2 * kSideCopyBytes;
+constexpr uint32_t kSmemBytes = OFF_DEC + 256 + 1024;
 static_assert(kSmemBytes <= 232448, "scan kernel shared memory");
 // TMEM columns: S^T fp32 | D1^T fp32 (o rows 0-63, U' rows 64-127) | S^T bf16 |
 // U'^T bf16 | the chunk group's 128 DW accumulator columns.
 constexpr uint32_t C_ST = 0, C_D1 = 128, C_SB = 256, C_UB = 320, C_GRP = 352;
-constexpr uint32_t C_GA = 480;  // gated: [PT; Tm] diag(exp G) as the group's A operand
+constexpr uint32_t C_GA = 480;  // [-diag(exp G); 0]: the Q block of the chunk group's A operand
 constexpr uint32_t ID_VP = idesc_bf16_f32(128, 128, 1, 0);  // A v^T (MN-major), B [PT;Tm] (K-major)
-constexpr uint32_t ID_SP = idesc_bf16_f32(128, 128, 0, 0);  // A S^T (TMEM), B [Q';-W] (K-major)
+constexpr uint32_t ID_SP = idesc_bf16_f32(128, 128, 0, 0) | (1u << 14);  // A S^T (TMEM), B -[-Q'; W] (K-major, negated)
 constexpr uint32_t ID_KB = idesc_bf16_f32(128, 128, 0, 1);  // A U'^T (TMEM) or [PT;Tm], B K (MN-major)
 
 struct Smem {
@@ -1267,11 +1336,16 @@ struct Smem {
     __device__ uint32_t v(int c) const { return base + OFF_V + (uint32_t)(c % kVBufs) * kTile; }
     __device__ uint32_t tp(int g) const { return base + OFF_TP + (uint32_t)g * kTile; }
     __device__ uint32_t qw(int g) const { return base + OFF_QW + (uint32_t)g * 2u * kTile; }
+    __device__ uint32_t side(int g) const { return base + OFF_SIDE + (uint32_t)g * kSideCopyBytes; }
 };
 
+// Gated (tm_ws2, side): the decay-scaled tile goes to the [Q'; -W] buffer
+// of the same set (free until the chunk group's epilogue overwrites it) and
+// the decay vectors to the set's side slot, all on the [PT; Tm] barrier.
 __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q,
                          const CUtensorMap* tm_k, const CUtensorMap* tm_v, const CUtensorMap* tm_ws,
-                         const SeqSpan& sp, int nchunks) {
+                         const SeqSpan& sp, int nchunks, const CUtensorMap* tm_ws2,
+                         const float* side) {
     const int z = sp.z, r0 = sp.row0, w0 = sp.wsbase;
     int nkq = 0, nv = 0, ntp = 0;
     long long t0 = clock64();
@@ -1314,8 +1388,12 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
             const int g = ntp & 1, it = ntp >> 1;
             if (it == 0 || mbar_test_wait(ctl.bar(B_FREE + g), (uint32_t)(it - 1) & 1u)) {
                 const uint32_t bar = ctl.bar(B_TP_FULL + g);
-                mbar_arrive_expect_tx(bar, kTile);
+                mbar_arrive_expect_tx(bar, kTile + (side ? kTile + kSideCopyBytes : 0u));
                 tma_load_3d(sm.tp(g), tm_ws, bar, 0, (w0 + ntp) * 128, z);
+                if (side) {
+                    tma_load_3d(sm.qw(g), tm_ws2, bar, 0, (w0 + ntp) * 128, z);
+                    bulk_load(sm.side(g), side + (size_t)ntp * kSideFloats, kSideCopyBytes, bar);
+                }
                 if (ntp + 2 < nchunks) tma_prefetch_l2_3d(tm_ws, 0, (w0 + ntp + 2) * 128, z);
                 ++ntp;
                 progressed = true;
@@ -1357,16 +1435,12 @@ __device__ __forceinline__ void tmem_pack64(uint32_t src, uint32_t dst, float* r
     tmem_st32(dst, p);
 }
 
-// Gated forms of the two packs.  S^T: packed, then scaled in place by the
-// chunk's keep factor exp G_C.  U'^T: token column e scaled by dec[e] =
-// exp(G_C - G_e) (shared memory) as it is packed.
-__device__ __forceinline__ void tmem_pack64_keep(uint32_t src, uint32_t dst, float keep) {
+// Gated: S^T scaled in place by the chunk's keep factor exp G_C (64 fp32
+// columns), and U'^T packed with token column e scaled by dec[e] =
+// exp(G_C - G_e) (shared memory).
+__device__ __forceinline__ void tmem_scale64(uint32_t src, float keep) {
     float x[64];
     tmem_ld64f(src, x);
-    uint32_t p[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) p[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
-    tmem_st32(dst, p);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         uint32_t r[32];
@@ -1392,13 +1466,16 @@ __device__ __forceinline__ void tmem_pack64_cols(uint32_t src, uint32_t dst,
 
 // kRec: also record S at every chunk start (the backward's recompute); the
 // forward proper is compiled without it, so its state chain carries no test.
-// kGate: S <- exp(G_C) S + K^T diag(exp(G_C - G_s)) U' per chunk, with the
-// decay vectors read from side (global) and staged in sdec (shared memory).
+// kGate: S <- exp(G_C) S + K^T diag(exp(G_C - G_s)) U' per chunk.  The decay
+// vectors arrive with [PT; Tm] (sside, one slot per buffer set); once the
+// chunk group has released [Q'; -W] they are read, dec into sdec for the U'
+// pack, before the D1 MMAs free the slot, and the keep scaling of S^T runs
+// while those MMAs (which read the bf16 copy) are in flight.
 template <bool kRec, bool kGate>
 __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                            const float* __restrict__ S0, float* __restrict__ S_T,
                            float* __restrict__ S_chunks, int bh, int nchunks,
-                           const float* __restrict__ side, float* sdec) {
+                           const float* sside, float* sdec) {
     constexpr int kBar = 1;
     const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
     // S0^T into TMEM: lane t holds dv column t of S0 (zeros without S0).
@@ -1412,24 +1489,13 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
     }
     tmem_wait_st();
 
+    static_assert(!(kGate && kRec), "no state recording on the gated form");
     for (int c = 0; c < nchunks; ++c) {
         const int g = c & 1;
-        float keep = 1.f;
-        float4 dec4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if constexpr (kGate) {  // issued before the wait; sdec is free (last read before a barrier)
-            const float* const sd = side + (size_t)c * kSideFloats;
-            keep = __ldg(sd + 128);
-            if (t < 16) dec4 = __ldg(reinterpret_cast<const float4*>(sd + 64) + t);
-        }
         if (c > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(c - 1), t, kBar)) return;
         tc_fence_after_sync();
         // S^T -> bf16 (dk 0-63, then 64-127); S itself recorded when asked
-        if constexpr (kGate) {
-            static_assert(!kRec, "no state recording on the gated form");
-            if (t < 16) reinterpret_cast<float4*>(sdec)[t] = dec4;
-            tmem_pack64_keep(lane + C_ST, lane + C_SB, keep);
-            tmem_pack64_keep(lane + C_ST + 64u, lane + C_SB + 32u, keep);
-        } else if constexpr (kRec) {
+        if constexpr (kRec) {
             float* const rec = S_chunks + ((size_t)bh * nchunks + c) * kD * kD + t;
             tmem_pack64(lane + C_ST, lane + C_SB, rec);
             tmem_pack64(lane + C_ST + 64u, lane + C_SB + 32u, rec + 64 * kD);
@@ -1441,9 +1507,21 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         tc_fence_before_sync();
         wg_sync(kBar);
         bool ok = true;
-        if (t == 0) {
-            // the o writer started D1^T with its v part once D1^T was free
+        if (t == 0)  // the o writer started D1^T with its v part once D1^T was free
             ok = ctl.wait(B_QW_READY + g, (uint32_t)(c >> 1)) && ctl.wait(B_VP_DONE, (uint32_t)c);
+        float keep = 1.f;
+        if constexpr (kGate) {
+            // [Q'; -W] written, so this chunk's decay vectors are in: the
+            // wait on their barrier returns at once (its next phase needs
+            // the D1 MMAs below) and orders their bytes before the reads.
+            if (t == 0 && ok) ok = ctl.wait(B_TP_FULL + g, (uint32_t)(c >> 1));
+            if (wg_sync_or(kBar, !ok)) return;
+            const float* const slot = sside + g * (kSideCopyBytes / 4);
+            keep = slot[128];
+            if (t < 16) reinterpret_cast<float4*>(sdec)[t] = reinterpret_cast<const float4*>(slot + 64)[t];
+            wg_sync(kBar);  // the slot is read before the D1 MMAs release it
+        }
+        if (t == 0) {
             if (ok) {
                 tc_fence_after_sync();
                 const uint32_t qw = sm.qw(g);
@@ -1454,9 +1532,16 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                                 ID_SP, 1);
                 mma_commit(ctl.bar(B_D1_FULL));
                 mma_commit(ctl.bar(B_FREE + g));
-                ok = ctl.wait(B_D1_FULL, (uint32_t)c);
-                if (ok) mbar_arrive(ctl.bar(B_O_READY));
             }
+        }
+        if constexpr (kGate) {  // S^T <- keep S^T while the D1 MMAs read the bf16 copy
+            __syncwarp();
+            tmem_scale64(lane + C_ST, keep);
+            tmem_scale64(lane + C_ST + 64u, keep);
+        }
+        if (t == 0 && ok) {
+            ok = ctl.wait(B_D1_FULL, (uint32_t)c);
+            if (ok) mbar_arrive(ctl.bar(B_O_READY));
         }
         if (wg_sync_or(kBar, !ok)) return;
         tc_fence_after_sync();
@@ -1492,96 +1577,68 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
     }
 }
 
-// Chunk group: [Q'; -W] of every chunk as the B operand tile of the state MMA
-// (2 dk-half regions of 128 rows x 64 bf16): DW = [PT; Tm] K into its 128
-// accumulator columns, then row t of [Q - PT K; -W] from DW and the chunk's q
-// rows.  Thread t owns TMEM lane t; thread 0 issues.
-// Gated (kGate): the key term uses K scaled by exp G per token, i.e.
-// DW = [PT; Tm] diag(exp G) K: row t of [PT; Tm] is scaled by exp G column
-// by column into TMEM (C_GA) and the MMA reads it from there; Q' = exp(G_t) q_t
-// - (PT diag(exp G) K)_t.  side holds the chunk's decay vectors.
+// Chunk group: [-Q'; W] = A [K; Q] in one chain of MMAs over the chunk's
+// 128 rows of k and q, with A = [[PT, -I]; [Tm, 0]], or for Gated DeltaNet
+// A = [[PT diag(exp G), -diag(exp G)]; [Tm diag(exp G), 0]] (Q' = diag(exp G) Q
+// - PT diag(exp G) K and W = Tm diag(exp G) K).  The left block is the [PT; Tm]
+// tile (gated: the decay-scaled tile, loaded into this set's [Q'; -W]
+// buffer), the right block sits in TMEM (C_GA): row t < 64 holds -exp G_t at
+// token t.  The epilogue only converts: the D1 MMAs negate this operand.
+__device__ __forceinline__ void put_diag(uint32_t taddr, int t, float v) {
+    uint32_t r[32];
+    const uint32_t pv = (t & 1) ? pack_bf16(0.f, v) : pack_bf16(v, 0.f);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) r[e] = (t < 64 && e == (t >> 1)) ? pv : 0u;
+    tmem_st32(taddr, r);
+}
+
 template <bool kGate>
 __device__ void group_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int nchunks,
-                           const float* __restrict__ side, float* seg) {
+                           const float* sside) {
     constexpr int kBar = 2;
-    const int row = t & 63;
     const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
+    put_diag(lane + C_GA, t, -1.f);  // gated: rows t < 64 are rewritten per chunk
+    tmem_wait_st();
+    tc_fence_before_sync();
+    wg_sync(kBar);
     for (int c = 0; c < nchunks; ++c) {
         const int g = c & 1;
         const uint32_t kq = sm.kq(c), tp = sm.tp(g), qw = sm.qw(g);
         bool ok = true;
-        float4 eg_in = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (kGate && t < 16)  // issued before the waits; seg was last read before a barrier
-            eg_in = __ldg(reinterpret_cast<const float4*>(side + (size_t)c * kSideFloats) + t);
         // [PT; Tm] is loaded only after the state released this buffer set,
         // so the [Q'; -W] tile is free as well.
         if (t == 0)
             ok = ctl.wait(B_KQ_FULL + c % kKQ, (uint32_t)(c / kKQ)) &&
                  ctl.wait(B_TP_FULL + g, (uint32_t)(c >> 1));
-        float eg_row = 1.f;
-        if constexpr (kGate) {  // row t of [PT; Tm] diag(exp G) into TMEM
-            if (t < 16) reinterpret_cast<float4*>(seg)[t] = eg_in;
+        if constexpr (kGate) {  // -exp G_t into row t of the TMEM block (the last MMAs are done)
             if (wg_sync_or(kBar, !ok)) return;
-            const float4* const eg4 = reinterpret_cast<const float4*>(seg);
-            uint32_t pk[32];
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                const uint4 tv = ld_shared_v4(tp + sw128(t, cc));
-                const float4 e0 = eg4[2 * cc], e1 = eg4[2 * cc + 1];
-                const float2 a0 = unpack_bf16(tv.x), a1 = unpack_bf16(tv.y),
-                             a2 = unpack_bf16(tv.z), a3 = unpack_bf16(tv.w);
-                pk[4 * cc + 0] = pack_bf16(a0.x * e0.x, a0.y * e0.y);
-                pk[4 * cc + 1] = pack_bf16(a1.x * e0.z, a1.y * e0.w);
-                pk[4 * cc + 2] = pack_bf16(a2.x * e1.x, a2.y * e1.y);
-                pk[4 * cc + 3] = pack_bf16(a3.x * e1.z, a3.y * e1.w);
+            if (t < 64) {
+                put_diag(lane + C_GA, t, -sside[g * (kSideCopyBytes / 4) + t]);
+                tmem_wait_st();
             }
-            eg_row = seg[row];
-            tmem_st32(lane + C_GA, pk);
-            tmem_wait_st();
             tc_fence_before_sync();
             wg_sync(kBar);
         }
         if (t == 0 && ok) {
             tc_fence_after_sync();
+            const uint32_t a = kGate ? qw : tp;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                if constexpr (kGate)
-                    mma_bf16_ts(tmem + C_GRP, tmem + C_GA + 8u * kk,
-                                sw128_desc(kq + 2048u * kk, kRegKQ, 1024), ID_KB, kk > 0);
-                else
-                    mma_bf16_ss(tmem + C_GRP, sw128_desc(tp + 32u * kk, 16, 1024),
-                                sw128_desc(kq + 2048u * kk, kRegKQ, 1024), ID_KB, kk > 0);
-            }
+            for (int kk = 0; kk < 4; ++kk)  // [PT; Tm] K over the chunk's tokens
+                mma_bf16_ss(tmem + C_GRP, sw128_desc(a + 32u * kk, 16, 1024),
+                            sw128_desc(kq + 2048u * kk, kRegKQ, 1024), ID_KB, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // - diag Q
+                mma_bf16_ts(tmem + C_GRP, tmem + C_GA + 8u * kk,
+                            sw128_desc(kq + 8192u + 2048u * kk, kRegKQ, 1024), ID_KB, 1);
             mma_commit(ctl.bar(B_DW_FULL));
             ok = ctl.wait(B_DW_FULL, (uint32_t)c);
         }
         if (wg_sync_or(kBar, !ok)) return;
         tc_fence_after_sync();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {  // row t of [Q'; -W], dk half h
+        for (int h = 0; h < 2; ++h) {  // row t of [-Q'; W], dk half h
             float x[64];
             tmem_ld64f(lane + C_GRP + 64u * h, x);
-            if (t < 64) {
-                const uint32_t region = kq + (uint32_t)h * kRegKQ;
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint4 qv = ld_shared_v4(region + sw128(64 + row, cc));
-                    const float2 a0 = unpack_bf16(qv.x), a1 = unpack_bf16(qv.y),
-                                 a2 = unpack_bf16(qv.z), a3 = unpack_bf16(qv.w);
-                    float* d = x + 8 * cc;
-                    d[0] = fmaf(eg_row, a0.x, -d[0]);
-                    d[1] = fmaf(eg_row, a0.y, -d[1]);
-                    d[2] = fmaf(eg_row, a1.x, -d[2]);
-                    d[3] = fmaf(eg_row, a1.y, -d[3]);
-                    d[4] = fmaf(eg_row, a2.x, -d[4]);
-                    d[5] = fmaf(eg_row, a2.y, -d[5]);
-                    d[6] = fmaf(eg_row, a3.x, -d[6]);
-                    d[7] = fmaf(eg_row, a3.y, -d[7]);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 64; ++e) x[e] = -x[e];
-            }
             store_row64_bf16(qw + (uint32_t)h * kTile, t, x);
         }
         fence_proxy_async_smem();
@@ -1646,6 +1703,7 @@ template <bool kRec, int NMAX, bool kGate = false>
 __global__ void __launch_bounds__(512, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ws,
+                  const __grid_constant__ CUtensorMap tm_ws2,
                   const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
                   float* __restrict__ S_T, float* __restrict__ S_chunks, int T, int H,
                   const __grid_constant__ SeqTable<NMAX> seqs, const float* __restrict__ side) {
@@ -1657,6 +1715,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const Ctl ctl{base + scan::OFF_BAR, reinterpret_cast<volatile int*>(misc)};
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
     float* const sside = reinterpret_cast<float*>(smem_raw + (base - raw_addr) + scan::OFF_SIDE);
+    float* const sdec = reinterpret_cast<float*>(smem_raw + (base - raw_addr) + scan::OFF_DEC);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x;  // the state's index: (batch, head) or (sequence, head)
     const SeqSpan sp = scan_span(seqs, bh, H, T);
@@ -1672,6 +1731,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_ws);
+        if (kGate) prefetch_tensormap(&tm_ws2);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_holder), 512);
@@ -1683,15 +1743,17 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t tmem = *tmem_holder;
 
     if (warp == 0) {
-        if (lane == 0) scan::producer(ctl, sm, &tm_q, &tm_k, &tm_v, &tm_ws, sp, nchunks);
+        if (lane == 0)
+            scan::producer(ctl, sm, &tm_q, &tm_k, &tm_v, &tm_ws, sp, nchunks,
+                           kGate ? &tm_ws2 : nullptr, cside);
     } else if (warp >= 4 && warp < 8) {
         const int t = tid - 128;
-        scan::state_body<kRec, kGate>(ctl, sm, tmem, t, S0, S_T, S_chunks, bh, nchunks, cside,
-                                      sside + 64);
+        scan::state_body<kRec, kGate>(ctl, sm, tmem, t, S0, S_T, S_chunks, bh, nchunks, sside,
+                                      sdec);
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 0);
     } else if (warp >= 8 && warp < 12) {
         const int t = tid - 256;
-        scan::group_body<kGate>(ctl, sm, tmem, t, nchunks, cside, sside);
+        scan::group_body<kGate>(ctl, sm, tmem, t, nchunks, sside);
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 1);
     } else if (warp >= 12) {
         const int t = tid - 384;
@@ -1794,9 +1856,9 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
         const SeqTable<1> batched{};
         const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
         prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
-            mq, mk, mws, b, T, nchunks, (int)items, batched, nullptr, nullptr);
+            mq, mk, mws, b, T, nchunks, (int)items, batched, nullptr, nullptr, nullptr);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
-        scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, S0,
+        scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mws, S0,
                                                            static_cast<__nv_bfloat16*>(o), S_T,
                                                            S_chunks, T, 1, batched, nullptr);
         return cudaGetLastError();
@@ -1833,18 +1895,18 @@ cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v, 
         const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
         prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
             mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, 0, (int)items, seqs, nullptr,
-            nullptr);
+            nullptr, nullptr);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     scan_kernel<<<(unsigned)ctas, 512, scan::kSmemBytes, stream>>>(
-        mq, mk, mv, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, nullptr, T, H, seqs, nullptr);
+        mq, mk, mv, mws, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, nullptr, T, H, seqs, nullptr);
     return cudaGetLastError();
 }
 
 size_t chunk_tc_gated_workspace_bytes(int BH, int T) {
     if (BH <= 0 || T <= 0) return 0;
     const size_t chunks = (size_t)BH * (size_t)((T + kC - 1) / kC);
-    return chunks * kTile + chunks * kSideFloats * sizeof(float);
+    return chunks * (2 * kTile + kSideFloats * sizeof(float));
 }
 
 cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, const void* beta,
@@ -1857,12 +1919,14 @@ cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, c
     const int nchunks = (T + kC - 1) / kC;
     const long long items = (long long)BH * nchunks;
     if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
-    CUtensorMap mq, mk, mv, mws;
+    // workspace: [PT; Tm] tiles | decay-scaled tiles | decay vectors
+    uint8_t* const ws = static_cast<uint8_t*>(workspace);
+    __nv_bfloat16* const tile2 = reinterpret_cast<__nv_bfloat16*>(ws + (size_t)items * kTile);
+    float* const side = reinterpret_cast<float*>(ws + 2 * (size_t)items * kTile);
+    CUtensorMap mq, mk, mv, mws, mws2;
     if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mv, v, BH, T) ||
-        !make_ws_map(&mws, workspace, BH, nchunks))
+        !make_ws_map(&mws, workspace, BH, nchunks) || !make_ws_map(&mws2, tile2, BH, nchunks))
         return cudaErrorInvalidValue;
-    float* const side = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                                 (size_t)items * kTile);
     auto prep_kernel = chunk_prep_kernel<1, true>;
     auto scan_kernel = chunk_scan_kernel<false, 1, true>;
     cudaError_t err;
@@ -1875,9 +1939,9 @@ cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, c
     const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
     prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
         mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, nchunks, (int)items, batched, g,
-        side);
+        side, tile2);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, S0,
+    scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mws2, S0,
                                                        static_cast<__nv_bfloat16*>(o), S_T, nullptr,
                                                        T, 1, batched, side);
     return cudaGetLastError();

@@ -262,10 +262,11 @@ DN_API int dn_chunk_fwd_gated(const void *q, const void *k, const void *v,
                        float *S_T, int B, int H, int T, int dk, int dv, int C, int dt,
                        void *workspace, size_t workspace_bytes, void *stream);
 
-/* Scratch bytes of the tensor-core form of dn_chunk_fwd_gated: one 16 KB
- * [PT; Tm] tile and 1 KB of fp32 decay factors per (batch, head, chunk),
- * B * H * ceil(T / 64) * 17408 bytes; 0 where that form does not apply
- * (dk or dv != 128, fp32 I/O, C != 64, an empty problem).  Host-only. */
+/* Scratch bytes of the tensor-core form of dn_chunk_fwd_gated: two 16 KB
+ * tiles ([PT; Tm] and [PT; Tm] diag(exp G)) and 1 KB of fp32 decay factors
+ * per (batch, head, chunk), B * H * ceil(T / 64) * 33792 bytes; 0 where
+ * that form does not apply (dk or dv != 128, fp32 I/O, C != 64, an empty
+ * problem).  Host-only. */
 DN_API size_t dn_chunk_fwd_gated_workspace_bytes(int B, int H, int T, int dk, int dv,
                                           int C, int dt);
 

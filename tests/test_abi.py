@@ -72,11 +72,11 @@ def test_workspace_bytes(lib):
 
 
 def test_gated_workspace_bytes(lib):
-    """The gated tensor-core form adds 1 KB of fp32 decay factors per chunk
-    to the 16 KB tile; where that form does not apply it needs none."""
+    """The gated tensor-core form needs two 16 KB tiles and 1 KB of fp32
+    decay factors per chunk; where that form does not apply it needs none."""
     f = lib.dn_chunk_fwd_gated_workspace_bytes
-    assert f(8, 16, 2048, 128, 128, 64, 1) == 8 * 16 * 32 * (16384 + 1024)
-    assert f(1, 2, 130, 128, 128, 64, 1) == 2 * 3 * 17408
+    assert f(8, 16, 2048, 128, 128, 64, 1) == 8 * 16 * 32 * (2 * 16384 + 1024)
+    assert f(1, 2, 130, 128, 128, 64, 1) == 2 * 3 * 33792
     assert f(1, 1, 0, 128, 128, 64, 1) == 0
     assert f(8, 16, 2048, 128, 128, 64, 0) == 0
     assert f(8, 16, 2048, 64, 128, 64, 1) == 0

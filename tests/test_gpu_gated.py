@@ -70,26 +70,29 @@ def test_gated_strong_decay_and_edge_lengths():
 
 def _tc_workspace(B, H, T):
     n = dn.load().dn_chunk_fwd_gated_workspace_bytes(B, H, T, 128, 128, 64, 1)
-    assert n == B * H * ((T + 63) // 64) * 17408
+    assert n == B * H * ((T + 63) // 64) * 33792
     return torch.empty(n, dtype=torch.uint8, device="cuda")
 
 
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 1000])
-@pytest.mark.parametrize("lo", [0.9, 0.3], ids=["mild", "strong"])
-def test_gated_tc_chunk_ragged(T, lo):
+@pytest.mark.parametrize("lo,hi", [(0.9, 1.0), (0.3, 1.0), (0.05, 0.3)],
+                         ids=["mild", "strong", "extreme"])
+def test_gated_tc_chunk_ragged(T, lo, hi):
     """The tcgen05 form over ragged lengths (one partial chunk to 16
-    chunks), with an initial state, mild and strong decay (alpha down to 0.3:
-    exp G underflows inside a chunk)."""
+    chunks), with an initial state, and three decay regimes: mild, strong
+    (alpha down to 0.3) and extreme (alpha in (0.05, 0.3): a full chunk
+    decays by more than exp(-80), so its ratios take one exponential per
+    entry; a ragged tail chunk stays on the product form)."""
     B, H = 2, 3
     inp = workloads.chunk_inputs(B, H, T, 128, 128, dtype="bf16", seed=T + 7,
                                  feature_map="silu", s0_std=0.5)
-    g = workloads.gate_inputs(B, H, T, seed=T, lo=lo)
+    g = workloads.gate_inputs(B, H, T, seed=T, lo=lo, hi=hi)
     o, S = dn.chunk_fwd_gated(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g),
                               initial_state=dev(inp.S0), workspace=_tc_workspace(B, H, T))
     torch.cuda.synchronize()
     o_ref, S_ref = oracle.forward_gated(inp.q, inp.k, inp.v, inp.beta, g, inp.S0)
     _check(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
-           torch.bfloat16, f"tcgen05 T={T} lo={lo}")
+           torch.bfloat16, f"tcgen05 T={T} alpha in ({lo}, {hi})")
 
 
 def test_gated_tc_zero_decay_matches_the_plain_tc_kernel():

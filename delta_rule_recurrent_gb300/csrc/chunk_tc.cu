@@ -977,8 +977,10 @@ __device__ __forceinline__ SeqSpan scan_span(const SeqTable<NMAX>& seqs, int bh,
 // the cumulative log decay from the chunk start, A and P carry the ratios
 // exp(G_i - G_j) <= 1, and the item also writes the chunk's decay vectors
 // for the scan (exp G_t, exp(G_C - G_t) and exp G_C; kSideFloats per chunk)
-// and the decay-scaled tile [PT; Tm] diag(exp G) (tile2, row-major bf16, one
-// per item), the A operand of the scan's key term.
+// and the decay-scaled tile [PT; Tm] diag(exp G) (tm_ws2), the A operand of
+// the scan's key term.  That tile is rebuilt in the staging area once the
+// first store has read it, from fp32 rows: PT from its accumulator, Tm from
+// 64 more TMEM columns where it was kept when it was formed.
 constexpr int kPrepThreads = 128;
 constexpr int kSideFloats = 256;
 constexpr int kPrepCtasPerSm = 4;
@@ -1030,27 +1032,13 @@ __device__ __forceinline__ void decay_row_tmem(uint32_t taddr, const float* Gs, 
     tmem_wait_st();
 }
 
-// Row of the decay-scaled tile in global memory: x[e] exp(G_e), as bf16.
-__device__ __forceinline__ void store_row64_scaled(__nv_bfloat16* dst, const float (&x)[64],
-                                                   const float* Es) {
-    uint4* const d = reinterpret_cast<uint4*>(dst);
-    const float4* const e4 = reinterpret_cast<const float4*>(Es);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const float4 e0 = e4[2 * c], e1 = e4[2 * c + 1];
-        const float* const xs = x + 8 * c;
-        d[c] = make_uint4(pack_bf16(xs[0] * e0.x, xs[1] * e0.y), pack_bf16(xs[2] * e0.z, xs[3] * e0.w),
-                          pack_bf16(xs[4] * e1.x, xs[5] * e1.y), pack_bf16(xs[6] * e1.z, xs[7] * e1.w));
-    }
-}
-
 template <int NMAX, bool kGate>
 __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_ws, const __nv_bfloat16* __restrict__ beta,
                   int T, int nchunks, int items, const __grid_constant__ SeqTable<NMAX> seqs,
                   const float* __restrict__ gate, float* __restrict__ side,
-                  __nv_bfloat16* __restrict__ tile2) {
+                  const __grid_constant__ CUtensorMap tm_ws2) {
     static_assert(!kGate || NMAX == 1, "gating on the batched layout");
     constexpr int kBar = 1, B_TILES = 0, B_MMA = 1, B_END = 2;
     extern __shared__ uint8_t smem_raw[];
@@ -1076,9 +1064,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_ws);
+        if (kGate) prefetch_tensormap(&tm_ws2);
     }
     if (t < 32) {
-        tmem_alloc(smem_addr(tmem_holder), 64);
+        tmem_alloc(smem_addr(tmem_holder), kGate ? 128 : 64);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -1213,8 +1202,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 for (int j = 0; j < 64; ++j)
                     if (j > row) x[j] = 0.f;
             }
-            if (kGate && t < 64)  // Tm diag(exp G), row t
-                store_row64_scaled(tile2 + ((size_t)w * 128 + 64 + t) * 64, x, Es);
+            if (kGate && t < 64) {  // the fp32 Tm row, kept for the scaled tile
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(x[32 * h + e]);
+                    tmem_st32(tmem + lane_base + 64u + 32u * h, r);
+                }
+            }
             tc_fence_before_sync();
             wg_sync(kBar);
             store_row64_bf16(tp, t < 64 ? 64 + t : row, x);
@@ -1239,8 +1235,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             float x[64];
             tmem_ld64f(tmem + lane_base, x);
             store_row64_bf16(tp, t, x);
-            if constexpr (kGate)  // PT diag(exp G), row t
-                store_row64_scaled(tile2 + ((size_t)w * 128 + t) * 64, x, Es);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
@@ -1249,6 +1243,32 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const ChunkRef r = prep_item(seqs, w, nchunks, T);
             tma_store_3d(&tm_ws, tp, 0, r.wsrow, r.z);
             bulk_commit_group();
+            if constexpr (kGate) bulk_wait_group_read0();  // the staging area is free again
+        }
+        if constexpr (kGate) {  // [PT; Tm] diag(exp G) over the same staging area
+            tc_fence_before_sync();
+            wg_sync(kBar);
+            tc_fence_after_sync();
+            if (t < 64) {
+                tmem_wait_st();
+                float x[64];
+                tmem_ld64f(tmem + lane_base, x);  // PT, still in its accumulator
+#pragma unroll
+                for (int e = 0; e < 64; ++e) x[e] *= Es[e];
+                store_row64_bf16(tp, t, x);
+                tmem_ld64f(tmem + lane_base + 64u, x);  // Tm
+#pragma unroll
+                for (int e = 0; e < 64; ++e) x[e] *= Es[e];
+                store_row64_bf16(tp, 64 + t, x);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            wg_sync(kBar);
+            if (t == 0) {
+                const ChunkRef r = prep_item(seqs, w, nchunks, T);
+                tma_store_3d(&tm_ws2, tp, 0, r.wsrow, r.z);
+                bulk_commit_group();
+            }
         }
         if constexpr (kGate) {  // the chunk's decay vectors for the scan
             if (t < kC) {
@@ -1268,7 +1288,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     __syncthreads();
     if (t < 32) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, 64);
+        tmem_dealloc(tmem, kGate ? 128 : 64);
     }
 }
 
@@ -1856,7 +1876,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
         const SeqTable<1> batched{};
         const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
         prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
-            mq, mk, mws, b, T, nchunks, (int)items, batched, nullptr, nullptr, nullptr);
+            mq, mk, mws, b, T, nchunks, (int)items, batched, nullptr, nullptr, mws);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
         scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mws, S0,
                                                            static_cast<__nv_bfloat16*>(o), S_T,
@@ -1895,7 +1915,7 @@ cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v, 
         const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
         prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
             mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, 0, (int)items, seqs, nullptr,
-            nullptr, nullptr);
+            nullptr, mws);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     scan_kernel<<<(unsigned)ctas, 512, scan::kSmemBytes, stream>>>(
@@ -1939,7 +1959,7 @@ cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, c
     const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
     prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
         mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, nchunks, (int)items, batched, g,
-        side, tile2);
+        side, mws2);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mws2, S0,
                                                        static_cast<__nv_bfloat16*>(o), S_T, nullptr,

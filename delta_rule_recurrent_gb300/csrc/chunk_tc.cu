@@ -1573,7 +1573,6 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         tc_fence_before_sync();
         wg_sync(kBar);
         if (t == 0) {
-            mbar_arrive(ctl.bar(B_U_READ));
             tc_fence_after_sync();
             const uint32_t kq = sm.kq(c);
 #pragma unroll
@@ -1582,6 +1581,9 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                             sw128_desc(kq + 2048u * kk, kRegKQ, 1024), ID_KB, 1);
             mma_commit(ctl.bar(B_S_READY));
             mma_commit(ctl.bar(B_KQ_EMPTY + c % kStages));
+            // Only now may the o writer start the next chunk's v part: its MMAs
+            // then queue behind the state update the next S conversion waits on.
+            mbar_arrive(ctl.bar(B_U_READ));
         }
     }
     if (nchunks > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(nchunks - 1), t, kBar)) return;

@@ -352,11 +352,13 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
     if (tid < n) d_beta[tok0 + t0 + tid] = from_f32<T>(db);
 }
 
+// With `tiles` (the tensor-core state recompute's [PT; Tm] workspace), the
+// chain runs on tcgen05 (chunk_tc.cu) instead of chunk_bwd_chain_kernel.
 template <typename T, int DK, int DV>
 cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const void* beta,
                              const void* d_o, const float* d_S_T, void* d_q, void* d_k, void* d_v,
                              void* d_beta, float* d_S0, float* Sc, float* Gc, int BH, int Tlen,
-                             cudaStream_t stream) {
+                             const void* tiles, cudaStream_t stream) {
     constexpr int NV = DV < 64 ? DV : 64;
     // fp32 I/O keeps fp32 products; bf16 I/O runs them on tf32 tensor cores.
     using Ops = std::conditional_t<std::is_same_v<T, float>, simt::Fp32Ops, simt::Tf32Ops<8>>;
@@ -373,10 +375,15 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
         return err;
     const long long g_chain = (long long)BH * (DV / NV), g_grads = (long long)BH * nchunks;
     if (g_chain > 0x7fffffffLL || g_grads > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    chain<<<(unsigned)g_chain, Ops::kThreads, LC::kBytes, stream>>>(
-        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(beta),
-        static_cast<const T*>(d_o), d_S_T, static_cast<T*>(d_v), d_S0, Gc, Tlen);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (tiles)
+        err = launch_chunk_bwd_chain_tc(q, k, d_o, d_S_T, d_v, d_S0, Gc, tiles, BH, Tlen, stream);
+    else {
+        chain<<<(unsigned)g_chain, Ops::kThreads, LC::kBytes, stream>>>(
+            static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(beta),
+            static_cast<const T*>(d_o), d_S_T, static_cast<T*>(d_v), d_S0, Gc, Tlen);
+        err = cudaGetLastError();
+    }
+    if (err != cudaSuccess) return err;
     grads<<<(unsigned)g_grads, Ops::kThreads, LG::kBytes, stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
         static_cast<const T*>(beta), static_cast<const T*>(d_o), Sc, Gc, static_cast<T*>(d_q),
@@ -388,11 +395,11 @@ template <typename T>
 cudaError_t launch_bwd_dims(const void* q, const void* k, const void* v, const void* beta,
                             const void* d_o, const float* d_S_T, void* d_q, void* d_k, void* d_v,
                             void* d_beta, float* d_S0, float* Sc, float* Gc, int BH, int Tlen,
-                            int dk, int dv, cudaStream_t st) {
+                            int dk, int dv, const void* tiles, cudaStream_t st) {
 #define DN_BWD_CASE(DK_, DV_)                                                                   \
     if (dk == DK_ && dv == DV_)                                                                 \
         return launch_bwd_typed<T, DK_, DV_>(q, k, v, beta, d_o, d_S_T, d_q, d_k, d_v, d_beta,  \
-                                             d_S0, Sc, Gc, BH, Tlen, st);
+                                             d_S0, Sc, Gc, BH, Tlen, tiles, st);
     DN_BWD_CASE(128, 128)
     DN_BWD_CASE(128, 64)
     DN_BWD_CASE(64, 128)
@@ -422,17 +429,18 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
     const size_t per = (size_t)BH * ((T + kC - 1) / kC) * (size_t)dk * dv;
     float* const Sc = static_cast<float*>(workspace);
     float* const Gc = Sc + per;
-    cudaError_t err = chunk_tc_supports(dk, dv, dt)
-        ? launch_chunk_tc(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt, Gc + per, stream,
-                          Sc)
+    const bool tc = chunk_tc_supports(dk, dv, dt);
+    float* const tiles = Gc + per;  // the tensor-core recompute's [PT; Tm] tiles
+    cudaError_t err = tc
+        ? launch_chunk_tc(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt, tiles, stream, Sc)
         : launch_chunk_simt(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt, stream, Sc);
     if (err != cudaSuccess) return err;
     *stage = "gradient kernels";
     if (dt == 0)
         return launch_bwd_dims<float>(q, k, v, beta, d_o, d_S_T, d_q, d_k, d_v, d_beta, d_S0, Sc,
-                                      Gc, BH, T, dk, dv, stream);
+                                      Gc, BH, T, dk, dv, nullptr, stream);
     return launch_bwd_dims<__nv_bfloat16>(q, k, v, beta, d_o, d_S_T, d_q, d_k, d_v, d_beta, d_S0,
-                                          Sc, Gc, BH, T, dk, dv, stream);
+                                          Sc, Gc, BH, T, dk, dv, tc ? tiles : nullptr, stream);
 }
 
 }  // namespace dn

@@ -1790,6 +1790,346 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 }
 
+// ----------------------------------------------------- backward chain kernel
+// The backward's serial part on tcgen05: G = dL/dS from the last chunk to
+// the first, with G^T resident in TMEM (lanes: dv; columns: dk), as the
+// forward scan keeps S^T.  Per chunk, with the forward's own [PT; Tm] tile
+// (left in the workspace by the state recompute) read transposed through
+// MN-major descriptors:
+//     dV = Tm^T (P^T dO + K G) = PT^T dO + (K^T Tm)^T G
+//     G <- G + Q^T dO - K^T dV
+// i.e. in the transposed, dv-lane form
+//     dV^T = dO^T PT + G^T (K^T Tm),    G^T += dO^T Q - dV^T K.
+//   warp 0      TMA producer, chunks last to first: [K; Q] ring (3), dO (2),
+//               [PT; Tm] (2)
+//   warp 1      TMEM owner
+//   warps 4-7   state: thread t owns dv column t; records G at every chunk
+//               end, issues dV^T += G^T B2, converts dV^T, issues the G update
+//   warps 8-11  chunk group: B2 = K^T Tm (4 MMAs) -> bf16 tile (MN-major B)
+//   warps 12-15 d_v writer: starts each chunk's dV^T = dO^T PT and stores dV
+namespace bchain {
+constexpr int kStages = 3, kKQ = 6;
+constexpr uint32_t OFF_KQ = 0;
+constexpr uint32_t OFF_DO = OFF_KQ + kStages * kStageKQ;  // 2 x dO (2 dv-half regions)
+constexpr uint32_t OFF_TP = OFF_DO + 2 * kTile;           // 2 x [PT; Tm]
+constexpr uint32_t OFF_B2 = OFF_TP + 2 * kTile;           // 2 x K^T Tm (dk rows x 64 tokens)
+constexpr uint32_t OFF_BAR = OFF_B2 + 2 * kTile;
+enum : int {
+    B_KQ_FULL = 0,    // [6] q, k tiles landed                  (producer -> chunk group)
+    B_KQ_EMPTY = 6,   // [3] G update done with the stage        (state MMA -> producer)
+    B_DO_FULL = 9,    // [2] dO tile landed                      (producer -> writer)
+    B_DO_EMPTY = 11,  // [2] G update done with dO               (state MMA -> producer)
+    B_TP_FULL = 13,   // [2] [PT; Tm] landed                     (producer -> chunk group, writer)
+    B_B2_READY = 15,  // [2] K^T Tm tile written                 (chunk group -> state)
+    B_FREE = 17,      // [2] dV MMAs done with [PT; Tm] and B2   (state MMA -> producer)
+    B_DV_FULL = 19,   // dV^T done                               (own commit, state)
+    B_G_READY = 20,   // G update done                           (own commit, state)
+    B_B2_DONE = 21,   // K^T Tm done                             (own commit, chunk group)
+    B_DV_READY = 22,  // dV^T final                              (state -> writer)
+    B_DV_READ = 23,   // dV^T converted                          (state -> writer)
+    B_VP_DONE = 24,   // dO^T PT done                            (writer MMA -> state)
+    B_DRAIN = 25,     // [3] final drain per MMA issuer
+};
+constexpr int kBars = 28;
+constexpr uint32_t OFF_MISC = OFF_BAR + 8 * kBars;
+constexpr uint32_t kSmemBytes = OFF_MISC + 16 + 1024;
+static_assert(kSmemBytes <= 232448, "backward chain shared memory");
+// TMEM columns: G^T fp32 | G^T bf16 | dV^T fp32 | dV^T bf16 | K^T Tm fp32
+constexpr uint32_t C_GT = 0, C_GB = 128, C_DV = 192, C_VB = 256, C_B2 = 288;
+constexpr uint32_t ID_MM64 = idesc_bf16_f32(128, 64, 1, 1);   // A, B both MN-major, N = 64
+constexpr uint32_t ID_TM64 = idesc_bf16_f32(128, 64, 0, 1);   // A from TMEM, B MN-major, N = 64
+constexpr uint32_t ID_MM128 = idesc_bf16_f32(128, 128, 1, 1); // A, B both MN-major, N = 128
+constexpr uint32_t ID_TM128N = idesc_bf16_f32(128, 128, 0, 1) | (1u << 14);  // B negated
+
+struct Smem {
+    uint32_t base;
+    __device__ uint32_t kq(int i) const { return base + OFF_KQ + (uint32_t)(i % kStages) * kStageKQ; }
+    __device__ uint32_t dO(int i) const { return base + OFF_DO + (uint32_t)(i & 1) * kTile; }
+    __device__ uint32_t tp(int i) const { return base + OFF_TP + (uint32_t)(i & 1) * kTile; }
+    __device__ uint32_t b2(int i) const { return base + OFF_B2 + (uint32_t)(i & 1) * kTile; }
+};
+
+// Load i is chunk nchunks - 1 - i.
+__device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q,
+                         const CUtensorMap* tm_k, const CUtensorMap* tm_do,
+                         const CUtensorMap* tm_ws, int bh, int nchunks) {
+    int nkq = 0, ndo = 0, ntp = 0;
+    long long t0 = clock64();
+    while ((nkq < nchunks || ndo < nchunks || ntp < nchunks) && !ctl.aborted()) {
+        bool progressed = false;
+        if (nkq < nchunks &&
+            (nkq < kStages ||
+             mbar_test_wait(ctl.bar(B_KQ_EMPTY + nkq % kStages), (uint32_t)(nkq / kStages - 1) & 1u))) {
+            const int y = (nchunks - 1 - nkq) * kC;
+            const uint32_t st = sm.kq(nkq), bar = ctl.bar(B_KQ_FULL + nkq % kKQ);
+            mbar_arrive_expect_tx(bar, 4 * 8192);
+            tma_load_3d(st, tm_k, bar, 0, y, bh);
+            tma_load_3d(st + kRegKQ, tm_k, bar, 64, y, bh);
+            tma_load_3d(st + 8192, tm_q, bar, 0, y, bh);
+            tma_load_3d(st + kRegKQ + 8192, tm_q, bar, 64, y, bh);
+            if (nkq + kStages < nchunks) {  // warm L2 for this stage's next tiles
+                const int yn = (nchunks - 1 - nkq - kStages) * kC;
+                tma_prefetch_l2_3d(tm_k, 0, yn, bh);
+                tma_prefetch_l2_3d(tm_k, 64, yn, bh);
+                tma_prefetch_l2_3d(tm_q, 0, yn, bh);
+                tma_prefetch_l2_3d(tm_q, 64, yn, bh);
+            }
+            ++nkq;
+            progressed = true;
+        }
+        if (ndo < nchunks &&
+            (ndo < 2 || mbar_test_wait(ctl.bar(B_DO_EMPTY + (ndo & 1)), (uint32_t)(ndo / 2 - 1) & 1u))) {
+            const int y = (nchunks - 1 - ndo) * kC;
+            const uint32_t bar = ctl.bar(B_DO_FULL + (ndo & 1));
+            mbar_arrive_expect_tx(bar, 2 * 8192);
+            tma_load_3d(sm.dO(ndo), tm_do, bar, 0, y, bh);
+            tma_load_3d(sm.dO(ndo) + 8192, tm_do, bar, 64, y, bh);
+            ++ndo;
+            progressed = true;
+        }
+        if (ntp < nchunks) {
+            const int g = ntp & 1, it = ntp >> 1;
+            if (it == 0 || mbar_test_wait(ctl.bar(B_FREE + g), (uint32_t)(it - 1) & 1u)) {
+                const uint32_t bar = ctl.bar(B_TP_FULL + g);
+                mbar_arrive_expect_tx(bar, kTile);
+                tma_load_3d(sm.tp(ntp), tm_ws, bar, 0, (nchunks - 1 - ntp) * 128, bh);
+                ++ntp;
+                progressed = true;
+            }
+        }
+        if (progressed) {
+            t0 = clock64();
+        } else {
+            __nanosleep(64);
+            if (clock64() - t0 > kTimeoutCycles) ctl.raise();
+        }
+    }
+    for (int b = 0; b < kKQ; ++b) {  // leave nothing in flight (bounded waits)
+        const int n_b = (nkq - b + kKQ - 1) / kKQ;
+        if (n_b > 0) mbar_wait(ctl.bar(B_KQ_FULL + b), (uint32_t)(n_b - 1) & 1u, kTimeoutNs);
+    }
+    for (int b = 0; b < 2; ++b) {
+        const int n_b = (ndo - b + 1) / 2;
+        if (n_b > 0) mbar_wait(ctl.bar(B_DO_FULL + b), (uint32_t)(n_b - 1) & 1u, kTimeoutNs);
+        const int n_g = (ntp - b + 1) / 2;
+        if (n_g > 0) mbar_wait(ctl.bar(B_TP_FULL + b), (uint32_t)(n_g - 1) & 1u, kTimeoutNs);
+    }
+}
+
+__device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
+                           const float* __restrict__ d_S_T, float* __restrict__ d_S0,
+                           float* __restrict__ G_chunks, int bh, int nchunks) {
+    constexpr int kBar = 1;
+    const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
+    // d_S_T^T into TMEM: lane t holds dv column t (zeros without d_S_T).
+#pragma unroll
+    for (int part = 0; part < 4; ++part) {
+        uint32_t r[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            r[e] = d_S_T ? __float_as_uint(d_S_T[((size_t)bh * kD + 32 * part + e) * kD + t]) : 0u;
+        tmem_st32(lane + C_GT + 32u * part, r);
+    }
+    tmem_wait_st();
+    for (int i = 0; i < nchunks; ++i) {
+        const int c = nchunks - 1 - i;
+        if (i > 0 && !wg_wait(ctl, B_G_READY, (uint32_t)(i - 1), t, kBar)) return;
+        tc_fence_after_sync();
+        {   // G^T -> bf16, and G itself recorded as the gradient at chunk c's end
+            float* const rec = G_chunks + ((size_t)bh * nchunks + c) * kD * kD + t;
+            scan::tmem_pack64(lane + C_GT, lane + C_GB, rec);
+            scan::tmem_pack64(lane + C_GT + 64u, lane + C_GB + 32u, rec + 64 * kD);
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        wg_sync(kBar);
+        bool ok = true;
+        if (t == 0) {
+            ok = ctl.wait(B_B2_READY + (i & 1), (uint32_t)(i >> 1)) &&
+                 ctl.wait(B_VP_DONE, (uint32_t)i);
+            if (ok) {
+                tc_fence_after_sync();
+                const uint32_t b2 = sm.b2(i), dO = sm.dO(i), kq = sm.kq(i);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // dV^T += G^T (K^T Tm) over dk
+                    mma_bf16_ts(tmem + C_DV, tmem + C_GB + 8u * kk,
+                                sw128_desc(b2 + 2048u * kk, 8192, 1024), ID_TM64, 1);
+                mma_commit(ctl.bar(B_DV_FULL));
+                mma_commit(ctl.bar(B_FREE + (i & 1)));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)  // G^T += dO^T Q over the chunk's tokens
+                    mma_bf16_ss(tmem + C_GT, sw128_desc(dO + 2048u * kk, 8192, 1024),
+                                sw128_desc(kq + 8192u + 2048u * kk, kRegKQ, 1024), ID_MM128, 1);
+                ok = ctl.wait(B_DV_FULL, (uint32_t)i);
+                if (ok) mbar_arrive(ctl.bar(B_DV_READY));
+            }
+        }
+        if (wg_sync_or(kBar, !ok)) return;
+        tc_fence_after_sync();
+        scan::tmem_pack64(lane + C_DV, lane + C_VB);  // dV^T -> bf16 (tokens)
+        tmem_wait_st();
+        tc_fence_before_sync();
+        wg_sync(kBar);
+        if (t == 0) {
+            tc_fence_after_sync();
+            const uint32_t kq = sm.kq(i);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // G^T -= dV^T K
+                mma_bf16_ts(tmem + C_GT, tmem + C_VB + 8u * kk,
+                            sw128_desc(kq + 2048u * kk, kRegKQ, 1024), ID_TM128N, 1);
+            mma_commit(ctl.bar(B_G_READY));
+            mma_commit(ctl.bar(B_KQ_EMPTY + i % kStages));
+            mma_commit(ctl.bar(B_DO_EMPTY + (i & 1)));
+            mbar_arrive(ctl.bar(B_DV_READ));  // the writer may start the next dV^T
+        }
+    }
+    if (nchunks > 0 && !wg_wait(ctl, B_G_READY, (uint32_t)(nchunks - 1), t, kBar)) return;
+    tc_fence_after_sync();
+    if (d_S0) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float x[64];
+            tmem_ld64f(lane + C_GT + 64u * half, x);
+#pragma unroll
+            for (int e = 0; e < 64; ++e) d_S0[((size_t)bh * kD + 64 * half + e) * kD + t] = x[e];
+        }
+    }
+}
+
+__device__ void group_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int nchunks) {
+    constexpr int kBar = 2;
+    const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
+    for (int i = 0; i < nchunks; ++i) {
+        bool ok = true;
+        if (t == 0) {
+            ok = ctl.wait(B_KQ_FULL + i % kKQ, (uint32_t)(i / kKQ)) &&
+                 ctl.wait(B_TP_FULL + (i & 1), (uint32_t)(i >> 1));
+            if (ok) {
+                tc_fence_after_sync();
+                const uint32_t kq = sm.kq(i), tp = sm.tp(i);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)  // K^T Tm over the chunk's tokens
+                    mma_bf16_ss(tmem + C_B2, sw128_desc(kq + 2048u * kk, kRegKQ, 1024),
+                                sw128_desc(tp + 8192u + 2048u * kk, 8192, 1024), ID_MM64, kk > 0);
+                mma_commit(ctl.bar(B_B2_DONE));
+                ok = ctl.wait(B_B2_DONE, (uint32_t)i);
+            }
+        }
+        // B2 (this buffer set) is free: its last reader, the dV MMAs two
+        // chunks back, finished before [PT; Tm] could be reloaded.
+        if (wg_sync_or(kBar, !ok)) return;
+        tc_fence_after_sync();
+        float x[64];  // row t (dk) of K^T Tm, as the MN-major B tile
+        tmem_ld64f(lane + C_B2, x);
+        store_row64_bf16(sm.b2(i), t, x);
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        wg_sync(kBar);
+        if (t == 0) mbar_arrive(ctl.bar(B_B2_READY + (i & 1)));
+    }
+}
+
+__device__ void writer_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
+                            __nv_bfloat16* __restrict__ d_v, int bh, int T, int nchunks) {
+    constexpr int kBar = 3;
+    const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
+    // dV^T = dO^T PT for load i, once its dO and [PT; Tm] are in (thread 0).
+    auto start = [&](int i) -> bool {
+        if (!ctl.wait(B_TP_FULL + (i & 1), (uint32_t)(i >> 1)) ||
+            !ctl.wait(B_DO_FULL + (i & 1), (uint32_t)(i >> 1)))
+            return false;
+        tc_fence_after_sync();
+        const uint32_t dO = sm.dO(i), tp = sm.tp(i);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + C_DV, sw128_desc(dO + 2048u * kk, 8192, 1024),
+                        sw128_desc(tp + 2048u * kk, 8192, 1024), ID_MM64, kk > 0);
+        mma_commit(ctl.bar(B_VP_DONE));
+        return true;
+    };
+    bool ok = t != 0 || nchunks == 0 || start(0);
+    if (wg_sync_or(kBar, !ok)) return;
+    for (int i = 0; i < nchunks; ++i) {
+        const int c = nchunks - 1 - i;
+        ok = true;
+        if (t == 0) ok = ctl.wait(B_DV_READY, (uint32_t)i);
+        if (wg_sync_or(kBar, !ok)) return;
+        tc_fence_after_sync();
+        float x[64];  // dV^T: dv column t over the chunk's 64 tokens
+        tmem_ld64f(lane + C_DV, x);
+        tc_fence_before_sync();
+        wg_sync(kBar);
+        // dV^T is free once the state has converted it as well.
+        if (t == 0) ok = ctl.wait(B_DV_READ, (uint32_t)i) && (i + 1 >= nchunks || start(i + 1));
+        const int tok0 = c * kC;
+        __nv_bfloat16* const db = d_v + ((size_t)bh * T + tok0) * kD + t;
+#pragma unroll
+        for (int r = 0; r < 64; ++r)
+            if (tok0 + r < T) db[(size_t)r * kD] = __float2bfloat16_rn(x[r]);
+        if (wg_sync_or(kBar, !ok)) return;
+    }
+}
+}  // namespace bchain
+
+__global__ void __launch_bounds__(512, 1)
+chunk_bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_do,
+                          const __grid_constant__ CUtensorMap tm_ws, const float* __restrict__ d_S_T,
+                          __nv_bfloat16* __restrict__ d_v, float* __restrict__ d_S0,
+                          float* __restrict__ G_chunks, int T) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    const bchain::Smem sm{base};
+    int* const misc = reinterpret_cast<int*>(smem_raw + (base - raw_addr) + bchain::OFF_MISC);
+    const Ctl ctl{base + bchain::OFF_BAR, reinterpret_cast<volatile int*>(misc)};
+    uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.x;
+    const int nchunks = (T + kC - 1) / kC;
+
+    if (tid == 0) {
+        misc[0] = 0;
+        for (int b = 0; b < bchain::kBars; ++b) mbar_init(ctl.bar(b), 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_do);
+        prefetch_tensormap(&tm_ws);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_holder), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) bchain::producer(ctl, sm, &tm_q, &tm_k, &tm_do, &tm_ws, bh, nchunks);
+    } else if (warp >= 4 && warp < 8) {
+        const int t = tid - 128;
+        bchain::state_body(ctl, sm, tmem, t, d_S_T, d_S0, G_chunks, bh, nchunks);
+        if (t == 0) drain_mmas(ctl, bchain::B_DRAIN + 0);
+    } else if (warp >= 8 && warp < 12) {
+        const int t = tid - 256;
+        bchain::group_body(ctl, sm, tmem, t, nchunks);
+        if (t == 0) drain_mmas(ctl, bchain::B_DRAIN + 1);
+    } else if (warp >= 12) {
+        const int t = tid - 384;
+        bchain::writer_body(ctl, sm, tmem, t, d_v, bh, T, nchunks);
+        if (t == 0) drain_mmas(ctl, bchain::B_DRAIN + 2);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1966,6 +2306,26 @@ cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, c
     scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mws2, S0,
                                                        static_cast<__nv_bfloat16*>(o), S_T, nullptr,
                                                        T, 1, batched, side);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_bwd_chain_tc(const void* q, const void* k, const void* d_o,
+                                      const float* d_S_T, void* d_v, float* d_S0,
+                                      float* G_chunks, const void* tiles, int BH, int T,
+                                      cudaStream_t stream) {
+    if (BH <= 0 || T <= 0) return cudaSuccess;
+    const int nchunks = (T + kC - 1) / kC;
+    CUtensorMap mq, mk, mdo, mws;
+    if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mdo, d_o, BH, T) ||
+        !make_ws_map(&mws, const_cast<void*>(tiles), BH, nchunks))
+        return cudaErrorInvalidValue;
+    cudaError_t err;
+    if ((err = cudaFuncSetAttribute(chunk_bwd_chain_tc_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    bchain::kSmemBytes)) != cudaSuccess)
+        return err;
+    chunk_bwd_chain_tc_kernel<<<BH, 512, bchain::kSmemBytes, stream>>>(
+        mq, mk, mdo, mws, d_S_T, static_cast<__nv_bfloat16*>(d_v), d_S0, G_chunks, T);
     return cudaGetLastError();
 }
 

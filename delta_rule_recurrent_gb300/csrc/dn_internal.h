@@ -73,6 +73,14 @@ cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v,
                                    const void* beta, const float* S0, void* o, float* S_T,
                                    const VarlenTable& seqs, int H, int T, void* workspace,
                                    cudaStream_t stream);
+// The backward's chain on tcgen05 (bf16, dk = dv = 128): G = dL/dS from the
+// last chunk to the first, with the forward's [PT; Tm] tiles (`tiles`, the
+// workspace the state recompute used) read transposed.  Writes G at every
+// chunk end (G_chunks, [BH][chunk][dk][dv] fp32), d_v and d_S0 (if given).
+cudaError_t launch_chunk_bwd_chain_tc(const void* q, const void* k, const void* d_o,
+                                      const float* d_S_T, void* d_v, float* d_S0,
+                                      float* G_chunks, const void* tiles, int BH, int T,
+                                      cudaStream_t stream);
 // Gated DeltaNet on tensor cores (two passes; g the fp32 [BH][T] log keep
 // rate): the workspace holds the [PT; Tm] tiles and then kSideFloats fp32
 // decay values per chunk, chunk_tc_gated_workspace_bytes(BH, T) in all.

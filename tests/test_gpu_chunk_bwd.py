@@ -77,6 +77,21 @@ def test_edge_lengths_without_optional_states(T):
     _check(_gpu_grads(inp, d_o, None), ref, torch.float32, f"T={T}")
 
 
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 130])
+@pytest.mark.parametrize("states", [False, True], ids=["no-states", "states"])
+def test_tensor_core_chain_edge_lengths(T, states):
+    """bf16, dk = dv = 128: the tensor-core chain (chunks last to first, the
+    ragged chunk first) from one token to a ragged third chunk, with and
+    without the initial state and the final-state gradient."""
+    inp, d_o, d_S = _case(1, 3, T, 128, 128, "bf16", seed=100 + T,
+                          s0=0.3 if states else None, ds=0.3 if states else None)
+    ref = oracle.backward(inp.q, inp.k, inp.v, inp.beta, d_o, inp.S0, d_S)
+    got = _gpu_grads(inp, d_o, d_S) if states else [
+        x.double().cpu().numpy() for x in dn.chunk_bwd(
+            dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(d_o))]
+    _check(got, ref, torch.bfloat16, f"T={T} states={states}")
+
+
 def test_beta_zero_gives_zero_key_and_value_gradients():
     inp, d_o, d_S = _case(1, 2, 130, 64, 64, "f32", seed=3)
     inp.beta.zero_()

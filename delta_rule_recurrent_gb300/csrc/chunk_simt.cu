@@ -41,6 +41,7 @@
 //     S  <- diag(exp G_C) S + (K . exp(G_C - G))^T U'
 // The ratios sit inside the sums, so every exponent is <= 0 however strong
 // the decay (no 1 / Gamma factors).
+#include <type_traits>
 #include "dn_common.cuh"
 #include "dn_internal.h"
 #include "simt_mm.cuh"
@@ -103,6 +104,8 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
     float* eG = Gc + kC;               // exp(G_t)
     float* dec = eG + kC;              // exp(G_C - G_t)
     float* Gk = smem + L::kGk;         // KDA: cumulative log decay per key channel
+    float* eC = Gc;                    // KDA: exp(G_C) per key channel (DK <= 3 C floats)
+    static_assert(!kChan || DK <= 3 * kC, "room for exp(G_C)");
 
     const int tid = threadIdx.x;
     const int tx = tid & 15, ty = tid >> 4;
@@ -136,11 +139,31 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
         load_tile<kThreads, kC, DK, LK, DK>(Qs, q, tok0 + t0, n, 0);
         load_tile<kThreads, kC, NV, LV, DV>(Rs, v, tok0 + t0, n, j0);
         if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
+        // KDA: while the chunk's decay stays within exp(-80) on every key
+        // channel (G is non-increasing, so G_C is each channel's lowest), the
+        // ratio exp(G_i - G_j) is the product exp(G_i) exp(-G_j) of two normal
+        // fp32 numbers: K and Q become K exp(G), Q exp(G) in place and Gk
+        // becomes K exp(-G), so A, P, the state read and the update are plain
+        // products.  Otherwise every ratio takes its own clamped exponential.
+        bool sep = false;
         if constexpr (kChan) {  // per-channel rates, then prefix sums over the chunk
             load_tile<kThreads, kC, DK, LK, DK>(Gk, g, tok0 + t0, n, 0);
             __syncthreads();
             if (tid < DK)
                 for (int t = 1; t < kC; ++t) Gk[t * LK + tid] += Gk[(t - 1) * LK + tid];
+            __syncthreads();
+            sep = __syncthreads_and(tid >= DK || Gk[(kC - 1) * LK + tid] >= -80.f);
+            if (sep) {
+                if (tid < DK) eC[tid] = __expf(Gk[(kC - 1) * LK + tid]);
+                for (int e = tid; e < kC * DK; e += kThreads) {
+                    const int t = e / DK, d = e % DK;
+                    const float G = Gk[t * LK + d], kv = Ks[t * LK + d];
+                    const float ep = __expf(G);
+                    Ks[t * LK + d] = kv * ep;
+                    Qs[t * LK + d] *= ep;
+                    Gk[t * LK + d] = kv * __expf(-G);
+                }
+            }
         } else if (tid < 32) {  // prefix sums of the log keep rates (padding tokens keep everything)
             const int t = 2 * tid;
             const float a = (g && t < n) ? g[tok0 + t0 + t] : 0.f;
@@ -163,7 +186,11 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
         __syncthreads();
 
         // ---- A = tril(diag(beta) K K^T, -1) and P = tril(Q K^T) ----
-        {
+        // (the KDA forms choose once per chunk, so every inner loop below is
+        // compiled for one form and carries no per-element branch)
+        auto form_ap = [&](auto per_entry) {
+            constexpr bool kExp = decltype(per_entry)::value;
+            const float* const Bk = (kChan && !kExp) ? Gk : Ks;  // KDA product form: K exp(-G)
             float aa[4][4], ap[4][4];
             zero<64, 64>(aa);
             zero<64, 64>(ap);
@@ -174,9 +201,9 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
                 for (int i = 0; i < 4; ++i) {
                     ak[i] = Ks[(ty + 16 * i) * LK + kk];
                     aq[i] = Qs[(ty + 16 * i) * LK + kk];
-                    bk[i] = Ks[(tx + 16 * i) * LK + kk];
+                    bk[i] = Bk[(tx + 16 * i) * LK + kk];
                 }
-                if constexpr (kChan) {  // the channel's decay ratio inside the sum
+                if constexpr (kExp) {  // the channel's decay ratio inside the sum
                     float gi[4], gj[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -210,16 +237,24 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
                     Am[m * kLC + nn] = nn < m ? bs[m] * (aa[i][j] * r) : 0.f;
                     Pm[m * kLC + nn] = nn <= m ? ap[i][j] * r : 0.f;
                 }
-        }
+        };
+        if (kChan && !sep)
+            form_ap(std::true_type{});
+        else
+            form_ap(std::false_type{});
         __syncthreads();
 
         // ---- R' = diag(beta) (V - diag(exp G) K S), in place over V ----
         {
             float acc[4][NV / 16];
             zero<64, NV>(acc);
-            mm_acc<64, NV, DK>(acc, [&](int m, int kk) {
-                return kChan ? Ks[m * LK + kk] * __expf(Gk[m * LK + kk]) : Ks[m * LK + kk];
-            }, [&](int kk, int nn) { return Ss[kk * LV + nn]; });
+            const auto state = [&](int kk, int nn) { return Ss[kk * LV + nn]; };
+            if (kChan && !sep)
+                mm_acc<64, NV, DK>(acc, [&](int m, int kk) {
+                    return Ks[m * LK + kk] * __expf(Gk[m * LK + kk]);
+                }, state);
+            else
+                mm_acc<64, NV, DK>(acc, [&](int m, int kk) { return Ks[m * LK + kk]; }, state);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -250,9 +285,13 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
         if (o) {
             float acc[4][NV / 16];
             zero<64, NV>(acc);
-            mm_acc<64, NV, DK>(acc, [&](int m, int kk) {
-                return kChan ? Qs[m * LK + kk] * __expf(Gk[m * LK + kk]) : Qs[m * LK + kk];
-            }, [&](int kk, int nn) { return Ss[kk * LV + nn]; });
+            const auto state = [&](int kk, int nn) { return Ss[kk * LV + nn]; };
+            if (kChan && !sep)
+                mm_acc<64, NV, DK>(acc, [&](int m, int kk) {
+                    return Qs[m * LK + kk] * __expf(Gk[m * LK + kk]);
+                }, state);
+            else
+                mm_acc<64, NV, DK>(acc, [&](int m, int kk) { return Qs[m * LK + kk]; }, state);
             if constexpr (!kChan) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
@@ -277,14 +316,24 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
         {
             float acc[DK / 16][NV / 16];
             zero<DK, NV>(acc);
-            mm_acc<DK, NV, kC>(acc, [&](int m, int kk) {
-                return kChan ? Ks[kk * LK + m] * __expf(Gk[(kC - 1) * LK + m] - Gk[kk * LK + m])
-                             : Ks[kk * LK + m] * dec[kk];
-            }, [&](int kk, int nn) { return Us[kk * LV + nn]; });
+            const auto upd = [&](int kk, int nn) { return Us[kk * LV + nn]; };
+            if constexpr (kChan) {
+                if (sep)
+                    mm_acc<DK, NV, kC>(acc, [&](int m, int kk) { return Gk[kk * LK + m] * eC[m]; },
+                                       upd);
+                else
+                    mm_acc<DK, NV, kC>(acc, [&](int m, int kk) {
+                        return Ks[kk * LK + m] * __expf(Gk[(kC - 1) * LK + m] - Gk[kk * LK + m]);
+                    }, upd);
+            } else {
+                mm_acc<DK, NV, kC>(acc, [&](int m, int kk) { return Ks[kk * LK + m] * dec[kk]; },
+                                   upd);
+            }
 #pragma unroll
             for (int i = 0; i < DK / 16; ++i) {
                 const int row = ty + 16 * i;
-                const float keep = kChan ? __expf(Gk[(kC - 1) * LK + row]) : eG[kC - 1];
+                const float keep = kChan ? (sep ? eC[row] : __expf(Gk[(kC - 1) * LK + row]))
+                                         : eG[kC - 1];
 #pragma unroll
                 for (int j = 0; j < NV / 16; ++j) {
                     float* const sp = Ss + row * LV + tx + 16 * j;

@@ -4,6 +4,7 @@
     python -m delta_rule_recurrent_gb300.profile_run decode [--B 256] [--steps 4]
     python -m delta_rule_recurrent_gb300.profile_run bwd [--B 8] [--T 2048] [--reps 2]
     python -m delta_rule_recurrent_gb300.profile_run gated [--B 8] [--T 2048] [--reps 3] [--no-workspace]
+    python -m delta_rule_recurrent_gb300.profile_run kda [--B 8] [--T 2048] [--reps 3]
 
 `chunk` runs the chunkwise forward on the 1.3B-layer shape (B8 H16 T2048
 dk=dv=128, bf16; B and T can be reduced; the tensor-core path runs in two
@@ -11,7 +12,8 @@ passes unless --no-workspace selects its fused kernel); `decode` runs consecutiv
 steps on the decode workload's shape (B256 H16 dk=dv=128, fp32 state); `bwd`
 runs the chunkwise backward (dn_chunk_bwd) on the 1.3B-layer shape; `gated`
 runs the Gated DeltaNet chunkwise forward there (keep rates U(0.9, 1); two
-tcgen05 passes, or the CUDA-core kernel with --no-workspace).  Inputs
+tcgen05 passes, or the CUDA-core kernel with --no-workspace); `kda` runs the
+KDA chunkwise forward there (per-channel keep rates U(0.9, 1)).  Inputs
 come from the seeded generators in `workloads`.
 """
 from __future__ import annotations
@@ -30,7 +32,7 @@ def main(argv=None):
     import workloads
 
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("what", choices=["chunk", "decode", "bwd", "gated"])
+    ap.add_argument("what", choices=["chunk", "decode", "bwd", "gated", "kda"])
     ap.add_argument("--B", type=int, default=None)
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--algo", default="auto", choices=list(dn.ALGOS))
@@ -54,6 +56,14 @@ def main(argv=None):
         g = workloads.gate_inputs(B, H, T, seed=7).to(dev)
         for _ in range(a.reps):
             o, _ = dn.chunk_fwd_gated(q, k, v, b, g, workspace=None if a.no_workspace else "auto")
+    elif a.what == "kda":
+        over = {k: v for k, v in (("B", a.B), ("T", a.T)) if v is not None}
+        inp = workloads.workload_inputs("layer1p3b_bf16", **over)
+        B, H, T, d = inp.q.shape
+        q, k, v, b = (x.to(dev) for x in (inp.q, inp.k, inp.v, inp.beta))
+        g = workloads.gate_inputs(B, H, T, seed=7, channels=d).to(dev)
+        for _ in range(a.reps):
+            o, _ = dn.chunk_fwd_kda(q, k, v, b, g)
     elif a.what == "bwd":
         over = {k: v for k, v in (("B", a.B), ("T", a.T)) if v is not None}
         inp = workloads.workload_inputs("layer1p3b_bf16", **over)

@@ -25,11 +25,13 @@
 namespace dn {
 namespace {
 
-template <typename T, int DK, int DV, int NT>
+// kMode: 0 no decay, 1 one log keep rate per head (Gated DeltaNet), 2 one
+// per key channel (KDA).
+template <typename T, int DK, int DV, int NT, int kMode>
 __global__ void __launch_bounds__(NT)
 recurrent_step_kernel(const T* __restrict__ q, const T* __restrict__ k,
                       const T* __restrict__ v, const T* __restrict__ beta,
-                      const float* __restrict__ g, int g_per_channel, float* __restrict__ S,
+                      const float* __restrict__ g, float* __restrict__ S,
                       T* __restrict__ o) {
     constexpr int CG = DV / 4;    // float4 column groups per state row
     constexpr int RG = NT / CG;   // row groups (threads sharing a column group)
@@ -49,6 +51,14 @@ recurrent_step_kernel(const T* __restrict__ q, const T* __restrict__ k,
     float4 s[RPT];
 #pragma unroll
     for (int r = 0; r < RPT; ++r) s[r] = Sh[(size_t)(rg + r * RG) * CG + cg];
+    // ... and the log keep rates with them, ahead of the barrier below.
+    float graw[kMode == 2 ? RPT : 1];
+    if constexpr (kMode == 2) {
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) graw[r] = g[(size_t)head * DK + rg + r * RG];
+    } else if constexpr (kMode == 1) {
+        graw[0] = g[head];
+    }
 
     for (int i = tid; i < DK; i += NT) {
         ks[i] = to_f32(k[(size_t)head * DK + i]);
@@ -67,9 +77,14 @@ recurrent_step_kernel(const T* __restrict__ q, const T* __restrict__ k,
 
     // keep rate of each of this thread's state rows (1 without decay)
     float a[RPT];
+    if constexpr (kMode == 2) {
 #pragma unroll
-    for (int r = 0; r < RPT; ++r)
-        a[r] = !g ? 1.f : expf(g_per_channel ? g[(size_t)head * DK + rg + r * RG] : g[head]);
+        for (int r = 0; r < RPT; ++r) a[r] = __expf(graw[r]);
+    } else {
+        const float ah = kMode == 1 ? expf(graw[0]) : 1.f;
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) a[r] = ah;
+    }
 
     float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
 #pragma unroll
@@ -123,10 +138,17 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
                          const void* beta, const float* g, int gpc, float* S, void* o, int BH,
                          cudaStream_t stream) {
     constexpr int NT = 256;
-    recurrent_step_kernel<T, DK, DV, NT><<<BH, NT, 0, stream>>>(
-        static_cast<const T*>(q), static_cast<const T*>(k),
-        static_cast<const T*>(v), static_cast<const T*>(beta), g, gpc, S,
-        static_cast<T*>(o));
+    const T* const qt = static_cast<const T*>(q);
+    const T* const kt = static_cast<const T*>(k);
+    const T* const vt = static_cast<const T*>(v);
+    const T* const bt = static_cast<const T*>(beta);
+    T* const ot = static_cast<T*>(o);
+    if (!g)
+        recurrent_step_kernel<T, DK, DV, NT, 0><<<BH, NT, 0, stream>>>(qt, kt, vt, bt, g, S, ot);
+    else if (gpc)
+        recurrent_step_kernel<T, DK, DV, NT, 2><<<BH, NT, 0, stream>>>(qt, kt, vt, bt, g, S, ot);
+    else
+        recurrent_step_kernel<T, DK, DV, NT, 1><<<BH, NT, 0, stream>>>(qt, kt, vt, bt, g, S, ot);
     return cudaGetLastError();
 }
 

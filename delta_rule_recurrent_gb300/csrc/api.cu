@@ -126,8 +126,8 @@ int dn_chunk_fwd_algo(const void* q, const void* k, const void* v, const void* b
     if (dk <= 0 || dv <= 0 || C <= 0)
         return fail(DN_ERR_INVALID_ARG, "dk, dv and C must be positive");
     if (!supported_dim(dk) || !supported_dim(dv))
-        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this build supports 64 and 128", dk, dv);
-    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this build supports 64", C);
+        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this library supports 64 and 128", dk, dv);
+    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this library supports 64", C);
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
     const size_t need_ws = dn_chunk_fwd_workspace_bytes(B, H, T, dk, dv, C, dt);
@@ -295,8 +295,8 @@ int dn_chunk_fwd_varlen(const void* q, const void* k, const void* v, const void*
     if (dk <= 0 || dv <= 0 || C <= 0)
         return fail(DN_ERR_INVALID_ARG, "dk, dv and C must be positive");
     if (!supported_dim(dk) || !supported_dim(dv))
-        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this build supports 64 and 128", dk, dv);
-    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this build supports 64", C);
+        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this library supports 64 and 128", dk, dv);
+    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this library supports 64", C);
     static thread_local dn::VarlenTable tab;
     if (int st = varlen_table(cu_seqlens, N, T, &tab)) return st;
     const size_t need_ws = dn_chunk_fwd_varlen_workspace_bytes(cu_seqlens, N, H, dk, dv, C, dt);
@@ -364,8 +364,8 @@ static int chunk_fwd_decayed(const void* q, const void* k, const void* v, const 
     if (dk <= 0 || dv <= 0 || C <= 0)
         return fail(DN_ERR_INVALID_ARG, "dk, dv and C must be positive");
     if (!supported_dim(dk) || !supported_dim(dv))
-        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this build supports 64 and 128", dk, dv);
-    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this build supports 64", C);
+        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this library supports 64 and 128", dk, dv);
+    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this library supports 64", C);
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
     const size_t need_ws =
@@ -454,7 +454,7 @@ static int recurrent_step_decayed(const void* q, const void* k, const void* v,
     if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
     if (dk <= 0 || dv <= 0) return fail(DN_ERR_INVALID_ARG, "dk and dv must be positive");
     if (!supported_dim(dk) || !supported_dim(dv))
-        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this build supports 64 and 128", dk, dv);
+        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this library supports 64 and 128", dk, dv);
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
     if (BH == 0) return ok();
@@ -498,7 +498,7 @@ int dn_recurrent_step(const void* q, const void* k, const void* v, const void* b
     if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
     if (dk <= 0 || dv <= 0) return fail(DN_ERR_INVALID_ARG, "dk and dv must be positive");
     if (!supported_dim(dk) || !supported_dim(dv))
-        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this build supports 64 and 128", dk, dv);
+        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this library supports 64 and 128", dk, dv);
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
     if (BH == 0) return ok();
@@ -539,8 +539,8 @@ int dn_chunk_bwd(const void* q, const void* k, const void* v, const void* beta, 
     if (dk <= 0 || dv <= 0 || C <= 0)
         return fail(DN_ERR_INVALID_ARG, "dk, dv and C must be positive");
     if (!supported_dim(dk) || !supported_dim(dv))
-        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this build supports 64 and 128", dk, dv);
-    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this build supports 64", C);
+        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this library supports 64 and 128", dk, dv);
+    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this library supports 64", C);
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
     const size_t need_ws = dn_chunk_bwd_workspace_bytes(B, H, T, dk, dv, C, dt);

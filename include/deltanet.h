@@ -49,7 +49,7 @@ extern "C" {
 typedef enum {
     DN_OK = 0,
     DN_ERR_INVALID_ARG = 1, /* NULL / host / misaligned / aliasing pointer, bad size */
-    DN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement     */
+    DN_ERR_UNSUPPORTED = 2, /* valid request this library does not implement   */
     DN_ERR_CUDA = 3         /* the CUDA runtime reported an error              */
 } dn_status;
 

@@ -62,7 +62,7 @@ def test_tiny_fp32_workload_gradients():
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_ragged_shapes(dk, dv, dtype):
     """Several chunks and a ragged tail, initial state and final-state
-    gradient present, every (dk, dv) the build covers."""
+    gradient present, every (dk, dv) the library covers."""
     inp, d_o, d_S = _case(2, 2, 200, dk, dv, dtype, seed=dk + dv)
     ref = oracle.backward(inp.q, inp.k, inp.v, inp.beta, d_o, inp.S0, d_S)
     _check(_gpu_grads(inp, d_o, d_S), ref, workloads.torch_dtype(dtype), f"{dtype} {dk}x{dv}")

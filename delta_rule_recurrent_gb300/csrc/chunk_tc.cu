@@ -1512,8 +1512,24 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
     static_assert(!(kGate && kRec), "no state recording on the gated form");
     for (int c = 0; c < nchunks; ++c) {
         const int g = c & 1;
-        if (c > 0 && !wg_wait(ctl, B_S_READY, (uint32_t)(c - 1), t, kBar)) return;
+        {   // the previous update done; gated: this chunk's decay vectors in too
+            // (their barrier's next phase needs this chunk's D1 MMAs, so the
+            // wait cannot see a phase two ahead, and it orders their bytes
+            // before the reads below)
+            bool ok = true;
+            if (t == 0) {
+                if (c > 0) ok = ctl.wait(B_S_READY, (uint32_t)(c - 1));
+                if (kGate && ok) ok = ctl.wait(B_TP_FULL + g, (uint32_t)(c >> 1));
+            }
+            if ((c > 0 || kGate) && wg_sync_or(kBar, !ok)) return;
+        }
         tc_fence_after_sync();
+        float keep = 1.f;
+        if constexpr (kGate) {  // read before the conversion's barrier, i.e. before D1 frees the slot
+            const float* const slot = sside + g * (kSideCopyBytes / 4);
+            keep = slot[128];
+            if (t < 16) reinterpret_cast<float4*>(sdec)[t] = reinterpret_cast<const float4*>(slot + 64)[t];
+        }
         // S^T -> bf16 (dk 0-63, then 64-127); S itself recorded when asked
         if constexpr (kRec) {
             float* const rec = S_chunks + ((size_t)bh * nchunks + c) * kD * kD + t;
@@ -1529,18 +1545,6 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         bool ok = true;
         if (t == 0)  // the o writer started D1^T with its v part once D1^T was free
             ok = ctl.wait(B_QW_READY + g, (uint32_t)(c >> 1)) && ctl.wait(B_VP_DONE, (uint32_t)c);
-        float keep = 1.f;
-        if constexpr (kGate) {
-            // [Q'; -W] written, so this chunk's decay vectors are in: the
-            // wait on their barrier returns at once (its next phase needs
-            // the D1 MMAs below) and orders their bytes before the reads.
-            if (t == 0 && ok) ok = ctl.wait(B_TP_FULL + g, (uint32_t)(c >> 1));
-            if (wg_sync_or(kBar, !ok)) return;
-            const float* const slot = sside + g * (kSideCopyBytes / 4);
-            keep = slot[128];
-            if (t < 16) reinterpret_cast<float4*>(sdec)[t] = reinterpret_cast<const float4*>(slot + 64)[t];
-            wg_sync(kBar);  // the slot is read before the D1 MMAs release it
-        }
         if (t == 0) {
             if (ok) {
                 tc_fence_after_sync();

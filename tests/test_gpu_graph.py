@@ -69,3 +69,26 @@ def test_chunk_fwd_replayed_from_a_graph_equal_eager(workspace):
         assert torch.equal(o_g, o_e)
         assert torch.equal(S_g, S_e)
     assert dn.load().dn_device_error() == 0
+
+
+def test_gated_tensor_core_call_replayed_from_a_graph_equals_eager():
+    """The gated two-pass call (decay-scaled tiles and decay vectors in the
+    caller's workspace) captured and replayed: the same bits as eager."""
+    B, H, T, d = 2, 4, 700, 128
+    inp = workloads.chunk_inputs(B, H, T, d, d, dtype="bf16", seed=9, s0_std=0.1)
+    q, k, v, b, S0 = (dev(x) for x in (inp.q, inp.k, inp.v, inp.beta, inp.S0))
+    g = dev(workloads.gate_inputs(B, H, T, seed=9, lo=0.5))
+    ws = torch.empty(dn.load().dn_chunk_fwd_gated_workspace_bytes(B, H, T, d, d, 64, 1),
+                     dtype=torch.uint8, device="cuda")
+    o_e, S_e = dn.chunk_fwd_gated(q, k, v, b, g, initial_state=S0, workspace=ws)
+    o_g, S_g = torch.zeros_like(o_e), torch.zeros_like(S_e)
+    gr = _capture(lambda: dn.chunk_fwd_gated(q, k, v, b, g, initial_state=S0, out=o_g,
+                                             final_state=S_g, workspace=ws))
+    for _ in range(2):
+        o_g.zero_()
+        S_g.zero_()
+        gr.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o_g, o_e)
+        assert torch.equal(S_g, S_e)
+    assert dn.load().dn_device_error() == 0

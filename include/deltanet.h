@@ -196,9 +196,11 @@ DN_API int dn_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
  * S0.  The pages run this pass after the forward and recompute the chunk
  * states instead of storing them ("Hardware-efficient implementation",
  * section 3 of paperlayer.ai/abs/2406.06484v6); the result is the exact
- * gradient of the recurrence up to rounding.  The gradient arithmetic is
- * fp32 on CUDA cores for both I/O types; the states are recomputed by the
- * tensor-core forward where it covers the shape (bf16, dk = dv = 128).
+ * gradient of the recurrence up to rounding.  Where the tensor-core forward
+ * covers the shape (bf16, dk = dv = 128) it recomputes the states and the
+ * chain of state gradients (last chunk to first) runs on tcgen05 with fp32
+ * accumulation; the per-chunk gradients run as fp32 CUDA-core products for
+ * fp32 I/O and as tf32 tensor-core products (fp32 accumulation) for bf16.
  *
  * Arguments:
  *   q, k, v, beta, S0   as for dn_chunk_fwd (S0 may be NULL: zeros)

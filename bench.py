@@ -166,13 +166,22 @@ def dist_env():
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest x over all ranks (the slowest rank's time): an all-reduce
+    on the process group's device (NCCL: the GPU, gloo: host memory)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank: float, seconds: float) -> float:
+    """Whole-job throughput of weak-scaling replicas: every rank processes the
+    same units, and the job takes as long as its slowest rank."""
+    return world * units_per_rank / seconds
 
 
 def barrier(world):
@@ -484,7 +493,7 @@ def run_ours(args, rank, world, local):
 
     # ---------------- numbers ----------------------------------------------
     tokens = B * T
-    value = world * tokens * args.steps / region_s
+    value = job_throughput(world, tokens * args.steps, region_s)
     launch_s = statistics.mean(per_launch) / 1e3
     flops = chunk_flops_per_token_head(C, dk, dv) * B * H * T
     cbytes = chunk_bytes(B, H, T, dk, dv, q.element_size(), False, True)

@@ -1,0 +1,67 @@
+"""The bench's multi-process path on CPU: two gloo ranks (world size 2).
+
+The operator shards over independent (batch, head) pairs with no exchange
+step, so under torchrun each rank runs the same per-GPU workload (replicas)
+and the only cross-rank operations are the timing barrier and the
+max-over-ranks reduction of the measured time.  These run here as gloo ranks
+on the host; the job's throughput is every rank's units over the slowest
+rank's time.
+"""
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        r, w, local = bench.dist_env()
+        bench.barrier(w)
+        seconds = 1.0 + 0.25 * r            # rank 1 is the slow one
+        slowest = bench.max_over_ranks(seconds, w)
+        bench.barrier(w)
+        out[r] = (r, w, local, slowest, bench.job_throughput(w, 1000.0, slowest))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_time_and_the_job_throughput():
+    world, port = 2, _free_port()
+    with mp.Manager() as manager:
+        out = manager.dict()
+        mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    assert sorted(res) == [0, 1]
+    for r, (rank, w, local, slowest, value) in res.items():
+        assert (rank, w, local) == (r, world, r)
+        assert slowest == pytest.approx(1.25)
+        assert value == pytest.approx(2 * 1000.0 / 1.25)
+
+
+def test_single_process_needs_no_process_group():
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    bench.barrier(1)
+    assert bench.job_throughput(1, 10.0, 2.0) == 5.0
+
+
+def test_reference_arm_runs_on_rank_zero_only(capsys):
+    """Under torchrun only rank 0 times the oracle and prints its line; any
+    other rank returns at once without work."""
+    import argparse
+    args = argparse.Namespace(steps=1, warmup=3)
+    assert bench.run_reference(args, rank=1, world=2) is None
+    assert capsys.readouterr().out == ""

@@ -1,0 +1,158 @@
+"""The regroupings the tensor-core kernels compute, pinned to the oracle.
+
+CPU only, fp64.  Each test walks a sequence chunk by chunk using exactly the
+products and operand blocks a kernel forms (not the kernel's code: numpy
+matrices in the same arrangement) and compares the result with the oracle's
+token-by-token recurrence, at a chunk length of 16 over 37 tokens (two full
+chunks and a ragged one) and dk != dv, so that a dropped term, a sign, a
+transposed block or a misplaced decay factor fails:
+
+- the forward scan: D1 = [PT; Tm] V - ([[PT, -I]; [Tm, 0]] [K; Q]) S, the
+  chunk group's one MMA chain and the D1 MMAs' negated operand;
+- the gated scan: the same with the decay-scaled blocks
+  [[PT E, -E]; [Tm E, 0]] (E = diag(exp G)), the keep factor exp(G_C) on the
+  state and exp(G_C - G_s) on U';
+- the backward chain: dV = PT^T dO + (K^T Tm)^T G, G <- G + Q^T dO - K^T dV,
+  reading the forward's [PT; Tm] transposed;
+- KDA on CUDA cores: the per-channel ratio as exp(G_i[d]) exp(-G_j[d]).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from tests.pins import _unit
+
+C = 16
+
+
+def _case(seed, T=37, dk=5, dv=7, gate=False, kda=False):
+    r = np.random.default_rng(seed)
+    q = _unit(r.standard_normal((1, 1, T, dk)))
+    k = _unit(r.standard_normal((1, 1, T, dk)))
+    v = r.standard_normal((1, 1, T, dv))
+    beta = r.uniform(0.05, 1.5, size=(1, 1, T))
+    S0 = r.standard_normal((1, 1, dk, dv)) * 0.5
+    g = None
+    if gate:
+        g = np.log(r.uniform(0.5, 1.0, size=(1, 1, T)))
+    if kda:
+        g = np.log(r.uniform(0.5, 1.0, size=(1, 1, T, dk)))
+    return q, k, v, beta, S0, g
+
+
+def _chunk_tiles(K, Q, bt, ratio=None):
+    """[PT; Tm] as the prepare pass forms it (ratio: in-chunk decay)."""
+    n = K.shape[0]
+    KK, QK = K @ K.T, Q @ K.T
+    if ratio is not None:
+        KK, QK = KK * ratio, QK * ratio
+    A = np.tril(bt[:, None] * KK, -1)
+    Tm = np.linalg.solve(np.eye(n) + A, np.diag(bt))
+    P = np.tril(QK)
+    return P @ Tm, Tm
+
+
+def _rel(a, b):
+    return float(np.max(np.abs(a - b)) / max(1.0, float(np.max(np.abs(b)))))
+
+
+def test_forward_scan_regrouping():
+    q, k, v, beta, S0, _ = _case(1)
+    K_, Q_, V_, b_ = k[0, 0], q[0, 0], v[0, 0], beta[0, 0]
+    S = S0[0, 0].copy()
+    o = np.zeros_like(V_)
+    for t0 in range(0, K_.shape[0], C):
+        sl = slice(t0, t0 + C)
+        K, Q, V, bt = K_[sl], Q_[sl], V_[sl], b_[sl]
+        n = K.shape[0]
+        PT, Tm = _chunk_tiles(K, Q, bt)
+        left = np.vstack([PT, Tm])                                    # [PT; Tm]
+        Ablk = np.block([[PT, -np.eye(n)], [Tm, np.zeros((n, n))]])   # the chain's A
+        negQW = Ablk @ np.vstack([K, Q])                              # [-Q'; W]
+        D1 = left @ V - negQW @ S                                     # negated B operand
+        o[sl] = D1[:n]
+        S = S + K.T @ D1[n:]                                          # S += K^T U'
+    o_ref, S_ref = oracle.forward(q, k, v, beta, S0)
+    assert _rel(o, o_ref[0, 0]) < 1e-10
+    assert _rel(S, S_ref[0, 0]) < 1e-10
+
+
+def test_gated_scan_regrouping():
+    q, k, v, beta, S0, g = _case(2, gate=True)
+    K_, Q_, V_, b_, g_ = k[0, 0], q[0, 0], v[0, 0], beta[0, 0], g[0, 0]
+    S = S0[0, 0].copy()
+    o = np.zeros_like(V_)
+    for t0 in range(0, K_.shape[0], C):
+        sl = slice(t0, t0 + C)
+        K, Q, V, bt = K_[sl], Q_[sl], V_[sl], b_[sl]
+        n = K.shape[0]
+        G = np.cumsum(g_[sl])
+        ratio = np.exp(np.minimum(G[:, None] - G[None, :], 0.0))
+        PT, Tm = _chunk_tiles(K, Q, bt, ratio)
+        E = np.diag(np.exp(G))
+        Ablk = np.block([[PT @ E, -E], [Tm @ E, np.zeros((n, n))]])
+        negQW = Ablk @ np.vstack([K, Q])
+        D1 = np.vstack([PT, Tm]) @ V - negQW @ S
+        o[sl] = D1[:n]
+        dec = np.exp(G[-1] - G)
+        S = np.exp(G[-1]) * S + K.T @ (dec[:, None] * D1[n:])
+    o_ref, S_ref = oracle.forward_gated(q, k, v, beta, g, S0)
+    assert _rel(o, o_ref[0, 0]) < 1e-10
+    assert _rel(S, S_ref[0, 0]) < 1e-10
+
+
+def test_backward_chain_regrouping():
+    """The chain's dV and state gradients; the oracle's d_v and d_S0."""
+    q, k, v, beta, S0, _ = _case(3)
+    r = np.random.default_rng(33)
+    dO = r.standard_normal(v.shape)
+    dS_T = r.standard_normal(S0.shape)
+    K_, Q_, V_, b_, dO_ = k[0, 0], q[0, 0], v[0, 0], beta[0, 0], dO[0, 0]
+    T = K_.shape[0]
+    starts = list(range(0, T, C))
+    tiles = [_chunk_tiles(K_[t0:t0 + C], Q_[t0:t0 + C], b_[t0:t0 + C]) for t0 in starts]
+    G = dS_T[0, 0].copy()
+    dV = np.zeros_like(V_)
+    for t0, (PT, Tm) in reversed(list(zip(starts, tiles))):
+        sl = slice(t0, t0 + C)
+        K, Q, D = K_[sl], Q_[sl], dO_[sl]
+        B2 = K.T @ Tm                       # the chunk group's tile (dk x tokens)
+        dVc = PT.T @ D + B2.T @ G           # dV^T = dO^T PT + G^T (K^T Tm)
+        dV[sl] = dVc
+        G = G + Q.T @ D - K.T @ dVc         # G^T += dO^T Q - dV^T K
+    ref = oracle.backward(q, k, v, beta, dO, S0, dS_T)
+    assert _rel(dV, ref[2][0, 0]) < 1e-9
+    assert _rel(G, ref[4][0, 0]) < 1e-9
+
+
+@pytest.mark.parametrize("scale", [1.0, 40.0], ids=["mild", "strong"])
+def test_kda_separable_ratio(scale):
+    """A and P from K exp(G), Q exp(G) and K exp(-G), against the per-entry
+    ratio inside the sums, and the whole KDA chunk walk against the oracle
+    (strong: G reaches about -40 per channel inside a chunk, still normal)."""
+    q, k, v, beta, S0, g = _case(4, kda=True)
+    g = g * scale
+    K_, Q_, V_, b_, g_ = k[0, 0], q[0, 0], v[0, 0], beta[0, 0], g[0, 0]
+    S = S0[0, 0].copy()
+    o = np.zeros_like(V_)
+    for t0 in range(0, K_.shape[0], C):
+        sl = slice(t0, t0 + C)
+        K, Q, V, bt = K_[sl], Q_[sl], V_[sl], b_[sl]
+        n = K.shape[0]
+        Gk = np.cumsum(g_[sl], axis=0)                      # [n][dk]
+        Kp, Km, Qp = K * np.exp(Gk), K * np.exp(-Gk), Q * np.exp(Gk)
+        A_sep, P_sep = Kp @ Km.T, Qp @ Km.T
+        ratio = np.exp(np.minimum(Gk[:, None, :] - Gk[None, :, :], 0.0))
+        A_dir = np.einsum("id,jd,ijd->ij", K, K, ratio)
+        mask = np.tril(np.ones((n, n)), -1).astype(bool)
+        assert np.allclose(A_sep[mask], A_dir[mask], rtol=1e-9, atol=1e-12)
+        A = np.tril(bt[:, None] * A_sep, -1)
+        P = np.tril(P_sep)
+        Tm = np.linalg.solve(np.eye(n) + A, np.diag(bt))
+        U = Tm @ (V - Kp @ S)
+        o[sl] = Qp @ S + P @ U
+        eC = np.exp(Gk[-1])
+        S = eC[:, None] * S + (Km * eC).T @ U
+    o_ref, S_ref = oracle.forward_kda(q, k, v, beta, g, S0)
+    assert _rel(o, o_ref[0, 0]) < 1e-9
+    assert _rel(S, S_ref[0, 0]) < 1e-9

@@ -15,6 +15,8 @@ transposed block or a misplaced decay factor fails:
 - the backward chain: dV = PT^T dO + (K^T Tm)^T G, G <- G + Q^T dO - K^T dV,
   reading the forward's [PT; Tm] transposed;
 - KDA on CUDA cores: the per-channel ratio as exp(G_i[d]) exp(-G_j[d]).
+- the per-chunk gradients in feature-lane form (the layout a tcgen05
+  gradient kernel takes), dP and dTm as diagonal blocks of one product.
 """
 import numpy as np
 import pytest
@@ -156,3 +158,59 @@ def test_kda_separable_ratio(scale):
     o_ref, S_ref = oracle.forward_kda(q, k, v, beta, g, S0)
     assert _rel(o, o_ref[0, 0]) < 1e-9
     assert _rel(S, S_ref[0, 0]) < 1e-9
+
+
+def test_gradient_kernel_feature_lane_plan():
+    """The per-chunk gradients in the feature-lane form a tcgen05 gradient
+    kernel would use (every product with a 128-wide feature dimension as M):
+    R^T = V^T - S^T K^T, U'^T = R^T Tm^T, dU'^T = dO^T P + G^T K^T,
+    dV^T = dU'^T Tm, dP and dTm as the diagonal blocks of one product
+    [dO; dU'] [U'; R]^T, dQ^T = S dO^T + K^T dP^T and
+    dK^T = Q^T dP + G U'^T - S dV^T + K^T Z; against the oracle's gradient."""
+    q, k, v, beta, S0, _ = _case(5)
+    r = np.random.default_rng(55)
+    dO = r.standard_normal(v.shape)
+    dS_T = r.standard_normal(S0.shape)
+    K_, Q_, V_, b_, dO_ = k[0, 0], q[0, 0], v[0, 0], beta[0, 0], dO[0, 0]
+    T = K_.shape[0]
+    starts = list(range(0, T, C))
+    S_at, S = [], S0[0, 0].copy()
+    for t0 in starts:  # the states at chunk starts (the recompute)
+        sl = slice(t0, t0 + C)
+        _, Tm = _chunk_tiles(K_[sl], Q_[sl], b_[sl])
+        S_at.append(S)
+        S = S + K_[sl].T @ (Tm @ (V_[sl] - K_[sl] @ S))
+    G_end, G = [None] * len(starts), dS_T[0, 0].copy()
+    for i in reversed(range(len(starts))):  # the chain: G at every chunk end
+        sl = slice(starts[i], starts[i] + C)
+        PT, Tm = _chunk_tiles(K_[sl], Q_[sl], b_[sl])
+        G_end[i] = G
+        dVc = PT.T @ dO_[sl] + (K_[sl].T @ Tm).T @ G
+        G = G + Q_[sl].T @ dO_[sl] - K_[sl].T @ dVc
+    dq, dk, dv, db = (np.zeros_like(Q_), np.zeros_like(K_), np.zeros_like(V_),
+                      np.zeros_like(b_))
+    for i, t0 in enumerate(starts):
+        sl = slice(t0, t0 + C)
+        K, Q, V, D, bt, S, G = K_[sl], Q_[sl], V_[sl], dO_[sl], b_[sl], S_at[i], G_end[i]
+        n = K.shape[0]
+        KK = K @ K.T
+        X = np.linalg.inv(np.eye(n) + np.tril(bt[:, None] * KK, -1))
+        Tm = X * bt[None, :]
+        P = np.tril(Q @ K.T)
+        Rt = V.T - S.T @ K.T                       # dv x n
+        Ut = Rt @ Tm.T                             # U'^T
+        dUt = D.T @ P + G.T @ K.T                  # dU'^T
+        dVt = dUt @ Tm                             # dV^T
+        D5 = np.vstack([D, dUt.T]) @ np.vstack([Ut.T, Rt.T]).T
+        dP = np.tril(D5[:n, :n])
+        dTm = D5[n:, n:]
+        M1 = (dTm * bt[None, :]) @ X.T
+        dA = np.tril(-X.T @ M1, -1)
+        Z = bt[:, None] * dA + (bt[:, None] * dA).T
+        dQt = S @ D.T + K.T @ dP.T                 # dk x n
+        dKt = Q.T @ dP + G @ Ut - S @ dVt + K.T @ Z
+        dq[sl], dk[sl], dv[sl] = dQt.T, dKt.T, dVt.T
+        db[sl] = np.sum(X * dTm, axis=0) + np.sum(dA * KK, axis=1)
+    ref = oracle.backward(q, k, v, beta, dO, S0, dS_T)
+    for got, want in zip((dq, dk, dv, db), ref[:4]):
+        assert _rel(got, want[0, 0]) < 1e-9

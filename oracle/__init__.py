@@ -72,6 +72,10 @@ def _load():
         lib.dn_oracle_forward_gated.restype = ctypes.c_int
         lib.dn_oracle_forward_kda.argtypes = [dp] * 7 + [ctypes.c_long] * 4 + [ctypes.c_int]
         lib.dn_oracle_forward_kda.restype = ctypes.c_int
+        lib.dn_oracle_prepare_rows.argtypes = [dp, dp, ctypes.c_long, ctypes.c_long,
+                                               ctypes.c_int, ctypes.c_double,
+                                               ctypes.c_double]
+        lib.dn_oracle_prepare_rows.restype = None
         _lib = lib
     return _lib
 
@@ -280,3 +284,21 @@ def recurrent_step_kda(q, k, v, beta, g, S, nthreads: int | None = None):
     o, S_new = forward_kda(q[:, :, None, :], k[:, :, None, :], v[:, :, None, :],
                            beta[:, :, None], g[:, :, None, :], S, nthreads=nthreads)
     return o[:, :, 0, :], S_new
+
+
+def prepare_qk(q, k, scale: float = 1.0, l2norm: bool = False, eps: float = 1e-6):
+    """The optional input preparation, in fp64: with ``l2norm`` every row of
+    q and k (the last axis, the head dimension) becomes x / sqrt(sum x^2 + eps);
+    then q is multiplied by ``scale``; k is never scaled.  Any leading shape.
+    Returns ``(q', k')`` as fp64 numpy arrays; feed them to any form above."""
+    q, k = _f64(q), _f64(k)
+    if q.shape != k.shape or q.ndim < 1:
+        raise ValueError("q and k must have the same shape")
+    d = q.shape[-1]
+    rows = q.size // d if d else 0
+    qo, ko = np.empty_like(q), np.empty_like(k)
+    lib = _load()
+    lib.dn_oracle_prepare_rows(_ptr(q), _ptr(qo), rows, d, int(l2norm), float(scale),
+                               float(eps))
+    lib.dn_oracle_prepare_rows(_ptr(k), _ptr(ko), rows, d, int(l2norm), 1.0, float(eps))
+    return qo, ko

@@ -373,3 +373,38 @@ int dn_oracle_forward_kda(const double *q, const double *k, const double *v,
     }
     return failed ? -1 : 0;
 }
+
+/*
+ * Optional input preparation ahead of any of the forms above, one row of
+ * length d at a time:
+ *
+ *   normalised   y = x / sqrt(sum_i x_i^2 + eps)     (when normalize != 0)
+ *   scaled       y = scale * y
+ *
+ * The normalisation is the l2norm helper of the Gated DeltaNet PyTorch code
+ * on "DeltaNet 引入 Delta Rule" (garden.houmin.site/infra/delta-net), which
+ * normalises queries and keys over the head dimension with eps = 1e-6 and
+ * divides the queries by the square root of the head dimension; the layer of
+ * "fla/layers/delta_net.py" asks its kernels for the same normalisation
+ * (use_qk_l2norm_in_kernel).  The KDA read of "Kimi Delta Attention"
+ * (fr.news.hada.io/topic?id=31925) scales q by d_k^{-1/2}.  The queries get
+ * the scale, the keys do not.
+ *   x, y   [rows][d]   (y may equal x)
+ */
+void dn_oracle_prepare_rows(const double *x, double *y, long rows, long d,
+                            int normalize, double scale, double eps)
+{
+    for (long r = 0; r < rows; ++r) {
+        const double *xr = x + r * d;
+        double *yr = y + r * d;
+        double f = scale;
+        if (normalize) {
+            double ss = 0.0;
+            for (long i = 0; i < d; ++i)
+                ss += xr[i] * xr[i];
+            f = scale / sqrt(ss + eps);
+        }
+        for (long i = 0; i < d; ++i)
+            yr[i] = xr[i] * f;
+    }
+}

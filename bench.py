@@ -402,6 +402,20 @@ def run_ours(args, rank, world, local):
         vl_region_s = max_over_ranks(vl_region_s, world)
         del vq, vk, vv, vb, vws
 
+        # ---------------- q/k preparation: L2 norm + query scale ------------
+        qc, kc = q.clone(), k.clone()
+
+        def prep_step(_i):  # in place: idempotent once normalised, same traffic
+            dn.qk_prepare(qc, kc, scale=dk ** -0.5, l2norm=True, inplace=True)
+
+        psteps = max(1, min(args.steps, 20))
+        for i in range(min(args.warmup, 3)):
+            prep_step(i)
+        torch.cuda.synchronize()
+        pr_region_s, pr_launch = timed_loop(prep_step, psteps, stream, world)
+        pr_region_s = max_over_ranks(pr_region_s, world)
+        del qc, kc
+
         # ---------------- Gated DeltaNet: chunk forward and decode step -----
         gate = workloads.gate_inputs(B, H, T, seed=w["seed"]).to(dev)
         og = torch.empty_like(o)
@@ -578,6 +592,18 @@ def run_ours(args, rank, world, local):
                                 "unit": "TFLOP/s",
                                 "frac": flops / vl_launch_s / 1e12 / peaks["bf16_tflops"]}},
     }
+    pr_launch_s = statistics.mean(pr_launch) / 1e3
+    pbytes = 4 * B * H * T * dk * q.element_size()  # q and k read once and written once
+    qk_prep = {
+        "workload": HEADLINE, "steps": psteps, "value": world * tokens * psteps / pr_region_s,
+        "unit": "tokens/s", "ms_per_step": 1e3 * pr_region_s / psteps,
+        "op": "q, k <- x / sqrt(sum x^2 + 1e-6) per row; q *= dk^-0.5 (in place)",
+        "roofline": {"bound": "hbm", "achieved": pbytes / pr_launch_s / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": pbytes / pr_launch_s / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{peak_src} (copy bandwidth)", "bytes_per_launch": pbytes,
+                     "launch_us": pr_launch_s * 1e6},
+    }
     g_launch_s = statistics.mean(g_launch) / 1e3
     gs_launch_s = statistics.mean(gs_launch) / 1e3
     gflops = chunk_flops_per_token_head(C, dk, dv) * B * H * T
@@ -665,14 +691,19 @@ def run_ours(args, rank, world, local):
         "decode": decode,
         "backward": backward,
         "varlen": varlen,
+        "qk_prepare": qk_prep,
         "gated": gated,
         "kda": kda,
         "e2e": {"value": world * tokens * e2e_steps / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": 1e3 * e2e_s / e2e_steps},
-        "gpu_launches": launches_per_call * (args.steps + e2e_steps) + nsteps
-                        + (nsteps if dec_graph[0] else 0) + 3 * bwd_steps + gsteps + nsteps
-                        + launches_per_call * vsteps + gsteps + nsteps,
+        "gpu_launches": (launches_per_call * (args.steps + e2e_steps)   # chunk forward, e2e
+                         + nsteps + (nsteps if dec_graph[0] else 0)     # decode, graph replay
+                         + (4 if tc else 3) * bwd_steps                 # recompute, chain, grads
+                         + launches_per_call * vsteps                   # varlen
+                         + psteps                                       # q/k preparation
+                         + (2 if gneed else 1) * gsteps + gsteps + nsteps  # gated: both forms, decode
+                         + gsteps + nsteps),                            # KDA chunk, decode
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

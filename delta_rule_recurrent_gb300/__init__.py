@@ -16,10 +16,13 @@ the computation runs in the library's sm_103a kernels.
         # Gated DeltaNet: log keep rate g per token (per head for a step)
     chunk_fwd_kda(q, k, v, beta, g, ...), recurrent_step_kda(q, k, v, beta, g, state)
         # KDA: one log keep rate per key channel
+    qk_prepare(q, k, scale=1.0, l2norm=True)  # optional q/k L2-norm and query scale
 
 Shapes: q, k ``[B, H, T, dk]``; v ``[B, H, T, dv]``; beta ``[B, H, T]``;
 state ``[B, H, dk, dv]`` fp32 (the pages' dv x dk state, transposed).  For a
-decoding step the T axis is absent.  q and k must already be L2-normalised.
+decoding step the T axis is absent.  q and k are used as given unless a
+forward is called with ``qk_l2norm=True`` and/or ``scale=...``, which run
+``qk_prepare`` on them first (the backward takes prepared q and k).
 """
 from __future__ import annotations
 
@@ -29,7 +32,7 @@ from ._lib import (DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05, DN_BF16, DN_F32,
                    DeltaNetError, check, header_symbols, lib_path, load)
 
 __all__ = ["chunk_fwd", "chunk_bwd", "recurrent_step", "chunk_fwd_varlen", "chunk_fwd_gated",
-           "recurrent_step_gated", "chunk_fwd_kda", "recurrent_step_kda", "DeltaRule", "DeltaNetError", "load", "lib_path",
+           "recurrent_step_gated", "chunk_fwd_kda", "recurrent_step_kda", "qk_prepare", "DeltaRule", "DeltaNetError", "load", "lib_path",
            "header_symbols", "ALGOS"]
 
 ALGOS = {"auto": DN_ALGO_AUTO, "simt": DN_ALGO_SIMT, "tcgen05": DN_ALGO_TCGEN05}
@@ -55,10 +58,42 @@ def _stream_handle(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
+def qk_prepare(q: torch.Tensor, k: torch.Tensor, scale: float = 1.0, l2norm: bool = True,
+               eps: float = 1e-6, inplace: bool = False):
+    """Optional input preparation (``dn_qk_prepare``): with ``l2norm`` every
+    row of q and k (the last axis) becomes x / sqrt(sum x^2 + eps); q is then
+    multiplied by ``scale``.  Returns ``(q', k')``, new tensors unless
+    ``inplace``; without ``l2norm`` k is returned as it is."""
+    dev = q.device
+    _check_cuda("q", q, dev)
+    _check_cuda("k", k, dev)
+    dt = _dtype_code(q)
+    if k.dtype != q.dtype or k.shape != q.shape or q.dim() < 1:
+        raise ValueError("q and k must share one shape and dtype")
+    d = q.shape[-1]
+    rows = q.numel() // d if d else 0
+    q_out = q if inplace else torch.empty_like(q)
+    k_out = k if (inplace or not l2norm) else torch.empty_like(k)
+    lib = load()
+    with torch.cuda.device(dev):
+        check(lib.dn_qk_prepare(q.data_ptr(), k.data_ptr(), q_out.data_ptr(), k_out.data_ptr(),
+                                rows, d, int(bool(l2norm)), float(scale), float(eps), dt,
+                                _stream_handle(dev)))
+    return q_out, k_out
+
+
+def _prepared(q, k, scale, qk_l2norm):
+    """q and k after the optional preparation a forward was asked for."""
+    if scale is None and not qk_l2norm:
+        return q, k
+    return qk_prepare(q, k, 1.0 if scale is None else scale, bool(qk_l2norm))
+
+
 def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
               initial_state: torch.Tensor | None = None, output_final_state: bool = True,
               chunk_size: int = 64, algo: str = "auto", out: torch.Tensor | None = None,
-              final_state: torch.Tensor | None = None, workspace="auto"):
+              final_state: torch.Tensor | None = None, workspace="auto",
+              scale: float | None = None, qk_l2norm: bool = False):
     """Chunkwise delta-rule forward (``dn_chunk_fwd``).
 
     Returns ``(o, S_T)``; ``S_T`` is None when ``output_final_state`` is
@@ -67,11 +102,13 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Ten
     allocates the scratch ``dn_chunk_fwd_workspace_bytes`` asks for (the
     two-pass tensor-core path), None runs without scratch (one fused kernel),
     and a uint8 CUDA tensor of at least that many bytes is used as given.
+    ``qk_l2norm`` / ``scale`` run ``qk_prepare`` on q and k first.
     """
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
         _check_cuda(name, t, dev)
     dt = _dtype_code(q)
+    q, k = _prepared(q, k, scale, qk_l2norm)
     if not (k.dtype == v.dtype == beta.dtype == q.dtype):
         raise TypeError("q, k, v and beta must share one dtype")
     if q.dim() != 4 or k.shape != q.shape or v.dim() != 4:
@@ -120,13 +157,16 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Ten
 
 
 def recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
-                   state: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+                   state: torch.Tensor, out: torch.Tensor | None = None,
+                   scale: float | None = None, qk_l2norm: bool = False) -> torch.Tensor:
     """One fused decoding step (``dn_recurrent_step``); ``state`` is updated
-    in place and the step's output ``o`` ``[B, H, dv]`` is returned."""
+    in place and the step's output ``o`` ``[B, H, dv]`` is returned.
+    ``qk_l2norm`` / ``scale`` run ``qk_prepare`` on q and k first."""
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("state", state)):
         _check_cuda(name, t, dev)
     dt = _dtype_code(q)
+    q, k = _prepared(q, k, scale, qk_l2norm)
     if not (k.dtype == v.dtype == beta.dtype == q.dtype):
         raise TypeError("q, k, v and beta must share one dtype")
     if q.dim() != 3 or k.shape != q.shape or v.dim() != 3:
@@ -233,32 +273,37 @@ def chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: tor
                     g: torch.Tensor, initial_state: torch.Tensor | None = None,
                     output_final_state: bool = True, chunk_size: int = 64,
                     out: torch.Tensor | None = None, final_state: torch.Tensor | None = None,
-                    workspace="auto"):
+                    workspace="auto", scale: float | None = None, qk_l2norm: bool = False):
     """Gated DeltaNet, chunkwise (``dn_chunk_fwd_gated``): ``g`` is the fp32
     ``[B, H, T]`` log keep rate.  Returns ``(o, S_T)`` as ``chunk_fwd``.
     ``workspace``: "auto" allocates the scratch of the two-pass tensor-core
     form where it applies (``dn_chunk_fwd_gated_workspace_bytes``), None runs
-    the fp32 CUDA-core kernel, a uint8 CUDA tensor supplies the scratch."""
+    the fp32 CUDA-core kernel, a uint8 CUDA tensor supplies the scratch.
+    ``qk_l2norm`` / ``scale`` run ``qk_prepare`` on q and k first."""
     return _chunk_decayed(q, k, v, beta, g, False, initial_state, output_final_state,
-                          chunk_size, out, final_state, workspace)
+                          chunk_size, out, final_state, workspace, scale, qk_l2norm)
 
 
 def chunk_fwd_kda(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
                   g: torch.Tensor, initial_state: torch.Tensor | None = None,
                   output_final_state: bool = True, chunk_size: int = 64,
-                  out: torch.Tensor | None = None, final_state: torch.Tensor | None = None):
+                  out: torch.Tensor | None = None, final_state: torch.Tensor | None = None,
+                  scale: float | None = None, qk_l2norm: bool = False):
     """Kimi Delta Attention, chunkwise (``dn_chunk_fwd_kda``): ``g`` is the
-    fp32 ``[B, H, T, dk]`` per-key-channel log keep rate."""
+    fp32 ``[B, H, T, dk]`` per-key-channel log keep rate.  The page's read
+    scales q by d_k^{-1/2}: ``scale=dk ** -0.5`` applies it.
+    ``qk_l2norm`` / ``scale`` run ``qk_prepare`` on q and k first."""
     return _chunk_decayed(q, k, v, beta, g, True, initial_state, output_final_state,
-                          chunk_size, out, final_state, None)
+                          chunk_size, out, final_state, None, scale, qk_l2norm)
 
 
 def _chunk_decayed(q, k, v, beta, g, per_channel, initial_state, output_final_state,
-                   chunk_size, out, final_state, workspace):
+                   chunk_size, out, final_state, workspace, scale=None, qk_l2norm=False):
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
         _check_cuda(name, t, dev)
     dt = _dtype_code(q)
+    q, k = _prepared(q, k, scale, qk_l2norm)
     if not (k.dtype == v.dtype == beta.dtype == q.dtype):
         raise TypeError("q, k, v and beta must share one dtype")
     if q.dim() != 4 or k.shape != q.shape or v.dim() != 4:
@@ -303,25 +348,30 @@ def _chunk_decayed(q, k, v, beta, g, per_channel, initial_state, output_final_st
 
 def recurrent_step_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
                          g: torch.Tensor, state: torch.Tensor,
-                         out: torch.Tensor | None = None) -> torch.Tensor:
+                         out: torch.Tensor | None = None, scale: float | None = None,
+                         qk_l2norm: bool = False) -> torch.Tensor:
     """One Gated DeltaNet decoding step (``dn_recurrent_step_gated``); ``g``
-    is the fp32 ``[B, H]`` log keep rate; ``state`` is updated in place."""
-    return _step_decayed(q, k, v, beta, g, False, state, out)
+    is the fp32 ``[B, H]`` log keep rate; ``state`` is updated in place.
+    ``qk_l2norm`` / ``scale`` run ``qk_prepare`` on q and k first."""
+    return _step_decayed(q, k, v, beta, g, False, state, out, scale, qk_l2norm)
 
 
 def recurrent_step_kda(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
                        g: torch.Tensor, state: torch.Tensor,
-                       out: torch.Tensor | None = None) -> torch.Tensor:
+                       out: torch.Tensor | None = None, scale: float | None = None,
+                       qk_l2norm: bool = False) -> torch.Tensor:
     """One KDA decoding step (``dn_recurrent_step_kda``); ``g`` is the fp32
-    ``[B, H, dk]`` per-key-channel log keep rate; ``state`` updated in place."""
-    return _step_decayed(q, k, v, beta, g, True, state, out)
+    ``[B, H, dk]`` per-key-channel log keep rate; ``state`` updated in place.
+    ``qk_l2norm`` / ``scale`` run ``qk_prepare`` on q and k first."""
+    return _step_decayed(q, k, v, beta, g, True, state, out, scale, qk_l2norm)
 
 
-def _step_decayed(q, k, v, beta, g, per_channel, state, out):
+def _step_decayed(q, k, v, beta, g, per_channel, state, out, scale=None, qk_l2norm=False):
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("state", state)):
         _check_cuda(name, t, dev)
     dt = _dtype_code(q)
+    q, k = _prepared(q, k, scale, qk_l2norm)
     B, H, dk = q.shape
     dv = v.shape[2]
     _check_gate(g, (B, H, dk) if per_channel else (B, H), dev)
@@ -340,7 +390,7 @@ def _step_decayed(q, k, v, beta, g, per_channel, state, out):
 def chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
                      cu_seqlens, initial_state: torch.Tensor | None = None,
                      output_final_state: bool = True, chunk_size: int = 64,
-                     workspace="auto"):
+                     workspace="auto", scale: float | None = None, qk_l2norm: bool = False):
     """Packed variable-length sequences (``dn_chunk_fwd_varlen``).
 
     q, k ``[H, T, dk]``, v ``[H, T, dv]``, beta ``[H, T]`` hold N sequences
@@ -348,12 +398,14 @@ def chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
     offsets.  Returns ``(o [H, T, dv], S_T [N, H, dk, dv] or None)``.
     ``workspace``: "auto" (the two-pass tensor-core path where it applies),
     None (the CUDA-core path) or a uint8 CUDA tensor.
+    ``qk_l2norm`` / ``scale`` run ``qk_prepare`` on q and k first.
     """
     import ctypes
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
         _check_cuda(name, t, dev)
     dt = _dtype_code(q)
+    q, k = _prepared(q, k, scale, qk_l2norm)
     if not (k.dtype == v.dtype == beta.dtype == q.dtype):
         raise TypeError("q, k, v and beta must share one dtype")
     if q.dim() != 3 or k.shape != q.shape or v.dim() != 3:

@@ -44,6 +44,8 @@ SIGNATURES = {
     "dn_recurrent_step_gated": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp] + [_int] * 5 + [_vp]),
     "dn_chunk_fwd_kda": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp] + [_int] * 7 + [_vp]),
     "dn_recurrent_step_kda": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp] + [_int] * 5 + [_vp]),
+    "dn_qk_prepare": (_int, [_vp, _vp, _vp, _vp, ctypes.c_longlong, _int, _int, ctypes.c_float,
+                              ctypes.c_float, _int, _vp]),
     "dn_status_string": (ctypes.c_char_p, [_int]),
     "dn_last_error": (ctypes.c_char_p, []),
     "dn_abi_version": (_int, []),
@@ -90,7 +92,7 @@ def load(path: Path | None = None):
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)
         fn.restype, fn.argtypes = res, args
-    if lib.dn_abi_version() != 2:
+    if lib.dn_abi_version() != 3:
         raise RuntimeError("libdeltanet ABI version mismatch")
     if path is None:
         _lib = lib

@@ -1,5 +1,6 @@
 // api.cu -- the C ABI declared in include/deltanet.h: argument checks and
 // dispatch.  Every check runs on the host before anything is enqueued.
+#include <math.h>
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -518,6 +519,39 @@ int dn_recurrent_step(const void* q, const void* k, const void* v, const void* b
     return cuda_status(dn::launch_recurrent_step(q, k, v, beta, S, o, (int)BH, dk, dv, dt,
                                                  static_cast<cudaStream_t>(stream)),
                        "recurrent step launch");
+}
+
+int dn_qk_prepare(const void* q, const void* k, void* q_out, void* k_out, long long rows,
+                  int d, int normalize, float scale, float eps, int dt, void* stream) {
+    if (rows < 0) return fail(DN_ERR_INVALID_ARG, "negative row count %lld", rows);
+    if (rows > (1LL << 40)) return fail(DN_ERR_INVALID_ARG, "row count %lld too large", rows);
+    if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
+    if (d <= 0) return fail(DN_ERR_INVALID_ARG, "d must be positive");
+    if (!supported_dim(d))
+        return fail(DN_ERR_UNSUPPORTED, "d=%d: this library supports 64 and 128", d);
+    if (!isfinite(scale)) return fail(DN_ERR_INVALID_ARG, "scale must be finite");
+    if (!isfinite(eps) || eps < 0.0f)
+        return fail(DN_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (rows == 0) return ok();
+    const size_t bytes = (size_t)rows * d * elem_size(dt);
+    const Span sq{"q", q, bytes}, sqo{"q_out", q_out, bytes}, sk{"k", k, bytes},
+        sko{"k_out", k_out, bytes};
+    int dev = 0;
+    if (int st = current_device(&dev)) return st;
+    for (const Span* s : {&sq, &sqo})
+        if (int st = check_device_ptr(*s, 16, dev)) return st;
+    if (q_out != q && overlaps(sqo, sq)) return fail(DN_ERR_INVALID_ARG, "q_out overlaps q");
+    if (normalize) {
+        for (const Span* s : {&sk, &sko})
+            if (int st = check_device_ptr(*s, 16, dev)) return st;
+        if (k_out != k && overlaps(sko, sk)) return fail(DN_ERR_INVALID_ARG, "k_out overlaps k");
+        if (overlaps(sqo, sk)) return fail(DN_ERR_INVALID_ARG, "q_out overlaps k");
+        if (overlaps(sko, sq)) return fail(DN_ERR_INVALID_ARG, "k_out overlaps q");
+        if (overlaps(sqo, sko)) return fail(DN_ERR_INVALID_ARG, "q_out overlaps k_out");
+    }
+    return cuda_status(dn::launch_qk_prepare(q, k, q_out, k_out, rows, d, normalize ? 1 : 0,
+                                             scale, eps, dt, static_cast<cudaStream_t>(stream)),
+                       "q/k preparation launch");
 }
 
 size_t dn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt) {

@@ -29,6 +29,13 @@ cudaError_t launch_recurrent_step(const void* q, const void* k, const void* v,
                                   int dk, int dv, int dt, cudaStream_t stream,
                                   const float* g = nullptr, int g_per_channel = 0);
 
+// Optional input preparation (see dn_qk_prepare): rows of d (64 or 128)
+// elements; q rows scaled by `scale` (after the L2 normalisation when
+// normalize != 0), k rows normalised (only when normalize != 0).
+cudaError_t launch_qk_prepare(const void* q, const void* k, void* q_out, void* k_out,
+                              long long rows, int d, int normalize, float scale, float eps,
+                              int dt, cudaStream_t stream);
+
 // Chunkwise forward with fp32 CUDA-core arithmetic (any T >= 1).  o may be
 // nullptr (no outputs); S_chunks, if given, receives the state at the start
 // of every chunk ([BH][ceil(T/64)][dk][dv] fp32), for the backward pass; g,

@@ -21,9 +21,9 @@
  *     synchronises, and enqueues its kernels on `stream` (a cudaStream_t;
  *     NULL means the legacy default stream).  Results are ready when the
  *     stream reaches them.
- *   - q and k are used as given (the caller L2-normalises them); there is no
- *     query scale; beta is used as given (0..1, or 0..2 for the
- *     negative-eigenvalue variant), with no clamping.
+ *   - q and k are used as given: the caller L2-normalises them and applies
+ *     any query scale, or runs dn_qk_prepare first.  beta is used as given
+ *     (0..1, or 0..2 for the negative-eigenvalue variant), with no clamping.
  *   - Arguments are checked on the host before anything is enqueued; a
  *     rejected call enqueues nothing.  Kernels have no device traps and no
  *     unbounded waits.  Launch failures are reported as DN_ERR_CUDA.
@@ -334,10 +334,46 @@ DN_API int dn_recurrent_step_kda(const void *q, const void *k, const void *v,
                           const void *beta, const float *g, float *S, void *o,
                           int B, int H, int dk, int dv, int dt, void *stream);
 
+/*
+ * dn_qk_prepare -- optional input preparation for every entry point above:
+ * the query/key L2 normalisation and query scale that the pages apply
+ * before the recurrence.  Per row of d elements (the head dimension):
+ *     q_out = scale * q / sqrt(sum q^2 + eps)     (normalize != 0)
+ *     k_out =         k / sqrt(sum k^2 + eps)     (normalize != 0)
+ *     q_out = scale * q                           (normalize == 0; k, k_out unused)
+ * This is the l2norm helper and the 1/sqrt(head_dim) query factor of the
+ * Gated DeltaNet PyTorch code on "DeltaNet 引入 Delta Rule"
+ * (garden.houmin.site/infra/delta-net), which the DeltaNet layer of
+ * "fla/layers/delta_net.py" asks its kernels for (use_qk_l2norm_in_kernel),
+ * and the d_k^{-1/2} read of "Kimi Delta Attention"
+ * (fr.news.hada.io/topic?id=31925); the pages use eps = 1e-6.  The keys are
+ * never scaled: the read o_t = S_t q_t is linear in q, so the scale
+ * multiplies the outputs and leaves the state as it is.
+ *
+ * Arithmetic in fp32 (sum of squares, reciprocal square root, products),
+ * rounded once to `dt` on the store.  One kernel over all rows; it runs as
+ * its own pass (reads q and k once, writes them once) ahead of the
+ * recurrence.
+ *
+ * Arguments:
+ *   q, q_out   [rows, d]  dtype `dt`; q_out may be q itself (in place) but
+ *                         must not partially overlap it
+ *   k, k_out   [rows, d]  dtype `dt`; read and written only when
+ *                         normalize != 0 (k_out may be k)
+ *   rows >= 0 (B * H * T for the chunkwise forms, B * H for a step,
+ *   H * T for packed sequences); d 64 or 128; scale finite; eps finite,
+ *   >= 0 (with eps = 0 a zero row gives NaN); dt DN_F32 or DN_BF16.
+ * Errors: DN_ERR_INVALID_ARG (pointers, sizes, overlaps, non-finite scale or
+ * eps), DN_ERR_UNSUPPORTED (other d), DN_ERR_CUDA.
+ */
+DN_API int dn_qk_prepare(const void *q, const void *k, void *q_out, void *k_out,
+                  long long rows, int d, int normalize, float scale, float eps,
+                  int dt, void *stream);
+
 /* ABI version of this header (bumped on incompatible changes). */
 DN_API int dn_abi_version(void);
 
-#define DN_ABI_VERSION 2
+#define DN_ABI_VERSION 3
 
 #ifdef __cplusplus
 }

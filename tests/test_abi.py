@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dn_abi_version() == 2
+    assert lib.dn_abi_version() == 3
     assert lib.dn_status_string(0) == b"DN_OK"
     assert lib.dn_status_string(1) == b"DN_ERR_INVALID_ARG"
     assert lib.dn_status_string(2) == b"DN_ERR_UNSUPPORTED"
@@ -193,3 +193,24 @@ def test_varlen_rejects_bad_offsets_before_any_cuda_call(lib):
     arr = (ctypes.c_int * 4)(0, 65, 65, 100)
     assert size(arr, 3, 2, 128, 128, 64, 1) == 2 * (2 + 0 + 1) * 16384
     assert size(arr, 3, 2, 64, 64, 64, 1) == 0
+
+
+def test_qk_prepare_rejects_before_any_cuda_call(lib):
+    """dn_qk_prepare checks its sizes, dtype, scale and eps on the host
+    first; an empty problem is a no-op that touches nothing."""
+    f = lib.dn_qk_prepare
+    null = [None] * 4
+
+    def call(rows=8, d=128, normalize=1, scale=1.0, eps=1e-6, dt=1):
+        return f(*null, rows, d, normalize, scale, eps, dt, None)
+
+    assert call(rows=-1) == _lib.DN_ERR_INVALID_ARG
+    assert call(dt=7) == _lib.DN_ERR_INVALID_ARG
+    assert call(d=0) == _lib.DN_ERR_INVALID_ARG
+    assert call(d=96) == _lib.DN_ERR_UNSUPPORTED
+    assert call(scale=float("inf")) == _lib.DN_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == _lib.DN_ERR_INVALID_ARG
+    assert call(eps=-1e-6) == _lib.DN_ERR_INVALID_ARG
+    assert b"eps" in lib.dn_last_error()
+    assert call(rows=0) == _lib.DN_OK
+    assert call(rows=0, normalize=0) == _lib.DN_OK

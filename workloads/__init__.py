@@ -91,11 +91,13 @@ class DecodeInputs:
 def chunk_inputs(B: int, H: int, T: int, dk: int, dv: int, *, dtype="bf16",
                  seed: int = 0, feature_map: str = "none",
                  beta_scale: float = 1.0, s0_std: float | None = None,
-                 ) -> ChunkInputs:
+                 normalize: bool = True) -> ChunkInputs:
     """Random sequence inputs.
 
     feature_map: "none" (q, k = l2norm(N(0,1))) or "silu"
     (q, k = l2norm(silu(N(0,1)))).  beta = beta_scale * sigmoid(N(0,1)).
+    normalize=False leaves q and k as drawn (N(0,1), or silu of it), for
+    calls that normalise them in the library.
     """
     g = torch.Generator().manual_seed(int(seed))
     q = torch.randn(B, H, T, dk, generator=g)
@@ -109,7 +111,8 @@ def chunk_inputs(B: int, H: int, T: int, dk: int, dv: int, *, dtype="bf16",
         q, k = torch.nn.functional.silu(q), torch.nn.functional.silu(k)
     elif feature_map != "none":
         raise ValueError(f"unknown feature map {feature_map!r}")
-    q, k = l2norm(q), l2norm(k)
+    if normalize:
+        q, k = l2norm(q), l2norm(k)
     beta = torch.sigmoid(b) * float(beta_scale)
     dt = torch_dtype(dtype)
     return ChunkInputs(q.to(dt).contiguous(), k.to(dt).contiguous(),

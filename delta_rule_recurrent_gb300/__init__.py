@@ -108,7 +108,6 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Ten
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
         _check_cuda(name, t, dev)
     dt = _dtype_code(q)
-    q, k = _prepared(q, k, scale, qk_l2norm)
     if not (k.dtype == v.dtype == beta.dtype == q.dtype):
         raise TypeError("q, k, v and beta must share one dtype")
     if q.dim() != 4 or k.shape != q.shape or v.dim() != 4:
@@ -117,6 +116,7 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Ten
     dv = v.shape[3]
     if tuple(v.shape[:3]) != (B, H, T) or tuple(beta.shape) != (B, H, T):
         raise ValueError("v must be [B,H,T,dv] and beta [B,H,T]")
+    q, k = _prepared(q, k, scale, qk_l2norm)
     if initial_state is not None:
         _check_cuda("initial_state", initial_state, dev)
         if initial_state.dtype != torch.float32 or tuple(initial_state.shape) != (B, H, dk, dv):
@@ -166,7 +166,6 @@ def recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torc
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("state", state)):
         _check_cuda(name, t, dev)
     dt = _dtype_code(q)
-    q, k = _prepared(q, k, scale, qk_l2norm)
     if not (k.dtype == v.dtype == beta.dtype == q.dtype):
         raise TypeError("q, k, v and beta must share one dtype")
     if q.dim() != 3 or k.shape != q.shape or v.dim() != 3:
@@ -175,6 +174,7 @@ def recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torc
     dv = v.shape[2]
     if tuple(v.shape[:2]) != (B, H) or tuple(beta.shape) != (B, H):
         raise ValueError("v must be [B,H,dv] and beta [B,H]")
+    q, k = _prepared(q, k, scale, qk_l2norm)
     if state.dtype != torch.float32 or tuple(state.shape) != (B, H, dk, dv):
         raise ValueError("state must be float32 [B,H,dk,dv]")
     if out is None:
@@ -303,7 +303,6 @@ def _chunk_decayed(q, k, v, beta, g, per_channel, initial_state, output_final_st
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
         _check_cuda(name, t, dev)
     dt = _dtype_code(q)
-    q, k = _prepared(q, k, scale, qk_l2norm)
     if not (k.dtype == v.dtype == beta.dtype == q.dtype):
         raise TypeError("q, k, v and beta must share one dtype")
     if q.dim() != 4 or k.shape != q.shape or v.dim() != 4:
@@ -312,6 +311,7 @@ def _chunk_decayed(q, k, v, beta, g, per_channel, initial_state, output_final_st
     dv = v.shape[3]
     if tuple(v.shape[:3]) != (B, H, T) or tuple(beta.shape) != (B, H, T):
         raise ValueError("v must be [B,H,T,dv] and beta [B,H,T]")
+    q, k = _prepared(q, k, scale, qk_l2norm)
     _check_gate(g, (B, H, T, dk) if per_channel else (B, H, T), dev)
     if initial_state is not None:
         _check_cuda("initial_state", initial_state, dev)
@@ -319,10 +319,17 @@ def _chunk_decayed(q, k, v, beta, g, per_channel, initial_state, output_final_st
             raise ValueError("initial_state must be float32 [B,H,dk,dv]")
     if out is None:
         out = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev)
+    else:
+        _check_cuda("out", out, dev)
+        if out.dtype != q.dtype or tuple(out.shape) != (B, H, T, dv):
+            raise ValueError("out must match v's shape and dtype")
     S_T = None
     if output_final_state:
         S_T = final_state if final_state is not None else torch.empty(
             (B, H, dk, dv), dtype=torch.float32, device=dev)
+        _check_cuda("final_state", S_T, dev)
+        if S_T.dtype != torch.float32 or tuple(S_T.shape) != (B, H, dk, dv):
+            raise ValueError("final_state must be float32 [B,H,dk,dv]")
     lib = load()
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(), g.data_ptr(),
             initial_state.data_ptr() if initial_state is not None else None, out.data_ptr(),
@@ -371,14 +378,24 @@ def _step_decayed(q, k, v, beta, g, per_channel, state, out, scale=None, qk_l2no
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("state", state)):
         _check_cuda(name, t, dev)
     dt = _dtype_code(q)
-    q, k = _prepared(q, k, scale, qk_l2norm)
+    if not (k.dtype == v.dtype == beta.dtype == q.dtype):
+        raise TypeError("q, k, v and beta must share one dtype")
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3:
+        raise ValueError("q, k must be [B,H,dk] and v [B,H,dv]")
     B, H, dk = q.shape
     dv = v.shape[2]
+    if tuple(v.shape[:2]) != (B, H) or tuple(beta.shape) != (B, H):
+        raise ValueError("v must be [B,H,dv] and beta [B,H]")
+    q, k = _prepared(q, k, scale, qk_l2norm)
     _check_gate(g, (B, H, dk) if per_channel else (B, H), dev)
     if state.dtype != torch.float32 or tuple(state.shape) != (B, H, dk, dv):
         raise ValueError("state must be float32 [B,H,dk,dv]")
     if out is None:
         out = torch.empty((B, H, dv), dtype=q.dtype, device=dev)
+    else:
+        _check_cuda("out", out, dev)
+        if out.dtype != q.dtype or tuple(out.shape) != (B, H, dv):
+            raise ValueError("out must be [B,H,dv] in q's dtype")
     lib = load()
     with torch.cuda.device(dev):
         entry = lib.dn_recurrent_step_kda if per_channel else lib.dn_recurrent_step_gated
@@ -405,7 +422,6 @@ def chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
         _check_cuda(name, t, dev)
     dt = _dtype_code(q)
-    q, k = _prepared(q, k, scale, qk_l2norm)
     if not (k.dtype == v.dtype == beta.dtype == q.dtype):
         raise TypeError("q, k, v and beta must share one dtype")
     if q.dim() != 3 or k.shape != q.shape or v.dim() != 3:
@@ -414,6 +430,7 @@ def chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
     dv = v.shape[2]
     if tuple(v.shape[:2]) != (H, T) or tuple(beta.shape) != (H, T):
         raise ValueError("v must be [H,T,dv] and beta [H,T]")
+    q, k = _prepared(q, k, scale, qk_l2norm)
     cu = [int(x) for x in cu_seqlens]
     N = len(cu) - 1
     cu_arr = (ctypes.c_int * len(cu))(*cu)
@@ -432,6 +449,8 @@ def chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
         ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
     else:
         ws = workspace
+        if ws is not None:
+            _check_cuda("workspace", ws, dev)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     with torch.cuda.device(dev):
         check(lib.dn_chunk_fwd_varlen(

@@ -100,3 +100,29 @@ def test_kda_decode_steps(dtype):
     o_ref, S_ref = oracle.forward_kda(st["q"], st["k"], st["v"], st["beta"], st["g"], S0)
     _check(st["o"].double().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
            workloads.torch_dtype(dtype), f"decode {dtype}")
+
+
+def test_steps_reject_mismatched_inputs_before_any_launch():
+    """The decayed steps check dtypes and shapes in the binding: a bf16 beta
+    with fp32 q, or a beta of the wrong shape, would otherwise have the kernel
+    read past the buffer it was given."""
+    B, H, d = 2, 3, 64
+    q = torch.zeros(B, H, d, device="cuda")
+    S = torch.zeros(B, H, d, d, device="cuda")
+    g = torch.zeros(B, H, d, device="cuda")
+    with pytest.raises(TypeError, match="one dtype"):
+        dn.recurrent_step_kda(q, q, q, torch.zeros(B, H, device="cuda",
+                                                   dtype=torch.bfloat16), g, S)
+    with pytest.raises(ValueError, match="beta"):
+        dn.recurrent_step_kda(q, q, q, torch.zeros(B, device="cuda"), g, S)
+    with pytest.raises(ValueError, match="beta"):
+        dn.recurrent_step_gated(q, q, q, torch.zeros(B, H, 1, device="cuda"),
+                                torch.zeros(B, H, device="cuda"), S)
+    with pytest.raises(ValueError, match="out"):
+        dn.recurrent_step_gated(q, q, q, torch.zeros(B, H, device="cuda"),
+                                torch.zeros(B, H, device="cuda"), S,
+                                out=torch.zeros(B, H, d + 1, device="cuda"))
+    with pytest.raises(ValueError, match="final_state"):
+        dn.chunk_fwd_kda(q[:, :, None], q[:, :, None], q[:, :, None],
+                         torch.zeros(B, H, 1, device="cuda"), g[:, :, None],
+                         final_state=torch.zeros(B, H, d, device="cuda"))

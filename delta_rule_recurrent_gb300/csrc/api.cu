@@ -387,7 +387,8 @@ static int chunk_fwd_decayed(const void* q, const void* k, const void* v, const 
         for (const Span* s : {&sq, &sk, &sv, &so})
             if (int st = check_device_ptr(*s, 16, dev)) return st;
         if (int st = check_device_ptr(sb, es, dev)) return st;
-        if (int st = check_device_ptr(sg, sizeof(float), dev)) return st;
+        // the KDA kernel reads its [T][dk] g tile in 16-byte groups
+        if (int st = check_device_ptr(sg, per_channel ? 16 : sizeof(float), dev)) return st;
     }
     if (S0)
         if (int st = check_device_ptr(s0, 16, dev)) return st;

@@ -322,7 +322,9 @@ DN_API size_t dn_chunk_fwd_varlen_workspace_bytes(const int *cu_seqlens, int N, 
  * (in the stored [dk][dv] layout, row i of S is scaled by exp(g_t[i])).  The
  * page's read uses d_k^{-1/2} q_t; as everywhere in this library the caller
  * applies any query scale.
- *   g   [B, H, T, dk] fp32 for the chunkwise form, [B, H, dk] for a step
+ *   g   [B, H, T, dk] fp32 for the chunkwise form (16-byte aligned: the
+ *       kernel reads it in 16-byte rows), [B, H, dk] for a step (4-byte
+ *       aligned)
  * Every other argument, layout and error as for dn_chunk_fwd_gated (with no
  * workspace) / dn_recurrent_step_gated.  fp32 arithmetic on CUDA cores.
  */

@@ -559,7 +559,10 @@ def run_ours(args, rank, world, local):
     nchunks = -(-T // C)
     bflops = bwd_flops_per_chunk(C, dk, dv) * B * H * nchunks
     bwd_launch_s = statistics.mean(bwd_launch) / 1e3
-    if tc:  # bf16 I/O: the products run as tf32 MMAs (the solve and the rest on CUDA cores)
+    # The backward picks its own path (the tensor-core recompute and chain for bf16,
+    # d = 128), whatever --algo says for the forward.
+    bwd_tc = _tc_used(lib, dk, dv, q.dtype)
+    if bwd_tc:  # bf16 I/O: the products run as tf32 MMAs (the solve and the rest on CUDA cores)
         bpeak = peaks["bf16_tflops"] * TF32_PER_BF16
         bbound, barith = "tensor", "tf32 mma.sync products, fp32 accumulation"
         bsrc = f"{peak_src} bf16 burst x nominal tf32/bf16 ratio (1.1/2.25)"
@@ -569,7 +572,7 @@ def run_ours(args, rank, world, local):
     backward = {
         "workload": HEADLINE, "steps": bwd_steps, "value": world * tokens * bwd_steps / bwd_region_s,
         "unit": "tokens/s", "ms_per_step": 1e3 * bwd_region_s / bwd_steps,
-        "arith": barith, "launches_per_call": 3,
+        "arith": barith, "launches_per_call": 4 if bwd_tc else 3,
         "roofline": {"bound": bbound, "achieved": bflops / bwd_launch_s / 1e12, "peak": bpeak,
                      "unit": "TFLOP/s", "frac": bflops / bwd_launch_s / 1e12 / bpeak,
                      "traffic": None, "peak_source": bsrc,
@@ -699,7 +702,7 @@ def run_ours(args, rank, world, local):
                 "ms_per_step": 1e3 * e2e_s / e2e_steps},
         "gpu_launches": (launches_per_call * (args.steps + e2e_steps)   # chunk forward, e2e
                          + nsteps + (nsteps if dec_graph[0] else 0)     # decode, graph replay
-                         + (4 if tc else 3) * bwd_steps                 # recompute, chain, grads
+                         + (4 if bwd_tc else 3) * bwd_steps             # recompute, chain, grads
                          + launches_per_call * vsteps                   # varlen
                          + psteps                                       # q/k preparation
                          + (2 if gneed else 1) * gsteps + gsteps + nsteps  # gated: both forms, decode

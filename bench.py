@@ -46,6 +46,12 @@ def chunk_flops_per_token_head(C, dk, dv):
     return C * (3 * dk + 2 * dv) + 6 * dk * dv + C * C / 3.0
 
 
+def chunk_dense_flops_per_token_head(C, dk, dv):
+    """The same products counted as full tiles (the triangles not skipped),
+    as tensor cores execute them: 2C(3dk + 2dv) + 6 dk dv + C^2/3."""
+    return 2 * C * (3 * dk + 2 * dv) + 6 * dk * dv + C * C / 3.0
+
+
 def bwd_flops_per_chunk(C, dk, dv):
     """FLOPs the chunkwise backward executes per (batch, head, chunk), dense
     tiles as the three kernels form them (the forward recompute of the chunk
@@ -510,6 +516,7 @@ def run_ours(args, rank, world, local):
     value = job_throughput(world, tokens * args.steps, region_s)
     launch_s = statistics.mean(per_launch) / 1e3
     flops = chunk_flops_per_token_head(C, dk, dv) * B * H * T
+    dflops = chunk_dense_flops_per_token_head(C, dk, dv) * B * H * T
     cbytes = chunk_bytes(B, H, T, dk, dv, q.element_size(), False, True)
     tflops = flops / launch_s / 1e12
     # A "launch" here is one dn_chunk_fwd call; on the two-pass path that is
@@ -533,6 +540,8 @@ def run_ours(args, rank, world, local):
         "launch_us": launch_s * 1e6,
         "tensor": {"achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                    "frac": tflops / peaks["bf16_tflops"], "flops_per_launch": flops,
+                   "dense_tile_flops_per_launch": dflops,
+                   "dense_tile_frac": dflops / launch_s / 1e12 / peaks["bf16_tflops"],
                    "peak_source": f"{peak_src} (bf16 dense burst)"},
     }
     dbytes = decode_bytes(Bd, Hd, dkd, dvd, 2)

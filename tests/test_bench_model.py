@@ -41,6 +41,18 @@ def test_chunk_flops_match_the_product_count():
     assert total == pytest.approx(36.87e9, rel=1e-3)
 
 
+def test_dense_tile_flops_count_the_triangles_in_full():
+    """Every triangular product counted as its full square: A and P as full
+    C x C x dk products, T K, T V and P U' as full C x C products; the
+    solve's C^3/3 and the three dk x dv products as before."""
+    per_chunk = (2 * C * C * D + 2 * C * C * D + C ** 3 / 3 + 2 * C * C * D + 2 * C * C * D
+                 + 2 * C * D * D * 3 + 2 * C * C * D)
+    assert bench.chunk_dense_flops_per_token_head(C, D, D) == pytest.approx(per_chunk / C,
+                                                                           rel=1e-12)
+    assert bench.chunk_dense_flops_per_token_head(C, D, D) * B * H * T == pytest.approx(
+        47.6e9, rel=1e-3)
+
+
 def test_chunk_bytes_count_each_tensor_once():
     q = k = B * H * T * D * 2
     v = o = B * H * T * D * 2

@@ -178,3 +178,19 @@ def test_gated_decode_zero_decay_matches_the_plain_step_exactly():
     o2 = dn.recurrent_step_gated(dev(x.q), dev(x.k), dev(x.v), dev(x.beta),
                                  torch.zeros(B, H, device="cuda"), S2)
     assert torch.equal(o1, o2) and torch.equal(S1, S2)
+
+
+@pytest.mark.parametrize("form", ["gated", "kda"])
+def test_zero_length_sequence_passes_the_state_through(form):
+    """T = 0: no token, so S_T is S0 (or zeros without S0), and o is empty."""
+    B, H, d = 2, 3, 128
+    z = torch.zeros(B, H, 0, d, dtype=torch.bfloat16, device="cuda")
+    beta = torch.zeros(B, H, 0, dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros((B, H, 0, d) if form == "kda" else (B, H, 0), device="cuda")
+    S0 = workloads.decode_state(B, H, d, d, std=0.1, seed=3).cuda()
+    fwd = dn.chunk_fwd_kda if form == "kda" else dn.chunk_fwd_gated
+    o, S = fwd(z, z, z, beta, g, initial_state=S0)
+    o0, S_zero = fwd(z, z, z, beta, g)
+    torch.cuda.synchronize()
+    assert o.shape == (B, H, 0, d) and torch.equal(S, S0)
+    assert torch.count_nonzero(S_zero) == 0

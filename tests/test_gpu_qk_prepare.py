@@ -174,3 +174,10 @@ def test_rejections():
         from delta_rule_recurrent_gb300._lib import check
         check(lib.dn_qk_prepare(q.data_ptr(), k.data_ptr(), k.data_ptr(), q.data_ptr(), 4, 128,
                                 1, 1.0, 1e-6, 1, None))
+
+
+def test_empty_tensors_are_a_no_op():
+    z = torch.zeros(2, 3, 0, 128, dtype=torch.bfloat16, device="cuda")
+    qo, ko = dn.qk_prepare(z, z, scale=0.5, l2norm=True)
+    torch.cuda.synchronize()
+    assert qo.shape == z.shape and ko.shape == z.shape

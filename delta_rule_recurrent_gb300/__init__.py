@@ -10,7 +10,7 @@ the computation runs in the library's sm_103a kernels.
     recurrent_step(q, k, v, beta, state) -> o   # decoding, state in place
     chunk_bwd(q, k, v, beta, d_o, initial_state=None, d_final_state=None)
         -> (d_q, d_k, d_v, d_beta, d_initial_state)   # training backward
-    DeltaRule.apply(q, k, v, beta, initial_state)     # autograd: (o, final_state)
+    DeltaRule.apply(q, k, v, beta, initial_state, scale)  # autograd: (o, final_state)
     chunk_fwd_varlen(q, k, v, beta, cu_seqlens, ...)  # packed sequences, [H, T, d]
     chunk_fwd_gated(q, k, v, beta, g, ...), recurrent_step_gated(q, k, v, beta, g, state)
         # Gated DeltaNet: log keep rate g per token (per head for a step)
@@ -241,17 +241,24 @@ def chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Ten
 
 
 class DeltaRule(torch.autograd.Function):
-    """Autograd wrapper: ``DeltaRule.apply(q, k, v, beta, initial_state)``
-    returns ``(o, final_state)`` from ``chunk_fwd``; the backward pass calls
-    ``chunk_bwd`` (the chunk states are recomputed there, not stored)."""
+    """Autograd wrapper: ``DeltaRule.apply(q, k, v, beta, initial_state,
+    scale)`` returns ``(o, final_state)`` from ``chunk_fwd``; the backward
+    pass calls ``chunk_bwd`` (the chunk states are recomputed there, not
+    stored).  ``scale`` (None for none) multiplies q before the recurrence
+    (``qk_prepare``); the backward multiplies the q gradient by it with the
+    same kernel, since d(s q) = s dq.  The L2 normalisation has no backward
+    here: pass normalised q and k."""
 
     @staticmethod
-    def forward(ctx, q, k, v, beta, initial_state=None):
+    def forward(ctx, q, k, v, beta, initial_state=None, scale=None):
         q, k, v, beta = (t.contiguous() for t in (q, k, v, beta))
         if initial_state is not None:
             initial_state = initial_state.contiguous()
+        if scale is not None:
+            q, _ = qk_prepare(q, k, scale=scale, l2norm=False)
         o, S_T = chunk_fwd(q, k, v, beta, initial_state=initial_state, output_final_state=True)
         ctx.save_for_backward(q, k, v, beta, initial_state)
+        ctx.scale = scale
         return o, S_T
 
     @staticmethod
@@ -260,7 +267,9 @@ class DeltaRule(torch.autograd.Function):
         d_o = torch.zeros_like(v) if d_o is None else d_o.contiguous()
         d_S_T = None if d_S_T is None else d_S_T.contiguous().float()
         d_q, d_k, d_v, d_beta, d_S0 = chunk_bwd(q, k, v, beta, d_o.to(v.dtype), S0, d_S_T)
-        return d_q, d_k, d_v, d_beta, (d_S0 if S0 is not None else None)
+        if ctx.scale is not None:
+            qk_prepare(d_q, d_q, scale=ctx.scale, l2norm=False, inplace=True)
+        return d_q, d_k, d_v, d_beta, (d_S0 if S0 is not None else None), None
 
 
 def _check_gate(g: torch.Tensor, shape, dev) -> None:

@@ -146,3 +146,21 @@ def test_autograd_function_matches_the_entry_point():
         assert torch.equal(leaf.grad, g)
     ref = oracle.backward(inp.q, inp.k, inp.v, inp.beta, d_o, inp.S0, d_S)
     _check([x.grad.double().cpu().numpy() for x in leaves], ref, torch.bfloat16, "autograd")
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+def test_autograd_with_a_query_scale(dtype, d):
+    """DeltaRule.apply(..., scale=s): the forward reads s q; the gradients are
+    the oracle's for s q, with the q gradient multiplied by s (chain rule)."""
+    inp, d_o, d_S = _case(1, 2, 130, d, d, dtype, seed=8)
+    s = d ** -0.5
+    leaves = [dev(x).requires_grad_() for x in (inp.q, inp.k, inp.v, inp.beta, inp.S0)]
+    o, S_T = dn.DeltaRule.apply(*leaves, s)
+    torch.autograd.backward([o, S_T], [dev(d_o), dev(d_S)])
+    qs, _ = oracle.prepare_qk(inp.q, inp.k, scale=s)
+    o_ref, _ = oracle.forward(qs, inp.k, inp.v, inp.beta, inp.S0)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    assert rel_l2(o.detach().double().cpu().numpy(), o_ref) <= TOL[dt]
+    ref = list(oracle.backward(qs, inp.k, inp.v, inp.beta, d_o, inp.S0, d_S))
+    ref[0] = ref[0] * s
+    _check([x.grad.double().cpu().numpy() for x in leaves], ref, dt, "autograd, scaled q")

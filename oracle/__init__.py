@@ -76,6 +76,10 @@ def _load():
                                                ctypes.c_int, ctypes.c_double,
                                                ctypes.c_double]
         lib.dn_oracle_prepare_rows.restype = None
+        lib.dn_oracle_prepare_rows_backward.argtypes = [dp, dp, dp, ctypes.c_long,
+                                                        ctypes.c_long, ctypes.c_int,
+                                                        ctypes.c_double, ctypes.c_double]
+        lib.dn_oracle_prepare_rows_backward.restype = None
         _lib = lib
     return _lib
 
@@ -302,3 +306,22 @@ def prepare_qk(q, k, scale: float = 1.0, l2norm: bool = False, eps: float = 1e-6
                                float(eps))
     lib.dn_oracle_prepare_rows(_ptr(k), _ptr(ko), rows, d, int(l2norm), 1.0, float(eps))
     return qo, ko
+
+
+def prepare_qk_backward(q, k, d_q, d_k, scale: float = 1.0, l2norm: bool = False,
+                        eps: float = 1e-6):
+    """Gradients of ``prepare_qk`` with respect to its raw inputs, in fp64:
+    given the raw q, k and the gradients d_q, d_k of the prepared q', k',
+    returns ``(dq_raw, dk_raw)`` (the keys carry no scale)."""
+    q, k, d_q, d_k = _f64(q), _f64(k), _f64(d_q), _f64(d_k)
+    if not (q.shape == k.shape == d_q.shape == d_k.shape) or q.ndim < 1:
+        raise ValueError("q, k, d_q and d_k must share one shape")
+    d = q.shape[-1]
+    rows = q.size // d if d else 0
+    gq, gk = np.empty_like(q), np.empty_like(k)
+    lib = _load()
+    lib.dn_oracle_prepare_rows_backward(_ptr(q), _ptr(d_q), _ptr(gq), rows, d, int(l2norm),
+                                        float(scale), float(eps))
+    lib.dn_oracle_prepare_rows_backward(_ptr(k), _ptr(d_k), _ptr(gk), rows, d, int(l2norm),
+                                        1.0, float(eps))
+    return gq, gk

@@ -408,3 +408,38 @@ void dn_oracle_prepare_rows(const double *x, double *y, long rows, long d,
             yr[i] = xr[i] * f;
     }
 }
+
+/*
+ * Gradient of the preparation above, per row: given the row x and the
+ * gradient dy of its output y = scale * x / n (n = sqrt(sum x^2 + eps)),
+ *
+ *   dx = (scale / n) (dy - x (x . dy) / n^2)     (normalize != 0)
+ *   dx = scale dy                                (normalize == 0)
+ *
+ * which is the chain rule through y_i = scale x_i / n with
+ * dn/dx_i = x_i / n.  x, dy, dx are [rows][d] (dx may equal dy).
+ */
+void dn_oracle_prepare_rows_backward(const double *x, const double *dy, double *dx,
+                                     long rows, long d, int normalize, double scale,
+                                     double eps)
+{
+    for (long r = 0; r < rows; ++r) {
+        const double *xr = x + r * d;
+        const double *gr = dy + r * d;
+        double *out = dx + r * d;
+        if (!normalize) {
+            for (long i = 0; i < d; ++i)
+                out[i] = scale * gr[i];
+            continue;
+        }
+        double ss = 0.0, xg = 0.0;
+        for (long i = 0; i < d; ++i) {
+            ss += xr[i] * xr[i];
+            xg += xr[i] * gr[i];
+        }
+        const double n2 = ss + eps;
+        const double n = sqrt(n2);
+        for (long i = 0; i < d; ++i)
+            out[i] = scale / n * (gr[i] - xr[i] * xg / n2);
+    }
+}

@@ -11,6 +11,8 @@ Each pin takes the preparation as a function ``prep(q, k, scale, l2norm,
 eps) -> (q', k')`` and returns True when it holds.  The oracle must pass
 every pin, and each planted mistake below (a plausible slip in writing the
 preparation, planted in a numpy copy on the CPU) must fail at least one.
+The preparation's gradient (``oracle.prepare_qk_backward``) is held the same
+way to central finite differences of the forward and to closed forms.
 """
 from fractions import Fraction
 
@@ -156,4 +158,114 @@ def test_planted_mistake_is_caught(oracle_lib, name):
             ok = False
         if not ok:
             failed.append(pin_name)
+    assert failed, f"mutant {name} passes every pin"
+
+
+# ---- the preparation's gradient (oracle.prepare_qk_backward) ------------------
+#
+# Each pin takes the gradient as ``bwd(q, k, d_q, d_k, scale, l2norm, eps)``.
+# The central pin differentiates the (pinned) forward preparation numerically,
+# so it shares nothing with the gradient's own code.
+
+def _oracle_bwd(q, k, d_q, d_k, scale, l2norm, eps):
+    return oracle.prepare_qk_backward(q, k, d_q, d_k, scale=scale, l2norm=l2norm, eps=eps)
+
+
+def bpin_finite_differences(bwd):
+    """<d_q, dq'/dx . e> by central differences of the forward preparation,
+    every input coordinate of a few rows, against the analytic gradient."""
+    r = np.random.default_rng(3)
+    q, k = r.standard_normal((2, 3, 6)), r.standard_normal((2, 3, 6))
+    dq, dk = r.standard_normal(q.shape), r.standard_normal(k.shape)
+    s, eps, h = 0.375, 1e-3, 1e-6
+    gq, gk = bwd(q, k, dq, dk, s, True, eps)
+    num_q, num_k = np.zeros_like(q), np.zeros_like(k)
+    for idx in np.ndindex(q.shape):
+        for x, num, is_q in ((q, num_q, True), (k, num_k, False)):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = (xp, k) if is_q else (q, xp)
+            args_m = (xm, k) if is_q else (q, xm)
+            yp = oracle.prepare_qk(*args_p, scale=s, l2norm=True, eps=eps)
+            ym = oracle.prepare_qk(*args_m, scale=s, l2norm=True, eps=eps)
+            num[idx] = (np.sum(dq * (yp[0] - ym[0])) + np.sum(dk * (yp[1] - ym[1]))) / (2 * h)
+    return np.max(np.abs(gq - num_q)) < 1e-7 and np.max(np.abs(gk - num_k)) < 1e-7
+
+
+def bpin_gradient_orthogonal_to_the_row(bwd):
+    """With eps = 0 the output does not change along x itself, so x . dx = 0."""
+    r = np.random.default_rng(4)
+    x, g = r.standard_normal((5, 32)), r.standard_normal((5, 32))
+    gq, _ = bwd(x, x, g, g, 2.0, True, 0.0)
+    return np.max(np.abs(np.sum(gq * x, axis=-1))) < 1e-13
+
+
+def bpin_scale_only(bwd):
+    """Without the normalisation: dq = scale dq', dk = dk'."""
+    r = np.random.default_rng(5)
+    x, g = r.standard_normal((4, 16)), r.standard_normal((4, 16))
+    gq, gk = bwd(x, x, g, g, 0.25, False, 1e-6)
+    return bool(np.array_equal(gq, 0.25 * g) and np.array_equal(gk, g))
+
+
+def bpin_zero_row(bwd):
+    """At x = 0 the map is x scale / sqrt(eps): dx = scale dy / sqrt(eps)."""
+    g = np.arange(1.0, 9.0).reshape(1, 8)
+    gq, gk = bwd(np.zeros((1, 8)), np.zeros((1, 8)), g, g, 3.0, True, 0.25)
+    return np.max(np.abs(gq - 6.0 * g)) < 1e-14 and np.max(np.abs(gk - 2.0 * g)) < 1e-14
+
+
+def bpin_inverse_scaling_in_x(bwd):
+    """With eps = 0 the output is invariant to x -> c x, so dx scales as 1/c."""
+    r = np.random.default_rng(6)
+    x, g = r.standard_normal((3, 8)), r.standard_normal((3, 8))
+    g1, _ = bwd(x, x, g, g, 1.0, True, 0.0)
+    g4, _ = bwd(4.0 * x, x, g, g, 1.0, True, 0.0)
+    return np.max(np.abs(g4 - g1 / 4.0)) < 1e-14
+
+
+BPINS = {f.__name__[5:]: f for f in (
+    bpin_finite_differences, bpin_gradient_orthogonal_to_the_row, bpin_scale_only,
+    bpin_zero_row, bpin_inverse_scaling_in_x)}
+
+
+def _bwd_mutant(slip):
+    def bwd(q, k, d_q, d_k, scale, l2norm, eps):
+        def one(x, g, s):
+            x, g = np.asarray(x, np.float64), np.asarray(g, np.float64)
+            if not l2norm:
+                return (1.0 if slip == "scale_dropped" else s) * g
+            n2 = np.sum(x * x, axis=-1, keepdims=True) + eps
+            n = np.sqrt(n2)
+            xg = np.sum(x * g, axis=-1, keepdims=True)
+            if slip == "missing_1_over_n2":
+                return s / n * (g - x * xg)
+            if slip == "wrong_sign":
+                return s / n * (g + x * xg / n2)
+            if slip == "scale_dropped":
+                return 1.0 / n * (g - x * xg / n2)
+            return s / n * (g - x * xg / n2)
+        kscale = scale if slip == "keys_scaled" else 1.0
+        return one(q, d_q, scale), one(k, d_k, kscale)
+    return bwd
+
+
+BMUTANTS = {name: _bwd_mutant(name) for name in
+            ("missing_1_over_n2", "wrong_sign", "scale_dropped", "keys_scaled")}
+
+
+@pytest.mark.parametrize("name", sorted(BPINS))
+def test_oracle_gradient_satisfies_pin(oracle_lib, name):
+    assert BPINS[name](_oracle_bwd), name
+
+
+def test_a_correct_numpy_gradient_passes_every_pin(oracle_lib):
+    right = _bwd_mutant("none")
+    assert [n for n, pin in BPINS.items() if not pin(right)] == []
+
+
+@pytest.mark.parametrize("name", sorted(BMUTANTS))
+def test_planted_gradient_mistake_is_caught(oracle_lib, name):
+    failed = [n for n, pin in BPINS.items() if not pin(BMUTANTS[name])]
     assert failed, f"mutant {name} passes every pin"

@@ -17,6 +17,8 @@ transposed block or a misplaced decay factor fails:
 - KDA on CUDA cores: the per-channel ratio as exp(G_i[d]) exp(-G_j[d]).
 - the per-chunk gradients in feature-lane form (the layout a tcgen05
   gradient kernel takes), dP and dTm as diagonal blocks of one product.
+- the independence of the value columns (plain, gated, KDA), which lets a
+  scan split dv across CTAs with no exchange.
 """
 import numpy as np
 import pytest
@@ -214,3 +216,20 @@ def test_gradient_kernel_feature_lane_plan():
     ref = oracle.backward(q, k, v, beta, dO, S0, dS_T)
     for got, want in zip((dq, dk, dv, db), ref[:4]):
         assert _rel(got, want[0, 0]) < 1e-9
+
+
+@pytest.mark.parametrize("form", ["plain", "gated", "kda"])
+def test_value_columns_are_independent(form):
+    """Column j of the state, of U' and of the output depends only on column
+    j of v and of S0, so a scan may split the value dimension across CTAs
+    with no exchange: the oracle run on a column slice of v and S0 gives
+    that slice of the full run's o and S_T, exactly."""
+    q, k, v, beta, S0, g = _case(6, dv=9, gate=form == "gated", kda=form == "kda")
+    run = {"plain": lambda vv, SS: oracle.forward(q, k, vv, beta, SS),
+           "gated": lambda vv, SS: oracle.forward_gated(q, k, vv, beta, g, SS),
+           "kda": lambda vv, SS: oracle.forward_kda(q, k, vv, beta, g, SS)}[form]
+    o, S = run(v, S0)
+    for cols in (slice(0, 4), slice(4, 9), slice(2, 3)):
+        o_c, S_c = run(np.ascontiguousarray(v[..., cols]), np.ascontiguousarray(S0[..., cols]))
+        assert np.array_equal(o_c, o[..., cols])
+        assert np.array_equal(S_c, S[..., cols])

@@ -233,3 +233,41 @@ def test_value_columns_are_independent(form):
         o_c, S_c = run(np.ascontiguousarray(v[..., cols]), np.ascontiguousarray(S0[..., cols]))
         assert np.array_equal(o_c, o[..., cols])
         assert np.array_equal(S_c, S[..., cols])
+
+
+@pytest.mark.parametrize("form", ["plain", "gated", "kda"])
+def test_sequence_split_through_augmented_columns(form):
+    """A sequence cut into segments, each run from its own start with no
+    knowledge of the others, then joined by a short scan over segments.
+
+    The state is linear in the initial state, S_t = A_t S_start + B_t (A_t
+    the product of the transitions so far, decay included).  Running a
+    segment with value columns [v | 0] from the initial state [0 | I] gives,
+    column by column (the columns are independent): o_zero and B in the
+    first dv columns, and in the last dk columns the transformed queries
+    q~_t = A_t^T q_t (outputs) and A (final state).  Then per segment
+    o = o_zero + q~ S_start and S_end = A S_start + B."""
+    q, k, v, beta, S0, g = _case(7, T=41, gate=form == "gated", kda=form == "kda")
+    dk, dv = q.shape[-1], v.shape[-1]
+
+    def run(sl, vv, SS):
+        if form == "plain":
+            return oracle.forward(q[..., sl, :], k[..., sl, :], vv, beta[..., sl], SS)
+        gg = g[..., sl, :] if form == "kda" else g[..., sl]
+        f = oracle.forward_kda if form == "kda" else oracle.forward_gated
+        return f(q[..., sl, :], k[..., sl, :], vv, beta[..., sl], gg, SS)
+
+    o_full, S_full = run(slice(None), v, S0)
+    S_start = S0[0, 0]
+    outs = []
+    for a, b in ((0, 13), (13, 29), (29, 41)):
+        sl = slice(a, b)
+        v_aug = np.concatenate([v[..., sl, :], np.zeros((1, 1, b - a, dk))], axis=-1)
+        S_aug = np.concatenate([np.zeros((1, 1, dk, dv)), np.eye(dk)[None, None]], axis=-1)
+        o_aug, S_end_aug = run(sl, v_aug, S_aug)
+        o_zero, q_t = o_aug[0, 0, :, :dv], o_aug[0, 0, :, dv:]
+        B, A = S_end_aug[0, 0, :, :dv], S_end_aug[0, 0, :, dv:]
+        outs.append(o_zero + q_t @ S_start)
+        S_start = A @ S_start + B
+    assert _rel(np.concatenate(outs), o_full[0, 0]) < 1e-12
+    assert _rel(S_start, S_full[0, 0]) < 1e-12

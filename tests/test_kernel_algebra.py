@@ -19,6 +19,8 @@ transposed block or a misplaced decay factor fails:
   gradient kernel takes), dP and dTm as diagonal blocks of one product.
 - the independence of the value columns (plain, gated, KDA), which lets a
   scan split dv across CTAs with no exchange.
+- a sequence split through augmented state columns ([v | 0] from [0 | I]),
+  and the same as two packed-sequence calls plus a scan over segments.
 """
 import numpy as np
 import pytest
@@ -271,3 +273,32 @@ def test_sequence_split_through_augmented_columns(form):
         S_start = A @ S_start + B
     assert _rel(np.concatenate(outs), o_full[0, 0]) < 1e-12
     assert _rel(S_start, S_full[0, 0]) < 1e-12
+
+
+def test_sequence_split_as_two_packed_calls():
+    """The long-prefill plan in the packed-sequence calling convention
+    (q, k, v, beta [H, T, d]; cu_seqlens at the segment cuts; one initial
+    state per segment [N, H, dk, dv]): one call with [v, S0 = 0] and one with
+    [0, S0 = I] (dv = dk there), then per head the scan over segments and
+    the correction, against one unsplit run per head."""
+    r = np.random.default_rng(8)
+    H, T, d = 3, 150, 6
+    q = _unit(r.standard_normal((H, T, d)))
+    k = _unit(r.standard_normal((H, T, d)))
+    v = r.standard_normal((H, T, d))
+    beta = r.uniform(0.05, 1.5, (H, T))
+    S0 = 0.5 * r.standard_normal((H, d, d))
+    cu = [0, 40, 64, 129, 150]
+    N = len(cu) - 1
+    o_zero, B = oracle.forward_varlen(q, k, v, beta, cu)
+    eye = np.broadcast_to(np.eye(d), (N, H, d, d))
+    q_t, A = oracle.forward_varlen(q, k, np.zeros_like(v), beta, cu, S0=eye)
+    o_full, S_full = oracle.forward(q[None], k[None], v[None], beta[None], S0[None])
+    for h in range(H):
+        S_start = S0[h]
+        for n in range(N):
+            sl = slice(cu[n], cu[n + 1])
+            o_seg = o_zero[h, sl] + q_t[h, sl] @ S_start
+            assert _rel(o_seg, o_full[0, h, sl]) < 1e-12
+            S_start = A[n, h] @ S_start + B[n, h]
+        assert _rel(S_start, S_full[0, h]) < 1e-12

@@ -194,3 +194,35 @@ def test_zero_length_sequence_passes_the_state_through(form):
     torch.cuda.synchronize()
     assert o.shape == (B, H, 0, d) and torch.equal(S, S0)
     assert torch.count_nonzero(S_zero) == 0
+
+
+@pytest.mark.parametrize("form", ["gated", "kda"])
+def test_decode_at_the_bench_shape_sampled_heads(form):
+    """B256 H16 d128 bf16 (the decode workload's shape and the bench's launch
+    configuration), eight chained steps with one keep rate per head (gated)
+    or per key channel (KDA); 12 heads replayed by the oracle."""
+    w = workloads.WORKLOADS["decode_bf16"]
+    B, H, d, seed = w["B"], w["H"], w["dk"], w["seed"]
+    steps = 8
+    bi, hi = sample_heads(B, H, 12, seed=13)
+    S0 = workloads.decode_state(B, H, d, d, std=w["s0_std"], seed=seed)
+    S = dev(S0)
+    g = workloads.gate_inputs(B, H, seed=seed, channels=d if form == "kda" else None)
+    step = dn.recurrent_step_kda if form == "kda" else dn.recurrent_step_gated
+    rec = {n: [] for n in ("q", "k", "v", "beta", "o")}
+    for t in range(steps):
+        x = workloads.decode_step_inputs(B, H, d, d, step=t, dtype="bf16", seed=seed,
+                                         beta_scale=w["beta_scale"])
+        o = step(dev(x.q), dev(x.k), dev(x.v), dev(x.beta), dev(g), S)
+        for n in ("q", "k", "v", "beta"):
+            rec[n].append(take_heads(getattr(x, n), bi, hi))
+        rec["o"].append(take_heads(o.cpu(), bi, hi))
+    torch.cuda.synchronize()
+    st = {n: torch.stack(v_, dim=2) for n, v_ in rec.items()}  # [1, n, steps, ...]
+    g_s = take_heads(g, bi, hi)
+    g_seq = (g_s[:, :, None, :] if form == "kda" else g_s[:, :, None]).expand(
+        *st["beta"].shape, *([d] if form == "kda" else [])).contiguous()
+    f = oracle.forward_kda if form == "kda" else oracle.forward_gated
+    o_ref, S_ref = f(st["q"], st["k"], st["v"], st["beta"], g_seq, take_heads(S0, bi, hi))
+    _check(st["o"].double().numpy(), take_heads(S.cpu(), bi, hi).double().numpy(), o_ref, S_ref,
+           torch.bfloat16, f"{form} decode, bench shape")

@@ -82,3 +82,29 @@ def test_varlen_all_empty_passes_the_states_through():
     o, S = dn.chunk_fwd_varlen(z, z, z, torch.zeros(H, 0, dtype=torch.bfloat16, device="cuda"),
                                [0, 0, 0, 0], initial_state=S0)
     assert torch.equal(S, S0) and o.numel() == 0
+
+
+def test_varlen_bench_packing_sampled_sequences():
+    """The bench's packing: the 1.3B-layer tokens (B8 x T2048 per head, H16,
+    d128, bf16) re-read head-major as 64 packed sequences of seeded lengths,
+    on the tensor-core path; five sequences on two heads checked against
+    the oracle (outputs and final states), first and last included."""
+    w = workloads.WORKLOADS["layer1p3b_bf16"]
+    inp = workloads.workload_inputs("layer1p3b_bf16")
+    B, H, T, d = inp.q.shape
+    lens = workloads.varlen_lengths(64, B * T, seed=w["seed"])
+    cu = [0]
+    for ln in lens:
+        cu.append(cu[-1] + ln)
+    vq, vk, vv = (x.transpose(0, 1).reshape(H, B * T, -1).contiguous() for x in (inp.q, inp.k, inp.v))
+    vb = inp.beta.transpose(0, 1).reshape(H, B * T).contiguous()
+    o, S = dn.chunk_fwd_varlen(vq.cuda(), vk.cuda(), vv.cuda(), vb.cuda(), cu)
+    torch.cuda.synchronize()
+    o, S = o.cpu(), S.cpu()
+    for n in (0, 17, 40, 62, 63):
+        a, b = cu[n], cu[n + 1]
+        for h in (0, H - 1):
+            o_ref, S_ref = oracle.forward(vq[None, h:h + 1, a:b], vk[None, h:h + 1, a:b],
+                                          vv[None, h:h + 1, a:b], vb[None, h:h + 1, a:b])
+            assert rel_l2(o[h, a:b].double().numpy(), o_ref[0, 0]) <= TOL[torch.bfloat16], (n, h)
+            assert rel_l2(S[n, h].double().numpy(), S_ref[0, 0]) <= TOL[torch.bfloat16], (n, h)

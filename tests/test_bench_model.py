@@ -85,3 +85,14 @@ def test_traffic_table_entries_name_their_capture():
         assert set(entry) == {"bytes_per_launch", "source_sha", "capture"}, name
         assert (Path(bench.ROOT) / entry["capture"]).exists(), entry["capture"]
         assert entry["bytes_per_launch"] > 0
+
+
+def test_varlen_packing_covers_every_token_once():
+    """The bench's packed-sequence leg: 64 seeded lengths that tile the
+    headline's B * T tokens per head exactly, none negative, the same for the
+    same seed (so the bench and its full-size parity test pack alike)."""
+    import workloads
+    lens = workloads.varlen_lengths(64, B * T, seed=1002)
+    assert len(lens) == 64 and sum(lens) == B * T and min(lens) >= 0
+    assert lens == workloads.varlen_lengths(64, B * T, seed=1002)
+    assert max(lens) > min(lens)  # ragged, not an even split

@@ -27,8 +27,13 @@
  *   - Arguments are checked on the host before anything is enqueued; a
  *     rejected call enqueues nothing.  Kernels have no device traps and no
  *     unbounded waits.  Launch failures are reported as DN_ERR_CUDA.
- *   - The library keeps no mutable global state apart from a thread-local
- *     error message, so calls from several threads are safe.
+ *   - Global state: a thread-local error message (dn_last_error); per device,
+ *     one word where a tensor-core kernel records the first of its bounded
+ *     waits that ran out (read and cleared by dn_device_error); and the
+ *     static scratch array of dn_chunk_fwd_noalloc with its looked-up device
+ *     address.  Calls from several threads are safe, except that
+ *     dn_chunk_fwd_noalloc calls whose kernels overlap on one device race on
+ *     that array.
  */
 #ifndef DELTANET_H
 #define DELTANET_H
@@ -179,7 +184,9 @@ DN_API const char *dn_last_error(void);
  *     on the GPU (on different streams, say) race; serialise them.
  *   - The first call on each device looks the array's address up
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the life of the
+ *     process: after cudaDeviceReset (which unloads the library's device
+ *     code) do not call this entry point again on that device.
  *   - It calls no cudaMalloc, cudaFree or other allocating routine.
  * Arguments, layouts and the remaining errors are those of dn_chunk_fwd.
  */

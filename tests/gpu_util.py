@@ -43,3 +43,48 @@ def take_heads(x, bi, hi):
     if x is None:
         return None
     return x[torch.as_tensor(bi), torch.as_tensor(hi)].unsqueeze(0)
+
+
+def per_head_rel_l2(x, ref):
+    """Relative L2 error of every (batch, head) slice of [B, H, ...] arrays."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert x.shape == ref.shape, (x.shape, ref.shape)
+    B, H = ref.shape[:2]
+    num = np.linalg.norm((x - ref).reshape(B, H, -1), axis=2)
+    den = np.linalg.norm(ref.reshape(B, H, -1), axis=2)
+    return np.where(den > 0, num / np.where(den > 0, den, 1.0), num)
+
+
+def per_chunk_rel_l2(o, o_ref, C=64):
+    """Relative L2 error of every (batch, head, C-token chunk) of [B, H, T, d]
+    outputs; the last chunk may be short."""
+    o = np.asarray(o, dtype=np.float64)
+    o_ref = np.asarray(o_ref, dtype=np.float64)
+    B, H, T, d = o_ref.shape
+    n = (T + C - 1) // C
+    pad = n * C - T
+    diff = np.pad(o - o_ref, ((0, 0), (0, 0), (0, pad), (0, 0))).reshape(B, H, n, C * d)
+    ref = np.pad(o_ref, ((0, 0), (0, 0), (0, pad), (0, 0))).reshape(B, H, n, C * d)
+    num, den = np.linalg.norm(diff, axis=3), np.linalg.norm(ref, axis=3)
+    return np.where(den > 0, num / np.where(den > 0, den, 1.0), num)
+
+
+def check_every_head(o, S, o_ref, S_ref, tol, what=""):
+    """The parity bar on every (batch, head) separately, for o and the final
+    state, and on every 64-token chunk of o: one wrong head, or one wrong
+    chunk inside a head, fails even when the whole-tensor error would hide
+    it.  Returns the worst errors seen."""
+    eo = per_head_rel_l2(o, o_ref)
+    ec = per_chunk_rel_l2(o, o_ref)
+    worst = {"o_head": float(eo.max()), "o_chunk": float(ec.max())}
+    bo = np.unravel_index(int(np.argmax(eo)), eo.shape)
+    assert eo.max() <= tol, f"{what} o rel L2 {eo.max():.3e} at (b, h) = {bo}"
+    bc = np.unravel_index(int(np.argmax(ec)), ec.shape)
+    assert ec.max() <= tol, f"{what} o rel L2 {ec.max():.3e} at (b, h, chunk) = {bc}"
+    if S is not None or S_ref is not None:
+        eS = per_head_rel_l2(S, S_ref)
+        worst["S_head"] = float(eS.max())
+        bS = np.unravel_index(int(np.argmax(eS)), eS.shape)
+        assert eS.max() <= tol, f"{what} S_T rel L2 {eS.max():.3e} at (b, h) = {bS}"
+    return worst

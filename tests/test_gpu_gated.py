@@ -4,6 +4,7 @@ relative L2 <= 1e-4 (fp32 I/O) and <= 1e-2 (bf16 I/O) on o and the state.
 The chunkwise form has two kernels: the fp32 CUDA-core one (workspace=None,
 every shape) and the two-pass tcgen05 one (a workspace, dk = dv = 128 bf16).
 """
+import functools
 import numpy as np
 import pytest
 import torch
@@ -12,7 +13,7 @@ import delta_rule_recurrent_gb300 as dn
 import oracle
 import workloads
 from tests.conftest import rel_l2
-from tests.gpu_util import TOL, dev, sample_heads, take_heads
+from tests.gpu_util import TOL, check_every_head, dev, sample_heads, take_heads
 
 pytestmark = pytest.mark.gpu
 
@@ -132,20 +133,25 @@ def test_gated_tc_workspace_too_small_is_rejected():
                            workspace=ws)
 
 
-@pytest.mark.parametrize("workspace", ["auto", None], ids=["tcgen05", "cuda-cores"])
-def test_gated_layer_1p3b_sampled_heads(workspace):
+@functools.lru_cache(maxsize=1)
+def _oracle_gated_1p3b():
+    """The gated oracle on the whole 1.3B-layer workload, once per session."""
     inp = workloads.workload_inputs("layer1p3b_bf16")
     B, H, T, d = inp.q.shape
     g = workloads.gate_inputs(B, H, T, seed=7)
+    return inp, g, oracle.forward_gated(inp.q, inp.k, inp.v, inp.beta, g)
+
+
+@pytest.mark.parametrize("workspace", ["auto", None], ids=["tcgen05", "cuda-cores"])
+def test_gated_layer_1p3b_every_head(workspace):
+    """The 1.3B-layer shape with keep rates in (0.9, 1): every head and every
+    64-token chunk against the gated oracle."""
+    inp, g, (o_ref, S_ref) = _oracle_gated_1p3b()
     o, S = dn.chunk_fwd_gated(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g),
                               workspace=workspace)
     torch.cuda.synchronize()
-    bi, hi = sample_heads(B, H, 4, seed=8)
-    o_ref, S_ref = oracle.forward_gated(*(take_heads(x, bi, hi) for x in
-                                          (inp.q, inp.k, inp.v, inp.beta, g)))
-    ib, ih = torch.as_tensor(bi).cuda(), torch.as_tensor(hi).cuda()
-    _check(o[ib, ih].double().cpu().numpy()[None], S[ib, ih].double().cpu().numpy()[None],
-           o_ref, S_ref, torch.bfloat16, "1.3B")
+    check_every_head(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
+                     TOL[torch.bfloat16], "gated 1.3B")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])

@@ -9,7 +9,7 @@ import delta_rule_recurrent_gb300 as dn
 import oracle
 import workloads
 from tests.conftest import rel_l2
-from tests.gpu_util import TOL, dev, sample_heads, take_heads
+from tests.gpu_util import TOL, check_every_head, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -67,18 +67,17 @@ def test_kda_strong_decay_and_edge_lengths():
                torch.float32, f"T={T}")
 
 
-def test_kda_layer_1p3b_sampled_heads():
+def test_kda_layer_1p3b_every_head():
+    """The 1.3B-layer shape with per-channel keep rates in (0.9, 1): every head
+    and every 64-token chunk against the KDA oracle."""
     inp = workloads.workload_inputs("layer1p3b_bf16")
     B, H, T, d = inp.q.shape
     g = workloads.gate_inputs(B, H, T, seed=9, channels=d)
     o, S = dn.chunk_fwd_kda(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g))
     torch.cuda.synchronize()
-    bi, hi = sample_heads(B, H, 3, seed=10)
-    o_ref, S_ref = oracle.forward_kda(*(take_heads(x, bi, hi) for x in
-                                        (inp.q, inp.k, inp.v, inp.beta, g)))
-    ib, ih = torch.as_tensor(bi).cuda(), torch.as_tensor(hi).cuda()
-    _check(o[ib, ih].double().cpu().numpy()[None], S[ib, ih].double().cpu().numpy()[None],
-           o_ref, S_ref, torch.bfloat16, "1.3B")
+    o_ref, S_ref = oracle.forward_kda(inp.q, inp.k, inp.v, inp.beta, g)
+    check_every_head(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
+                     TOL[torch.bfloat16], "KDA 1.3B")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])

@@ -422,6 +422,22 @@ def run_ours(args, rank, world, local):
         pr_region_s = max_over_ranks(pr_region_s, world)
         del qc, kc
 
+        # ---------------- the same call on raw q, k, prepared in its kernels --
+        raw = workloads.workload_inputs(HEADLINE, normalize=False)
+        rq, rk = raw.q.to(dev), raw.k.to(dev)
+        del raw
+
+        def fused_prep_step(_i):
+            dn.chunk_fwd(rq, rk, v, beta, out=o, final_state=S_T, algo=algo, workspace=ws,
+                         qk_l2norm=True, scale=dk ** -0.5)
+
+        for i in range(min(args.warmup, 3)):
+            fused_prep_step(i)
+        torch.cuda.synchronize()
+        fp_region_s, fp_launch = timed_loop(fused_prep_step, psteps, stream, world)
+        fp_region_s = max_over_ranks(fp_region_s, world)
+        del rq, rk
+
         # ---------------- Gated DeltaNet: chunk forward and decode step -----
         gate = workloads.gate_inputs(B, H, T, seed=w["seed"]).to(dev)
         og = torch.empty_like(o)
@@ -616,6 +632,18 @@ def run_ours(args, rank, world, local):
                      "peak_source": f"{peak_src} (copy bandwidth)", "bytes_per_launch": pbytes,
                      "launch_us": pr_launch_s * 1e6},
     }
+    fp_launch_s = statistics.mean(fp_launch) / 1e3
+    qk_prep["in_kernel"] = {
+        "op": "the headline chunk forward on raw q, k with qk_l2norm=True, scale=dk^-0.5 "
+              "(normalised and scaled as the kernels load them)",
+        "steps": psteps, "value": world * tokens * psteps / fp_region_s, "unit": "tokens/s",
+        "ms_per_step": 1e3 * fp_region_s / psteps, "launch_us": fp_launch_s * 1e6,
+        "vs_plain_call": fp_launch_s / launch_s,
+        "roofline": {"bound": "hbm", "achieved": cbytes / fp_launch_s / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": cbytes / fp_launch_s / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{peak_src} (copy bandwidth)", "bytes_per_launch": cbytes},
+    }
     g_launch_s = statistics.mean(g_launch) / 1e3
     gs_launch_s = statistics.mean(gs_launch) / 1e3
     gflops = chunk_flops_per_token_head(C, dk, dv) * B * H * T
@@ -714,6 +742,7 @@ def run_ours(args, rank, world, local):
                          + (4 if bwd_tc else 3) * bwd_steps             # recompute, chain, grads
                          + launches_per_call * vsteps                   # varlen
                          + psteps                                       # q/k preparation
+                         + launches_per_call * psteps                   # forward preparing q, k
                          + (2 if gneed else 1) * gsteps + gsteps + nsteps  # gated: both forms, decode
                          + gsteps + nsteps),                            # KDA chunk, decode
         "clocks": clk,

@@ -16,23 +16,29 @@ the computation runs in the library's sm_103a kernels.
         # Gated DeltaNet: log keep rate g per token (per head for a step)
     chunk_fwd_kda(q, k, v, beta, g, ...), recurrent_step_kda(q, k, v, beta, g, state)
         # KDA: one log keep rate per key channel
-    qk_prepare(q, k, scale=1.0, l2norm=True)  # optional q/k L2-norm and query scale
+    qk_prepare(q, k, scale=1.0, l2norm=True)  # the q/k L2-norm and query scale as a pass
+    qk_prepare_bwd(q, k, d_q_out, d_k_out, scale, l2norm)  # its gradient
 
 Shapes: q, k ``[B, H, T, dk]``; v ``[B, H, T, dv]``; beta ``[B, H, T]``;
 state ``[B, H, dk, dv]`` fp32 (the pages' dv x dk state, transposed).  For a
 decoding step the T axis is absent.  q and k are used as given unless a
-forward is called with ``qk_l2norm=True`` and/or ``scale=...``, which run
-``qk_prepare`` on them first (the backward takes prepared q and k).
+forward or step is called with ``qk_l2norm=True`` and/or ``scale=...``: the
+kernels then L2-normalise q and k (and scale q) as they load them (the
+``*_qk`` entry points); the backward takes prepared q and k, and
+``DeltaRule`` chains the preparation's gradient after it.
 """
 from __future__ import annotations
 
 import torch
 
+import ctypes
+
 from ._lib import (DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05, DN_BF16, DN_F32,
-                   DeltaNetError, check, header_symbols, lib_path, load)
+                   DeltaNetError, QkNorm, check, header_symbols, lib_path, load)
 
 __all__ = ["chunk_fwd", "chunk_bwd", "recurrent_step", "chunk_fwd_varlen", "chunk_fwd_gated",
-           "recurrent_step_gated", "chunk_fwd_kda", "recurrent_step_kda", "qk_prepare", "DeltaRule", "DeltaNetError", "load", "lib_path",
+           "recurrent_step_gated", "chunk_fwd_kda", "recurrent_step_kda", "qk_prepare",
+           "qk_prepare_bwd", "DeltaRule", "DeltaNetError", "load", "lib_path",
            "header_symbols", "ALGOS"]
 
 ALGOS = {"auto": DN_ALGO_AUTO, "simt": DN_ALGO_SIMT, "tcgen05": DN_ALGO_TCGEN05}
@@ -82,11 +88,44 @@ def qk_prepare(q: torch.Tensor, k: torch.Tensor, scale: float = 1.0, l2norm: boo
     return q_out, k_out
 
 
-def _prepared(q, k, scale, qk_l2norm):
-    """q and k after the optional preparation a forward was asked for."""
+def qk_prepare_bwd(q: torch.Tensor, k: torch.Tensor, d_q_out: torch.Tensor,
+                   d_k_out: torch.Tensor | None, scale: float = 1.0, l2norm: bool = True,
+                   eps: float = 1e-6):
+    """Gradient of ``qk_prepare`` (``dn_qk_prepare_bwd``): given the raw q, k
+    and the gradients of the prepared q', k', returns ``(d_q, d_k)`` with
+    respect to the raw inputs (``d_k`` is ``d_k_out`` itself without
+    ``l2norm``, since k is then used as given)."""
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("d_q_out", d_q_out)):
+        _check_cuda(name, t, dev)
+    dt = _dtype_code(q)
+    if k.shape != q.shape or d_q_out.shape != q.shape or k.dtype != q.dtype or \
+            d_q_out.dtype != q.dtype:
+        raise ValueError("q, k and d_q_out must share one shape and dtype")
+    if l2norm:
+        _check_cuda("d_k_out", d_k_out, dev)
+        if d_k_out.shape != q.shape or d_k_out.dtype != q.dtype:
+            raise ValueError("d_k_out must match q")
+    d = q.shape[-1]
+    rows = q.numel() // d if d else 0
+    d_q = torch.empty_like(q)
+    d_k = torch.empty_like(k) if l2norm else d_k_out
+    lib = load()
+    with torch.cuda.device(dev):
+        check(lib.dn_qk_prepare_bwd(
+            q.data_ptr(), k.data_ptr(), d_q_out.data_ptr(),
+            d_k_out.data_ptr() if l2norm else None, d_q.data_ptr(),
+            d_k.data_ptr() if l2norm else None, rows, d, int(bool(l2norm)), float(scale),
+            float(eps), dt, _stream_handle(dev)))
+    return d_q, d_k
+
+
+def _norm(scale, qk_l2norm, eps=1e-6):
+    """The dn_qk_norm a forward or step was asked for (None: none)."""
     if scale is None and not qk_l2norm:
-        return q, k
-    return qk_prepare(q, k, 1.0 if scale is None else scale, bool(qk_l2norm))
+        return None
+    return ctypes.byref(QkNorm(int(bool(qk_l2norm)), 1.0 if scale is None else float(scale),
+                               float(eps)))
 
 
 def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
@@ -102,7 +141,8 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Ten
     allocates the scratch ``dn_chunk_fwd_workspace_bytes`` asks for (the
     two-pass tensor-core path), None runs without scratch (one fused kernel),
     and a uint8 CUDA tensor of at least that many bytes is used as given.
-    ``qk_l2norm`` / ``scale`` run ``qk_prepare`` on q and k first.
+    ``qk_l2norm`` / ``scale``: the kernels L2-normalise q and k and scale q
+    as they load them (``dn_chunk_fwd_qk``).
     """
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
@@ -116,7 +156,6 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Ten
     dv = v.shape[3]
     if tuple(v.shape[:3]) != (B, H, T) or tuple(beta.shape) != (B, H, T):
         raise ValueError("v must be [B,H,T,dv] and beta [B,H,T]")
-    q, k = _prepared(q, k, scale, qk_l2norm)
     if initial_state is not None:
         _check_cuda("initial_state", initial_state, dev)
         if initial_state.dtype != torch.float32 or tuple(initial_state.shape) != (B, H, dk, dv):
@@ -146,13 +185,13 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Ten
         _check_cuda("workspace", workspace, dev)
         ws, ws_bytes = workspace, workspace.numel() * workspace.element_size()
     with torch.cuda.device(dev):
-        check(lib.dn_chunk_fwd_algo(
+        check(lib.dn_chunk_fwd_qk(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(),
             initial_state.data_ptr() if initial_state is not None else None,
             out.data_ptr(), S_T.data_ptr() if S_T is not None else None,
             B, H, T, dk, dv, chunk_size, dt,
             ws.data_ptr() if ws is not None else None, ws_bytes,
-            _stream_handle(dev), ALGOS[algo]))
+            _stream_handle(dev), ALGOS[algo], _norm(scale, qk_l2norm)))
     return out, S_T
 
 
@@ -161,7 +200,8 @@ def recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torc
                    scale: float | None = None, qk_l2norm: bool = False) -> torch.Tensor:
     """One fused decoding step (``dn_recurrent_step``); ``state`` is updated
     in place and the step's output ``o`` ``[B, H, dv]`` is returned.
-    ``qk_l2norm`` / ``scale`` run ``qk_prepare`` on q and k first."""
+    ``qk_l2norm`` / ``scale``: the step L2-normalises q and k and scales q
+    as it loads them."""
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("state", state)):
         _check_cuda(name, t, dev)
@@ -174,7 +214,6 @@ def recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torc
     dv = v.shape[2]
     if tuple(v.shape[:2]) != (B, H) or tuple(beta.shape) != (B, H):
         raise ValueError("v must be [B,H,dv] and beta [B,H]")
-    q, k = _prepared(q, k, scale, qk_l2norm)
     if state.dtype != torch.float32 or tuple(state.shape) != (B, H, dk, dv):
         raise ValueError("state must be float32 [B,H,dk,dv]")
     if out is None:
@@ -185,9 +224,9 @@ def recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torc
             raise ValueError("out must be [B,H,dv] in q's dtype")
     lib = load()
     with torch.cuda.device(dev):
-        check(lib.dn_recurrent_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(),
-                                    state.data_ptr(), out.data_ptr(), B, H, dk, dv, dt,
-                                    _stream_handle(dev)))
+        check(lib.dn_recurrent_step_qk(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                       beta.data_ptr(), state.data_ptr(), out.data_ptr(), B, H,
+                                       dk, dv, dt, _stream_handle(dev), _norm(scale, qk_l2norm)))
     return out
 
 
@@ -242,23 +281,23 @@ def chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Ten
 
 class DeltaRule(torch.autograd.Function):
     """Autograd wrapper: ``DeltaRule.apply(q, k, v, beta, initial_state,
-    scale)`` returns ``(o, final_state)`` from ``chunk_fwd``; the backward
-    pass calls ``chunk_bwd`` (the chunk states are recomputed there, not
-    stored).  ``scale`` (None for none) multiplies q before the recurrence
-    (``qk_prepare``); the backward multiplies the q gradient by it with the
-    same kernel, since d(s q) = s dq.  The L2 normalisation has no backward
-    here: pass normalised q and k."""
+    scale, qk_l2norm)`` returns ``(o, final_state)`` from ``chunk_fwd``; the
+    backward pass calls ``chunk_bwd`` (the chunk states are recomputed there,
+    not stored).  ``qk_l2norm`` L2-normalises q and k and ``scale`` (None for
+    none) multiplies q, inside the forward's kernels; the backward forms the
+    prepared q and k again (``qk_prepare``), takes the recurrence's gradient
+    with respect to them and chains the preparation's gradient
+    (``qk_prepare_bwd``) to reach the raw q and k."""
 
     @staticmethod
-    def forward(ctx, q, k, v, beta, initial_state=None, scale=None):
+    def forward(ctx, q, k, v, beta, initial_state=None, scale=None, qk_l2norm=False):
         q, k, v, beta = (t.contiguous() for t in (q, k, v, beta))
         if initial_state is not None:
             initial_state = initial_state.contiguous()
-        if scale is not None:
-            q, _ = qk_prepare(q, k, scale=scale, l2norm=False)
-        o, S_T = chunk_fwd(q, k, v, beta, initial_state=initial_state, output_final_state=True)
+        o, S_T = chunk_fwd(q, k, v, beta, initial_state=initial_state, output_final_state=True,
+                           scale=scale, qk_l2norm=qk_l2norm)
         ctx.save_for_backward(q, k, v, beta, initial_state)
-        ctx.scale = scale
+        ctx.scale, ctx.l2norm = scale, bool(qk_l2norm)
         return o, S_T
 
     @staticmethod
@@ -266,10 +305,13 @@ class DeltaRule(torch.autograd.Function):
         q, k, v, beta, S0 = ctx.saved_tensors
         d_o = torch.zeros_like(v) if d_o is None else d_o.contiguous()
         d_S_T = None if d_S_T is None else d_S_T.contiguous().float()
-        d_q, d_k, d_v, d_beta, d_S0 = chunk_bwd(q, k, v, beta, d_o.to(v.dtype), S0, d_S_T)
-        if ctx.scale is not None:
-            qk_prepare(d_q, d_q, scale=ctx.scale, l2norm=False, inplace=True)
-        return d_q, d_k, d_v, d_beta, (d_S0 if S0 is not None else None), None
+        prepared = ctx.scale is not None or ctx.l2norm
+        scale = 1.0 if ctx.scale is None else ctx.scale
+        qp, kp = qk_prepare(q, k, scale=scale, l2norm=ctx.l2norm) if prepared else (q, k)
+        d_q, d_k, d_v, d_beta, d_S0 = chunk_bwd(qp, kp, v, beta, d_o.to(v.dtype), S0, d_S_T)
+        if prepared:
+            d_q, d_k = qk_prepare_bwd(q, k, d_q, d_k, scale=scale, l2norm=ctx.l2norm)
+        return d_q, d_k, d_v, d_beta, (d_S0 if S0 is not None else None), None, None
 
 
 def _check_gate(g: torch.Tensor, shape, dev) -> None:
@@ -288,7 +330,7 @@ def chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: tor
     ``workspace``: "auto" allocates the scratch of the two-pass tensor-core
     form where it applies (``dn_chunk_fwd_gated_workspace_bytes``), None runs
     the fp32 CUDA-core kernel, a uint8 CUDA tensor supplies the scratch.
-    ``qk_l2norm`` / ``scale`` run ``qk_prepare`` on q and k first."""
+    ``qk_l2norm`` / ``scale``: prepared inside the kernels, as ``chunk_fwd``."""
     return _chunk_decayed(q, k, v, beta, g, False, initial_state, output_final_state,
                           chunk_size, out, final_state, workspace, scale, qk_l2norm)
 
@@ -297,13 +339,16 @@ def chunk_fwd_kda(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch
                   g: torch.Tensor, initial_state: torch.Tensor | None = None,
                   output_final_state: bool = True, chunk_size: int = 64,
                   out: torch.Tensor | None = None, final_state: torch.Tensor | None = None,
-                  scale: float | None = None, qk_l2norm: bool = False):
+                  workspace="auto", scale: float | None = None, qk_l2norm: bool = False):
     """Kimi Delta Attention, chunkwise (``dn_chunk_fwd_kda``): ``g`` is the
     fp32 ``[B, H, T, dk]`` per-key-channel log keep rate.  The page's read
     scales q by d_k^{-1/2}: ``scale=dk ** -0.5`` applies it.
-    ``qk_l2norm`` / ``scale`` run ``qk_prepare`` on q and k first."""
+    ``qk_l2norm`` / ``scale``: prepared inside the kernels, as ``chunk_fwd``.
+    ``workspace``: "auto" allocates the scratch of the tensor-core form where
+    it applies (``dn_chunk_fwd_kda_workspace_bytes``), None runs the fp32
+    CUDA-core kernel, a uint8 CUDA tensor supplies the scratch."""
     return _chunk_decayed(q, k, v, beta, g, True, initial_state, output_final_state,
-                          chunk_size, out, final_state, None, scale, qk_l2norm)
+                          chunk_size, out, final_state, workspace, scale, qk_l2norm)
 
 
 def _chunk_decayed(q, k, v, beta, g, per_channel, initial_state, output_final_state,
@@ -320,7 +365,6 @@ def _chunk_decayed(q, k, v, beta, g, per_channel, initial_state, output_final_st
     dv = v.shape[3]
     if tuple(v.shape[:3]) != (B, H, T) or tuple(beta.shape) != (B, H, T):
         raise ValueError("v must be [B,H,T,dv] and beta [B,H,T]")
-    q, k = _prepared(q, k, scale, qk_l2norm)
     _check_gate(g, (B, H, T, dk) if per_channel else (B, H, T), dev)
     if initial_state is not None:
         _check_cuda("initial_state", initial_state, dev)
@@ -343,22 +387,22 @@ def _chunk_decayed(q, k, v, beta, g, per_channel, initial_state, output_final_st
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(), g.data_ptr(),
             initial_state.data_ptr() if initial_state is not None else None, out.data_ptr(),
             S_T.data_ptr() if S_T is not None else None, B, H, T, dk, dv, chunk_size, dt)
+    sizer = (lib.dn_chunk_fwd_kda_workspace_bytes if per_channel
+             else lib.dn_chunk_fwd_gated_workspace_bytes)
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be 'auto', None or a uint8 CUDA tensor")
+        need = sizer(B, H, T, dk, dv, chunk_size, dt)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
+    else:
+        ws = workspace
+        if ws is not None:
+            _check_cuda("workspace", ws, dev)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    entry = lib.dn_chunk_fwd_kda_qk if per_channel else lib.dn_chunk_fwd_gated_qk
     with torch.cuda.device(dev):
-        if per_channel:
-            check(lib.dn_chunk_fwd_kda(*args, _stream_handle(dev)))
-            return out, S_T
-        if isinstance(workspace, str):
-            if workspace != "auto":
-                raise ValueError("workspace must be 'auto', None or a uint8 CUDA tensor")
-            need = lib.dn_chunk_fwd_gated_workspace_bytes(B, H, T, dk, dv, chunk_size, dt)
-            ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
-        else:
-            ws = workspace
-            if ws is not None:
-                _check_cuda("workspace", ws, dev)
-        ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
-        check(lib.dn_chunk_fwd_gated(*args, ws.data_ptr() if ws is not None else None, ws_bytes,
-                                     _stream_handle(dev)))
+        check(entry(*args, ws.data_ptr() if ws is not None else None, ws_bytes,
+                    _stream_handle(dev), _norm(scale, qk_l2norm)))
     return out, S_T
 
 
@@ -368,7 +412,7 @@ def recurrent_step_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta
                          qk_l2norm: bool = False) -> torch.Tensor:
     """One Gated DeltaNet decoding step (``dn_recurrent_step_gated``); ``g``
     is the fp32 ``[B, H]`` log keep rate; ``state`` is updated in place.
-    ``qk_l2norm`` / ``scale`` run ``qk_prepare`` on q and k first."""
+    ``qk_l2norm`` / ``scale``: prepared inside the kernel."""
     return _step_decayed(q, k, v, beta, g, False, state, out, scale, qk_l2norm)
 
 
@@ -378,7 +422,7 @@ def recurrent_step_kda(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: 
                        qk_l2norm: bool = False) -> torch.Tensor:
     """One KDA decoding step (``dn_recurrent_step_kda``); ``g`` is the fp32
     ``[B, H, dk]`` per-key-channel log keep rate; ``state`` updated in place.
-    ``qk_l2norm`` / ``scale`` run ``qk_prepare`` on q and k first."""
+    ``qk_l2norm`` / ``scale``: prepared inside the kernel."""
     return _step_decayed(q, k, v, beta, g, True, state, out, scale, qk_l2norm)
 
 
@@ -395,7 +439,6 @@ def _step_decayed(q, k, v, beta, g, per_channel, state, out, scale=None, qk_l2no
     dv = v.shape[2]
     if tuple(v.shape[:2]) != (B, H) or tuple(beta.shape) != (B, H):
         raise ValueError("v must be [B,H,dv] and beta [B,H]")
-    q, k = _prepared(q, k, scale, qk_l2norm)
     _check_gate(g, (B, H, dk) if per_channel else (B, H), dev)
     if state.dtype != torch.float32 or tuple(state.shape) != (B, H, dk, dv):
         raise ValueError("state must be float32 [B,H,dk,dv]")
@@ -407,9 +450,10 @@ def _step_decayed(q, k, v, beta, g, per_channel, state, out, scale=None, qk_l2no
             raise ValueError("out must be [B,H,dv] in q's dtype")
     lib = load()
     with torch.cuda.device(dev):
-        entry = lib.dn_recurrent_step_kda if per_channel else lib.dn_recurrent_step_gated
+        entry = lib.dn_recurrent_step_kda_qk if per_channel else lib.dn_recurrent_step_gated_qk
         check(entry(q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(), g.data_ptr(),
-                    state.data_ptr(), out.data_ptr(), B, H, dk, dv, dt, _stream_handle(dev)))
+                    state.data_ptr(), out.data_ptr(), B, H, dk, dv, dt, _stream_handle(dev),
+                    _norm(scale, qk_l2norm)))
     return out
 
 
@@ -424,9 +468,8 @@ def chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
     offsets.  Returns ``(o [H, T, dv], S_T [N, H, dk, dv] or None)``.
     ``workspace``: "auto" (the two-pass tensor-core path where it applies),
     None (the CUDA-core path) or a uint8 CUDA tensor.
-    ``qk_l2norm`` / ``scale`` run ``qk_prepare`` on q and k first.
+    ``qk_l2norm`` / ``scale``: prepared inside the kernels, as ``chunk_fwd``.
     """
-    import ctypes
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
         _check_cuda(name, t, dev)
@@ -439,7 +482,6 @@ def chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
     dv = v.shape[2]
     if tuple(v.shape[:2]) != (H, T) or tuple(beta.shape) != (H, T):
         raise ValueError("v must be [H,T,dv] and beta [H,T]")
-    q, k = _prepared(q, k, scale, qk_l2norm)
     cu = [int(x) for x in cu_seqlens]
     N = len(cu) - 1
     cu_arr = (ctypes.c_int * len(cu))(*cu)
@@ -462,9 +504,10 @@ def chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
             _check_cuda("workspace", ws, dev)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     with torch.cuda.device(dev):
-        check(lib.dn_chunk_fwd_varlen(
+        check(lib.dn_chunk_fwd_varlen_qk(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(),
             initial_state.data_ptr() if initial_state is not None else None, out.data_ptr(),
             S_T.data_ptr() if S_T is not None else None, cu_arr, N, H, T, dk, dv, chunk_size, dt,
-            ws.data_ptr() if ws is not None else None, ws_bytes, _stream_handle(dev)))
+            ws.data_ptr() if ws is not None else None, ws_bytes, _stream_handle(dev),
+            _norm(scale, qk_l2norm)))
     return out, S_T

@@ -16,10 +16,20 @@ HEADER = INCLUDE / "deltanet.h"
 DN_OK, DN_ERR_INVALID_ARG, DN_ERR_UNSUPPORTED, DN_ERR_CUDA = 0, 1, 2, 3
 DN_F32, DN_BF16 = 0, 1
 DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05 = 0, 1, 2
+ABI_VERSION = 4
 
 _vp, _fp = ctypes.c_void_p, ctypes.c_void_p
 _int, _size = ctypes.c_int, ctypes.c_size_t
 _ip = ctypes.POINTER(ctypes.c_int)
+_f32, _ll = ctypes.c_float, ctypes.c_longlong
+
+
+class QkNorm(ctypes.Structure):
+    """dn_qk_norm: the in-kernel preparation of q and k."""
+    _fields_ = [("l2norm", ctypes.c_int), ("scale", ctypes.c_float), ("eps", ctypes.c_float)]
+
+
+_np = ctypes.POINTER(QkNorm)
 
 # Signatures of every entry point in include/deltanet.h.
 SIGNATURES = {
@@ -44,8 +54,22 @@ SIGNATURES = {
     "dn_recurrent_step_gated": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp] + [_int] * 5 + [_vp]),
     "dn_chunk_fwd_kda": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp] + [_int] * 7 + [_vp]),
     "dn_recurrent_step_kda": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp] + [_int] * 5 + [_vp]),
-    "dn_qk_prepare": (_int, [_vp, _vp, _vp, _vp, ctypes.c_longlong, _int, _int, ctypes.c_float,
-                              ctypes.c_float, _int, _vp]),
+    "dn_qk_prepare": (_int, [_vp, _vp, _vp, _vp, _ll, _int, _int, _f32, _f32, _int, _vp]),
+    "dn_qk_prepare_bwd": (_int, [_vp] * 6 + [_ll, _int, _int, _f32, _f32, _int, _vp]),
+    "dn_chunk_fwd_qk": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _fp] + [_int] * 7
+                        + [_vp, _size, _vp, _int, _np]),
+    "dn_chunk_fwd_gated_qk": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp] + [_int] * 7
+                              + [_vp, _size, _vp, _np]),
+    "dn_chunk_fwd_varlen_qk": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _fp, _ip] + [_int] * 7
+                               + [_vp, _size, _vp, _np]),
+    "dn_chunk_fwd_kda_qk": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp] + [_int] * 7
+                            + [_vp, _size, _vp, _np]),
+    "dn_chunk_fwd_kda_workspace_bytes": (_size, [_int] * 7),
+    "dn_recurrent_step_qk": (_int, [_vp, _vp, _vp, _vp, _fp, _vp] + [_int] * 5 + [_vp, _np]),
+    "dn_recurrent_step_gated_qk": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp] + [_int] * 5
+                                   + [_vp, _np]),
+    "dn_recurrent_step_kda_qk": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp] + [_int] * 5
+                                 + [_vp, _np]),
     "dn_status_string": (ctypes.c_char_p, [_int]),
     "dn_last_error": (ctypes.c_char_p, []),
     "dn_abi_version": (_int, []),
@@ -92,7 +116,7 @@ def load(path: Path | None = None):
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)
         fn.restype, fn.argtypes = res, args
-    if lib.dn_abi_version() != 3:
+    if lib.dn_abi_version() != ABI_VERSION:
         raise RuntimeError("libdeltanet ABI version mismatch")
     if path is None:
         _lib = lib

@@ -112,23 +112,114 @@ size_t dn_chunk_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, 
     if (B <= 0 || H <= 0 || T <= 0 || C != 64 || !dn::chunk_tc_supports(dk, dv, dt)) return 0;
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return 0;
-    return dn::chunk_tc_workspace_bytes((int)BH, T);
+    const size_t chunks = (size_t)BH * (size_t)((T + 63) / 64);
+    return dn::chunk_tc_workspace_bytes((int)BH, T) + chunks * dn::chunk_tc_side_bytes_per_chunk();
 }
 
-int dn_chunk_fwd_algo(const void* q, const void* k, const void* v, const void* beta,
-                      const float* S0, void* o, float* S_T, int B, int H, int T, int dk,
-                      int dv, int C, int dt, void* workspace, size_t workspace_bytes,
-                      void* stream, int algo) {
-    if (B < 0 || H < 0 || T < 0)
-        return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d T=%d)", B, H, T);
+// The optional in-kernel preparation of q and k (NULL: none).
+static int norm_options(const dn_qk_norm* norm, dn::QkNorm* out) {
+    *out = dn::kNoNorm;
+    if (!norm) return DN_OK;
+    if (!isfinite(norm->scale)) return fail(DN_ERR_INVALID_ARG, "dn_qk_norm.scale must be finite");
+    if (norm->l2norm && (!isfinite(norm->eps) || norm->eps < 0.0f))
+        return fail(DN_ERR_INVALID_ARG, "dn_qk_norm.eps must be finite and >= 0");
+    out->l2norm = norm->l2norm ? 1 : 0;
+    out->qscale = norm->scale;
+    out->eps = norm->l2norm ? norm->eps : 0.0f;
+    return DN_OK;
+}
+
+// The checks every chunkwise forward shares: sizes, dtype, supported shape.
+static int check_chunk_sizes(long long nseq, int H, int T, int dk, int dv, int C, int dt,
+                             const char* nname) {
+    if (nseq < 0 || H < 0 || T < 0)
+        return fail(DN_ERR_INVALID_ARG, "negative size (%s=%lld H=%d T=%d)", nname, nseq, H, T);
     if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
-    if (algo != DN_ALGO_AUTO && algo != DN_ALGO_SIMT && algo != DN_ALGO_TCGEN05)
-        return fail(DN_ERR_INVALID_ARG, "unknown algo %d", algo);
     if (dk <= 0 || dv <= 0 || C <= 0)
         return fail(DN_ERR_INVALID_ARG, "dk, dv and C must be positive");
     if (!supported_dim(dk) || !supported_dim(dv))
         return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this library supports 64 and 128", dk, dv);
     if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this library supports 64", C);
+    return DN_OK;
+}
+
+// The tensors of one chunkwise forward (g: the log keep rates of the
+// decayed forms, g_align its required alignment, 0 when the form has none).
+struct ChunkSpans {
+    Span q, k, v, beta, g, o, S0, S_T;
+    size_t beta_align, g_align, state_bytes;
+};
+
+static ChunkSpans chunk_spans(const void* q, const void* k, const void* v, const void* beta,
+                              const float* g, size_t g_per_token, size_t g_align,
+                              const float* S0, void* o, float* S_T, size_t ntok, long long nstate,
+                              int dk, int dv, int dt) {
+    const size_t es = elem_size(dt);
+    const size_t state_bytes = (size_t)nstate * dk * dv * sizeof(float);
+    return ChunkSpans{Span{"q", q, ntok * dk * es},
+                      Span{"k", k, ntok * dk * es},
+                      Span{"v", v, ntok * dv * es},
+                      Span{"beta", beta, ntok * es},
+                      Span{"g", g, ntok * g_per_token * sizeof(float)},
+                      Span{"o", o, ntok * dv * es},
+                      Span{"S0", S0, state_bytes},
+                      Span{"S_T", S_T, state_bytes},
+                      es, g_align, state_bytes};
+}
+
+// Device, alignment and overlap checks of a chunkwise forward's tensors;
+// with_tokens is false for T = 0 (only the states are touched then).
+static int check_chunk_spans(const ChunkSpans& c, bool with_tokens, int dev) {
+    if (with_tokens) {
+        for (const Span* s : {&c.q, &c.k, &c.v, &c.o})
+            if (int st = check_device_ptr(*s, 16, dev)) return st;
+        if (int st = check_device_ptr(c.beta, c.beta_align, dev)) return st;
+        if (c.g_align)
+            if (int st = check_device_ptr(c.g, c.g_align, dev)) return st;
+    }
+    if (c.S0.p)
+        if (int st = check_device_ptr(c.S0, 16, dev)) return st;
+    if (c.S_T.p)
+        if (int st = check_device_ptr(c.S_T, 16, dev)) return st;
+    if (with_tokens) {
+        for (const Span* s : {&c.q, &c.k, &c.v, &c.beta, &c.g, &c.S0, &c.S_T})
+            if (overlaps(c.o, *s)) return fail(DN_ERR_INVALID_ARG, "o overlaps %s", s->name);
+        for (const Span* s : {&c.q, &c.k, &c.v, &c.beta, &c.g})
+            if (overlaps(c.S_T, *s)) return fail(DN_ERR_INVALID_ARG, "S_T overlaps %s", s->name);
+    }
+    if (c.S_T.p && c.S0.p && c.S_T.p != c.S0.p && overlaps(c.S_T, c.S0))
+        return fail(DN_ERR_INVALID_ARG, "S_T partly overlaps S0");
+    return DN_OK;
+}
+
+// A workspace of `need` bytes: device memory of this device, 16-byte
+// aligned, overlapping none of the call's tensors.
+static int check_workspace(const ChunkSpans& c, void* workspace, size_t need, int dev) {
+    const Span sw{"workspace", workspace, need};
+    if (int st = check_device_ptr(sw, 16, dev)) return st;
+    for (const Span* s : {&c.q, &c.k, &c.v, &c.beta, &c.g, &c.o, &c.S0, &c.S_T})
+        if (overlaps(sw, *s)) return fail(DN_ERR_INVALID_ARG, "workspace overlaps %s", s->name);
+    return DN_OK;
+}
+
+// T = 0: no token, so S_T is S0 (or zeros without S0).
+static int pass_state_through(const float* S0, float* S_T, size_t state_bytes, cudaStream_t st) {
+    if (!S_T || S_T == S0) return ok();
+    if (S0)
+        return cuda_status(cudaMemcpyAsync(S_T, S0, state_bytes, cudaMemcpyDeviceToDevice, st),
+                           "cudaMemcpyAsync(S_T <- S0)");
+    return cuda_status(cudaMemsetAsync(S_T, 0, state_bytes, st), "cudaMemsetAsync(S_T)");
+}
+
+int dn_chunk_fwd_qk(const void* q, const void* k, const void* v, const void* beta,
+                    const float* S0, void* o, float* S_T, int B, int H, int T, int dk, int dv,
+                    int C, int dt, void* workspace, size_t workspace_bytes, void* stream,
+                    int algo, const dn_qk_norm* norm) {
+    if (int st = check_chunk_sizes(B, H, T, dk, dv, C, dt, "B")) return st;
+    if (algo != DN_ALGO_AUTO && algo != DN_ALGO_SIMT && algo != DN_ALGO_TCGEN05)
+        return fail(DN_ERR_INVALID_ARG, "unknown algo %d", algo);
+    dn::QkNorm nm;
+    if (int st = norm_options(norm, &nm)) return st;
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
     const size_t need_ws = dn_chunk_fwd_workspace_bytes(B, H, T, dk, dv, C, dt);
@@ -139,60 +230,39 @@ int dn_chunk_fwd_algo(const void* q, const void* k, const void* v, const void* b
         return fail(DN_ERR_UNSUPPORTED, "tcgen05 path does not cover dk=%d dv=%d dtype=%d", dk,
                     dv, dt);
     if (BH == 0) return ok();
-
-    const size_t es = elem_size(dt);
-    const size_t ntok = (size_t)BH * (size_t)T;
-    const size_t state_bytes = (size_t)BH * dk * dv * sizeof(float);
-    const Span sq{"q", q, ntok * dk * es}, sk{"k", k, ntok * dk * es}, sv{"v", v, ntok * dv * es},
-        sb{"beta", beta, ntok * es}, so{"o", o, ntok * dv * es}, s0{"S0", S0, state_bytes},
-        sT{"S_T", S_T, state_bytes};
+    const ChunkSpans c = chunk_spans(q, k, v, beta, nullptr, 0, 0, S0, o, S_T,
+                                     (size_t)BH * (size_t)T, BH, dk, dv, dt);
     int dev = 0;
     if (int st = current_device(&dev)) return st;
-    if (T > 0) {
-        for (const Span* s : {&sq, &sk, &sv, &so})
-            if (int st = check_device_ptr(*s, 16, dev)) return st;
-        if (int st = check_device_ptr(sb, es, dev)) return st;
-    }
-    if (S0)
-        if (int st = check_device_ptr(s0, 16, dev)) return st;
-    if (S_T)
-        if (int st = check_device_ptr(sT, 16, dev)) return st;
-    if (T > 0)
-        for (const Span* s : {&sq, &sk, &sv, &sb, &s0, &sT})
-            if (overlaps(so, *s)) return fail(DN_ERR_INVALID_ARG, "o overlaps %s", s->name);
-    for (const Span* s : {&sq, &sk, &sv, &sb})
-        if (T > 0 && overlaps(sT, *s)) return fail(DN_ERR_INVALID_ARG, "S_T overlaps %s", s->name);
-    if (S_T && S0 && S_T != S0 && overlaps(sT, s0))
-        return fail(DN_ERR_INVALID_ARG, "S_T partly overlaps S0");
-
+    if (int st = check_chunk_spans(c, T > 0, dev)) return st;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (T == 0) {
-        if (!S_T || S_T == S0) return ok();
-        if (S0)
-            return cuda_status(cudaMemcpyAsync(S_T, S0, state_bytes, cudaMemcpyDeviceToDevice, st),
-                               "cudaMemcpyAsync(S_T <- S0)");
-        return cuda_status(cudaMemsetAsync(S_T, 0, state_bytes, st), "cudaMemsetAsync(S_T)");
-    }
+    if (T == 0) return pass_state_through(S0, S_T, c.state_bytes, st);
     const bool use_tc = algo == DN_ALGO_TCGEN05 ||
                         (algo == DN_ALGO_AUTO && dn::chunk_tc_supports(dk, dv, dt));
     void* const ws = (use_tc && workspace && need_ws > 0) ? workspace : nullptr;
-    if (ws) {
-        const Span sw{"workspace", ws, need_ws};
-        if (int st2 = check_device_ptr(sw, 16, dev)) return st2;
-        for (const Span* s : {&sq, &sk, &sv, &sb, &so, &s0, &sT})
-            if (overlaps(sw, *s)) return fail(DN_ERR_INVALID_ARG, "workspace overlaps %s", s->name);
-    }
+    if (ws)
+        if (int st2 = check_workspace(c, ws, need_ws, dev)) return st2;
     cudaError_t e = use_tc
-        ? dn::launch_chunk_tc(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, ws, st)
-        : dn::launch_chunk_simt(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, st);
+        ? dn::launch_chunk_tc(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, ws, st, nullptr,
+                              nm)
+        : dn::launch_chunk_simt(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, st, nullptr,
+                                nullptr, nm);
     return cuda_status(e, use_tc ? "chunk forward (tcgen05) launch" : "chunk forward (SIMT) launch");
+}
+
+int dn_chunk_fwd_algo(const void* q, const void* k, const void* v, const void* beta,
+                      const float* S0, void* o, float* S_T, int B, int H, int T, int dk,
+                      int dv, int C, int dt, void* workspace, size_t workspace_bytes,
+                      void* stream, int algo) {
+    return dn_chunk_fwd_qk(q, k, v, beta, S0, o, S_T, B, H, T, dk, dv, C, dt, workspace,
+                           workspace_bytes, stream, algo, nullptr);
 }
 
 int dn_chunk_fwd(const void* q, const void* k, const void* v, const void* beta, const float* S0,
                  void* o, float* S_T, int B, int H, int T, int dk, int dv, int C, int dt,
                  void* workspace, size_t workspace_bytes, void* stream) {
-    return dn_chunk_fwd_algo(q, k, v, beta, S0, o, S_T, B, H, T, dk, dv, C, dt, workspace,
-                             workspace_bytes, stream, DN_ALGO_AUTO);
+    return dn_chunk_fwd_qk(q, k, v, beta, S0, o, S_T, B, H, T, dk, dv, C, dt, workspace,
+                           workspace_bytes, stream, DN_ALGO_AUTO, nullptr);
 }
 
 int dn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const void* beta,
@@ -213,40 +283,13 @@ int dn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const void
                     "B*H*ceil(T/64) = %lld chunk tiles; the no-alloc entry point holds %zu",
                     tiles, dn::noalloc_max_tiles());
     if (BH == 0) return ok();
-
-    const size_t es = elem_size(dt);
-    const size_t ntok = (size_t)BH * (size_t)T;
-    const size_t state_bytes = (size_t)BH * dk * dv * sizeof(float);
-    const Span sq{"q", q, ntok * dk * es}, sk{"k", k, ntok * dk * es}, sv{"v", v, ntok * dv * es},
-        sb{"beta", beta, ntok * es}, so{"o", o, ntok * dv * es}, s0{"S0", S0, state_bytes},
-        sT{"S_T", S_T, state_bytes};
+    const ChunkSpans c = chunk_spans(q, k, v, beta, nullptr, 0, 0, S0, o, S_T,
+                                     (size_t)BH * (size_t)T, BH, dk, dv, dt);
     int dev = 0;
     if (int st = current_device(&dev)) return st;
-    if (T > 0) {
-        for (const Span* s : {&sq, &sk, &sv, &so})
-            if (int st = check_device_ptr(*s, 16, dev)) return st;
-        if (int st = check_device_ptr(sb, es, dev)) return st;
-    }
-    if (S0)
-        if (int st = check_device_ptr(s0, 16, dev)) return st;
-    if (S_T)
-        if (int st = check_device_ptr(sT, 16, dev)) return st;
-    if (T > 0)
-        for (const Span* s : {&sq, &sk, &sv, &sb, &s0, &sT})
-            if (overlaps(so, *s)) return fail(DN_ERR_INVALID_ARG, "o overlaps %s", s->name);
-    for (const Span* s : {&sq, &sk, &sv, &sb})
-        if (T > 0 && overlaps(sT, *s)) return fail(DN_ERR_INVALID_ARG, "S_T overlaps %s", s->name);
-    if (S_T && S0 && S_T != S0 && overlaps(sT, s0))
-        return fail(DN_ERR_INVALID_ARG, "S_T partly overlaps S0");
-
+    if (int st = check_chunk_spans(c, T > 0, dev)) return st;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (T == 0) {
-        if (!S_T || S_T == S0) return ok();
-        if (S0)
-            return cuda_status(cudaMemcpyAsync(S_T, S0, state_bytes, cudaMemcpyDeviceToDevice, st),
-                               "cudaMemcpyAsync(S_T <- S0)");
-        return cuda_status(cudaMemsetAsync(S_T, 0, state_bytes, st), "cudaMemsetAsync(S_T)");
-    }
+    if (T == 0) return pass_state_through(S0, S_T, c.state_bytes, st);
     return cuda_status(
         dn::launch_chunk_tc_noalloc(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, st),
         "chunk forward (tcgen05, static scratch) launch");
@@ -283,21 +326,16 @@ size_t dn_chunk_fwd_varlen_workspace_bytes(const int* cu_seqlens, int N, int H, 
         if (len < 0) return 0;
         chunks += (len + 63) / 64;
     }
-    return (size_t)H * (size_t)chunks * 16384;
+    return (size_t)H * (size_t)chunks * (16384 + dn::chunk_tc_side_bytes_per_chunk());
 }
 
-int dn_chunk_fwd_varlen(const void* q, const void* k, const void* v, const void* beta,
-                        const float* S0, void* o, float* S_T, const int* cu_seqlens, int N, int H,
-                        int T, int dk, int dv, int C, int dt, void* workspace,
-                        size_t workspace_bytes, void* stream) {
-    if (N < 0 || H < 0 || T < 0)
-        return fail(DN_ERR_INVALID_ARG, "negative size (N=%d H=%d T=%d)", N, H, T);
-    if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
-    if (dk <= 0 || dv <= 0 || C <= 0)
-        return fail(DN_ERR_INVALID_ARG, "dk, dv and C must be positive");
-    if (!supported_dim(dk) || !supported_dim(dv))
-        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this library supports 64 and 128", dk, dv);
-    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this library supports 64", C);
+int dn_chunk_fwd_varlen_qk(const void* q, const void* k, const void* v, const void* beta,
+                           const float* S0, void* o, float* S_T, const int* cu_seqlens, int N,
+                           int H, int T, int dk, int dv, int C, int dt, void* workspace,
+                           size_t workspace_bytes, void* stream, const dn_qk_norm* norm) {
+    if (int st = check_chunk_sizes(N, H, T, dk, dv, C, dt, "N")) return st;
+    dn::QkNorm nm;
+    if (int st = norm_options(norm, &nm)) return st;
     static thread_local dn::VarlenTable tab;
     if (int st = varlen_table(cu_seqlens, N, T, &tab)) return st;
     const size_t need_ws = dn_chunk_fwd_varlen_workspace_bytes(cu_seqlens, N, H, dk, dv, C, dt);
@@ -305,126 +343,29 @@ int dn_chunk_fwd_varlen(const void* q, const void* k, const void* v, const void*
         return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed (or pass NULL)",
                     workspace_bytes, need_ws);
     if ((long long)N * H == 0) return ok();
-    const size_t es = elem_size(dt);
-    const size_t ntok = (size_t)H * (size_t)T;
-    const size_t state_bytes = (size_t)N * H * dk * dv * sizeof(float);
-    const Span sq{"q", q, ntok * dk * es}, sk{"k", k, ntok * dk * es}, sv{"v", v, ntok * dv * es},
-        sb{"beta", beta, ntok * es}, so{"o", o, ntok * dv * es}, s0{"S0", S0, state_bytes},
-        sT{"S_T", S_T, state_bytes};
+    const ChunkSpans c = chunk_spans(q, k, v, beta, nullptr, 0, 0, S0, o, S_T,
+                                     (size_t)H * (size_t)T, (long long)N * H, dk, dv, dt);
     int dev = 0;
     if (int st = current_device(&dev)) return st;
-    if (T > 0) {
-        for (const Span* s : {&sq, &sk, &sv, &so})
-            if (int st = check_device_ptr(*s, 16, dev)) return st;
-        if (int st = check_device_ptr(sb, es, dev)) return st;
-    }
-    if (S0)
-        if (int st = check_device_ptr(s0, 16, dev)) return st;
-    if (S_T)
-        if (int st = check_device_ptr(sT, 16, dev)) return st;
-    if (T > 0)
-        for (const Span* s : {&sq, &sk, &sv, &sb, &s0, &sT})
-            if (overlaps(so, *s)) return fail(DN_ERR_INVALID_ARG, "o overlaps %s", s->name);
-    for (const Span* s : {&sq, &sk, &sv, &sb})
-        if (T > 0 && overlaps(sT, *s)) return fail(DN_ERR_INVALID_ARG, "S_T overlaps %s", s->name);
-    if (S_T && S0 && S_T != S0 && overlaps(sT, s0))
-        return fail(DN_ERR_INVALID_ARG, "S_T partly overlaps S0");
+    if (int st = check_chunk_spans(c, T > 0, dev)) return st;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (T == 0) {  // every sequence is empty
-        if (!S_T || S_T == S0) return ok();
-        if (S0)
-            return cuda_status(cudaMemcpyAsync(S_T, S0, state_bytes, cudaMemcpyDeviceToDevice, st),
-                               "cudaMemcpyAsync(S_T <- S0)");
-        return cuda_status(cudaMemsetAsync(S_T, 0, state_bytes, st), "cudaMemsetAsync(S_T)");
-    }
+    if (T == 0) return pass_state_through(S0, S_T, c.state_bytes, st);  // every sequence is empty
     const bool use_tc = workspace && need_ws > 0;
-    if (use_tc) {
-        const Span sw{"workspace", workspace, need_ws};
-        if (int st2 = check_device_ptr(sw, 16, dev)) return st2;
-        for (const Span* s : {&sq, &sk, &sv, &sb, &so, &s0, &sT})
-            if (overlaps(sw, *s)) return fail(DN_ERR_INVALID_ARG, "workspace overlaps %s", s->name);
-    }
+    if (use_tc)
+        if (int st2 = check_workspace(c, workspace, need_ws, dev)) return st2;
     const cudaError_t e = use_tc
-        ? dn::launch_chunk_tc_varlen(q, k, v, beta, S0, o, S_T, tab, H, T, workspace, st)
-        : dn::launch_chunk_simt_varlen(q, k, v, beta, S0, o, S_T, tab, H, T, dk, dv, dt, st);
+        ? dn::launch_chunk_tc_varlen(q, k, v, beta, S0, o, S_T, tab, H, T, workspace, st, nm)
+        : dn::launch_chunk_simt_varlen(q, k, v, beta, S0, o, S_T, tab, H, T, dk, dv, dt, st, nm);
     return cuda_status(e, use_tc ? "varlen chunk forward (tcgen05) launch"
                                  : "varlen chunk forward (SIMT) launch");
 }
 
-// The decayed chunkwise forms: Gated DeltaNet (one log keep rate per token,
-// per_channel = 0) and KDA (one per token and key channel, per_channel = 1).
-// Gated: a workspace of dn_chunk_fwd_gated_workspace_bytes bytes selects the
-// two-pass tensor-core form where it applies.
-static int chunk_fwd_decayed(const void* q, const void* k, const void* v, const void* beta,
-                             const float* g, int per_channel, const float* S0, void* o,
-                             float* S_T, int B, int H, int T, int dk, int dv, int C, int dt,
-                             void* workspace, size_t workspace_bytes, void* stream) {
-    if (B < 0 || H < 0 || T < 0)
-        return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d T=%d)", B, H, T);
-    if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
-    if (dk <= 0 || dv <= 0 || C <= 0)
-        return fail(DN_ERR_INVALID_ARG, "dk, dv and C must be positive");
-    if (!supported_dim(dk) || !supported_dim(dv))
-        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this library supports 64 and 128", dk, dv);
-    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this library supports 64", C);
-    const long long BH = (long long)B * H;
-    if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
-    const size_t need_ws =
-        per_channel ? 0 : dn_chunk_fwd_gated_workspace_bytes(B, H, T, dk, dv, C, dt);
-    if (workspace && workspace_bytes < need_ws)
-        return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed (or pass NULL)",
-                    workspace_bytes, need_ws);
-    if (BH == 0) return ok();
-    const size_t es = elem_size(dt);
-    const size_t ntok = (size_t)BH * (size_t)T;
-    const size_t state_bytes = (size_t)BH * dk * dv * sizeof(float);
-    const Span sq{"q", q, ntok * dk * es}, sk{"k", k, ntok * dk * es}, sv{"v", v, ntok * dv * es},
-        sb{"beta", beta, ntok * es}, sg{"g", g, ntok * (per_channel ? dk : 1) * sizeof(float)},
-        so{"o", o, ntok * dv * es}, s0{"S0", S0, state_bytes}, sT{"S_T", S_T, state_bytes};
-    int dev = 0;
-    if (int st = current_device(&dev)) return st;
-    if (T > 0) {
-        for (const Span* s : {&sq, &sk, &sv, &so})
-            if (int st = check_device_ptr(*s, 16, dev)) return st;
-        if (int st = check_device_ptr(sb, es, dev)) return st;
-        // the KDA kernel reads its [T][dk] g tile in 16-byte groups
-        if (int st = check_device_ptr(sg, per_channel ? 16 : sizeof(float), dev)) return st;
-    }
-    if (S0)
-        if (int st = check_device_ptr(s0, 16, dev)) return st;
-    if (S_T)
-        if (int st = check_device_ptr(sT, 16, dev)) return st;
-    if (T > 0)
-        for (const Span* s : {&sq, &sk, &sv, &sb, &sg, &s0, &sT})
-            if (overlaps(so, *s)) return fail(DN_ERR_INVALID_ARG, "o overlaps %s", s->name);
-    for (const Span* s : {&sq, &sk, &sv, &sb, &sg})
-        if (T > 0 && overlaps(sT, *s)) return fail(DN_ERR_INVALID_ARG, "S_T overlaps %s", s->name);
-    if (S_T && S0 && S_T != S0 && overlaps(sT, s0))
-        return fail(DN_ERR_INVALID_ARG, "S_T partly overlaps S0");
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (T == 0) {
-        if (!S_T || S_T == S0) return ok();
-        if (S0)
-            return cuda_status(cudaMemcpyAsync(S_T, S0, state_bytes, cudaMemcpyDeviceToDevice, st),
-                               "cudaMemcpyAsync(S_T <- S0)");
-        return cuda_status(cudaMemsetAsync(S_T, 0, state_bytes, st), "cudaMemsetAsync(S_T)");
-    }
-    if (per_channel)
-        return cuda_status(
-            dn::launch_chunk_simt_kda(q, k, v, beta, g, S0, o, S_T, (int)BH, T, dk, dv, dt, st),
-            "KDA chunk forward launch");
-    if (workspace && need_ws > 0) {
-        const Span sw{"workspace", workspace, need_ws};
-        if (int st2 = check_device_ptr(sw, 16, dev)) return st2;
-        for (const Span* s : {&sq, &sk, &sv, &sb, &sg, &so, &s0, &sT})
-            if (overlaps(sw, *s)) return fail(DN_ERR_INVALID_ARG, "workspace overlaps %s", s->name);
-        return cuda_status(dn::launch_chunk_tc_gated(q, k, v, beta, g, S0, o, S_T, (int)BH, T, dk,
-                                                     dv, dt, workspace, st),
-                           "gated chunk forward (tcgen05) launch");
-    }
-    return cuda_status(dn::launch_chunk_simt(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, st,
-                                             nullptr, g),
-                       "gated chunk forward launch");
+int dn_chunk_fwd_varlen(const void* q, const void* k, const void* v, const void* beta,
+                        const float* S0, void* o, float* S_T, const int* cu_seqlens, int N, int H,
+                        int T, int dk, int dv, int C, int dt, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    return dn_chunk_fwd_varlen_qk(q, k, v, beta, S0, o, S_T, cu_seqlens, N, H, T, dk, dv, C, dt,
+                                  workspace, workspace_bytes, stream, nullptr);
 }
 
 size_t dn_chunk_fwd_gated_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt) {
@@ -434,36 +375,107 @@ size_t dn_chunk_fwd_gated_workspace_bytes(int B, int H, int T, int dk, int dv, i
     return dn::chunk_tc_gated_workspace_bytes((int)BH, T);
 }
 
+size_t dn_chunk_fwd_kda_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt) {
+    (void)B, (void)H, (void)T, (void)dk, (void)dv, (void)C, (void)dt;
+    return 0;
+}
+
+// The decayed chunkwise forms: Gated DeltaNet (one log keep rate per token,
+// per_channel = 0) and KDA (one per token and key channel, per_channel = 1).
+// A workspace of the form's size selects its two-pass tensor-core path where
+// that size is non-zero.
+static int chunk_fwd_decayed(const void* q, const void* k, const void* v, const void* beta,
+                             const float* g, int per_channel, const float* S0, void* o,
+                             float* S_T, int B, int H, int T, int dk, int dv, int C, int dt,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             const dn_qk_norm* norm) {
+    if (int st = check_chunk_sizes(B, H, T, dk, dv, C, dt, "B")) return st;
+    dn::QkNorm nm;
+    if (int st = norm_options(norm, &nm)) return st;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
+    const size_t need_ws = per_channel
+        ? dn_chunk_fwd_kda_workspace_bytes(B, H, T, dk, dv, C, dt)
+        : dn_chunk_fwd_gated_workspace_bytes(B, H, T, dk, dv, C, dt);
+    if (workspace && workspace_bytes < need_ws)
+        return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed (or pass NULL)",
+                    workspace_bytes, need_ws);
+    if (BH == 0) return ok();
+    // the KDA kernel reads its [T][dk] g tile in 16-byte groups
+    const ChunkSpans c = chunk_spans(q, k, v, beta, g, per_channel ? (size_t)dk : 1,
+                                     per_channel ? 16 : sizeof(float), S0, o, S_T,
+                                     (size_t)BH * (size_t)T, BH, dk, dv, dt);
+    int dev = 0;
+    if (int st = current_device(&dev)) return st;
+    if (int st = check_chunk_spans(c, T > 0, dev)) return st;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) return pass_state_through(S0, S_T, c.state_bytes, st);
+    const bool use_tc = workspace && need_ws > 0;
+    if (use_tc)
+        if (int st2 = check_workspace(c, workspace, need_ws, dev)) return st2;
+    if (per_channel)
+        return cuda_status(dn::launch_chunk_simt_kda(q, k, v, beta, g, S0, o, S_T, (int)BH, T,
+                                                     dk, dv, dt, st, nm),
+                           "KDA chunk forward launch");
+    if (use_tc)
+        return cuda_status(dn::launch_chunk_tc_gated(q, k, v, beta, g, S0, o, S_T, (int)BH, T, dk,
+                                                     dv, dt, workspace, st, nm),
+                           "gated chunk forward (tcgen05) launch");
+    return cuda_status(dn::launch_chunk_simt(q, k, v, beta, S0, o, S_T, (int)BH, T, dk, dv, dt, st,
+                                             nullptr, g, nm),
+                       "gated chunk forward launch");
+}
+
+int dn_chunk_fwd_gated_qk(const void* q, const void* k, const void* v, const void* beta,
+                          const float* g, const float* S0, void* o, float* S_T, int B, int H,
+                          int T, int dk, int dv, int C, int dt, void* workspace,
+                          size_t workspace_bytes, void* stream, const dn_qk_norm* norm) {
+    return chunk_fwd_decayed(q, k, v, beta, g, 0, S0, o, S_T, B, H, T, dk, dv, C, dt, workspace,
+                             workspace_bytes, stream, norm);
+}
+
 int dn_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* beta,
                        const float* g, const float* S0, void* o, float* S_T, int B, int H,
                        int T, int dk, int dv, int C, int dt, void* workspace,
                        size_t workspace_bytes, void* stream) {
     return chunk_fwd_decayed(q, k, v, beta, g, 0, S0, o, S_T, B, H, T, dk, dv, C, dt, workspace,
-                             workspace_bytes, stream);
+                             workspace_bytes, stream, nullptr);
+}
+
+int dn_chunk_fwd_kda_qk(const void* q, const void* k, const void* v, const void* beta,
+                        const float* g, const float* S0, void* o, float* S_T, int B, int H, int T,
+                        int dk, int dv, int C, int dt, void* workspace, size_t workspace_bytes,
+                        void* stream, const dn_qk_norm* norm) {
+    return chunk_fwd_decayed(q, k, v, beta, g, 1, S0, o, S_T, B, H, T, dk, dv, C, dt, workspace,
+                             workspace_bytes, stream, norm);
 }
 
 int dn_chunk_fwd_kda(const void* q, const void* k, const void* v, const void* beta,
                      const float* g, const float* S0, void* o, float* S_T, int B, int H, int T,
                      int dk, int dv, int C, int dt, void* stream) {
     return chunk_fwd_decayed(q, k, v, beta, g, 1, S0, o, S_T, B, H, T, dk, dv, C, dt, nullptr, 0,
-                             stream);
+                             stream, nullptr);
 }
 
-static int recurrent_step_decayed(const void* q, const void* k, const void* v,
-                                  const void* beta, const float* g, int per_channel, float* S,
-                                  void* o, int B, int H, int dk, int dv, int dt, void* stream) {
+// One decoding step of any form: g_mode 0 (none), 1 (per head), 2 (per key
+// channel).
+static int recurrent_step_any(const void* q, const void* k, const void* v, const void* beta,
+                              const float* g, int g_mode, float* S, void* o, int B, int H, int dk,
+                              int dv, int dt, void* stream, const dn_qk_norm* norm) {
     if (B < 0 || H < 0) return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d)", B, H);
     if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
     if (dk <= 0 || dv <= 0) return fail(DN_ERR_INVALID_ARG, "dk and dv must be positive");
     if (!supported_dim(dk) || !supported_dim(dv))
         return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this library supports 64 and 128", dk, dv);
+    dn::QkNorm nm;
+    if (int st = norm_options(norm, &nm)) return st;
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
     if (BH == 0) return ok();
     const size_t es = elem_size(dt);
     const Span sq{"q", q, (size_t)BH * dk * es}, sk{"k", k, (size_t)BH * dk * es},
         sv{"v", v, (size_t)BH * dv * es}, sb{"beta", beta, (size_t)BH * es},
-        sg{"g", g, (size_t)BH * (per_channel ? dk : 1) * sizeof(float)},
+        sg{"g", g, (size_t)BH * (g_mode == 2 ? dk : 1) * sizeof(float)},
         so{"o", o, (size_t)BH * dv * es},
         sS{"S", S, (size_t)BH * dk * dv * sizeof(float)};
     int dev = 0;
@@ -471,59 +483,57 @@ static int recurrent_step_decayed(const void* q, const void* k, const void* v,
     for (const Span* s : {&sq, &sk, &sv, &so, &sS})
         if (int st = check_device_ptr(*s, 16, dev)) return st;
     if (int st = check_device_ptr(sb, es, dev)) return st;
-    if (int st = check_device_ptr(sg, sizeof(float), dev)) return st;
+    if (g_mode)
+        if (int st = check_device_ptr(sg, sizeof(float), dev)) return st;
     for (const Span* s : {&sq, &sk, &sv, &sb, &sg, &sS})
         if (overlaps(so, *s)) return fail(DN_ERR_INVALID_ARG, "o overlaps %s", s->name);
     for (const Span* s : {&sq, &sk, &sv, &sb, &sg})
         if (overlaps(sS, *s)) return fail(DN_ERR_INVALID_ARG, "S overlaps %s", s->name);
+    static const char* const what[3] = {"recurrent step launch", "gated recurrent step launch",
+                                        "KDA recurrent step launch"};
     return cuda_status(dn::launch_recurrent_step(q, k, v, beta, S, o, (int)BH, dk, dv, dt,
-                                                 static_cast<cudaStream_t>(stream), g,
-                                                 per_channel),
-                       per_channel ? "KDA recurrent step launch" : "gated recurrent step launch");
+                                                 static_cast<cudaStream_t>(stream),
+                                                 g_mode ? g : nullptr, g_mode == 2 ? 1 : 0, nm),
+                       what[g_mode]);
+}
+
+int dn_recurrent_step_qk(const void* q, const void* k, const void* v, const void* beta, float* S,
+                         void* o, int B, int H, int dk, int dv, int dt, void* stream,
+                         const dn_qk_norm* norm) {
+    return recurrent_step_any(q, k, v, beta, nullptr, 0, S, o, B, H, dk, dv, dt, stream, norm);
+}
+
+int dn_recurrent_step(const void* q, const void* k, const void* v, const void* beta, float* S,
+                      void* o, int B, int H, int dk, int dv, int dt, void* stream) {
+    return recurrent_step_any(q, k, v, beta, nullptr, 0, S, o, B, H, dk, dv, dt, stream, nullptr);
+}
+
+int dn_recurrent_step_gated_qk(const void* q, const void* k, const void* v, const void* beta,
+                               const float* g, float* S, void* o, int B, int H, int dk, int dv,
+                               int dt, void* stream, const dn_qk_norm* norm) {
+    return recurrent_step_any(q, k, v, beta, g, 1, S, o, B, H, dk, dv, dt, stream, norm);
 }
 
 int dn_recurrent_step_gated(const void* q, const void* k, const void* v, const void* beta,
                             const float* g, float* S, void* o, int B, int H, int dk, int dv,
                             int dt, void* stream) {
-    return recurrent_step_decayed(q, k, v, beta, g, 0, S, o, B, H, dk, dv, dt, stream);
+    return recurrent_step_any(q, k, v, beta, g, 1, S, o, B, H, dk, dv, dt, stream, nullptr);
+}
+
+int dn_recurrent_step_kda_qk(const void* q, const void* k, const void* v, const void* beta,
+                             const float* g, float* S, void* o, int B, int H, int dk, int dv,
+                             int dt, void* stream, const dn_qk_norm* norm) {
+    return recurrent_step_any(q, k, v, beta, g, 2, S, o, B, H, dk, dv, dt, stream, norm);
 }
 
 int dn_recurrent_step_kda(const void* q, const void* k, const void* v, const void* beta,
                           const float* g, float* S, void* o, int B, int H, int dk, int dv,
                           int dt, void* stream) {
-    return recurrent_step_decayed(q, k, v, beta, g, 1, S, o, B, H, dk, dv, dt, stream);
+    return recurrent_step_any(q, k, v, beta, g, 2, S, o, B, H, dk, dv, dt, stream, nullptr);
 }
 
-int dn_recurrent_step(const void* q, const void* k, const void* v, const void* beta, float* S,
-                      void* o, int B, int H, int dk, int dv, int dt, void* stream) {
-    if (B < 0 || H < 0) return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d)", B, H);
-    if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
-    if (dk <= 0 || dv <= 0) return fail(DN_ERR_INVALID_ARG, "dk and dv must be positive");
-    if (!supported_dim(dk) || !supported_dim(dv))
-        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this library supports 64 and 128", dk, dv);
-    const long long BH = (long long)B * H;
-    if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
-    if (BH == 0) return ok();
-    const size_t es = elem_size(dt);
-    const Span sq{"q", q, (size_t)BH * dk * es}, sk{"k", k, (size_t)BH * dk * es},
-        sv{"v", v, (size_t)BH * dv * es}, sb{"beta", beta, (size_t)BH * es},
-        so{"o", o, (size_t)BH * dv * es}, sS{"S", S, (size_t)BH * dk * dv * sizeof(float)};
-    int dev = 0;
-    if (int st = current_device(&dev)) return st;
-    for (const Span* s : {&sq, &sk, &sv, &so, &sS})
-        if (int st = check_device_ptr(*s, 16, dev)) return st;
-    if (int st = check_device_ptr(sb, es, dev)) return st;
-    for (const Span* s : {&sq, &sk, &sv, &sb, &sS})
-        if (overlaps(so, *s)) return fail(DN_ERR_INVALID_ARG, "o overlaps %s", s->name);
-    for (const Span* s : {&sq, &sk, &sv, &sb})
-        if (overlaps(sS, *s)) return fail(DN_ERR_INVALID_ARG, "S overlaps %s", s->name);
-    return cuda_status(dn::launch_recurrent_step(q, k, v, beta, S, o, (int)BH, dk, dv, dt,
-                                                 static_cast<cudaStream_t>(stream)),
-                       "recurrent step launch");
-}
-
-int dn_qk_prepare(const void* q, const void* k, void* q_out, void* k_out, long long rows,
-                  int d, int normalize, float scale, float eps, int dt, void* stream) {
+// Row count, dtype, d and the options of the preparation and its gradient.
+static int check_prepare_args(long long rows, int d, float scale, float eps, int dt) {
     if (rows < 0) return fail(DN_ERR_INVALID_ARG, "negative row count %lld", rows);
     if (rows > (1LL << 40)) return fail(DN_ERR_INVALID_ARG, "row count %lld too large", rows);
     if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
@@ -533,6 +543,12 @@ int dn_qk_prepare(const void* q, const void* k, void* q_out, void* k_out, long l
     if (!isfinite(scale)) return fail(DN_ERR_INVALID_ARG, "scale must be finite");
     if (!isfinite(eps) || eps < 0.0f)
         return fail(DN_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    return DN_OK;
+}
+
+int dn_qk_prepare(const void* q, const void* k, void* q_out, void* k_out, long long rows,
+                  int d, int normalize, float scale, float eps, int dt, void* stream) {
+    if (int st = check_prepare_args(rows, d, scale, eps, dt)) return st;
     if (rows == 0) return ok();
     const size_t bytes = (size_t)rows * d * elem_size(dt);
     const Span sq{"q", q, bytes}, sqo{"q_out", q_out, bytes}, sk{"k", k, bytes},
@@ -553,6 +569,41 @@ int dn_qk_prepare(const void* q, const void* k, void* q_out, void* k_out, long l
     return cuda_status(dn::launch_qk_prepare(q, k, q_out, k_out, rows, d, normalize ? 1 : 0,
                                              scale, eps, dt, static_cast<cudaStream_t>(stream)),
                        "q/k preparation launch");
+}
+
+int dn_qk_prepare_bwd(const void* q, const void* k, const void* d_q_out, const void* d_k_out,
+                      void* d_q, void* d_k, long long rows, int d, int normalize, float scale,
+                      float eps, int dt, void* stream) {
+    if (int st = check_prepare_args(rows, d, scale, eps, dt)) return st;
+    if (rows == 0) return ok();
+    const size_t bytes = (size_t)rows * d * elem_size(dt);
+    const Span sq{"q", q, bytes}, sk{"k", k, bytes}, sgq{"d_q_out", d_q_out, bytes},
+        sgk{"d_k_out", d_k_out, bytes}, sdq{"d_q", d_q, bytes}, sdk{"d_k", d_k, bytes};
+    int dev = 0;
+    if (int st = current_device(&dev)) return st;
+    for (const Span* s : {&sgq, &sdq})
+        if (int st = check_device_ptr(*s, 16, dev)) return st;
+    if (normalize)
+        for (const Span* s : {&sq, &sk, &sgk, &sdk})
+            if (int st = check_device_ptr(*s, 16, dev)) return st;
+    // Each output may be its own incoming gradient (in place); otherwise
+    // outputs overlap no input and not each other.
+    const Span* ins[] = {&sq, &sk, &sgq, &sgk};
+    const Span* outs[] = {&sdq, &sdk};
+    for (const Span* o : outs) {
+        if (o == &sdk && !normalize) continue;
+        for (const Span* i : ins) {
+            if (!normalize && (i == &sq || i == &sk || i == &sgk)) continue;
+            const bool self = (o == &sdq && i == &sgq) || (o == &sdk && i == &sgk);
+            if (self && o->p == i->p) continue;
+            if (overlaps(*o, *i)) return fail(DN_ERR_INVALID_ARG, "%s overlaps %s", o->name, i->name);
+        }
+    }
+    if (normalize && overlaps(sdq, sdk)) return fail(DN_ERR_INVALID_ARG, "d_q overlaps d_k");
+    return cuda_status(dn::launch_qk_prepare_bwd(q, k, d_q_out, d_k_out, d_q, d_k, rows, d,
+                                                 normalize ? 1 : 0, scale, eps, dt,
+                                                 static_cast<cudaStream_t>(stream)),
+                       "q/k preparation gradient launch");
 }
 
 size_t dn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt) {

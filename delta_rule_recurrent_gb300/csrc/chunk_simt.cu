@@ -85,7 +85,7 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
                   const float* __restrict__ S0, T* __restrict__ o,
                   float* __restrict__ S_T, float* __restrict__ S_chunks,
                   const float* __restrict__ g, int Ttot, int H,
-                  const __grid_constant__ SeqTable<NMAX> seqs) {
+                  const __grid_constant__ SeqTable<NMAX> seqs, QkNorm nm) {
     using L = SimtSmem<DK, NV, kChan>;
     constexpr int LK = L::LK, LV = L::LV;
     constexpr int NSLICE = DV / NV;
@@ -139,6 +139,21 @@ chunk_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
         load_tile<kThreads, kC, DK, LK, DK>(Qs, q, tok0 + t0, n, 0);
         load_tile<kThreads, kC, NV, LV, DV>(Rs, v, tok0 + t0, n, j0);
         if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
+        if (norm_active(nm)) {  // q and k prepared in place: thread r owns row r of [K; Q]
+            __syncthreads();
+            static_assert(2 * kC <= kThreads, "a thread per row");
+            const bool is_q = tid >= kC;
+            if (tid < 2 * kC && (is_q || nm.l2norm)) {
+                float* const row = is_q ? Qs + (tid - kC) * LK : Ks + tid * LK;
+                float f = is_q ? nm.qscale : 1.f;
+                if (nm.l2norm) {
+                    float ss = 0.f;
+                    for (int d = 0; d < DK; ++d) ss = fmaf(row[d], row[d], ss);
+                    f *= rsqrtf(ss + nm.eps);
+                }
+                for (int d = 0; d < DK; ++d) row[d] *= f;
+            }
+        }
         // KDA: while the chunk's decay stays within exp(-80) on every key
         // channel (G is non-increasing, so G_C is each channel's lowest), the
         // ratio exp(G_i - G_j) is the product exp(G_i) exp(-G_j) of two normal
@@ -356,7 +371,8 @@ template <typename T, int DK, int DV, int NMAX = 1, bool kChan = false>
 cudaError_t launch_typed(const void* q, const void* k, const void* v,
                          const void* beta, const float* S0, void* o, float* S_T,
                          float* S_chunks, const float* g, int BH, int Tlen, cudaStream_t stream,
-                         int H = 1, const SeqTable<NMAX>* seqs = nullptr) {
+                         int H = 1, const SeqTable<NMAX>* seqs = nullptr,
+                         const QkNorm& nm = kNoNorm) {
     constexpr int NV = DV < 64 ? DV : 64;
     using L = SimtSmem<DK, NV, kChan>;
     auto kern = chunk_simt_kernel<T, DK, DV, NV, NMAX, kChan>;
@@ -368,7 +384,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
     kern<<<(unsigned)grid, kThreads, L::kBytes, stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k),
         static_cast<const T*>(v), static_cast<const T*>(beta), S0,
-        static_cast<T*>(o), S_T, S_chunks, g, Tlen, H, seqs ? *seqs : SeqTable<NMAX>{});
+        static_cast<T*>(o), S_T, S_chunks, g, Tlen, H, seqs ? *seqs : SeqTable<NMAX>{}, nm);
     return cudaGetLastError();
 }
 
@@ -376,10 +392,11 @@ template <typename T>
 cudaError_t launch_dims(const void* q, const void* k, const void* v,
                         const void* beta, const float* S0, void* o, float* S_T,
                         float* Sc, const float* g, int BH, int Tlen, int dk, int dv,
-                        cudaStream_t st) {
+                        cudaStream_t st, const QkNorm& nm) {
 #define DN_SIMT_CASE(DK_, DV_)                                                             \
     if (dk == DK_ && dv == DV_)                                                            \
-        return launch_typed<T, DK_, DV_>(q, k, v, beta, S0, o, S_T, Sc, g, BH, Tlen, st);
+        return launch_typed<T, DK_, DV_>(q, k, v, beta, S0, o, S_T, Sc, g, BH, Tlen, st, 1, \
+                                         static_cast<const SeqTable<1>*>(nullptr), nm);
     DN_SIMT_CASE(128, 128)
     DN_SIMT_CASE(128, 64)
     DN_SIMT_CASE(64, 128)
@@ -393,25 +410,28 @@ cudaError_t launch_dims(const void* q, const void* k, const void* v,
 cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v,
                               const void* beta, const float* S0, void* o,
                               float* S_T, int BH, int T, int dk, int dv, int dt,
-                              cudaStream_t stream, float* S_chunks, const float* g) {
+                              cudaStream_t stream, float* S_chunks, const float* g,
+                              const QkNorm& norm) {
     if (BH <= 0 || T <= 0) return cudaSuccess;
     if (dt == 0)
-        return launch_dims<float>(q, k, v, beta, S0, o, S_T, S_chunks, g, BH, T, dk, dv, stream);
+        return launch_dims<float>(q, k, v, beta, S0, o, S_T, S_chunks, g, BH, T, dk, dv, stream,
+                                  norm);
     return launch_dims<__nv_bfloat16>(q, k, v, beta, S0, o, S_T, S_chunks, g, BH, T, dk, dv,
-                                      stream);
+                                      stream, norm);
 }
 
 cudaError_t launch_chunk_simt_varlen(const void* q, const void* k, const void* v,
                                      const void* beta, const float* S0, void* o, float* S_T,
                                      const VarlenTable& seqs, int H, int T, int dk, int dv,
-                                     int dt, cudaStream_t st) {
+                                     int dt, cudaStream_t st, const QkNorm& norm) {
     const long long ctas = (long long)seqs.n * H;
     if (ctas <= 0) return cudaSuccess;
     if (ctas > 0x3fffffffLL) return cudaErrorInvalidValue;
 #define DN_SIMT_VARLEN(T_, DK_, DV_)                                                           \
     if (dk == DK_ && dv == DV_)                                                                \
         return launch_typed<T_, DK_, DV_, kMaxVarlenSeqs>(q, k, v, beta, S0, o, S_T, nullptr,  \
-                                                          nullptr, (int)ctas, T, st, H, &seqs);
+                                                          nullptr, (int)ctas, T, st, H, &seqs,  \
+                                                          norm);
     if (dt == 0) {
         DN_SIMT_VARLEN(float, 128, 128)
         DN_SIMT_VARLEN(float, 128, 64)
@@ -429,11 +449,13 @@ cudaError_t launch_chunk_simt_varlen(const void* q, const void* k, const void* v
 
 cudaError_t launch_chunk_simt_kda(const void* q, const void* k, const void* v, const void* beta,
                                   const float* g, const float* S0, void* o, float* S_T, int BH,
-                                  int T, int dk, int dv, int dt, cudaStream_t st) {
+                                  int T, int dk, int dv, int dt, cudaStream_t st,
+                                  const QkNorm& norm) {
     if (BH <= 0 || T <= 0) return cudaSuccess;
 #define DN_SIMT_KDA(T_, DK_, DV_)                                                              \
     if (dk == DK_ && dv == DV_)                                                                \
-        return launch_typed<T_, DK_, DV_, 1, true>(q, k, v, beta, S0, o, S_T, nullptr, g, BH, T, st);
+        return launch_typed<T_, DK_, DV_, 1, true>(q, k, v, beta, S0, o, S_T, nullptr, g, BH, T, \
+                                                   st, 1, nullptr, norm);
     if (dt == 0) {
         DN_SIMT_KDA(float, 128, 128)
         DN_SIMT_KDA(float, 128, 64)

@@ -199,6 +199,85 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// The preparation factor of row r (0..127) of a [K; Q] stage (rows 0-63 k,
+// 64-127 q; two 16 KB dk-half regions of 128-byte swizzled rows): with
+// l2norm 1 / sqrt(sum x^2 + eps) over the row's bf16 values (fp32 sum), and
+// for a q row times qscale.  Reads the stage only.
+__device__ __forceinline__ float kq_row_factor(uint32_t stage, int r, const QkNorm& nm) {
+    float f = r >= 64 ? nm.qscale : 1.f;
+    if (nm.l2norm) {
+        float ss = 0.f;
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+            const uint4 w = ld_shared_v4(stage + (uint32_t)(i >> 3) * kRegKQ + sw128(r, i & 7));
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 p = unpack_bf16(u[j]);
+                ss = fmaf(p.x, p.x, ss);
+                ss = fmaf(p.y, p.y, ss);
+            }
+        }
+        f *= rsqrtf(ss + nm.eps);
+    }
+    return f;
+}
+
+// One dk half (t >> 6) of k row (t & 63) of a [K; Q] stage scaled in place
+// by f and rounded to bf16 (a warpgroup of 128 threads covers the 64 k rows).
+__device__ __forceinline__ void scale_k_half_row(uint32_t stage, int t, float f) {
+    const int r = t & 63;
+    const uint32_t region = stage + (uint32_t)(t >> 6) * kRegKQ;
+#pragma unroll 4
+    for (int c = 0; c < 8; ++c) {
+        const uint32_t a = region + sw128(r, c);
+        const uint4 w = ld_shared_v4(a);
+        const float2 x0 = unpack_bf16(w.x), x1 = unpack_bf16(w.y), x2 = unpack_bf16(w.z),
+                     x3 = unpack_bf16(w.w);
+        st_shared_v4(a, pack_bf16(x0.x * f, x0.y * f), pack_bf16(x1.x * f, x1.y * f),
+                     pack_bf16(x2.x * f, x2.y * f), pack_bf16(x3.x * f, x3.y * f));
+    }
+}
+
+// Row r (0..127) of a [K; Q] stage -- rows 0-63 k, 64-127 q, each row split
+// over two 16 KB dk-half regions of 128-byte swizzled rows, as TMA lands it --
+// prepared in place by the calling thread: with l2norm the row becomes
+// x / sqrt(sum x^2 + eps) (the sum in fp32 over the row's bf16 values), a q
+// row is then multiplied by qscale, and the result is rounded once to bf16.
+// Without l2norm a k row is left as it is.  The caller fences the writes
+// into the async proxy before an MMA reads the stage.
+__device__ __forceinline__ void prepare_kq_row(uint32_t stage, int r, const QkNorm& nm) {
+    const bool is_q = r >= 64;
+    if (!is_q && !nm.l2norm) return;
+    // Two passes over the row (sum of squares, then scale), each reading one
+    // 16-byte chunk at a time, so the caller's registers are left alone.
+    float f = is_q ? nm.qscale : 1.f;
+    if (nm.l2norm) {
+        float ss = 0.f;
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+            const uint4 w = ld_shared_v4(stage + (uint32_t)(i >> 3) * kRegKQ + sw128(r, i & 7));
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 p = unpack_bf16(u[j]);
+                ss = fmaf(p.x, p.x, ss);
+                ss = fmaf(p.y, p.y, ss);
+            }
+        }
+        f *= rsqrtf(ss + nm.eps);
+    }
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t a = stage + (uint32_t)(i >> 3) * kRegKQ + sw128(r, i & 7);
+        const uint4 w = ld_shared_v4(a);
+        const float2 x0 = unpack_bf16(w.x), x1 = unpack_bf16(w.y), x2 = unpack_bf16(w.z),
+                     x3 = unpack_bf16(w.w);
+        st_shared_v4(a, pack_bf16(x0.x * f, x0.y * f), pack_bf16(x1.x * f, x1.y * f),
+                     pack_bf16(x2.x * f, x2.y * f), pack_bf16(x3.x * f, x3.y * f));
+    }
+}
+
 struct Ctl {
     uint32_t bars;             // shared address of mbarrier 0
     volatile int* abort_flag;  // set by whichever role times out first
@@ -735,7 +814,7 @@ __device__ __forceinline__ void issue_dw(uint32_t tmem, uint32_t colQW, uint32_t
 // chunk c = g + 2 it.
 __device__ void chunk_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                                 int g, const __nv_bfloat16* __restrict__ beta, int bh, int T,
-                                int nchunks) {
+                                int nchunks, const QkNorm& nm) {
     constexpr int kF = kKQBars;
     const int barid = 2 + g;
     const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
@@ -758,10 +837,18 @@ __device__ void chunk_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, i
             const int nx = (c + 2) * kC + t;
             bnext = nx < T ? ld_nc_u16(beta_bh + nx) : (uint16_t)0;
         }
-        // G = [K; Q] K^T
+        // G = [K; Q] K^T (on the prepared rows, when q and k are prepared here)
         bool ok = true;
+        const bool prep = norm_active(nm);
+        if (prep) {
+            if (t == 0) ok = ctl.wait(B_KQ_FULL + c % kF, (uint32_t)(c / kF));
+            if (wg_sync_or(barid, !ok)) return;
+            prepare_kq_row(kq, t, nm);
+            fence_proxy_async_smem();
+            wg_sync(barid);
+        }
         if (t == 0) {
-            ok = ctl.wait(B_KQ_FULL + c % kF, (uint32_t)(c / kF));
+            ok = prep || ctl.wait(B_KQ_FULL + c % kF, (uint32_t)(c / kF));
             if (ok) {
                 tc_fence_after_sync();
 #pragma unroll
@@ -856,8 +943,9 @@ __device__ void chunk_role_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, i
 }
 
 __device__ void chunk_role(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int g,
-                           const __nv_bfloat16* __restrict__ beta, int bh, int T, int nchunks) {
-    chunk_role_body(ctl, sm, tmem, t, g, beta, bh, T, nchunks);
+                           const __nv_bfloat16* __restrict__ beta, int bh, int T, int nchunks,
+                           const QkNorm& nm) {
+    chunk_role_body(ctl, sm, tmem, t, g, beta, bh, T, nchunks, nm);
     if (t == 0) drain_mmas(ctl, B_DRAIN + 1 + g);
 }
 
@@ -867,7 +955,7 @@ __global__ void __launch_bounds__(512, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                 const __nv_bfloat16* __restrict__ beta, const float* __restrict__ S0,
-                float* __restrict__ S_T, int T) {
+                float* __restrict__ S_T, int T, QkNorm nm) {
     using L = Layout;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -905,7 +993,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         state_role(ctl, sm, tmem, tid - 128, S0, S_T, &tm_o, bh, nchunks);
     } else if (warp >= 8) {
         const int g = (warp - 8) >> 2;
-        chunk_role(ctl, sm, tmem, tid - 256 - 128 * g, g, beta, bh, T, nchunks);
+        chunk_role(ctl, sm, tmem, tid - 256 - 128 * g, g, beta, bh, T, nchunks, nm);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -990,7 +1078,11 @@ constexpr uint32_t P_OFF_Y = P_OFF_X + kXBytes;    // solve scratch
 constexpr uint32_t P_OFF_BETA = P_OFF_Y + kYBytes; // 64 fp32
 constexpr uint32_t P_OFF_G = P_OFF_BETA + 256;     // 64 fp32 cumulative log decay + 2 partials
 constexpr uint32_t P_OFF_E = P_OFF_G + 272;        // exp G_t, then exp(-G_t) (64 fp32 each)
-constexpr uint32_t P_OFF_BAR = P_OFF_E + 512;      // mbarriers: tiles landed, MMA done, drain
+constexpr uint32_t P_OFF_DK = P_OFF_E + 512;       // prepared inputs: d_k of the 64 k rows
+static_assert(P_OFF_DK % 16 == 0, "d_k read as float4");
+// (named barrier 2 joins the 64 threads of the A rows: the gated prefix sums
+// and the d_k exchange use it at different points of an item)
+constexpr uint32_t P_OFF_BAR = P_OFF_DK + 256;     // mbarriers: tiles landed, MMA done, drain
 constexpr uint32_t P_OFF_MISC = P_OFF_BAR + 24;    // abort flag, TMEM address
 constexpr uint32_t kPrepSmemBytes = P_OFF_MISC + 16 + 1024;
 static_assert(kPrepCtasPerSm * (kPrepSmemBytes + 1024) <= 233472, "prepare kernel occupancy");
@@ -1038,7 +1130,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                   const __grid_constant__ CUtensorMap tm_ws, const __nv_bfloat16* __restrict__ beta,
                   int T, int nchunks, int items, const __grid_constant__ SeqTable<NMAX> seqs,
                   const float* __restrict__ gate, float* __restrict__ side,
-                  const __grid_constant__ CUtensorMap tm_ws2) {
+                  const __grid_constant__ CUtensorMap tm_ws2, QkNorm nm) {
     static_assert(!kGate || NMAX == 1, "gating on the batched layout");
     constexpr int kBar = 1, B_TILES = 0, B_MMA = 1, B_END = 2;
     extern __shared__ uint8_t smem_raw[];
@@ -1050,6 +1142,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     float* const betas = reinterpret_cast<float*>(gbase + P_OFF_BETA);
     float* const Gs = reinterpret_cast<float*>(gbase + P_OFF_G);  // [64] then 2 warp partials
     float* const Es = reinterpret_cast<float*>(gbase + P_OFF_E);  // exp G_t [64], exp(-G_t) [64]
+    float* const Ds = reinterpret_cast<float*>(gbase + P_OFF_DK);  // d_k [64]
     int* const misc = reinterpret_cast<int*>(gbase + P_OFF_MISC);
     const Ctl ctl{base + P_OFF_BAR, reinterpret_cast<volatile int*>(misc)};
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
@@ -1128,10 +1221,21 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 Es[64 + t] = __expf(-G);
             }
         }
-        // G = [K; Q] K^T
+        // G = [K; Q] K^T.  Prepared inputs: the raw products are scaled as they
+        // leave TMEM, A_ij by d_k[i] d_k[j] and P_ij by d_q[i] d_k[j].  A q
+        // row's thread reads its factor d_q from the tile while the MMA runs;
+        // d_k comes from the diagonal of K K^T (the squared norms, accumulated
+        // in fp32) when A is read out.
         bool ok = true;
+        const bool prep = norm_active(nm);
+        float own_d = 1.f;  // d_k of A row t (t < 64) or d_q of P row t - 64
+        if (prep) {
+            if (t == 0) ok = ctl.wait(B_TILES, (uint32_t)n);
+            if (wg_sync_or(kBar, !ok)) break;
+            if (t >= 64) own_d = kq_row_factor(kq, t, nm);
+        }
         if (t == 0) {
-            ok = ctl.wait(B_TILES, (uint32_t)n);
+            ok = prep || ctl.wait(B_TILES, (uint32_t)n);
             if (ok) {
                 tc_fence_after_sync();
 #pragma unroll
@@ -1144,9 +1248,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 ok = ctl.wait(B_MMA, (uint32_t)(2 * n));
             }
             if (ok) {
-                // [K; Q] is spent: fetch the next item's tiles now.  The previous
-                // [PT; Tm] store must have read the solve array before A goes in.
-                if (wn < items) {
+                // [K; Q] is spent: fetch the next item's tiles now (with prepared
+                // inputs only once the q rows' read pass is over, below).  The
+                // previous [PT; Tm] store must have read the solve array before A
+                // goes in.
+                if (wn < items && !prep) {
                     load_tiles(wn);
                     ++loads;
                 }
@@ -1156,6 +1262,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (t < kC && wn < items) bnext = load_beta(wn);
         if (kGate && t < kC && wn < items) gnext = load_gate(wn);
         if (wg_sync_or(kBar, !ok)) break;
+        if (prep && t == 0 && wn < items) {
+            load_tiles(wn);
+            ++loads;
+        }
         tc_fence_after_sync();
         // A (TMEM rows 0-63) into the solve array; P (rows 64-127) stays in TMEM.
         if (t < 64) {
@@ -1166,8 +1276,30 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             float x[64];
             tmem_ld64f(tmem + lane_base, x);
-            const float bi = betas[row];
+            float bi = betas[row];
+            if (prep) {  // d_k[i] = 1 / sqrt(k_i . k_i + eps), shared by the 64 A rows
+                if (nm.l2norm) {
+                    float kk = 0.f;  // the diagonal entry, selected without indexing registers
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) kk = j == row ? x[j] : kk;
+                    own_d = rsqrtf(kk + nm.eps);
+                }
+                Ds[row] = own_d;
+                wg_sync(2, 64);
+            }
             if (kGate && sep) decay_row(x, Es, row);  // exp(G_i - G_j), j < i
+            if (prep) {  // d_k[i] d_k[j]
+                bi *= own_d;
+                const float4* const d4 = reinterpret_cast<const float4*>(Ds);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float4 d = d4[j];
+                    x[4 * j] *= d.x;
+                    x[4 * j + 1] *= d.y;
+                    x[4 * j + 2] *= d.z;
+                    x[4 * j + 3] *= d.w;
+                }
+            }
 #pragma unroll
             for (int j = 0; j < 64; j += 4)
                 sts4(X + row * kP + j,
@@ -1198,6 +1330,17 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
                 tmem_ld64f(tmem + lane_base, x);
                 if (kGate && sep) decay_row(x, Es, row);  // exp(G_i - G_j), j <= i
+                if (prep) {  // d_q[i] d_k[j]
+                    const float4* const d4 = reinterpret_cast<const float4*>(Ds);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float4 d = d4[j];
+                        x[4 * j] *= own_d * d.x;
+                        x[4 * j + 1] *= own_d * d.y;
+                        x[4 * j + 2] *= own_d * d.z;
+                        x[4 * j + 3] *= own_d * d.w;
+                    }
+                }
 #pragma unroll
                 for (int j = 0; j < 64; ++j)
                     if (j > row) x[j] = 0.f;
@@ -1254,11 +1397,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 float x[64];
                 tmem_ld64f(tmem + lane_base, x);  // PT, still in its accumulator
 #pragma unroll
-                for (int e = 0; e < 64; ++e) x[e] *= Es[e];
+                for (int e = 0; e < 64; ++e) x[e] *= prep ? Es[e] * Ds[e] : Es[e];
                 store_row64_bf16(tp, t, x);
                 tmem_ld64f(tmem + lane_base + 64u, x);  // Tm
 #pragma unroll
-                for (int e = 0; e < 64; ++e) x[e] *= Es[e];
+                for (int e = 0; e < 64; ++e) x[e] *= prep ? Es[e] * Ds[e] : Es[e];
                 store_row64_bf16(tp, 64 + t, x);
             }
             fence_proxy_async_smem();
@@ -1270,13 +1413,18 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 bulk_commit_group();
             }
         }
-        if constexpr (kGate) {  // the chunk's decay vectors for the scan
-            if (t < kC) {
-                float* const sd = side + (size_t)w * kSideFloats;  // w = bh * nchunks + c
-                sd[t] = Es[t];                           // exp G_t
-                sd[64 + t] = __expf(Gs[63] - Gs[t]);     // exp(G_C - G_t)
-                if (t == 0) sd[128] = __expf(Gs[63]);    // exp G_C
+        if constexpr (kGate) {  // the chunk's decay vectors for the scan (prepared
+            // inputs fold d_q into the q factor and d_k into the U' factor)
+            float* const sd = side + (size_t)w * kSideFloats;  // w = bh * nchunks + c
+            if (t >= 64) {
+                sd[t - 64] = Es[t - 64] * own_d;                  // exp G_t (d_q[t])
+            } else {
+                sd[64 + t] = __expf(Gs[63] - Gs[t]) * own_d;      // exp(G_C - G_t) (d_k[t])
+                if (t == 0) sd[128] = __expf(Gs[63]);             // exp G_C
             }
+        } else if (prep) {  // the row factors for the scan: d_q [64], then d_k [64]
+            float* const sd = side + (size_t)w * kSideFloats;
+            sd[t >= 64 ? t - 64 : 64 + t] = own_d;
         }
     }
     if (t == 0) {
@@ -1342,6 +1490,8 @@ constexpr uint32_t OFF_SIDE = OFF_MISC + 16;
 constexpr uint32_t OFF_DEC = OFF_SIDE + 2 * kSideCopyBytes;
 constexpr uint32_t kSmemBytes = OFF_DEC + 256 + 1024;
 static_assert(kSmemBytes <= 232448, "scan kernel shared memory");
+static_assert(OFF_SIDE % 16 == 0 && kSideCopyBytes % 16 == 0 && OFF_DEC % 16 == 0,
+              "bulk copies into the side slots need 16-byte alignment");
 // TMEM columns: S^T fp32 | D1^T fp32 (o rows 0-63, U' rows 64-127) | S^T bf16 |
 // U'^T bf16 | the chunk group's 128 DW accumulator columns.
 constexpr uint32_t C_ST = 0, C_D1 = 128, C_SB = 256, C_UB = 320, C_GRP = 352;
@@ -1362,6 +1512,8 @@ struct Smem {
 // Gated (tm_ws2, side): the decay-scaled tile goes to the [Q'; -W] buffer
 // of the same set (free until the chunk group's epilogue overwrites it) and
 // the decay vectors to the set's side slot, all on the [PT; Tm] barrier.
+// Prepared inputs on the plain form (side only): the chunk's row factors
+// go to the side slot the same way.
 __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q,
                          const CUtensorMap* tm_k, const CUtensorMap* tm_v, const CUtensorMap* tm_ws,
                          const SeqSpan& sp, int nchunks, const CUtensorMap* tm_ws2,
@@ -1408,12 +1560,11 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
             const int g = ntp & 1, it = ntp >> 1;
             if (it == 0 || mbar_test_wait(ctl.bar(B_FREE + g), (uint32_t)(it - 1) & 1u)) {
                 const uint32_t bar = ctl.bar(B_TP_FULL + g);
-                mbar_arrive_expect_tx(bar, kTile + (side ? kTile + kSideCopyBytes : 0u));
+                mbar_arrive_expect_tx(bar, kTile + (tm_ws2 ? kTile : 0u) +
+                                               (side ? kSideCopyBytes : 0u));
                 tma_load_3d(sm.tp(g), tm_ws, bar, 0, (w0 + ntp) * 128, z);
-                if (side) {
-                    tma_load_3d(sm.qw(g), tm_ws2, bar, 0, (w0 + ntp) * 128, z);
-                    bulk_load(sm.side(g), side + (size_t)ntp * kSideFloats, kSideCopyBytes, bar);
-                }
+                if (tm_ws2) tma_load_3d(sm.qw(g), tm_ws2, bar, 0, (w0 + ntp) * 128, z);
+                if (side) bulk_load(sm.side(g), side + (size_t)ntp * kSideFloats, kSideCopyBytes, bar);
                 if (ntp + 2 < nchunks) tma_prefetch_l2_3d(tm_ws, 0, (w0 + ntp + 2) * 128, z);
                 ++ntp;
                 progressed = true;
@@ -1604,7 +1755,11 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
 }
 
 // Chunk group: [-Q'; W] = A [K; Q] in one chain of MMAs over the chunk's
-// 128 rows of k and q, with A = [[PT, -I]; [Tm, 0]], or for Gated DeltaNet
+// 128 rows of k and q, with A = [[PT, -I]; [Tm, 0]] (prepared inputs: the
+// row factors d_q, d_k arrive with the tile; the group scales the stage's k
+// rows to diag(d_k) K, which the state's update then reads too, and A's q
+// block is -diag(d_q); the gated form gets both factors folded into its side
+// vectors and scaled tile instead), or for Gated DeltaNet
 // A = [[PT diag(exp G), -diag(exp G)]; [Tm diag(exp G), 0]] (Q' = diag(exp G) Q
 // - PT diag(exp G) K and W = Tm diag(exp G) K).  The left block is the [PT; Tm]
 // tile (gated: the decay-scaled tile, loaded into this set's [Q'; -W]
@@ -1620,7 +1775,7 @@ __device__ __forceinline__ void put_diag(uint32_t taddr, int t, float v) {
 
 template <bool kGate>
 __device__ void group_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int nchunks,
-                           const float* sside) {
+                           const float* sside, bool prep) {
     constexpr int kBar = 2;
     const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
     put_diag(lane + C_GA, t, -1.f);  // gated: rows t < 64 are rewritten per chunk
@@ -1636,10 +1791,15 @@ __device__ void group_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         if (t == 0)
             ok = ctl.wait(B_KQ_FULL + c % kKQ, (uint32_t)(c / kKQ)) &&
                  ctl.wait(B_TP_FULL + g, (uint32_t)(c >> 1));
-        if constexpr (kGate) {  // -exp G_t into row t of the TMEM block (the last MMAs are done)
+        if (kGate || prep) {
             if (wg_sync_or(kBar, !ok)) return;
-            if (t < 64) {
-                put_diag(lane + C_GA, t, -sside[g * (kSideCopyBytes / 4) + t]);
+            const float* const slot = sside + g * (kSideCopyBytes / 4);
+            if (!kGate) {  // prepared inputs: K <- diag(d_k) K in the stage, before any MMA
+                scale_k_half_row(kq, t, slot[64 + (t & 63)]);  // reads it (the state's update too)
+                fence_proxy_async_smem();
+            }
+            if (t < 64) {  // row t of the TMEM block: -exp G_t (gated) or -d_q[t]
+                put_diag(lane + C_GA, t, -slot[t]);  // (the last MMAs that read it are done)
                 tmem_wait_st();
             }
             tc_fence_before_sync();
@@ -1723,8 +1883,11 @@ __device__ void writer_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t
 }
 }  // namespace scan
 
-// kGate: side holds every chunk's decay vectors (kSideFloats per chunk, in
-// workspace-tile order), written by the gated prepare kernel.
+// side (kSideFloats per chunk, in workspace-tile order, written by the
+// prepare kernel): kGate, every chunk's decay vectors (with the q and k row
+// factors folded in when q and k are prepared); otherwise, when q and k are
+// prepared in the kernels, every chunk's row factors d_q [64], d_k [64]
+// (NULL if they are not).
 template <bool kRec, int NMAX, bool kGate = false>
 __global__ void __launch_bounds__(512, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -1747,7 +1910,10 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const SeqSpan sp = scan_span(seqs, bh, H, T);
     const int nchunks = (sp.len + kC - 1) / kC;
     static_assert(!kGate || NMAX == 1, "gating on the batched layout");
-    const float* const cside = kGate ? side + (size_t)bh * nchunks * kSideFloats : nullptr;
+    // this sequence's first chunk among the per-chunk side vectors
+    size_t side0 = (size_t)bh * nchunks;
+    if constexpr (NMAX > 1) side0 = (size_t)sp.z * seqs.chunk[seqs.n] + sp.wsbase;
+    const float* const cside = side ? side + side0 * kSideFloats : nullptr;
 
     if (tid == 0) {
         misc[0] = 0;
@@ -1779,7 +1945,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 0);
     } else if (warp >= 8 && warp < 12) {
         const int t = tid - 256;
-        scan::group_body<kGate>(ctl, sm, tmem, t, nchunks, sside);
+        scan::group_body<kGate>(ctl, sm, tmem, t, nchunks, sside, !kGate && side != nullptr);
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 1);
     } else if (warp >= 12) {
         const int t = tid - 384;
@@ -2192,9 +2358,13 @@ size_t chunk_tc_workspace_bytes(int BH, int T) {
     return (size_t)BH * (size_t)((T + kC - 1) / kC) * kTile;
 }
 
+size_t chunk_tc_side_bytes_per_chunk() { return kSideFloats * sizeof(float); }
+
+
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const void* beta,
                             const float* S0, void* o, float* S_T, int BH, int T, int dk, int dv,
-                            int dt, void* workspace, cudaStream_t stream, float* S_chunks) {
+                            int dt, void* workspace, cudaStream_t stream, float* S_chunks,
+                            const QkNorm& norm) {
     if (!chunk_tc_supports(dk, dv, dt)) return cudaErrorNotSupported;
     if (BH <= 0 || T <= 0) return cudaSuccess;
     // Outputs may be skipped (o == nullptr) only on the two-pass path.
@@ -2212,6 +2382,10 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
     if (workspace) {
         const long long items = (long long)BH * nchunks;
         if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+        // prepared inputs: the row factors follow the tiles in the workspace
+        float* const side = norm_active(norm)
+            ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + (size_t)items * kTile)
+            : nullptr;
         auto prep_kernel = chunk_prep_kernel<1, false>;
         auto scan_kernel = S_chunks ? chunk_scan_kernel<true, 1> : chunk_scan_kernel<false, 1>;
         if ((err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -2222,23 +2396,24 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
         const SeqTable<1> batched{};
         const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
         prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
-            mq, mk, mws, b, T, nchunks, (int)items, batched, nullptr, nullptr, mws);
+            mq, mk, mws, b, T, nchunks, (int)items, batched, nullptr, side, mws, norm);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
         scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mws, S0,
                                                            static_cast<__nv_bfloat16*>(o), S_T,
-                                                           S_chunks, T, 1, batched, nullptr);
+                                                           S_chunks, T, 1, batched, side);
         return cudaGetLastError();
     }
     if ((err = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Layout::kSmemBytes)) != cudaSuccess)
         return err;
-    chunk_tc_kernel<<<BH, 512, Layout::kSmemBytes, stream>>>(mq, mk, mv, mo, b, S0, S_T, T);
+    chunk_tc_kernel<<<BH, 512, Layout::kSmemBytes, stream>>>(mq, mk, mv, mo, b, S0, S_T, T, norm);
     return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v, const void* beta,
                                    const float* S0, void* o, float* S_T, const VarlenTable& seqs,
-                                   int H, int T, void* workspace, cudaStream_t stream) {
+                                   int H, int T, void* workspace, cudaStream_t stream,
+                                   const QkNorm& norm) {
     const int total = seqs.chunk[seqs.n];
     const long long ctas = (long long)seqs.n * H, items = (long long)H * total;
     if (ctas <= 0) return cudaSuccess;
@@ -2246,6 +2421,9 @@ cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v, 
     CUtensorMap mq, mk, mv, mws;
     memset(&mws, 0, sizeof(mws));
     const int Tmap = T > 0 ? T : 1, nmap = total > 0 ? total : 1;
+    float* const side = norm_active(norm)
+        ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + (size_t)items * kTile)
+        : nullptr;
     if (!make_map(&mq, q, H, Tmap) || !make_map(&mk, k, H, Tmap) || !make_map(&mv, v, H, Tmap) ||
         !make_ws_map(&mws, workspace, H, nmap))
         return cudaErrorInvalidValue;
@@ -2261,11 +2439,11 @@ cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v, 
         const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
         prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
             mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, 0, (int)items, seqs, nullptr,
-            nullptr, mws);
+            side, mws, norm);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     scan_kernel<<<(unsigned)ctas, 512, scan::kSmemBytes, stream>>>(
-        mq, mk, mv, mws, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, nullptr, T, H, seqs, nullptr);
+        mq, mk, mv, mws, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, nullptr, T, H, seqs, side);
     return cudaGetLastError();
 }
 
@@ -2278,7 +2456,7 @@ size_t chunk_tc_gated_workspace_bytes(int BH, int T) {
 cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, const void* beta,
                                   const float* g, const float* S0, void* o, float* S_T, int BH,
                                   int T, int dk, int dv, int dt, void* workspace,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, const QkNorm& norm) {
     if (!chunk_tc_supports(dk, dv, dt)) return cudaErrorNotSupported;
     if (BH <= 0 || T <= 0) return cudaSuccess;
     if (!workspace || !o || !g) return cudaErrorInvalidValue;
@@ -2305,7 +2483,7 @@ cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, c
     const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
     prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
         mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, nchunks, (int)items, batched, g,
-        side, mws2);
+        side, mws2, norm);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mws2, S0,
                                                        static_cast<__nv_bfloat16*>(o), S_T, nullptr,

@@ -13,6 +13,9 @@
 // one rate per key channel (KDA, "Kimi Delta Attention : atténuation par
 // canal") row i of the stored state decays by alpha[i] instead.
 //
+// With a dn_qk_norm, q and k are L2-normalised (and q scaled) in fp32 after
+// they are loaded, before any product uses them.
+//
 // Work split: one CTA per head.  A thread owns one float4 column group of
 // the value channel and DK / RG rows of the key channel, so a warp's loads
 // and stores cover 512 contiguous bytes, and the whole head's state sits in
@@ -32,7 +35,7 @@ __global__ void __launch_bounds__(NT)
 recurrent_step_kernel(const T* __restrict__ q, const T* __restrict__ k,
                       const T* __restrict__ v, const T* __restrict__ beta,
                       const float* __restrict__ g, float* __restrict__ S,
-                      T* __restrict__ o) {
+                      T* __restrict__ o, QkNorm nm) {
     constexpr int CG = DV / 4;    // float4 column groups per state row
     constexpr int RG = NT / CG;   // row groups (threads sharing a column group)
     constexpr int RPT = DK / RG;  // state rows per thread
@@ -67,6 +70,21 @@ recurrent_step_kernel(const T* __restrict__ q, const T* __restrict__ k,
     for (int j = tid; j < DV; j += NT) vs[j] = to_f32(v[(size_t)head * DV + j]);
     if (tid == 0) beta_s = to_f32(beta[head]);
     __syncthreads();
+    if (norm_active(nm)) {  // k prepared by warp 0, q by warp 1, in fp32
+        if (tid < 64) {
+            const bool is_q = tid >= 32;
+            float* const x = is_q ? qs : ks;
+            float f = is_q ? nm.qscale : 1.f;
+            if (nm.l2norm) {
+                float ss = 0.f;
+                for (int i = tid & 31; i < DK; i += 32) ss = fmaf(x[i], x[i], ss);
+                f *= rsqrtf(warp_sum(ss) + nm.eps);
+            }
+            if (is_q || nm.l2norm)
+                for (int i = tid & 31; i < DK; i += 32) x[i] *= f;
+        }
+        __syncthreads();
+    }
 
     if (tid < 32) {
         float a = 0.f;
@@ -136,7 +154,7 @@ recurrent_step_kernel(const T* __restrict__ q, const T* __restrict__ k,
 template <typename T, int DK, int DV>
 cudaError_t launch_typed(const void* q, const void* k, const void* v,
                          const void* beta, const float* g, int gpc, float* S, void* o, int BH,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, const QkNorm& nm) {
     constexpr int NT = 256;
     const T* const qt = static_cast<const T*>(q);
     const T* const kt = static_cast<const T*>(k);
@@ -144,22 +162,25 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
     const T* const bt = static_cast<const T*>(beta);
     T* const ot = static_cast<T*>(o);
     if (!g)
-        recurrent_step_kernel<T, DK, DV, NT, 0><<<BH, NT, 0, stream>>>(qt, kt, vt, bt, g, S, ot);
+        recurrent_step_kernel<T, DK, DV, NT, 0><<<BH, NT, 0, stream>>>(qt, kt, vt, bt, g, S, ot, nm);
     else if (gpc)
-        recurrent_step_kernel<T, DK, DV, NT, 2><<<BH, NT, 0, stream>>>(qt, kt, vt, bt, g, S, ot);
+        recurrent_step_kernel<T, DK, DV, NT, 2><<<BH, NT, 0, stream>>>(qt, kt, vt, bt, g, S, ot, nm);
     else
-        recurrent_step_kernel<T, DK, DV, NT, 1><<<BH, NT, 0, stream>>>(qt, kt, vt, bt, g, S, ot);
+        recurrent_step_kernel<T, DK, DV, NT, 1><<<BH, NT, 0, stream>>>(qt, kt, vt, bt, g, S, ot, nm);
     return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_dims(const void* q, const void* k, const void* v,
                         const void* beta, const float* g, int gpc, float* S, void* o, int BH,
-                        int dk, int dv, cudaStream_t st) {
-    if (dk == 128 && dv == 128) return launch_typed<T, 128, 128>(q, k, v, beta, g, gpc, S, o, BH, st);
-    if (dk == 128 && dv == 64) return launch_typed<T, 128, 64>(q, k, v, beta, g, gpc, S, o, BH, st);
-    if (dk == 64 && dv == 128) return launch_typed<T, 64, 128>(q, k, v, beta, g, gpc, S, o, BH, st);
-    if (dk == 64 && dv == 64) return launch_typed<T, 64, 64>(q, k, v, beta, g, gpc, S, o, BH, st);
+                        int dk, int dv, cudaStream_t st, const QkNorm& nm) {
+    if (dk == 128 && dv == 128)
+        return launch_typed<T, 128, 128>(q, k, v, beta, g, gpc, S, o, BH, st, nm);
+    if (dk == 128 && dv == 64)
+        return launch_typed<T, 128, 64>(q, k, v, beta, g, gpc, S, o, BH, st, nm);
+    if (dk == 64 && dv == 128)
+        return launch_typed<T, 64, 128>(q, k, v, beta, g, gpc, S, o, BH, st, nm);
+    if (dk == 64 && dv == 64) return launch_typed<T, 64, 64>(q, k, v, beta, g, gpc, S, o, BH, st, nm);
     return cudaErrorNotSupported;
 }
 
@@ -168,10 +189,12 @@ cudaError_t launch_dims(const void* q, const void* k, const void* v,
 cudaError_t launch_recurrent_step(const void* q, const void* k, const void* v,
                                   const void* beta, float* S, void* o, int BH,
                                   int dk, int dv, int dt, cudaStream_t stream, const float* g,
-                                  int g_per_channel) {
+                                  int g_per_channel, const QkNorm& norm) {
     if (BH <= 0) return cudaSuccess;
-    if (dt == 0) return launch_dims<float>(q, k, v, beta, g, g_per_channel, S, o, BH, dk, dv, stream);
-    return launch_dims<__nv_bfloat16>(q, k, v, beta, g, g_per_channel, S, o, BH, dk, dv, stream);
+    if (dt == 0)
+        return launch_dims<float>(q, k, v, beta, g, g_per_channel, S, o, BH, dk, dv, stream, norm);
+    return launch_dims<__nv_bfloat16>(q, k, v, beta, g, g_per_channel, S, o, BH, dk, dv, stream,
+                                      norm);
 }
 
 }  // namespace dn

@@ -9,6 +9,20 @@
 
 namespace dn {
 
+// Optional preparation of q and k inside the kernels that read them (the
+// ABI's dn_qk_norm): with l2norm every row of q and k (the head dimension)
+// becomes x / sqrt(sum x^2 + eps); q is then multiplied by qscale.  Each
+// kernel applies it to the rows it loads, before any product uses them.
+struct QkNorm {
+    int l2norm;
+    float qscale;
+    float eps;
+};
+constexpr QkNorm kNoNorm{0, 1.0f, 0.0f};
+__host__ __device__ inline bool norm_active(const QkNorm& n) {
+    return n.l2norm != 0 || n.qscale != 1.0f;
+}
+
 // Packed variable-length sequences: sequence n is tokens start[n] ..
 // start[n+1] - 1 of an [H][T][d] tensor, and chunk[n] counts the 64-token
 // chunks of the sequences before it.  Kernels take the table by value (a
@@ -27,7 +41,8 @@ using VarlenTable = SeqTable<kMaxVarlenSeqs>;
 cudaError_t launch_recurrent_step(const void* q, const void* k, const void* v,
                                   const void* beta, float* S, void* o, int BH,
                                   int dk, int dv, int dt, cudaStream_t stream,
-                                  const float* g = nullptr, int g_per_channel = 0);
+                                  const float* g = nullptr, int g_per_channel = 0,
+                                  const QkNorm& norm = kNoNorm);
 
 // Optional input preparation (see dn_qk_prepare): rows of d (64 or 128)
 // elements; q rows scaled by `scale` (after the L2 normalisation when
@@ -35,6 +50,13 @@ cudaError_t launch_recurrent_step(const void* q, const void* k, const void* v,
 cudaError_t launch_qk_prepare(const void* q, const void* k, void* q_out, void* k_out,
                               long long rows, int d, int normalize, float scale, float eps,
                               int dt, cudaStream_t stream);
+// Its gradient (see dn_qk_prepare_bwd): dq, dk from the raw rows q, k and
+// the gradients dq_out, dk_out of the prepared ones (dk untouched when
+// normalize == 0).
+cudaError_t launch_qk_prepare_bwd(const void* q, const void* k, const void* dq_out,
+                                  const void* dk_out, void* dq, void* dk, long long rows, int d,
+                                  int normalize, float scale, float eps, int dt,
+                                  cudaStream_t stream);
 
 // Chunkwise forward with fp32 CUDA-core arithmetic (any T >= 1).  o may be
 // nullptr (no outputs); S_chunks, if given, receives the state at the start
@@ -44,7 +66,7 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v,
                               const void* beta, const float* S0, void* o,
                               float* S_T, int BH, int T, int dk, int dv, int dt,
                               cudaStream_t stream, float* S_chunks = nullptr,
-                              const float* g = nullptr);
+                              const float* g = nullptr, const QkNorm& norm = kNoNorm);
 
 // Chunkwise backward (fp32 CUDA-core arithmetic): the gradients of
 // L = <d_o, o> + <d_S_T, S_T> for dn_chunk_fwd's outputs.  The workspace
@@ -68,10 +90,14 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
 // state at the start of every chunk ([BH][ceil(T/64)][dk][dv]).
 bool chunk_tc_supports(int dk, int dv, int dt);
 size_t chunk_tc_workspace_bytes(int BH, int T);
+// With prepared inputs (a QkNorm) the two-pass forms also keep the row
+// factors of every chunk after the tiles: this many bytes per chunk.
+size_t chunk_tc_side_bytes_per_chunk();
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v,
                             const void* beta, const float* S0, void* o,
                             float* S_T, int BH, int T, int dk, int dv, int dt,
-                            void* workspace, cudaStream_t stream, float* S_chunks = nullptr);
+                            void* workspace, cudaStream_t stream, float* S_chunks = nullptr,
+                            const QkNorm& norm = kNoNorm);
 
 // Varlen forms: q, k, v, beta, o are [H][T][.] (T the packed length), the
 // states [seqs.n][H][dk][dv].  The tensor-core form runs in two passes and
@@ -79,7 +105,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v,
 cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v,
                                    const void* beta, const float* S0, void* o, float* S_T,
                                    const VarlenTable& seqs, int H, int T, void* workspace,
-                                   cudaStream_t stream);
+                                   cudaStream_t stream, const QkNorm& norm = kNoNorm);
 // The backward's chain on tcgen05 (bf16, dk = dv = 128): G = dL/dS from the
 // last chunk to the first, with the forward's [PT; Tm] tiles (`tiles`, the
 // workspace the state recompute used) read transposed.  Writes G at every
@@ -95,15 +121,16 @@ size_t chunk_tc_gated_workspace_bytes(int BH, int T);
 cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, const void* beta,
                                   const float* g, const float* S0, void* o, float* S_T, int BH,
                                   int T, int dk, int dv, int dt, void* workspace,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, const QkNorm& norm = kNoNorm);
 // KDA: g is the fp32 [BH][T][dk] per-key-channel log keep rate.
 cudaError_t launch_chunk_simt_kda(const void* q, const void* k, const void* v, const void* beta,
                                   const float* g, const float* S0, void* o, float* S_T, int BH,
-                                  int T, int dk, int dv, int dt, cudaStream_t stream);
+                                  int T, int dk, int dv, int dt, cudaStream_t stream,
+                                  const QkNorm& norm = kNoNorm);
 cudaError_t launch_chunk_simt_varlen(const void* q, const void* k, const void* v,
                                      const void* beta, const float* S0, void* o, float* S_T,
                                      const VarlenTable& seqs, int H, int T, int dk, int dv,
-                                     int dt, cudaStream_t stream);
+                                     int dt, cudaStream_t stream, const QkNorm& norm = kNoNorm);
 
 // As launch_chunk_tc with the workspace in a static device array of
 // noalloc_max_tiles tiles (the caller has checked the size).  The array's

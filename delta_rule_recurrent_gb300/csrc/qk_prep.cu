@@ -116,6 +116,75 @@ qk_prepare_kernel(const T* q, const T* k, T* q_out, T* k_out, long long rows,
     }
 }
 
+// Gradient of the preparation with respect to its raw rows.  For a row x
+// with output y = f x, f = scale / n and n = sqrt(sum x^2 + eps) (chain rule
+// through dn/dx_i = x_i / n):
+//     dx = f (dy - x (x . dy) / n^2)      (normalize != 0)
+//     dx = scale dy                       (normalize == 0; k rows not visited)
+// Rows [0, rows) are q rows, [rows, 2 rows) k rows (no scale).  dx may equal
+// dy: each lane reads its elements of x and dy before the shuffles that end
+// with its own writes.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads)
+qk_prepare_bwd_kernel(const T* q, const T* k, const T* dq_out, const T* dk_out, T* dq, T* dk,
+                      long long rows, int normalize, float scale, float eps) {
+    constexpr int E = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long long nrows = normalize ? 2 * rows : rows;
+    const long long warp = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * kThreads) >> 5;
+    for (long long r = warp; r < nrows; r += nwarps) {  // warp-uniform
+        const bool is_q = r < rows;
+        const long long off = (is_q ? r : r - rows) * D + lane * E;
+        float g[E];
+        load_lane((is_q ? dq_out : dk_out) + off, g);
+        const float s = is_q ? scale : 1.0f;
+        float y[E];
+        if (normalize) {
+            float x[E];
+            load_lane((is_q ? q : k) + off, x);
+            float ss = 0.0f, xg = 0.0f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                ss = fmaf(x[e], x[e], ss);
+                xg = fmaf(x[e], g[e], xg);
+            }
+            const float n2 = warp_sum(ss) + eps;
+            const float inv = rsqrtf(n2);
+            const float c = warp_sum(xg) / n2;
+#pragma unroll
+            for (int e = 0; e < E; ++e) y[e] = s * inv * fmaf(-x[e], c, g[e]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) y[e] = s * g[e];
+        }
+        store_lane((is_q ? dq : dk) + off, y);
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_bwd_typed(const void* q, const void* k, const void* dq_out, const void* dk_out,
+                             void* dq, void* dk, long long rows, int normalize, float scale,
+                             float eps, cudaStream_t stream) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qk_prepare_bwd_kernel<T, D>,
+                                                          kThreads, 0);
+    if (e != cudaSuccess) return e;
+    const long long nrows = normalize ? 2 * rows : rows;
+    const long long per_block = kThreads / 32;
+    const long long need = (nrows + per_block - 1) / per_block;
+    const long long full = (long long)sms * (per_sm > 0 ? per_sm : 1);
+    const unsigned grid = (unsigned)(need < full ? need : full);
+    qk_prepare_bwd_kernel<T, D><<<grid, kThreads, 0, stream>>>(
+        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(dq_out),
+        static_cast<const T*>(dk_out), static_cast<T*>(dq), static_cast<T*>(dk), rows,
+        normalize, scale, eps);
+    return cudaGetLastError();
+}
+
 template <typename T, int D>
 cudaError_t launch_typed(const void* q, const void* k, void* q_out, void* k_out,
                          long long rows, int normalize, float scale, float eps,
@@ -155,6 +224,23 @@ cudaError_t launch_qk_prepare(const void* q, const void* k, void* q_out, void* k
                                                 stream);
     return launch_typed<__nv_bfloat16, 64>(q, k, q_out, k_out, rows, normalize, scale, eps,
                                            stream);
+}
+
+cudaError_t launch_qk_prepare_bwd(const void* q, const void* k, const void* dq_out,
+                                  const void* dk_out, void* dq, void* dk, long long rows, int d,
+                                  int normalize, float scale, float eps, int dt,
+                                  cudaStream_t stream) {
+    if (rows <= 0) return cudaSuccess;
+#define DN_PREP_BWD(T_, D_)                                                                    \
+    return launch_bwd_typed<T_, D_>(q, k, dq_out, dk_out, dq, dk, rows, normalize, scale, eps, \
+                                    stream)
+    if (dt == 0) {
+        if (d == 128) DN_PREP_BWD(float, 128);
+        DN_PREP_BWD(float, 64);
+    }
+    if (d == 128) DN_PREP_BWD(__nv_bfloat16, 128);
+    DN_PREP_BWD(__nv_bfloat16, 64);
+#undef DN_PREP_BWD
 }
 
 }  // namespace dn

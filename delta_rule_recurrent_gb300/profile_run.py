@@ -1,6 +1,6 @@
 """Runs one workload a few times through the public API, for profiler captures.
 
-    python -m delta_rule_recurrent_gb300.profile_run chunk [--B 8] [--T 2048] [--algo auto] [--reps 3] [--no-workspace]
+    python -m delta_rule_recurrent_gb300.profile_run chunk [--B 8] [--T 2048] [--algo auto] [--reps 3] [--no-workspace] [--qk-l2norm]
     python -m delta_rule_recurrent_gb300.profile_run decode [--B 256] [--steps 4]
     python -m delta_rule_recurrent_gb300.profile_run bwd [--B 8] [--T 2048] [--reps 2]
     python -m delta_rule_recurrent_gb300.profile_run gated [--B 8] [--T 2048] [--reps 3] [--no-workspace]
@@ -39,15 +39,18 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--steps", type=int, default=4)
     ap.add_argument("--no-workspace", action="store_true")
+    ap.add_argument("--qk-l2norm", action="store_true",
+                    help="chunk: raw q, k normalised and scaled inside the kernels")
     a = ap.parse_args(argv)
     dev = torch.device("cuda:0")
     if a.what == "chunk":
         over = {k: v for k, v in (("B", a.B), ("T", a.T)) if v is not None}
-        inp = workloads.workload_inputs("layer1p3b_bf16", **over)
+        inp = workloads.workload_inputs("layer1p3b_bf16", normalize=not a.qk_l2norm, **over)
         q, k, v, b = (x.to(dev) for x in (inp.q, inp.k, inp.v, inp.beta))
+        prep = dict(qk_l2norm=True, scale=inp.q.shape[-1] ** -0.5) if a.qk_l2norm else {}
         for _ in range(a.reps):
             o, _ = dn.chunk_fwd(q, k, v, b, algo=a.algo,
-                                workspace=None if a.no_workspace else "auto")
+                                workspace=None if a.no_workspace else "auto", **prep)
     elif a.what == "gated":
         over = {k: v for k, v in (("B", a.B), ("T", a.T)) if v is not None}
         inp = workloads.workload_inputs("layer1p3b_bf16", **over)

@@ -123,8 +123,10 @@ DN_API int dn_chunk_fwd_algo(const void *q, const void *k, const void *v,
                       void *stream, int algo);
 
 /* Scratch bytes the fastest dn_chunk_fwd path uses for this problem: one
- * 16 KB bf16 [PT; T] tile (128 x 64) per (batch, head, chunk) on the
- * tensor-core path (bf16, dk = dv = 128, C = 64), else 0.  Host-only. */
+ * 16 KB bf16 [PT; T] tile (128 x 64) and 1 KB of fp32 side vectors (the q
+ * and k row factors when dn_chunk_fwd_qk prepares q and k) per (batch, head,
+ * chunk) on the tensor-core path (bf16, dk = dv = 128, C = 64), else 0.
+ * Host-only. */
 DN_API size_t dn_chunk_fwd_workspace_bytes(int B, int H, int T, int dk, int dv,
                                     int C, int dt);
 
@@ -379,10 +381,95 @@ DN_API int dn_qk_prepare(const void *q, const void *k, void *q_out, void *k_out,
                   long long rows, int d, int normalize, float scale, float eps,
                   int dt, void *stream);
 
+/*
+ * dn_qk_prepare_bwd -- gradient of dn_qk_prepare with respect to its raw
+ * inputs, for training through the preparation.  Given the raw rows q, k and
+ * the gradients d_q_out, d_k_out of the prepared rows, per row x with
+ * n = sqrt(sum x^2 + eps) and f = scale / n (scale = 1 for k):
+ *     d_x = f (d_out - x (x . d_out) / n^2)      (normalize != 0)
+ *     d_q = scale d_q_out                        (normalize == 0; k unused)
+ * the chain rule through y = f x with dn/dx_i = x_i / n.  fp32 arithmetic,
+ * rounded once to `dt`.
+ *   q, k, d_q_out, d_k_out  [rows, d] dtype `dt` (k, d_k_out, d_k are read /
+ *                           written only when normalize != 0; q only then)
+ *   d_q, d_k                [rows, d] written; each may be its own incoming
+ *                           gradient (d_q == d_q_out, in place) but must
+ *                           not otherwise overlap an input or each other
+ *   rows, d, normalize, scale, eps, dt, stream  as for dn_qk_prepare
+ * Errors as for dn_qk_prepare.
+ */
+DN_API int dn_qk_prepare_bwd(const void *q, const void *k, const void *d_q_out,
+                             const void *d_k_out, void *d_q, void *d_k, long long rows,
+                             int d, int normalize, float scale, float eps, int dt,
+                             void *stream);
+
+/*
+ * In-kernel preparation of q and k.  The pages' layer asks its kernels to
+ * L2-normalise q and k themselves (use_qk_l2norm_in_kernel, DeltaNet.forward
+ * of fla/layers/delta_net.py) and scales the query by 1/sqrt(d_head) ("DeltaNet
+ * 引入 Delta Rule", garden.houmin.site/infra/delta-net; the d_k^{-1/2} read of
+ * "Kimi Delta Attention", fr.news.hada.io/topic?id=31925).  The *_qk entry
+ * points below take a dn_qk_norm (NULL: q and k used as given) and apply
+ *     q <- scale * q / sqrt(sum q^2 + eps),  k <- k / sqrt(sum k^2 + eps)
+ * (with l2norm == 0: q <- scale * q, k as given) to every row of the head
+ * dimension as the kernels load it, before any product uses it; q and k in
+ * memory are not modified.  The arithmetic is fp32 (sum of squares,
+ * reciprocal square root, products); the tensor-core kernels round the
+ * prepared rows to bf16 as their MMA operands, the CUDA-core kernels keep
+ * them in fp32.  This is dn_qk_prepare's arithmetic without its separate
+ * pass over q and k.  scale must be finite; with l2norm, eps finite and >= 0.
+ */
+typedef struct {
+    int l2norm;   /* nonzero: L2-normalise every row of q and k */
+    float scale;  /* multiplies q after the normalisation (1.0f: none) */
+    float eps;    /* added to the sum of squares (the pages use 1e-6) */
+} dn_qk_norm;
+
+/* dn_chunk_fwd_algo with an optional dn_qk_norm. */
+DN_API int dn_chunk_fwd_qk(const void *q, const void *k, const void *v, const void *beta,
+                           const float *S0, void *o, float *S_T, int B, int H, int T,
+                           int dk, int dv, int C, int dt, void *workspace,
+                           size_t workspace_bytes, void *stream, int algo,
+                           const dn_qk_norm *norm);
+/* dn_chunk_fwd_gated with an optional dn_qk_norm. */
+DN_API int dn_chunk_fwd_gated_qk(const void *q, const void *k, const void *v,
+                                 const void *beta, const float *g, const float *S0, void *o,
+                                 float *S_T, int B, int H, int T, int dk, int dv, int C,
+                                 int dt, void *workspace, size_t workspace_bytes,
+                                 void *stream, const dn_qk_norm *norm);
+/* dn_chunk_fwd_varlen with an optional dn_qk_norm. */
+DN_API int dn_chunk_fwd_varlen_qk(const void *q, const void *k, const void *v,
+                                  const void *beta, const float *S0, void *o, float *S_T,
+                                  const int *cu_seqlens, int N, int H, int T, int dk, int dv,
+                                  int C, int dt, void *workspace, size_t workspace_bytes,
+                                  void *stream, const dn_qk_norm *norm);
+/* dn_chunk_fwd_kda with a workspace (dn_chunk_fwd_kda_workspace_bytes; where
+ * that size is non-zero it selects the tensor-core form, NULL the CUDA-core
+ * kernel) and an optional dn_qk_norm. */
+DN_API int dn_chunk_fwd_kda_qk(const void *q, const void *k, const void *v,
+                               const void *beta, const float *g, const float *S0, void *o,
+                               float *S_T, int B, int H, int T, int dk, int dv, int C, int dt,
+                               void *workspace, size_t workspace_bytes, void *stream,
+                               const dn_qk_norm *norm);
+DN_API size_t dn_chunk_fwd_kda_workspace_bytes(int B, int H, int T, int dk, int dv, int C,
+                                               int dt);
+/* The decoding steps with an optional dn_qk_norm. */
+DN_API int dn_recurrent_step_qk(const void *q, const void *k, const void *v,
+                                const void *beta, float *S, void *o, int B, int H, int dk,
+                                int dv, int dt, void *stream, const dn_qk_norm *norm);
+DN_API int dn_recurrent_step_gated_qk(const void *q, const void *k, const void *v,
+                                      const void *beta, const float *g, float *S, void *o,
+                                      int B, int H, int dk, int dv, int dt, void *stream,
+                                      const dn_qk_norm *norm);
+DN_API int dn_recurrent_step_kda_qk(const void *q, const void *k, const void *v,
+                                    const void *beta, const float *g, float *S, void *o,
+                                    int B, int H, int dk, int dv, int dt, void *stream,
+                                    const dn_qk_norm *norm);
+
 /* ABI version of this header (bumped on incompatible changes). */
 DN_API int dn_abi_version(void);
 
-#define DN_ABI_VERSION 3
+#define DN_ABI_VERSION 4
 
 #ifdef __cplusplus
 }

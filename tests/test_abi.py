@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dn_abi_version() == 3
+    assert lib.dn_abi_version() == 4
     assert lib.dn_status_string(0) == b"DN_OK"
     assert lib.dn_status_string(1) == b"DN_ERR_INVALID_ARG"
     assert lib.dn_status_string(2) == b"DN_ERR_UNSUPPORTED"
@@ -58,11 +58,13 @@ def test_abi_version_and_status_strings(lib):
 
 def test_workspace_bytes(lib):
     """The tensor-core path (bf16, dk = dv = 128, C = 64) asks for one 16 KB
-    [PT; Tm] tile per (batch, head, chunk); every other case needs none."""
+    [PT; Tm] tile and 1 KB of side vectors per (batch, head, chunk); every
+    other case needs none."""
     f = lib.dn_chunk_fwd_workspace_bytes
-    assert f(8, 16, 2048, 128, 128, 64, 1) == 8 * 16 * 32 * 16384
-    assert f(1, 2, 130, 128, 128, 64, 1) == 2 * 3 * 16384
-    assert f(1, 1, 1, 128, 128, 64, 1) == 16384
+    # one 16 KB [PT; T] tile and 1 KB of row factors (prepared inputs) per chunk
+    assert f(8, 16, 2048, 128, 128, 64, 1) == 8 * 16 * 32 * (16384 + 1024)
+    assert f(1, 2, 130, 128, 128, 64, 1) == 2 * 3 * (16384 + 1024)
+    assert f(1, 1, 1, 128, 128, 64, 1) == 16384 + 1024
     assert f(1, 1, 0, 128, 128, 64, 1) == 0
     assert f(0, 4, 64, 128, 128, 64, 1) == 0
     assert f(8, 16, 2048, 128, 128, 64, 0) == 0  # fp32 I/O
@@ -191,7 +193,7 @@ def test_varlen_rejects_bad_offsets_before_any_cuda_call(lib):
     assert b"1024" in lib.dn_last_error()
     size = lib.dn_chunk_fwd_varlen_workspace_bytes
     arr = (ctypes.c_int * 4)(0, 65, 65, 100)
-    assert size(arr, 3, 2, 128, 128, 64, 1) == 2 * (2 + 0 + 1) * 16384
+    assert size(arr, 3, 2, 128, 128, 64, 1) == 2 * (2 + 0 + 1) * (16384 + 1024)
     assert size(arr, 3, 2, 64, 64, 64, 1) == 0
 
 

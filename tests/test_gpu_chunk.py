@@ -137,7 +137,7 @@ def test_workspace_checks():
     q, k, v, b = (dev(x) for x in (inp.q, inp.k, inp.v, inp.beta))
     lib = _lib.load()
     need = lib.dn_chunk_fwd_workspace_bytes(1, 2, 130, 128, 128, 64, 1)
-    assert need == 2 * 3 * 16384
+    assert need == 2 * 3 * (16384 + 1024)
     short = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(_lib.DeltaNetError, match="INVALID_ARG"):
         dn.chunk_fwd(q, k, v, b, workspace=short)

@@ -175,12 +175,15 @@ def decode_state(B: int, H: int, dk: int, dv: int, *, std: float = 0.1,
 
 def decode_step_inputs(B: int, H: int, dk: int, dv: int, *, step: int,
                        dtype="bf16", seed: int = 0,
-                       beta_scale: float = 2.0) -> DecodeInputs:
+                       beta_scale: float = 2.0, normalize: bool = True) -> DecodeInputs:
     """Inputs of decoding step ``step``: q, k = l2norm(N(0,1)), v ~ N(0,1),
-    beta = beta_scale * sigmoid(N(0,1)); seeded by (seed, step)."""
+    beta = beta_scale * sigmoid(N(0,1)); seeded by (seed, step).
+    normalize=False leaves q and k as drawn."""
     g = torch.Generator().manual_seed(int(seed) * 100003 + 7919 * int(step) + 1)
-    q = l2norm(torch.randn(B, H, dk, generator=g))
-    k = l2norm(torch.randn(B, H, dk, generator=g))
+    q = torch.randn(B, H, dk, generator=g)
+    k = torch.randn(B, H, dk, generator=g)
+    if normalize:
+        q, k = l2norm(q), l2norm(k)
     v = torch.randn(B, H, dv, generator=g)
     beta = torch.sigmoid(torch.randn(B, H, generator=g)) * float(beta_scale)
     dt = torch_dtype(dtype)
@@ -192,7 +195,7 @@ def workload_inputs(name: str, **overrides):
     """Inputs of a named sequence workload (not the decode one).
 
     Keyword overrides replace shape entries (B, H, T) to draw a smaller case
-    with the same recipe.  Returns ChunkInputs, or (ChunkInputs, expected_o)
+    with the same recipe; normalize=False leaves q and k unnormalised.  Returns ChunkInputs, or (ChunkInputs, expected_o)
     for the recall workload.
     """
     w = dict(WORKLOADS[name])
@@ -204,7 +207,7 @@ def workload_inputs(name: str, **overrides):
     return chunk_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
                         dtype=w["dtype"], seed=w["seed"],
                         feature_map="silu" if w["recipe"] == "silu" else "none",
-                        s0_std=w["s0_std"])
+                        s0_std=w["s0_std"], normalize=w.get("normalize", True))
 
 
 def decode_inputs_on_device(B: int, H: int, dk: int, dv: int, steps: int, *,

@@ -36,6 +36,8 @@ sys.path.insert(0, str(ROOT))
 METRIC = "delta-rule chunk fwd tokens/s on 1 GB300 + % roofline; decode step HBM GB/s"
 HEADLINE = "layer1p3b_bf16"
 DECODE = "decode_bf16"
+LONG = "long_prefill_bf16"
+E_SLICES = 4  # batch slices of the pipelined end-to-end leg
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 2**20
 
@@ -162,6 +164,25 @@ class ClockSampler:
         seen = sorted({names[i] for r in busy for i, flag in enumerate(r[3]) if flag == "Active"})
         return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": max(r[1] for r in rows),
                 "reasons": seen, "samples": len(busy)}
+
+
+def free_port() -> int:
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch_replicas(n: int, argv, script: str | None = None) -> int:
+    """Runs `script` (this file by default; the script that was started, from
+    main) as n ranks of one node under torchrun, one process per GPU,
+    rendezvous on 127.0.0.1; returns torchrun's exit code.  `python bench.py
+    --gpus N` without a torchrun environment goes through here, so it runs
+    the same replicas a torchrun launch of it does."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr=127.0.0.1", f"--master-port={free_port()}",
+           script or str(Path(__file__).resolve()), *argv]
+    return subprocess.call(cmd)
 
 
 def dist_env():
@@ -503,22 +524,79 @@ def run_ours(args, rank, world, local):
         kd_region_s, kd_launch = timed_loop(kda_decode_step, nsteps, stream, world)
         kd_region_s = max_over_ranks(kd_region_s, world)
         del dkgate, Sdk
+
+        # ---------------- long prefill: one long sequence per head, carried state --
+        wl = workloads.WORKLOADS[LONG]
+        lp = workloads.workload_inputs(LONG)
+        Bl, Hl, Tl, dkl, dvl = lp.shape
+        lq, lk, lv, lb = (x.to(dev) for x in (lp.q, lp.k, lp.v, lp.beta))
+        lS0 = lp.S0.to(dev)
+        lo = torch.empty(Bl, Hl, Tl, dvl, dtype=lq.dtype, device=dev)
+        lST = torch.empty(Bl, Hl, dkl, dvl, dtype=torch.float32, device=dev)
+        lneed = lib.dn_chunk_fwd_workspace_bytes(Bl, Hl, Tl, dkl, dvl, wl["C"],
+                                                 1 if lq.dtype == torch.bfloat16 else 0)
+        lws = torch.empty(lneed, dtype=torch.uint8, device=dev) if lneed else None
+
+        def long_step(_i):
+            dn.chunk_fwd(lq, lk, lv, lb, initial_state=lS0, out=lo, final_state=lST, algo=algo,
+                         workspace=lws)
+
+        lsteps = max(1, min(args.steps, 10))
+        for i in range(min(args.warmup, 3)):
+            long_step(i)
+        torch.cuda.synchronize()
+        lp_region_s, lp_launch = timed_loop(long_step, lsteps, stream, world)
+        lp_region_s = max_over_ranks(lp_region_s, world)
+        del lp, lq, lk, lv, lb, lS0, lo, lST, lws
     clk = clocks.summary()
     del dq, dkk, dvv, db
 
     # ---------------- e2e: public API from pinned host buffers --------------
+    # The batch in E_SLICES slices: slice i's inputs go host -> device on one
+    # copy stream, its forward runs on the compute stream once they are in,
+    # and its outputs (o and the final state) go device -> host on a second
+    # copy stream, so the copies of one slice overlap the compute and the
+    # copies of the others.  Every copy is one cudaMemcpyAsync of a
+    # contiguous slice.
     hq, hk, hv, hb = (x.pin_memory() for x in (inp.q, inp.k, inp.v, inp.beta))
     ho = torch.empty(B, H, T, dv, dtype=q.dtype).pin_memory()
+    hS = torch.empty(B, H, dk, dv, dtype=torch.float32).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hb))
-    d2h = ho.numel() * ho.element_size()
+    d2h = ho.numel() * ho.element_size() + hS.numel() * hS.element_size()
+    n_sl = E_SLICES if B % E_SLICES == 0 else 1
+    bs = B // n_sl
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    sl_ws = []
+    for i in range(n_sl):
+        need = lib.dn_chunk_fwd_workspace_bytes(bs, H, T, dk, dv, C,
+                                                1 if q.dtype == torch.bfloat16 else 0)
+        sl_ws.append(torch.empty(need, dtype=torch.uint8, device=dev) if need else None)
 
     def e2e_step(_i):
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        beta.copy_(hb, non_blocking=True)
-        dn.chunk_fwd(q, k, v, beta, out=o, final_state=S_T, algo=algo, workspace=ws)
-        ho.copy_(o, non_blocking=True)
+        arrived, done = [], []
+        up.wait_stream(stream)  # the previous step's forward has read its inputs
+        for i in range(n_sl):
+            sl = slice(i * bs, (i + 1) * bs)
+            with torch.cuda.stream(up):
+                for dst, src in ((q, hq), (k, hk), (v, hv), (beta, hb)):
+                    dst[sl].copy_(src[sl], non_blocking=True)
+                arrived.append(torch.cuda.Event())
+                arrived[-1].record(up)
+        for i in range(n_sl):
+            sl = slice(i * bs, (i + 1) * bs)
+            stream.wait_event(arrived[i])
+            dn.chunk_fwd(q[sl], k[sl], v[sl], beta[sl], out=o[sl], final_state=S_T[sl],
+                         algo=algo, workspace=sl_ws[i])
+            done.append(torch.cuda.Event())
+            done[-1].record(stream)
+        with torch.cuda.stream(down):
+            for i in range(n_sl):
+                sl = slice(i * bs, (i + 1) * bs)
+                down.wait_event(done[i])
+                ho[sl].copy_(o[sl], non_blocking=True)
+                hS[sl].copy_(S_T[sl], non_blocking=True)
+        stream.wait_stream(down)  # the step ends when its results are on the host
+        stream.wait_stream(up)
 
     for i in range(min(args.warmup, 3)):
         e2e_step(i)
@@ -526,6 +604,22 @@ def run_ours(args, rank, world, local):
     e2e_steps = max(1, min(args.steps, 50))
     e2e_s, _ = timed_loop(e2e_step, e2e_steps, stream, world)
     e2e_s = max_over_ranks(e2e_s, world)
+    # link rates seen by the copies alone (same buffers, same streams)
+    torch.cuda.synchronize()
+    c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    c0.record(up)
+    with torch.cuda.stream(up):
+        for dst, src in ((q, hq), (k, hk), (v, hv), (beta, hb)):
+            dst.copy_(src, non_blocking=True)
+    c1.record(up)
+    down.wait_event(c1)
+    with torch.cuda.stream(down):
+        ho.copy_(o, non_blocking=True)
+        hS.copy_(S_T, non_blocking=True)
+    c2.record(down)
+    torch.cuda.synchronize()
+    h2d_gbs = h2d / (c0.elapsed_time(c1) / 1e3) / 1e9
+    d2h_gbs = d2h / (c1.elapsed_time(c2) / 1e3) / 1e9
 
     # ---------------- numbers ----------------------------------------------
     tokens = B * T
@@ -644,6 +738,23 @@ def run_ours(args, rank, world, local):
                      "frac": cbytes / fp_launch_s / 1e9 / peaks["hbm_gbs"], "traffic": None,
                      "peak_source": f"{peak_src} (copy bandwidth)", "bytes_per_launch": cbytes},
     }
+    lp_launch_s = statistics.mean(lp_launch) / 1e3
+    lbytes = chunk_bytes(Bl, Hl, Tl, dkl, dvl, 2, True, True)
+    lflops = chunk_flops_per_token_head(wl["C"], dkl, dvl) * Bl * Hl * Tl
+    long_prefill = {
+        "workload": LONG, "steps": lsteps, "value": world * Bl * Tl * lsteps / lp_region_s,
+        "unit": "tokens/s", "ms_per_step": 1e3 * lp_region_s / lsteps,
+        "config": {"B": Bl, "H": Hl, "T": Tl, "dk": dkl, "dv": dvl, "S0": "N(0, 0.1^2) fp32"},
+        "roofline": {"bound": "hbm", "achieved": lbytes / lp_launch_s / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": lbytes / lp_launch_s / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{peak_src} (copy bandwidth)", "bytes_per_launch": lbytes,
+                     "launch_us": lp_launch_s * 1e6,
+                     "tensor": {"achieved": lflops / lp_launch_s / 1e12,
+                                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                "frac": lflops / lp_launch_s / 1e12 / peaks["bf16_tflops"],
+                                "flops_per_launch": lflops}},
+    }
     g_launch_s = statistics.mean(g_launch) / 1e3
     gs_launch_s = statistics.mean(gs_launch) / 1e3
     gflops = chunk_flops_per_token_head(C, dk, dv) * B * H * T
@@ -736,8 +847,14 @@ def run_ours(args, rank, world, local):
         "kda": kda,
         "e2e": {"value": world * tokens * e2e_steps / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": 1e3 * e2e_s / e2e_steps},
-        "gpu_launches": (launches_per_call * (args.steps + e2e_steps)   # chunk forward, e2e
+                "ms_per_step": 1e3 * e2e_s / e2e_steps,
+                "pipeline": f"{n_sl} batch slices: host->device copies, forward and "
+                            "device->host copies (o and the final state) on three streams",
+                "copy_only_ms": 1e3 * (h2d / h2d_gbs + d2h / d2h_gbs) / 1e9,
+                "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs},
+        "long_prefill": long_prefill,
+        "gpu_launches": (launches_per_call * (args.steps + n_sl * e2e_steps)  # chunk fwd, e2e
+                         + launches_per_call * lsteps                   # long prefill
                          + nsteps + (nsteps if dec_graph[0] else 0)     # decode, graph replay
                          + (4 if bwd_tc else 3) * bwd_steps             # recompute, chain, grads
                          + launches_per_call * vsteps                   # varlen
@@ -790,6 +907,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_replicas(args.gpus, sys.argv[1:], script=sys.argv[0]))
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
@@ -797,8 +916,9 @@ def main():
     if world > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     try:
         run_ours(args, rank, world, local)
     finally:

@@ -65,3 +65,25 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     args = argparse.Namespace(steps=1, warmup=3)
     assert bench.run_reference(args, rank=1, world=2) is None
     assert capsys.readouterr().out == ""
+
+
+def test_gpus_flag_launches_replica_ranks():
+    """``--gpus 2`` outside torchrun makes the bench re-run itself as two
+    ranks under torchrun (rendezvous on 127.0.0.1), each with its own rank
+    environment; the ranks here run the CPU stand-in of the GPU legs on gloo,
+    and rank 0 alone prints one line with n_gpus = 2 and the slowest rank's
+    time."""
+    import json
+    import subprocess
+    import sys
+    from pathlib import Path
+    stub = Path(__file__).with_name("bench_rank_stub.py")
+    res = subprocess.run([sys.executable, str(stub), "--gpus", "2", "--steps", "3",
+                          "--warmup", "3"], capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2 and line["local_rank"] == 0
+    assert line["seconds"] >= 0.1  # the slow rank's sleep
+    assert line["value"] == pytest.approx(2 * 3000.0 / line["seconds"])

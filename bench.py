@@ -501,16 +501,26 @@ def run_ours(args, rank, world, local):
         # ---------------- KDA: per-key-channel decay, chunk forward and step --
         kgate = workloads.gate_inputs(B, H, T, seed=w["seed"], channels=dk).to(dev)
         ok_, Sk_ = torch.empty_like(o), torch.empty_like(S_T)
+        kneed = lib.dn_chunk_fwd_kda_workspace_bytes(B, H, T, dk, dv, C, 1 if tc else 0)
+        kws = torch.empty(kneed, dtype=torch.uint8, device=dev) if kneed else None
 
-        def kda_step(_i):
-            dn.chunk_fwd_kda(q, k, v, beta, kgate, out=ok_, final_state=Sk_)
+        def kda_step(_i):  # the tcgen05 form where it applies
+            dn.chunk_fwd_kda(q, k, v, beta, kgate, out=ok_, final_state=Sk_, workspace=kws)
+
+        def kda_simt_step(_i):
+            dn.chunk_fwd_kda(q, k, v, beta, kgate, out=ok_, final_state=Sk_, workspace=None)
 
         for i in range(min(args.warmup, 3)):
             kda_step(i)
         torch.cuda.synchronize()
         k_region_s, k_launch = timed_loop(kda_step, gsteps, stream, world)
         k_region_s = max_over_ranks(k_region_s, world)
-        del kgate, ok_, Sk_
+        ksteps = max(1, min(args.steps, 3))
+        kda_simt_step(0)
+        torch.cuda.synchronize()
+        ks_region_s, ks_launch = timed_loop(kda_simt_step, ksteps, stream, world)
+        ks_region_s = max_over_ranks(ks_region_s, world)
+        del kgate, ok_, Sk_, kws
 
         dkgate = workloads.gate_inputs(Bd, Hd, seed=wd["seed"], channels=dkd).to(dev)
         Sdk = Sd.clone()
@@ -808,17 +818,41 @@ def run_ours(args, rank, world, local):
     k_launch_s = statistics.mean(k_launch) / 1e3
     kd_launch_s = statistics.mean(kd_launch) / 1e3
     kdbytes = dbytes + Bd * Hd * dkd * 4  # plus the fp32 per-channel log keep rates
+    ks_launch_s = statistics.mean(ks_launch) / 1e3
+    kbytes = cbytes + B * H * T * dk * 4  # plus the fp32 log keep rate per token, head and channel
+    if kneed:
+        k_arith = "tcgen05 bf16 MMAs, fp32 accumulation (decayed operands, two passes)"
+        k_roof = {"bound": "hbm", "achieved": kbytes / k_launch_s / 1e9, "peak": peaks["hbm_gbs"],
+                  "unit": "GB/s", "frac": kbytes / k_launch_s / 1e9 / peaks["hbm_gbs"],
+                  "traffic": None, "peak_source": f"{peak_src} (copy bandwidth)",
+                  "bytes_per_launch": kbytes, "launch_us": k_launch_s * 1e6,
+                  "tensor": {"achieved": gflops / k_launch_s / 1e12, "peak": peaks["bf16_tflops"],
+                             "unit": "TFLOP/s",
+                             "frac": gflops / k_launch_s / 1e12 / peaks["bf16_tflops"],
+                             "flops_per_launch": gflops}}
+    else:
+        k_arith = "fp32 CUDA cores"
+        k_roof = {"bound": "alu", "achieved": gflops / k_launch_s / 1e12, "peak": alu_peak,
+                  "unit": "TFLOP/s", "frac": gflops / k_launch_s / 1e12 / alu_peak,
+                  "traffic": None, "peak_source": alu_src, "flops_per_launch": gflops,
+                  "launch_us": k_launch_s * 1e6}
     kda = {
         "chunk": {"workload": HEADLINE, "steps": gsteps,
                   "value": world * tokens * gsteps / k_region_s, "unit": "tokens/s",
-                  "ms_per_step": 1e3 * k_region_s / gsteps, "arith": "fp32 CUDA cores",
-                  "gate": "alpha ~ U(0.9, 1) per key channel",
-                  "roofline": {"bound": "alu", "achieved": gflops / k_launch_s / 1e12,
-                               "peak": fp32_alu_tflops(2070.0), "unit": "TFLOP/s",
-                               "frac": gflops / k_launch_s / 1e12 / fp32_alu_tflops(2070.0),
-                               "traffic": None,
-                               "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz",
-                               "flops_per_launch": gflops, "launch_us": k_launch_s * 1e6}},
+                  "ms_per_step": 1e3 * k_region_s / gsteps, "arith": k_arith,
+                  "gate": "alpha ~ U(0.9, 1) per key channel", "workspace_bytes": kneed,
+                  "launches_per_call": 4 if kneed else 1, "vs_plain_call": k_launch_s / launch_s,
+                  "roofline": k_roof},
+        "chunk_cuda_cores": {"workload": HEADLINE, "steps": ksteps,
+                             "value": world * tokens * ksteps / ks_region_s, "unit": "tokens/s",
+                             "ms_per_step": 1e3 * ks_region_s / ksteps, "arith": "fp32 CUDA cores",
+                             "note": "the same call with no workspace",
+                             "roofline": {"bound": "alu", "achieved": gflops / ks_launch_s / 1e12,
+                                          "peak": alu_peak, "unit": "TFLOP/s",
+                                          "frac": gflops / ks_launch_s / 1e12 / alu_peak,
+                                          "traffic": None, "peak_source": alu_src,
+                                          "flops_per_launch": gflops,
+                                          "launch_us": ks_launch_s * 1e6}},
         "decode": {"workload": DECODE, "steps": nsteps,
                    "value": world * Bd * nsteps / kd_region_s, "unit": "tokens/s",
                    "ms_per_step": 1e3 * kd_region_s / nsteps,
@@ -861,7 +895,7 @@ def run_ours(args, rank, world, local):
                          + psteps                                       # q/k preparation
                          + launches_per_call * psteps                   # forward preparing q, k
                          + (2 if gneed else 1) * gsteps + gsteps + nsteps  # gated: both forms, decode
-                         + gsteps + nsteps),                            # KDA chunk, decode
+                         + (4 if kneed else 1) * gsteps + ksteps + nsteps),  # KDA: both forms, decode
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

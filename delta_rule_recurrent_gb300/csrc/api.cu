@@ -376,8 +376,10 @@ size_t dn_chunk_fwd_gated_workspace_bytes(int B, int H, int T, int dk, int dv, i
 }
 
 size_t dn_chunk_fwd_kda_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt) {
-    (void)B, (void)H, (void)T, (void)dk, (void)dv, (void)C, (void)dt;
-    return 0;
+    if (B <= 0 || H <= 0 || T <= 0 || C != 64 || !dn::chunk_tc_supports(dk, dv, dt)) return 0;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return 0;
+    return dn::chunk_tc_kda_workspace_bytes((int)BH, T);
 }
 
 // The decayed chunkwise forms: Gated DeltaNet (one log keep rate per token,
@@ -413,6 +415,10 @@ static int chunk_fwd_decayed(const void* q, const void* k, const void* v, const 
     const bool use_tc = workspace && need_ws > 0;
     if (use_tc)
         if (int st2 = check_workspace(c, workspace, need_ws, dev)) return st2;
+    if (per_channel && use_tc)
+        return cuda_status(dn::launch_chunk_tc_kda(q, k, v, beta, g, S0, o, S_T, (int)BH, T, dk,
+                                                   dv, dt, workspace, st, nm),
+                           "KDA chunk forward (tcgen05) launch");
     if (per_channel)
         return cuda_status(dn::launch_chunk_simt_kda(q, k, v, beta, g, S0, o, S_T, (int)BH, T,
                                                      dk, dv, dt, st, nm),

@@ -1086,6 +1086,13 @@ constexpr uint32_t P_OFF_BAR = P_OFF_DK + 256;     // mbarriers: tiles landed, M
 constexpr uint32_t P_OFF_MISC = P_OFF_BAR + 24;    // abort flag, TMEM address
 constexpr uint32_t kPrepSmemBytes = P_OFF_MISC + 16 + 1024;
 static_assert(kPrepCtasPerSm * (kPrepSmemBytes + 1024) <= 233472, "prepare kernel occupancy");
+// kSepB (the KDA form): the right factor of G = [K; Q] B^T is its own tile,
+// B = K . exp(-G), loaded with [K; Q] into a 16 KB region after the rest.
+constexpr uint32_t P_OFF_KB = (P_OFF_MISC + 16 + 1023) & ~1023u;
+constexpr uint32_t kPrepSmemBytesSepB = P_OFF_KB + 16384 + 1024;
+constexpr int kPrepCtasPerSmSepB = 3;
+static_assert(kPrepCtasPerSmSepB * (kPrepSmemBytesSepB + 1024) <= 233472,
+              "prepare kernel occupancy (separate right factor)");
 static_assert(P_OFF_X % 1024 == 0 && kXBytes >= kTile, "[PT; Tm] over the solve array");
 
 // Row i of A or P times the decay ratios exp(G_i - G_j) (entries past the
@@ -1124,14 +1131,18 @@ __device__ __forceinline__ void decay_row_tmem(uint32_t taddr, const float* Gs, 
     tmem_wait_st();
 }
 
-template <int NMAX, bool kGate>
-__global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
+// kSepB: KDA's decayed operands; [K; Q] are the loaded K . exp G, Q . exp G
+// and tm_ws2 maps the right factor K . exp(-G) (G = [K; Q] (K exp(-G))^T
+// carries every ratio exp(G_i - G_j) inside its sums).
+template <int NMAX, bool kGate, bool kSepB = false>
+__global__ void __launch_bounds__(kPrepThreads, kSepB ? kPrepCtasPerSmSepB : kPrepCtasPerSm)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_ws, const __nv_bfloat16* __restrict__ beta,
                   int T, int nchunks, int items, const __grid_constant__ SeqTable<NMAX> seqs,
                   const float* __restrict__ gate, float* __restrict__ side,
                   const __grid_constant__ CUtensorMap tm_ws2, QkNorm nm) {
     static_assert(!kGate || NMAX == 1, "gating on the batched layout");
+    static_assert(!kSepB || (NMAX == 1 && !kGate), "a separate right factor on the batched layout");
     constexpr int kBar = 1, B_TILES = 0, B_MMA = 1, B_END = 2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -1147,7 +1158,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const Ctl ctl{base + P_OFF_BAR, reinterpret_cast<volatile int*>(misc)};
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
     const int t = threadIdx.x, row = t & 63;
-    const uint32_t kq = base + P_OFF_KQ, tp = base + P_OFF_X;
+    const uint32_t kq = base + P_OFF_KQ, tp = base + P_OFF_X, kb = base + P_OFF_KB;
     const uint32_t lane_base = (uint32_t)(32 * (t >> 5)) << 16;
 
     if (t == 0) {
@@ -1157,7 +1168,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_ws);
-        if (kGate) prefetch_tensormap(&tm_ws2);
+        if (kGate || kSepB) prefetch_tensormap(&tm_ws2);
     }
     if (t < 32) {
         tmem_alloc(smem_addr(tmem_holder), kGate ? 128 : 64);
@@ -1172,11 +1183,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     auto load_tiles = [&](int w) {
         const ChunkRef r = prep_item(seqs, w, nchunks, T);
         const uint32_t bar = ctl.bar(B_TILES);
-        mbar_arrive_expect_tx(bar, 4 * 8192);
+        mbar_arrive_expect_tx(bar, (kSepB ? 6 : 4) * 8192);
         tma_load_3d(kq, &tm_k, bar, 0, r.row0, r.z);
         tma_load_3d(kq + kRegKQ, &tm_k, bar, 64, r.row0, r.z);
         tma_load_3d(kq + 8192, &tm_q, bar, 0, r.row0, r.z);
         tma_load_3d(kq + kRegKQ + 8192, &tm_q, bar, 64, r.row0, r.z);
+        if constexpr (kSepB) {  // the right factor: two 64 x 64 dk halves
+            tma_load_3d(kb, &tm_ws2, bar, 0, r.row0, r.z);
+            tma_load_3d(kb + 8192, &tm_ws2, bar, 64, r.row0, r.z);
+        }
     };
     // Strength of token t of item w (0 past T), as volatile loads kept in place.
     auto load_beta = [&](int w) -> uint16_t {
@@ -1241,7 +1256,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t a = kq + (uint32_t)(kk >> 2) * kRegKQ + (uint32_t)(kk & 3) * 32u;
-                    mma_bf16_ss(tmem, sw128_desc(a, 16, 1024), sw128_desc(a, 16, 1024), IDESC_G,
+                    const uint32_t bb =
+                        kSepB ? kb + (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u : a;
+                    mma_bf16_ss(tmem, sw128_desc(a, 16, 1024), sw128_desc(bb, 16, 1024), IDESC_G,
                                 kk > 0);
                 }
                 mma_commit(ctl.bar(B_MMA));
@@ -1488,7 +1505,8 @@ constexpr uint32_t OFF_MISC = OFF_BAR + 8 * kBars;     // abort flag, TMEM addre
 constexpr uint32_t kSideCopyBytes = 528;
 constexpr uint32_t OFF_SIDE = OFF_MISC + 16;
 constexpr uint32_t OFF_DEC = OFF_SIDE + 2 * kSideCopyBytes;
-constexpr uint32_t kSmemBytes = OFF_DEC + 256 + 1024;
+constexpr uint32_t kSmemBytes = OFF_DEC + 512 + 1024;  // dec: 64 (gated) or 128 (KDA) fp32
+static_assert(2 * (kStageKQ + kTile) <= kStages * kStageKQ, "KDA's two stages in the ring");
 static_assert(kSmemBytes <= 232448, "scan kernel shared memory");
 static_assert(OFF_SIDE % 16 == 0 && kSideCopyBytes % 16 == 0 && OFF_DEC % 16 == 0,
               "bulk copies into the side slots need 16-byte alignment");
@@ -1500,9 +1518,15 @@ constexpr uint32_t ID_VP = idesc_bf16_f32(128, 128, 1, 0);  // A v^T (MN-major),
 constexpr uint32_t ID_SP = idesc_bf16_f32(128, 128, 0, 0) | (1u << 14);  // A S^T (TMEM), B -[-Q'; W] (K-major, negated)
 constexpr uint32_t ID_KB = idesc_bf16_f32(128, 128, 0, 1);  // A U'^T (TMEM) or [PT;Tm], B K (MN-major)
 
+// The [K; Q] ring: kStages stages of 32 KB, or for KDA (kda = true) two
+// stages of 48 KB, each [K~; Q~] followed by the state update's K^ tile (two
+// 64-row dk halves); nst stages use 2 nst full barriers and nst empty ones.
 struct Smem {
     uint32_t base;
-    __device__ uint32_t kq(int c) const { return base + OFF_KQ + (uint32_t)(c % kStages) * kStageKQ; }
+    int nst = kStages;
+    uint32_t stride = kStageKQ;
+    __device__ uint32_t kq(int c) const { return base + OFF_KQ + (uint32_t)(c % nst) * stride; }
+    __device__ uint32_t kh(int c) const { return kq(c) + kStageKQ; }
     __device__ uint32_t v(int c) const { return base + OFF_V + (uint32_t)(c % kVBufs) * kTile; }
     __device__ uint32_t tp(int g) const { return base + OFF_TP + (uint32_t)g * kTile; }
     __device__ uint32_t qw(int g) const { return base + OFF_QW + (uint32_t)g * 2u * kTile; }
@@ -1517,27 +1541,36 @@ struct Smem {
 __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q,
                          const CUtensorMap* tm_k, const CUtensorMap* tm_v, const CUtensorMap* tm_ws,
                          const SeqSpan& sp, int nchunks, const CUtensorMap* tm_ws2,
-                         const float* side) {
+                         const float* side, const CUtensorMap* tm_kh) {
     const int z = sp.z, r0 = sp.row0, w0 = sp.wsbase;
+    const int ns = sm.nst, nkqb = 2 * sm.nst;
     int nkq = 0, nv = 0, ntp = 0;
     long long t0 = clock64();
     while ((nkq < nchunks || nv < nchunks || ntp < nchunks) && !ctl.aborted()) {
         bool progressed = false;
         if (nkq < nchunks &&
-            (nkq < kStages ||
-             mbar_test_wait(ctl.bar(B_KQ_EMPTY + nkq % kStages), (uint32_t)(nkq / kStages - 1) & 1u))) {
-            const uint32_t st = sm.kq(nkq), bar = ctl.bar(B_KQ_FULL + nkq % kKQ);
-            mbar_arrive_expect_tx(bar, 4 * 8192);
+            (nkq < ns ||
+             mbar_test_wait(ctl.bar(B_KQ_EMPTY + nkq % ns), (uint32_t)(nkq / ns - 1) & 1u))) {
+            const uint32_t st = sm.kq(nkq), bar = ctl.bar(B_KQ_FULL + nkq % nkqb);
+            mbar_arrive_expect_tx(bar, (tm_kh ? 6 : 4) * 8192);
             tma_load_3d(st, tm_k, bar, 0, r0 + nkq * kC, z);
             tma_load_3d(st + kRegKQ, tm_k, bar, 64, r0 + nkq * kC, z);
             tma_load_3d(st + 8192, tm_q, bar, 0, r0 + nkq * kC, z);
             tma_load_3d(st + kRegKQ + 8192, tm_q, bar, 64, r0 + nkq * kC, z);
-            if (nkq + kStages < nchunks) {  // warm L2 for this stage's next tiles
-                const int y = r0 + (nkq + kStages) * kC;
+            if (tm_kh) {  // KDA: the state update's K^ rides with the stage
+                tma_load_3d(sm.kh(nkq), tm_kh, bar, 0, r0 + nkq * kC, z);
+                tma_load_3d(sm.kh(nkq) + 8192, tm_kh, bar, 64, r0 + nkq * kC, z);
+            }
+            if (nkq + ns < nchunks) {  // warm L2 for this stage's next tiles
+                const int y = r0 + (nkq + ns) * kC;
                 tma_prefetch_l2_3d(tm_k, 0, y, z);
                 tma_prefetch_l2_3d(tm_k, 64, y, z);
                 tma_prefetch_l2_3d(tm_q, 0, y, z);
                 tma_prefetch_l2_3d(tm_q, 64, y, z);
+                if (tm_kh) {
+                    tma_prefetch_l2_3d(tm_kh, 0, y, z);
+                    tma_prefetch_l2_3d(tm_kh, 64, y, z);
+                }
             }
             ++nkq;
             progressed = true;
@@ -1577,8 +1610,8 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
             if (clock64() - t0 > kTimeoutCycles) ctl.raise();
         }
     }
-    for (int b = 0; b < kKQ; ++b) {  // leave nothing in flight (bounded waits)
-        const int n_b = (nkq - b + kKQ - 1) / kKQ;
+    for (int b = 0; b < nkqb; ++b) {  // leave nothing in flight (bounded waits)
+        const int n_b = (nkq - b + nkqb - 1) / nkqb;
         if (n_b > 0) mbar_wait(ctl.bar(B_KQ_FULL + b), (uint32_t)(n_b - 1) & 1u, kTimeoutNs);
     }
     for (int b = 0; b < kVBufs; ++b) {
@@ -1620,6 +1653,26 @@ __device__ __forceinline__ void tmem_scale64(uint32_t src, float keep) {
         tmem_st32(src + 32u * h, r);
     }
 }
+// KDA: S^T scaled in place column by column (64 fp32 columns: key channels
+// d0 .. d0 + 63) by keep[d] = exp G_C[d] (shared memory).
+__device__ __forceinline__ void tmem_scale64_cols(uint32_t src, const float* __restrict__ keep) {
+    float x[64];
+    tmem_ld64f(src, x);
+    const float4* const k4 = reinterpret_cast<const float4*>(keep);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r[32];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float4 f = k4[8 * h + e];
+            r[4 * e] = __float_as_uint(f.x * x[32 * h + 4 * e]);
+            r[4 * e + 1] = __float_as_uint(f.y * x[32 * h + 4 * e + 1]);
+            r[4 * e + 2] = __float_as_uint(f.z * x[32 * h + 4 * e + 2]);
+            r[4 * e + 3] = __float_as_uint(f.w * x[32 * h + 4 * e + 3]);
+        }
+        tmem_st32(src + 32u * h, r);
+    }
+}
 __device__ __forceinline__ void tmem_pack64_cols(uint32_t src, uint32_t dst,
                                                  const float* __restrict__ dec) {
     float x[64];
@@ -1642,7 +1695,10 @@ __device__ __forceinline__ void tmem_pack64_cols(uint32_t src, uint32_t dst,
 // chunk group has released [Q'; -W] they are read, dec into sdec for the U'
 // pack, before the D1 MMAs free the slot, and the keep scaling of S^T runs
 // while those MMAs (which read the bf16 copy) are in flight.
-template <bool kRec, bool kGate>
+// kKda: S <- diag(exp G_C) S + K^T U' with K^ = K . exp(G_C - G) from the
+// stage; the 128 per-channel keep factors arrive with [PT; Tm] the same way,
+// are copied to sdec and scale S^T's columns while the D1 MMAs run.
+template <bool kRec, bool kGate, bool kKda = false>
 __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                            const float* __restrict__ S0, float* __restrict__ S_T,
                            float* __restrict__ S_chunks, int bh, int nchunks,
@@ -1660,7 +1716,8 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
     }
     tmem_wait_st();
 
-    static_assert(!(kGate && kRec), "no state recording on the gated form");
+    static_assert(!((kGate || kKda) && kRec), "no state recording on the decayed forms");
+    constexpr bool kSide = kGate || kKda;
     for (int c = 0; c < nchunks; ++c) {
         const int g = c & 1;
         {   // the previous update done; gated: this chunk's decay vectors in too
@@ -1670,9 +1727,9 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
             bool ok = true;
             if (t == 0) {
                 if (c > 0) ok = ctl.wait(B_S_READY, (uint32_t)(c - 1));
-                if (kGate && ok) ok = ctl.wait(B_TP_FULL + g, (uint32_t)(c >> 1));
+                if (kSide && ok) ok = ctl.wait(B_TP_FULL + g, (uint32_t)(c >> 1));
             }
-            if ((c > 0 || kGate) && wg_sync_or(kBar, !ok)) return;
+            if ((c > 0 || kSide) && wg_sync_or(kBar, !ok)) return;
         }
         tc_fence_after_sync();
         float keep = 1.f;
@@ -1680,6 +1737,10 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
             const float* const slot = sside + g * (kSideCopyBytes / 4);
             keep = slot[128];
             if (t < 16) reinterpret_cast<float4*>(sdec)[t] = reinterpret_cast<const float4*>(slot + 64)[t];
+        }
+        if constexpr (kKda) {  // exp G_C per key channel, read before D1 frees the slot
+            const float* const slot = sside + g * (kSideCopyBytes / 4);
+            if (t < 32) reinterpret_cast<float4*>(sdec)[t] = reinterpret_cast<const float4*>(slot)[t];
         }
         // S^T -> bf16 (dk 0-63, then 64-127); S itself recorded when asked
         if constexpr (kRec) {
@@ -1714,6 +1775,11 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
             tmem_scale64(lane + C_ST, keep);
             tmem_scale64(lane + C_ST + 64u, keep);
         }
+        if constexpr (kKda) {  // S^T <- S^T diag(exp G_C) while the D1 MMAs read the bf16 copy
+            __syncwarp();
+            tmem_scale64_cols(lane + C_ST, sdec);
+            tmem_scale64_cols(lane + C_ST + 64u, sdec + 64);
+        }
         if (t == 0 && ok) {
             ok = ctl.wait(B_D1_FULL, (uint32_t)c);
             if (ok) mbar_arrive(ctl.bar(B_O_READY));
@@ -1729,13 +1795,14 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         wg_sync(kBar);
         if (t == 0) {
             tc_fence_after_sync();
-            const uint32_t kq = sm.kq(c);
+            // S^T += U'^T K over the chunk's tokens (KDA: K^, 64-row dk halves)
+            const uint32_t kb = kKda ? sm.kh(c) : sm.kq(c), lbo = kKda ? 8192u : kRegKQ;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)  // S^T += U'^T K over the chunk's tokens
-                mma_bf16_ts(tmem + C_ST, tmem + C_UB + 8u * kk,
-                            sw128_desc(kq + 2048u * kk, kRegKQ, 1024), ID_KB, 1);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ts(tmem + C_ST, tmem + C_UB + 8u * kk, sw128_desc(kb + 2048u * kk, lbo, 1024),
+                            ID_KB, 1);
             mma_commit(ctl.bar(B_S_READY));
-            mma_commit(ctl.bar(B_KQ_EMPTY + c % kStages));
+            mma_commit(ctl.bar(B_KQ_EMPTY + c % sm.nst));
             // Only now may the o writer start the next chunk's v part: its MMAs
             // then queue behind the state update the next S conversion waits on.
             mbar_arrive(ctl.bar(B_U_READ));
@@ -1789,7 +1856,7 @@ __device__ void group_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         // [PT; Tm] is loaded only after the state released this buffer set,
         // so the [Q'; -W] tile is free as well.
         if (t == 0)
-            ok = ctl.wait(B_KQ_FULL + c % kKQ, (uint32_t)(c / kKQ)) &&
+            ok = ctl.wait(B_KQ_FULL + c % (2 * sm.nst), (uint32_t)(c / (2 * sm.nst))) &&
                  ctl.wait(B_TP_FULL + g, (uint32_t)(c >> 1));
         if (kGate || prep) {
             if (wg_sync_or(kBar, !ok)) return;
@@ -1888,7 +1955,10 @@ __device__ void writer_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t
 // factors folded in when q and k are prepared); otherwise, when q and k are
 // prepared in the kernels, every chunk's row factors d_q [64], d_k [64]
 // (NULL if they are not).
-template <bool kRec, int NMAX, bool kGate = false>
+// kKda: tm_ws2 maps K^ = K . exp(G_C - G) (the state update's operand, loaded
+// with each stage), tm_q / tm_k the decayed Q . exp G, K . exp G, and side
+// holds exp G_C per key channel for every chunk.
+template <bool kRec, int NMAX, bool kGate = false, bool kKda = false>
 __global__ void __launch_bounds__(512, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ws,
@@ -1899,7 +1969,9 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
-    const scan::Smem sm{base};
+    static_assert(!(kKda && (kGate || kRec || NMAX != 1)), "KDA on the batched forward");
+    const scan::Smem sm{base, kKda ? 2 : scan::kStages,
+                        kKda ? kStageKQ + kTile : kStageKQ};
     int* const misc = reinterpret_cast<int*>(smem_raw + (base - raw_addr) + scan::OFF_MISC);
     const Ctl ctl{base + scan::OFF_BAR, reinterpret_cast<volatile int*>(misc)};
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
@@ -1923,7 +1995,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_ws);
-        if (kGate) prefetch_tensormap(&tm_ws2);
+        if (kGate || kKda) prefetch_tensormap(&tm_ws2);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_holder), 512);
@@ -1937,15 +2009,16 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (warp == 0) {
         if (lane == 0)
             scan::producer(ctl, sm, &tm_q, &tm_k, &tm_v, &tm_ws, sp, nchunks,
-                           kGate ? &tm_ws2 : nullptr, cside);
+                           kGate ? &tm_ws2 : nullptr, cside, kKda ? &tm_ws2 : nullptr);
     } else if (warp >= 4 && warp < 8) {
         const int t = tid - 128;
-        scan::state_body<kRec, kGate>(ctl, sm, tmem, t, S0, S_T, S_chunks, bh, nchunks, sside,
+        scan::state_body<kRec, kGate, kKda>(ctl, sm, tmem, t, S0, S_T, S_chunks, bh, nchunks, sside,
                                       sdec);
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 0);
     } else if (warp >= 8 && warp < 12) {
         const int t = tid - 256;
-        scan::group_body<kGate>(ctl, sm, tmem, t, nchunks, sside, !kGate && side != nullptr);
+        scan::group_body<kGate>(ctl, sm, tmem, t, nchunks, sside,
+                                !kGate && !kKda && side != nullptr);
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 1);
     } else if (warp >= 12) {
         const int t = tid - 384;
@@ -2486,6 +2559,66 @@ cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, c
         side, mws2, norm);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mws2, S0,
+                                                       static_cast<__nv_bfloat16*>(o), S_T, nullptr,
+                                                       T, 1, batched, side);
+    return cudaGetLastError();
+}
+
+size_t chunk_tc_kda_workspace_bytes(int BH, int T) {
+    if (BH <= 0 || T <= 0) return 0;
+    const size_t items = (size_t)BH * (size_t)((T + kC - 1) / kC);
+    const size_t op = (size_t)BH * (size_t)T * kD * sizeof(__nv_bfloat16);  // one [BH][T][128] operand
+    const size_t fix = ((items + 1) * sizeof(int) + 255) & ~(size_t)255;
+    return items * (kTile + kSideFloats * sizeof(float)) + 4 * op + fix;
+}
+
+// KDA on tensor cores: the decayed operands (kda_decay_kernel), the prepare
+// pass on [K~; Q~] (K-)^T, the exact tiles of any chunk beyond the separable
+// range (kda_fix_kernel), then the scan with K^ and the per-channel keep.
+// Workspace: [PT; Tm] tiles | side vectors | Q~ | K~ | K^ | K- (the four
+// operands [BH][T][128] bf16 each) | the list of chunks past the separable
+// range (a count and up to one index per chunk).
+cudaError_t launch_chunk_tc_kda(const void* q, const void* k, const void* v, const void* beta,
+                                const float* g, const float* S0, void* o, float* S_T, int BH,
+                                int T, int dk, int dv, int dt, void* workspace,
+                                cudaStream_t stream, const QkNorm& norm) {
+    if (!chunk_tc_supports(dk, dv, dt)) return cudaErrorNotSupported;
+    if (BH <= 0 || T <= 0) return cudaSuccess;
+    if (!workspace || !o || !g) return cudaErrorInvalidValue;
+    const int nchunks = (T + kC - 1) / kC;
+    const long long items = (long long)BH * nchunks;
+    if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    uint8_t* const ws = static_cast<uint8_t*>(workspace);
+    const size_t op = (size_t)BH * (size_t)T * kD * sizeof(__nv_bfloat16);
+    float* const side = reinterpret_cast<float*>(ws + (size_t)items * kTile);
+    uint8_t* const qt = ws + (size_t)items * (kTile + kSideFloats * sizeof(float));
+    uint8_t* const kt = qt + op;
+    uint8_t* const kh = kt + op;
+    uint8_t* const kb = kh + op;
+    int* const fix = reinterpret_cast<int*>(kb + op);
+    cudaError_t err = launch_kda_decay(q, k, g, qt, kt, kh, kb, side, fix, BH, T, norm, stream);
+    if (err != cudaSuccess) return err;
+    CUtensorMap mq, mk, mv, mws, mkh, mkb;
+    if (!make_map(&mq, qt, BH, T) || !make_map(&mk, kt, BH, T) || !make_map(&mv, v, BH, T) ||
+        !make_map(&mkh, kh, BH, T) || !make_map(&mkb, kb, BH, T) ||
+        !make_ws_map(&mws, workspace, BH, nchunks))
+        return cudaErrorInvalidValue;
+    auto prep_kernel = chunk_prep_kernel<1, false, true>;
+    auto scan_kernel = chunk_scan_kernel<false, 1, false, true>;
+    if ((err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kPrepSmemBytesSepB)) != cudaSuccess ||
+        (err = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    scan::kSmemBytes)) != cudaSuccess)
+        return err;
+    const SeqTable<1> batched{};
+    const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSmSepB);
+    prep_kernel<<<grid, kPrepThreads, kPrepSmemBytesSepB, stream>>>(
+        mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, nchunks, (int)items, batched,
+        nullptr, nullptr, mkb, kNoNorm);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if ((err = launch_kda_fix(q, k, beta, g, fix, workspace, BH, T, norm, stream)) != cudaSuccess)
+        return err;
+    scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mkh, S0,
                                                        static_cast<__nv_bfloat16*>(o), S_T, nullptr,
                                                        T, 1, batched, side);
     return cudaGetLastError();

@@ -122,6 +122,23 @@ cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, c
                                   const float* g, const float* S0, void* o, float* S_T, int BH,
                                   int T, int dk, int dv, int dt, void* workspace,
                                   cudaStream_t stream, const QkNorm& norm = kNoNorm);
+// KDA on tensor cores (bf16, dk = dv = 128; g the fp32 [BH][T][dk] per-key-
+// channel log keep rate), with a workspace of chunk_tc_kda_workspace_bytes.
+size_t chunk_tc_kda_workspace_bytes(int BH, int T);
+cudaError_t launch_chunk_tc_kda(const void* q, const void* k, const void* v, const void* beta,
+                                const float* g, const float* S0, void* o, float* S_T, int BH,
+                                int T, int dk, int dv, int dt, void* workspace,
+                                cudaStream_t stream, const QkNorm& norm = kNoNorm);
+// Its CUDA-core parts (kda_tc.cu): the decayed operands of every chunk
+// (qt, kt, kh, kb: [BH][T][128] bf16; side: 256 fp32 per chunk) with the list
+// of chunks beyond the separable range (fix: a count, then chunk indices;
+// 1 + BH * nchunks ints), and the exact [PT; Tm] tiles of those chunks.
+cudaError_t launch_kda_decay(const void* q, const void* k, const float* g, void* qt, void* kt,
+                             void* kh, void* kb, float* side, int* fix, int BH, int T,
+                             const QkNorm& nm, cudaStream_t stream);
+cudaError_t launch_kda_fix(const void* q, const void* k, const void* beta, const float* g,
+                           const int* fix, void* tiles, int BH, int T, const QkNorm& nm,
+                           cudaStream_t stream);
 // KDA: g is the fp32 [BH][T][dk] per-key-channel log keep rate.
 cudaError_t launch_chunk_simt_kda(const void* q, const void* k, const void* v, const void* beta,
                                   const float* g, const float* S0, void* o, float* S_T, int BH,

@@ -85,6 +85,26 @@ def test_gated_workspace_bytes(lib):
     assert f(8, 16, 2048, 128, 128, 32, 1) == 0
 
 
+def test_kda_workspace_bytes(lib):
+    """The KDA tensor-core form needs, per chunk, a 16 KB [PT; Tm] tile and
+    1 KB of side vectors, four bf16 [B, H, T, 128] operands (K . exp G,
+    Q . exp G, K . exp(G_C - G), K . exp(-G)), and a list of the chunks past
+    the separable range (a count and one int per chunk, rounded up to 256
+    bytes); elsewhere none."""
+    f = lib.dn_chunk_fwd_kda_workspace_bytes
+
+    def size(BH, T):
+        chunks = BH * ((T + 63) // 64)
+        return chunks * (16384 + 1024) + 4 * BH * T * 256 + -(-(chunks + 1) * 4 // 256) * 256
+
+    assert f(8, 16, 2048, 128, 128, 64, 1) == size(128, 2048)
+    assert f(1, 2, 130, 128, 128, 64, 1) == size(2, 130)
+    assert size(2, 130) == 2 * (3 * (16384 + 1024) + 4 * 130 * 256) + 256
+    assert f(1, 1, 0, 128, 128, 64, 1) == 0
+    assert f(8, 16, 2048, 128, 128, 64, 0) == 0
+    assert f(8, 16, 2048, 64, 64, 64, 1) == 0
+
+
 def test_gated_rejects_a_short_workspace_before_any_cuda_call(lib):
     need = lib.dn_chunk_fwd_gated_workspace_bytes(1, 2, 130, 128, 128, 64, 1)
     st = lib.dn_chunk_fwd_gated(None, None, None, None, None, None, None, None, 1, 2, 130,

@@ -125,3 +125,76 @@ def test_steps_reject_mismatched_inputs_before_any_launch():
         dn.chunk_fwd_kda(q[:, :, None], q[:, :, None], q[:, :, None],
                          torch.zeros(B, H, 1, device="cuda"), g[:, :, None],
                          final_state=torch.zeros(B, H, d, device="cuda"))
+
+
+def _kda_tc_workspace(B, H, T):
+    n = dn.load().dn_chunk_fwd_kda_workspace_bytes(B, H, T, 128, 128, 64, 1)
+    assert n > 0
+    return torch.empty(n, dtype=torch.uint8, device="cuda")
+
+
+REGIMES = {"mild": (0.9, 1.0), "strong": (0.3, 1.0), "extreme": (0.05, 0.3)}
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 1000])
+@pytest.mark.parametrize("regime", list(REGIMES))
+def test_kda_tc_chunk_ragged(T, regime):
+    """The tensor-core form (bf16, dk = dv = 128) over ragged lengths, with an
+    initial state, in three decay regimes: mild and strong keep every chunk
+    within the separable range (one tensor-core product forms A and P);
+    extreme (per-token keep rates 0.05-0.3) takes whole chunks past exp(-80)
+    on every channel, so their tiles come from the exact CUDA-core path."""
+    B, H = 2, 3
+    lo, hi = REGIMES[regime]
+    inp = workloads.chunk_inputs(B, H, T, 128, 128, dtype="bf16", seed=T + 11,
+                                 feature_map="silu", s0_std=0.5)
+    g = workloads.gate_inputs(B, H, T, seed=T + 3, lo=lo, hi=hi, channels=128)
+    o, S = dn.chunk_fwd_kda(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g),
+                            initial_state=dev(inp.S0), workspace=_kda_tc_workspace(B, H, T))
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.forward_kda(inp.q, inp.k, inp.v, inp.beta, g, inp.S0)
+    check_every_head(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
+                     TOL[torch.bfloat16], f"KDA tcgen05 {regime} T{T}")
+
+
+def test_kda_tc_mixed_channels_take_the_exact_path():
+    """Half the key channels decay hard (keep 0.05-0.3) and half barely (0.95-1):
+    every full chunk leaves the separable range on some channel, and the
+    exact tiles must agree with the oracle with the slow channels intact."""
+    B, H, T = 1, 4, 300
+    inp = workloads.chunk_inputs(B, H, T, 128, 128, dtype="bf16", seed=71,
+                                 feature_map="silu", s0_std=0.3)
+    g_hard = workloads.gate_inputs(B, H, T, seed=72, lo=0.05, hi=0.3, channels=128)
+    g_soft = workloads.gate_inputs(B, H, T, seed=73, lo=0.95, hi=1.0, channels=128)
+    g = torch.where(torch.arange(128) % 2 == 0, g_hard, g_soft).contiguous()
+    o, S = dn.chunk_fwd_kda(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g),
+                            initial_state=dev(inp.S0))
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.forward_kda(inp.q, inp.k, inp.v, inp.beta, g, inp.S0)
+    check_every_head(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
+                     TOL[torch.bfloat16], "KDA tcgen05 mixed channels")
+
+
+def test_kda_tc_agrees_with_the_cuda_core_kernel():
+    B, H, T = 2, 2, 700
+    inp = workloads.chunk_inputs(B, H, T, 128, 128, dtype="bf16", seed=74,
+                                 feature_map="silu", s0_std=0.2)
+    g = workloads.gate_inputs(B, H, T, seed=75, lo=0.8, channels=128)
+    args = [dev(x) for x in (inp.q, inp.k, inp.v, inp.beta, g)]
+    o1, S1 = dn.chunk_fwd_kda(*args, initial_state=dev(inp.S0), workspace="auto")
+    o2, S2 = dn.chunk_fwd_kda(*args, initial_state=dev(inp.S0), workspace=None)
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.forward_kda(inp.q, inp.k, inp.v, inp.beta, g, inp.S0)
+    for o, S, what in ((o1, S1, "tcgen05"), (o2, S2, "cuda cores")):
+        check_every_head(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref,
+                         TOL[torch.bfloat16], what)
+    assert rel_l2(o1.double().cpu().numpy(), o2.double().cpu().numpy()) <= TOL[torch.bfloat16]
+
+
+def test_kda_tc_workspace_too_small_is_rejected():
+    B, H, T = 1, 2, 100
+    inp = workloads.chunk_inputs(B, H, T, 128, 128, dtype="bf16", seed=1)
+    g = workloads.gate_inputs(B, H, T, seed=1, channels=128)
+    ws = _kda_tc_workspace(B, H, T)[:-16]
+    with pytest.raises(RuntimeError, match="workspace"):
+        dn.chunk_fwd_kda(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta), dev(g), workspace=ws)

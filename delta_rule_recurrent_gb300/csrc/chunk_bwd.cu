@@ -410,13 +410,15 @@ cudaError_t launch_bwd_dims(const void* q, const void* k, const void* v, const v
 
 }  // namespace
 
-// Workspace: S at every chunk start, G at every chunk end (fp32), then the
-// tensor-core forward's own scratch where that path records the states.
+// Workspace.  Tensor-core path (bf16, dk = dv = 128): S at every chunk start
+// and G at every chunk end as bf16, the forward's [PT; Tm] tiles and every
+// chunk's (I + A)^{-1} (bf16 64 x 64).  Otherwise S and G in fp32.
 size_t chunk_bwd_workspace_bytes(int BH, int T, int dk, int dv, int dt) {
     if (BH <= 0 || T <= 0) return 0;
-    const size_t states =
-        2 * (size_t)BH * (size_t)((T + kC - 1) / kC) * (size_t)dk * (size_t)dv * sizeof(float);
-    return states + (chunk_tc_supports(dk, dv, dt) ? chunk_tc_workspace_bytes(BH, T) : 0);
+    const size_t items = (size_t)BH * (size_t)((T + kC - 1) / kC);
+    if (chunk_tc_supports(dk, dv, dt))
+        return items * (4 * (size_t)dk * dv * 2 + 64 * 64 * 2) + chunk_tc_workspace_bytes(BH, T);
+    return 2 * items * (size_t)dk * (size_t)dv * sizeof(float);
 }
 
 cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const void* beta,
@@ -426,21 +428,37 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
                              const char** stage) {
     if (BH <= 0 || T <= 0) return cudaSuccess;
     *stage = "state recompute";
-    const size_t per = (size_t)BH * ((T + kC - 1) / kC) * (size_t)dk * dv;
+    const size_t items = (size_t)BH * ((T + kC - 1) / kC);
+    const size_t per = items * (size_t)dk * dv;
+    if (chunk_tc_supports(dk, dv, dt)) {
+        // The tensor-core path: the two-pass forward records S (a bf16 hi
+        // and lo tile per chunk) and X, the tcgen05 chain G (likewise) and
+        // d_v, the tcgen05 gradient kernel d_q, d_k and d_beta.
+        __nv_bfloat16* const Sb = static_cast<__nv_bfloat16*>(workspace);
+        __nv_bfloat16* const Gb = Sb + 2 * per;
+        __nv_bfloat16* const Xb = Gb + 2 * per;
+        void* const tiles = Xb + items * 64 * 64;
+        cudaError_t err = launch_chunk_tc(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt,
+                                          tiles, stream, Sb, kNoNorm, Xb);
+        if (err != cudaSuccess) return err;
+        *stage = "state-gradient chain";
+        err = launch_chunk_bwd_chain_tc(q, k, d_o, d_S_T, d_v, d_S0, Gb, tiles, BH, T, stream);
+        if (err != cudaSuccess) return err;
+        *stage = "gradient kernel";
+        return launch_chunk_bwd_grads_tc(q, k, v, beta, d_o, Sb, Gb, Xb, tiles, d_q, d_k, d_beta,
+                                         BH, T, stream);
+    }
     float* const Sc = static_cast<float*>(workspace);
     float* const Gc = Sc + per;
-    const bool tc = chunk_tc_supports(dk, dv, dt);
-    float* const tiles = Gc + per;  // the tensor-core recompute's [PT; Tm] tiles
-    cudaError_t err = tc
-        ? launch_chunk_tc(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt, tiles, stream, Sc)
-        : launch_chunk_simt(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt, stream, Sc);
+    cudaError_t err =
+        launch_chunk_simt(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt, stream, Sc);
     if (err != cudaSuccess) return err;
     *stage = "gradient kernels";
     if (dt == 0)
         return launch_bwd_dims<float>(q, k, v, beta, d_o, d_S_T, d_q, d_k, d_v, d_beta, d_S0, Sc,
                                       Gc, BH, T, dk, dv, nullptr, stream);
     return launch_bwd_dims<__nv_bfloat16>(q, k, v, beta, d_o, d_S_T, d_q, d_k, d_v, d_beta, d_S0,
-                                          Sc, Gc, BH, T, dk, dv, tc ? tiles : nullptr, stream);
+                                          Sc, Gc, BH, T, dk, dv, nullptr, stream);
 }
 
 }  // namespace dn

@@ -1140,7 +1140,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                   const __grid_constant__ CUtensorMap tm_ws, const __nv_bfloat16* __restrict__ beta,
                   int T, int nchunks, int items, const __grid_constant__ SeqTable<NMAX> seqs,
                   const float* __restrict__ gate, float* __restrict__ side,
-                  const __grid_constant__ CUtensorMap tm_ws2, QkNorm nm) {
+                  const __grid_constant__ CUtensorMap tm_ws2, QkNorm nm,
+                  __nv_bfloat16* __restrict__ xrec) {
     static_assert(!kGate || NMAX == 1, "gating on the batched layout");
     static_assert(!kSepB || (NMAX == 1 && !kGate), "a separate right factor on the batched layout");
     constexpr int kBar = 1, B_TILES = 0, B_MMA = 1, B_END = 2;
@@ -1331,9 +1332,18 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         {
             float x[64];
             if (t < 64) {
+                // the backward's state recompute also records X = (I + A)^{-1} (bf16,
+                // [64][64] row-major per chunk), which the gradient of A needs
+                uint4* const xr = xrec ? reinterpret_cast<uint4*>(xrec + (size_t)w * 4096 + t * 64)
+                                       : nullptr;
 #pragma unroll
                 for (int e = 0; e < 64; e += 4) {
                     const float4 xv = lds4(X + t * kP + e), bv = lds4(betas + e);
+                    if (xrec && (e & 7) == 4) {
+                        const float4 xp = lds4(X + t * kP + e - 4);
+                        xr[e >> 3] = make_uint4(pack_bf16(xp.x, xp.y), pack_bf16(xp.z, xp.w),
+                                                pack_bf16(xv.x, xv.y), pack_bf16(xv.z, xv.w));
+                    }
                     x[e] = xv.x * bv.x;
                     x[e + 1] = xv.y * bv.y;
                     x[e + 2] = xv.z * bv.z;
@@ -1625,13 +1635,19 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
 }
 
 // 64 fp32 TMEM columns (lane of the calling thread) -> 32 bf16-pair columns;
-// with `rec`, the fp32 values also go to rec[e * kD], e = 0..63.
-__device__ __forceinline__ void tmem_pack64(uint32_t src, uint32_t dst, float* rec = nullptr) {
+// with `rec`, the values also go to rec[e * kD], e = 0..63, rounded to bf16
+// as in the packed operand.
+__device__ __forceinline__ void tmem_pack64(uint32_t src, uint32_t dst,
+                                            __nv_bfloat16* rec = nullptr) {
     float x[64];
     tmem_ld64f(src, x);
-    if (rec) {
+    if (rec) {  // x = hi + lo: hi here, lo one [128][128] tile further on
 #pragma unroll
-        for (int e = 0; e < 64; ++e) rec[(size_t)e * kD] = x[e];
+        for (int e = 0; e < 64; ++e) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(x[e]);
+            rec[(size_t)e * kD] = h;
+            rec[(size_t)(kD + e) * kD] = __float2bfloat16_rn(x[e] - __bfloat162float(h));
+        }
     }
     uint32_t p[32];
 #pragma unroll
@@ -1688,7 +1704,9 @@ __device__ __forceinline__ void tmem_pack64_cols(uint32_t src, uint32_t dst,
     tmem_st32(dst, p);
 }
 
-// kRec: also record S at every chunk start (the backward's recompute); the
+// kRec: also record S at every chunk start (the backward's recompute) as two
+// bf16 tiles, hi = bf16(S) and lo = bf16(S - hi), whose sum carries S to
+// about 16 significant bits; the
 // forward proper is compiled without it, so its state chain carries no test.
 // kGate: S <- exp(G_C) S + K^T diag(exp(G_C - G_s)) U' per chunk.  The decay
 // vectors arrive with [PT; Tm] (sside, one slot per buffer set); once the
@@ -1701,7 +1719,7 @@ __device__ __forceinline__ void tmem_pack64_cols(uint32_t src, uint32_t dst,
 template <bool kRec, bool kGate, bool kKda = false>
 __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                            const float* __restrict__ S0, float* __restrict__ S_T,
-                           float* __restrict__ S_chunks, int bh, int nchunks,
+                           __nv_bfloat16* __restrict__ S_chunks, int bh, int nchunks,
                            const float* sside, float* sdec) {
     constexpr int kBar = 1;
     const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
@@ -1744,7 +1762,7 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         }
         // S^T -> bf16 (dk 0-63, then 64-127); S itself recorded when asked
         if constexpr (kRec) {
-            float* const rec = S_chunks + ((size_t)bh * nchunks + c) * kD * kD + t;
+            __nv_bfloat16* const rec = S_chunks + 2 * ((size_t)bh * nchunks + c) * kD * kD + t;
             tmem_pack64(lane + C_ST, lane + C_SB, rec);
             tmem_pack64(lane + C_ST + 64u, lane + C_SB + 32u, rec + 64 * kD);
         } else {
@@ -1964,7 +1982,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ws,
                   const __grid_constant__ CUtensorMap tm_ws2,
                   const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
-                  float* __restrict__ S_T, float* __restrict__ S_chunks, int T, int H,
+                  float* __restrict__ S_T, __nv_bfloat16* __restrict__ S_chunks, int T, int H,
                   const __grid_constant__ SeqTable<NMAX> seqs, const float* __restrict__ side) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -2161,7 +2179,7 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
 
 __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                            const float* __restrict__ d_S_T, float* __restrict__ d_S0,
-                           float* __restrict__ G_chunks, int bh, int nchunks) {
+                           __nv_bfloat16* __restrict__ G_chunks, int bh, int nchunks) {
     constexpr int kBar = 1;
     const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
     // d_S_T^T into TMEM: lane t holds dv column t (zeros without d_S_T).
@@ -2179,7 +2197,7 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         if (i > 0 && !wg_wait(ctl, B_G_READY, (uint32_t)(i - 1), t, kBar)) return;
         tc_fence_after_sync();
         {   // G^T -> bf16, and G itself recorded as the gradient at chunk c's end
-            float* const rec = G_chunks + ((size_t)bh * nchunks + c) * kD * kD + t;
+            __nv_bfloat16* const rec = G_chunks + 2 * ((size_t)bh * nchunks + c) * kD * kD + t;
             scan::tmem_pack64(lane + C_GT, lane + C_GB, rec);
             scan::tmem_pack64(lane + C_GT + 64u, lane + C_GB + 32u, rec + 64 * kD);
         }
@@ -2320,7 +2338,7 @@ chunk_bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_do,
                           const __grid_constant__ CUtensorMap tm_ws, const float* __restrict__ d_S_T,
                           __nv_bfloat16* __restrict__ d_v, float* __restrict__ d_S0,
-                          float* __restrict__ G_chunks, int T) {
+                          __nv_bfloat16* __restrict__ G_chunks, int T) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -2373,6 +2391,442 @@ chunk_bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
 }
 
+// ------------------------------------------------- backward gradient kernel
+// The backward's per-chunk gradients on tcgen05 (bf16 operands, fp32
+// accumulation in TMEM), one CTA of one warpgroup per (batch, head, chunk).
+// With the chunk's rows K, Q, V, dO, strengths beta, the state S at its start
+// and the state gradient G at its end (both [dk][dv], as the recompute and
+// the chain recorded them), X = (I + A)^{-1} and Tm = X diag(beta):
+//     R = V - K S,  U' = Tm R,  dU' = P^T dO + K G,  dV = Tm^T dU'
+//     dP = tril(dO U'^T),  dTm = dU' R^T
+//     dQ = dO S^T + dP K,   dK = dP^T Q + U' G^T - dV S^T + Z K
+//     dA = strict_tril(-X^T dTm Tm^T),  Z = diag(beta) dA + (diag(beta) dA)^T
+//     dbeta_j = sum_i X_ij dTm_ij + sum_l dA_jl (K K^T)_jl
+// (the algebra of chunk_bwd.cu, with dTm diag(beta) X^T = dTm Tm^T).  Every
+// product runs transposed, with a feature (dk or dv) on the 128 TMEM lanes
+// and the chunk's 64 tokens on the columns, so each MMA is M = 128:
+//     R^T = V^T - S^T K^T,       U'^T = R^T Tm^T,       dU'^T = dO^T P + G^T K^T
+//     dV^T = dU'^T Tm,           [dU'; dO] [U'; R]^T   (dTm and dP as two of its blocks)
+//     M1 = dTm Tm^T,             [X^T; 0] [M1 | dTm]   (dA and diag(X^T dTm))
+//     [dQ^T | dK^T] = S [dO; -dV]^T + K^T [dP; Z]^T, plus Q^T dP + G U'^T on dK^T.
+// Results that feed a later product as a [token][feature] operand are
+// written into shared memory one feature column per thread (thread = TMEM
+// lane), the 128-byte swizzled layout TMA writes; results used as a left
+// operand from TMEM are packed to bf16 pairs in place.  One thread issues
+// every MMA; each phase ends on an MMA commit, waited with the bounded waits
+// of the forward kernels.
+namespace bgrad {
+// Shared memory over the phases (the "lo" tiles carry what bf16 rounding
+// drops from S, G, R and dU', so that d_beta, a dot product of dU' with R
+// that cancels heavily, keeps fp32-like accuracy):
+//   DV rows 0-63: G lo (dk 0-63) -> dU' hi;  rows 64-127: dO;
+//   DV rows 128-191: V -> dU' lo -> -dV;  UR: S lo -> [U'; R hi];
+//   TP rows 0-63 and PZ rows 0-63: G lo (dk 64-127) -> R lo -> (PZ) dP.
+constexpr uint32_t kRegDV = 192 * 128;                // a dv half of [dU'; dO; V or -dV]
+constexpr uint32_t OFF_KQ = 0;                        // [K; Q]: 2 dk halves x 128 rows
+constexpr uint32_t OFF_DV = OFF_KQ + kStageKQ;        // 2 dv halves x 192 rows
+constexpr uint32_t OFF_S = OFF_DV + 2 * kRegDV;       // S: 2 dv halves x 128 dk rows (fp32 dA later)
+constexpr uint32_t OFF_G = OFF_S + 2 * kTile;         // G: likewise
+constexpr uint32_t OFF_TP = OFF_G + 2 * kTile;        // rows 64-127: Tm
+constexpr uint32_t OFF_PZ = OFF_TP + kTile;           // rows 0-63 dP [t][s]; 64-127 P [s][t], then Z
+constexpr uint32_t OFF_UR = OFF_PZ + kTile;           // 2 dv halves x [U'; R]; later the [M1 | dTm] blocks
+constexpr uint32_t OFF_XI = OFF_UR + 2 * kTile;       // X [t][a] bf16
+constexpr uint32_t OFF_ZB = OFF_XI + 8192;            // zeros: the lower block of [X^T; 0]
+constexpr uint32_t OFF_BAR = OFF_ZB + 8192;
+constexpr int kBars = 4;                              // loads, MMA commits, drain
+constexpr uint32_t OFF_BETA = OFF_BAR + 8 * kBars;    // 64 fp32
+constexpr uint32_t OFF_MISC = OFF_BETA + 256;         // abort flag, TMEM address
+constexpr uint32_t kSmemBytes = OFF_MISC + 16 + 1024;
+static_assert(kSmemBytes <= 232448, "gradient kernel shared memory");
+static_assert(OFF_DV % 1024 == 0 && OFF_S % 1024 == 0 && OFF_UR % 1024 == 0 &&
+              OFF_XI % 1024 == 0 && OFF_ZB % 1024 == 0 && kRegDV % 1024 == 0, "tile alignment");
+constexpr int kDAPitch = 65;  // fp32 dA rows over the spent S
+// TMEM columns (512 allocated):
+constexpr uint32_t C_G1 = 0;    // [K; Q] K^T: K K^T (rows 0-63), Q K^T (rows 64-127)
+constexpr uint32_t C_R = 64;    // R^T, then dV^T, then M1
+constexpr uint32_t C_B = 128;   // a bf16 left operand: R^T, then dU'^T, then the dTm block
+constexpr uint32_t C_U = 160;   // U'^T
+constexpr uint32_t C_E = 224;   // dU'^T
+constexpr uint32_t C_QK = 160;  // [dQ^T | dK^T], over U'^T and dU'^T once they are read
+constexpr uint32_t C_PT = 288;  // [dU'; dO] [U'; R]^T, then [X^T; 0] [M1 | dTm]
+enum : int { B_LOAD = 0, B_MMA = 1, B_END = 2 };
+
+// Thread j (a feature lane) writes its 64 values, one per token row t, into
+// column j of rows row0 .. row0 + 63 of a [row][feature] tile whose two
+// 64-feature halves are regions `stride` bytes apart, times `sign`, as bf16.
+__device__ __forceinline__ void store_col64(uint32_t region0, uint32_t stride, int row0, int j,
+                                            const float (&x)[64], float sign) {
+    const uint32_t region = region0 + (uint32_t)(j >> 6) * stride;
+    const int cj = j & 63;
+#pragma unroll
+    for (int t = 0; t < 64; ++t) {
+        const uint32_t a = region + sw128(row0 + t, cj >> 3) + (uint32_t)(cj & 7) * 2u;
+        const __nv_bfloat16 h = __float2bfloat16_rn(sign * x[t]);
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(*reinterpret_cast<const uint16_t*>(&h))
+                     : "memory");
+    }
+}
+// The matching read: column j of rows row0 .. row0 + 63 into x (as fp32).
+__device__ __forceinline__ void load_col64(uint32_t region0, uint32_t stride, int row0, int j,
+                                           float (&x)[64]) {
+    const uint32_t region = region0 + (uint32_t)(j >> 6) * stride;
+    const int cj = j & 63;
+#pragma unroll
+    for (int t = 0; t < 64; ++t) {
+        const uint32_t a = region + sw128(row0 + t, cj >> 3) + (uint32_t)(cj & 7) * 2u;
+        uint16_t u;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(u) : "r"(a) : "memory");
+        x[t] = __bfloat162float(__ushort_as_bfloat16(u));
+    }
+}
+// What bf16 rounding drops from x (x - bf16(x), exact in fp32).
+__device__ __forceinline__ float bf16_rest(float x) {
+    return x - __bfloat162float(__float2bfloat16_rn(x));
+}
+// 64 fp32 values -> 32 bf16-pair TMEM columns of the calling thread's lane.
+__device__ __forceinline__ void pack64_tmem(uint32_t dst, const float (&x)[64]) {
+    uint32_t p[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) p[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+    tmem_st32(dst, p);
+}
+
+// One thread's MMA phases (tcgen05, issued by thread 0).
+__device__ __forceinline__ void issue_phase(int phase, uint32_t tmem, uint32_t base) {
+    const uint32_t kq = base + OFF_KQ, dv = base + OFF_DV, ss = base + OFF_S, gg = base + OFF_G;
+    const uint32_t tp = base + OFF_TP, pz = base + OFF_PZ, ur = base + OFF_UR, xi = base + OFF_XI;
+    // K-major operand step kk over a 128-element K split in two regions `stride` apart
+    auto kmaj = [](uint32_t a, uint32_t stride, int kk) {
+        return sw128_desc(a + (uint32_t)(kk >> 2) * stride + (uint32_t)(kk & 3) * 32u, 16, 1024);
+    };
+    // MN-major operand step kk (16 rows) with 64-element blocks `lbo` apart
+    auto mnmaj = [](uint32_t a, uint32_t lbo, int kk) {
+        return sw128_desc(a + (uint32_t)kk * 2048u, lbo, 1024);
+    };
+    constexpr uint32_t kNegB = 1u << 14;
+    if (phase == 0) {
+        // G1 = [K; Q] K^T
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_G1, kmaj(kq, kRegKQ, kk), kmaj(kq, kRegKQ, kk),
+                        idesc_bf16_f32(128, 64, 0, 0), kk > 0);
+        // -(S^T K^T): A = S^T (MN-major, dv blocks), B = K^T (K-major), B negated;
+        // S = hi + lo (lo over UR)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_R, mnmaj(ss, kTile, kk), kmaj(kq, kRegKQ, kk),
+                        idesc_bf16_f32(128, 64, 1, 0) | kNegB, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_R, mnmaj(ur, kTile, kk), kmaj(kq, kRegKQ, kk),
+                        idesc_bf16_f32(128, 64, 1, 0) | kNegB, 1);
+    } else if (phase == 1) {
+        // U'^T = R^T Tm^T: A = R^T (TMEM), B = Tm^T (K-major Tm rows)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ts(tmem + C_U, tmem + C_B + 8u * kk, kmaj(tp + 8192u, 0, kk),
+                        idesc_bf16_f32(128, 64, 0, 0), kk > 0);
+        // dU'^T = dO^T P + G^T K^T
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + C_E, mnmaj(dv + 8192u, kRegDV, kk), mnmaj(pz + 8192u, 8192, kk),
+                        idesc_bf16_f32(128, 64, 1, 1), kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_E, mnmaj(gg, kTile, kk), kmaj(kq, kRegKQ, kk),
+                        idesc_bf16_f32(128, 64, 1, 0), 1);
+        // ... + G lo^T K^T: dk rows 0-63 over DV rows 0-63, 64-127 over TP / PZ rows 0-63
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_E, kk < 4 ? mnmaj(dv, kRegDV, kk) : mnmaj(tp, kTile, kk - 4),
+                        kmaj(kq, kRegKQ, kk), idesc_bf16_f32(128, 64, 1, 0), 1);
+    } else if (phase == 2) {
+        // dV^T = dU'^T Tm: A = dU'^T (TMEM), B = Tm (MN-major Tm rows)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ts(tmem + C_R, tmem + C_B + 8u * kk, mnmaj(tp + 8192u, 8192, kk),
+                        idesc_bf16_f32(128, 64, 0, 1), kk > 0);
+        // [dU'; dO] [U'; R]^T (N = 128), then the dTm block's lo terms:
+        // + [dU' hi; dO] R lo^T (R lo over TP / PZ rows 0-63) + [dU' lo; -] R hi^T
+        // (dU' lo in DV rows 128-191; rows 64-127 of that A read the next 8 KB,
+        // which only reach the unused rows of the block)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_PT, kmaj(dv, kRegDV, kk), kmaj(ur, kTile, kk),
+                        idesc_bf16_f32(128, 128, 0, 0), kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_PT + 64u, kmaj(dv, kRegDV, kk), kmaj(tp, kTile, kk),
+                        idesc_bf16_f32(128, 64, 0, 0), 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_PT + 64u, kmaj(dv + 16384u, kRegDV, kk),
+                        kmaj(ur + 8192u, kTile, kk), idesc_bf16_f32(128, 64, 0, 0), 1);
+    } else if (phase == 3) {
+        // M1 = dTm Tm^T: A = [dTm; -] (TMEM), B = Tm^T (K-major)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ts(tmem + C_R, tmem + C_B + 8u * kk, kmaj(tp + 8192u, 0, kk),
+                        idesc_bf16_f32(128, 64, 0, 0), kk > 0);
+        // [dQ^T | dK^T] = S [dO; -dV]^T (N = 128)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_QK, kmaj(ss, kTile, kk), kmaj(dv + 8192u, kRegDV, kk),
+                        idesc_bf16_f32(128, 128, 0, 0), kk > 0);
+        // dK^T += Q^T dP (A = Q^T MN-major, B = dP MN-major) + G U'^T (K-major both)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + C_QK + 64u, mnmaj(kq + 8192u, kRegKQ, kk), mnmaj(pz, 8192, kk),
+                        idesc_bf16_f32(128, 64, 1, 1), 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_QK + 64u, kmaj(gg, kTile, kk), kmaj(ur, kTile, kk),
+                        idesc_bf16_f32(128, 64, 0, 0), 1);
+    } else if (phase == 4) {
+        // [X^T; 0] [M1 | dTm]: A MN-major (blocks X, zeros), B MN-major (blocks M1, dTm)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + C_PT, mnmaj(xi, 8192, kk), mnmaj(ur + 8192u, kTile, kk),
+                        idesc_bf16_f32(128, 128, 1, 1), kk > 0);
+    } else {
+        // [dQ^T | dK^T] += K^T [dP; Z]^T: A = K^T (MN-major), B = [dP; Z] (K-major)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + C_QK, mnmaj(kq, kRegKQ, kk), kmaj(pz, 0, kk),
+                        idesc_bf16_f32(128, 128, 1, 0), 1);
+    }
+}
+}  // namespace bgrad
+
+__global__ void __launch_bounds__(128, 1)
+chunk_bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_do,
+                          const __grid_constant__ CUtensorMap tm_s,
+                          const __grid_constant__ CUtensorMap tm_g,
+                          const __grid_constant__ CUtensorMap tm_g64,
+                          const __grid_constant__ CUtensorMap tm_x,
+                          const __grid_constant__ CUtensorMap tm_tm,
+                          const __nv_bfloat16* __restrict__ beta, __nv_bfloat16* __restrict__ d_q,
+                          __nv_bfloat16* __restrict__ d_k, __nv_bfloat16* __restrict__ d_beta,
+                          int T, int nchunks) {
+    using namespace bgrad;
+    constexpr int kBar = 1;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* const gbase = smem_raw + (base - raw_addr);
+    int* const misc = reinterpret_cast<int*>(gbase + OFF_MISC);
+    const Ctl ctl{base + OFF_BAR, reinterpret_cast<volatile int*>(misc)};
+    uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
+    float* const betas = reinterpret_cast<float*>(gbase + OFF_BETA);
+    float* const dAs = reinterpret_cast<float*>(gbase + OFF_S);  // over S once its MMAs are done
+    const int t = threadIdx.x;
+    const int item = blockIdx.x, bh = item / nchunks, c = item % nchunks;
+    const int t0 = c * kC, n = min(kC, T - t0);
+    const size_t row0 = (size_t)bh * T + t0;
+    const uint32_t lane = (uint32_t)(32 * (t >> 5)) << 16;
+
+    if (t == 0) {
+        misc[0] = 0;
+        for (int b = 0; b < kBars; ++b) mbar_init(ctl.bar(b), 1);
+        fence_mbar_init();
+        for (const CUtensorMap* m : {&tm_q, &tm_k, &tm_v, &tm_do, &tm_s, &tm_g, &tm_g64, &tm_x, &tm_tm})
+            prefetch_tensormap(m);
+    }
+    if (t < 32) {
+        tmem_alloc(smem_addr(tmem_holder), 512);
+        tmem_relinquish();
+    }
+    {   // zeros for the lower block of [X^T; 0]
+        uint4* const zb = reinterpret_cast<uint4*>(gbase + OFF_ZB);
+        for (int i = t; i < 512; i += 128) zb[i] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
+    if (t < kC) betas[t] = t < n ? __bfloat162float(beta[row0 + t]) : 0.f;
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t kq = base + OFF_KQ, dv = base + OFF_DV, pz = base + OFF_PZ, ur = base + OFF_UR;
+    const uint32_t tp = base + OFF_TP;
+
+    bool ok = true;
+    if (t == 0) {  // every operand tile of the chunk, on one barrier
+        const uint32_t bar = ctl.bar(B_LOAD);
+        mbar_arrive_expect_tx(bar, kStageKQ + 2 * kTile + 8 * kTile + 8192 + 8192);
+        const int z = bh, y = t0, hi = 2 * item, lo = hi + 1;
+        tma_load_3d(kq, &tm_k, bar, 0, y, z);
+        tma_load_3d(kq + kRegKQ, &tm_k, bar, 64, y, z);
+        tma_load_3d(kq + 8192, &tm_q, bar, 0, y, z);
+        tma_load_3d(kq + kRegKQ + 8192, &tm_q, bar, 64, y, z);
+        tma_load_3d(dv + 8192, &tm_do, bar, 0, y, z);
+        tma_load_3d(dv + kRegDV + 8192, &tm_do, bar, 64, y, z);
+        tma_load_3d(dv + 16384, &tm_v, bar, 0, y, z);
+        tma_load_3d(dv + kRegDV + 16384, &tm_v, bar, 64, y, z);
+        tma_load_3d(base + OFF_S, &tm_s, bar, 0, 0, hi);
+        tma_load_3d(base + OFF_S + kTile, &tm_s, bar, 64, 0, hi);
+        tma_load_3d(ur, &tm_s, bar, 0, 0, lo);
+        tma_load_3d(ur + kTile, &tm_s, bar, 64, 0, lo);
+        tma_load_3d(base + OFF_G, &tm_g, bar, 0, 0, hi);
+        tma_load_3d(base + OFF_G + kTile, &tm_g, bar, 64, 0, hi);
+        tma_load_3d(dv, &tm_g64, bar, 0, 0, lo);
+        tma_load_3d(dv + kRegDV, &tm_g64, bar, 64, 0, lo);
+        tma_load_3d(tp, &tm_g64, bar, 0, 64, lo);
+        tma_load_3d(tp + kTile, &tm_g64, bar, 64, 64, lo);
+        tma_load_3d(tp + 8192, &tm_tm, bar, 0, c * 128 + 64, bh);
+        tma_load_3d(base + OFF_XI, &tm_x, bar, 0, 0, item);
+        ok = ctl.wait(B_LOAD, 0);
+    }
+    int phase = 0;
+    // Issues MMA phase `phase` (thread 0) and waits for it; false if a wait gave up.
+    auto run = [&]() -> bool {
+        bool good = true;
+        if (t == 0) {
+            tc_fence_after_sync();
+            issue_phase(phase, tmem, base);
+            mma_commit(ctl.bar(B_MMA));
+            good = ctl.wait(B_MMA, (uint32_t)phase);
+        }
+        ++phase;
+        const bool bad = wg_sync_or(kBar, !good);
+        tc_fence_after_sync();
+        return !bad;
+    };
+    if (wg_sync_or(kBar, !ok)) goto done;
+    // ---- R^T (negated S^T K^T), K K^T and Q K^T
+    if (!run()) goto done;
+    {
+        float x[64];
+        if (t >= 64) {  // P = tril(Q K^T): row s = t - 64, as [s][t] bf16
+            tmem_ld64f(tmem + lane + C_G1, x);
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+                if (e > t - 64) x[e] = 0.f;
+            store_row64_bf16(pz, t, x);
+        }
+        float v[64];
+        tmem_ld64f(tmem + lane + C_R, x);
+        load_col64(dv, kRegDV, 128, t, v);  // V column t
+#pragma unroll
+        for (int e = 0; e < 64; ++e) x[e] += v[e];  // R^T row t (dv lane t)
+        pack64_tmem(tmem + lane + C_B, x);
+        store_col64(ur, kTile, 64, t, x, 1.f);  // R [t][dv]
+    }
+    tmem_wait_st();
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    wg_sync(kBar);
+    // ---- U'^T and dU'^T
+    if (!run()) goto done;
+    {
+        float x[64], v[64];
+        tmem_ld64f(tmem + lane + C_U, x);
+        store_col64(ur, kTile, 0, t, x, 1.f);  // U' [t][dv]
+        tmem_ld64f(tmem + lane + C_R, x);      // R^T row t again, as in the last step
+        load_col64(dv, kRegDV, 128, t, v);
+#pragma unroll
+        for (int e = 0; e < 64; ++e) x[e] = bf16_rest(x[e] + v[e]);
+        store_col64(tp, kTile, 0, t, x, 1.f);  // R lo [t][dv]
+        tmem_ld64f(tmem + lane + C_E, x);
+        pack64_tmem(tmem + lane + C_B, x);     // dU'^T as the next left operand
+        store_col64(dv, kRegDV, 0, t, x, 1.f);  // dU' hi [t][dv]
+#pragma unroll
+        for (int e = 0; e < 64; ++e) x[e] = bf16_rest(x[e]);
+        store_col64(dv, kRegDV, 128, t, x, 1.f);  // dU' lo over V
+    }
+    tmem_wait_st();
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    wg_sync(kBar);
+    // ---- dV^T and [dU'; dO] [U'; R]^T
+    if (!run()) goto done;
+    {
+        float x[64];
+        tmem_ld64f(tmem + lane + C_R, x);
+        store_col64(dv, kRegDV, 128, t, x, -1.f);  // -dV [t][dv] over V
+        tmem_ld64f(tmem + lane + C_PT + 64u, x);   // row t: dTm (t < 64), dO R^T (t >= 64)
+        pack64_tmem(tmem + lane + C_B, x);          // [dTm; -] as the left operand of M1
+        if (t < 64) store_row64_bf16(ur + kTile + 8192u, t, x);  // the dTm block of [M1 | dTm]
+        if (t >= 64) {  // dP = tril(dO U'^T): row t - 64, as [t][s] bf16
+            tmem_ld64f(tmem + lane + C_PT, x);
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+                if (e > t - 64) x[e] = 0.f;
+            store_row64_bf16(pz, t - 64, x);
+        }
+    }
+    tmem_wait_st();
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    wg_sync(kBar);
+    // ---- M1 = dTm Tm^T, and [dQ^T | dK^T] from S, Q, G
+    if (!run()) goto done;
+    if (t < 64) {  // M1 row t, the M1 block of [M1 | dTm]
+        float x[64];
+        tmem_ld64f(tmem + lane + C_R, x);
+        store_row64_bf16(ur + 8192u, t, x);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    wg_sync(kBar);
+    // ---- [X^T; 0] [M1 | dTm]: dA and diag(X^T dTm); then Z and dbeta
+    if (!run()) goto done;
+    {
+        float db = 0.f;
+        if (t < 64) {  // row a = t
+            float x[64];
+            tmem_ld64f(tmem + lane + C_PT + 64u, x);
+#pragma unroll
+            for (int e = 0; e < 64; ++e) db = e == t ? x[e] : db;  // sum_i X_ia dTm_ia
+            tmem_ld64f(tmem + lane + C_PT, x);
+            float kk[64];
+            tmem_ld64f(tmem + lane + C_G1, kk);  // (K K^T) row a
+#pragma unroll
+            for (int e = 0; e < 64; ++e) {
+                const float a = e < t ? -x[e] : 0.f;  // dA = strict_tril(-X^T M1)
+                dAs[t * kDAPitch + e] = a;
+                db = fmaf(a, kk[e], db);
+            }
+        }
+        wg_sync(kBar);
+        if (t < 64) {  // Z row a = beta_a dA[a][:] + beta_b dA[:][a]
+            float z[64];
+            const float ba = betas[t];
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+                z[e] = ba * dAs[t * kDAPitch + e] + betas[e] * dAs[e * kDAPitch + t];
+            store_row64_bf16(pz, 64 + t, z);
+            if (t < n) d_beta[row0 + t] = __float2bfloat16_rn(db);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    wg_sync(kBar);
+    // ---- [dQ^T | dK^T] += K^T [dP; Z]^T, then out
+    if (!run()) goto done;
+    {
+        float x[64];
+        tmem_ld64f(tmem + lane + C_QK, x);  // dQ^T row t (dk lane t)
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+            if (e < n) d_q[(row0 + e) * kD + t] = __float2bfloat16_rn(x[e]);
+        tmem_ld64f(tmem + lane + C_QK + 64u, x);
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+            if (e < n) d_k[(row0 + e) * kD + t] = __float2bfloat16_rn(x[e]);
+    }
+done:
+    if (t == 0) drain_mmas(ctl, B_END);
+    tc_fence_before_sync();
+    __syncthreads();
+    if (t < 32) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -2402,15 +2856,43 @@ bool make_map(CUtensorMap* map, const void* ptr, int BH, int T) {
 }
 
 // 3-D map over the workspace [BH][nchunks * 128][64] bf16, one [PT; Tm] tile per box.
-bool make_ws_map(CUtensorMap* map, void* ptr, int BH, int nchunks) {
+bool make_ws_map(CUtensorMap* map, void* ptr, int BH, int nchunks, int box_rows = 128) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {64, (cuuint64_t)nchunks * 128, (cuuint64_t)BH};
     cuuint64_t strides[2] = {128, (cuuint64_t)nchunks * kTile};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over [128][128] bf16 matrices ([tiles][row][col]), in 64-column
+// boxes of box_rows rows: the recorded states and state gradients, a hi and a
+// lo tile per chunk.
+bool make_state_map(CUtensorMap* map, const void* ptr, int tiles, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kD, (cuuint64_t)tiles};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kD * kD * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over per-chunk [64][64] bf16 matrices (the recorded (I + A)^{-1}).
+bool make_x_map(CUtensorMap* map, const void* ptr, int items) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, 64, (cuuint64_t)items};
+    cuuint64_t strides[2] = {128, 8192};
+    cuuint32_t box[3] = {64, 64, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -2436,8 +2918,9 @@ size_t chunk_tc_side_bytes_per_chunk() { return kSideFloats * sizeof(float); }
 
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const void* beta,
                             const float* S0, void* o, float* S_T, int BH, int T, int dk, int dv,
-                            int dt, void* workspace, cudaStream_t stream, float* S_chunks,
-                            const QkNorm& norm) {
+                            int dt, void* workspace, cudaStream_t stream, void* S_rec,
+                            const QkNorm& norm, void* X_rec) {
+    __nv_bfloat16* const S_chunks = static_cast<__nv_bfloat16*>(S_rec);
     if (!chunk_tc_supports(dk, dv, dt)) return cudaErrorNotSupported;
     if (BH <= 0 || T <= 0) return cudaSuccess;
     // Outputs may be skipped (o == nullptr) only on the two-pass path.
@@ -2469,7 +2952,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
         const SeqTable<1> batched{};
         const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
         prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
-            mq, mk, mws, b, T, nchunks, (int)items, batched, nullptr, side, mws, norm);
+            mq, mk, mws, b, T, nchunks, (int)items, batched, nullptr, side, mws, norm,
+            static_cast<__nv_bfloat16*>(X_rec));
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
         scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mws, S0,
                                                            static_cast<__nv_bfloat16*>(o), S_T,
@@ -2512,7 +2996,7 @@ cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v, 
         const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
         prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
             mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, 0, (int)items, seqs, nullptr,
-            side, mws, norm);
+            side, mws, norm, nullptr);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     scan_kernel<<<(unsigned)ctas, 512, scan::kSmemBytes, stream>>>(
@@ -2556,7 +3040,7 @@ cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, c
     const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
     prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
         mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, nchunks, (int)items, batched, g,
-        side, mws2, norm);
+        side, mws2, norm, nullptr);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mws2, S0,
                                                        static_cast<__nv_bfloat16*>(o), S_T, nullptr,
@@ -2614,7 +3098,7 @@ cudaError_t launch_chunk_tc_kda(const void* q, const void* k, const void* v, con
     const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSmSepB);
     prep_kernel<<<grid, kPrepThreads, kPrepSmemBytesSepB, stream>>>(
         mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, nchunks, (int)items, batched,
-        nullptr, nullptr, mkb, kNoNorm);
+        nullptr, nullptr, mkb, kNoNorm, nullptr);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = launch_kda_fix(q, k, beta, g, fix, workspace, BH, T, norm, stream)) != cudaSuccess)
         return err;
@@ -2626,7 +3110,7 @@ cudaError_t launch_chunk_tc_kda(const void* q, const void* k, const void* v, con
 
 cudaError_t launch_chunk_bwd_chain_tc(const void* q, const void* k, const void* d_o,
                                       const float* d_S_T, void* d_v, float* d_S0,
-                                      float* G_chunks, const void* tiles, int BH, int T,
+                                      void* G_chunks, const void* tiles, int BH, int T,
                                       cudaStream_t stream) {
     if (BH <= 0 || T <= 0) return cudaSuccess;
     const int nchunks = (T + kC - 1) / kC;
@@ -2640,7 +3124,37 @@ cudaError_t launch_chunk_bwd_chain_tc(const void* q, const void* k, const void* 
                                     bchain::kSmemBytes)) != cudaSuccess)
         return err;
     chunk_bwd_chain_tc_kernel<<<BH, 512, bchain::kSmemBytes, stream>>>(
-        mq, mk, mdo, mws, d_S_T, static_cast<__nv_bfloat16*>(d_v), d_S0, G_chunks, T);
+        mq, mk, mdo, mws, d_S_T, static_cast<__nv_bfloat16*>(d_v), d_S0,
+        static_cast<__nv_bfloat16*>(G_chunks), T);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_bwd_grads_tc(const void* q, const void* k, const void* v,
+                                      const void* beta, const void* d_o, const void* S_rec,
+                                      const void* G_rec, const void* X_rec, const void* tiles,
+                                      void* d_q, void* d_k, void* d_beta, int BH, int T,
+                                      cudaStream_t stream) {
+    if (BH <= 0 || T <= 0) return cudaSuccess;
+    const int nchunks = (T + kC - 1) / kC;
+    const long long items = (long long)BH * nchunks;
+    if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if (2 * items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    CUtensorMap mq, mk, mv, mdo, ms, mg, mg64, mx, mtm;
+    if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mv, v, BH, T) ||
+        !make_map(&mdo, d_o, BH, T) || !make_state_map(&ms, S_rec, 2 * (int)items, 128) ||
+        !make_state_map(&mg, G_rec, 2 * (int)items, 128) ||
+        !make_state_map(&mg64, G_rec, 2 * (int)items, 64) || !make_x_map(&mx, X_rec, (int)items) ||
+        !make_ws_map(&mtm, const_cast<void*>(tiles), BH, nchunks, 64))
+        return cudaErrorInvalidValue;
+    cudaError_t err;
+    if ((err = cudaFuncSetAttribute(chunk_bwd_grads_tc_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    bgrad::kSmemBytes)) != cudaSuccess)
+        return err;
+    chunk_bwd_grads_tc_kernel<<<(unsigned)items, 128, bgrad::kSmemBytes, stream>>>(
+        mq, mk, mv, mdo, ms, mg, mg64, mx, mtm, static_cast<const __nv_bfloat16*>(beta),
+        static_cast<__nv_bfloat16*>(d_q), static_cast<__nv_bfloat16*>(d_k),
+        static_cast<__nv_bfloat16*>(d_beta), T, nchunks);
     return cudaGetLastError();
 }
 

@@ -86,8 +86,10 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
 // workspace of chunk_tc_workspace_bytes(BH, T) bytes (16-byte aligned) it runs
 // in two passes: every chunk's [PT; Tm] in parallel, then the sequences;
 // with workspace == nullptr one fused kernel does both.  On the two-pass path
-// o may be nullptr (no outputs) and S_chunks, if given, receives the fp32
-// state at the start of every chunk ([BH][ceil(T/64)][dk][dv]).
+// o may be nullptr (no outputs) and S_rec, if given, receives the fp32
+// state at the start of every chunk as two bf16 tiles, hi = bf16(S) and
+// lo = bf16(S - hi) ([BH][ceil(T/64)][2][dk][dv]), and X_rec, if given, every
+// chunk's (I + A)^{-1} ([BH][ceil(T/64)][64][64] bf16), for the backward.
 bool chunk_tc_supports(int dk, int dv, int dt);
 size_t chunk_tc_workspace_bytes(int BH, int T);
 // With prepared inputs (a QkNorm) the two-pass forms also keep the row
@@ -96,8 +98,8 @@ size_t chunk_tc_side_bytes_per_chunk();
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v,
                             const void* beta, const float* S0, void* o,
                             float* S_T, int BH, int T, int dk, int dv, int dt,
-                            void* workspace, cudaStream_t stream, float* S_chunks = nullptr,
-                            const QkNorm& norm = kNoNorm);
+                            void* workspace, cudaStream_t stream, void* S_rec = nullptr,
+                            const QkNorm& norm = kNoNorm, void* X_rec = nullptr);
 
 // Varlen forms: q, k, v, beta, o are [H][T][.] (T the packed length), the
 // states [seqs.n][H][dk][dv].  The tensor-core form runs in two passes and
@@ -109,10 +111,20 @@ cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v,
 // The backward's chain on tcgen05 (bf16, dk = dv = 128): G = dL/dS from the
 // last chunk to the first, with the forward's [PT; Tm] tiles (`tiles`, the
 // workspace the state recompute used) read transposed.  Writes G at every
-// chunk end (G_chunks, [BH][chunk][dk][dv] fp32), d_v and d_S0 (if given).
+// chunk end (G_chunks, [BH][chunk][2][dk][dv] bf16: hi and lo tiles as for
+// S_rec), d_v and d_S0 (if given).
 cudaError_t launch_chunk_bwd_chain_tc(const void* q, const void* k, const void* d_o,
                                       const float* d_S_T, void* d_v, float* d_S0,
-                                      float* G_chunks, const void* tiles, int BH, int T,
+                                      void* G_chunks, const void* tiles, int BH, int T,
+                                      cudaStream_t stream);
+// The backward's per-chunk gradients on tcgen05 (bf16, dk = dv = 128): d_q,
+// d_k and d_beta of every chunk from its inputs, the state at its start
+// (S_rec), the state gradient at its end (G_rec), its (I + A)^{-1} (X_rec)
+// and its [PT; Tm] tile, all as the recompute and the chain recorded them.
+cudaError_t launch_chunk_bwd_grads_tc(const void* q, const void* k, const void* v,
+                                      const void* beta, const void* d_o, const void* S_rec,
+                                      const void* G_rec, const void* X_rec, const void* tiles,
+                                      void* d_q, void* d_k, void* d_beta, int BH, int T,
                                       cudaStream_t stream);
 // Gated DeltaNet on tensor cores (two passes; g the fp32 [BH][T] log keep
 // rate): the workspace holds the [PT; Tm] tiles and then kSideFloats fp32

@@ -2393,224 +2393,220 @@ chunk_bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
 // ------------------------------------------------- backward gradient kernel
 // The backward's per-chunk gradients on tcgen05 (bf16 operands, fp32
-// accumulation in TMEM), one CTA of one warpgroup per (batch, head, chunk).
+// accumulation in TMEM), one CTA of four warpgroups per (batch, head, chunk).
 // With the chunk's rows K, Q, V, dO, strengths beta, the state S at its start
-// and the state gradient G at its end (both [dk][dv], as the recompute and
-// the chain recorded them), X = (I + A)^{-1} and Tm = X diag(beta):
+// and the state gradient G at its end (both [dk][dv], each recorded as a bf16
+// hi and lo tile), X = (I + A)^{-1} and Tm = X diag(beta):
 //     R = V - K S,  U' = Tm R,  dU' = P^T dO + K G,  dV = Tm^T dU'
 //     dP = tril(dO U'^T),  dTm = dU' R^T
 //     dQ = dO S^T + dP K,   dK = dP^T Q + U' G^T - dV S^T + Z K
 //     dA = strict_tril(-X^T dTm Tm^T),  Z = diag(beta) dA + (diag(beta) dA)^T
-//     dbeta_j = sum_i X_ij dTm_ij + sum_l dA_jl (K K^T)_jl
-// (the algebra of chunk_bwd.cu, with dTm diag(beta) X^T = dTm Tm^T).  Every
-// product runs transposed, with a feature (dk or dv) on the 128 TMEM lanes
-// and the chunk's 64 tokens on the columns, so each MMA is M = 128:
-//     R^T = V^T - S^T K^T,       U'^T = R^T Tm^T,       dU'^T = dO^T P + G^T K^T
-//     dV^T = dU'^T Tm,           [dU'; dO] [U'; R]^T   (dTm and dP as two of its blocks)
-//     M1 = dTm Tm^T,             [X^T; 0] [M1 | dTm]   (dA and diag(X^T dTm))
-//     [dQ^T | dK^T] = S [dO; -dV]^T + K^T [dP; Z]^T, plus Q^T dP + G U'^T on dK^T.
-// Results that feed a later product as a [token][feature] operand are
-// written into shared memory one feature column per thread (thread = TMEM
-// lane), the 128-byte swizzled layout TMA writes; results used as a left
-// operand from TMEM are packed to bf16 pairs in place.  One thread issues
-// every MMA; each phase ends on an MMA commit, waited with the bounded waits
-// of the forward kernels.
+//     dbeta_a = (dTm^T X)_aa + sum_e dA_ae (K K^T)_ae
+// (the algebra of chunk_bwd.cu).  Every product has M = 128 on the TMEM
+// lanes: a feature (dk or dv) for the [feature][token] results, the chunk's
+// tokens (twice) for the token-by-token ones.  By phase:
+//   0: [K; Q] K^T (K K^T and Q K^T);  R^T = V^T I - S^T K^T  (S = hi + lo)
+//   1: U'^T = R^T Tm^T;               dU'^T = dO^T P + G^T K^T  (G = hi + lo)
+//   2: dV^T = dU'^T Tm;  [R; U'] dU'^T (dTm^T, plus the lo parts of R and dU',
+//      since d_beta is a dot product of dU' with R that can cancel heavily);
+//      [R; U'] dO^T (dP^T)
+//   3: M1 = dTm^T X (its diagonal: the first d_beta term);  dQ^T = S dO^T;
+//      dK^T = -S dV^T + Q^T dP + G U'^T
+//   4: dA^T = -Tm M1
+//   5: [dQ^T | dK^T] += K^T [dP | Z]
+// A thread owns one TMEM lane and 16 of the 64 token columns (warpgroup w:
+// columns 16w .. 16w + 15).  Each result a later product reads from shared
+// memory is stored as [lane][token] rows in the 128-byte swizzled layout and
+// read by the MMA as an MN-major operand (K-major where the product sums over
+// tokens), so the epilogues write 16-byte rows; a left operand taken from
+// TMEM is packed to bf16 pairs in place.  One thread issues every MMA; each
+// phase ends on an MMA commit, waited with the bounded waits of the forward
+// kernels.
 namespace bgrad {
-// Shared memory over the phases (the "lo" tiles carry what bf16 rounding
-// drops from S, G, R and dU', so that d_beta, a dot product of dU' with R
-// that cancels heavily, keeps fp32-like accuracy):
-//   DV rows 0-63: G lo (dk 0-63) -> dU' hi;  rows 64-127: dO;
-//   DV rows 128-191: V -> dU' lo -> -dV;  UR: S lo -> [U'; R hi];
-//   TP rows 0-63 and PZ rows 0-63: G lo (dk 64-127) -> R lo -> (PZ) dP.
-constexpr uint32_t kRegDV = 192 * 128;                // a dv half of [dU'; dO; V or -dV]
-constexpr uint32_t OFF_KQ = 0;                        // [K; Q]: 2 dk halves x 128 rows
-constexpr uint32_t OFF_DV = OFF_KQ + kStageKQ;        // 2 dv halves x 192 rows
-constexpr uint32_t OFF_S = OFF_DV + 2 * kRegDV;       // S: 2 dv halves x 128 dk rows (fp32 dA later)
-constexpr uint32_t OFF_G = OFF_S + 2 * kTile;         // G: likewise
-constexpr uint32_t OFF_TP = OFF_G + 2 * kTile;        // rows 64-127: Tm
-constexpr uint32_t OFF_PZ = OFF_TP + kTile;           // rows 0-63 dP [t][s]; 64-127 P [s][t], then Z
-constexpr uint32_t OFF_UR = OFF_PZ + kTile;           // 2 dv halves x [U'; R]; later the [M1 | dTm] blocks
-constexpr uint32_t OFF_XI = OFF_UR + 2 * kTile;       // X [t][a] bf16
-constexpr uint32_t OFF_ZB = OFF_XI + 8192;            // zeros: the lower block of [X^T; 0]
-constexpr uint32_t OFF_BAR = OFF_ZB + 8192;
-constexpr int kBars = 4;                              // loads, MMA commits, drain
-constexpr uint32_t OFF_BETA = OFF_BAR + 8 * kBars;    // 64 fp32
-constexpr uint32_t OFF_MISC = OFF_BETA + 256;         // abort flag, TMEM address
+constexpr int kThreads = 512;
+// Shared memory; a region is reused once the phases that read it are done.
+constexpr uint32_t OFF_KQ = 0;                    // [K; Q]: 2 dk halves x 128 token rows
+constexpr uint32_t OFF_DO = OFF_KQ + kStageKQ;    // dO [t][dv]: 2 dv halves x 64 rows
+constexpr uint32_t OFF_V = OFF_DO + kTile;        // V [t][dv] -> R^T lo -> -dV^T -> M1
+constexpr uint32_t OFF_S = OFF_V + kTile;         // S hi: 2 dv halves x 128 dk rows -> fp32 dA
+constexpr uint32_t OFF_G = OFF_S + 2 * kTile;     // G hi
+constexpr uint32_t OFF_UR = OFF_G + 2 * kTile;    // S lo -> [R^T | U'^T], [dv][t] each
+constexpr uint32_t OFF_DUH = OFF_UR + 2 * kTile;  // G lo (dv 0-63) -> dU'^T hi
+constexpr uint32_t OFF_DUL = OFF_DUH + kTile;     // G lo (dv 64-127) -> dU'^T lo
+constexpr uint32_t OFF_PZ = OFF_DUL + kTile;      // rows 0-63: P -> dP^T; rows 64-127: I -> Z
+constexpr uint32_t OFF_TM = OFF_PZ + kTile;       // Tm [i][a]
+constexpr uint32_t OFF_X = OFF_TM + 8192;         // X [i][a]
+constexpr uint32_t OFF_BAR = OFF_X + 8192;
+constexpr int kLoadGroups = 5;                    // the next chunk's loads, by the phase that frees them
+constexpr int kBars = 2 + kLoadGroups;            // MMA commits, drain, load groups
+constexpr uint32_t OFF_BETA = OFF_BAR + 64;       // 64 fp32
+constexpr uint32_t OFF_DB = OFF_BETA + 256;       // d_beta parts: [5][64] fp32
+constexpr uint32_t OFF_MISC = OFF_DB + 5 * 256;   // abort flag, TMEM address
 constexpr uint32_t kSmemBytes = OFF_MISC + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "gradient kernel shared memory");
-static_assert(OFF_DV % 1024 == 0 && OFF_S % 1024 == 0 && OFF_UR % 1024 == 0 &&
-              OFF_XI % 1024 == 0 && OFF_ZB % 1024 == 0 && kRegDV % 1024 == 0, "tile alignment");
+static_assert(OFF_DO % 1024 == 0 && OFF_V % 1024 == 0 && OFF_S % 1024 == 0 &&
+              OFF_UR % 1024 == 0 && OFF_PZ % 1024 == 0 && OFF_TM % 1024 == 0 &&
+              OFF_X % 1024 == 0, "tile alignment");
+static_assert(8 * kBars <= 64, "barrier space");
 constexpr int kDAPitch = 65;  // fp32 dA rows over the spent S
 // TMEM columns (512 allocated):
-constexpr uint32_t C_G1 = 0;    // [K; Q] K^T: K K^T (rows 0-63), Q K^T (rows 64-127)
+constexpr uint32_t C_G1 = 0;    // [K; Q] K^T: K K^T (lanes 0-63), Q K^T (lanes 64-127)
 constexpr uint32_t C_R = 64;    // R^T, then dV^T, then M1
-constexpr uint32_t C_B = 128;   // a bf16 left operand: R^T, then dU'^T, then the dTm block
+constexpr uint32_t C_B = 128;   // a bf16 left operand: R^T, then dU'^T, then dTm^T
 constexpr uint32_t C_U = 160;   // U'^T
+constexpr uint32_t C_DK = 160;  // dK^T, over U'^T once it is read
 constexpr uint32_t C_E = 224;   // dU'^T
-constexpr uint32_t C_QK = 160;  // [dQ^T | dK^T], over U'^T and dU'^T once they are read
-constexpr uint32_t C_PT = 288;  // [dU'; dO] [U'; R]^T, then [X^T; 0] [M1 | dTm]
-enum : int { B_LOAD = 0, B_MMA = 1, B_END = 2 };
+constexpr uint32_t C_PT = 288;  // [dTm^T | dP^T] (lanes 0-63 | 64-127), then dA^T
+constexpr uint32_t C_DQ = 416;  // dQ^T
+enum : int { B_MMA = 0, B_END = 1, B_LD = 2 };
 
-// Thread j (a feature lane) writes its 64 values, one per token row t, into
-// column j of rows row0 .. row0 + 63 of a [row][feature] tile whose two
-// 64-feature halves are regions `stride` bytes apart, times `sign`, as bf16.
-__device__ __forceinline__ void store_col64(uint32_t region0, uint32_t stride, int row0, int j,
-                                            const float (&x)[64], float sign) {
-    const uint32_t region = region0 + (uint32_t)(j >> 6) * stride;
-    const int cj = j & 63;
+__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&x)[16]) {
+    uint32_t r[16];
+    tmem_ld16(taddr, r);
+    tmem_wait_ld();
 #pragma unroll
-    for (int t = 0; t < 64; ++t) {
-        const uint32_t a = region + sw128(row0 + t, cj >> 3) + (uint32_t)(cj & 7) * 2u;
-        const __nv_bfloat16 h = __float2bfloat16_rn(sign * x[t]);
-        asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(*reinterpret_cast<const uint16_t*>(&h))
-                     : "memory");
-    }
+    for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(r[i]);
 }
-// The matching read: column j of rows row0 .. row0 + 63 into x (as fp32).
-__device__ __forceinline__ void load_col64(uint32_t region0, uint32_t stride, int row0, int j,
-                                           float (&x)[64]) {
-    const uint32_t region = region0 + (uint32_t)(j >> 6) * stride;
-    const int cj = j & 63;
+// 16 fp32 values -> 8 bf16-pair TMEM columns of the calling thread's lane.
+__device__ __forceinline__ void pack16_tmem(uint32_t dst, const float (&x)[16]) {
+    uint32_t p[8];
 #pragma unroll
-    for (int t = 0; t < 64; ++t) {
-        const uint32_t a = region + sw128(row0 + t, cj >> 3) + (uint32_t)(cj & 7) * 2u;
-        uint16_t u;
-        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(u) : "r"(a) : "memory");
-        x[t] = __bfloat162float(__ushort_as_bfloat16(u));
-    }
+    for (int e = 0; e < 8; ++e) p[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+    tmem_st8(dst, p);
+}
+// 16 values as bf16 into columns 16g .. 16g + 15 of row r of a swizzled
+// [row][64] region.
+__device__ __forceinline__ void store_row16(uint32_t region, int r, int g, const float (&x)[16]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        st_shared_v4(region + sw128(r, 2 * g + h), pack_bf16(x[8 * h + 0], x[8 * h + 1]),
+                     pack_bf16(x[8 * h + 2], x[8 * h + 3]), pack_bf16(x[8 * h + 4], x[8 * h + 5]),
+                     pack_bf16(x[8 * h + 6], x[8 * h + 7]));
 }
 // What bf16 rounding drops from x (x - bf16(x), exact in fp32).
 __device__ __forceinline__ float bf16_rest(float x) {
     return x - __bfloat162float(__float2bfloat16_rn(x));
 }
-// 64 fp32 values -> 32 bf16-pair TMEM columns of the calling thread's lane.
-__device__ __forceinline__ void pack64_tmem(uint32_t dst, const float (&x)[64]) {
-    uint32_t p[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) p[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
-    tmem_st32(dst, p);
-}
 
-// One thread's MMA phases (tcgen05, issued by thread 0).
-__device__ __forceinline__ void issue_phase(int phase, uint32_t tmem, uint32_t base) {
-    const uint32_t kq = base + OFF_KQ, dv = base + OFF_DV, ss = base + OFF_S, gg = base + OFF_G;
-    const uint32_t tp = base + OFF_TP, pz = base + OFF_PZ, ur = base + OFF_UR, xi = base + OFF_XI;
-    // K-major operand step kk over a 128-element K split in two regions `stride` apart
-    auto kmaj = [](uint32_t a, uint32_t stride, int kk) {
-        return sw128_desc(a + (uint32_t)(kk >> 2) * stride + (uint32_t)(kk & 3) * 32u, 16, 1024);
+// The MMA groups (tcgen05, issued by thread 0).  d0 is the descriptor of the
+// 1024-aligned shared base: every operand lies at a fixed offset from it, so
+// a descriptor is d0 plus a constant (start address in 16-byte units in the
+// low field, the MN-major block stride in the LBO field).  Groups 0, 2, 3, 5,
+// 6, 7 are the phases, each followed by its commit; group 1 (G's part of
+// dU'^T and dQ^T = S dO^T) and group 4 (G U'^T) need nothing the epilogues
+// write and run while the epilogue before them does.
+__device__ __forceinline__ void issue_group(int grp, uint32_t tmem, uint64_t d0) {
+    // K-major operand at `off`, step kk over a K split in 64-element regions `stride` apart
+    // (LBO field 1, unused by the swizzled K-major layout)
+    auto kmaj = [d0](uint32_t off, uint32_t stride, int kk) -> uint64_t {
+        return d0 + ((off + (uint32_t)(kk >> 2) * stride + (uint32_t)(kk & 3) * 32u) >> 4) +
+               (1ull << 16);
     };
-    // MN-major operand step kk (16 rows) with 64-element blocks `lbo` apart
-    auto mnmaj = [](uint32_t a, uint32_t lbo, int kk) {
-        return sw128_desc(a + (uint32_t)kk * 2048u, lbo, 1024);
+    // MN-major operand at `off`, step kk (16 K rows), 64-element M/N blocks `lbo` apart
+    auto mnmaj = [d0](uint32_t off, uint32_t lbo, int kk) -> uint64_t {
+        return d0 + ((off + (uint32_t)kk * 2048u) >> 4) + ((uint64_t)(lbo >> 4) << 16);
     };
     constexpr uint32_t kNegB = 1u << 14;
-    if (phase == 0) {
-        // G1 = [K; Q] K^T
+    constexpr uint32_t KK = idesc_bf16_f32(128, 64, 0, 0), KM = idesc_bf16_f32(128, 64, 0, 1),
+                       MK = idesc_bf16_f32(128, 64, 1, 0), MM = idesc_bf16_f32(128, 64, 1, 1);
+    switch (grp) {
+    case 0:  // [K; Q] K^T;  R^T = V^T I (I over PZ rows 64-127) - S hi^T K^T - S lo^T K^T
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + C_G1, kmaj(kq, kRegKQ, kk), kmaj(kq, kRegKQ, kk),
-                        idesc_bf16_f32(128, 64, 0, 0), kk > 0);
-        // -(S^T K^T): A = S^T (MN-major, dv blocks), B = K^T (K-major), B negated;
-        // S = hi + lo (lo over UR)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + C_R, mnmaj(ss, kTile, kk), kmaj(kq, kRegKQ, kk),
-                        idesc_bf16_f32(128, 64, 1, 0) | kNegB, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + C_R, mnmaj(ur, kTile, kk), kmaj(kq, kRegKQ, kk),
-                        idesc_bf16_f32(128, 64, 1, 0) | kNegB, 1);
-    } else if (phase == 1) {
-        // U'^T = R^T Tm^T: A = R^T (TMEM), B = Tm^T (K-major Tm rows)
+            mma_bf16_ss(tmem + C_G1, kmaj(OFF_KQ, kRegKQ, kk), kmaj(OFF_KQ, kRegKQ, kk), KK, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ts(tmem + C_U, tmem + C_B + 8u * kk, kmaj(tp + 8192u, 0, kk),
-                        idesc_bf16_f32(128, 64, 0, 0), kk > 0);
-        // dU'^T = dO^T P + G^T K^T
+            mma_bf16_ss(tmem + C_R, mnmaj(OFF_V, 8192, kk), kmaj(OFF_PZ + 8192, 0, kk), MK, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_R, mnmaj(OFF_S, kTile, kk), kmaj(OFF_KQ, kRegKQ, kk), MK | kNegB, 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_R, mnmaj(OFF_UR, kTile, kk), kmaj(OFF_KQ, kRegKQ, kk), MK | kNegB, 1);
+        break;
+    case 1:  // dU'^T = G hi^T K^T + G lo^T K^T (G lo over DUH / DUL) ...;  dQ^T = S dO^T
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_E, mnmaj(OFF_G, kTile, kk), kmaj(OFF_KQ, kRegKQ, kk), MK, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_E, mnmaj(OFF_DUH, kTile, kk), kmaj(OFF_KQ, kRegKQ, kk), MK, 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_DQ, kmaj(OFF_S, kTile, kk), kmaj(OFF_DO, 8192, kk), KK, kk > 0);
+        break;
+    case 2:  // U'^T = R^T Tm^T (A = R^T from TMEM);  dU'^T += dO^T P
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(tmem + C_E, mnmaj(dv + 8192u, kRegDV, kk), mnmaj(pz + 8192u, 8192, kk),
-                        idesc_bf16_f32(128, 64, 1, 1), kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + C_E, mnmaj(gg, kTile, kk), kmaj(kq, kRegKQ, kk),
-                        idesc_bf16_f32(128, 64, 1, 0), 1);
-        // ... + G lo^T K^T: dk rows 0-63 over DV rows 0-63, 64-127 over TP / PZ rows 0-63
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + C_E, kk < 4 ? mnmaj(dv, kRegDV, kk) : mnmaj(tp, kTile, kk - 4),
-                        kmaj(kq, kRegKQ, kk), idesc_bf16_f32(128, 64, 1, 0), 1);
-    } else if (phase == 2) {
-        // dV^T = dU'^T Tm: A = dU'^T (TMEM), B = Tm (MN-major Tm rows)
+            mma_bf16_ts(tmem + C_U, tmem + C_B + 8u * kk, kmaj(OFF_TM, 0, kk), KK, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ts(tmem + C_R, tmem + C_B + 8u * kk, mnmaj(tp + 8192u, 8192, kk),
-                        idesc_bf16_f32(128, 64, 0, 1), kk > 0);
-        // [dU'; dO] [U'; R]^T (N = 128), then the dTm block's lo terms:
-        // + [dU' hi; dO] R lo^T (R lo over TP / PZ rows 0-63) + [dU' lo; -] R hi^T
-        // (dU' lo in DV rows 128-191; rows 64-127 of that A read the next 8 KB,
-        // which only reach the unused rows of the block)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + C_PT, kmaj(dv, kRegDV, kk), kmaj(ur, kTile, kk),
-                        idesc_bf16_f32(128, 128, 0, 0), kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + C_PT + 64u, kmaj(dv, kRegDV, kk), kmaj(tp, kTile, kk),
-                        idesc_bf16_f32(128, 64, 0, 0), 1);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + C_PT + 64u, kmaj(dv + 16384u, kRegDV, kk),
-                        kmaj(ur + 8192u, kTile, kk), idesc_bf16_f32(128, 64, 0, 0), 1);
-    } else if (phase == 3) {
-        // M1 = dTm Tm^T: A = [dTm; -] (TMEM), B = Tm^T (K-major)
+            mma_bf16_ss(tmem + C_E, mnmaj(OFF_DO, 8192, kk), mnmaj(OFF_PZ, 8192, kk), MM, 1);
+        break;
+    case 3:  // dV^T = dU'^T Tm;  dTm^T = [R; U'] dU'^T + [R lo; -] dU'^T + [R; U'] dU' lo^T
+             // (lanes 0-63; the second A reads S hi as its unused upper block);
+             // dP^T = [R; U'] dO^T (lanes 64-127)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ts(tmem + C_R, tmem + C_B + 8u * kk, kmaj(tp + 8192u, 0, kk),
-                        idesc_bf16_f32(128, 64, 0, 0), kk > 0);
-        // [dQ^T | dK^T] = S [dO; -dV]^T (N = 128)
+            mma_bf16_ts(tmem + C_R, tmem + C_B + 8u * kk, mnmaj(OFF_TM, 8192, kk), KM, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + C_QK, kmaj(ss, kTile, kk), kmaj(dv + 8192u, kRegDV, kk),
-                        idesc_bf16_f32(128, 128, 0, 0), kk > 0);
-        // dK^T += Q^T dP (A = Q^T MN-major, B = dP MN-major) + G U'^T (K-major both)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(tmem + C_QK + 64u, mnmaj(kq + 8192u, kRegKQ, kk), mnmaj(pz, 8192, kk),
-                        idesc_bf16_f32(128, 64, 1, 1), 1);
+            mma_bf16_ss(tmem + C_PT, mnmaj(OFF_UR, kTile, kk), mnmaj(OFF_DUH, 8192, kk), MM, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + C_QK + 64u, kmaj(gg, kTile, kk), kmaj(ur, kTile, kk),
-                        idesc_bf16_f32(128, 64, 0, 0), 1);
-    } else if (phase == 4) {
-        // [X^T; 0] [M1 | dTm]: A MN-major (blocks X, zeros), B MN-major (blocks M1, dTm)
+            mma_bf16_ss(tmem + C_PT, mnmaj(OFF_V, kTile, kk), mnmaj(OFF_DUH, 8192, kk), MM, 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_PT, mnmaj(OFF_UR, kTile, kk), mnmaj(OFF_DUL, 8192, kk), MM, 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_PT + 64u, mnmaj(OFF_UR, kTile, kk), kmaj(OFF_DO, 8192, kk), MK, kk > 0);
+        break;
+    case 4:  // dK^T = G U'^T (over U'^T's columns, read by now)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_DK, kmaj(OFF_G, kTile, kk), mnmaj(OFF_UR + kTile, 8192, kk), KM, kk > 0);
+        break;
+    case 5:  // M1 = dTm^T X (A = dTm^T from TMEM);  dK^T += S (-dV^T) + Q^T dP
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(tmem + C_PT, mnmaj(xi, 8192, kk), mnmaj(ur + 8192u, kTile, kk),
-                        idesc_bf16_f32(128, 128, 1, 1), kk > 0);
-    } else {
-        // [dQ^T | dK^T] += K^T [dP; Z]^T: A = K^T (MN-major), B = [dP; Z] (K-major)
+            mma_bf16_ts(tmem + C_R, tmem + C_B + 8u * kk, mnmaj(OFF_X, 8192, kk), KM, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C_DK, kmaj(OFF_S, kTile, kk), mnmaj(OFF_V, 8192, kk), KM, 1);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(tmem + C_QK, mnmaj(kq, kRegKQ, kk), kmaj(pz, 0, kk),
-                        idesc_bf16_f32(128, 128, 1, 0), 1);
+            mma_bf16_ss(tmem + C_DK, mnmaj(OFF_KQ + 8192, kRegKQ, kk), kmaj(OFF_PZ, 0, kk), MK, 1);
+        break;
+    case 6:  // dA^T = -Tm M1 (rows 64-127 of that A read X: unused lanes)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + C_PT, kmaj(OFF_TM, 0, kk), mnmaj(OFF_V, 8192, kk), KM | kNegB, kk > 0);
+        break;
+    default:  // dQ^T += K^T dP^T;  dK^T += K^T Z
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + C_DQ, mnmaj(OFF_KQ, kRegKQ, kk), mnmaj(OFF_PZ, 8192, kk), MM, 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + C_DK, mnmaj(OFF_KQ, kRegKQ, kk), mnmaj(OFF_PZ + 8192, 8192, kk), MM, 1);
+        break;
     }
 }
 }  // namespace bgrad
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(bgrad::kThreads, 1)
 chunk_bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_do,
                           const __grid_constant__ CUtensorMap tm_s,
                           const __grid_constant__ CUtensorMap tm_g,
-                          const __grid_constant__ CUtensorMap tm_g64,
                           const __grid_constant__ CUtensorMap tm_x,
                           const __grid_constant__ CUtensorMap tm_tm,
                           const __nv_bfloat16* __restrict__ beta, __nv_bfloat16* __restrict__ d_q,
                           __nv_bfloat16* __restrict__ d_k, __nv_bfloat16* __restrict__ d_beta,
-                          int T, int nchunks) {
+                          int T, int nchunks, int items) {
     using namespace bgrad;
     constexpr int kBar = 1;
     extern __shared__ uint8_t smem_raw[];
@@ -2621,204 +2617,241 @@ chunk_bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const Ctl ctl{base + OFF_BAR, reinterpret_cast<volatile int*>(misc)};
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
     float* const betas = reinterpret_cast<float*>(gbase + OFF_BETA);
+    float* const db = reinterpret_cast<float*>(gbase + OFF_DB);
     float* const dAs = reinterpret_cast<float*>(gbase + OFF_S);  // over S once its MMAs are done
     const int t = threadIdx.x;
-    const int item = blockIdx.x, bh = item / nchunks, c = item % nchunks;
-    const int t0 = c * kC, n = min(kC, T - t0);
-    const size_t row0 = (size_t)bh * T + t0;
-    const uint32_t lane = (uint32_t)(32 * (t >> 5)) << 16;
+    // Thread t: TMEM lane L (warp t / 32 reaches lanes 32 (t / 32 % 4) ..), token columns col0 ..
+    const int q4 = (t >> 5) & 3, g = t >> 7;
+    const int L = 32 * q4 + (t & 31), col0 = 16 * g;
+    const uint32_t lane = (uint32_t)(32 * q4) << 16;
+    const uint32_t kq = base + OFF_KQ, dO = base + OFF_DO, v = base + OFF_V, ss = base + OFF_S;
+    const uint32_t gg = base + OFF_G, ur = base + OFF_UR, duh = base + OFF_DUH;
+    const uint32_t dul = base + OFF_DUL, pz = base + OFF_PZ, tm = base + OFF_TM;
+
+    // Thread 0: the TMA loads of chunk `it` (the CTA's j-th), in the five groups
+    // the phases free their regions for; `pend` marks groups issued and not yet
+    // waited, `ppar` the parity each will complete.
+    uint32_t pend = 0, ppar = 0;
+    auto load = [&](int grp, int it, int j) {
+        const int ibh = it / nchunks, ic = it % nchunks, y = ic * kC, hi = 2 * it, lo = hi + 1;
+        const uint32_t bar = ctl.bar(B_LD + grp);
+        pend |= 1u << grp;
+        ppar = (ppar & ~(1u << grp)) | ((uint32_t)(j & 1) << grp);
+        if (grp == 0) {  // G lo
+            mbar_arrive_expect_tx(bar, 2 * kTile);
+            tma_load_3d(duh, &tm_g, bar, 0, 0, lo);
+            tma_load_3d(dul, &tm_g, bar, 64, 0, lo);
+        } else if (grp == 1) {  // Q, dO, G hi, S lo
+            mbar_arrive_expect_tx(bar, 2 * 8192 + 2 * 8192 + 4 * kTile);
+            tma_load_3d(kq + 8192, &tm_q, bar, 0, y, ibh);
+            tma_load_3d(kq + kRegKQ + 8192, &tm_q, bar, 64, y, ibh);
+            tma_load_3d(dO, &tm_do, bar, 0, y, ibh);
+            tma_load_3d(dO + 8192, &tm_do, bar, 64, y, ibh);
+            tma_load_3d(gg, &tm_g, bar, 0, 0, hi);
+            tma_load_3d(gg + kTile, &tm_g, bar, 64, 0, hi);
+            tma_load_3d(ur, &tm_s, bar, 0, 0, lo);
+            tma_load_3d(ur + kTile, &tm_s, bar, 64, 0, lo);
+        } else if (grp == 2) {  // V, Tm, X
+            mbar_arrive_expect_tx(bar, 2 * 8192 + 8192 + 8192);
+            tma_load_3d(v, &tm_v, bar, 0, y, ibh);
+            tma_load_3d(v + 8192, &tm_v, bar, 64, y, ibh);
+            tma_load_3d(tm, &tm_tm, bar, 0, ic * 128 + 64, ibh);
+            tma_load_3d(base + OFF_X, &tm_x, bar, 0, 0, it);
+        } else if (grp == 3) {  // S hi
+            mbar_arrive_expect_tx(bar, 2 * kTile);
+            tma_load_3d(ss, &tm_s, bar, 0, 0, hi);
+            tma_load_3d(ss + kTile, &tm_s, bar, 64, 0, hi);
+        } else {  // K
+            mbar_arrive_expect_tx(bar, 2 * 8192);
+            tma_load_3d(kq, &tm_k, bar, 0, y, ibh);
+            tma_load_3d(kq + kRegKQ, &tm_k, bar, 64, y, ibh);
+        }
+    };
 
     if (t == 0) {
         misc[0] = 0;
         for (int b = 0; b < kBars; ++b) mbar_init(ctl.bar(b), 1);
         fence_mbar_init();
-        for (const CUtensorMap* m : {&tm_q, &tm_k, &tm_v, &tm_do, &tm_s, &tm_g, &tm_g64, &tm_x, &tm_tm})
+        for (const CUtensorMap* m : {&tm_q, &tm_k, &tm_v, &tm_do, &tm_s, &tm_g, &tm_x, &tm_tm})
             prefetch_tensormap(m);
+        for (int grp = 0; grp < kLoadGroups; ++grp) load(grp, blockIdx.x, 0);
     }
     if (t < 32) {
         tmem_alloc(smem_addr(tmem_holder), 512);
         tmem_relinquish();
     }
-    {   // zeros for the lower block of [X^T; 0]
-        uint4* const zb = reinterpret_cast<uint4*>(gbase + OFF_ZB);
-        for (int i = t; i < 512; i += 128) zb[i] = make_uint4(0u, 0u, 0u, 0u);
-        fence_proxy_async_smem();
-    }
-    if (t < kC) betas[t] = t < n ? __bfloat162float(beta[row0 + t]) : 0.f;
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_holder;
-    const uint32_t kq = base + OFF_KQ, dv = base + OFF_DV, pz = base + OFF_PZ, ur = base + OFF_UR;
-    const uint32_t tp = base + OFF_TP;
+    const uint32_t tl = tmem + lane;
 
-    bool ok = true;
-    if (t == 0) {  // every operand tile of the chunk, on one barrier
-        const uint32_t bar = ctl.bar(B_LOAD);
-        mbar_arrive_expect_tx(bar, kStageKQ + 2 * kTile + 8 * kTile + 8192 + 8192);
-        const int z = bh, y = t0, hi = 2 * item, lo = hi + 1;
-        tma_load_3d(kq, &tm_k, bar, 0, y, z);
-        tma_load_3d(kq + kRegKQ, &tm_k, bar, 64, y, z);
-        tma_load_3d(kq + 8192, &tm_q, bar, 0, y, z);
-        tma_load_3d(kq + kRegKQ + 8192, &tm_q, bar, 64, y, z);
-        tma_load_3d(dv + 8192, &tm_do, bar, 0, y, z);
-        tma_load_3d(dv + kRegDV + 8192, &tm_do, bar, 64, y, z);
-        tma_load_3d(dv + 16384, &tm_v, bar, 0, y, z);
-        tma_load_3d(dv + kRegDV + 16384, &tm_v, bar, 64, y, z);
-        tma_load_3d(base + OFF_S, &tm_s, bar, 0, 0, hi);
-        tma_load_3d(base + OFF_S + kTile, &tm_s, bar, 64, 0, hi);
-        tma_load_3d(ur, &tm_s, bar, 0, 0, lo);
-        tma_load_3d(ur + kTile, &tm_s, bar, 64, 0, lo);
-        tma_load_3d(base + OFF_G, &tm_g, bar, 0, 0, hi);
-        tma_load_3d(base + OFF_G + kTile, &tm_g, bar, 64, 0, hi);
-        tma_load_3d(dv, &tm_g64, bar, 0, 0, lo);
-        tma_load_3d(dv + kRegDV, &tm_g64, bar, 64, 0, lo);
-        tma_load_3d(tp, &tm_g64, bar, 0, 64, lo);
-        tma_load_3d(tp + kTile, &tm_g64, bar, 64, 64, lo);
-        tma_load_3d(tp + 8192, &tm_tm, bar, 0, c * 128 + 64, bh);
-        tma_load_3d(base + OFF_XI, &tm_x, bar, 0, 0, item);
-        ok = ctl.wait(B_LOAD, 0);
-    }
     int phase = 0;
-    // Issues MMA phase `phase` (thread 0) and waits for it; false if a wait gave up.
+    const uint64_t d0 = sw128_desc(base, 0, 1024);
+    // Issues MMA phase `phase % 6` (thread 0), and after its commit the group
+    // that needs nothing of the coming epilogue; waits for the phase.  False
+    // if a wait gave up.
     auto run = [&]() -> bool {
         bool good = true;
         if (t == 0) {
+            const int p = phase % 6;  // groups 0, 2, 3, 5, 6, 7; then 1 after phase 0, 4 after phase 2
             tc_fence_after_sync();
-            issue_phase(phase, tmem, base);
+            issue_group(p == 0 ? 0 : p + (p < 3 ? 1 : 2), tmem, d0);
             mma_commit(ctl.bar(B_MMA));
+            if (p == 0 || p == 2) issue_group(p == 0 ? 1 : 4, tmem, d0);
             good = ctl.wait(B_MMA, (uint32_t)phase);
         }
         ++phase;
-        const bool bad = wg_sync_or(kBar, !good);
+        const bool bad = wg_sync_or(kBar, !good, kThreads);
         tc_fence_after_sync();
         return !bad;
     };
-    if (wg_sync_or(kBar, !ok)) goto done;
-    // ---- R^T (negated S^T K^T), K K^T and Q K^T
-    if (!run()) goto done;
-    {
-        float x[64];
-        if (t >= 64) {  // P = tril(Q K^T): row s = t - 64, as [s][t] bf16
-            tmem_ld64f(tmem + lane + C_G1, x);
-#pragma unroll
-            for (int e = 0; e < 64; ++e)
-                if (e > t - 64) x[e] = 0.f;
-            store_row64_bf16(pz, t, x);
+    // After an epilogue: its shared-memory rows and TMEM stores visible to the next MMAs.
+    auto publish = [&]() {
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        wg_sync(kBar, kThreads);
+    };
+    float x[16];
+    // beta of the CTA's next chunk, read a chunk ahead (thread t < 64: token t)
+    float bnext = 0.f;
+    if (t < kC && (int)blockIdx.x < items) {
+        const int c = blockIdx.x % nchunks;
+        if (c * kC + t < T) bnext = __bfloat162float(beta[(size_t)(blockIdx.x / nchunks) * T + c * kC + t]);
+    }
+    for (int item = blockIdx.x, it = 0; item < items; item += gridDim.x, ++it) {
+        const int bh = item / nchunks, c = item % nchunks;
+        const int t0 = c * kC, n = min(kC, T - t0);
+        const size_t row0 = (size_t)bh * T + t0;
+        const int next = item + (int)gridDim.x < items ? item + (int)gridDim.x : -1;
+        {   // the 64 x 64 identity over PZ rows 64-127 (Z of the last chunk is spent), a 16-byte chunk per thread
+            const int r = t >> 3, lc = (t & 7) ^ (r & 7);  // row, and the logical chunk stored there
+            const uint32_t one = lc == (r >> 3) ? ((r & 1) ? 0x3F800000u : 0x00003F80u) : 0u;
+            const int wi = (r & 7) >> 1;                    // the 32-bit word holding column r
+            st_shared_v4(pz + 8192u + (uint32_t)(r * 128 + (t & 7) * 16), wi == 0 ? one : 0u,
+                         wi == 1 ? one : 0u, wi == 2 ? one : 0u, wi == 3 ? one : 0u);
+            fence_proxy_async_smem();
         }
-        float v[64];
-        tmem_ld64f(tmem + lane + C_R, x);
-        load_col64(dv, kRegDV, 128, t, v);  // V column t
-#pragma unroll
-        for (int e = 0; e < 64; ++e) x[e] += v[e];  // R^T row t (dv lane t)
-        pack64_tmem(tmem + lane + C_B, x);
-        store_col64(ur, kTile, 64, t, x, 1.f);  // R [t][dv]
-    }
-    tmem_wait_st();
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    wg_sync(kBar);
-    // ---- U'^T and dU'^T
-    if (!run()) goto done;
-    {
-        float x[64], v[64];
-        tmem_ld64f(tmem + lane + C_U, x);
-        store_col64(ur, kTile, 0, t, x, 1.f);  // U' [t][dv]
-        tmem_ld64f(tmem + lane + C_R, x);      // R^T row t again, as in the last step
-        load_col64(dv, kRegDV, 128, t, v);
-#pragma unroll
-        for (int e = 0; e < 64; ++e) x[e] = bf16_rest(x[e] + v[e]);
-        store_col64(tp, kTile, 0, t, x, 1.f);  // R lo [t][dv]
-        tmem_ld64f(tmem + lane + C_E, x);
-        pack64_tmem(tmem + lane + C_B, x);     // dU'^T as the next left operand
-        store_col64(dv, kRegDV, 0, t, x, 1.f);  // dU' hi [t][dv]
-#pragma unroll
-        for (int e = 0; e < 64; ++e) x[e] = bf16_rest(x[e]);
-        store_col64(dv, kRegDV, 128, t, x, 1.f);  // dU' lo over V
-    }
-    tmem_wait_st();
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    wg_sync(kBar);
-    // ---- dV^T and [dU'; dO] [U'; R]^T
-    if (!run()) goto done;
-    {
-        float x[64];
-        tmem_ld64f(tmem + lane + C_R, x);
-        store_col64(dv, kRegDV, 128, t, x, -1.f);  // -dV [t][dv] over V
-        tmem_ld64f(tmem + lane + C_PT + 64u, x);   // row t: dTm (t < 64), dO R^T (t >= 64)
-        pack64_tmem(tmem + lane + C_B, x);          // [dTm; -] as the left operand of M1
-        if (t < 64) store_row64_bf16(ur + kTile + 8192u, t, x);  // the dTm block of [M1 | dTm]
-        if (t >= 64) {  // dP = tril(dO U'^T): row t - 64, as [t][s] bf16
-            tmem_ld64f(tmem + lane + C_PT, x);
-#pragma unroll
-            for (int e = 0; e < 64; ++e)
-                if (e > t - 64) x[e] = 0.f;
-            store_row64_bf16(pz, t - 64, x);
+        if (t < kC) betas[t] = bnext;
+        bool ok = true;
+        if (t == 0) {
+            for (int grp = 0; grp < kLoadGroups && ok; ++grp) ok = ctl.wait(B_LD + grp, (uint32_t)it);
+            if (ok) pend = 0;
         }
-    }
-    tmem_wait_st();
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    wg_sync(kBar);
-    // ---- M1 = dTm Tm^T, and [dQ^T | dK^T] from S, Q, G
-    if (!run()) goto done;
-    if (t < 64) {  // M1 row t, the M1 block of [M1 | dTm]
-        float x[64];
-        tmem_ld64f(tmem + lane + C_R, x);
-        store_row64_bf16(ur + 8192u, t, x);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    wg_sync(kBar);
-    // ---- [X^T; 0] [M1 | dTm]: dA and diag(X^T dTm); then Z and dbeta
-    if (!run()) goto done;
-    {
-        float db = 0.f;
-        if (t < 64) {  // row a = t
-            float x[64];
-            tmem_ld64f(tmem + lane + C_PT + 64u, x);
+        if (wg_sync_or(kBar, !ok, kThreads)) goto done;
+        if (t < kC && next >= 0) {
+            const int nc = next % nchunks;
+            bnext = nc * kC + t < T
+                        ? __bfloat162float(beta[(size_t)(next / nchunks) * T + nc * kC + t])
+                        : 0.f;
+        }
+        // ---- K K^T, Q K^T and R^T
+        if (!run()) goto done;
+        if (q4 >= 2) {  // P = tril(Q K^T): query row s = L - 64, key columns col0 ..
+            tmem_ld16f(tl + C_G1 + col0, x);
 #pragma unroll
-            for (int e = 0; e < 64; ++e) db = e == t ? x[e] : db;  // sum_i X_ia dTm_ia
-            tmem_ld64f(tmem + lane + C_PT, x);
-            float kk[64];
-            tmem_ld64f(tmem + lane + C_G1, kk);  // (K K^T) row a
+            for (int e = 0; e < 16; ++e)
+                if (col0 + e > L - 64) x[e] = 0.f;
+            store_row16(pz, L - 64, g, x);
+        }
+        tmem_ld16f(tl + C_R + col0, x);  // R^T row L (dv)
+        pack16_tmem(tl + C_B + 8u * g, x);
+        store_row16(ur, L, g, x);
 #pragma unroll
-            for (int e = 0; e < 64; ++e) {
-                const float a = e < t ? -x[e] : 0.f;  // dA = strict_tril(-X^T M1)
-                dAs[t * kDAPitch + e] = a;
-                db = fmaf(a, kk[e], db);
+        for (int e = 0; e < 16; ++e) x[e] = bf16_rest(x[e]);
+        store_row16(v, L, g, x);  // R^T lo over V
+        publish();
+        // ---- U'^T and dU'^T
+        if (!run()) goto done;
+        tmem_ld16f(tl + C_U + col0, x);
+        store_row16(ur + kTile, L, g, x);
+        tmem_ld16f(tl + C_E + col0, x);
+        pack16_tmem(tl + C_B + 8u * g, x);
+        store_row16(duh, L, g, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] = bf16_rest(x[e]);
+        store_row16(dul, L, g, x);
+        publish();
+        // ---- dV^T, dTm^T and dP^T; dU' is spent: the next chunk's G lo
+        if (!run()) goto done;
+        if (t == 0 && next >= 0) load(0, next, it + 1);
+        tmem_ld16f(tl + C_R + col0, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] = -x[e];
+        store_row16(v, L, g, x);  // -dV^T over R^T lo
+        tmem_ld16f(tl + C_PT + col0, x);
+        pack16_tmem(tl + C_B + 8u * g, x);  // dTm^T (lanes 0-63) as the left operand of M1
+        if (q4 >= 2) {  // dP^T row a = L - 64 (key), query columns col0 ..: kept where query >= key
+            tmem_ld16f(tl + C_PT + 64u + col0, x);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                if (col0 + e < L - 64) x[e] = 0.f;
+            store_row16(pz, L - 64, g, x);
+        }
+        publish();
+        // ---- M1 = dTm^T X, dQ^T, dK^T; Q, dO, G, U' are spent: the next chunk's Q, dO, G hi, S lo
+        if (!run()) goto done;
+        if (t == 0 && next >= 0) load(1, next, it + 1);
+        if (q4 < 2) {  // M1 row a = L; its diagonal is the first d_beta term
+            tmem_ld16f(tl + C_R + col0, x);
+            store_row16(v, L, g, x);
+            float d = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) d = col0 + e == L ? x[e] : d;
+            if ((L >> 4) == g) db[L] = d;
+        }
+        publish();
+        // ---- dA^T = -Tm M1; M1, Tm, X are spent: the next chunk's V, Tm, X
+        if (!run()) goto done;
+        if (t == 0 && next >= 0) load(2, next, it + 1);
+        if (q4 < 2) {  // dA^T row L: dA[j][L] for j = col0 .. (strictly lower: j > L)
+            tmem_ld16f(tl + C_PT + col0, x);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                dAs[(col0 + e) * kDAPitch + L] = col0 + e > L ? x[e] : 0.f;
+        }
+        wg_sync(kBar, kThreads);
+        if (q4 < 2) {  // row a = L of dA: Z[a][col0 ..] and this thread's part of d_beta
+            float kk[16];
+            tmem_ld16f(tl + C_G1 + col0, kk);  // (K K^T)[a][col0 ..]
+            const float ba = betas[L];
+            float part = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int b = col0 + e;
+                const float dab = dAs[L * kDAPitch + b];
+                x[e] = ba * dab + betas[b] * dAs[b * kDAPitch + L];
+                part = fmaf(dab, kk[e], part);
             }
+            store_row16(pz + 8192u, L, g, x);  // Z over I
+            db[64 * (1 + g) + L] = part;
         }
-        wg_sync(kBar);
-        if (t < 64) {  // Z row a = beta_a dA[a][:] + beta_b dA[:][a]
-            float z[64];
-            const float ba = betas[t];
+        publish();
+        if (t == 0 && next >= 0) load(3, next, it + 1);  // dA is spent: the next chunk's S hi
+        if (t < kC && t < n)
+            d_beta[row0 + t] =
+                __float2bfloat16_rn(db[t] + db[64 + t] + db[128 + t] + db[192 + t] + db[256 + t]);
+        // ---- [dQ^T | dK^T] += K^T [dP | Z]; K is spent: the next chunk's K; then out
+        if (!run()) goto done;
+        if (t == 0 && next >= 0) load(4, next, it + 1);
+        tmem_ld16f(tl + C_DQ + col0, x);  // dQ^T row L (dk)
 #pragma unroll
-            for (int e = 0; e < 64; ++e)
-                z[e] = ba * dAs[t * kDAPitch + e] + betas[e] * dAs[e * kDAPitch + t];
-            store_row64_bf16(pz, 64 + t, z);
-            if (t < n) d_beta[row0 + t] = __float2bfloat16_rn(db);
-        }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    wg_sync(kBar);
-    // ---- [dQ^T | dK^T] += K^T [dP; Z]^T, then out
-    if (!run()) goto done;
-    {
-        float x[64];
-        tmem_ld64f(tmem + lane + C_QK, x);  // dQ^T row t (dk lane t)
+        for (int e = 0; e < 16; ++e)
+            if (col0 + e < n) d_q[(row0 + col0 + e) * kD + L] = __float2bfloat16_rn(x[e]);
+        tmem_ld16f(tl + C_DK + col0, x);
 #pragma unroll
-        for (int e = 0; e < 64; ++e)
-            if (e < n) d_q[(row0 + e) * kD + t] = __float2bfloat16_rn(x[e]);
-        tmem_ld64f(tmem + lane + C_QK + 64u, x);
-#pragma unroll
-        for (int e = 0; e < 64; ++e)
-            if (e < n) d_k[(row0 + e) * kD + t] = __float2bfloat16_rn(x[e]);
+        for (int e = 0; e < 16; ++e)
+            if (col0 + e < n) d_k[(row0 + col0 + e) * kD + L] = __float2bfloat16_rn(x[e]);
+        tc_fence_before_sync();
     }
 done:
-    if (t == 0) drain_mmas(ctl, B_END);
+    if (t == 0) {
+        drain_mmas(ctl, B_END);
+        // loads still in flight after a wait gave up: let them land (bounded) before exiting
+        for (int grp = 0; grp < kLoadGroups; ++grp)
+            if (pend & (1u << grp)) mbar_wait(ctl.bar(B_LD + grp), (ppar >> grp) & 1u, kTimeoutNs);
+    }
     tc_fence_before_sync();
     __syncthreads();
     if (t < 32) {
@@ -3139,11 +3172,10 @@ cudaError_t launch_chunk_bwd_grads_tc(const void* q, const void* k, const void* 
     const long long items = (long long)BH * nchunks;
     if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
     if (2 * items > 0x7fffffffLL) return cudaErrorInvalidValue;
-    CUtensorMap mq, mk, mv, mdo, ms, mg, mg64, mx, mtm;
+    CUtensorMap mq, mk, mv, mdo, ms, mg, mx, mtm;
     if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mv, v, BH, T) ||
         !make_map(&mdo, d_o, BH, T) || !make_state_map(&ms, S_rec, 2 * (int)items, 128) ||
-        !make_state_map(&mg, G_rec, 2 * (int)items, 128) ||
-        !make_state_map(&mg64, G_rec, 2 * (int)items, 64) || !make_x_map(&mx, X_rec, (int)items) ||
+        !make_state_map(&mg, G_rec, 2 * (int)items, 128) || !make_x_map(&mx, X_rec, (int)items) ||
         !make_ws_map(&mtm, const_cast<void*>(tiles), BH, nchunks, 64))
         return cudaErrorInvalidValue;
     cudaError_t err;
@@ -3151,10 +3183,11 @@ cudaError_t launch_chunk_bwd_grads_tc(const void* q, const void* k, const void* 
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     bgrad::kSmemBytes)) != cudaSuccess)
         return err;
-    chunk_bwd_grads_tc_kernel<<<(unsigned)items, 128, bgrad::kSmemBytes, stream>>>(
-        mq, mk, mv, mdo, ms, mg, mg64, mx, mtm, static_cast<const __nv_bfloat16*>(beta),
+    const int grid = (int)std::min<long long>(items, (long long)sm_count());
+    chunk_bwd_grads_tc_kernel<<<grid, bgrad::kThreads, bgrad::kSmemBytes, stream>>>(
+        mq, mk, mv, mdo, ms, mg, mx, mtm, static_cast<const __nv_bfloat16*>(beta),
         static_cast<__nv_bfloat16*>(d_q), static_cast<__nv_bfloat16*>(d_k),
-        static_cast<__nv_bfloat16*>(d_beta), T, nchunks);
+        static_cast<__nv_bfloat16*>(d_beta), T, nchunks, (int)items);
     return cudaGetLastError();
 }
 

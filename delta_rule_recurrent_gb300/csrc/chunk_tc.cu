@@ -2409,10 +2409,10 @@ chunk_bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 //   1: U'^T = R^T Tm^T;               dU'^T = dO^T P + G^T K^T  (G = hi + lo)
 //   2: dV^T = dU'^T Tm;  [R; U'] dU'^T (dTm^T, plus the lo parts of R and dU',
 //      since d_beta is a dot product of dU' with R that can cancel heavily);
-//      [R; U'] dO^T (dP^T)
+//      [R; U'] dO^T (dP^T);  dK^T = G U'^T
 //   3: M1 = dTm^T X (its diagonal: the first d_beta term);  dQ^T = S dO^T;
-//      dK^T = -S dV^T + Q^T dP + G U'^T
-//   4: dA^T = -Tm M1
+//      dK^T += -S dV^T + Q^T dP
+//   4: dA^T = -Tm M1 and dA = -M1^T Tm^T (Z needs both a row and a column of dA)
 //   5: [dQ^T | dK^T] += K^T [dP | Z]
 // A thread owns one TMEM lane and 16 of the 64 token columns (warpgroup w:
 // columns 16w .. 16w + 15).  Each result a later product reads from shared
@@ -2423,12 +2423,13 @@ chunk_bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 // phase ends on an MMA commit, waited with the bounded waits of the forward
 // kernels.
 namespace bgrad {
-constexpr int kThreads = 512;
+constexpr int kEpiThreads = 512;              // four warpgroups: the epilogues
+constexpr int kThreads = kEpiThreads + 32;    // and one warp that issues loads and MMAs
 // Shared memory; a region is reused once the phases that read it are done.
 constexpr uint32_t OFF_KQ = 0;                    // [K; Q]: 2 dk halves x 128 token rows
 constexpr uint32_t OFF_DO = OFF_KQ + kStageKQ;    // dO [t][dv]: 2 dv halves x 64 rows
 constexpr uint32_t OFF_V = OFF_DO + kTile;        // V [t][dv] -> R^T lo -> -dV^T -> M1
-constexpr uint32_t OFF_S = OFF_V + kTile;         // S hi: 2 dv halves x 128 dk rows -> fp32 dA
+constexpr uint32_t OFF_S = OFF_V + kTile;         // S hi: 2 dv halves x 128 dk rows
 constexpr uint32_t OFF_G = OFF_S + 2 * kTile;     // G hi
 constexpr uint32_t OFF_UR = OFF_G + 2 * kTile;    // S lo -> [R^T | U'^T], [dv][t] each
 constexpr uint32_t OFF_DUH = OFF_UR + 2 * kTile;  // G lo (dv 0-63) -> dU'^T hi
@@ -2437,7 +2438,7 @@ constexpr uint32_t OFF_PZ = OFF_DUL + kTile;      // rows 0-63: P -> dP^T; rows 
 constexpr uint32_t OFF_TM = OFF_PZ + kTile;       // Tm [i][a]
 constexpr uint32_t OFF_X = OFF_TM + 8192;         // X [i][a]
 constexpr uint32_t OFF_BAR = OFF_X + 8192;
-constexpr int kLoadGroups = 5;                    // the next chunk's loads, by the phase that frees them
+constexpr int kLoadGroups = 4;                    // the next chunk's loads, by the phase that frees them
 constexpr int kBars = 2 + kLoadGroups;            // MMA commits, drain, load groups
 constexpr uint32_t OFF_BETA = OFF_BAR + 64;       // 64 fp32
 constexpr uint32_t OFF_DB = OFF_BETA + 256;       // d_beta parts: [5][64] fp32
@@ -2448,10 +2449,9 @@ static_assert(OFF_DO % 1024 == 0 && OFF_V % 1024 == 0 && OFF_S % 1024 == 0 &&
               OFF_UR % 1024 == 0 && OFF_PZ % 1024 == 0 && OFF_TM % 1024 == 0 &&
               OFF_X % 1024 == 0, "tile alignment");
 static_assert(8 * kBars <= 64, "barrier space");
-constexpr int kDAPitch = 65;  // fp32 dA rows over the spent S
 // TMEM columns (512 allocated):
 constexpr uint32_t C_G1 = 0;    // [K; Q] K^T: K K^T (lanes 0-63), Q K^T (lanes 64-127)
-constexpr uint32_t C_R = 64;    // R^T, then dV^T, then M1
+constexpr uint32_t C_R = 64;    // R^T, then dV^T, then M1, then dA
 constexpr uint32_t C_B = 128;   // a bf16 left operand: R^T, then dU'^T, then dTm^T
 constexpr uint32_t C_U = 160;   // U'^T
 constexpr uint32_t C_DK = 160;  // dK^T, over U'^T once it is read
@@ -2493,8 +2493,8 @@ __device__ __forceinline__ float bf16_rest(float x) {
 // a descriptor is d0 plus a constant (start address in 16-byte units in the
 // low field, the MN-major block stride in the LBO field).  Groups 0, 2, 3, 5,
 // 6, 7 are the phases, each followed by its commit; group 1 (G's part of
-// dU'^T and dQ^T = S dO^T) and group 4 (G U'^T) need nothing the epilogues
-// write and run while the epilogue before them does.
+// dU'^T and dQ^T = S dO^T) needs nothing the epilogues write and runs while
+// the first epilogue does.
 __device__ __forceinline__ void issue_group(int grp, uint32_t tmem, uint64_t d0) {
     // K-major operand at `off`, step kk over a K split in 64-element regions `stride` apart
     // (LBO field 1, unused by the swizzled K-major layout)
@@ -2561,8 +2561,7 @@ __device__ __forceinline__ void issue_group(int grp, uint32_t tmem, uint64_t d0)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ss(tmem + C_PT + 64u, mnmaj(OFF_UR, kTile, kk), kmaj(OFF_DO, 8192, kk), MK, kk > 0);
-        break;
-    case 4:  // dK^T = G U'^T (over U'^T's columns, read by now)
+        // dK^T = G U'^T (over U'^T's columns, read by now)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ss(tmem + C_DK, kmaj(OFF_G, kTile, kk), mnmaj(OFF_UR + kTile, 8192, kk), KM, kk > 0);
@@ -2578,10 +2577,14 @@ __device__ __forceinline__ void issue_group(int grp, uint32_t tmem, uint64_t d0)
         for (int kk = 0; kk < 4; ++kk)
             mma_bf16_ss(tmem + C_DK, mnmaj(OFF_KQ + 8192, kRegKQ, kk), kmaj(OFF_PZ, 0, kk), MK, 1);
         break;
-    case 6:  // dA^T = -Tm M1 (rows 64-127 of that A read X: unused lanes)
+    case 6:  // dA^T = -Tm M1 and dA = -M1^T Tm^T (rows 64-127 of the As read X, and V's
+             // second half: unused lanes)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
             mma_bf16_ss(tmem + C_PT, kmaj(OFF_TM, 0, kk), mnmaj(OFF_V, 8192, kk), KM | kNegB, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + C_R, mnmaj(OFF_V, 8192, kk), kmaj(OFF_TM, 0, kk), MK | kNegB, kk > 0);
         break;
     default:  // dQ^T += K^T dP^T;  dK^T += K^T Z
 #pragma unroll
@@ -2608,7 +2611,7 @@ chunk_bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                           __nv_bfloat16* __restrict__ d_k, __nv_bfloat16* __restrict__ d_beta,
                           int T, int nchunks, int items) {
     using namespace bgrad;
-    constexpr int kBar = 1;
+    constexpr int kBarE = 1, kBarP = 2;  // epilogue warps only; epilogue warps and the issuer
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -2618,49 +2621,47 @@ chunk_bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
     float* const betas = reinterpret_cast<float*>(gbase + OFF_BETA);
     float* const db = reinterpret_cast<float*>(gbase + OFF_DB);
-    float* const dAs = reinterpret_cast<float*>(gbase + OFF_S);  // over S once its MMAs are done
     const int t = threadIdx.x;
-    // Thread t: TMEM lane L (warp t / 32 reaches lanes 32 (t / 32 % 4) ..), token columns col0 ..
-    const int q4 = (t >> 5) & 3, g = t >> 7;
+    const bool issuer = t >= kEpiThreads;  // warp 16; its lane 0 issues every TMA load and MMA
+    // Epilogue thread t: TMEM lane L (warp t / 32 reaches lanes 32 (t / 32 % 4) ..), token columns col0 ..
+    const int q4 = (t >> 5) & 3, g = (t >> 7) & 3;
     const int L = 32 * q4 + (t & 31), col0 = 16 * g;
     const uint32_t lane = (uint32_t)(32 * q4) << 16;
     const uint32_t kq = base + OFF_KQ, dO = base + OFF_DO, v = base + OFF_V, ss = base + OFF_S;
     const uint32_t gg = base + OFF_G, ur = base + OFF_UR, duh = base + OFF_DUH;
     const uint32_t dul = base + OFF_DUL, pz = base + OFF_PZ, tm = base + OFF_TM;
 
-    // Thread 0: the TMA loads of chunk `it` (the CTA's j-th), in the five groups
-    // the phases free their regions for; `pend` marks groups issued and not yet
-    // waited, `ppar` the parity each will complete.
+    // The issuer's TMA loads of chunk `it` (the CTA's j-th), in the four groups
+    // the phases free their regions for; `pend` marks groups issued and not
+    // yet waited, `ppar` the parity each will complete.
     uint32_t pend = 0, ppar = 0;
     auto load = [&](int grp, int it, int j) {
         const int ibh = it / nchunks, ic = it % nchunks, y = ic * kC, hi = 2 * it, lo = hi + 1;
         const uint32_t bar = ctl.bar(B_LD + grp);
         pend |= 1u << grp;
         ppar = (ppar & ~(1u << grp)) | ((uint32_t)(j & 1) << grp);
-        if (grp == 0) {  // G lo
-            mbar_arrive_expect_tx(bar, 2 * kTile);
+        if (grp == 0) {  // G lo, dO, G hi, S lo
+            mbar_arrive_expect_tx(bar, 2 * kTile + 2 * 8192 + 4 * kTile);
             tma_load_3d(duh, &tm_g, bar, 0, 0, lo);
             tma_load_3d(dul, &tm_g, bar, 64, 0, lo);
-        } else if (grp == 1) {  // Q, dO, G hi, S lo
-            mbar_arrive_expect_tx(bar, 2 * 8192 + 2 * 8192 + 4 * kTile);
-            tma_load_3d(kq + 8192, &tm_q, bar, 0, y, ibh);
-            tma_load_3d(kq + kRegKQ + 8192, &tm_q, bar, 64, y, ibh);
             tma_load_3d(dO, &tm_do, bar, 0, y, ibh);
             tma_load_3d(dO + 8192, &tm_do, bar, 64, y, ibh);
             tma_load_3d(gg, &tm_g, bar, 0, 0, hi);
             tma_load_3d(gg + kTile, &tm_g, bar, 64, 0, hi);
             tma_load_3d(ur, &tm_s, bar, 0, 0, lo);
             tma_load_3d(ur + kTile, &tm_s, bar, 64, 0, lo);
+        } else if (grp == 1) {  // Q, S hi
+            mbar_arrive_expect_tx(bar, 2 * 8192 + 2 * kTile);
+            tma_load_3d(kq + 8192, &tm_q, bar, 0, y, ibh);
+            tma_load_3d(kq + kRegKQ + 8192, &tm_q, bar, 64, y, ibh);
+            tma_load_3d(ss, &tm_s, bar, 0, 0, hi);
+            tma_load_3d(ss + kTile, &tm_s, bar, 64, 0, hi);
         } else if (grp == 2) {  // V, Tm, X
             mbar_arrive_expect_tx(bar, 2 * 8192 + 8192 + 8192);
             tma_load_3d(v, &tm_v, bar, 0, y, ibh);
             tma_load_3d(v + 8192, &tm_v, bar, 64, y, ibh);
             tma_load_3d(tm, &tm_tm, bar, 0, ic * 128 + 64, ibh);
             tma_load_3d(base + OFF_X, &tm_x, bar, 0, 0, it);
-        } else if (grp == 3) {  // S hi
-            mbar_arrive_expect_tx(bar, 2 * kTile);
-            tma_load_3d(ss, &tm_s, bar, 0, 0, hi);
-            tma_load_3d(ss + kTile, &tm_s, bar, 64, 0, hi);
         } else {  // K
             mbar_arrive_expect_tx(bar, 2 * 8192);
             tma_load_3d(kq, &tm_k, bar, 0, y, ibh);
@@ -2668,7 +2669,7 @@ chunk_bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
     };
 
-    if (t == 0) {
+    if (t == kEpiThreads) {
         misc[0] = 0;
         for (int b = 0; b < kBars; ++b) mbar_init(ctl.bar(b), 1);
         fence_mbar_init();
@@ -2685,168 +2686,194 @@ chunk_bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_holder;
     const uint32_t tl = tmem + lane;
-
-    int phase = 0;
     const uint64_t d0 = sw128_desc(base, 0, 1024);
-    // Issues MMA phase `phase % 6` (thread 0), and after its commit the group
-    // that needs nothing of the coming epilogue; waits for the phase.  False
-    // if a wait gave up.
-    auto run = [&]() -> bool {
-        bool good = true;
-        if (t == 0) {
-            const int p = phase % 6;  // groups 0, 2, 3, 5, 6, 7; then 1 after phase 0, 4 after phase 2
-            tc_fence_after_sync();
-            issue_group(p == 0 ? 0 : p + (p < 3 ? 1 : 2), tmem, d0);
-            mma_commit(ctl.bar(B_MMA));
-            if (p == 0 || p == 2) issue_group(p == 0 ? 1 : 4, tmem, d0);
-            good = ctl.wait(B_MMA, (uint32_t)phase);
+
+    // Every thread passes the same sequence of barriers on kBarP: one before
+    // the first chunk, then one after each of the first five epilogues of a
+    // chunk and one at its end.  A barrier ORs a failure flag across the CTA,
+    // and everyone leaves for `done` at the same barrier.
+    if (issuer) {
+        const bool lead = t == kEpiThreads;
+        bool bad = false;
+        int phase = 0;
+        if (wg_sync_or(kBarP, false, kThreads)) goto done;
+        for (int item = blockIdx.x, it = 0; item < items; item += gridDim.x, ++it) {
+            const int next = item + (int)gridDim.x < items ? item + (int)gridDim.x : -1;
+            if (lead) {
+                for (int grp = 0; grp < kLoadGroups && !bad; ++grp)
+                    bad = !ctl.wait(B_LD + grp, (uint32_t)it);
+                if (!bad) pend = 0;
+            }
+#pragma unroll 1
+            for (int p = 0; p < 6; ++p, ++phase) {
+                if (p > 0 && wg_sync_or(kBarP, bad, kThreads)) goto done;  // epilogue p - 1 done
+                if (!lead || bad) continue;
+                // groups 0, 2, 3, 5, 6, 7; group 1 after phase 0's commit
+                tc_fence_after_sync();
+                issue_group(p == 0 ? 0 : p + (p < 3 ? 1 : 2), tmem, d0);
+                mma_commit(ctl.bar(B_MMA));
+                if (p == 0) issue_group(1, tmem, d0);
+                // phases 2 to 5 free regions for the next chunk's load groups 0 to 3
+                if (p >= 2 && next >= 0) {
+                    bad = !ctl.wait(B_MMA, (uint32_t)phase);
+                    if (!bad) load(p - 2, next, it + 1);
+                }
+            }
+            if (wg_sync_or(kBarP, bad, kThreads)) goto done;  // the chunk's end
         }
-        ++phase;
-        const bool bad = wg_sync_or(kBar, !good, kThreads);
-        tc_fence_after_sync();
-        return !bad;
-    };
-    // After an epilogue: its shared-memory rows and TMEM stores visible to the next MMAs.
-    auto publish = [&]() {
-        tmem_wait_st();
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        wg_sync(kBar, kThreads);
-    };
-    float x[16];
-    // beta of the CTA's next chunk, read a chunk ahead (thread t < 64: token t)
-    float bnext = 0.f;
-    if (t < kC && (int)blockIdx.x < items) {
-        const int c = blockIdx.x % nchunks;
-        if (c * kC + t < T) bnext = __bfloat162float(beta[(size_t)(blockIdx.x / nchunks) * T + c * kC + t]);
+        goto done;
     }
-    for (int item = blockIdx.x, it = 0; item < items; item += gridDim.x, ++it) {
-        const int bh = item / nchunks, c = item % nchunks;
-        const int t0 = c * kC, n = min(kC, T - t0);
-        const size_t row0 = (size_t)bh * T + t0;
-        const int next = item + (int)gridDim.x < items ? item + (int)gridDim.x : -1;
-        {   // the 64 x 64 identity over PZ rows 64-127 (Z of the last chunk is spent), a 16-byte chunk per thread
-            const int r = t >> 3, lc = (t & 7) ^ (r & 7);  // row, and the logical chunk stored there
+    {
+        // After an epilogue: its shared-memory rows and TMEM stores visible to
+        // the next MMAs; true when someone gave up.
+        auto publish = [&](bool bad) -> bool {
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            return wg_sync_or(kBarP, bad, kThreads);
+        };
+        int phase = 0;
+        // Waits for the current phase's MMAs (thread 0, bounded); false if a wait gave up.
+        auto mma_done = [&]() -> bool {
+            bool good = true;
+            if (t == 0) good = ctl.wait(B_MMA, (uint32_t)phase);
+            ++phase;
+            const bool bad = wg_sync_or(kBarE, !good, kEpiThreads);
+            tc_fence_after_sync();
+            return !bad;
+        };
+        float x[16];
+        // beta of the CTA's next chunk, read a chunk ahead (thread t < 64: token t)
+        float bnext = 0.f;
+        if (t < kC && (int)blockIdx.x < items) {
+            const int c = blockIdx.x % nchunks;
+            if (c * kC + t < T)
+                bnext = __bfloat162float(beta[(size_t)(blockIdx.x / nchunks) * T + c * kC + t]);
+        }
+        // Operands of the next chunk that the threads write: the 64 x 64
+        // identity over PZ rows 64-127 (one 16-byte chunk per thread) and beta.
+        auto next_operands = [&]() {
+            const int r = t >> 3, lc = (t & 7) ^ (r & 7);  // row, the logical chunk stored there
             const uint32_t one = lc == (r >> 3) ? ((r & 1) ? 0x3F800000u : 0x00003F80u) : 0u;
             const int wi = (r & 7) >> 1;                    // the 32-bit word holding column r
             st_shared_v4(pz + 8192u + (uint32_t)(r * 128 + (t & 7) * 16), wi == 0 ? one : 0u,
                          wi == 1 ? one : 0u, wi == 2 ? one : 0u, wi == 3 ? one : 0u);
-            fence_proxy_async_smem();
-        }
-        if (t < kC) betas[t] = bnext;
-        bool ok = true;
-        if (t == 0) {
-            for (int grp = 0; grp < kLoadGroups && ok; ++grp) ok = ctl.wait(B_LD + grp, (uint32_t)it);
-            if (ok) pend = 0;
-        }
-        if (wg_sync_or(kBar, !ok, kThreads)) goto done;
-        if (t < kC && next >= 0) {
-            const int nc = next % nchunks;
-            bnext = nc * kC + t < T
-                        ? __bfloat162float(beta[(size_t)(next / nchunks) * T + nc * kC + t])
-                        : 0.f;
-        }
-        // ---- K K^T, Q K^T and R^T
-        if (!run()) goto done;
-        if (q4 >= 2) {  // P = tril(Q K^T): query row s = L - 64, key columns col0 ..
-            tmem_ld16f(tl + C_G1 + col0, x);
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                if (col0 + e > L - 64) x[e] = 0.f;
-            store_row16(pz, L - 64, g, x);
-        }
-        tmem_ld16f(tl + C_R + col0, x);  // R^T row L (dv)
-        pack16_tmem(tl + C_B + 8u * g, x);
-        store_row16(ur, L, g, x);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) x[e] = bf16_rest(x[e]);
-        store_row16(v, L, g, x);  // R^T lo over V
-        publish();
-        // ---- U'^T and dU'^T
-        if (!run()) goto done;
-        tmem_ld16f(tl + C_U + col0, x);
-        store_row16(ur + kTile, L, g, x);
-        tmem_ld16f(tl + C_E + col0, x);
-        pack16_tmem(tl + C_B + 8u * g, x);
-        store_row16(duh, L, g, x);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) x[e] = bf16_rest(x[e]);
-        store_row16(dul, L, g, x);
-        publish();
-        // ---- dV^T, dTm^T and dP^T; dU' is spent: the next chunk's G lo
-        if (!run()) goto done;
-        if (t == 0 && next >= 0) load(0, next, it + 1);
-        tmem_ld16f(tl + C_R + col0, x);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) x[e] = -x[e];
-        store_row16(v, L, g, x);  // -dV^T over R^T lo
-        tmem_ld16f(tl + C_PT + col0, x);
-        pack16_tmem(tl + C_B + 8u * g, x);  // dTm^T (lanes 0-63) as the left operand of M1
-        if (q4 >= 2) {  // dP^T row a = L - 64 (key), query columns col0 ..: kept where query >= key
-            tmem_ld16f(tl + C_PT + 64u + col0, x);
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                if (col0 + e < L - 64) x[e] = 0.f;
-            store_row16(pz, L - 64, g, x);
-        }
-        publish();
-        // ---- M1 = dTm^T X, dQ^T, dK^T; Q, dO, G, U' are spent: the next chunk's Q, dO, G hi, S lo
-        if (!run()) goto done;
-        if (t == 0 && next >= 0) load(1, next, it + 1);
-        if (q4 < 2) {  // M1 row a = L; its diagonal is the first d_beta term
-            tmem_ld16f(tl + C_R + col0, x);
-            store_row16(v, L, g, x);
-            float d = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) d = col0 + e == L ? x[e] : d;
-            if ((L >> 4) == g) db[L] = d;
-        }
-        publish();
-        // ---- dA^T = -Tm M1; M1, Tm, X are spent: the next chunk's V, Tm, X
-        if (!run()) goto done;
-        if (t == 0 && next >= 0) load(2, next, it + 1);
-        if (q4 < 2) {  // dA^T row L: dA[j][L] for j = col0 .. (strictly lower: j > L)
-            tmem_ld16f(tl + C_PT + col0, x);
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                dAs[(col0 + e) * kDAPitch + L] = col0 + e > L ? x[e] : 0.f;
-        }
-        wg_sync(kBar, kThreads);
-        if (q4 < 2) {  // row a = L of dA: Z[a][col0 ..] and this thread's part of d_beta
-            float kk[16];
-            tmem_ld16f(tl + C_G1 + col0, kk);  // (K K^T)[a][col0 ..]
-            const float ba = betas[L];
-            float part = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int b = col0 + e;
-                const float dab = dAs[L * kDAPitch + b];
-                x[e] = ba * dab + betas[b] * dAs[b * kDAPitch + L];
-                part = fmaf(dab, kk[e], part);
+            if (t < kC) betas[t] = bnext;
+        };
+        next_operands();
+        if (publish(false)) goto done;
+        for (int item = blockIdx.x; item < items; item += gridDim.x) {
+            const int bh = item / nchunks, c = item % nchunks;
+            const int t0 = c * kC, n = min(kC, T - t0);
+            const size_t row0 = (size_t)bh * T + t0;
+            const int next = item + (int)gridDim.x < items ? item + (int)gridDim.x : -1;
+            if (t < kC && next >= 0) {
+                const int nc = next % nchunks;
+                bnext = nc * kC + t < T
+                            ? __bfloat162float(beta[(size_t)(next / nchunks) * T + nc * kC + t])
+                            : 0.f;
             }
-            store_row16(pz + 8192u, L, g, x);  // Z over I
-            db[64 * (1 + g) + L] = part;
+            bool ok;
+            // ---- K K^T, Q K^T and R^T
+            if ((ok = mma_done())) {
+                if (q4 >= 2) {  // P = tril(Q K^T): query row s = L - 64, key columns col0 ..
+                    tmem_ld16f(tl + C_G1 + col0, x);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        if (col0 + e > L - 64) x[e] = 0.f;
+                    store_row16(pz, L - 64, g, x);
+                }
+                tmem_ld16f(tl + C_R + col0, x);  // R^T row L (dv)
+                pack16_tmem(tl + C_B + 8u * g, x);
+                store_row16(ur, L, g, x);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) x[e] = bf16_rest(x[e]);
+                store_row16(v, L, g, x);  // R^T lo over V
+            }
+            if (publish(!ok)) goto done;
+            // ---- U'^T and dU'^T
+            if ((ok = mma_done())) {
+                tmem_ld16f(tl + C_U + col0, x);
+                store_row16(ur + kTile, L, g, x);
+                tmem_ld16f(tl + C_E + col0, x);
+                pack16_tmem(tl + C_B + 8u * g, x);
+                store_row16(duh, L, g, x);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) x[e] = bf16_rest(x[e]);
+                store_row16(dul, L, g, x);
+            }
+            if (publish(!ok)) goto done;
+            // ---- dV^T, dTm^T, dP^T and G U'^T (then the issuer loads the next
+            // chunk's G lo, dO, G hi, S lo over what they spent)
+            if ((ok = mma_done())) {
+                tmem_ld16f(tl + C_R + col0, x);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) x[e] = -x[e];
+                store_row16(v, L, g, x);  // -dV^T over R^T lo
+                tmem_ld16f(tl + C_PT + col0, x);
+                pack16_tmem(tl + C_B + 8u * g, x);  // dTm^T (lanes 0-63) as the left operand of M1
+                if (q4 >= 2) {  // dP^T row a = L - 64 (key), query columns col0 ..: query >= key
+                    tmem_ld16f(tl + C_PT + 64u + col0, x);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        if (col0 + e < L - 64) x[e] = 0.f;
+                    store_row16(pz, L - 64, g, x);
+                }
+            }
+            if (publish(!ok)) goto done;
+            // ---- M1 = dTm^T X, dK^T (then the next chunk's Q, S hi)
+            if ((ok = mma_done())) {
+                if (q4 < 2) {  // M1 row a = L; its diagonal is the first d_beta term
+                    tmem_ld16f(tl + C_R + col0, x);
+                    store_row16(v, L, g, x);
+                    float d = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) d = col0 + e == L ? x[e] : d;
+                    if ((L >> 4) == g) db[L] = d;
+                }
+            }
+            if (publish(!ok)) goto done;
+            // ---- dA^T and dA (then the next chunk's V, Tm, X)
+            if ((ok = mma_done())) {
+                if (q4 < 2) {  // row a = L: Z[a][col0 ..] and this thread's part of d_beta
+                    float ar[16], ac[16];
+                    tmem_ld16f(tl + C_R + col0, ar);   // dA[a][b], kept for b < a (strictly lower)
+                    tmem_ld16f(tl + C_PT + col0, ac);  // dA^T[a][b] = dA[b][a], kept for b > a
+                    tmem_ld16f(tl + C_G1 + col0, x);   // (K K^T)[a][b]
+                    const float ba = betas[L];
+                    float part = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int b = col0 + e;
+                        const float dab = b < L ? ar[e] : 0.f;
+                        part = fmaf(dab, x[e], part);
+                        x[e] = ba * dab + (b > L ? betas[b] * ac[e] : 0.f);
+                    }
+                    store_row16(pz + 8192u, L, g, x);  // Z over I
+                    db[64 * (1 + g) + L] = part;
+                }
+            }
+            if (publish(!ok)) goto done;
+            if (t < kC && t < n)
+                d_beta[row0 + t] = __float2bfloat16_rn(db[t] + db[64 + t] + db[128 + t] +
+                                                       db[192 + t] + db[256 + t]);
+            // ---- [dQ^T | dK^T] += K^T [dP | Z] (then the next chunk's K); out
+            if ((ok = mma_done())) {
+                tmem_ld16f(tl + C_DQ + col0, x);  // dQ^T row L (dk)
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (col0 + e < n) d_q[(row0 + col0 + e) * kD + L] = __float2bfloat16_rn(x[e]);
+                tmem_ld16f(tl + C_DK + col0, x);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (col0 + e < n) d_k[(row0 + col0 + e) * kD + L] = __float2bfloat16_rn(x[e]);
+                if (next >= 0) next_operands();  // Z and beta are spent
+            }
+            if (publish(!ok)) goto done;  // the chunk's end
         }
-        publish();
-        if (t == 0 && next >= 0) load(3, next, it + 1);  // dA is spent: the next chunk's S hi
-        if (t < kC && t < n)
-            d_beta[row0 + t] =
-                __float2bfloat16_rn(db[t] + db[64 + t] + db[128 + t] + db[192 + t] + db[256 + t]);
-        // ---- [dQ^T | dK^T] += K^T [dP | Z]; K is spent: the next chunk's K; then out
-        if (!run()) goto done;
-        if (t == 0 && next >= 0) load(4, next, it + 1);
-        tmem_ld16f(tl + C_DQ + col0, x);  // dQ^T row L (dk)
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-            if (col0 + e < n) d_q[(row0 + col0 + e) * kD + L] = __float2bfloat16_rn(x[e]);
-        tmem_ld16f(tl + C_DK + col0, x);
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-            if (col0 + e < n) d_k[(row0 + col0 + e) * kD + L] = __float2bfloat16_rn(x[e]);
-        tc_fence_before_sync();
     }
 done:
-    if (t == 0) {
+    if (t == kEpiThreads) {
         drain_mmas(ctl, B_END);
         // loads still in flight after a wait gave up: let them land (bounded) before exiting
         for (int grp = 0; grp < kLoadGroups; ++grp)

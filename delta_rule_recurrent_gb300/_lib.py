@@ -16,7 +16,7 @@ HEADER = INCLUDE / "deltanet.h"
 DN_OK, DN_ERR_INVALID_ARG, DN_ERR_UNSUPPORTED, DN_ERR_CUDA = 0, 1, 2, 3
 DN_F32, DN_BF16 = 0, 1
 DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05 = 0, 1, 2
-ABI_VERSION = 4
+ABI_VERSION = 5
 
 _vp, _fp = ctypes.c_void_p, ctypes.c_void_p
 _int, _size = ctypes.c_int, ctypes.c_size_t
@@ -74,6 +74,7 @@ SIGNATURES = {
     "dn_last_error": (ctypes.c_char_p, []),
     "dn_abi_version": (_int, []),
     "dn_device_error": (_int, []),
+    "dn_debug_first_wait_ns": (_int, [ctypes.c_ulonglong]),
 }
 
 _lib = None

@@ -108,6 +108,15 @@ int dn_device_error(void) {
     return e == ~0u ? -1 : (int)e;
 }
 
+int dn_debug_first_wait_ns(unsigned long long ns) {
+    const cudaError_t e = dn::set_first_wait_limit(ns);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(DN_ERR_CUDA, "setting the wait limit: %s", cudaGetErrorString(e));
+    }
+    return DN_OK;
+}
+
 size_t dn_chunk_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt) {
     if (B <= 0 || H <= 0 || T <= 0 || C != 64 || !dn::chunk_tc_supports(dk, dv, dt)) return 0;
     const long long BH = (long long)B * H;

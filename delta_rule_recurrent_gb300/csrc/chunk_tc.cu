@@ -44,6 +44,8 @@ namespace dn {
 
 // First device-side error recorded by a tensor-core chunk kernel (0 = none).
 __device__ unsigned int g_chunk_tc_error = 0;
+// The limit of the gradient kernel's first bounded wait (a testing hook; 0:
+// that wait gives up at once).  Every other wait keeps kTimeoutNs.
 
 namespace {
 
@@ -52,6 +54,7 @@ using namespace ptx;
 constexpr int kC = 64;         // chunk length
 constexpr int kD = 128;        // dk = dv
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s without progress
+__device__ unsigned long long g_first_wait_ns = kTimeoutNs;
 // The polling roles count SM cycles (clock64 is cheap to read); at the
 // GB300's clocks 4e9 cycles is 2 s or more.
 constexpr long long kTimeoutCycles = 4000000000ll;
@@ -288,8 +291,13 @@ struct Ctl {
         atomicCAS(&g_chunk_tc_error, 0u, (unsigned)kErrTimeout);
     }
     // Bounded wait for the phase of barrier b with the given parity.  Gives up
-    // when another role has aborted, or after kTimeoutNs (raising the abort).
-    __device__ bool wait(int b, uint32_t parity) const {
+    // when another role has aborted, or after `limit` ns (raising the abort;
+    // a limit of 0 gives up without looking).
+    __device__ bool wait(int b, uint32_t parity, uint64_t limit = kTimeoutNs) const {
+        if (limit == 0) {
+            raise();
+            return false;
+        }
         const uint32_t a = bar(b);
         if (mbar_try_wait(a, parity & 1u)) return true;
         const uint64_t t0 = globaltimer_ns();
@@ -298,7 +306,7 @@ struct Ctl {
             for (int i = 0; i < 32; ++i)
                 if (mbar_try_wait(a, parity & 1u)) return true;
             if (aborted()) return false;
-            if (globaltimer_ns() - t0 > kTimeoutNs) {
+            if (globaltimer_ns() - t0 > limit) {
                 raise();
                 return false;
             }
@@ -2701,7 +2709,8 @@ chunk_bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             const int next = item + (int)gridDim.x < items ? item + (int)gridDim.x : -1;
             if (lead) {
                 for (int grp = 0; grp < kLoadGroups && !bad; ++grp)
-                    bad = !ctl.wait(B_LD + grp, (uint32_t)it);
+                    bad = !ctl.wait(B_LD + grp, (uint32_t)it,
+                                    it == 0 && grp == 0 ? g_first_wait_ns : kTimeoutNs);
                 if (!bad) pend = 0;
             }
 #pragma unroll 1
@@ -3247,6 +3256,10 @@ cudaError_t launch_chunk_tc_noalloc(const void* q, const void* k, const void* v,
     }
     if (chunk_tc_workspace_bytes(BH, T) > kNoAllocTiles * kTile) return cudaErrorInvalidValue;
     return launch_chunk_tc(q, k, v, beta, S0, o, S_T, BH, T, dk, dv, dt, ws, stream);
+}
+
+cudaError_t set_first_wait_limit(unsigned long long ns) {
+    return cudaMemcpyToSymbol(g_first_wait_ns, &ns, sizeof(ns));
 }
 
 unsigned int chunk_tc_take_device_error() {

@@ -174,5 +174,8 @@ cudaError_t launch_chunk_tc_noalloc(const void* q, const void* k, const void* v,
 // Returns and clears the error word the tensor-core kernel sets when one of
 // its bounded waits runs out (0 = none, ~0u = could not read it).  Synchronous.
 unsigned int chunk_tc_take_device_error();
+// Sets the limit of the tensor-core gradient kernel's first bounded wait
+// (0: it gives up at once) on the current device.
+cudaError_t set_first_wait_limit(unsigned long long ns);
 
 }  // namespace dn

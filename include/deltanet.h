@@ -156,11 +156,25 @@ DN_API int dn_recurrent_step(const void *q, const void *k, const void *v,
  * dn_device_error -- returns the first error code a kernel recorded on the
  * device since the previous call (0 if none) and clears it.  Kernels whose
  * internal waits are bounded record a code instead of hanging when a wait
- * runs out (1: a TMA load never completed, 2: a tensor-core operation never
- * completed); the outputs of such a call are then undefined.  This call
- * synchronises the current device.  Returns -1 if the word could not be read.
+ * runs out (1: a TMA load or a tensor-core operation did not complete within
+ * its limit); such a kernel then waits (bounded) for what it started, frees
+ * its tensor memory and returns, and the outputs of the call are undefined.
+ * This call synchronises the current device.  Returns -1 if the word could
+ * not be read.
  */
 DN_API int dn_device_error(void);
+
+/*
+ * dn_debug_first_wait_ns -- a testing hook for the failure path above, with
+ * no counterpart in the method: sets, for the current device, the limit in
+ * nanoseconds of the first bounded wait of the tensor-core gradient kernel
+ * (the dn_chunk_bwd path for bf16, dk = dv = 128).  0 makes that wait give up
+ * at once, so the kernel records code 1 and returns without results; the
+ * default is 2e9 (every other wait keeps it).  Process-wide state: set it
+ * only while no dn_chunk_bwd call is in flight.  Returns DN_OK or
+ * DN_ERR_CUDA.
+ */
+DN_API int dn_debug_first_wait_ns(unsigned long long ns);
 
 /* Static text for a dn_status value. */
 DN_API const char *dn_status_string(int status);
@@ -469,7 +483,7 @@ DN_API int dn_recurrent_step_kda_qk(const void *q, const void *k, const void *v,
 /* ABI version of this header (bumped on incompatible changes). */
 DN_API int dn_abi_version(void);
 
-#define DN_ABI_VERSION 4
+#define DN_ABI_VERSION 5
 
 #ifdef __cplusplus
 }

@@ -36,7 +36,7 @@ import ctypes
 from ._lib import (DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05, DN_BF16, DN_F32,
                    DeltaNetError, QkNorm, check, header_symbols, lib_path, load)
 
-__all__ = ["chunk_fwd", "chunk_bwd", "recurrent_step", "chunk_fwd_varlen", "chunk_fwd_gated",
+__all__ = ["chunk_fwd", "chunk_fwd_split", "chunk_bwd", "recurrent_step", "chunk_fwd_varlen", "chunk_fwd_gated",
            "recurrent_step_gated", "chunk_fwd_kda", "recurrent_step_kda", "qk_prepare",
            "qk_prepare_bwd", "DeltaRule", "DeltaNetError", "load", "lib_path",
            "header_symbols", "ALGOS"]
@@ -128,22 +128,9 @@ def _norm(scale, qk_l2norm, eps=1e-6):
                                float(eps)))
 
 
-def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
-              initial_state: torch.Tensor | None = None, output_final_state: bool = True,
-              chunk_size: int = 64, algo: str = "auto", out: torch.Tensor | None = None,
-              final_state: torch.Tensor | None = None, workspace="auto",
-              scale: float | None = None, qk_l2norm: bool = False):
-    """Chunkwise delta-rule forward (``dn_chunk_fwd``).
-
-    Returns ``(o, S_T)``; ``S_T`` is None when ``output_final_state`` is
-    False.  ``final_state`` may be ``initial_state`` itself to update it in
-    place; ``out`` may supply the output buffer.  ``workspace``: "auto"
-    allocates the scratch ``dn_chunk_fwd_workspace_bytes`` asks for (the
-    two-pass tensor-core path), None runs without scratch (one fused kernel),
-    and a uint8 CUDA tensor of at least that many bytes is used as given.
-    ``qk_l2norm`` / ``scale``: the kernels L2-normalise q and k and scale q
-    as they load them (``dn_chunk_fwd_qk``).
-    """
+def _forward_tensors(q, k, v, beta, initial_state, output_final_state, out, final_state):
+    """Checks a [B,H,T,d] forward's tensors; allocates o and S_T when not given.
+    Returns (device, dtype code, (B, H, T, dk, dv), o, S_T or None)."""
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta)):
         _check_cuda(name, t, dev)
@@ -173,6 +160,27 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Ten
         _check_cuda("final_state", S_T, dev)
         if S_T.dtype != torch.float32 or tuple(S_T.shape) != (B, H, dk, dv):
             raise ValueError("final_state must be float32 [B,H,dk,dv]")
+    return dev, dt, (B, H, T, dk, dv), out, S_T
+
+
+def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+              initial_state: torch.Tensor | None = None, output_final_state: bool = True,
+              chunk_size: int = 64, algo: str = "auto", out: torch.Tensor | None = None,
+              final_state: torch.Tensor | None = None, workspace="auto",
+              scale: float | None = None, qk_l2norm: bool = False):
+    """Chunkwise delta-rule forward (``dn_chunk_fwd``).
+
+    Returns ``(o, S_T)``; ``S_T`` is None when ``output_final_state`` is
+    False.  ``final_state`` may be ``initial_state`` itself to update it in
+    place; ``out`` may supply the output buffer.  ``workspace``: "auto"
+    allocates the scratch ``dn_chunk_fwd_workspace_bytes`` asks for (the
+    two-pass tensor-core path), None runs without scratch (one fused kernel),
+    and a uint8 CUDA tensor of at least that many bytes is used as given.
+    ``qk_l2norm`` / ``scale``: the kernels L2-normalise q and k and scale q
+    as they load them (``dn_chunk_fwd_qk``).
+    """
+    dev, dt, (B, H, T, dk, dv), out, S_T = _forward_tensors(
+        q, k, v, beta, initial_state, output_final_state, out, final_state)
     lib = load()
     ws_bytes = lib.dn_chunk_fwd_workspace_bytes(B, H, T, dk, dv, chunk_size, dt)
     if isinstance(workspace, str):
@@ -192,6 +200,34 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Ten
             B, H, T, dk, dv, chunk_size, dt,
             ws.data_ptr() if ws is not None else None, ws_bytes,
             _stream_handle(dev), ALGOS[algo], _norm(scale, qk_l2norm)))
+    return out, S_T
+
+
+def chunk_fwd_split(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                    initial_state: torch.Tensor | None = None, output_final_state: bool = True,
+                    segments: int = 0, chunk_size: int = 64, out: torch.Tensor | None = None,
+                    final_state: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None):
+    """The chunkwise forward for a few long sequences (``dn_chunk_fwd_split``):
+    each sequence cut into ``segments`` runs scanned in parallel (0: enough
+    to fill the GPU once).  bf16, dk = dv = 128.  Arguments and results as
+    for ``chunk_fwd``; ``workspace`` is a uint8 CUDA tensor of at least
+    ``dn_chunk_fwd_split_workspace_bytes`` bytes, or None to allocate one."""
+    dev, dt, (B, H, T, dk, dv), out, S_T = _forward_tensors(
+        q, k, v, beta, initial_state, output_final_state, out, final_state)
+    lib = load()
+    with torch.cuda.device(dev):
+        ws_bytes = lib.dn_chunk_fwd_split_workspace_bytes(B, H, T, dk, dv, chunk_size, dt,
+                                                          segments)
+        if workspace is None:
+            workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+        _check_cuda("workspace", workspace, dev)
+        check(lib.dn_chunk_fwd_split(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(),
+            initial_state.data_ptr() if initial_state is not None else None,
+            out.data_ptr(), S_T.data_ptr() if S_T is not None else None,
+            B, H, T, dk, dv, chunk_size, dt, segments, workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_handle(dev)))
     return out, S_T
 
 

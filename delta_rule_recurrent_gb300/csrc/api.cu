@@ -274,6 +274,52 @@ int dn_chunk_fwd(const void* q, const void* k, const void* v, const void* beta, 
                            workspace_bytes, stream, DN_ALGO_AUTO, nullptr);
 }
 
+static int split_segments(long long BH, int T, int segments) {
+    return segments > 0 ? segments : dn::chunk_tc_split_segments((int)BH, T);
+}
+
+size_t dn_chunk_fwd_split_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt,
+                                          int segments) {
+    if (B <= 0 || H <= 0 || T <= 0 || C != 64 || segments < 0 ||
+        segments > dn::kMaxVarlenSeqs || !dn::chunk_tc_supports(dk, dv, dt))
+        return 0;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return 0;
+    return dn::chunk_tc_split_workspace_bytes((int)BH, T, split_segments(BH, T, segments));
+}
+
+int dn_chunk_fwd_split(const void* q, const void* k, const void* v, const void* beta,
+                       const float* S0, void* o, float* S_T, int B, int H, int T, int dk, int dv,
+                       int C, int dt, int segments, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+    if (int st = check_chunk_sizes(B, H, T, dk, dv, C, dt, "B")) return st;
+    if (!dn::chunk_tc_supports(dk, dv, dt))
+        return fail(DN_ERR_UNSUPPORTED, "the split runs on tensor cores: dk=%d dv=%d dtype=%d", dk,
+                    dv, dt);
+    if (segments < 0 || segments > dn::kMaxVarlenSeqs)
+        return fail(DN_ERR_INVALID_ARG, "segments %d outside 0 .. %d", segments,
+                    dn::kMaxVarlenSeqs);
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
+    if (BH == 0) return ok();
+    const ChunkSpans c = chunk_spans(q, k, v, beta, nullptr, 0, 0, S0, o, S_T,
+                                     (size_t)BH * (size_t)T, BH, dk, dv, dt);
+    int dev = 0;
+    if (int st = current_device(&dev)) return st;
+    if (int st = check_chunk_spans(c, T > 0, dev)) return st;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) return pass_state_through(S0, S_T, c.state_bytes, st);
+    const int nseg = split_segments(BH, T, segments);
+    const size_t need = dn::chunk_tc_split_workspace_bytes((int)BH, T, nseg);
+    if (!workspace || workspace_bytes < need)
+        return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                    need);
+    if (int st2 = check_workspace(c, workspace, need, dev)) return st2;
+    return cuda_status(dn::launch_chunk_tc_split(q, k, v, beta, S0, o, S_T, (int)BH, T, nseg,
+                                                 workspace, st),
+                       "chunk forward (sequence split) launch");
+}
+
 int dn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const void* beta,
                          const float* S0, void* o, float* S_T, int B, int H, int T, int dk,
                          int dv, int C, int dt, void* stream) {

@@ -1556,10 +1556,12 @@ struct Smem {
 // the decay vectors to the set's side slot, all on the [PT; Tm] barrier.
 // Prepared inputs on the plain form (side only): the chunk's row factors
 // go to the side slot the same way.
+// zero_v: the v buffers hold zeros from the start; each chunk's v barrier
+// is only arrived on.
 __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q,
                          const CUtensorMap* tm_k, const CUtensorMap* tm_v, const CUtensorMap* tm_ws,
                          const SeqSpan& sp, int nchunks, const CUtensorMap* tm_ws2,
-                         const float* side, const CUtensorMap* tm_kh) {
+                         const float* side, const CUtensorMap* tm_kh, bool zero_v) {
     const int z = sp.z, r0 = sp.row0, w0 = sp.wsbase;
     const int ns = sm.nst, nkqb = 2 * sm.nst;
     int nkq = 0, nv = 0, ntp = 0;
@@ -1597,12 +1599,16 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
             (nv < kVBufs ||
              mbar_test_wait(ctl.bar(B_V_EMPTY + nv % kVBufs), (uint32_t)(nv / kVBufs - 1) & 1u))) {
             const uint32_t bar = ctl.bar(B_V_FULL + nv % kVBufs);
-            mbar_arrive_expect_tx(bar, 2 * 8192);
-            tma_load_3d(sm.v(nv), tm_v, bar, 0, r0 + nv * kC, z);
-            tma_load_3d(sm.v(nv) + 8192, tm_v, bar, 64, r0 + nv * kC, z);
-            if (nv + kVBufs < nchunks) {
-                tma_prefetch_l2_3d(tm_v, 0, r0 + (nv + kVBufs) * kC, z);
-                tma_prefetch_l2_3d(tm_v, 64, r0 + (nv + kVBufs) * kC, z);
+            if (zero_v) {
+                mbar_arrive(bar);
+            } else {
+                mbar_arrive_expect_tx(bar, 2 * 8192);
+                tma_load_3d(sm.v(nv), tm_v, bar, 0, r0 + nv * kC, z);
+                tma_load_3d(sm.v(nv) + 8192, tm_v, bar, 64, r0 + nv * kC, z);
+                if (nv + kVBufs < nchunks) {
+                    tma_prefetch_l2_3d(tm_v, 0, r0 + (nv + kVBufs) * kC, z);
+                    tma_prefetch_l2_3d(tm_v, 64, r0 + (nv + kVBufs) * kC, z);
+                }
             }
             ++nv;
             progressed = true;
@@ -1984,7 +1990,9 @@ __device__ void writer_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t
 // kKda: tm_ws2 maps K^ = K . exp(G_C - G) (the state update's operand, loaded
 // with each stage), tm_q / tm_k the decayed Q . exp G, K . exp G, and side
 // holds exp G_C per key channel for every chunk.
-template <bool kRec, int NMAX, bool kGate = false, bool kKda = false>
+// kZeroV: the values are all zero (tm_v is not read): the state's transition
+// alone.
+template <bool kRec, int NMAX, bool kGate = false, bool kKda = false, bool kZeroV = false>
 __global__ void __launch_bounds__(512, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ws,
@@ -2023,6 +2031,11 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         prefetch_tensormap(&tm_ws);
         if (kGate || kKda) prefetch_tensormap(&tm_ws2);
     }
+    if constexpr (kZeroV) {  // the v buffers, zero for good
+        for (int i = tid; i < scan::kVBufs * (int)(kTile / 16); i += 512)
+            st_shared_v4(sm.v(0) + 16u * (uint32_t)i, 0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_holder), 512);
         tmem_relinquish();
@@ -2035,7 +2048,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (warp == 0) {
         if (lane == 0)
             scan::producer(ctl, sm, &tm_q, &tm_k, &tm_v, &tm_ws, sp, nchunks,
-                           kGate ? &tm_ws2 : nullptr, cside, kKda ? &tm_ws2 : nullptr);
+                           kGate ? &tm_ws2 : nullptr, cside, kKda ? &tm_ws2 : nullptr, kZeroV);
     } else if (warp >= 4 && warp < 8) {
         const int t = tid - 128;
         scan::state_body<kRec, kGate, kKda>(ctl, sm, tmem, t, S0, S_T, S_chunks, bh, nchunks, sside,
@@ -3071,6 +3084,197 @@ cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v, 
     scan_kernel<<<(unsigned)ctas, 512, scan::kSmemBytes, stream>>>(
         mq, mk, mv, mws, mws, S0, static_cast<__nv_bfloat16*>(o), S_T, nullptr, T, H, seqs, side);
     return cudaGetLastError();
+}
+
+// ------------------------------------------------ sequence split (few, long sequences)
+// The state after a stretch of chunks is linear in the state before it:
+// S_end = A S_start + B, with A (dk x dk) the product of the chunks'
+// transitions I - K^T Tm K and B the end state from a zero start
+// ("Chunkwise parallelization", paperlayer.ai/abs/2406.06484v6: the chunks'
+// states are what carries one chunk's effect to the next; the value columns
+// and the start state enter linearly).  A sequence cut into n segments of
+// whole chunks then runs as
+//   1. the prepare pass over every chunk, once;
+//   2. the scan over segments 0 .. n-2 from S = 0 with the values v: B;
+//   3. the same scan from S = I with zero values (v is not read; the value
+//      buffers hold zeros): A;
+//   4. S_start[0] = S0, S_start[s + 1] = A[s] S_start[s] + B[s], in fp32;
+//   5. the scan over every segment from its S_start, writing o and its end
+//      state (in place), the last of which is S_T.
+// Passes 2, 3 and 5 run n * BH CTAs, so a few long sequences fill the GPU.
+
+namespace {
+// `mats` [128][128] identities.
+__global__ void split_identity_kernel(float* __restrict__ A, long long mats) {
+    const long long total = mats * kD * kD;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int e = (int)(i % (kD * kD));
+        A[i] = e / kD == e % kD ? 1.f : 0.f;
+    }
+}
+
+// S_start of every segment of sequence blockIdx.x ([seg][BH][dk][dv] fp32),
+// 16 value columns per CTA (blockIdx.y), from A and B of the segments before:
+// thread t owns row t % 128 and 4 of the columns; A[s] is staged in shared
+// memory (rows padded to 129 floats) while A[s + 1] and the next B entries
+// are read into registers.
+constexpr int kCombineThreads = 512;
+constexpr size_t kCombineSmem = ((size_t)kD * (kD + 1) + (size_t)kD * 16) * sizeof(float);
+__global__ void __launch_bounds__(kCombineThreads) split_combine_kernel(
+    const float* __restrict__ A, const float* __restrict__ Bm, const float* __restrict__ S0,
+    float* __restrict__ Sst, int nseg, int BH) {
+    extern __shared__ float smf[];
+    constexpr int kP = kD + 1, kPer = kD * kD / kCombineThreads;
+    float* const as = smf;             // A[s], [128][129]
+    float* const xs = smf + kD * kP;   // S_start[s], this CTA's columns, [128][16]
+    const int bh = blockIdx.x, c0 = blockIdx.y * 16, t = threadIdx.x;
+    const int r = t & (kD - 1), cb = (t >> 7) * 4;
+    const size_t mat = (size_t)kD * kD;
+    for (int i = t; i < kD * 16; i += kCombineThreads) {
+        const size_t e = (size_t)bh * mat + (size_t)(i >> 4) * kD + c0 + (i & 15);
+        const float x = S0 ? S0[e] : 0.f;
+        xs[i] = x;
+        Sst[e] = x;
+    }
+    float pre[kPer];  // A[s] on its way: element t + 512 m
+    float4 bnext;     // B[s][r][c0 + cb ..]
+    auto fetch = [&](int s) {
+        const size_t off = ((size_t)s * BH + bh) * mat;
+#pragma unroll
+        for (int m = 0; m < kPer; ++m) pre[m] = __ldg(A + off + t + kCombineThreads * m);
+        bnext = __ldg(reinterpret_cast<const float4*>(Bm + off + (size_t)r * kD + c0 + cb));
+    };
+    if (nseg > 1) fetch(0);
+    for (int s = 0; s + 1 < nseg; ++s) {
+        __syncthreads();  // the last step's reads of as and writes of xs are done
+#pragma unroll
+        for (int m = 0; m < kPer; ++m) {
+            const int i = t + kCombineThreads * m;
+            as[(i >> 7) * kP + (i & (kD - 1))] = pre[m];
+        }
+        float acc[4] = {bnext.x, bnext.y, bnext.z, bnext.w};
+        if (s + 2 < nseg) fetch(s + 1);
+        __syncthreads();
+#pragma unroll 8
+        for (int k = 0; k < kD; ++k) {
+            const float a = as[r * kP + k];
+            const float4 x = *reinterpret_cast<const float4*>(xs + k * 16 + cb);
+            acc[0] = fmaf(a, x.x, acc[0]);
+            acc[1] = fmaf(a, x.y, acc[1]);
+            acc[2] = fmaf(a, x.z, acc[2]);
+            acc[3] = fmaf(a, x.w, acc[3]);
+        }
+        __syncthreads();  // every thread has read xs
+        const float4 out = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4*>(xs + r * 16 + cb) = out;
+        *reinterpret_cast<float4*>(Sst + ((size_t)(s + 1) * BH + bh) * mat + (size_t)r * kD + c0 +
+                                   cb) = out;
+    }
+}
+
+int split_segments_fit(int nchunks, int nseg) {
+    if (nseg < 1) nseg = 1;
+    if (nseg > nchunks) nseg = nchunks;
+    const int per = (nchunks + nseg - 1) / nseg;
+    return (nchunks + per - 1) / per;
+}
+
+}  // namespace
+
+int chunk_tc_split_segments(int BH, int T) {
+    if (BH <= 0 || T <= 0) return 1;
+    const int nchunks = (T + kC - 1) / kC;
+    const int s = std::min(std::max(1, sm_count() / BH), kMaxVarlenSeqs);
+    return split_segments_fit(nchunks, s);
+}
+
+size_t chunk_tc_split_workspace_bytes(int BH, int T, int nseg) {
+    if (BH <= 0 || T <= 0 || nseg < 1) return 0;
+    const size_t nchunks = (size_t)((T + kC - 1) / kC);
+    return (size_t)BH * nchunks * kTile + 3 * (size_t)nseg * BH * kD * kD * sizeof(float);
+}
+
+cudaError_t launch_chunk_tc_split(const void* q, const void* k, const void* v, const void* beta,
+                                  const float* S0, void* o, float* S_T, int BH, int T, int nseg,
+                                  void* workspace, cudaStream_t stream) {
+    if (BH <= 0 || T <= 0) return cudaSuccess;
+    if (!workspace || !o || nseg < 1 || nseg > kMaxVarlenSeqs) return cudaErrorInvalidValue;
+    const int nchunks = (T + kC - 1) / kC;
+    const int n = split_segments_fit(nchunks, nseg), per = (nchunks + n - 1) / n;
+    if ((long long)n * BH > 0x7fffffffLL || (long long)BH * nchunks > 0x7fffffffLL)
+        return cudaErrorInvalidValue;
+    uint8_t* const w = static_cast<uint8_t*>(workspace);
+    const size_t mat = (size_t)kD * kD, states = (size_t)nseg * BH * mat;
+    void* const tiles = w;
+    float* const Abuf = reinterpret_cast<float*>(w + (size_t)BH * nchunks * kTile);
+    float* const Bbuf = Abuf + states;
+    float* const Sst = Bbuf + states;
+    // segments of `per` whole chunks (the last one ragged)
+    static thread_local VarlenTable seqs;
+    seqs.n = n;
+    for (int i = 0; i < n; ++i) {
+        seqs.chunk[i] = i * per;
+        seqs.start[i] = i * per * kC;
+    }
+    seqs.chunk[n] = nchunks;
+    seqs.start[n] = T;
+    CUtensorMap mq, mk, mv, mws;
+    if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mv, v, BH, T) ||
+        !make_ws_map(&mws, tiles, BH, nchunks))
+        return cudaErrorInvalidValue;
+    // the runs are whole chunks of each sequence, so the batched prepare pass
+    // lays the tiles out as the scans over runs read them
+    auto prep_kernel = chunk_prep_kernel<1, false>;
+    auto scan_kernel = chunk_scan_kernel<false, kMaxVarlenSeqs>;
+    auto zero_scan = chunk_scan_kernel<false, kMaxVarlenSeqs, false, false, true>;
+    cudaError_t err;
+    if ((err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kPrepSmemBytes)) != cudaSuccess ||
+        (err = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    scan::kSmemBytes)) != cudaSuccess ||
+        (err = cudaFuncSetAttribute(zero_scan, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    scan::kSmemBytes)) != cudaSuccess ||
+        (err = cudaFuncSetAttribute(split_combine_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kCombineSmem)) != cudaSuccess)
+        return err;
+    const long long items = (long long)BH * nchunks;
+    {
+        const SeqTable<1> batched{};
+        const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
+        prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
+            mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, nchunks, (int)items, batched,
+            nullptr, nullptr, mws, kNoNorm, nullptr);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    __nv_bfloat16* const ob = static_cast<__nv_bfloat16*>(o);
+    if (n == 1) {  // one segment: the plain scan
+        scan_kernel<<<(unsigned)BH, 512, scan::kSmemBytes, stream>>>(
+            mq, mk, mv, mws, mws, S0, ob, S_T, nullptr, T, BH, seqs, nullptr);
+        return cudaGetLastError();
+    }
+    seqs.n = n - 1;  // passes 2 and 3 leave out the last segment
+    const unsigned ctas = (unsigned)((n - 1) * BH);
+    scan_kernel<<<ctas, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mws, nullptr, nullptr,
+                                                          Bbuf, nullptr, T, BH, seqs, nullptr);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    split_identity_kernel<<<sm_count() * 4, 256, 0, stream>>>(Abuf, (long long)(n - 1) * BH);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    zero_scan<<<ctas, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mws, Abuf, nullptr, Abuf,
+                                                        nullptr, T, BH, seqs, nullptr);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    split_combine_kernel<<<dim3((unsigned)BH, kD / 16), kCombineThreads, kCombineSmem, stream>>>(
+        Abuf, Bbuf, S0, Sst, n, BH);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    seqs.n = n;
+    scan_kernel<<<(unsigned)(n * BH), 512, scan::kSmemBytes, stream>>>(
+        mq, mk, mv, mws, mws, Sst, ob, Sst, nullptr, T, BH, seqs, nullptr);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (S_T)
+        err = cudaMemcpyAsync(S_T, Sst + (size_t)(n - 1) * BH * mat, (size_t)BH * mat * sizeof(float),
+                              cudaMemcpyDeviceToDevice, stream);
+    return err;
 }
 
 size_t chunk_tc_gated_workspace_bytes(int BH, int T) {

@@ -108,6 +108,16 @@ cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v,
                                    const void* beta, const float* S0, void* o, float* S_T,
                                    const VarlenTable& seqs, int H, int T, void* workspace,
                                    cudaStream_t stream, const QkNorm& norm = kNoNorm);
+// Few long sequences on tensor cores (bf16, dk = dv = 128): each sequence
+// cut into segments of whole chunks that run in parallel, their start states
+// joined through the segments' transitions.  chunk_tc_split_segments is the
+// segment count that fills the GPU once; the workspace holds the tiles and
+// three [nseg][BH][dk][dv] fp32 state arrays.  o is required.
+int chunk_tc_split_segments(int BH, int T);
+size_t chunk_tc_split_workspace_bytes(int BH, int T, int nseg);
+cudaError_t launch_chunk_tc_split(const void* q, const void* k, const void* v, const void* beta,
+                                  const float* S0, void* o, float* S_T, int BH, int T, int nseg,
+                                  void* workspace, cudaStream_t stream);
 // The backward's chain on tcgen05 (bf16, dk = dv = 128): G = dL/dS from the
 // last chunk to the first, with the forward's [PT; Tm] tiles (`tiles`, the
 // workspace the state recompute used) read transposed.  Writes G at every

@@ -165,6 +165,37 @@ DN_API int dn_recurrent_step(const void *q, const void *k, const void *v,
 DN_API int dn_device_error(void);
 
 /*
+ * dn_chunk_fwd_split -- dn_chunk_fwd for a few long sequences (bf16,
+ * dk = dv = 128, C = 64): each sequence is cut into `segments` runs of whole
+ * chunks that are scanned in parallel.  The state is linear in its start
+ * value, S_end = A S_start + B per run, where A is the product of the runs'
+ * chunk transitions (I - K^T T K) and B its end state from zero ("Chunkwise
+ * parallelization", paperlayer.ai/abs/2406.06484v6: the chunk states are the
+ * only thing carried from chunk to chunk).  The call scans every run but the
+ * last from zero (B) and from the identity with zero values (A), joins the
+ * start states in fp32, then scans every run from its own start writing o and
+ * the final state.  Results agree with dn_chunk_fwd within bf16 rounding; the
+ * chunk arithmetic is the same, only the start states of the runs are formed
+ * differently.
+ *   arguments as for dn_chunk_fwd; o is required;
+ *   segments  number of runs, 1 .. 1024, or 0 to fill the current device's
+ *             SMs once (SMs / (B * H), at least 1); capped at the chunk count;
+ *   workspace device scratch of dn_chunk_fwd_split_workspace_bytes(...) bytes
+ *             (required), 16-byte aligned.
+ * S0 == S_T is allowed.  Errors: as dn_chunk_fwd; DN_ERR_UNSUPPORTED outside
+ * bf16 with dk = dv = 128.
+ */
+DN_API int dn_chunk_fwd_split(const void *q, const void *k, const void *v, const void *beta,
+                              const float *S0, void *o, float *S_T, int B, int H, int T, int dk,
+                              int dv, int C, int dt, int segments, void *workspace,
+                              size_t workspace_bytes, void *stream);
+/* Scratch bytes dn_chunk_fwd_split needs (0 for unsupported arguments): the
+ * tiles of every chunk and three fp32 states per run and head.
+ * With segments = 0 it queries the current device.  Host-only. */
+DN_API size_t dn_chunk_fwd_split_workspace_bytes(int B, int H, int T, int dk, int dv, int C,
+                                                 int dt, int segments);
+
+/*
  * dn_debug_first_wait_ns -- a testing hook for the failure path above, with
  * no counterpart in the method: sets, for the current device, the limit in
  * nanoseconds of the first bounded wait of the tensor-core gradient kernel
@@ -483,7 +514,7 @@ DN_API int dn_recurrent_step_kda_qk(const void *q, const void *k, const void *v,
 /* ABI version of this header (bumped on incompatible changes). */
 DN_API int dn_abi_version(void);
 
-#define DN_ABI_VERSION 5
+#define DN_ABI_VERSION 6
 
 #ifdef __cplusplus
 }

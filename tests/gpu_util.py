@@ -15,10 +15,17 @@ def dev(t):
     return None if t is None else t.to("cuda:0", non_blocking=False).contiguous()
 
 
-def run_chunk(inp, algo="auto", want_state=True):
+def run_chunk(inp, algo="auto", want_state=True, segments=0):
     """Runs the library on ChunkInputs; returns (o, S_T) as fp64 numpy.
     algo "tcgen05-fused" is the tensor-core path without a workspace (one
-    fused kernel); "tcgen05" and "auto" get the workspace (two passes)."""
+    fused kernel); "tcgen05" and "auto" get the workspace (two passes);
+    "split" is dn_chunk_fwd_split with `segments` runs per sequence."""
+    if algo == "split":
+        o, S = dn.chunk_fwd_split(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.beta),
+                                  initial_state=dev(inp.S0), output_final_state=want_state,
+                                  segments=segments)
+        torch.cuda.synchronize()
+        return o.double().cpu().numpy(), (S.double().cpu().numpy() if S is not None else None)
     ws = "auto"
     if algo.endswith("-fused"):
         algo, ws = algo[: -len("-fused")], None

@@ -76,10 +76,11 @@ def test_layer_1p3b_workload_every_head(algo):
     check_every_head(o, S, o_ref, S_ref, TOL[torch.bfloat16], f"1.3B layer {algo}")
 
 
-@pytest.mark.parametrize("algo", ALGOS_BF16)
+@pytest.mark.parametrize("algo", ALGOS_BF16 + ["split"])
 def test_long_prefill_workload_every_head(algo):
     """B1 H16 T32768 d128 bf16 with an fp32 initial state; all 16 heads and
-    all 512 chunks of each."""
+    all 512 chunks of each ("split": the sequence cut into as many runs as
+    fill the GPU once, as the long-prefill benchmark runs it)."""
     inp, (o_ref, S_ref) = _oracle_workload("long_prefill_bf16")
     o, S = run_chunk(inp, algo)
     assert np.isfinite(o).all() and np.isfinite(S).all()

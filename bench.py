@@ -67,9 +67,6 @@ def fp32_alu_tflops(sm_mhz, sms=152, lanes=128):
     return sms * lanes * 2 * sm_mhz * 1e6 / 1e12
 
 
-# Nominal dense tensor rates per GB300 (PFLOP/s): tf32 against bf16.
-TF32_PER_BF16 = 1.1 / 2.25
-
 
 def chunk_bytes(B, H, T, dk, dv, esize, with_s0, with_st):
     """Algorithmic HBM bytes of one chunk forward: q, k, v, beta read, o
@@ -543,21 +540,39 @@ def run_ours(args, rank, world, local):
         lS0 = lp.S0.to(dev)
         lo = torch.empty(Bl, Hl, Tl, dvl, dtype=lq.dtype, device=dev)
         lST = torch.empty(Bl, Hl, dkl, dvl, dtype=torch.float32, device=dev)
-        lneed = lib.dn_chunk_fwd_workspace_bytes(Bl, Hl, Tl, dkl, dvl, wl["C"],
-                                                 1 if lq.dtype == torch.bfloat16 else 0)
+        ldt = 1 if lq.dtype == torch.bfloat16 else 0
+        lneed = lib.dn_chunk_fwd_workspace_bytes(Bl, Hl, Tl, dkl, dvl, wl["C"], ldt)
         lws = torch.empty(lneed, dtype=torch.uint8, device=dev) if lneed else None
+        # The sequence split (dn_chunk_fwd_split) where the tensor cores cover
+        # the shape: each sequence cut into as many runs as fill the GPU once.
+        sneed = lib.dn_chunk_fwd_split_workspace_bytes(Bl, Hl, Tl, dkl, dvl, wl["C"], ldt, 0)
+        lsplit = tc and sneed > 0
+        sws = torch.empty(sneed, dtype=torch.uint8, device=dev) if lsplit else None
+        nchl = (Tl + wl["C"] - 1) // wl["C"]
+        runs = min(max(1, torch.cuda.get_device_properties(dev).multi_processor_count
+                       // (Bl * Hl)), nchl, 1024)
+        runs = -(-nchl // -(-nchl // runs))  # runs of whole chunks, none empty
+        long_launches = (6 if runs > 1 else 2) if lsplit else launches_per_call
 
-        def long_step(_i):
+        def long_plain(_i):
             dn.chunk_fwd(lq, lk, lv, lb, initial_state=lS0, out=lo, final_state=lST, algo=algo,
                          workspace=lws)
+
+        def long_step(_i):
+            if not lsplit:
+                return long_plain(_i)
+            dn.chunk_fwd_split(lq, lk, lv, lb, initial_state=lS0, out=lo, final_state=lST,
+                               segments=0, workspace=sws)
 
         lsteps = max(1, min(args.steps, 10))
         for i in range(min(args.warmup, 3)):
             long_step(i)
+            long_plain(i)
         torch.cuda.synchronize()
         lp_region_s, lp_launch = timed_loop(long_step, lsteps, stream, world)
         lp_region_s = max_over_ranks(lp_region_s, world)
-        del lp, lq, lk, lv, lb, lS0, lo, lST, lws
+        _, lp_plain_launch = timed_loop(long_plain, lsteps, stream, world)
+        del lp, lq, lk, lv, lb, lS0, lo, lST, lws, sws
     clk = clocks.summary()
     del dq, dkk, dvv, db
 
@@ -691,10 +706,12 @@ def run_ours(args, rank, world, local):
     # The backward picks its own path (the tensor-core recompute and chain for bf16,
     # d = 128), whatever --algo says for the forward.
     bwd_tc = _tc_used(lib, dk, dv, q.dtype)
-    if bwd_tc:  # bf16 I/O: the products run as tf32 MMAs (the solve and the rest on CUDA cores)
-        bpeak = peaks["bf16_tflops"] * TF32_PER_BF16
-        bbound, barith = "tensor", "tf32 mma.sync products, fp32 accumulation"
-        bsrc = f"{peak_src} bf16 burst x nominal tf32/bf16 ratio (1.1/2.25)"
+    if bwd_tc:  # bf16 I/O: recompute, chain and gradients on tcgen05 (the solve on CUDA cores)
+        bpeak = peaks["bf16_tflops"]
+        bbound = "tensor"
+        barith = ("tcgen05 bf16 MMAs, fp32 accumulation; states and state gradients "
+                  "carried as bf16 hi/lo tile pairs")
+        bsrc = f"{peak_src} (bf16 dense burst)"
     else:
         bpeak, bbound, barith = fp32_alu_tflops(2070.0), "alu", "fp32 CUDA cores"
         bsrc = "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz"
@@ -755,6 +772,9 @@ def run_ours(args, rank, world, local):
         "workload": LONG, "steps": lsteps, "value": world * Bl * Tl * lsteps / lp_region_s,
         "unit": "tokens/s", "ms_per_step": 1e3 * lp_region_s / lsteps,
         "config": {"B": Bl, "H": Hl, "T": Tl, "dk": dkl, "dv": dvl, "S0": "N(0, 0.1^2) fp32"},
+        "path": (f"dn_chunk_fwd_split: {runs} runs per sequence scanned in parallel, "
+                 "joined through their transitions" if lsplit else "dn_chunk_fwd"),
+        "plain_call_us": 1e3 * statistics.mean(lp_plain_launch),
         "roofline": {"bound": "hbm", "achieved": lbytes / lp_launch_s / 1e9,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": lbytes / lp_launch_s / 1e9 / peaks["hbm_gbs"], "traffic": None,
@@ -888,7 +908,7 @@ def run_ours(args, rank, world, local):
                 "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs},
         "long_prefill": long_prefill,
         "gpu_launches": (launches_per_call * (args.steps + n_sl * e2e_steps)  # chunk fwd, e2e
-                         + launches_per_call * lsteps                   # long prefill
+                         + (long_launches + launches_per_call) * lsteps  # long prefill: split, plain
                          + nsteps + (nsteps if dec_graph[0] else 0)     # decode, graph replay
                          + (4 if bwd_tc else 3) * bwd_steps             # recompute, chain, grads
                          + launches_per_call * vsteps                   # varlen

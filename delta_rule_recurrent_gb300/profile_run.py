@@ -5,6 +5,7 @@
     python -m delta_rule_recurrent_gb300.profile_run bwd [--B 8] [--T 2048] [--reps 2]
     python -m delta_rule_recurrent_gb300.profile_run gated [--B 8] [--T 2048] [--reps 3] [--no-workspace]
     python -m delta_rule_recurrent_gb300.profile_run kda [--B 8] [--T 2048] [--reps 3]
+    python -m delta_rule_recurrent_gb300.profile_run long [--T 32768] [--reps 2] [--segments 0]
 
 `chunk` runs the chunkwise forward on the 1.3B-layer shape (B8 H16 T2048
 dk=dv=128, bf16; B and T can be reduced; the tensor-core path runs in two
@@ -13,8 +14,10 @@ steps on the decode workload's shape (B256 H16 dk=dv=128, fp32 state); `bwd`
 runs the chunkwise backward (dn_chunk_bwd) on the 1.3B-layer shape; `gated`
 runs the Gated DeltaNet chunkwise forward there (keep rates U(0.9, 1); two
 tcgen05 passes, or the CUDA-core kernel with --no-workspace); `kda` runs the
-KDA chunkwise forward there (per-channel keep rates U(0.9, 1)).  Inputs
-come from the seeded generators in `workloads`.
+KDA chunkwise forward there (per-channel keep rates U(0.9, 1)); `long` runs
+the long-prefill shape (B1 H16 T32768, fp32 initial state) through the
+sequence split (dn_chunk_fwd_split; --segments 0 fills the GPU once).
+Inputs come from the seeded generators in `workloads`.
 """
 from __future__ import annotations
 
@@ -32,13 +35,14 @@ def main(argv=None):
     import workloads
 
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("what", choices=["chunk", "decode", "bwd", "gated", "kda"])
+    ap.add_argument("what", choices=["chunk", "decode", "bwd", "gated", "kda", "long"])
     ap.add_argument("--B", type=int, default=None)
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--algo", default="auto", choices=list(dn.ALGOS))
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--steps", type=int, default=4)
     ap.add_argument("--no-workspace", action="store_true")
+    ap.add_argument("--segments", type=int, default=0, help="long: runs per sequence")
     ap.add_argument("--qk-l2norm", action="store_true",
                     help="chunk: raw q, k normalised and scaled inside the kernels")
     a = ap.parse_args(argv)
@@ -67,6 +71,12 @@ def main(argv=None):
         g = workloads.gate_inputs(B, H, T, seed=7, channels=d).to(dev)
         for _ in range(a.reps):
             o, _ = dn.chunk_fwd_kda(q, k, v, b, g)
+    elif a.what == "long":
+        over = {"T": a.T} if a.T is not None else {}
+        inp = workloads.workload_inputs("long_prefill_bf16", **over)
+        q, k, v, b, S0 = (x.to(dev) for x in (inp.q, inp.k, inp.v, inp.beta, inp.S0))
+        for _ in range(a.reps):
+            o, _ = dn.chunk_fwd_split(q, k, v, b, initial_state=S0, segments=a.segments)
     elif a.what == "bwd":
         over = {k: v for k, v in (("B", a.B), ("T", a.T)) if v is not None}
         inp = workloads.workload_inputs("layer1p3b_bf16", **over)

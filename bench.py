@@ -721,7 +721,9 @@ def run_ours(args, rank, world, local):
         "arith": barith, "launches_per_call": 4 if bwd_tc else 3,
         "roofline": {"bound": bbound, "achieved": bflops / bwd_launch_s / 1e12, "peak": bpeak,
                      "unit": "TFLOP/s", "frac": bflops / bwd_launch_s / 1e12 / bpeak,
-                     "traffic": None, "peak_source": bsrc,
+                     "traffic": kernel_traffic("chunk_bwd_grads_tc", "chunk_tc.cu") if bwd_tc else None,
+                     "traffic_kernel": "chunk_bwd_grads_tc (the dominant kernel)" if bwd_tc else None,
+                     "peak_source": bsrc,
                      "flops_per_launch": bflops, "launch_us": bwd_launch_s * 1e6},
         "config": {"d_o": "N(0,1)", "d_S_T": "N(0,0.1^2)", "S0": "none"},
     }

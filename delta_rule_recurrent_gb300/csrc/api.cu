@@ -118,7 +118,7 @@ int dn_debug_first_wait_ns(unsigned long long ns) {
 }
 
 size_t dn_chunk_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt) {
-    if (B <= 0 || H <= 0 || T <= 0 || C != 64 || !dn::chunk_tc_supports(dk, dv, dt)) return 0;
+    if (B <= 0 || H <= 0 || T <= 0 || C != 64 || !dn::chunk_tc_fwd_supports(dk, dv, dt)) return 0;
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return 0;
     const size_t chunks = (size_t)BH * (size_t)((T + 63) / 64);
@@ -235,9 +235,13 @@ int dn_chunk_fwd_qk(const void* q, const void* k, const void* v, const void* bet
     if (workspace && workspace_bytes < need_ws)
         return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed (or pass NULL)",
                     workspace_bytes, need_ws);
-    if (algo == DN_ALGO_TCGEN05 && !dn::chunk_tc_supports(dk, dv, dt))
+    if (algo == DN_ALGO_TCGEN05 && !dn::chunk_tc_fwd_supports(dk, dv, dt))
         return fail(DN_ERR_UNSUPPORTED, "tcgen05 path does not cover dk=%d dv=%d dtype=%d", dk,
                     dv, dt);
+    // the fused tensor-core kernel (no workspace) covers 128-wide heads only
+    const bool fused_ok = dn::chunk_tc_supports(dk, dv, dt);
+    if (algo == DN_ALGO_TCGEN05 && !workspace && !fused_ok && B > 0 && H > 0 && T > 0)
+        return fail(DN_ERR_UNSUPPORTED, "tcgen05 without a workspace covers dk = dv = 128 only");
     if (BH == 0) return ok();
     const ChunkSpans c = chunk_spans(q, k, v, beta, nullptr, 0, 0, S0, o, S_T,
                                      (size_t)BH * (size_t)T, BH, dk, dv, dt);
@@ -247,7 +251,8 @@ int dn_chunk_fwd_qk(const void* q, const void* k, const void* v, const void* bet
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (T == 0) return pass_state_through(S0, S_T, c.state_bytes, st);
     const bool use_tc = algo == DN_ALGO_TCGEN05 ||
-                        (algo == DN_ALGO_AUTO && dn::chunk_tc_supports(dk, dv, dt));
+                        (algo == DN_ALGO_AUTO && dn::chunk_tc_fwd_supports(dk, dv, dt) &&
+                         (workspace || fused_ok));
     void* const ws = (use_tc && workspace && need_ws > 0) ? workspace : nullptr;
     if (ws)
         if (int st2 = check_workspace(c, ws, need_ws, dev)) return st2;

@@ -1142,7 +1142,9 @@ __device__ __forceinline__ void decay_row_tmem(uint32_t taddr, const float* Gs, 
 // kSepB: KDA's decayed operands; [K; Q] are the loaded K . exp G, Q . exp G
 // and tm_ws2 maps the right factor K . exp(-G) (G = [K; Q] (K exp(-G))^T
 // carries every ratio exp(G_i - G_j) inside its sums).
-template <int NMAX, bool kGate, bool kSepB = false>
+// kDIO = 64: heads of 64 features, loaded into the first column half of the
+// 128-wide tile; the second half stays zero.
+template <int NMAX, bool kGate, bool kSepB = false, int kDIO = kD>
 __global__ void __launch_bounds__(kPrepThreads, kSepB ? kPrepCtasPerSmSepB : kPrepCtasPerSm)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_ws, const __nv_bfloat16* __restrict__ beta,
@@ -1152,6 +1154,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                   __nv_bfloat16* __restrict__ xrec) {
     static_assert(!kGate || NMAX == 1, "gating on the batched layout");
     static_assert(!kSepB || (NMAX == 1 && !kGate), "a separate right factor on the batched layout");
+    static_assert(kDIO == kD || (kDIO == 64 && NMAX == 1 && !kGate && !kSepB),
+                  "64-wide heads on the plain batched forward");
     constexpr int kBar = 1, B_TILES = 0, B_MMA = 1, B_END = 2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -1183,6 +1187,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tmem_alloc(smem_addr(tmem_holder), kGate ? 128 : 64);
         tmem_relinquish();
     }
+    if constexpr (kDIO == 64) {  // the tile's second feature half, zero for good
+        for (int i = t; i < (int)(kRegKQ / 16); i += kPrepThreads)
+            st_shared_v4(kq + kRegKQ + 16u * (uint32_t)i, 0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -1192,11 +1201,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     auto load_tiles = [&](int w) {
         const ChunkRef r = prep_item(seqs, w, nchunks, T);
         const uint32_t bar = ctl.bar(B_TILES);
-        mbar_arrive_expect_tx(bar, (kSepB ? 6 : 4) * 8192);
+        mbar_arrive_expect_tx(bar, (kDIO == 64 ? 2 : kSepB ? 6 : 4) * 8192);
         tma_load_3d(kq, &tm_k, bar, 0, r.row0, r.z);
-        tma_load_3d(kq + kRegKQ, &tm_k, bar, 64, r.row0, r.z);
         tma_load_3d(kq + 8192, &tm_q, bar, 0, r.row0, r.z);
-        tma_load_3d(kq + kRegKQ + 8192, &tm_q, bar, 64, r.row0, r.z);
+        if constexpr (kDIO != 64) {
+            tma_load_3d(kq + kRegKQ, &tm_k, bar, 64, r.row0, r.z);
+            tma_load_3d(kq + kRegKQ + 8192, &tm_q, bar, 64, r.row0, r.z);
+        }
         if constexpr (kSepB) {  // the right factor: two 64 x 64 dk halves
             tma_load_3d(kb, &tm_ws2, bar, 0, r.row0, r.z);
             tma_load_3d(kb + 8192, &tm_ws2, bar, 64, r.row0, r.z);
@@ -1558,10 +1569,12 @@ struct Smem {
 // go to the side slot the same way.
 // zero_v: the v buffers hold zeros from the start; each chunk's v barrier
 // is only arrived on.
+// d64: heads of 64 features: only the first 64-column half of each k, q and
+// v tile is loaded; the second halves hold zeros from the start.
 __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q,
                          const CUtensorMap* tm_k, const CUtensorMap* tm_v, const CUtensorMap* tm_ws,
                          const SeqSpan& sp, int nchunks, const CUtensorMap* tm_ws2,
-                         const float* side, const CUtensorMap* tm_kh, bool zero_v) {
+                         const float* side, const CUtensorMap* tm_kh, bool zero_v, bool d64) {
     const int z = sp.z, r0 = sp.row0, w0 = sp.wsbase;
     const int ns = sm.nst, nkqb = 2 * sm.nst;
     int nkq = 0, nv = 0, ntp = 0;
@@ -1572,11 +1585,13 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
             (nkq < ns ||
              mbar_test_wait(ctl.bar(B_KQ_EMPTY + nkq % ns), (uint32_t)(nkq / ns - 1) & 1u))) {
             const uint32_t st = sm.kq(nkq), bar = ctl.bar(B_KQ_FULL + nkq % nkqb);
-            mbar_arrive_expect_tx(bar, (tm_kh ? 6 : 4) * 8192);
+            mbar_arrive_expect_tx(bar, (d64 ? 2 : tm_kh ? 6 : 4) * 8192);
             tma_load_3d(st, tm_k, bar, 0, r0 + nkq * kC, z);
-            tma_load_3d(st + kRegKQ, tm_k, bar, 64, r0 + nkq * kC, z);
             tma_load_3d(st + 8192, tm_q, bar, 0, r0 + nkq * kC, z);
-            tma_load_3d(st + kRegKQ + 8192, tm_q, bar, 64, r0 + nkq * kC, z);
+            if (!d64) {
+                tma_load_3d(st + kRegKQ, tm_k, bar, 64, r0 + nkq * kC, z);
+                tma_load_3d(st + kRegKQ + 8192, tm_q, bar, 64, r0 + nkq * kC, z);
+            }
             if (tm_kh) {  // KDA: the state update's K^ rides with the stage
                 tma_load_3d(sm.kh(nkq), tm_kh, bar, 0, r0 + nkq * kC, z);
                 tma_load_3d(sm.kh(nkq) + 8192, tm_kh, bar, 64, r0 + nkq * kC, z);
@@ -1584,9 +1599,11 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
             if (nkq + ns < nchunks) {  // warm L2 for this stage's next tiles
                 const int y = r0 + (nkq + ns) * kC;
                 tma_prefetch_l2_3d(tm_k, 0, y, z);
-                tma_prefetch_l2_3d(tm_k, 64, y, z);
                 tma_prefetch_l2_3d(tm_q, 0, y, z);
-                tma_prefetch_l2_3d(tm_q, 64, y, z);
+                if (!d64) {
+                    tma_prefetch_l2_3d(tm_k, 64, y, z);
+                    tma_prefetch_l2_3d(tm_q, 64, y, z);
+                }
                 if (tm_kh) {
                     tma_prefetch_l2_3d(tm_kh, 0, y, z);
                     tma_prefetch_l2_3d(tm_kh, 64, y, z);
@@ -1602,12 +1619,12 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
             if (zero_v) {
                 mbar_arrive(bar);
             } else {
-                mbar_arrive_expect_tx(bar, 2 * 8192);
+                mbar_arrive_expect_tx(bar, (d64 ? 1 : 2) * 8192);
                 tma_load_3d(sm.v(nv), tm_v, bar, 0, r0 + nv * kC, z);
-                tma_load_3d(sm.v(nv) + 8192, tm_v, bar, 64, r0 + nv * kC, z);
+                if (!d64) tma_load_3d(sm.v(nv) + 8192, tm_v, bar, 64, r0 + nv * kC, z);
                 if (nv + kVBufs < nchunks) {
                     tma_prefetch_l2_3d(tm_v, 0, r0 + (nv + kVBufs) * kC, z);
-                    tma_prefetch_l2_3d(tm_v, 64, r0 + (nv + kVBufs) * kC, z);
+                    if (!d64) tma_prefetch_l2_3d(tm_v, 64, r0 + (nv + kVBufs) * kC, z);
                 }
             }
             ++nv;
@@ -1730,20 +1747,23 @@ __device__ __forceinline__ void tmem_pack64_cols(uint32_t src, uint32_t dst,
 // kKda: S <- diag(exp G_C) S + K^T U' with K^ = K . exp(G_C - G) from the
 // stage; the 128 per-channel keep factors arrive with [PT; Tm] the same way,
 // are copied to sdec and scale S^T's columns while the D1 MMAs run.
-template <bool kRec, bool kGate, bool kKda = false>
+// kDIO: the heads' width in S0 and S_T ([dk][dv] = kDIO x kDIO; 64 or 128).
+template <bool kRec, bool kGate, bool kKda = false, int kDIO = kD>
 __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                            const float* __restrict__ S0, float* __restrict__ S_T,
                            __nv_bfloat16* __restrict__ S_chunks, int bh, int nchunks,
                            const float* sside, float* sdec) {
     constexpr int kBar = 1;
     const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
-    // S0^T into TMEM: lane t holds dv column t of S0 (zeros without S0).
+    // S0^T into TMEM: lane t holds dv column t of S0 (zeros without S0, and
+    // outside a 64-wide head's block).
 #pragma unroll
     for (int part = 0; part < 4; ++part) {
         uint32_t r[32];
+        const bool in = S0 && t < kDIO && 32 * part < kDIO;
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-            r[e] = S0 ? __float_as_uint(S0[((size_t)bh * kD + 32 * part + e) * kD + t]) : 0u;
+            r[e] = in ? __float_as_uint(S0[((size_t)bh * kDIO + 32 * part + e) * kDIO + t]) : 0u;
         tmem_st32(lane + C_ST + 32u * part, r);
     }
     tmem_wait_st();
@@ -1847,8 +1867,11 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         for (int half = 0; half < 2; ++half) {
             float x[64];
             tmem_ld64f(lane + C_ST + 64u * half, x);
+            if (t < kDIO && 64 * half < kDIO) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) S_T[((size_t)bh * kD + 64 * half + i) * kD + t] = x[i];
+                for (int i = 0; i < 64; ++i)
+                    S_T[((size_t)bh * kDIO + 64 * half + i) * kDIO + t] = x[i];
+            }
         }
     }
 }
@@ -1943,7 +1966,8 @@ __device__ __forceinline__ void issue_vpart(uint32_t tmem, uint32_t v, uint32_t 
 
 // o writer: thread t owns dv column t (TMEM lane t); thread 0 issues the v part.
 __device__ void writer_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
-                            __nv_bfloat16* __restrict__ o, size_t obase, int len, int nchunks) {
+                            __nv_bfloat16* __restrict__ o, size_t obase, int len, int nchunks,
+                            int dio) {
     constexpr int kBar = 3;
     const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
     // v part of chunk cn, once its v tile and [PT; Tm] are in (thread 0).
@@ -1971,11 +1995,11 @@ __device__ void writer_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t
         // D1^T is free once the state has read the U' rows as well.
         if (t == 0) ok = ctl.wait(B_U_READ, (uint32_t)c) && (c + 1 >= nchunks || start(c + 1));
         const int tok0 = c * kC;
-        if (o) {  // (no outputs when only the chunk states are wanted)
-            __nv_bfloat16* const ob = o + (obase + tok0) * kD + t;
+        if (o && t < dio) {  // (no outputs when only the chunk states are wanted)
+            __nv_bfloat16* const ob = o + (obase + tok0) * dio + t;
 #pragma unroll
             for (int r = 0; r < 64; ++r)
-                if (tok0 + r < len) ob[(size_t)r * kD] = __float2bfloat16_rn(ov[r]);
+                if (tok0 + r < len) ob[(size_t)r * dio] = __float2bfloat16_rn(ov[r]);
         }
         if (wg_sync_or(kBar, !ok)) return;
     }
@@ -1991,8 +2015,10 @@ __device__ void writer_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t
 // with each stage), tm_q / tm_k the decayed Q . exp G, K . exp G, and side
 // holds exp G_C per key channel for every chunk.
 // kZeroV: the values are all zero (tm_v is not read): the state's transition
-// alone.
-template <bool kRec, int NMAX, bool kGate = false, bool kKda = false, bool kZeroV = false>
+// alone.  kDIO = 64: heads of 64 features (the maps over 64-column rows),
+// computed as 128-wide tiles whose second halves stay zero.
+template <bool kRec, int NMAX, bool kGate = false, bool kKda = false, bool kZeroV = false,
+          int kDIO = kD>
 __global__ void __launch_bounds__(512, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ws,
@@ -2031,9 +2057,19 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         prefetch_tensormap(&tm_ws);
         if (kGate || kKda) prefetch_tensormap(&tm_ws2);
     }
+    static_assert(kDIO == kD || (kDIO == 64 && !kRec && !kGate && !kKda && NMAX == 1),
+                  "64-wide heads on the plain batched forward");
     if constexpr (kZeroV) {  // the v buffers, zero for good
         for (int i = tid; i < scan::kVBufs * (int)(kTile / 16); i += 512)
             st_shared_v4(sm.v(0) + 16u * (uint32_t)i, 0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
+    if constexpr (kDIO == 64) {  // the second feature halves of the k, q and v tiles, zero for good
+        for (int i = tid; i < sm.nst * (int)(kRegKQ / 16); i += 512)
+            st_shared_v4(sm.kq(i / (int)(kRegKQ / 16)) + kRegKQ + 16u * (uint32_t)(i % (kRegKQ / 16)),
+                         0u, 0u, 0u, 0u);
+        for (int i = tid; i < scan::kVBufs * 512; i += 512)
+            st_shared_v4(sm.v(i / 512) + 8192u + 16u * (uint32_t)(i % 512), 0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
     }
     if (warp == 1) {
@@ -2048,10 +2084,11 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (warp == 0) {
         if (lane == 0)
             scan::producer(ctl, sm, &tm_q, &tm_k, &tm_v, &tm_ws, sp, nchunks,
-                           kGate ? &tm_ws2 : nullptr, cside, kKda ? &tm_ws2 : nullptr, kZeroV);
+                           kGate ? &tm_ws2 : nullptr, cside, kKda ? &tm_ws2 : nullptr, kZeroV,
+                           kDIO == 64);
     } else if (warp >= 4 && warp < 8) {
         const int t = tid - 128;
-        scan::state_body<kRec, kGate, kKda>(ctl, sm, tmem, t, S0, S_T, S_chunks, bh, nchunks, sside,
+        scan::state_body<kRec, kGate, kKda, kDIO>(ctl, sm, tmem, t, S0, S_T, S_chunks, bh, nchunks, sside,
                                       sdec);
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 0);
     } else if (warp >= 8 && warp < 12) {
@@ -2061,7 +2098,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 1);
     } else if (warp >= 12) {
         const int t = tid - 384;
-        scan::writer_body(ctl, sm, tmem, t, o, sp.obase, sp.len, nchunks);
+        scan::writer_body(ctl, sm, tmem, t, o, sp.obase, sp.len, nchunks, kDIO);
         if (t == 0) drain_mmas(ctl, scan::B_DRAIN + 2);
     }
     tc_fence_before_sync();
@@ -2925,11 +2962,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 3-D map over a [BH][T][128] bf16 tensor with 64 x 64 x 1 boxes, 128B swizzle.
-bool make_map(CUtensorMap* map, const void* ptr, int BH, int T) {
+bool make_map(CUtensorMap* map, const void* ptr, int BH, int T, int d = kD) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)T, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)T * kD * 2};
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
     cuuint32_t box[3] = {64, 64, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
@@ -2989,6 +3026,9 @@ int sm_count() {
 }  // namespace
 
 bool chunk_tc_supports(int dk, int dv, int dt) { return dk == kD && dv == kD && dt == 1; }
+bool chunk_tc_fwd_supports(int dk, int dv, int dt) {
+    return dt == 1 && dk == dv && (dk == kD || dk == 64);
+}
 
 size_t chunk_tc_workspace_bytes(int BH, int T) {
     if (BH <= 0 || T <= 0) return 0;
@@ -3003,7 +3043,10 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
                             int dt, void* workspace, cudaStream_t stream, void* S_rec,
                             const QkNorm& norm, void* X_rec) {
     __nv_bfloat16* const S_chunks = static_cast<__nv_bfloat16*>(S_rec);
-    if (!chunk_tc_supports(dk, dv, dt)) return cudaErrorNotSupported;
+    if (!chunk_tc_fwd_supports(dk, dv, dt)) return cudaErrorNotSupported;
+    // 64-wide heads: the two-pass form only, without the backward's records
+    const bool d64 = dk == 64;
+    if (d64 && (!workspace || S_chunks || X_rec)) return cudaErrorNotSupported;
     if (BH <= 0 || T <= 0) return cudaSuccess;
     // Outputs may be skipped (o == nullptr) only on the two-pass path.
     if (!workspace && (!o || S_chunks)) return cudaErrorInvalidValue;
@@ -3011,7 +3054,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
     CUtensorMap mq, mk, mv, mo, mws;
     memset(&mo, 0, sizeof(mo));
     memset(&mws, 0, sizeof(mws));
-    if (!make_map(&mq, q, BH, T) || !make_map(&mk, k, BH, T) || !make_map(&mv, v, BH, T) ||
+    if (!make_map(&mq, q, BH, T, dk) || !make_map(&mk, k, BH, T, dk) ||
+        !make_map(&mv, v, BH, T, dv) ||
         (!workspace && !make_map(&mo, o, BH, T)) ||
         (workspace && !make_ws_map(&mws, workspace, BH, nchunks)))
         return cudaErrorInvalidValue;
@@ -3024,8 +3068,10 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
         float* const side = norm_active(norm)
             ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + (size_t)items * kTile)
             : nullptr;
-        auto prep_kernel = chunk_prep_kernel<1, false>;
-        auto scan_kernel = S_chunks ? chunk_scan_kernel<true, 1> : chunk_scan_kernel<false, 1>;
+        auto prep_kernel = d64 ? chunk_prep_kernel<1, false, false, 64> : chunk_prep_kernel<1, false>;
+        auto scan_kernel = d64        ? chunk_scan_kernel<false, 1, false, false, false, 64>
+                           : S_chunks ? chunk_scan_kernel<true, 1>
+                                      : chunk_scan_kernel<false, 1>;
         if ((err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kPrepSmemBytes)) != cudaSuccess ||
             (err = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -91,6 +91,10 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
 // lo = bf16(S - hi) ([BH][ceil(T/64)][2][dk][dv]), and X_rec, if given, every
 // chunk's (I + A)^{-1} ([BH][ceil(T/64)][64][64] bf16), for the backward.
 bool chunk_tc_supports(int dk, int dv, int dt);
+// The plain forward's tensor-core path also covers 64-wide heads (bf16,
+// dk = dv = 64) in its two-pass form: the tiles keep 128 columns, the second
+// half zero.
+bool chunk_tc_fwd_supports(int dk, int dv, int dt);
 size_t chunk_tc_workspace_bytes(int BH, int T);
 // With prepared inputs (a QkNorm) the two-pass forms also keep the row
 // factors of every chunk after the tiles: this many bytes per chunk.

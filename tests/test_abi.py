@@ -57,9 +57,9 @@ def test_abi_version_and_status_strings(lib):
 
 
 def test_workspace_bytes(lib):
-    """The tensor-core path (bf16, dk = dv = 128, C = 64) asks for one 16 KB
-    [PT; Tm] tile and 1 KB of side vectors per (batch, head, chunk); every
-    other case needs none."""
+    """The tensor-core path (bf16, dk = dv = 128 or 64, C = 64) asks for one
+    16 KB [PT; Tm] tile and 1 KB of side vectors per (batch, head, chunk);
+    every other case needs none."""
     f = lib.dn_chunk_fwd_workspace_bytes
     # one 16 KB [PT; T] tile and 1 KB of row factors (prepared inputs) per chunk
     assert f(8, 16, 2048, 128, 128, 64, 1) == 8 * 16 * 32 * (16384 + 1024)
@@ -68,7 +68,7 @@ def test_workspace_bytes(lib):
     assert f(1, 1, 0, 128, 128, 64, 1) == 0
     assert f(0, 4, 64, 128, 128, 64, 1) == 0
     assert f(8, 16, 2048, 128, 128, 64, 0) == 0  # fp32 I/O
-    assert f(8, 16, 2048, 64, 64, 64, 1) == 0    # d = 64
+    assert f(8, 16, 2048, 64, 64, 64, 1) == 8 * 16 * 32 * (16384 + 1024)  # d = 64, same tiles
     assert f(8, 16, 2048, 128, 64, 64, 1) == 0
     assert f(8, 16, 2048, 128, 128, 32, 1) == 0  # other chunk length
 

@@ -80,9 +80,10 @@ def test_the_chunk_forward_is_bound_by_hbm():
 
 
 def test_traffic_table_entries_name_their_capture():
+    """Each entry names its capture; one scaled from a smaller case says how."""
     table = json.loads((Path(bench.ROOT) / "profiles" / "traffic.json").read_text())
     for name, entry in table.items():
-        assert set(entry) == {"bytes_per_launch", "source_sha", "capture"}, name
+        assert set(entry) - {"scaled"} == {"bytes_per_launch", "source_sha", "capture"}, name
         assert (Path(bench.ROOT) / entry["capture"]).exists(), entry["capture"]
         assert entry["bytes_per_launch"] > 0
 

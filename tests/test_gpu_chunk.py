@@ -46,7 +46,7 @@ def test_tiny_fp32_workload():
     _check(o, S, o_ref, S_ref, torch.float32, "tiny")
 
 
-@pytest.mark.parametrize("algo", ["simt", "auto"])
+@pytest.mark.parametrize("algo", ["simt", "tcgen05", "auto"])
 def test_recall_workload(algo):
     """B4 H4 T1024 d64 bf16 associative recall: oracle parity and the closed
     form (each re-queried key returns its stored value)."""
@@ -112,6 +112,46 @@ def test_tensor_core_path_ragged(T, with_s0, algo):
     o, S = run_chunk(inp, algo)
     o_ref, S_ref = oracle.forward(inp.q, inp.k, inp.v, inp.beta, inp.S0)
     _check(o, S, o_ref, S_ref, torch.bfloat16, f"{algo} T{T}")
+
+
+@pytest.mark.parametrize("T", [1, 37, 64, 65, 200, 1000])
+@pytest.mark.parametrize("with_s0", [False, True])
+def test_tensor_core_path_64_wide_heads(T, with_s0):
+    """dk = dv = 64 on the two-pass tcgen05 path (128-wide tiles whose second
+    halves stay zero): ragged lengths, with and without a carried state, and
+    the inputs prepared inside the kernels."""
+    inp = workloads.chunk_inputs(3, 2, T, 64, 64, dtype="bf16", seed=300 + T,
+                                 feature_map="silu", s0_std=0.2 if with_s0 else None)
+    o, S = run_chunk(inp, "tcgen05")
+    o_ref, S_ref = oracle.forward(inp.q, inp.k, inp.v, inp.beta, inp.S0)
+    _check(o, S, o_ref, S_ref, torch.bfloat16, f"d64 T{T}")
+    raw = workloads.chunk_inputs(3, 2, T, 64, 64, dtype="bf16", seed=300 + T,
+                                 feature_map="silu", s0_std=0.2 if with_s0 else None,
+                                 normalize=False)
+    import delta_rule_recurrent_gb300 as dn
+    o2, S2 = dn.chunk_fwd(dev(raw.q), dev(raw.k), dev(raw.v), dev(raw.beta),
+                          initial_state=dev(raw.S0), algo="tcgen05", qk_l2norm=True,
+                          scale=0.125)
+    torch.cuda.synchronize()
+    qp, kp = oracle.prepare_qk(raw.q, raw.k, scale=0.125, l2norm=True)
+    o_ref2, S_ref2 = oracle.forward(qp, kp, raw.v, raw.beta, raw.S0)
+    _check(o2.double().cpu().numpy(), S2.double().cpu().numpy(), o_ref2, S_ref2,
+           torch.bfloat16, f"d64 prepared T{T}")
+
+
+def test_64_wide_heads_need_a_workspace_on_tensor_cores():
+    """The fused tensor-core kernel covers 128-wide heads only: tcgen05 without
+    a workspace is refused at d = 64, and auto falls back to the CUDA cores."""
+    import delta_rule_recurrent_gb300 as dn
+    inp = workloads.chunk_inputs(1, 2, 100, 64, 64, dtype="bf16", seed=5, s0_std=0.1)
+    args = [dev(x) for x in (inp.q, inp.k, inp.v, inp.beta)]
+    with pytest.raises(dn.DeltaNetError, match="UNSUPPORTED"):
+        dn.chunk_fwd(*args, algo="tcgen05", workspace=None)
+    o, S = dn.chunk_fwd(*args, initial_state=dev(inp.S0), algo="auto", workspace=None)
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.forward(inp.q, inp.k, inp.v, inp.beta, inp.S0)
+    _check(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref, torch.bfloat16,
+           "d64 auto without workspace")
 
 
 def test_split_and_fused_agree():

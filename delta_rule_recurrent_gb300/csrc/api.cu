@@ -681,29 +681,16 @@ size_t dn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, 
     return dn::chunk_bwd_workspace_bytes((int)BH, T, dk, dv, dt);
 }
 
-int dn_chunk_bwd(const void* q, const void* k, const void* v, const void* beta, const float* S0,
-                 const void* d_o, const float* d_S_T, void* d_q, void* d_k, void* d_v,
-                 void* d_beta, float* d_S0, int B, int H, int T, int dk, int dv, int C, int dt,
-                 void* workspace, size_t workspace_bytes, void* stream) {
-    if (B < 0 || H < 0 || T < 0)
-        return fail(DN_ERR_INVALID_ARG, "negative size (B=%d H=%d T=%d)", B, H, T);
-    if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
-    if (dk <= 0 || dv <= 0 || C <= 0)
-        return fail(DN_ERR_INVALID_ARG, "dk, dv and C must be positive");
-    if (!supported_dim(dk) || !supported_dim(dv))
-        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this library supports 64 and 128", dk, dv);
-    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this library supports 64", C);
-    const long long BH = (long long)B * H;
-    if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
-    const size_t need_ws = dn_chunk_bwd_workspace_bytes(B, H, T, dk, dv, C, dt);
-    if (workspace_bytes < need_ws || (need_ws > 0 && !workspace))
-        return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
-                    need_ws);
-    if (BH == 0) return ok();
-
+// The backward's pointer checks: ntok tokens of q, k, v, beta, d_o and their
+// gradients, nstate states of S0, d_S_T, d_S0, and the workspace; outputs
+// overlap no input and no other output.  T == 0 checks the states alone.
+static int check_bwd_spans(const void* q, const void* k, const void* v, const void* beta,
+                           const float* S0, const void* d_o, const float* d_S_T, void* d_q,
+                           void* d_k, void* d_v, void* d_beta, float* d_S0, size_t ntok,
+                           long long nstate, int T, int dk, int dv, int dt, void* workspace,
+                           size_t need_ws) {
     const size_t es = elem_size(dt);
-    const size_t ntok = (size_t)BH * (size_t)T;
-    const size_t state_bytes = (size_t)BH * dk * dv * sizeof(float);
+    const size_t state_bytes = (size_t)nstate * dk * dv * sizeof(float);
     const Span sq{"q", q, ntok * dk * es}, sk{"k", k, ntok * dk * es}, sv{"v", v, ntok * dv * es},
         sb{"beta", beta, ntok * es}, s0{"S0", S0, state_bytes}, sdo{"d_o", d_o, ntok * dv * es},
         sdT{"d_S_T", d_S_T, state_bytes}, sdq{"d_q", d_q, ntok * dk * es},
@@ -733,7 +720,38 @@ int dn_chunk_bwd(const void* q, const void* k, const void* v, const void* beta, 
             if (o2 != o && (T > 0 || o2 == &sd0) && overlaps(*o, *o2))
                 return fail(DN_ERR_INVALID_ARG, "%s overlaps %s", o->name, o2->name);
     }
+    return DN_OK;
+}
 
+// Shape and dtype checks shared by the backward entry points (n: B or N).
+static int check_bwd_sizes(int n, int H, int T, int dk, int dv, int C, int dt, const char* nn) {
+    if (n < 0 || H < 0 || T < 0)
+        return fail(DN_ERR_INVALID_ARG, "negative size (%s=%d H=%d T=%d)", nn, n, H, T);
+    if (dt != DN_F32 && dt != DN_BF16) return fail(DN_ERR_INVALID_ARG, "unknown dtype %d", dt);
+    if (dk <= 0 || dv <= 0 || C <= 0)
+        return fail(DN_ERR_INVALID_ARG, "dk, dv and C must be positive");
+    if (!supported_dim(dk) || !supported_dim(dv))
+        return fail(DN_ERR_UNSUPPORTED, "dk=%d dv=%d: this library supports 64 and 128", dk, dv);
+    if (C != 64) return fail(DN_ERR_UNSUPPORTED, "chunk length C=%d: this library supports 64", C);
+    return DN_OK;
+}
+
+int dn_chunk_bwd(const void* q, const void* k, const void* v, const void* beta, const float* S0,
+                 const void* d_o, const float* d_S_T, void* d_q, void* d_k, void* d_v,
+                 void* d_beta, float* d_S0, int B, int H, int T, int dk, int dv, int C, int dt,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+    if (int st = check_bwd_sizes(B, H, T, dk, dv, C, dt, "B")) return st;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
+    const size_t need_ws = dn_chunk_bwd_workspace_bytes(B, H, T, dk, dv, C, dt);
+    if (workspace_bytes < need_ws || (need_ws > 0 && !workspace))
+        return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                    need_ws);
+    if (BH == 0) return ok();
+    if (int st = check_bwd_spans(q, k, v, beta, S0, d_o, d_S_T, d_q, d_k, d_v, d_beta, d_S0,
+                                 (size_t)BH * (size_t)T, BH, T, dk, dv, dt, workspace, need_ws))
+        return st;
+    const size_t state_bytes = (size_t)BH * dk * dv * sizeof(float);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (T == 0) {  // the state passes through unchanged
         if (!d_S0) return ok();
@@ -749,6 +767,52 @@ int dn_chunk_bwd(const void* q, const void* k, const void* v, const void* beta, 
                                                st, &stage);
     if (e == cudaSuccess) return ok();
     return fail(DN_ERR_CUDA, "chunk backward (%s): %s", stage, cudaGetErrorString(e));
+}
+
+size_t dn_chunk_bwd_varlen_workspace_bytes(const int* cu_seqlens, int N, int H, int dk, int dv,
+                                           int C, int dt) {
+    if (!cu_seqlens || N <= 0 || N > dn::kMaxVarlenSeqs || H <= 0 || C != 64 ||
+        !supported_dim(dk) || !supported_dim(dv) || (dt != DN_F32 && dt != DN_BF16))
+        return 0;
+    for (int i = 0; i < N; ++i)
+        if (cu_seqlens[i + 1] < cu_seqlens[i]) return 0;
+    return dn::chunk_bwd_varlen_workspace_bytes(cu_seqlens, N, H, dk, dv, dt);
+}
+
+int dn_chunk_bwd_varlen(const void* q, const void* k, const void* v, const void* beta,
+                        const float* S0, const void* d_o, const float* d_S_T, void* d_q,
+                        void* d_k, void* d_v, void* d_beta, float* d_S0, const int* cu_seqlens,
+                        int N, int H, int T, int dk, int dv, int C, int dt, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    if (int st = check_bwd_sizes(N, H, T, dk, dv, C, dt, "N")) return st;
+    static thread_local dn::VarlenTable tab;
+    if (int st = varlen_table(cu_seqlens, N, T, &tab)) return st;
+    if ((long long)N * H == 0) return ok();
+    const size_t need_ws =
+        dn_chunk_bwd_varlen_workspace_bytes(cu_seqlens, N, H, dk, dv, C, dt);
+    if (workspace_bytes < need_ws || (need_ws > 0 && !workspace))
+        return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                    need_ws);
+    if (int st = check_bwd_spans(q, k, v, beta, S0, d_o, d_S_T, d_q, d_k, d_v, d_beta, d_S0,
+                                 (size_t)H * (size_t)T, (long long)N * H, T, dk, dv, dt,
+                                 workspace, need_ws))
+        return st;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t state_bytes = (size_t)N * H * dk * dv * sizeof(float);
+    if (T == 0) {  // every sequence is empty: the state gradient passes through
+        if (!d_S0) return ok();
+        if (d_S_T)
+            return cuda_status(
+                cudaMemcpyAsync(d_S0, d_S_T, state_bytes, cudaMemcpyDeviceToDevice, st),
+                "cudaMemcpyAsync(d_S0 <- d_S_T)");
+        return cuda_status(cudaMemsetAsync(d_S0, 0, state_bytes, st), "cudaMemsetAsync(d_S0)");
+    }
+    const char* stage = "launch";
+    const cudaError_t e = dn::launch_chunk_bwd_varlen(q, k, v, beta, S0, d_o, d_S_T, d_q, d_k, d_v,
+                                                      d_beta, d_S0, cu_seqlens, N, H, T, dk, dv,
+                                                      dt, workspace, st, &stage);
+    if (e == cudaSuccess) return ok();
+    return fail(DN_ERR_CUDA, "varlen chunk backward (%s): %s", stage, cudaGetErrorString(e));
 }
 
 }  // extern "C"

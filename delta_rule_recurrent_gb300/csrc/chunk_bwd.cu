@@ -30,6 +30,7 @@
 // The products run as fp32 FMA for fp32 I/O (held to 1e-4) and as warp-level
 // tf32 tensor-core MMAs for bf16 I/O (simt_mm.cuh); the triangular solve is
 // fp32 on CUDA cores in both.
+#include <algorithm>
 #include <type_traits>
 
 #include "dn_common.cuh"
@@ -459,6 +460,99 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
                                       Gc, BH, T, dk, dv, nullptr, stream);
     return launch_bwd_dims<__nv_bfloat16>(q, k, v, beta, d_o, d_S_T, d_q, d_k, d_v, d_beta, d_S0,
                                           Sc, Gc, BH, T, dk, dv, nullptr, stream);
+}
+
+// ------------------------------------------------- packed variable-length sequences
+// The backward of dn_chunk_fwd_varlen: sequence n is tokens cu[n] .. cu[n+1]-1
+// of the packed [H][T][d] tensors.  Each sequence runs as its own batched
+// backward (B = 1, H heads, its length) on contiguous copies: its rows of q,
+// k, v, beta and d_o are gathered with one strided copy per tensor (H rows of
+// len * d elements, T * d apart), and its gradients scattered back the same
+// way.  The copies and the launches of one sequence queue on the stream
+// behind the previous sequence's, so one set of scratch buffers serves all.
+namespace {
+constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+struct VarlenBwdScratch {
+    size_t ws, q, v, b;  // bytes: the batched backward's workspace, a dk tensor, a dv tensor, beta
+};
+VarlenBwdScratch varlen_bwd_scratch(int H, int lmax, int dk, int dv, int dt) {
+    const size_t es = dt ? 2 : 4, rows = (size_t)H * (size_t)lmax;
+    return {align256(chunk_bwd_workspace_bytes(H, lmax, dk, dv, dt)), align256(rows * dk * es),
+            align256(rows * dv * es), align256(rows * es)};
+}
+int varlen_max_len(const int* cu, int N) {
+    int lmax = 0;
+    for (int n = 0; n < N; ++n) lmax = std::max(lmax, cu[n + 1] - cu[n]);
+    return lmax;
+}
+}  // namespace
+
+size_t chunk_bwd_varlen_workspace_bytes(const int* cu, int N, int H, int dk, int dv, int dt) {
+    if (!cu || N <= 0 || H <= 0) return 0;
+    const int lmax = varlen_max_len(cu, N);
+    if (lmax <= 0) return 0;
+    const VarlenBwdScratch s = varlen_bwd_scratch(H, lmax, dk, dv, dt);
+    // inputs q, k, v, d_o, beta; gradients d_q, d_k, d_v, d_beta
+    return s.ws + 4 * s.q + 3 * s.v + 2 * s.b;
+}
+
+cudaError_t launch_chunk_bwd_varlen(const void* q, const void* k, const void* v, const void* beta,
+                                    const float* S0, const void* d_o, const float* d_S_T,
+                                    void* d_q, void* d_k, void* d_v, void* d_beta, float* d_S0,
+                                    const int* cu, int N, int H, int T, int dk, int dv, int dt,
+                                    void* workspace, cudaStream_t stream, const char** stage) {
+    const int lmax = varlen_max_len(cu, N);
+    const VarlenBwdScratch s = varlen_bwd_scratch(H, std::max(lmax, 1), dk, dv, dt);
+    uint8_t* p = static_cast<uint8_t*>(workspace);
+    void* const ws = p;
+    p += s.ws;
+    uint8_t *tq = p, *tk = p + s.q, *tdq = p + 2 * s.q, *tdk = p + 3 * s.q;
+    p += 4 * s.q;
+    uint8_t *tv = p, *tdo = p + s.v, *tdv = p + 2 * s.v;
+    p += 3 * s.v;
+    uint8_t *tb = p, *tdb = p + s.b;
+    const size_t es = dt ? 2 : 4, state = (size_t)H * dk * dv;
+    cudaError_t e = cudaSuccess;
+    // H rows of `width` bytes, `pitch` bytes apart on the packed side
+    auto gather = [&](void* dst, const void* src, size_t tok0, int len, int d) {
+        const size_t w = (size_t)len * d * es;
+        return cudaMemcpy2DAsync(dst, w, static_cast<const uint8_t*>(src) + tok0 * d * es,
+                                 (size_t)T * d * es, w, (size_t)H, cudaMemcpyDeviceToDevice, stream);
+    };
+    auto scatter = [&](void* dst, const void* src, size_t tok0, int len, int d) {
+        const size_t w = (size_t)len * d * es;
+        return cudaMemcpy2DAsync(static_cast<uint8_t*>(dst) + tok0 * d * es, (size_t)T * d * es,
+                                 src, w, w, (size_t)H, cudaMemcpyDeviceToDevice, stream);
+    };
+    for (int n = 0; n < N && e == cudaSuccess; ++n) {
+        const int a = cu[n], len = cu[n + 1] - cu[n];
+        const float* const s0 = S0 ? S0 + (size_t)n * state : nullptr;
+        const float* const dst = d_S_T ? d_S_T + (size_t)n * state : nullptr;
+        float* const ds0 = d_S0 ? d_S0 + (size_t)n * state : nullptr;
+        if (len == 0) {  // the state gradient passes through
+            *stage = "empty sequence";
+            if (ds0)
+                e = dst ? cudaMemcpyAsync(ds0, dst, state * sizeof(float), cudaMemcpyDeviceToDevice,
+                                          stream)
+                        : cudaMemsetAsync(ds0, 0, state * sizeof(float), stream);
+            continue;
+        }
+        *stage = "gathering a sequence";
+        if ((e = gather(tq, q, a, len, dk)) != cudaSuccess || (e = gather(tk, k, a, len, dk)) != cudaSuccess ||
+            (e = gather(tv, v, a, len, dv)) != cudaSuccess || (e = gather(tdo, d_o, a, len, dv)) != cudaSuccess ||
+            (e = gather(tb, beta, a, len, 1)) != cudaSuccess)
+            break;
+        if ((e = launch_chunk_bwd(tq, tk, tv, tb, s0, tdo, dst, tdq, tdk, tdv, tdb, ds0, H, len, dk,
+                                  dv, dt, ws, stream, stage)) != cudaSuccess)
+            break;
+        *stage = "scattering a sequence";
+        if ((e = scatter(d_q, tdq, a, len, dk)) != cudaSuccess ||
+            (e = scatter(d_k, tdk, a, len, dk)) != cudaSuccess ||
+            (e = scatter(d_v, tdv, a, len, dv)) != cudaSuccess ||
+            (e = scatter(d_beta, tdb, a, len, 1)) != cudaSuccess)
+            break;
+    }
+    return e;
 }
 
 }  // namespace dn

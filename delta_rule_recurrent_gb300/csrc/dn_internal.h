@@ -81,6 +81,16 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
                              int dk, int dv, int dt, void* workspace, cudaStream_t stream,
                              const char** stage);
 
+// The backward of the packed-sequence forward (cu: N + 1 host offsets into
+// the [H][T][d] tensors; states [N][H][dk][dv]): one batched backward per
+// sequence on gathered copies, in the scratch this many bytes hold.
+size_t chunk_bwd_varlen_workspace_bytes(const int* cu, int N, int H, int dk, int dv, int dt);
+cudaError_t launch_chunk_bwd_varlen(const void* q, const void* k, const void* v, const void* beta,
+                                    const float* S0, const void* d_o, const float* d_S_T,
+                                    void* d_q, void* d_k, void* d_v, void* d_beta, float* d_S0,
+                                    const int* cu, int N, int H, int T, int dk, int dv, int dt,
+                                    void* workspace, cudaStream_t stream, const char** stage);
+
 // Chunkwise forward on tcgen05 tensor cores.  Returns cudaErrorNotSupported
 // (without launching) for shapes or dtypes it does not cover.  With a
 // workspace of chunk_tc_workspace_bytes(BH, T) bytes (16-byte aligned) it runs

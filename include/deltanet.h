@@ -368,6 +368,32 @@ DN_API size_t dn_chunk_fwd_varlen_workspace_bytes(const int *cu_seqlens, int N, 
                                            int dk, int dv, int C, int dt);
 
 /*
+ * dn_chunk_bwd_varlen -- the gradients of dn_chunk_fwd_varlen's outputs, as
+ * dn_chunk_bwd gives them for the batched forward (the pages' backward with
+ * the states recomputed: "Hardware-efficient implementation",
+ * paperlayer.ai/abs/2406.06484v6), for N sequences packed along T.
+ *   q, k, d_q, d_k  [H, T, dk];  v, d_o, d_v  [H, T, dv];  beta, d_beta [H, T]
+ *   S0, d_S_T, d_S0 [N, H, dk, dv] fp32 (NULL: zero / not wanted)
+ *   cu_seqlens      host array of N + 1 ints, 0 = cu[0] <= ... <= cu[N] = T
+ *   workspace       device scratch of dn_chunk_bwd_varlen_workspace_bytes(...)
+ *                   bytes, 16-byte aligned.
+ * Each sequence runs as its own batched backward on copies of its rows
+ * gathered into the workspace, its gradients scattered back; an empty
+ * sequence passes d_S_T through to d_S0.  Errors and overlap rules as
+ * dn_chunk_bwd.
+ */
+DN_API int dn_chunk_bwd_varlen(const void *q, const void *k, const void *v, const void *beta,
+                               const float *S0, const void *d_o, const float *d_S_T, void *d_q,
+                               void *d_k, void *d_v, void *d_beta, float *d_S0,
+                               const int *cu_seqlens, int N, int H, int T, int dk, int dv, int C,
+                               int dt, void *workspace, size_t workspace_bytes, void *stream);
+/* Its scratch: the batched backward's for the longest sequence plus the
+ * gathered rows and gradients of one sequence (0 for invalid arguments).
+ * Host-only. */
+DN_API size_t dn_chunk_bwd_varlen_workspace_bytes(const int *cu_seqlens, int N, int H, int dk,
+                                                  int dv, int C, int dt);
+
+/*
  * dn_chunk_fwd_kda / dn_recurrent_step_kda -- Kimi Delta Attention: one keep
  * rate per key channel, D_t = Diag(exp(g_t)), decays the state's key
  * channels before the delta rule ("Kimi Delta Attention : atténuation par
@@ -514,7 +540,7 @@ DN_API int dn_recurrent_step_kda_qk(const void *q, const void *k, const void *v,
 /* ABI version of this header (bumped on incompatible changes). */
 DN_API int dn_abi_version(void);
 
-#define DN_ABI_VERSION 6
+#define DN_ABI_VERSION 7
 
 #ifdef __cplusplus
 }

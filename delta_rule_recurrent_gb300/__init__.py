@@ -36,7 +36,7 @@ import ctypes
 from ._lib import (DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05, DN_BF16, DN_F32,
                    DeltaNetError, QkNorm, check, header_symbols, lib_path, load)
 
-__all__ = ["chunk_fwd", "chunk_fwd_split", "chunk_bwd", "chunk_bwd_varlen", "recurrent_step", "chunk_fwd_varlen", "chunk_fwd_gated",
+__all__ = ["chunk_fwd", "chunk_fwd_split", "chunk_bwd", "chunk_bwd_varlen", "chunk_bwd_gated", "recurrent_step", "chunk_fwd_varlen", "chunk_fwd_gated",
            "recurrent_step_gated", "chunk_fwd_kda", "recurrent_step_kda", "qk_prepare",
            "qk_prepare_bwd", "DeltaRule", "DeltaNetError", "load", "lib_path",
            "header_symbols", "ALGOS"]
@@ -547,6 +547,54 @@ def chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
             ws.data_ptr() if ws is not None else None, ws_bytes, _stream_handle(dev),
             _norm(scale, qk_l2norm)))
     return out, S_T
+
+
+def chunk_bwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                    g: torch.Tensor, d_o: torch.Tensor, initial_state: torch.Tensor | None = None,
+                    d_final_state: torch.Tensor | None = None, chunk_size: int = 64,
+                    workspace: torch.Tensor | None = None):
+    """Gradients of ``chunk_fwd_gated`` (``dn_chunk_bwd_gated``).
+
+    ``g``: fp32 ``[B, H, T]`` log keep rates.  Returns ``(d_q, d_k, d_v,
+    d_beta, d_g, d_initial_state)`` for L = <d_o, o> + <d_final_state,
+    final_state>; ``d_g`` fp32 like ``g``.
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g), ("d_o", d_o)):
+        _check_cuda(name, t, dev)
+    dt = _dtype_code(q)
+    if not (k.dtype == v.dtype == beta.dtype == d_o.dtype == q.dtype):
+        raise TypeError("q, k, v, beta and d_o must share one dtype")
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or d_o.shape != v.shape:
+        raise ValueError("q, k must be [B,H,T,dk]; v and d_o [B,H,T,dv]")
+    B, H, T, dk = q.shape
+    dv = v.shape[3]
+    if tuple(v.shape[:3]) != (B, H, T) or tuple(beta.shape) != (B, H, T):
+        raise ValueError("v must be [B,H,T,dv] and beta [B,H,T]")
+    if g.dtype != torch.float32 or tuple(g.shape) != (B, H, T):
+        raise ValueError("g must be float32 [B,H,T]")
+    for name, t in (("initial_state", initial_state), ("d_final_state", d_final_state)):
+        if t is not None:
+            _check_cuda(name, t, dev)
+            if t.dtype != torch.float32 or tuple(t.shape) != (B, H, dk, dv):
+                raise ValueError(f"{name} must be float32 [B,H,dk,dv]")
+    lib = load()
+    need = lib.dn_chunk_bwd_gated_workspace_bytes(B, H, T, dk, dv, chunk_size, dt)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _check_cuda("workspace", workspace, dev)
+    grads = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+             torch.empty_like(beta), torch.empty_like(g),
+             torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)]
+    with torch.cuda.device(dev):
+        check(lib.dn_chunk_bwd_gated(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(), g.data_ptr(),
+            initial_state.data_ptr() if initial_state is not None else None, d_o.data_ptr(),
+            d_final_state.data_ptr() if d_final_state is not None else None,
+            *(x.data_ptr() for x in grads), B, H, T, dk, dv, chunk_size, dt,
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            _stream_handle(dev)))
+    return tuple(grads)
 
 
 def chunk_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,

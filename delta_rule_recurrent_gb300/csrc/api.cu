@@ -769,6 +769,69 @@ int dn_chunk_bwd(const void* q, const void* k, const void* v, const void* beta, 
     return fail(DN_ERR_CUDA, "chunk backward (%s): %s", stage, cudaGetErrorString(e));
 }
 
+size_t dn_chunk_bwd_gated_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt) {
+    if (B <= 0 || H <= 0 || T <= 0 || C != 64 || !supported_dim(dk) || !supported_dim(dv) ||
+        (dt != DN_F32 && dt != DN_BF16))
+        return 0;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return 0;
+    return dn::chunk_bwd_gated_workspace_bytes((int)BH, T, dk, dv);
+}
+
+int dn_chunk_bwd_gated(const void* q, const void* k, const void* v, const void* beta,
+                       const float* g, const float* S0, const void* d_o, const float* d_S_T,
+                       void* d_q, void* d_k, void* d_v, void* d_beta, float* d_g, float* d_S0,
+                       int B, int H, int T, int dk, int dv, int C, int dt, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    if (int st = check_bwd_sizes(B, H, T, dk, dv, C, dt, "B")) return st;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
+    const size_t need_ws = dn_chunk_bwd_gated_workspace_bytes(B, H, T, dk, dv, C, dt);
+    if (workspace_bytes < need_ws || (need_ws > 0 && !workspace))
+        return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                    need_ws);
+    if (BH == 0) return ok();
+    const size_t ntok = (size_t)BH * (size_t)T;
+    if (int st = check_bwd_spans(q, k, v, beta, S0, d_o, d_S_T, d_q, d_k, d_v, d_beta, d_S0,
+                                 ntok, BH, T, dk, dv, dt, workspace, need_ws))
+        return st;
+    if (T > 0) {  // the log keep rates and their gradient: fp32 [B, H, T]
+        int dev = 0;
+        if (int st = current_device(&dev)) return st;
+        const Span sg{"g", g, ntok * sizeof(float)}, sdg{"d_g", d_g, ntok * sizeof(float)};
+        if (int st = check_device_ptr(sg, 4, dev)) return st;
+        if (int st = check_device_ptr(sdg, 4, dev)) return st;
+        const size_t es = elem_size(dt), sb = (size_t)BH * dk * dv * sizeof(float);
+        const Span others[] = {{"q", q, ntok * dk * es},     {"k", k, ntok * dk * es},
+                               {"v", v, ntok * dv * es},     {"beta", beta, ntok * es},
+                               {"S0", S0, sb},               {"d_o", d_o, ntok * dv * es},
+                               {"d_S_T", d_S_T, sb},         {"d_q", d_q, ntok * dk * es},
+                               {"d_k", d_k, ntok * dk * es}, {"d_v", d_v, ntok * dv * es},
+                               {"d_beta", d_beta, ntok * es}, {"d_S0", d_S0, sb},
+                               {"workspace", workspace, need_ws}, {"g", g, ntok * sizeof(float)}};
+        for (const Span& s : others)
+            if (overlaps(sdg, s)) return fail(DN_ERR_INVALID_ARG, "d_g overlaps %s", s.name);
+        for (int i = 7; i < 13; ++i)  // the outputs and the workspace against g
+            if (overlaps(others[i], sg))
+                return fail(DN_ERR_INVALID_ARG, "%s overlaps g", others[i].name);
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {  // the state gradient passes through
+        const size_t sb = (size_t)BH * dk * dv * sizeof(float);
+        if (!d_S0) return ok();
+        if (d_S_T)
+            return cuda_status(cudaMemcpyAsync(d_S0, d_S_T, sb, cudaMemcpyDeviceToDevice, st),
+                               "cudaMemcpyAsync(d_S0 <- d_S_T)");
+        return cuda_status(cudaMemsetAsync(d_S0, 0, sb, st), "cudaMemsetAsync(d_S0)");
+    }
+    const char* stage = "launch";
+    const cudaError_t e = dn::launch_chunk_bwd_gated(q, k, v, beta, g, S0, d_o, d_S_T, d_q, d_k,
+                                                     d_v, d_beta, d_g, d_S0, (int)BH, T, dk, dv,
+                                                     dt, workspace, st, &stage);
+    if (e == cudaSuccess) return ok();
+    return fail(DN_ERR_CUDA, "gated chunk backward (%s): %s", stage, cudaGetErrorString(e));
+}
+
 size_t dn_chunk_bwd_varlen_workspace_bytes(const int* cu_seqlens, int N, int H, int dk, int dv,
                                            int C, int dt) {
     if (!cu_seqlens || N <= 0 || N > dn::kMaxVarlenSeqs || H <= 0 || C != 64 ||

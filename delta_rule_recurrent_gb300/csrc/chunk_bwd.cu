@@ -73,6 +73,52 @@ __device__ __forceinline__ void form_a_p(const float* Ks, const float* Qs, const
     Ops::for_each(ap, [&](int m, int nn, float x) { Pm[m * kLC + nn] = nn <= m ? x : 0.f; });
 }
 
+// Gated DeltaNet: the chunk's decay from its log keep rates g (fp32, 0 past
+// the end): Gl[t] = sum_{u <= t} g_u (thread t < 64 sums its own prefix),
+// gam[t] = exp Gl[t] and rg[t] = Gamma / gam[t], Gamma = gam[63] (the padded
+// tokens keep everything, so it is the decay through the last real token).
+// Ends without a barrier.
+__device__ __forceinline__ void chunk_decay(const float* __restrict__ g, size_t tok, int n,
+                                            float* gs, float* Gl, float* gam, float* rg, int tid) {
+    if (tid < kC) gs[tid] = tid < n ? g[tok + tid] : 0.f;
+    __syncthreads();
+    if (tid < kC) {
+        float s = 0.f;
+        for (int u = 0; u <= tid; ++u) s += gs[u];
+        Gl[tid] = s;
+    }
+    __syncthreads();
+    if (tid < kC) {
+        gam[tid] = expf(Gl[tid]);
+        rg[tid] = expf(Gl[kC - 1] - Gl[tid]);
+    }
+}
+// exp(G_i - G_j) for j <= i (at most 1), 0 above the diagonal
+__device__ __forceinline__ float decay_ratio(const float* Gl, int i, int j) {
+    return j <= i ? expf(Gl[i] - Gl[j]) : 0.f;
+}
+
+// A = tril(diag(beta) (K K^T o D), -1) and P = tril(Q K^T o D) with the
+// decay ratios D_ij = exp(G_i - G_j); (K K^T o D) itself too when KK is given.
+template <class Ops, int DK>
+__device__ __forceinline__ void form_a_p_gated(const float* Ks, const float* Qs, const float* bs,
+                                               const float* Gl, float* Am, float* Pm, float* KK) {
+    constexpr int LK = DK + Ops::kPad, kLC = kC + Ops::kPad;
+    typename Ops::template Acc<64, 64> aa, ap;
+    Ops::zero(aa);
+    Ops::zero(ap);
+    Ops::template mm<64, 64, DK>(aa, [&](int m, int i) { return Ks[m * LK + i]; },
+                                 [&](int i, int nn) { return Ks[nn * LK + i]; });
+    Ops::template mm<64, 64, DK>(ap, [&](int m, int i) { return Qs[m * LK + i]; },
+                                 [&](int i, int nn) { return Ks[nn * LK + i]; });
+    Ops::for_each(aa, [&](int m, int nn, float x) {
+        const float y = x * decay_ratio(Gl, m, nn);
+        Am[m * kLC + nn] = nn < m ? bs[m] * y : 0.f;
+        if (KK) KK[m * kLC + nn] = y;
+    });
+    Ops::for_each(ap, [&](int m, int nn, float x) { Pm[m * kLC + nn] = x * decay_ratio(Gl, m, nn); });
+}
+
 // ------------------------------------------------------------------ chain
 template <int DK, int NV, int PAD>
 struct ChainSmem {
@@ -88,7 +134,8 @@ struct ChainSmem {
     static constexpr int kP = kX + kC * kLC;      // C x kLC  tril(Q K^T)
     static constexpr int kY = kP + kC * kLC;      // solve scratch
     static constexpr int kB = kY + 3 * 16 * 17;   // C        beta
-    static constexpr int kFloats = kB + kC;
+    static constexpr int kGd = kB + kC;           // 4 x C    gated: g, G, gamma, Gamma / gamma
+    static constexpr int kFloats = kGd + 4 * kC;
     static constexpr size_t kBytes = sizeof(float) * kFloats;
     static_assert(kBytes <= 232448, "one CTA's shared memory");
 };
@@ -96,12 +143,17 @@ struct ChainSmem {
 // One CTA per (batch, head, slice of NV value channels): G = dL/dS from the
 // last chunk to the first.  Writes G at the end of every chunk (G_chunks,
 // [BH][chunk][dk][dv] fp32), d_v, and d_S0 (if given).
-template <class Ops, typename T, int DK, int DV, int NV>
+// kGate (Gated DeltaNet, g the fp32 [BH][T] log keep rates): per chunk
+//     dU' = P^T dO + diag(Gamma / gamma) K G,  dV = Tm^T dU',
+//     G <- Gamma G + (diag(gamma) Q)^T dO - (diag(gamma) K)^T dV
+// with P and A carrying the decay ratios.
+template <class Ops, typename T, int DK, int DV, int NV, bool kGate = false>
 __global__ void __launch_bounds__(Ops::kThreads, 1)
 chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
                        const T* __restrict__ beta, const T* __restrict__ d_o,
                        const float* __restrict__ d_S_T, T* __restrict__ d_v,
-                       float* __restrict__ d_S0, float* __restrict__ G_chunks, int Tlen) {
+                       float* __restrict__ d_S0, float* __restrict__ G_chunks, int Tlen,
+                       const float* __restrict__ gate) {
     using L = ChainSmem<DK, NV, Ops::kPad>;
     constexpr int LK = L::LK, LV = L::LV, kLC = L::kLC, NSLICE = DV / NV, NT = Ops::kThreads;
     extern __shared__ float smem[];
@@ -116,6 +168,10 @@ chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
     float* Pm = smem + L::kP;
     float* Ys = smem + L::kY;
     float* bs = smem + L::kB;
+    float* gs = smem + L::kGd;
+    float* Gl = gs + kC;
+    float* gam = Gl + kC;
+    float* rg = gam + kC;
     const int tid = threadIdx.x;
     const int bh = blockIdx.x / NSLICE, j0 = (blockIdx.x % NSLICE) * NV;
     const size_t tok0 = (size_t)bh * Tlen;
@@ -135,16 +191,21 @@ chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
         load_rows<NT, DK, LK, DK>(Qs, q, tok0, t0, n, 0);
         load_rows<NT, NV, LV, DV>(Ds, d_o, tok0, t0, n, j0);
         if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
+        if constexpr (kGate) chunk_decay(gate, tok0 + t0, n, gs, Gl, gam, rg, tid);
         __syncthreads();
-        form_a_p<Ops, DK>(Ks, Qs, bs, Am, Pm, nullptr);
+        if constexpr (kGate)
+            form_a_p_gated<Ops, DK>(Ks, Qs, bs, Gl, Am, Pm, nullptr);
+        else
+            form_a_p<Ops, DK>(Ks, Qs, bs, Am, Pm, nullptr);
         __syncthreads();
-        {   // dU' = P^T dO + K G
+        {   // dU' = P^T dO + K G  (gated: K's rows times Gamma / gamma)
             typename Ops::template Acc<64, NV> acc;
             Ops::zero(acc);
             Ops::template mm<64, NV, kC>(acc, [&](int m, int s) { return Pm[s * kLC + m]; },
                                [&](int s, int nn) { return Ds[s * LV + nn]; });
-            Ops::template mm<64, NV, DK>(acc, [&](int m, int i) { return Ks[m * LK + i]; },
-                               [&](int i, int nn) { return Gs[i * LV + nn]; });
+            Ops::template mm<64, NV, DK>(acc, [&](int m, int i) {
+                return kGate ? Ks[m * LK + i] * rg[m] : Ks[m * LK + i];
+            }, [&](int i, int nn) { return Gs[i * LV + nn]; });
             Ops::for_each(acc, [&](int m, int nn, float x) { Us[m * LV + nn] = x; });
         }
         unit_lower_inverse64<NT, kLC>(Am, Xm, Ys);  // ends with a barrier
@@ -160,14 +221,20 @@ chunk_bwd_chain_kernel(const T* __restrict__ q, const T* __restrict__ k,
             });
         }
         __syncthreads();
-        {   // G <- G + Q^T dO - K^T dV  (the gradient of the state chunk c starts from)
+        {   // G <- G + Q^T dO - K^T dV  (the gradient of the state chunk c starts from;
+            // gated: Gamma G and the rows of Q and K times gamma)
             typename Ops::template Acc<DK, NV> acc;
             Ops::zero(acc);
-            Ops::template mm<DK, NV, kC>(acc, [&](int i, int s) { return Qs[s * LK + i]; },
-                               [&](int s, int nn) { return Ds[s * LV + nn]; });
-            Ops::template mm<DK, NV, kC>(acc, [&](int i, int s) { return -Ks[s * LK + i]; },
-                               [&](int s, int nn) { return Vs[s * LV + nn]; });
-            Ops::for_each(acc, [&](int i, int nn, float x) { Gs[i * LV + nn] += x; });
+            Ops::template mm<DK, NV, kC>(acc, [&](int i, int s) {
+                return kGate ? Qs[s * LK + i] * gam[s] : Qs[s * LK + i];
+            }, [&](int s, int nn) { return Ds[s * LV + nn]; });
+            Ops::template mm<DK, NV, kC>(acc, [&](int i, int s) {
+                return kGate ? -Ks[s * LK + i] * gam[s] : -Ks[s * LK + i];
+            }, [&](int s, int nn) { return Vs[s * LV + nn]; });
+            const float keep = kGate ? gam[kC - 1] : 1.f;
+            Ops::for_each(acc, [&](int i, int nn, float x) {
+                Gs[i * LV + nn] = kGate ? keep * Gs[i * LV + nn] + x : Gs[i * LV + nn] + x;
+            });
         }
         __syncthreads();
     }
@@ -189,9 +256,13 @@ struct GradSmem {
     static constexpr int kP = kX + kC * kLC;      // C x kLC  tril(Q K^T)
     static constexpr int kKK = kP + kC * kLC;     // C x kLC  K K^T
     static constexpr int kB = kKK + kC * kLC;     // C        beta
+    // gated: g (then dG), G, gamma, Gamma / gamma, and the per-token sums
+    // t1 = gamma dO . (Q S), t2 = gamma dV . (K S), t3 = (Gamma / gamma) (K G) . U',
+    // then <G, S> in one float
+    static constexpr int kGd = kB + kC;           // 7 x C + 4
     // The work area: A and the solve scratch until X is formed, then the
     // value-slice operands, then C x C matrices once the slices are done.
-    static constexpr int kW = kB + kC;
+    static constexpr int kW = kGd + 7 * kC + 4;
     static constexpr int kA = kW;                 // C x kLC  A
     static constexpr int kY = kA + kC * kLC;      // solve scratch
     static constexpr int kV = kW;                 // C x LS   V
@@ -212,13 +283,18 @@ struct GradSmem {
 // One CTA per (batch, head, chunk): the chunk's d_q, d_k and d_beta from S at
 // its start (S_chunks) and G at its end (G_chunks), over all value channels
 // in slices of NS.
-template <class Ops, typename T, int DK, int DV>
+// kGate (Gated DeltaNet): the chunk algebra with the decay ratios in A and P,
+// gamma on K S in R and on Q S in O, Gamma / gamma on K in the state update,
+// and d_g: per token dG_i (the decay ratios' terms, gamma's and Gamma's) summed
+// from each token to the chunk's end.
+template <class Ops, typename T, int DK, int DV, bool kGate = false>
 __global__ void __launch_bounds__(Ops::kThreads, 1)
 chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
                        const T* __restrict__ v, const T* __restrict__ beta,
                        const T* __restrict__ d_o, const float* __restrict__ S_chunks,
                        const float* __restrict__ G_chunks, T* __restrict__ d_q,
-                       T* __restrict__ d_k, T* __restrict__ d_beta, int Tlen, int nchunks) {
+                       T* __restrict__ d_k, T* __restrict__ d_beta, int Tlen, int nchunks,
+                       const float* __restrict__ gate, float* __restrict__ d_g) {
     constexpr int NS = 32;
     using L = GradSmem<DK, NS, Ops::kPad>;
     constexpr int LK = L::LK, LS = L::LS, kLC = L::kLC, NT = Ops::kThreads;
@@ -239,6 +315,14 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
     float* Fs = smem + L::kF;
     float* Ss = smem + L::kS;
     float* Gs = smem + L::kG;
+    float* gs = smem + L::kGd;  // g, then dG
+    float* Gl = gs + kC;
+    float* gam = Gl + kC;
+    float* rg = gam + kC;
+    float* t1 = rg + kC;
+    float* t2 = t1 + kC;
+    float* t3 = t2 + kC;
+    float* t4 = t3 + kC;
     const int tid = threadIdx.x;
     const int bh = blockIdx.x / nchunks, c = blockIdx.x % nchunks;
     const int t0 = c * kC, n = min(kC, Tlen - t0);
@@ -248,8 +332,15 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
     load_rows<NT, DK, LK, DK>(Ks, k, tok0, t0, n, 0);
     load_rows<NT, DK, LK, DK>(Qs, q, tok0, t0, n, 0);
     if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
+    if constexpr (kGate) {
+        if (tid < 3 * kC + 1) t1[tid] = 0.f;  // t1, t2, t3 and <G, S>
+        chunk_decay(gate, tok0 + t0, n, gs, Gl, gam, rg, tid);
+    }
     __syncthreads();
-    form_a_p<Ops, DK>(Ks, Qs, bs, Am, Pm, KK);
+    if constexpr (kGate)
+        form_a_p_gated<Ops, DK>(Ks, Qs, bs, Gl, Am, Pm, KK);
+    else
+        form_a_p<Ops, DK>(Ks, Qs, bs, Am, Pm, KK);
     __syncthreads();
     unit_lower_inverse64<NT, kLC>(Am, Xm, Ys);  // ends with a barrier
 
@@ -259,13 +350,21 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
     Ops::zero(aK);
     Ops::zero(aP);
     Ops::zero(aT);
+    float t4p = 0.f;  // gated: this thread's part of <G, S>
     for (int js = 0; js < DV; js += NS) {
         load_rows<NT, NS, LS, DV>(Vs, v, tok0, t0, n, js);
         load_rows<NT, NS, LS, DV>(Ds, d_o, tok0, t0, n, js);
         load_tile<NT, DK, NS, LS, DV>(Ss, S_chunks + st0, 0, DK, js);
         load_tile<NT, DK, NS, LS, DV>(Gs, G_chunks + st0, 0, DK, js);
         __syncthreads();
-        {   // R = V - K S and dU' = P^T dO + K G
+        if constexpr (kGate)
+            for (int e = tid; e < DK * NS; e += NT) {
+                const int i = e / NS, jj = e % NS;
+                t4p = fmaf(Gs[i * LS + jj], Ss[i * LS + jj], t4p);
+            }
+        {   // R = V - K S and dU' = P^T dO + K G.  Gated: Rs holds W = diag(gamma) K S
+            // (R = V - W), Us the term diag(Gamma / gamma) K G until U' replaces it,
+            // and t1 gathers gamma dO . (Q S)
             typename Ops::template Acc<64, NS> r, e;
             Ops::zero(r);
             Ops::zero(e);
@@ -273,37 +372,72 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
                                [&](int i, int nn) { return Ss[i * LS + nn]; });
             Ops::template mm<64, NS, kC>(e, [&](int m, int s) { return Pm[s * kLC + m]; },
                                [&](int s, int nn) { return Ds[s * LS + nn]; });
-            Ops::template mm<64, NS, DK>(e, [&](int m, int i) { return Ks[m * LK + i]; },
-                               [&](int i, int nn) { return Gs[i * LS + nn]; });
-            Ops::for_each(r, [&](int m, int nn, float x) { Rs[m * LS + nn] = Vs[m * LS + nn] - x; });
-            Ops::for_each(e, [&](int m, int nn, float x) { Es[m * LS + nn] = x; });
+            if constexpr (kGate) {
+                typename Ops::template Acc<64, NS> kg, qs;
+                Ops::zero(kg);
+                Ops::zero(qs);
+                Ops::template mm<64, NS, DK>(kg, [&](int m, int i) { return Ks[m * LK + i]; },
+                                   [&](int i, int nn) { return Gs[i * LS + nn]; });
+                Ops::template mm<64, NS, DK>(qs, [&](int m, int i) { return Qs[m * LK + i]; },
+                                   [&](int i, int nn) { return Ss[i * LS + nn]; });
+                Ops::for_each(r, [&](int m, int nn, float x) { Rs[m * LS + nn] = gam[m] * x; });
+                Ops::for_each(e, [&](int m, int nn, float x) { Es[m * LS + nn] = x; });
+                Ops::for_each(kg, [&](int m, int nn, float x) {
+                    const float y = rg[m] * x;
+                    Es[m * LS + nn] += y;
+                    Us[m * LS + nn] = y;
+                });
+                Ops::for_each(qs, [&](int m, int nn, float x) {
+                    atomicAdd(&t1[m], gam[m] * Ds[m * LS + nn] * x);
+                });
+            } else {
+                Ops::template mm<64, NS, DK>(e, [&](int m, int i) { return Ks[m * LK + i]; },
+                                   [&](int i, int nn) { return Gs[i * LS + nn]; });
+                Ops::for_each(r, [&](int m, int nn, float x) { Rs[m * LS + nn] = Vs[m * LS + nn] - x; });
+                Ops::for_each(e, [&](int m, int nn, float x) { Es[m * LS + nn] = x; });
+            }
         }
         __syncthreads();
-        {   // U' = X diag(beta) R and dV = diag(beta) X^T dU'
+        // R as stored, or V - W in the gated form
+        auto Rv = [&](int s, int nn) {
+            return kGate ? Vs[s * LS + nn] - Rs[s * LS + nn] : Rs[s * LS + nn];
+        };
+        {   // U' = X diag(beta) R and dV = diag(beta) X^T dU' (gated: t3 and t2 too)
             typename Ops::template Acc<64, NS> u, f;
             Ops::zero(u);
             Ops::zero(f);
             Ops::template mm<64, NS, kC>(u, [&](int m, int s) { return Xm[m * kLC + s] * bs[s]; },
-                               [&](int s, int nn) { return Rs[s * LS + nn]; });
+                               [&](int s, int nn) { return Rv(s, nn); });
             Ops::template mm<64, NS, kC>(f, [&](int m, int s) { return Xm[s * kLC + m]; },
                                [&](int s, int nn) { return Es[s * LS + nn]; });
-            Ops::for_each(u, [&](int m, int nn, float x) { Us[m * LS + nn] = x; });
-            Ops::for_each(f, [&](int m, int nn, float x) { Fs[m * LS + nn] = bs[m] * x; });
+            Ops::for_each(u, [&](int m, int nn, float x) {
+                if constexpr (kGate) atomicAdd(&t3[m], Us[m * LS + nn] * x);
+                Us[m * LS + nn] = x;
+            });
+            Ops::for_each(f, [&](int m, int nn, float x) {
+                Fs[m * LS + nn] = bs[m] * x;
+                if constexpr (kGate) atomicAdd(&t2[m], bs[m] * x * Rs[m * LS + nn]);
+            });
         }
         __syncthreads();
         // dP += dO U'^T, dTm += dU' R^T, dQ += dO S^T, dK += U' G^T - dV S^T
+        // (gated: dQ's rows times gamma, U' G^T's times Gamma / gamma, dV S^T's times gamma)
         Ops::template mm<64, 64, NS>(aP, [&](int m, int j) { return Ds[m * LS + j]; },
                            [&](int j, int nn) { return Us[nn * LS + j]; });
         Ops::template mm<64, 64, NS>(aT, [&](int m, int j) { return Es[m * LS + j]; },
-                           [&](int j, int nn) { return Rs[nn * LS + j]; });
-        Ops::template mm<64, DK, NS>(aQ, [&](int m, int j) { return Ds[m * LS + j]; },
-                           [&](int j, int i) { return Ss[i * LS + j]; });
-        Ops::template mm<64, DK, NS>(aK, [&](int m, int j) { return Us[m * LS + j]; },
-                           [&](int j, int i) { return Gs[i * LS + j]; });
-        Ops::template mm<64, DK, NS>(aK, [&](int m, int j) { return -Fs[m * LS + j]; },
-                           [&](int j, int i) { return Ss[i * LS + j]; });
+                           [&](int j, int nn) { return Rv(nn, j); });
+        Ops::template mm<64, DK, NS>(aQ, [&](int m, int j) {
+            return kGate ? Ds[m * LS + j] * gam[m] : Ds[m * LS + j];
+        }, [&](int j, int i) { return Ss[i * LS + j]; });
+        Ops::template mm<64, DK, NS>(aK, [&](int m, int j) {
+            return kGate ? Us[m * LS + j] * rg[m] : Us[m * LS + j];
+        }, [&](int j, int i) { return Gs[i * LS + j]; });
+        Ops::template mm<64, DK, NS>(aK, [&](int m, int j) {
+            return kGate ? -Fs[m * LS + j] * gam[m] : -Fs[m * LS + j];
+        }, [&](int j, int i) { return Ss[i * LS + j]; });
         __syncthreads();
     }
+    if constexpr (kGate) atomicAdd(t4, t4p);
 
     // The work area now holds C x C matrices.
     float* dPm = smem + L::kW;
@@ -313,11 +447,13 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
     Ops::for_each(aP, [&](int m, int nn, float x) { dPm[m * kLC + nn] = nn <= m ? x : 0.f; });
     Ops::for_each(aT, [&](int m, int nn, float x) { dTs[m * kLC + nn] = x; });
     __syncthreads();
-    // dQ += dP K, dK += dP^T Q
-    Ops::template mm<64, DK, kC>(aQ, [&](int m, int s) { return dPm[m * kLC + s]; },
-                       [&](int s, int i) { return Ks[s * LK + i]; });
-    Ops::template mm<64, DK, kC>(aK, [&](int m, int s) { return dPm[s * kLC + m]; },
-                       [&](int s, int i) { return Qs[s * LK + i]; });
+    // dQ += dP K, dK += dP^T Q (gated: dP times the decay ratios)
+    Ops::template mm<64, DK, kC>(aQ, [&](int m, int s) {
+        return kGate ? dPm[m * kLC + s] * decay_ratio(Gl, m, s) : dPm[m * kLC + s];
+    }, [&](int s, int i) { return Ks[s * LK + i]; });
+    Ops::template mm<64, DK, kC>(aK, [&](int m, int s) {
+        return kGate ? dPm[s * kLC + m] * decay_ratio(Gl, s, m) : dPm[s * kLC + m];
+    }, [&](int s, int i) { return Qs[s * LK + i]; });
     {   // M1 = (dTm diag(beta)) X^T
         typename Ops::template Acc<64, 64> acc;
         Ops::zero(acc);
@@ -339,10 +475,37 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
     __syncthreads();
     if (tid < kC)
         for (int l = 0; l < kC; ++l) db = fmaf(dAm[tid * kLC + l], KK[tid * kLC + l], db);
-    // dK += Z K with Z = diag(beta) dA + (diag(beta) dA)^T
+    // dK += Z K with Z = diag(beta) dA + (diag(beta) dA)^T (gated: dA times the decay ratios)
     Ops::template mm<64, DK, kC>(aK, [&](int m, int s) {
-        return bs[m] * dAm[m * kLC + s] + bs[s] * dAm[s * kLC + m];
+        return kGate ? bs[m] * dAm[m * kLC + s] * decay_ratio(Gl, m, s) +
+                           bs[s] * dAm[s * kLC + m] * decay_ratio(Gl, s, m)
+                     : bs[m] * dAm[m * kLC + s] + bs[s] * dAm[s * kLC + m];
     }, [&](int s, int i) { return Ks[s * LK + i]; });
+    if constexpr (kGate) {  // dG per token, then d_g = its sums from each token to the chunk's end
+        if (tid < kC) {
+            const int i = tid;
+            float dG = t1[i] - t2[i] - t3[i];
+            for (int j = 0; j < kC; ++j) {
+                // A_ij = beta_i (K K^T o D)_ij (j < i) and P (with the ratios) as formed
+                const float aij = j < i ? bs[i] * KK[i * kLC + j] : 0.f;
+                const float aji = i < j ? bs[j] * KK[j * kLC + i] : 0.f;
+                dG += dAm[i * kLC + j] * aij - dAm[j * kLC + i] * aji;
+                dG += dPm[i * kLC + j] * Pm[i * kLC + j] - dPm[j * kLC + i] * Pm[j * kLC + i];
+            }
+            if (i == n - 1) {  // <G, S_next> = Gamma <G, S> + sum_j t3_j
+                float s3 = 0.f;
+                for (int j = 0; j < kC; ++j) s3 += t3[j];
+                dG += gam[kC - 1] * t4[0] + s3;
+            }
+            gs[i] = dG;
+        }
+        __syncthreads();
+        if (tid < n) {
+            float s = 0.f;
+            for (int i = tid; i < n; ++i) s += gs[i];
+            d_g[tok0 + t0 + tid] = s;
+        }
+    }
 
     Ops::for_each(aQ, [&](int m, int i, float x) {
         if (m < n) d_q[(tok0 + t0 + m) * DK + i] = from_f32<T>(x);
@@ -381,14 +544,48 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
     else {
         chain<<<(unsigned)g_chain, Ops::kThreads, LC::kBytes, stream>>>(
             static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(beta),
-            static_cast<const T*>(d_o), d_S_T, static_cast<T*>(d_v), d_S0, Gc, Tlen);
+            static_cast<const T*>(d_o), d_S_T, static_cast<T*>(d_v), d_S0, Gc, Tlen, nullptr);
         err = cudaGetLastError();
     }
     if (err != cudaSuccess) return err;
     grads<<<(unsigned)g_grads, Ops::kThreads, LG::kBytes, stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
         static_cast<const T*>(beta), static_cast<const T*>(d_o), Sc, Gc, static_cast<T*>(d_q),
-        static_cast<T*>(d_k), static_cast<T*>(d_beta), Tlen, nchunks);
+        static_cast<T*>(d_k), static_cast<T*>(d_beta), Tlen, nchunks, nullptr, nullptr);
+    return cudaGetLastError();
+}
+
+// Gated DeltaNet's backward: the chain and the per-chunk gradients with the
+// decay, on CUDA cores with fp32 products for both I/O types (the decay's
+// gradient sums terms that cancel, and tf32 products would not hold it).
+template <typename T, int DK, int DV>
+cudaError_t launch_bwd_gated_typed(const void* q, const void* k, const void* v, const void* beta,
+                                   const float* g, const void* d_o, const float* d_S_T, void* d_q,
+                                   void* d_k, void* d_v, void* d_beta, float* d_g, float* d_S0,
+                                   float* Sc, float* Gc, int BH, int Tlen, cudaStream_t stream) {
+    constexpr int NV = DV < 64 ? DV : 64;
+    using Ops = simt::Fp32Ops;
+    using LC = ChainSmem<DK, NV, Ops::kPad>;
+    using LG = GradSmem<DK, 32, Ops::kPad>;
+    const int nchunks = (Tlen + kC - 1) / kC;
+    auto chain = chunk_bwd_chain_kernel<Ops, T, DK, DV, NV, true>;
+    auto grads = chunk_bwd_grads_kernel<Ops, T, DK, DV, true>;
+    cudaError_t err;
+    if ((err = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)LC::kBytes)) != cudaSuccess ||
+        (err = cudaFuncSetAttribute(grads, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)LG::kBytes)) != cudaSuccess)
+        return err;
+    const long long g_chain = (long long)BH * (DV / NV), g_grads = (long long)BH * nchunks;
+    if (g_chain > 0x7fffffffLL || g_grads > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    chain<<<(unsigned)g_chain, Ops::kThreads, LC::kBytes, stream>>>(
+        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(beta),
+        static_cast<const T*>(d_o), d_S_T, static_cast<T*>(d_v), d_S0, Gc, Tlen, g);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    grads<<<(unsigned)g_grads, Ops::kThreads, LG::kBytes, stream>>>(
+        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
+        static_cast<const T*>(beta), static_cast<const T*>(d_o), Sc, Gc, static_cast<T*>(d_q),
+        static_cast<T*>(d_k), static_cast<T*>(d_beta), Tlen, nchunks, g, d_g);
     return cudaGetLastError();
 }
 
@@ -410,6 +607,46 @@ cudaError_t launch_bwd_dims(const void* q, const void* k, const void* v, const v
 }
 
 }  // namespace
+
+size_t chunk_bwd_gated_workspace_bytes(int BH, int T, int dk, int dv) {
+    if (BH <= 0 || T <= 0) return 0;
+    const size_t items = (size_t)BH * (size_t)((T + kC - 1) / kC);
+    return 2 * items * (size_t)dk * (size_t)dv * sizeof(float);
+}
+
+cudaError_t launch_chunk_bwd_gated(const void* q, const void* k, const void* v, const void* beta,
+                                   const float* g, const float* S0, const void* d_o,
+                                   const float* d_S_T, void* d_q, void* d_k, void* d_v,
+                                   void* d_beta, float* d_g, float* d_S0, int BH, int T, int dk,
+                                   int dv, int dt, void* workspace, cudaStream_t stream,
+                                   const char** stage) {
+    if (BH <= 0 || T <= 0) return cudaSuccess;
+    *stage = "state recompute";
+    const size_t per = (size_t)BH * ((T + kC - 1) / kC) * (size_t)dk * dv;
+    float* const Sc = static_cast<float*>(workspace);
+    float* const Gc = Sc + per;
+    cudaError_t err =
+        launch_chunk_simt(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt, stream, Sc, g);
+    if (err != cudaSuccess) return err;
+    *stage = "gated chain and gradients";
+#define DN_GBWD_CASE(T_, DK_, DV_)                                                              \
+    if (dk == DK_ && dv == DV_)                                                                 \
+        return launch_bwd_gated_typed<T_, DK_, DV_>(q, k, v, beta, g, d_o, d_S_T, d_q, d_k, d_v,\
+                                                     d_beta, d_g, d_S0, Sc, Gc, BH, T, stream);
+    if (dt == 0) {
+        DN_GBWD_CASE(float, 128, 128)
+        DN_GBWD_CASE(float, 128, 64)
+        DN_GBWD_CASE(float, 64, 128)
+        DN_GBWD_CASE(float, 64, 64)
+    } else {
+        DN_GBWD_CASE(__nv_bfloat16, 128, 128)
+        DN_GBWD_CASE(__nv_bfloat16, 128, 64)
+        DN_GBWD_CASE(__nv_bfloat16, 64, 128)
+        DN_GBWD_CASE(__nv_bfloat16, 64, 64)
+    }
+#undef DN_GBWD_CASE
+    return cudaErrorNotSupported;
+}
 
 // Workspace.  Tensor-core path (bf16, dk = dv = 128): S at every chunk start
 // and G at every chunk end as bf16, the forward's [PT; Tm] tiles and every

@@ -81,6 +81,18 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
                              int dk, int dv, int dt, void* workspace, cudaStream_t stream,
                              const char** stage);
 
+// Gated DeltaNet's backward (g the fp32 [BH][T] log keep rates; d_g its
+// gradient, fp32 [BH][T]): the CUDA-core forward records every chunk's start
+// state, then the chain and the per-chunk gradients run with the decay, on
+// CUDA cores in fp32.  The workspace holds the fp32 S and G of every chunk.
+size_t chunk_bwd_gated_workspace_bytes(int BH, int T, int dk, int dv);
+cudaError_t launch_chunk_bwd_gated(const void* q, const void* k, const void* v, const void* beta,
+                                   const float* g, const float* S0, const void* d_o,
+                                   const float* d_S_T, void* d_q, void* d_k, void* d_v,
+                                   void* d_beta, float* d_g, float* d_S0, int BH, int T, int dk,
+                                   int dv, int dt, void* workspace, cudaStream_t stream,
+                                   const char** stage);
+
 // The backward of the packed-sequence forward (cu: N + 1 host offsets into
 // the [H][T][d] tensors; states [N][H][dk][dv]): one batched backward per
 // sequence on gathered copies, in the scratch this many bytes hold.

@@ -368,6 +368,32 @@ DN_API size_t dn_chunk_fwd_varlen_workspace_bytes(const int *cu_seqlens, int N, 
                                            int dk, int dv, int C, int dt);
 
 /*
+ * dn_chunk_bwd_gated -- the gradients of dn_chunk_fwd_gated's outputs: for
+ * L = <d_o, o> + <d_S_T, S_T>, the gradients with respect to q, k, v, beta,
+ * the log keep rates g and S0 ("Gated DeltaNet", garden.houmin.site/infra/
+ * delta-net; "Gated DeltaNet : oublier d'abord l'état entier",
+ * fr.news.hada.io/topic?id=31925; the states recomputed as in
+ * "Hardware-efficient implementation", paperlayer.ai/abs/2406.06484v6).
+ *   g, d_g  [B, H, T] fp32 (4-byte aligned); the rest as dn_chunk_bwd.
+ *   workspace  device scratch of dn_chunk_bwd_gated_workspace_bytes(...) bytes.
+ * The forward's states are recomputed on the CUDA cores and the gradients
+ * formed chunk by chunk on the CUDA cores in fp32 (both I/O types).  d_g is
+ * the gradient of each token's log keep rate, through every later ratio
+ * exp(G_i - G_j), keep factor and state carried out of its chunk.  Errors and
+ * overlap rules as dn_chunk_bwd; d_g may overlap nothing else.
+ */
+DN_API int dn_chunk_bwd_gated(const void *q, const void *k, const void *v, const void *beta,
+                              const float *g, const float *S0, const void *d_o,
+                              const float *d_S_T, void *d_q, void *d_k, void *d_v, void *d_beta,
+                              float *d_g, float *d_S0, int B, int H, int T, int dk, int dv, int C,
+                              int dt, void *workspace, size_t workspace_bytes, void *stream);
+/* Its scratch: the fp32 state and state gradient of every chunk,
+ * 2 * B * H * ceil(T / 64) * dk * dv * 4 bytes (0 for invalid arguments).
+ * Host-only. */
+DN_API size_t dn_chunk_bwd_gated_workspace_bytes(int B, int H, int T, int dk, int dv, int C,
+                                                 int dt);
+
+/*
  * dn_chunk_bwd_varlen -- the gradients of dn_chunk_fwd_varlen's outputs, as
  * dn_chunk_bwd gives them for the batched forward (the pages' backward with
  * the states recomputed: "Hardware-efficient implementation",
@@ -540,7 +566,7 @@ DN_API int dn_recurrent_step_kda_qk(const void *q, const void *k, const void *v,
 /* ABI version of this header (bumped on incompatible changes). */
 DN_API int dn_abi_version(void);
 
-#define DN_ABI_VERSION 7
+#define DN_ABI_VERSION 8
 
 #ifdef __cplusplus
 }

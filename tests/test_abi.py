@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dn_abi_version() == 7
+    assert lib.dn_abi_version() == 8
     assert lib.dn_status_string(0) == b"DN_OK"
     assert lib.dn_status_string(1) == b"DN_ERR_INVALID_ARG"
     assert lib.dn_status_string(2) == b"DN_ERR_UNSUPPORTED"

@@ -775,7 +775,7 @@ size_t dn_chunk_bwd_gated_workspace_bytes(int B, int H, int T, int dk, int dv, i
         return 0;
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return 0;
-    return dn::chunk_bwd_gated_workspace_bytes((int)BH, T, dk, dv);
+    return dn::chunk_bwd_gated_workspace_bytes((int)BH, T, dk, dv, dt);
 }
 
 int dn_chunk_bwd_gated(const void* q, const void* k, const void* v, const void* beta,

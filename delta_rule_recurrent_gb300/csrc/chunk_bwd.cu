@@ -556,15 +556,15 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
 }
 
 // Gated DeltaNet's backward: the chain and the per-chunk gradients with the
-// decay, on CUDA cores with fp32 products for both I/O types (the decay's
-// gradient sums terms that cancel, and tf32 products would not hold it).
+// decay; fp32 products on the CUDA cores for fp32 I/O, tf32 tensor-core
+// products (fp32 accumulation) for bf16 I/O, as the plain backward.
 template <typename T, int DK, int DV>
 cudaError_t launch_bwd_gated_typed(const void* q, const void* k, const void* v, const void* beta,
                                    const float* g, const void* d_o, const float* d_S_T, void* d_q,
                                    void* d_k, void* d_v, void* d_beta, float* d_g, float* d_S0,
                                    float* Sc, float* Gc, int BH, int Tlen, cudaStream_t stream) {
     constexpr int NV = DV < 64 ? DV : 64;
-    using Ops = simt::Fp32Ops;
+    using Ops = std::conditional_t<std::is_same_v<T, float>, simt::Fp32Ops, simt::Tf32Ops<8>>;
     using LC = ChainSmem<DK, NV, Ops::kPad>;
     using LG = GradSmem<DK, 32, Ops::kPad>;
     const int nchunks = (Tlen + kC - 1) / kC;
@@ -608,10 +608,11 @@ cudaError_t launch_bwd_dims(const void* q, const void* k, const void* v, const v
 
 }  // namespace
 
-size_t chunk_bwd_gated_workspace_bytes(int BH, int T, int dk, int dv) {
+size_t chunk_bwd_gated_workspace_bytes(int BH, int T, int dk, int dv, int dt) {
     if (BH <= 0 || T <= 0) return 0;
     const size_t items = (size_t)BH * (size_t)((T + kC - 1) / kC);
-    return 2 * items * (size_t)dk * (size_t)dv * sizeof(float);
+    const size_t states = 2 * items * (size_t)dk * (size_t)dv * sizeof(float);
+    return states + (chunk_tc_supports(dk, dv, dt) ? chunk_tc_gated_workspace_bytes(BH, T) : 0);
 }
 
 cudaError_t launch_chunk_bwd_gated(const void* q, const void* k, const void* v, const void* beta,
@@ -626,7 +627,11 @@ cudaError_t launch_chunk_bwd_gated(const void* q, const void* k, const void* v, 
     float* const Sc = static_cast<float*>(workspace);
     float* const Gc = Sc + per;
     cudaError_t err =
-        launch_chunk_simt(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt, stream, Sc, g);
+        chunk_tc_supports(dk, dv, dt)
+            ? launch_chunk_tc_gated(q, k, v, beta, g, S0, nullptr, nullptr, BH, T, dk, dv, dt,
+                                    Gc + per, stream, kNoNorm, Sc)
+            : launch_chunk_simt(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt, stream,
+                                Sc, g);
     if (err != cudaSuccess) return err;
     *stage = "gated chain and gradients";
 #define DN_GBWD_CASE(T_, DK_, DV_)                                                              \

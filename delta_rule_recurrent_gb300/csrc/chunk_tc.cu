@@ -1686,6 +1686,18 @@ __device__ __forceinline__ void tmem_pack64(uint32_t src, uint32_t dst,
     tmem_st32(dst, p);
 }
 
+// As tmem_pack64, recording the fp32 values (rec[e * kD], e = 0..63).
+__device__ __forceinline__ void tmem_pack64_rec32(uint32_t src, uint32_t dst, float* rec) {
+    float x[64];
+    tmem_ld64f(src, x);
+#pragma unroll
+    for (int e = 0; e < 64; ++e) rec[(size_t)e * kD] = x[e];
+    uint32_t p[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) p[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+    tmem_st32(dst, p);
+}
+
 // Gated: S^T scaled in place by the chunk's keep factor exp G_C (64 fp32
 // columns), and U'^T packed with token column e scaled by dec[e] =
 // exp(G_C - G_e) (shared memory).
@@ -1768,7 +1780,7 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
     }
     tmem_wait_st();
 
-    static_assert(!((kGate || kKda) && kRec), "no state recording on the decayed forms");
+    static_assert(!(kKda && kRec), "no state recording on the KDA form");
     constexpr bool kSide = kGate || kKda;
     for (int c = 0; c < nchunks; ++c) {
         const int g = c & 1;
@@ -1794,8 +1806,15 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
             const float* const slot = sside + g * (kSideCopyBytes / 4);
             if (t < 32) reinterpret_cast<float4*>(sdec)[t] = reinterpret_cast<const float4*>(slot)[t];
         }
-        // S^T -> bf16 (dk 0-63, then 64-127); S itself recorded when asked
-        if constexpr (kRec) {
+        // S^T -> bf16 (dk 0-63, then 64-127); S itself recorded when asked: the
+        // plain form as a bf16 hi/lo tile pair, the gated one in fp32 (S_chunks
+        // then points at fp32 [BH][chunk][dk][dv])
+        if constexpr (kRec && kGate) {
+            float* const rec32 = reinterpret_cast<float*>(S_chunks) +
+                                 ((size_t)bh * nchunks + c) * kD * kD + t;
+            tmem_pack64_rec32(lane + C_ST, lane + C_SB, rec32);
+            tmem_pack64_rec32(lane + C_ST + 64u, lane + C_SB + 32u, rec32 + 64 * kD);
+        } else if constexpr (kRec) {
             __nv_bfloat16* const rec = S_chunks + 2 * ((size_t)bh * nchunks + c) * kD * kD + t;
             tmem_pack64(lane + C_ST, lane + C_SB, rec);
             tmem_pack64(lane + C_ST + 64u, lane + C_SB + 32u, rec + 64 * kD);
@@ -3332,10 +3351,10 @@ size_t chunk_tc_gated_workspace_bytes(int BH, int T) {
 cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, const void* beta,
                                   const float* g, const float* S0, void* o, float* S_T, int BH,
                                   int T, int dk, int dv, int dt, void* workspace,
-                                  cudaStream_t stream, const QkNorm& norm) {
+                                  cudaStream_t stream, const QkNorm& norm, float* S_rec32) {
     if (!chunk_tc_supports(dk, dv, dt)) return cudaErrorNotSupported;
     if (BH <= 0 || T <= 0) return cudaSuccess;
-    if (!workspace || !o || !g) return cudaErrorInvalidValue;
+    if (!workspace || (!o && !S_rec32) || !g) return cudaErrorInvalidValue;
     const int nchunks = (T + kC - 1) / kC;
     const long long items = (long long)BH * nchunks;
     if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -3348,7 +3367,7 @@ cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, c
         !make_ws_map(&mws, workspace, BH, nchunks) || !make_ws_map(&mws2, tile2, BH, nchunks))
         return cudaErrorInvalidValue;
     auto prep_kernel = chunk_prep_kernel<1, true>;
-    auto scan_kernel = chunk_scan_kernel<false, 1, true>;
+    auto scan_kernel = S_rec32 ? chunk_scan_kernel<true, 1, true> : chunk_scan_kernel<false, 1, true>;
     cudaError_t err;
     if ((err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     kPrepSmemBytes)) != cudaSuccess ||
@@ -3362,7 +3381,8 @@ cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, c
         side, mws2, norm, nullptr);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mws2, S0,
-                                                       static_cast<__nv_bfloat16*>(o), S_T, nullptr,
+                                                       static_cast<__nv_bfloat16*>(o), S_T,
+                                                       reinterpret_cast<__nv_bfloat16*>(S_rec32),
                                                        T, 1, batched, side);
     return cudaGetLastError();
 }

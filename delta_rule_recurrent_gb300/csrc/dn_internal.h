@@ -82,10 +82,12 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
                              const char** stage);
 
 // Gated DeltaNet's backward (g the fp32 [BH][T] log keep rates; d_g its
-// gradient, fp32 [BH][T]): the CUDA-core forward records every chunk's start
-// state, then the chain and the per-chunk gradients run with the decay, on
-// CUDA cores in fp32.  The workspace holds the fp32 S and G of every chunk.
-size_t chunk_bwd_gated_workspace_bytes(int BH, int T, int dk, int dv);
+// gradient, fp32 [BH][T]): the forward records every chunk's start state
+// (the two-pass tensor-core form for bf16, d = 128, whose tiles then follow
+// in the workspace; else the CUDA-core form), then the chain and the
+// per-chunk gradients run with the decay on the CUDA cores.  The workspace
+// holds the fp32 S and G of every chunk.
+size_t chunk_bwd_gated_workspace_bytes(int BH, int T, int dk, int dv, int dt);
 cudaError_t launch_chunk_bwd_gated(const void* q, const void* k, const void* v, const void* beta,
                                    const float* g, const float* S0, const void* d_o,
                                    const float* d_S_T, void* d_q, void* d_k, void* d_v,
@@ -166,10 +168,13 @@ cudaError_t launch_chunk_bwd_grads_tc(const void* q, const void* k, const void* 
 // rate): the workspace holds the [PT; Tm] tiles and then kSideFloats fp32
 // decay values per chunk, chunk_tc_gated_workspace_bytes(BH, T) in all.
 size_t chunk_tc_gated_workspace_bytes(int BH, int T);
+// With S_rec32 it records every chunk's start state in fp32 ([BH][chunk][dk][dv],
+// the gated backward's recompute) and o may be nullptr.
 cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, const void* beta,
                                   const float* g, const float* S0, void* o, float* S_T, int BH,
                                   int T, int dk, int dv, int dt, void* workspace,
-                                  cudaStream_t stream, const QkNorm& norm = kNoNorm);
+                                  cudaStream_t stream, const QkNorm& norm = kNoNorm,
+                                  float* S_rec32 = nullptr);
 // KDA on tensor cores (bf16, dk = dv = 128; g the fp32 [BH][T][dk] per-key-
 // channel log keep rate), with a workspace of chunk_tc_kda_workspace_bytes.
 size_t chunk_tc_kda_workspace_bytes(int BH, int T);

@@ -376,8 +376,10 @@ DN_API size_t dn_chunk_fwd_varlen_workspace_bytes(const int *cu_seqlens, int N, 
  * "Hardware-efficient implementation", paperlayer.ai/abs/2406.06484v6).
  *   g, d_g  [B, H, T] fp32 (4-byte aligned); the rest as dn_chunk_bwd.
  *   workspace  device scratch of dn_chunk_bwd_gated_workspace_bytes(...) bytes.
- * The forward's states are recomputed on the CUDA cores and the gradients
- * formed chunk by chunk on the CUDA cores in fp32 (both I/O types).  d_g is
+ * The forward's states are recomputed (on tcgen05 for bf16 with dk = dv = 128,
+ * else on the CUDA cores) and the gradients formed chunk by chunk on the CUDA
+ * cores (fp32 products for fp32 I/O, tf32 tensor-core products with fp32
+ * accumulation for bf16).  d_g is
  * the gradient of each token's log keep rate, through every later ratio
  * exp(G_i - G_j), keep factor and state carried out of its chunk.  Errors and
  * overlap rules as dn_chunk_bwd; d_g may overlap nothing else.
@@ -388,8 +390,9 @@ DN_API int dn_chunk_bwd_gated(const void *q, const void *k, const void *v, const
                               float *d_g, float *d_S0, int B, int H, int T, int dk, int dv, int C,
                               int dt, void *workspace, size_t workspace_bytes, void *stream);
 /* Its scratch: the fp32 state and state gradient of every chunk,
- * 2 * B * H * ceil(T / 64) * dk * dv * 4 bytes (0 for invalid arguments).
- * Host-only. */
+ * 2 * B * H * ceil(T / 64) * dk * dv * 4 bytes, plus, for bf16 with
+ * dk = dv = 128, the tensor-core forward's scratch (as
+ * dn_chunk_fwd_gated_workspace_bytes); 0 for invalid arguments.  Host-only. */
 DN_API size_t dn_chunk_bwd_gated_workspace_bytes(int B, int H, int T, int dk, int dv, int C,
                                                  int dt);
 

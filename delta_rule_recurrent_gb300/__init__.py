@@ -14,6 +14,8 @@ the computation runs in the library's sm_103a kernels.
     chunk_fwd_varlen(q, k, v, beta, cu_seqlens, ...)  # packed sequences, [H, T, d]
     chunk_fwd_gated(q, k, v, beta, g, ...), recurrent_step_gated(q, k, v, beta, g, state)
         # Gated DeltaNet: log keep rate g per token (per head for a step)
+    chunk_bwd_gated(q, k, v, beta, g, d_o, ...) -> (d_q, d_k, d_v, d_beta, d_g, d_initial_state)
+    GatedDeltaRule.apply(q, k, v, beta, g, initial_state, scale, qk_l2norm)  # autograd
     chunk_fwd_kda(q, k, v, beta, g, ...), recurrent_step_kda(q, k, v, beta, g, state)
         # KDA: one log keep rate per key channel
     qk_prepare(q, k, scale=1.0, l2norm=True)  # the q/k L2-norm and query scale as a pass
@@ -38,7 +40,7 @@ from ._lib import (DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05, DN_BF16, DN_F32,
 
 __all__ = ["chunk_fwd", "chunk_fwd_split", "chunk_bwd", "chunk_bwd_varlen", "chunk_bwd_gated", "recurrent_step", "chunk_fwd_varlen", "chunk_fwd_gated",
            "recurrent_step_gated", "chunk_fwd_kda", "recurrent_step_kda", "qk_prepare",
-           "qk_prepare_bwd", "DeltaRule", "DeltaNetError", "load", "lib_path",
+           "qk_prepare_bwd", "DeltaRule", "GatedDeltaRule", "DeltaNetError", "load", "lib_path",
            "header_symbols", "ALGOS"]
 
 ALGOS = {"auto": DN_ALGO_AUTO, "simt": DN_ALGO_SIMT, "tcgen05": DN_ALGO_TCGEN05}
@@ -348,6 +350,40 @@ class DeltaRule(torch.autograd.Function):
         if prepared:
             d_q, d_k = qk_prepare_bwd(q, k, d_q, d_k, scale=scale, l2norm=ctx.l2norm)
         return d_q, d_k, d_v, d_beta, (d_S0 if S0 is not None else None), None, None
+
+
+class GatedDeltaRule(torch.autograd.Function):
+    """Autograd wrapper for Gated DeltaNet: ``GatedDeltaRule.apply(q, k, v,
+    beta, g, initial_state, scale, qk_l2norm)`` returns ``(o, final_state)``
+    from ``chunk_fwd_gated``; the backward calls ``chunk_bwd_gated`` (states
+    recomputed there) and chains the q/k preparation's gradient as
+    ``DeltaRule`` does.  ``g`` is the fp32 ``[B, H, T]`` log keep rate and
+    receives a gradient."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, beta, g, initial_state=None, scale=None, qk_l2norm=False):
+        q, k, v, beta, g = (t.contiguous() for t in (q, k, v, beta, g))
+        if initial_state is not None:
+            initial_state = initial_state.contiguous()
+        o, S_T = chunk_fwd_gated(q, k, v, beta, g, initial_state=initial_state,
+                                 output_final_state=True, scale=scale, qk_l2norm=qk_l2norm)
+        ctx.save_for_backward(q, k, v, beta, g, initial_state)
+        ctx.scale, ctx.l2norm = scale, bool(qk_l2norm)
+        return o, S_T
+
+    @staticmethod
+    def backward(ctx, d_o, d_S_T):
+        q, k, v, beta, g, S0 = ctx.saved_tensors
+        d_o = torch.zeros_like(v) if d_o is None else d_o.contiguous()
+        d_S_T = None if d_S_T is None else d_S_T.contiguous().float()
+        prepared = ctx.scale is not None or ctx.l2norm
+        scale = 1.0 if ctx.scale is None else ctx.scale
+        qp, kp = qk_prepare(q, k, scale=scale, l2norm=ctx.l2norm) if prepared else (q, k)
+        d_q, d_k, d_v, d_beta, d_g, d_S0 = chunk_bwd_gated(qp, kp, v, beta, g, d_o.to(v.dtype),
+                                                           S0, d_S_T)
+        if prepared:
+            d_q, d_k = qk_prepare_bwd(q, k, d_q, d_k, scale=scale, l2norm=ctx.l2norm)
+        return (d_q, d_k, d_v, d_beta, d_g, (d_S0 if S0 is not None else None), None, None)
 
 
 def _check_gate(g: torch.Tensor, shape, dev) -> None:

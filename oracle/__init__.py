@@ -74,6 +74,8 @@ def _load():
         lib.dn_oracle_forward_gated.restype = ctypes.c_int
         lib.dn_oracle_forward_kda.argtypes = [dp] * 7 + [ctypes.c_long] * 4 + [ctypes.c_int]
         lib.dn_oracle_forward_kda.restype = ctypes.c_int
+        lib.dn_oracle_backward_kda.argtypes = [dp] * 14 + [ctypes.c_long] * 4 + [ctypes.c_int]
+        lib.dn_oracle_backward_kda.restype = ctypes.c_int
         lib.dn_oracle_prepare_rows.argtypes = [dp, dp, ctypes.c_long, ctypes.c_long,
                                                ctypes.c_int, ctypes.c_double,
                                                ctypes.c_double]
@@ -321,6 +323,45 @@ def forward_kda(q, k, v, beta, g, S0=None, nthreads: int | None = None):
     if rc != 0:
         raise MemoryError("oracle could not allocate its scratch vector")
     return o, S
+
+
+def backward_kda(q, k, v, beta, g, dO, S0=None, dS_T=None, nthreads: int | None = None,
+                 max_bytes: int = 4 << 30):
+    """Gradients of L = <dO, o> + <dS_T, S_T> for the recurrence run by
+    ``forward_kda`` (its exact vector-Jacobian product, fp64).  Arguments as
+    for ``backward`` plus ``g`` ``[B, H, T, dk]`` (per-channel log keep
+    rates).  Returns ``(dq, dk, dv, dbeta, dg, dS0)``, ``dg`` shaped like g."""
+    q, k, v, beta, g, dO = _f64(q), _f64(k), _f64(v), _f64(beta), _f64(g), _f64(dO)
+    B, H, T, dk = q.shape
+    dv = v.shape[3]
+    if (k.shape != q.shape or v.shape[:3] != (B, H, T) or beta.shape != (B, H, T)
+            or g.shape != q.shape or dO.shape != v.shape):
+        raise ValueError("q, k, g [B,H,T,dk]; v, dO [B,H,T,dv]; beta [B,H,T]")
+    S0a = None if S0 is None else _f64(S0)
+    dSa = None if dS_T is None else _f64(dS_T)
+    for name, a in (("S0", S0a), ("dS_T", dSa)):
+        if a is not None and a.shape != (B, H, dk, dv):
+            raise ValueError(f"{name} must be [B,H,dk,dv]")
+    dq, dkk, dvv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    db, dg = np.zeros_like(beta), np.zeros_like(g)
+    dS0 = np.zeros((B, H, dk, dv), dtype=np.float64)
+    if B * H == 0:
+        return dq, dkk, dvv, db, dg, dS0
+    if T == 0:
+        if dSa is not None:
+            dS0[...] = dSa
+        return dq, dkk, dvv, db, dg, dS0
+    n = host_cores() if nthreads is None else int(nthreads)
+    n = max(1, min(n, max_bytes // max(8 * dk * dv * (T + 2), 1)))
+    null = ctypes.POINTER(ctypes.c_double)()
+    rc = _load().dn_oracle_backward_kda(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+        _ptr(S0a) if S0a is not None else null, _ptr(dO),
+        _ptr(dSa) if dSa is not None else null, _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(db),
+        _ptr(dg), _ptr(dS0), B * H, T, dk, dv, n)
+    if rc != 0:
+        raise MemoryError("oracle could not allocate its state history")
+    return dq, dkk, dvv, db, dg, dS0
 
 
 def recurrent_step_kda(q, k, v, beta, g, S, nthreads: int | None = None):

@@ -509,6 +509,147 @@ int dn_oracle_forward_kda(const double *q, const double *k, const double *v,
 }
 
 /*
+ * Gradient of the KDA recurrence above (its exact vector-Jacobian product),
+ * the per-channel counterpart of grad_one_head_gated: the same reverse pass
+ * through each token, in the reverse of the page's order, with G = dL/dS_t
+ * and the decay S~ = S_{t-1} D_t scaling key channel i by alpha_t[i]:
+ *   read     o_t = S_t q_t            G += dO_t q_t^T,  dq_t = S_t^T dO_t
+ *   write    S_t = S~ + u k_t^T       du = G k_t,       dk_t (part) = G^T u
+ *   correct  u = beta_t e,            e = v_t - S~ k_t
+ *                                     dv_t = beta_t du, dbeta_t = <du, e>
+ *   predict                           dk_t -= beta_t S~^T du
+ *                                     G -= beta_t du k_t^T   (now dL/dS~)
+ *   decay    S~ = S_{t-1} D_t         dalpha_t[i] = sum_j G[j][i] S_{t-1}[j][i],
+ *                                     dg_t[i] = alpha_t[i] dalpha_t[i],
+ *                                     G[j][i] *= alpha_t[i]  (now dL/dS_{t-1})
+ * g and dg are [T][dk]; every state S_0 .. S_T of the head is kept.
+ */
+static void grad_one_head_kda(const double *q, const double *k, const double *v,
+                              const double *beta, const double *g, const double *S0,
+                              const double *dO, const double *dST, double *dq, double *dk,
+                              double *dvv, double *dbeta, double *dg, double *dS0, long T,
+                              long dk_, long dv, double *states, double *G, double *e,
+                              double *du, double *alpha)
+{
+    const size_t n = (size_t)dk_ * (size_t)dv;
+    for (size_t x = 0; x < n; ++x)
+        states[x] = S0 ? S0[x] : 0.0;
+    for (long t = 0; t < T; ++t) {  /* forward, keeping S_t */
+        const double *Sp = states + (size_t)t * n;
+        double *St = states + (size_t)(t + 1) * n;
+        const double *kt = k + t * dk_;
+        for (long i = 0; i < dk_; ++i)
+            alpha[i] = exp(g[t * dk_ + i]);
+        for (long j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (long i = 0; i < dk_; ++i)
+                acc += alpha[i] * S_AT(Sp, dv, j, i) * kt[i];
+            e[j] = v[t * dv + j] - acc;
+        }
+        for (long j = 0; j < dv; ++j)
+            for (long i = 0; i < dk_; ++i)
+                S_AT(St, dv, j, i) = alpha[i] * S_AT(Sp, dv, j, i) + beta[t] * e[j] * kt[i];
+    }
+    for (size_t x = 0; x < n; ++x)
+        G[x] = dST ? dST[x] : 0.0;
+    for (long t = T - 1; t >= 0; --t) {
+        const double *Sp = states + (size_t)t * n;
+        const double *St = states + (size_t)(t + 1) * n;
+        const double *kt = k + t * dk_, *qt = q + t * dk_, *dOt = dO + t * dv;
+        const double bt = beta[t];
+        for (long i = 0; i < dk_; ++i)
+            alpha[i] = exp(g[t * dk_ + i]);
+        /* read */
+        for (long j = 0; j < dv; ++j)
+            for (long i = 0; i < dk_; ++i)
+                S_AT(G, dv, j, i) += dOt[j] * qt[i];
+        for (long i = 0; i < dk_; ++i) {
+            double acc = 0.0;
+            for (long j = 0; j < dv; ++j)
+                acc += S_AT(St, dv, j, i) * dOt[j];
+            dq[t * dk_ + i] = acc;
+        }
+        /* write, correct, predict (S~ = S_{t-1} D_t) */
+        for (long j = 0; j < dv; ++j) {
+            double a = 0.0, p = 0.0;
+            for (long i = 0; i < dk_; ++i) {
+                a += S_AT(G, dv, j, i) * kt[i];
+                p += alpha[i] * S_AT(Sp, dv, j, i) * kt[i];
+            }
+            du[j] = a;
+            e[j] = v[t * dv + j] - p;
+        }
+        double db = 0.0;
+        for (long j = 0; j < dv; ++j) {
+            dvv[t * dv + j] = bt * du[j];
+            db += du[j] * e[j];
+        }
+        dbeta[t] = db;
+        for (long i = 0; i < dk_; ++i) {
+            double acc = 0.0;
+            for (long j = 0; j < dv; ++j)
+                acc += S_AT(G, dv, j, i) * bt * e[j] - bt * alpha[i] * S_AT(Sp, dv, j, i) * du[j];
+            dk[t * dk_ + i] = acc;
+        }
+        for (long j = 0; j < dv; ++j)
+            for (long i = 0; i < dk_; ++i)
+                S_AT(G, dv, j, i) -= bt * du[j] * kt[i];
+        /* decay, channel by channel */
+        for (long i = 0; i < dk_; ++i) {
+            double da = 0.0;
+            for (long j = 0; j < dv; ++j)
+                da += S_AT(G, dv, j, i) * S_AT(Sp, dv, j, i);
+            dg[t * dk_ + i] = alpha[i] * da;
+        }
+        for (long j = 0; j < dv; ++j)
+            for (long i = 0; i < dk_; ++i)
+                S_AT(G, dv, j, i) *= alpha[i];
+    }
+    for (size_t x = 0; x < n; ++x)
+        dS0[x] = G[x];
+}
+
+/*
+ * Gradients of the KDA recurrence for all BH pairs (layouts as for
+ * dn_oracle_backward; g and dg [BH][T][dk]).  Returns 0, or -1 if scratch
+ * memory could not be had.
+ */
+int dn_oracle_backward_kda(const double *q, const double *k, const double *v,
+                           const double *beta, const double *g, const double *S0,
+                           const double *dO, const double *dST, double *dq, double *dk,
+                           double *dvv, double *dbeta, double *dg, double *dS0, long BH,
+                           long T, long dk_, long dv, int nthreads)
+{
+    int failed = 0;
+    const size_t n = (size_t)dk_ * (size_t)dv;
+    if (nthreads < 1)
+        nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+    {
+        double *states = (double *)malloc(sizeof(double) * (n * (size_t)(T + 1) + n +
+                                                            2 * (size_t)dv + (size_t)dk_ + 2));
+        if (!states) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long h = 0; h < BH; ++h) {
+            if (!states)
+                continue;
+            double *G = states + n * (size_t)(T + 1);
+            double *e = G + n, *du = e + dv + 1, *alpha = du + dv + 1;
+            grad_one_head_kda(q + h * T * dk_, k + h * T * dk_, v + h * T * dv, beta + h * T,
+                              g + h * T * dk_, S0 ? S0 + h * n : NULL, dO + h * T * dv,
+                              dST ? dST + h * n : NULL, dq + h * T * dk_, dk + h * T * dk_,
+                              dvv + h * T * dv, dbeta + h * T, dg + h * T * dk_, dS0 + h * n, T,
+                              dk_, dv, states, G, e, du, alpha);
+        }
+        free(states);
+    }
+    return failed ? -1 : 0;
+}
+
+/*
  * Optional input preparation ahead of any of the forms above, one row of
  * length d at a time:
  *

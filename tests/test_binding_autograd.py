@@ -115,3 +115,74 @@ def test_gradient_matches_finite_differences_of_the_prepared_forward(fakes, l2no
             xm[which][idx] -= h
             fd = (loss(*xp) - loss(*xm)) / (2 * h)
             assert abs(leaf.grad[idx].item() - fd) < 1e-7, (which, idx)
+
+
+@pytest.fixture
+def gated_fakes(monkeypatch):
+    calls = []
+
+    def chunk_fwd_gated(q, k, v, beta, g, initial_state=None, output_final_state=True,
+                        scale=None, qk_l2norm=False, **_):
+        calls.append("chunk_fwd_gated")
+        qp, kp = oracle.prepare_qk(q, k, 1.0 if scale is None else scale, bool(qk_l2norm))
+        o, S = oracle.forward_gated(qp, kp, v, beta, g, initial_state, nthreads=1)
+        return _t(o), _t(S)
+
+    def qk_prepare(q, k, scale=1.0, l2norm=True, eps=1e-6, inplace=False):
+        calls.append("qk_prepare")
+        qp, kp = oracle.prepare_qk(q, k, scale, l2norm, eps)
+        return _t(qp), _t(kp)
+
+    def qk_prepare_bwd(q, k, d_q_out, d_k_out, scale=1.0, l2norm=True, eps=1e-6):
+        calls.append("qk_prepare_bwd")
+        gq, gk = oracle.prepare_qk_backward(q, k, d_q_out, d_k_out, scale, l2norm, eps)
+        return _t(gq), (_t(gk) if l2norm else d_k_out)
+
+    def chunk_bwd_gated(q, k, v, beta, g, d_o, initial_state=None, d_final_state=None, **_):
+        calls.append("chunk_bwd_gated")
+        return tuple(_t(x) for x in oracle.backward_gated(q, k, v, beta, g, d_o, initial_state,
+                                                          d_final_state, nthreads=1))
+
+    monkeypatch.setattr(dn, "qk_prepare", qk_prepare)
+    monkeypatch.setattr(dn, "qk_prepare_bwd", qk_prepare_bwd)
+    monkeypatch.setattr(dn, "chunk_fwd_gated", chunk_fwd_gated)
+    monkeypatch.setattr(dn, "chunk_bwd_gated", chunk_bwd_gated)
+    return calls
+
+
+@pytest.mark.parametrize("scale,l2norm", [(None, False), (8 ** -0.5, True)])
+def test_gated_wrapper_wires_the_gate_gradient(gated_fakes, scale, l2norm):
+    """GatedDeltaRule: g gets the gated backward's d_g, the other leaves the
+    gated gradients for the prepared q and k carried back through the
+    preparation's gradient, and the decay is checked against a central
+    difference of the whole prepared forward."""
+    q, k, v, beta, S0, d_o, d_S = _inputs(seed=2, raw=l2norm)
+    g = np.log(np.random.default_rng(5).uniform(0.5, 1.0, beta.shape))
+    leaves = [_t(x).requires_grad_() for x in (q, k, v, beta, g, S0)]
+    o, S_T = dn.GatedDeltaRule.apply(*leaves, scale, l2norm)
+    torch.autograd.backward([o, S_T], [_t(d_o), _t(d_S)])
+    s = 1.0 if scale is None else scale
+    qp, kp = oracle.prepare_qk(q, k, s, l2norm)
+    ref = list(oracle.backward_gated(qp, kp, v, beta, g, d_o, S0, d_S, nthreads=1))
+    prepared = scale is not None or l2norm
+    if prepared:
+        ref[0], gk = oracle.prepare_qk_backward(q, k, ref[0], ref[1], s, l2norm)
+        if l2norm:
+            ref[1] = gk
+    for leaf, want in zip(leaves, ref):
+        assert np.allclose(leaf.grad.numpy(), want, rtol=0, atol=1e-12)
+    assert gated_fakes == (["chunk_fwd_gated", "qk_prepare", "chunk_bwd_gated",
+                            "qk_prepare_bwd"] if prepared else
+                           ["chunk_fwd_gated", "chunk_bwd_gated"])
+
+    def loss(gx):
+        o2, S2 = oracle.forward_gated(qp, kp, v, beta, gx, S0, nthreads=1)
+        return np.sum(d_o * o2) + np.sum(d_S * S2)
+
+    h = 1e-6
+    for idx in [(0, 0, 0), (0, 1, 7), (0, 0, 20)]:
+        gp, gm = g.copy(), g.copy()
+        gp[idx] += h
+        gm[idx] -= h
+        fd = (loss(gp) - loss(gm)) / (2 * h)
+        assert abs(leaves[4].grad[idx].item() - fd) < 1e-6 * max(1.0, abs(fd)), idx

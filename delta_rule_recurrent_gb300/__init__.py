@@ -16,6 +16,7 @@ the computation runs in the library's sm_103a kernels.
         # Gated DeltaNet: log keep rate g per token (per head for a step)
     chunk_bwd_gated(q, k, v, beta, g, d_o, ...) -> (d_q, d_k, d_v, d_beta, d_g, d_initial_state)
     GatedDeltaRule.apply(q, k, v, beta, g, initial_state, scale, qk_l2norm)  # autograd
+    chunk_bwd_kda(q, k, v, beta, g, d_o, ...), KdaDeltaRule.apply(...)  # KDA's gradients
     chunk_fwd_kda(q, k, v, beta, g, ...), recurrent_step_kda(q, k, v, beta, g, state)
         # KDA: one log keep rate per key channel
     qk_prepare(q, k, scale=1.0, l2norm=True)  # the q/k L2-norm and query scale as a pass
@@ -38,9 +39,9 @@ import ctypes
 from ._lib import (DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05, DN_BF16, DN_F32,
                    DeltaNetError, QkNorm, check, header_symbols, lib_path, load)
 
-__all__ = ["chunk_fwd", "chunk_fwd_split", "chunk_bwd", "chunk_bwd_varlen", "chunk_bwd_gated", "recurrent_step", "chunk_fwd_varlen", "chunk_fwd_gated",
+__all__ = ["chunk_fwd", "chunk_fwd_split", "chunk_bwd", "chunk_bwd_varlen", "chunk_bwd_gated", "chunk_bwd_kda", "recurrent_step", "chunk_fwd_varlen", "chunk_fwd_gated",
            "recurrent_step_gated", "chunk_fwd_kda", "recurrent_step_kda", "qk_prepare",
-           "qk_prepare_bwd", "DeltaRule", "GatedDeltaRule", "DeltaNetError", "load", "lib_path",
+           "qk_prepare_bwd", "DeltaRule", "GatedDeltaRule", "KdaDeltaRule", "DeltaNetError", "load", "lib_path",
            "header_symbols", "ALGOS"]
 
 ALGOS = {"auto": DN_ALGO_AUTO, "simt": DN_ALGO_SIMT, "tcgen05": DN_ALGO_TCGEN05}
@@ -352,6 +353,32 @@ class DeltaRule(torch.autograd.Function):
         return d_q, d_k, d_v, d_beta, (d_S0 if S0 is not None else None), None, None
 
 
+def _decayed_forward(ctx, per_channel, q, k, v, beta, g, initial_state, scale, qk_l2norm):
+    q, k, v, beta, g = (t.contiguous() for t in (q, k, v, beta, g))
+    if initial_state is not None:
+        initial_state = initial_state.contiguous()
+    fwd = chunk_fwd_kda if per_channel else chunk_fwd_gated
+    o, S_T = fwd(q, k, v, beta, g, initial_state=initial_state, output_final_state=True,
+                 scale=scale, qk_l2norm=qk_l2norm)
+    ctx.save_for_backward(q, k, v, beta, g, initial_state)
+    ctx.scale, ctx.l2norm = scale, bool(qk_l2norm)
+    return o, S_T
+
+
+def _decayed_backward(ctx, per_channel, d_o, d_S_T):
+    q, k, v, beta, g, S0 = ctx.saved_tensors
+    d_o = torch.zeros_like(v) if d_o is None else d_o.contiguous()
+    d_S_T = None if d_S_T is None else d_S_T.contiguous().float()
+    prepared = ctx.scale is not None or ctx.l2norm
+    scale = 1.0 if ctx.scale is None else ctx.scale
+    qp, kp = qk_prepare(q, k, scale=scale, l2norm=ctx.l2norm) if prepared else (q, k)
+    bwd = chunk_bwd_kda if per_channel else chunk_bwd_gated
+    d_q, d_k, d_v, d_beta, d_g, d_S0 = bwd(qp, kp, v, beta, g, d_o.to(v.dtype), S0, d_S_T)
+    if prepared:
+        d_q, d_k = qk_prepare_bwd(q, k, d_q, d_k, scale=scale, l2norm=ctx.l2norm)
+    return (d_q, d_k, d_v, d_beta, d_g, (d_S0 if S0 is not None else None), None, None)
+
+
 class GatedDeltaRule(torch.autograd.Function):
     """Autograd wrapper for Gated DeltaNet: ``GatedDeltaRule.apply(q, k, v,
     beta, g, initial_state, scale, qk_l2norm)`` returns ``(o, final_state)``
@@ -362,28 +389,25 @@ class GatedDeltaRule(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, q, k, v, beta, g, initial_state=None, scale=None, qk_l2norm=False):
-        q, k, v, beta, g = (t.contiguous() for t in (q, k, v, beta, g))
-        if initial_state is not None:
-            initial_state = initial_state.contiguous()
-        o, S_T = chunk_fwd_gated(q, k, v, beta, g, initial_state=initial_state,
-                                 output_final_state=True, scale=scale, qk_l2norm=qk_l2norm)
-        ctx.save_for_backward(q, k, v, beta, g, initial_state)
-        ctx.scale, ctx.l2norm = scale, bool(qk_l2norm)
-        return o, S_T
+        return _decayed_forward(ctx, False, q, k, v, beta, g, initial_state, scale, qk_l2norm)
 
     @staticmethod
     def backward(ctx, d_o, d_S_T):
-        q, k, v, beta, g, S0 = ctx.saved_tensors
-        d_o = torch.zeros_like(v) if d_o is None else d_o.contiguous()
-        d_S_T = None if d_S_T is None else d_S_T.contiguous().float()
-        prepared = ctx.scale is not None or ctx.l2norm
-        scale = 1.0 if ctx.scale is None else ctx.scale
-        qp, kp = qk_prepare(q, k, scale=scale, l2norm=ctx.l2norm) if prepared else (q, k)
-        d_q, d_k, d_v, d_beta, d_g, d_S0 = chunk_bwd_gated(qp, kp, v, beta, g, d_o.to(v.dtype),
-                                                           S0, d_S_T)
-        if prepared:
-            d_q, d_k = qk_prepare_bwd(q, k, d_q, d_k, scale=scale, l2norm=ctx.l2norm)
-        return (d_q, d_k, d_v, d_beta, d_g, (d_S0 if S0 is not None else None), None, None)
+        return _decayed_backward(ctx, False, d_o, d_S_T)
+
+
+class KdaDeltaRule(torch.autograd.Function):
+    """Autograd wrapper for KDA: as ``GatedDeltaRule`` with ``chunk_fwd_kda``
+    and ``chunk_bwd_kda``; ``g`` is the fp32 ``[B, H, T, dk]`` per-key-channel
+    log keep rate."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, beta, g, initial_state=None, scale=None, qk_l2norm=False):
+        return _decayed_forward(ctx, True, q, k, v, beta, g, initial_state, scale, qk_l2norm)
+
+    @staticmethod
+    def backward(ctx, d_o, d_S_T):
+        return _decayed_backward(ctx, True, d_o, d_S_T)
 
 
 def _check_gate(g: torch.Tensor, shape, dev) -> None:
@@ -595,6 +619,26 @@ def chunk_bwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: tor
     d_beta, d_g, d_initial_state)`` for L = <d_o, o> + <d_final_state,
     final_state>; ``d_g`` fp32 like ``g``.
     """
+    return _bwd_decayed(q, k, v, beta, g, d_o, initial_state, d_final_state, chunk_size,
+                        workspace, per_channel=False)
+
+
+def chunk_bwd_kda(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                  g: torch.Tensor, d_o: torch.Tensor, initial_state: torch.Tensor | None = None,
+                  d_final_state: torch.Tensor | None = None, chunk_size: int = 64,
+                  workspace: torch.Tensor | None = None):
+    """Gradients of ``chunk_fwd_kda`` (``dn_chunk_bwd_kda``).
+
+    ``g``: fp32 ``[B, H, T, dk]`` per-key-channel log keep rates.  Returns
+    ``(d_q, d_k, d_v, d_beta, d_g, d_initial_state)`` for L = <d_o, o> +
+    <d_final_state, final_state>; ``d_g`` fp32 like ``g``.
+    """
+    return _bwd_decayed(q, k, v, beta, g, d_o, initial_state, d_final_state, chunk_size,
+                        workspace, per_channel=True)
+
+
+def _bwd_decayed(q, k, v, beta, g, d_o, initial_state, d_final_state, chunk_size, workspace,
+                 per_channel):
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g), ("d_o", d_o)):
         _check_cuda(name, t, dev)
@@ -607,15 +651,18 @@ def chunk_bwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: tor
     dv = v.shape[3]
     if tuple(v.shape[:3]) != (B, H, T) or tuple(beta.shape) != (B, H, T):
         raise ValueError("v must be [B,H,T,dv] and beta [B,H,T]")
-    if g.dtype != torch.float32 or tuple(g.shape) != (B, H, T):
-        raise ValueError("g must be float32 [B,H,T]")
+    gshape = (B, H, T, dk) if per_channel else (B, H, T)
+    if g.dtype != torch.float32 or tuple(g.shape) != gshape:
+        raise ValueError(f"g must be float32 {list(gshape)}")
     for name, t in (("initial_state", initial_state), ("d_final_state", d_final_state)):
         if t is not None:
             _check_cuda(name, t, dev)
             if t.dtype != torch.float32 or tuple(t.shape) != (B, H, dk, dv):
                 raise ValueError(f"{name} must be float32 [B,H,dk,dv]")
     lib = load()
-    need = lib.dn_chunk_bwd_gated_workspace_bytes(B, H, T, dk, dv, chunk_size, dt)
+    fn, ws_fn = ((lib.dn_chunk_bwd_kda, lib.dn_chunk_bwd_kda_workspace_bytes) if per_channel else
+                 (lib.dn_chunk_bwd_gated, lib.dn_chunk_bwd_gated_workspace_bytes))
+    need = ws_fn(B, H, T, dk, dv, chunk_size, dt)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     _check_cuda("workspace", workspace, dev)
@@ -623,7 +670,7 @@ def chunk_bwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: tor
              torch.empty_like(beta), torch.empty_like(g),
              torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)]
     with torch.cuda.device(dev):
-        check(lib.dn_chunk_bwd_gated(
+        check(fn(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), beta.data_ptr(), g.data_ptr(),
             initial_state.data_ptr() if initial_state is not None else None, d_o.data_ptr(),
             d_final_state.data_ptr() if d_final_state is not None else None,

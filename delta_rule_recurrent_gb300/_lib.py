@@ -16,7 +16,7 @@ HEADER = INCLUDE / "deltanet.h"
 DN_OK, DN_ERR_INVALID_ARG, DN_ERR_UNSUPPORTED, DN_ERR_CUDA = 0, 1, 2, 3
 DN_F32, DN_BF16 = 0, 1
 DN_ALGO_AUTO, DN_ALGO_SIMT, DN_ALGO_TCGEN05 = 0, 1, 2
-ABI_VERSION = 8
+ABI_VERSION = 9
 
 _vp, _fp = ctypes.c_void_p, ctypes.c_void_p
 _int, _size = ctypes.c_int, ctypes.c_size_t
@@ -84,6 +84,9 @@ SIGNATURES = {
     "dn_chunk_bwd_gated": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp, _vp, _vp, _vp, _vp, _fp,
                                   _fp] + [_int] * 7 + [_vp, _size, _vp]),
     "dn_chunk_bwd_gated_workspace_bytes": (_size, [_int] * 7),
+    "dn_chunk_bwd_kda": (_int, [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp, _vp, _vp, _vp, _vp, _fp,
+                                _fp] + [_int] * 7 + [_vp, _size, _vp]),
+    "dn_chunk_bwd_kda_workspace_bytes": (_size, [_int] * 7),
 }
 
 _lib = None

@@ -778,15 +778,20 @@ size_t dn_chunk_bwd_gated_workspace_bytes(int B, int H, int T, int dk, int dv, i
     return dn::chunk_bwd_gated_workspace_bytes((int)BH, T, dk, dv, dt);
 }
 
-int dn_chunk_bwd_gated(const void* q, const void* k, const void* v, const void* beta,
-                       const float* g, const float* S0, const void* d_o, const float* d_S_T,
-                       void* d_q, void* d_k, void* d_v, void* d_beta, float* d_g, float* d_S0,
-                       int B, int H, int T, int dk, int dv, int C, int dt, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+// The gated and KDA backwards: g and d_g are fp32 with one rate per token
+// (gated) or per token and key channel (KDA).
+static int chunk_bwd_decayed(const void* q, const void* k, const void* v, const void* beta,
+                             const float* g, const float* S0, const void* d_o,
+                             const float* d_S_T, void* d_q, void* d_k, void* d_v, void* d_beta,
+                             float* d_g, float* d_S0, int B, int H, int T, int dk, int dv, int C,
+                             int dt, void* workspace, size_t workspace_bytes, void* stream,
+                             bool per_channel) {
     if (int st = check_bwd_sizes(B, H, T, dk, dv, C, dt, "B")) return st;
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return fail(DN_ERR_INVALID_ARG, "B*H too large");
-    const size_t need_ws = dn_chunk_bwd_gated_workspace_bytes(B, H, T, dk, dv, C, dt);
+    const size_t need_ws = per_channel
+                               ? dn_chunk_bwd_kda_workspace_bytes(B, H, T, dk, dv, C, dt)
+                               : dn_chunk_bwd_gated_workspace_bytes(B, H, T, dk, dv, C, dt);
     if (workspace_bytes < need_ws || (need_ws > 0 && !workspace))
         return fail(DN_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
                     need_ws);
@@ -795,11 +800,13 @@ int dn_chunk_bwd_gated(const void* q, const void* k, const void* v, const void* 
     if (int st = check_bwd_spans(q, k, v, beta, S0, d_o, d_S_T, d_q, d_k, d_v, d_beta, d_S0,
                                  ntok, BH, T, dk, dv, dt, workspace, need_ws))
         return st;
-    if (T > 0) {  // the log keep rates and their gradient: fp32 [B, H, T]
+    if (T > 0) {  // the log keep rates and their gradient
         int dev = 0;
         if (int st = current_device(&dev)) return st;
-        const Span sg{"g", g, ntok * sizeof(float)}, sdg{"d_g", d_g, ntok * sizeof(float)};
-        if (int st = check_device_ptr(sg, 4, dev)) return st;
+        const size_t gb = ntok * (per_channel ? (size_t)dk : 1) * sizeof(float);
+        const int galign = per_channel ? 16 : 4;  // KDA's rates load as 16-byte rows
+        const Span sg{"g", g, gb}, sdg{"d_g", d_g, gb};
+        if (int st = check_device_ptr(sg, galign, dev)) return st;
         if (int st = check_device_ptr(sdg, 4, dev)) return st;
         const size_t es = elem_size(dt), sb = (size_t)BH * dk * dv * sizeof(float);
         const Span others[] = {{"q", q, ntok * dk * es},     {"k", k, ntok * dk * es},
@@ -808,7 +815,7 @@ int dn_chunk_bwd_gated(const void* q, const void* k, const void* v, const void* 
                                {"d_S_T", d_S_T, sb},         {"d_q", d_q, ntok * dk * es},
                                {"d_k", d_k, ntok * dk * es}, {"d_v", d_v, ntok * dv * es},
                                {"d_beta", d_beta, ntok * es}, {"d_S0", d_S0, sb},
-                               {"workspace", workspace, need_ws}, {"g", g, ntok * sizeof(float)}};
+                               {"workspace", workspace, need_ws}, sg};
         for (const Span& s : others)
             if (overlaps(sdg, s)) return fail(DN_ERR_INVALID_ARG, "d_g overlaps %s", s.name);
         for (int i = 7; i < 13; ++i)  // the outputs and the workspace against g
@@ -825,11 +832,43 @@ int dn_chunk_bwd_gated(const void* q, const void* k, const void* v, const void* 
         return cuda_status(cudaMemsetAsync(d_S0, 0, sb, st), "cudaMemsetAsync(d_S0)");
     }
     const char* stage = "launch";
-    const cudaError_t e = dn::launch_chunk_bwd_gated(q, k, v, beta, g, S0, d_o, d_S_T, d_q, d_k,
-                                                     d_v, d_beta, d_g, d_S0, (int)BH, T, dk, dv,
-                                                     dt, workspace, st, &stage);
+    const cudaError_t e =
+        per_channel
+            ? dn::launch_chunk_bwd_kda(q, k, v, beta, g, S0, d_o, d_S_T, d_q, d_k, d_v, d_beta,
+                                       d_g, d_S0, (int)BH, T, dk, dv, dt, workspace, st, &stage)
+            : dn::launch_chunk_bwd_gated(q, k, v, beta, g, S0, d_o, d_S_T, d_q, d_k, d_v, d_beta,
+                                         d_g, d_S0, (int)BH, T, dk, dv, dt, workspace, st,
+                                         &stage);
     if (e == cudaSuccess) return ok();
-    return fail(DN_ERR_CUDA, "gated chunk backward (%s): %s", stage, cudaGetErrorString(e));
+    return fail(DN_ERR_CUDA, "%s chunk backward (%s): %s", per_channel ? "KDA" : "gated", stage,
+                cudaGetErrorString(e));
+}
+
+int dn_chunk_bwd_gated(const void* q, const void* k, const void* v, const void* beta,
+                       const float* g, const float* S0, const void* d_o, const float* d_S_T,
+                       void* d_q, void* d_k, void* d_v, void* d_beta, float* d_g, float* d_S0,
+                       int B, int H, int T, int dk, int dv, int C, int dt, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    return chunk_bwd_decayed(q, k, v, beta, g, S0, d_o, d_S_T, d_q, d_k, d_v, d_beta, d_g, d_S0,
+                             B, H, T, dk, dv, C, dt, workspace, workspace_bytes, stream, false);
+}
+
+size_t dn_chunk_bwd_kda_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int dt) {
+    if (B <= 0 || H <= 0 || T <= 0 || C != 64 || !supported_dim(dk) || !supported_dim(dv) ||
+        (dt != DN_F32 && dt != DN_BF16))
+        return 0;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return 0;
+    return dn::chunk_bwd_kda_workspace_bytes((int)BH, T, dk, dv);
+}
+
+int dn_chunk_bwd_kda(const void* q, const void* k, const void* v, const void* beta,
+                     const float* g, const float* S0, const void* d_o, const float* d_S_T,
+                     void* d_q, void* d_k, void* d_v, void* d_beta, float* d_g, float* d_S0,
+                     int B, int H, int T, int dk, int dv, int C, int dt, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+    return chunk_bwd_decayed(q, k, v, beta, g, S0, d_o, d_S_T, d_q, d_k, d_v, d_beta, d_g, d_S0,
+                             B, H, T, dk, dv, C, dt, workspace, workspace_bytes, stream, true);
 }
 
 size_t dn_chunk_bwd_varlen_workspace_bytes(const int* cu_seqlens, int N, int H, int dk, int dv,

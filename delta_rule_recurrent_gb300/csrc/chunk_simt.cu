@@ -450,12 +450,12 @@ cudaError_t launch_chunk_simt_varlen(const void* q, const void* k, const void* v
 cudaError_t launch_chunk_simt_kda(const void* q, const void* k, const void* v, const void* beta,
                                   const float* g, const float* S0, void* o, float* S_T, int BH,
                                   int T, int dk, int dv, int dt, cudaStream_t st,
-                                  const QkNorm& norm) {
+                                  const QkNorm& norm, float* S_chunks) {
     if (BH <= 0 || T <= 0) return cudaSuccess;
 #define DN_SIMT_KDA(T_, DK_, DV_)                                                              \
     if (dk == DK_ && dv == DV_)                                                                \
-        return launch_typed<T_, DK_, DV_, 1, true>(q, k, v, beta, S0, o, S_T, nullptr, g, BH, T, \
-                                                   st, 1, nullptr, norm);
+        return launch_typed<T_, DK_, DV_, 1, true>(q, k, v, beta, S0, o, S_T, S_chunks, g, BH,   \
+                                                   T, st, 1, nullptr, norm);
     if (dt == 0) {
         DN_SIMT_KDA(float, 128, 128)
         DN_SIMT_KDA(float, 128, 64)

@@ -95,6 +95,17 @@ cudaError_t launch_chunk_bwd_gated(const void* q, const void* k, const void* v, 
                                    int dv, int dt, void* workspace, cudaStream_t stream,
                                    const char** stage);
 
+// KDA's backward (g, d_g: fp32 [BH][T][dk]): the states recomputed by the
+// CUDA-core KDA forward, then its chain and per-chunk gradients with the
+// per-channel decay.  The workspace holds the fp32 S and G of every chunk.
+size_t chunk_bwd_kda_workspace_bytes(int BH, int T, int dk, int dv);
+cudaError_t launch_chunk_bwd_kda(const void* q, const void* k, const void* v, const void* beta,
+                                 const float* g, const float* S0, const void* d_o,
+                                 const float* d_S_T, void* d_q, void* d_k, void* d_v,
+                                 void* d_beta, float* d_g, float* d_S0, int BH, int T, int dk,
+                                 int dv, int dt, void* workspace, cudaStream_t stream,
+                                 const char** stage);
+
 // The backward of the packed-sequence forward (cu: N + 1 host offsets into
 // the [H][T][d] tensors; states [N][H][dk][dv]): one batched backward per
 // sequence on gathered copies, in the scratch this many bytes hold.
@@ -192,11 +203,13 @@ cudaError_t launch_kda_decay(const void* q, const void* k, const float* g, void*
 cudaError_t launch_kda_fix(const void* q, const void* k, const void* beta, const float* g,
                            const int* fix, void* tiles, int BH, int T, const QkNorm& nm,
                            cudaStream_t stream);
-// KDA: g is the fp32 [BH][T][dk] per-key-channel log keep rate.
+// KDA: g is the fp32 [BH][T][dk] per-key-channel log keep rate.  With
+// S_chunks (fp32 [BH][chunk][dk][dv]) it records the state at every chunk
+// start; o may then be null.
 cudaError_t launch_chunk_simt_kda(const void* q, const void* k, const void* v, const void* beta,
                                   const float* g, const float* S0, void* o, float* S_T, int BH,
                                   int T, int dk, int dv, int dt, cudaStream_t stream,
-                                  const QkNorm& norm = kNoNorm);
+                                  const QkNorm& norm = kNoNorm, float* S_chunks = nullptr);
 cudaError_t launch_chunk_simt_varlen(const void* q, const void* k, const void* v,
                                      const void* beta, const float* S0, void* o, float* S_T,
                                      const VarlenTable& seqs, int H, int T, int dk, int dv,

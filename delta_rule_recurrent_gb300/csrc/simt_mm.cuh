@@ -69,6 +69,17 @@ struct Fp32Ops {
 #pragma unroll
             for (int j = 0; j < N / 16; ++j) f(ty + 16 * i, tx + 16 * j, acc.v[i][j]);
     }
+
+    // f(m, n, a&, b&) for every element the calling thread owns in two
+    // accumulators of one shape (in place)
+    template <int M, int N, typename F>
+    static __device__ __forceinline__ void update2(Acc<M, N>& a, Acc<M, N>& b, F f) {
+        const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll
+        for (int i = 0; i < M / 16; ++i)
+#pragma unroll
+            for (int j = 0; j < N / 16; ++j) f(ty + 16 * i, tx + 16 * j, a.v[i][j], b.v[i][j]);
+    }
 };
 
 template <int NW>
@@ -144,6 +155,20 @@ struct Tf32Ops {
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
                     f(m0 + 64 * i + g + 8 * (r >> 1), n0 + 8 * j + 2 * q + (r & 1), acc.v[i][j][r]);
+    }
+
+    template <int M, int N, typename F>
+    static __device__ __forceinline__ void update2(Acc<M, N>& a, Acc<M, N>& b, F f) {
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+        const int m0 = 16 * (w & 3), n0 = (w >> 2) * (N / kParts);
+#pragma unroll
+        for (int i = 0; i < M / 64; ++i)
+#pragma unroll
+            for (int j = 0; j < N / (8 * kParts); ++j)
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    f(m0 + 64 * i + g + 8 * (r >> 1), n0 + 8 * j + 2 * q + (r & 1), a.v[i][j][r],
+                      b.v[i][j][r]);
     }
 };
 

@@ -6,6 +6,8 @@
     python -m delta_rule_recurrent_gb300.profile_run gated [--B 8] [--T 2048] [--reps 3] [--no-workspace]
     python -m delta_rule_recurrent_gb300.profile_run kda [--B 8] [--T 2048] [--reps 3]
     python -m delta_rule_recurrent_gb300.profile_run long [--T 32768] [--reps 2] [--segments 0]
+    python -m delta_rule_recurrent_gb300.profile_run gbwd [--B 8] [--T 2048] [--reps 2]
+    python -m delta_rule_recurrent_gb300.profile_run kbwd [--B 8] [--T 2048] [--reps 2]
 
 `chunk` runs the chunkwise forward on the 1.3B-layer shape (B8 H16 T2048
 dk=dv=128, bf16; B and T can be reduced; the tensor-core path runs in two
@@ -16,7 +18,9 @@ runs the Gated DeltaNet chunkwise forward there (keep rates U(0.9, 1); two
 tcgen05 passes, or the CUDA-core kernel with --no-workspace); `kda` runs the
 KDA chunkwise forward there (per-channel keep rates U(0.9, 1)); `long` runs
 the long-prefill shape (B1 H16 T32768, fp32 initial state) through the
-sequence split (dn_chunk_fwd_split; --segments 0 fills the GPU once).
+sequence split (dn_chunk_fwd_split; --segments 0 fills the GPU once);
+`gbwd` and `kbwd` run the Gated DeltaNet and KDA backwards on the 1.3B-layer
+shape (keep rates U(0.9, 1), per token or per key channel).
 Inputs come from the seeded generators in `workloads`.
 """
 from __future__ import annotations
@@ -35,7 +39,7 @@ def main(argv=None):
     import workloads
 
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("what", choices=["chunk", "decode", "bwd", "gated", "kda", "long"])
+    ap.add_argument("what", choices=["chunk", "decode", "bwd", "gated", "kda", "long", "gbwd", "kbwd"])
     ap.add_argument("--B", type=int, default=None)
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--algo", default="auto", choices=list(dn.ALGOS))
@@ -77,6 +81,17 @@ def main(argv=None):
         q, k, v, b, S0 = (x.to(dev) for x in (inp.q, inp.k, inp.v, inp.beta, inp.S0))
         for _ in range(a.reps):
             o, _ = dn.chunk_fwd_split(q, k, v, b, initial_state=S0, segments=a.segments)
+    elif a.what in ("gbwd", "kbwd"):
+        over = {k: v for k, v in (("B", a.B), ("T", a.T)) if v is not None}
+        inp = workloads.workload_inputs("layer1p3b_bf16", **over)
+        B, H, T, d = inp.q.shape
+        d_o, d_S = workloads.grad_inputs(B, H, T, d, d, dtype="bf16", seed=2, ds_std=0.1)
+        q, k, v, b, g_o, gS = (x.to(dev) for x in (inp.q, inp.k, inp.v, inp.beta, d_o, d_S))
+        kda = a.what == "kbwd"
+        g = workloads.gate_inputs(B, H, T, seed=7, channels=d if kda else None).to(dev)
+        fn = dn.chunk_bwd_kda if kda else dn.chunk_bwd_gated
+        for _ in range(a.reps):
+            o = fn(q, k, v, b, g, g_o, d_final_state=gS)[0]
     elif a.what == "bwd":
         over = {k: v for k, v in (("B", a.B), ("T", a.T)) if v is not None}
         inp = workloads.workload_inputs("layer1p3b_bf16", **over)

@@ -397,6 +397,35 @@ DN_API size_t dn_chunk_bwd_gated_workspace_bytes(int B, int H, int T, int dk, in
                                                  int dt);
 
 /*
+ * dn_chunk_bwd_kda -- the gradients of dn_chunk_fwd_kda's outputs: for
+ * L = <d_o, o> + <d_S_T, S_T>, the gradients with respect to q, k, v, beta,
+ * the per-key-channel log keep rates g and S0 ("Kimi Delta Attention :
+ * atténuation par canal" and "Transition diagonale-bas rang",
+ * fr.news.hada.io/topic?id=31925; the states recomputed as in
+ * "Hardware-efficient implementation", paperlayer.ai/abs/2406.06484v6).
+ *   g, d_g  [B, H, T, dk] fp32 (g 16-byte aligned); the rest as dn_chunk_bwd.
+ *   workspace  device scratch of dn_chunk_bwd_kda_workspace_bytes(...) bytes.
+ * The states are recomputed by the CUDA-core KDA forward and the gradients
+ * formed chunk by chunk on the CUDA cores (fp32 products for fp32 I/O, tf32
+ * tensor-core products with fp32 accumulation for bf16).  The decay ratios
+ * exp(G_t[c] - G_s[c]) sit inside the channel sums: as products of
+ * exp(G) and exp(-G) scaled operands while a chunk's decay stays within
+ * exp(-60) on every channel, else one exponential per ratio.  d_g[t][c] is
+ * the gradient of token t's log keep rate on key channel c.  Errors and
+ * overlap rules as dn_chunk_bwd; d_g may overlap nothing else.
+ */
+DN_API int dn_chunk_bwd_kda(const void *q, const void *k, const void *v, const void *beta,
+                            const float *g, const float *S0, const void *d_o,
+                            const float *d_S_T, void *d_q, void *d_k, void *d_v, void *d_beta,
+                            float *d_g, float *d_S0, int B, int H, int T, int dk, int dv, int C,
+                            int dt, void *workspace, size_t workspace_bytes, void *stream);
+/* Its scratch: the fp32 state and state gradient of every chunk,
+ * 2 * B * H * ceil(T / 64) * dk * dv * 4 bytes; 0 for invalid arguments.
+ * Host-only. */
+DN_API size_t dn_chunk_bwd_kda_workspace_bytes(int B, int H, int T, int dk, int dv, int C,
+                                               int dt);
+
+/*
  * dn_chunk_bwd_varlen -- the gradients of dn_chunk_fwd_varlen's outputs, as
  * dn_chunk_bwd gives them for the batched forward (the pages' backward with
  * the states recomputed: "Hardware-efficient implementation",
@@ -569,7 +598,7 @@ DN_API int dn_recurrent_step_kda_qk(const void *q, const void *k, const void *v,
 /* ABI version of this header (bumped on incompatible changes). */
 DN_API int dn_abi_version(void);
 
-#define DN_ABI_VERSION 8
+#define DN_ABI_VERSION 9
 
 #ifdef __cplusplus
 }

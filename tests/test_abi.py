@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dn_abi_version() == 8
+    assert lib.dn_abi_version() == 9
     assert lib.dn_status_string(0) == b"DN_OK"
     assert lib.dn_status_string(1) == b"DN_ERR_INVALID_ARG"
     assert lib.dn_status_string(2) == b"DN_ERR_UNSUPPORTED"
@@ -103,6 +103,25 @@ def test_kda_workspace_bytes(lib):
     assert f(1, 1, 0, 128, 128, 64, 1) == 0
     assert f(8, 16, 2048, 128, 128, 64, 0) == 0
     assert f(8, 16, 2048, 64, 64, 64, 1) == 0
+
+
+def test_kda_backward_workspace_bytes(lib):
+    """KDA's backward keeps the fp32 state and state gradient of every chunk;
+    invalid arguments need none."""
+    f = lib.dn_chunk_bwd_kda_workspace_bytes
+    assert f(8, 16, 2048, 128, 128, 64, 1) == 2 * 8 * 16 * 32 * 128 * 128 * 4
+    assert f(1, 2, 130, 64, 128, 64, 0) == 2 * 2 * 3 * 64 * 128 * 4
+    assert f(1, 1, 0, 128, 128, 64, 1) == 0
+    assert f(1, 1, 64, 96, 128, 64, 1) == 0
+    assert f(1, 1, 64, 128, 128, 32, 1) == 0
+
+
+def test_kda_backward_rejects_a_short_workspace_before_any_cuda_call(lib):
+    need = lib.dn_chunk_bwd_kda_workspace_bytes(1, 2, 130, 64, 64, 64, 0)
+    st = lib.dn_chunk_bwd_kda(*([None] * 14), 1, 2, 130, 64, 64, 64, 0,
+                              ctypes.c_void_p(4096), need - 1, None)
+    assert st == _lib.DN_ERR_INVALID_ARG
+    assert b"workspace" in lib.dn_last_error()
 
 
 def test_gated_rejects_a_short_workspace_before_any_cuda_call(lib):

@@ -859,7 +859,7 @@ size_t dn_chunk_bwd_kda_workspace_bytes(int B, int H, int T, int dk, int dv, int
         return 0;
     const long long BH = (long long)B * H;
     if (BH > 0x7fffffffLL) return 0;
-    return dn::chunk_bwd_kda_workspace_bytes((int)BH, T, dk, dv);
+    return dn::chunk_bwd_kda_workspace_bytes((int)BH, T, dk, dv, dt);
 }
 
 int dn_chunk_bwd_kda(const void* q, const void* k, const void* v, const void* beta,

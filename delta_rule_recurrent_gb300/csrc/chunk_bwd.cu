@@ -1188,10 +1188,11 @@ cudaError_t launch_chunk_bwd_gated(const void* q, const void* k, const void* v, 
     return cudaErrorNotSupported;
 }
 
-size_t chunk_bwd_kda_workspace_bytes(int BH, int T, int dk, int dv) {
+size_t chunk_bwd_kda_workspace_bytes(int BH, int T, int dk, int dv, int dt) {
     if (BH <= 0 || T <= 0) return 0;
     const size_t items = (size_t)BH * (size_t)((T + kC - 1) / kC);
-    return 2 * items * (size_t)dk * (size_t)dv * sizeof(float);
+    const size_t states = 2 * items * (size_t)dk * (size_t)dv * sizeof(float);
+    return states + (chunk_tc_supports(dk, dv, dt) ? chunk_tc_kda_workspace_bytes(BH, T) : 0);
 }
 
 cudaError_t launch_chunk_bwd_kda(const void* q, const void* k, const void* v, const void* beta,
@@ -1205,8 +1206,12 @@ cudaError_t launch_chunk_bwd_kda(const void* q, const void* k, const void* v, co
     const size_t per = (size_t)BH * ((T + kC - 1) / kC) * (size_t)dk * dv;
     float* const Sc = static_cast<float*>(workspace);
     float* const Gc = Sc + per;
-    cudaError_t err = launch_chunk_simt_kda(q, k, v, beta, g, S0, nullptr, nullptr, BH, T, dk, dv,
-                                            dt, stream, kNoNorm, Sc);
+    cudaError_t err =
+        chunk_tc_supports(dk, dv, dt)
+            ? launch_chunk_tc_kda(q, k, v, beta, g, S0, nullptr, nullptr, BH, T, dk, dv, dt,
+                                  Gc + per, stream, kNoNorm, Sc)
+            : launch_chunk_simt_kda(q, k, v, beta, g, S0, nullptr, nullptr, BH, T, dk, dv, dt,
+                                    stream, kNoNorm, Sc);
     if (err != cudaSuccess) return err;
     *stage = "KDA chain and gradients";
 #define DN_KBWD_CASE(T_, DK_, DV_)                                                              \

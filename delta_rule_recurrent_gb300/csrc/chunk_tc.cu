@@ -1780,7 +1780,6 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
     }
     tmem_wait_st();
 
-    static_assert(!(kKda && kRec), "no state recording on the KDA form");
     constexpr bool kSide = kGate || kKda;
     for (int c = 0; c < nchunks; ++c) {
         const int g = c & 1;
@@ -1807,9 +1806,9 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
             if (t < 32) reinterpret_cast<float4*>(sdec)[t] = reinterpret_cast<const float4*>(slot)[t];
         }
         // S^T -> bf16 (dk 0-63, then 64-127); S itself recorded when asked: the
-        // plain form as a bf16 hi/lo tile pair, the gated one in fp32 (S_chunks
-        // then points at fp32 [BH][chunk][dk][dv])
-        if constexpr (kRec && kGate) {
+        // plain form as a bf16 hi/lo tile pair, the gated and KDA ones in fp32
+        // (S_chunks then points at fp32 [BH][chunk][dk][dv])
+        if constexpr (kRec && kSide) {
             float* const rec32 = reinterpret_cast<float*>(S_chunks) +
                                  ((size_t)bh * nchunks + c) * kD * kD + t;
             tmem_pack64_rec32(lane + C_ST, lane + C_SB, rec32);
@@ -2048,7 +2047,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
-    static_assert(!(kKda && (kGate || kRec || NMAX != 1)), "KDA on the batched forward");
+    static_assert(!(kKda && (kGate || NMAX != 1)), "KDA on the batched forward");
     const scan::Smem sm{base, kKda ? 2 : scan::kStages,
                         kKda ? kStageKQ + kTile : kStageKQ};
     int* const misc = reinterpret_cast<int*>(smem_raw + (base - raw_addr) + scan::OFF_MISC);
@@ -3404,10 +3403,10 @@ size_t chunk_tc_kda_workspace_bytes(int BH, int T) {
 cudaError_t launch_chunk_tc_kda(const void* q, const void* k, const void* v, const void* beta,
                                 const float* g, const float* S0, void* o, float* S_T, int BH,
                                 int T, int dk, int dv, int dt, void* workspace,
-                                cudaStream_t stream, const QkNorm& norm) {
+                                cudaStream_t stream, const QkNorm& norm, float* S_rec32) {
     if (!chunk_tc_supports(dk, dv, dt)) return cudaErrorNotSupported;
     if (BH <= 0 || T <= 0) return cudaSuccess;
-    if (!workspace || !o || !g) return cudaErrorInvalidValue;
+    if (!workspace || (!o && !S_rec32) || !g) return cudaErrorInvalidValue;
     const int nchunks = (T + kC - 1) / kC;
     const long long items = (long long)BH * nchunks;
     if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -3427,7 +3426,8 @@ cudaError_t launch_chunk_tc_kda(const void* q, const void* k, const void* v, con
         !make_ws_map(&mws, workspace, BH, nchunks))
         return cudaErrorInvalidValue;
     auto prep_kernel = chunk_prep_kernel<1, false, true>;
-    auto scan_kernel = chunk_scan_kernel<false, 1, false, true>;
+    auto scan_kernel = S_rec32 ? chunk_scan_kernel<true, 1, false, true>
+                               : chunk_scan_kernel<false, 1, false, true>;
     if ((err = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     kPrepSmemBytesSepB)) != cudaSuccess ||
         (err = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -3442,7 +3442,8 @@ cudaError_t launch_chunk_tc_kda(const void* q, const void* k, const void* v, con
     if ((err = launch_kda_fix(q, k, beta, g, fix, workspace, BH, T, norm, stream)) != cudaSuccess)
         return err;
     scan_kernel<<<BH, 512, scan::kSmemBytes, stream>>>(mq, mk, mv, mws, mkh, S0,
-                                                       static_cast<__nv_bfloat16*>(o), S_T, nullptr,
+                                                       static_cast<__nv_bfloat16*>(o), S_T,
+                                                       reinterpret_cast<__nv_bfloat16*>(S_rec32),
                                                        T, 1, batched, side);
     return cudaGetLastError();
 }

@@ -96,9 +96,11 @@ cudaError_t launch_chunk_bwd_gated(const void* q, const void* k, const void* v, 
                                    const char** stage);
 
 // KDA's backward (g, d_g: fp32 [BH][T][dk]): the states recomputed by the
-// CUDA-core KDA forward, then its chain and per-chunk gradients with the
-// per-channel decay.  The workspace holds the fp32 S and G of every chunk.
-size_t chunk_bwd_kda_workspace_bytes(int BH, int T, int dk, int dv);
+// KDA forward (on tcgen05 for bf16 with dk = dv = 128, else on the CUDA
+// cores), then its chain and per-chunk gradients with the per-channel decay.
+// The workspace holds the fp32 S and G of every chunk, plus the tensor-core
+// forward's scratch where it runs.
+size_t chunk_bwd_kda_workspace_bytes(int BH, int T, int dk, int dv, int dt);
 cudaError_t launch_chunk_bwd_kda(const void* q, const void* k, const void* v, const void* beta,
                                  const float* g, const float* S0, const void* d_o,
                                  const float* d_S_T, void* d_q, void* d_k, void* d_v,
@@ -188,11 +190,14 @@ cudaError_t launch_chunk_tc_gated(const void* q, const void* k, const void* v, c
                                   float* S_rec32 = nullptr);
 // KDA on tensor cores (bf16, dk = dv = 128; g the fp32 [BH][T][dk] per-key-
 // channel log keep rate), with a workspace of chunk_tc_kda_workspace_bytes.
+// With S_rec32 (fp32 [BH][chunk][dk][dv]) the scan records the state at every
+// chunk start (for the backward's recompute) and o may be nullptr.
 size_t chunk_tc_kda_workspace_bytes(int BH, int T);
 cudaError_t launch_chunk_tc_kda(const void* q, const void* k, const void* v, const void* beta,
                                 const float* g, const float* S0, void* o, float* S_T, int BH,
                                 int T, int dk, int dv, int dt, void* workspace,
-                                cudaStream_t stream, const QkNorm& norm = kNoNorm);
+                                cudaStream_t stream, const QkNorm& norm = kNoNorm,
+                                float* S_rec32 = nullptr);
 // Its CUDA-core parts (kda_tc.cu): the decayed operands of every chunk
 // (qt, kt, kh, kb: [BH][T][128] bf16; side: 256 fp32 per chunk) with the list
 // of chunks beyond the separable range (fix: a count, then chunk indices;

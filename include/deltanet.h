@@ -405,8 +405,9 @@ DN_API size_t dn_chunk_bwd_gated_workspace_bytes(int B, int H, int T, int dk, in
  * "Hardware-efficient implementation", paperlayer.ai/abs/2406.06484v6).
  *   g, d_g  [B, H, T, dk] fp32 (g 16-byte aligned); the rest as dn_chunk_bwd.
  *   workspace  device scratch of dn_chunk_bwd_kda_workspace_bytes(...) bytes.
- * The states are recomputed by the CUDA-core KDA forward and the gradients
- * formed chunk by chunk on the CUDA cores (fp32 products for fp32 I/O, tf32
+ * The states are recomputed by the KDA forward (on tcgen05 for bf16 with
+ * dk = dv = 128, else on the CUDA cores) and the gradients formed chunk by
+ * chunk on the CUDA cores (fp32 products for fp32 I/O, tf32
  * tensor-core products with fp32 accumulation for bf16).  The decay ratios
  * exp(G_t[c] - G_s[c]) sit inside the channel sums: as products of
  * exp(G) and exp(-G) scaled operands while a chunk's decay stays within
@@ -420,8 +421,9 @@ DN_API int dn_chunk_bwd_kda(const void *q, const void *k, const void *v, const v
                             float *d_g, float *d_S0, int B, int H, int T, int dk, int dv, int C,
                             int dt, void *workspace, size_t workspace_bytes, void *stream);
 /* Its scratch: the fp32 state and state gradient of every chunk,
- * 2 * B * H * ceil(T / 64) * dk * dv * 4 bytes; 0 for invalid arguments.
- * Host-only. */
+ * 2 * B * H * ceil(T / 64) * dk * dv * 4 bytes, plus, for bf16 with
+ * dk = dv = 128, the tensor-core forward's scratch (as
+ * dn_chunk_fwd_kda_workspace_bytes); 0 for invalid arguments.  Host-only. */
 DN_API size_t dn_chunk_bwd_kda_workspace_bytes(int B, int H, int T, int dk, int dv, int C,
                                                int dt);
 

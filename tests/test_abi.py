@@ -106,10 +106,14 @@ def test_kda_workspace_bytes(lib):
 
 
 def test_kda_backward_workspace_bytes(lib):
-    """KDA's backward keeps the fp32 state and state gradient of every chunk;
+    """KDA's backward keeps the fp32 state and state gradient of every chunk,
+    plus the tensor-core forward's scratch where it recomputes the states;
     invalid arguments need none."""
     f = lib.dn_chunk_bwd_kda_workspace_bytes
-    assert f(8, 16, 2048, 128, 128, 64, 1) == 2 * 8 * 16 * 32 * 128 * 128 * 4
+    tc = lib.dn_chunk_fwd_kda_workspace_bytes(8, 16, 2048, 128, 128, 64, 1)
+    assert tc > 0
+    assert f(8, 16, 2048, 128, 128, 64, 1) == 2 * 8 * 16 * 32 * 128 * 128 * 4 + tc
+    assert f(8, 16, 2048, 128, 128, 64, 0) == 2 * 8 * 16 * 32 * 128 * 128 * 4
     assert f(1, 2, 130, 64, 128, 64, 0) == 2 * 2 * 3 * 64 * 128 * 4
     assert f(1, 1, 0, 128, 128, 64, 1) == 0
     assert f(1, 1, 64, 96, 128, 64, 1) == 0

@@ -641,17 +641,18 @@ struct ChainKdaSmem {
     static constexpr int kQ = kK + kC * LK;       // C x LK   queries, then Q o gamma
     static constexpr int kGk = kQ + kC * LK;      // C x LK   cumulative log decay, then K o f
     static constexpr int kD = kGk + kC * LK;      // C x LV   output gradient slice
-    static constexpr int kU = kD + kC * LV;       // C x LV   dU'
+    static constexpr int kU = kD + kC * LV;       // C x LV   A until X is formed, then dU'
     static constexpr int kV = kU + kC * LV;       // C x LV   dV
     static constexpr int kG = kV + kC * LV;       // DK x LV  state gradient slice
-    static constexpr int kA = kG + DK * LV;       // C x kLC  A
-    static constexpr int kX = kA + kC * kLC;      // C x kLC  (I + A)^{-1}
+    static constexpr int kA = kU;
+    static constexpr int kX = kG + DK * LV;       // C x kLC  (I + A)^{-1}
     static constexpr int kP = kX + kC * kLC;      // C x kLC  P
     static constexpr int kY = kP + kC * kLC;      // solve scratch
     static constexpr int kB = kY + 3 * 16 * 17;   // C        beta
     static constexpr int kGL = kB + kC;           // DK       G_L
     static constexpr int kFloats = kGL + DK;
     static constexpr size_t kBytes = sizeof(float) * kFloats;
+    static_assert(LV >= kLC, "A fits dU's region");
     static_assert(kBytes <= 232448, "one CTA's shared memory");
 };
 
@@ -714,8 +715,8 @@ chunk_bwd_chain_kda_kernel(const T* __restrict__ q, const T* __restrict__ k,
             Qs[t * LK + i] *= ga;
             Gk[t * LK + i] = kv * __expf(GL[i] - G);
         }
-        __syncthreads();
-        {   // dU' = P^T dO + (K o f) G
+        unit_lower_inverse64<NT, kLC>(Am, Xm, Ys);  // ends with a barrier; A is dead
+        {   // dU' = P^T dO + (K o f) G, over A's region
             typename Ops::template Acc<64, NV> acc;
             Ops::zero(acc);
             Ops::template mm<64, NV, kC>(acc, [&](int m, int s) { return Pm[s * kLC + m]; },
@@ -724,7 +725,7 @@ chunk_bwd_chain_kda_kernel(const T* __restrict__ q, const T* __restrict__ k,
                                [&](int i, int nn) { return Gs[i * LV + nn]; });
             Ops::for_each(acc, [&](int m, int nn, float x) { Us[m * LV + nn] = x; });
         }
-        unit_lower_inverse64<NT, kLC>(Am, Xm, Ys);  // ends with a barrier
+        __syncthreads();
         {   // dV = diag(beta) X^T dU'
             typename Ops::template Acc<64, NV> acc;
             Ops::zero(acc);
@@ -1098,7 +1099,7 @@ cudaError_t launch_bwd_kda_typed(const void* q, const void* k, const void* v, co
                                  const float* g, const void* d_o, const float* d_S_T, void* d_q,
                                  void* d_k, void* d_v, void* d_beta, float* d_g, float* d_S0,
                                  float* Sc, float* Gc, int BH, int Tlen, cudaStream_t stream) {
-    constexpr int NV = 32;
+    constexpr int NV = 64;
     using Ops = std::conditional_t<std::is_same_v<T, float>, simt::Fp32Ops, simt::Tf32Ops<8>>;
     using LC = ChainKdaSmem<DK, NV, Ops::kPad>;
     using LG = GradKdaSmem<DK, 16, Ops::kPad>;

@@ -36,6 +36,9 @@ sys.path.insert(0, str(ROOT))
 METRIC = "delta-rule chunk fwd tokens/s on 1 GB300 + % roofline; decode step HBM GB/s"
 HEADLINE = "layer1p3b_bf16"
 DECODE = "decode_bf16"
+# nominal dense tf32 / bf16 tensor rates (1.1 / 2.25 PFLOP/s): the peak of a tf32
+# contraction, scaled from the measured bf16 one
+TF32_PER_BF16_NOMINAL = 1.1 / 2.25
 LONG = "long_prefill_bf16"
 E_SLICES = 4  # batch slices of the pipelined end-to-end leg
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -532,6 +535,29 @@ def run_ours(args, rank, world, local):
         kd_region_s = max_over_ranks(kd_region_s, world)
         del dkgate, Sdk
 
+        # ---------------- the decayed backwards: Gated DeltaNet and KDA ---------
+        d_o, d_S = workloads.grad_inputs(B, H, T, dv, dk, dtype=w["dtype"], seed=w["seed"],
+                                         ds_std=0.1)
+        d_o, d_S = d_o.to(dev), d_S.to(dev)
+        dec_bwd = {}
+        for form, gshape, fn, wsfn in (
+                ("gated", None, dn.chunk_bwd_gated, lib.dn_chunk_bwd_gated_workspace_bytes),
+                ("kda", dk, dn.chunk_bwd_kda, lib.dn_chunk_bwd_kda_workspace_bytes)):
+            gg = workloads.gate_inputs(B, H, T, seed=w["seed"], channels=gshape).to(dev)
+            gws_b = torch.empty(wsfn(B, H, T, dk, dv, C, 1 if tc else 0), dtype=torch.uint8,
+                                device=dev)
+
+            def dec_bwd_step(_i, fn=fn, gg=gg, gws_b=gws_b):
+                fn(q, k, v, beta, gg, d_o, d_final_state=d_S, workspace=gws_b)
+
+            dsteps = max(1, min(args.steps, 3))
+            dec_bwd_step(0)
+            torch.cuda.synchronize()
+            r_s, r_launch = timed_loop(dec_bwd_step, dsteps, stream, world)
+            dec_bwd[form] = (max_over_ranks(r_s, world), r_launch, dsteps)
+            del gg, gws_b
+        del d_o, d_S
+
         # ---------------- long prefill: one long sequence per head, carried state --
         wl = workloads.WORKLOADS[LONG]
         lp = workloads.workload_inputs(LONG)
@@ -884,6 +910,32 @@ def run_ours(args, rank, world, local):
                                 "traffic": None, "peak_source": f"{peak_src} (copy bandwidth)",
                                 "bytes_per_launch": kdbytes, "launch_us": kd_launch_s * 1e6}},
     }
+    # The decayed backwards: recompute on tcgen05 (bf16, d = 128), chain and
+    # per-chunk gradients on tf32 mma.sync (bf16) or fp32 CUDA cores (fp32).
+    dec_tc = _tc_used(lib, dk, dv, q.dtype)
+    if dec_tc:
+        dpeak = peaks["bf16_tflops"] * TF32_PER_BF16_NOMINAL
+        dsrc = (f"{peak_src} bf16 dense burst x {TF32_PER_BF16_NOMINAL:.3f} "
+                "(nominal tf32 / bf16, 1.1 / 2.25 PFLOP/s)")
+        dbound, darith = "tensor", ("states recomputed on tcgen05; chain and per-chunk gradients "
+                                    "on tf32 mma.sync, fp32 accumulation")
+    else:
+        dpeak, dsrc = fp32_alu_tflops(2070.0), "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz"
+        dbound, darith = "alu", "fp32 CUDA cores"
+    decayed_backward = {}
+    for form, (r_s, r_launch, dsteps) in dec_bwd.items():
+        ls = statistics.mean(r_launch) / 1e3
+        decayed_backward[form] = {
+            "workload": HEADLINE, "steps": dsteps, "value": world * tokens * dsteps / r_s,
+            "unit": "tokens/s", "ms_per_step": 1e3 * r_s / dsteps, "arith": darith,
+            "gate": "alpha ~ U(0.9, 1)" + (" per key channel" if form == "kda" else ""),
+            "vs_plain_backward": ls / bwd_launch_s,
+            "roofline": {"bound": dbound, "achieved": bflops / ls / 1e12, "peak": dpeak,
+                         "unit": "TFLOP/s", "frac": bflops / ls / 1e12 / dpeak, "traffic": None,
+                         "peak_source": dsrc, "flops_per_launch": bflops,
+                         "flops_note": "the plain backward's products (the decay's elementwise "
+                                       "work not counted)",
+                         "launch_us": ls * 1e6}}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * region_s / args.steps,
@@ -901,6 +953,7 @@ def run_ours(args, rank, world, local):
         "qk_prepare": qk_prep,
         "gated": gated,
         "kda": kda,
+        "decayed_backward": decayed_backward,
         "e2e": {"value": world * tokens * e2e_steps / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": 1e3 * e2e_s / e2e_steps,
@@ -917,7 +970,11 @@ def run_ours(args, rank, world, local):
                          + psteps                                       # q/k preparation
                          + launches_per_call * psteps                   # forward preparing q, k
                          + (2 if gneed else 1) * gsteps + gsteps + nsteps  # gated: both forms, decode
-                         + (4 if kneed else 1) * gsteps + ksteps + nsteps),  # KDA: both forms, decode
+                         + (4 if kneed else 1) * gsteps + ksteps + nsteps   # KDA: both forms, decode
+                         # decayed backwards: recompute (2 or 4 launches on tcgen05, else 1),
+                         # chain, gradients
+                         + sum((2 + ((4 if f == "kda" else 2) if dec_tc else 1)) * d[2]
+                               for f, d in dec_bwd.items())),
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

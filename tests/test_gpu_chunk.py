@@ -195,9 +195,12 @@ def test_workspace_checks():
     _check(o.double().cpu().numpy(), S.double().cpu().numpy(), o_ref, S_ref, torch.bfloat16)
 
 
-def test_tensor_core_rejects_other_shapes():
+@pytest.mark.parametrize("dk,dv,dtype", [(128, 64, "bf16"), (64, 128, "bf16"), (128, 128, "f32")])
+def test_tensor_core_rejects_other_shapes(dk, dv, dtype):
+    """The tcgen05 path covers bf16 with dk = dv in {64, 128}; asking for it
+    on anything else is refused rather than run elsewhere."""
     from delta_rule_recurrent_gb300 import _lib
-    inp = workloads.chunk_inputs(1, 1, 64, 64, 64, dtype="bf16", seed=1)
+    inp = workloads.chunk_inputs(1, 1, 64, dk, dv, dtype=dtype, seed=1)
     with pytest.raises(_lib.DeltaNetError, match="UNSUPPORTED"):
         run_chunk(inp, "tcgen05")
 

@@ -260,9 +260,10 @@ struct GradSmem {
     // t1 = gamma dO . (Q S), t2 = gamma dV . (K S), t3 = (Gamma / gamma) (K G) . U',
     // then <G, S> in one float
     static constexpr int kGd = kB + kC;           // 7 x C + 4
+    static constexpr int kRs = kGd + 7 * kC + 4;  // 3 x 2 x C  gated: row-sum parts of t1, t2, t3
     // The work area: A and the solve scratch until X is formed, then the
     // value-slice operands, then C x C matrices once the slices are done.
-    static constexpr int kW = kGd + 7 * kC + 4;
+    static constexpr int kW = kRs + 6 * kC;
     static constexpr int kA = kW;                 // C x kLC  A
     static constexpr int kY = kA + kC * kLC;      // solve scratch
     static constexpr int kV = kW;                 // C x LS   V
@@ -323,6 +324,12 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
     float* t2 = t1 + kC;
     float* t3 = t2 + kC;
     float* t4 = t3 + kC;
+    // gated: each slice's row sums of t1, t2, t3 by column part (Ops::row_sums),
+    // added to t1, t2, t3 in a fixed order so that d_g is reproducible
+    float* rs1 = smem + L::kRs;
+    float* rs2 = rs1 + 2 * kC;
+    float* rs3 = rs2 + 2 * kC;
+    static_assert(Ops::kRowParts <= 2, "two column parts at most");
     const int tid = threadIdx.x;
     const int bh = blockIdx.x / nchunks, c = blockIdx.x % nchunks;
     const int t0 = c * kC, n = min(kC, Tlen - t0);
@@ -387,9 +394,9 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
                     Es[m * LS + nn] += y;
                     Us[m * LS + nn] = y;
                 });
-                Ops::for_each(qs, [&](int m, int nn, float x) {
-                    atomicAdd(&t1[m], gam[m] * Ds[m * LS + nn] * x);
-                });
+                Ops::row_sums(qs, [&](int m, int nn, float x) {
+                    return gam[m] * Ds[m * LS + nn] * x;
+                }, rs1);
             } else {
                 Ops::template mm<64, NS, DK>(e, [&](int m, int i) { return Ks[m * LK + i]; },
                                    [&](int i, int nn) { return Gs[i * LS + nn]; });
@@ -410,16 +417,29 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
                                [&](int s, int nn) { return Rv(s, nn); });
             Ops::template mm<64, NS, kC>(f, [&](int m, int s) { return Xm[s * kLC + m]; },
                                [&](int s, int nn) { return Es[s * LS + nn]; });
-            Ops::for_each(u, [&](int m, int nn, float x) {
-                if constexpr (kGate) atomicAdd(&t3[m], Us[m * LS + nn] * x);
-                Us[m * LS + nn] = x;
-            });
-            Ops::for_each(f, [&](int m, int nn, float x) {
-                Fs[m * LS + nn] = bs[m] * x;
-                if constexpr (kGate) atomicAdd(&t2[m], bs[m] * x * Rs[m * LS + nn]);
-            });
+            if constexpr (kGate) {  // each thread reads only the elements it then overwrites
+                Ops::row_sums(u, [&](int m, int nn, float x) { return Us[m * LS + nn] * x; }, rs3);
+                Ops::row_sums(f, [&](int m, int nn, float x) {
+                    return bs[m] * x * Rs[m * LS + nn];
+                }, rs2);
+            }
+            Ops::for_each(u, [&](int m, int nn, float x) { Us[m * LS + nn] = x; });
+            Ops::for_each(f, [&](int m, int nn, float x) { Fs[m * LS + nn] = bs[m] * x; });
         }
         __syncthreads();
+        if constexpr (kGate) {  // the slice's row sums, parts in order
+            if (tid < kC) {
+                float a1 = rs1[tid], a2 = rs2[tid], a3 = rs3[tid];
+                if (Ops::kRowParts == 2) {
+                    a1 += rs1[kC + tid];
+                    a2 += rs2[kC + tid];
+                    a3 += rs3[kC + tid];
+                }
+                t1[tid] += a1;
+                t2[tid] += a2;
+                t3[tid] += a3;
+            }
+        }
         // dP += dO U'^T, dTm += dU' R^T, dQ += dO S^T, dK += U' G^T - dV S^T
         // (gated: dQ's rows times gamma, U' G^T's times Gamma / gamma, dV S^T's times gamma)
         Ops::template mm<64, 64, NS>(aP, [&](int m, int j) { return Ds[m * LS + j]; },
@@ -437,7 +457,16 @@ chunk_bwd_grads_kernel(const T* __restrict__ q, const T* __restrict__ k,
         }, [&](int j, int i) { return Ss[i * LS + j]; });
         __syncthreads();
     }
-    if constexpr (kGate) atomicAdd(t4, t4p);
+    if constexpr (kGate) {  // <G, S>: warp sums, then the warps in order
+        const float wsum = warp_sum(t4p);
+        if ((tid & 31) == 0) rs1[tid >> 5] = wsum;
+        __syncthreads();
+        if (tid == 0) {
+            float s4 = 0.f;
+            for (int w = 0; w < NT / 32; ++w) s4 += rs1[w];
+            t4[0] = s4;
+        }
+    }
 
     // The work area now holds C x C matrices.
     float* dPm = smem + L::kW;

@@ -12,7 +12,7 @@
 //                in the m16n8 accumulator layout (lane 4g + q holds rows g,
 //                g + 8 at columns 2q, 2q + 1).
 // Each holds M N / kThreads floats per thread; an accumulator is only ever
-// read through the for_each of the policy that filled it.  kPad is the row padding
+// read through the for_each, update2 or row_sums of the policy that filled it.  kPad is the row padding
 // (floats) that keeps the policy's shared-memory operand reads free of bank
 // conflicts: an odd pitch for the per-thread FMA pattern, a pitch of 4 mod 32
 // for the fragment pattern (rows g = 0..7 by columns q = 0..3).
@@ -79,6 +79,24 @@ struct Fp32Ops {
         for (int i = 0; i < M / 16; ++i)
 #pragma unroll
             for (int j = 0; j < N / 16; ++j) f(ty + 16 * i, tx + 16 * j, a.v[i][j], b.v[i][j]);
+    }
+
+    // Row sums of f(m, n, value) in a fixed order: out[p * M + m] is the sum
+    // over the columns of part p (kRowParts parts), each written by exactly
+    // one thread.  Row ty + 16 i lives on the 16 lanes of one half-warp.
+    static constexpr int kRowParts = 1;
+    template <int M, int N, typename F>
+    static __device__ __forceinline__ void row_sums(const Acc<M, N>& acc, F f, float* out) {
+        const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll
+        for (int i = 0; i < M / 16; ++i) {
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < N / 16; ++j) s += f(ty + 16 * i, tx + 16 * j, acc.v[i][j]);
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+            if (tx == 0) out[ty + 16 * i] = s;
+        }
     }
 };
 
@@ -169,6 +187,31 @@ struct Tf32Ops {
                 for (int r = 0; r < 4; ++r)
                     f(m0 + 64 * i + g + 8 * (r >> 1), n0 + 8 * j + 2 * q + (r & 1), a.v[i][j][r],
                       b.v[i][j][r]);
+    }
+
+    // Row sums as Fp32Ops::row_sums; part p is the column part of warps
+    // w / 4 = p, and row g (g + 8) of a warp's block lives on its lanes 4 g .. 4 g + 3.
+    static constexpr int kRowParts = kParts;
+    template <int M, int N, typename F>
+    static __device__ __forceinline__ void row_sums(const Acc<M, N>& acc, F f, float* out) {
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+        const int m0 = 16 * (w & 3), n0 = (w >> 2) * (N / kParts), part = w >> 2;
+#pragma unroll
+        for (int i = 0; i < M / 64; ++i) {
+            float s[2] = {0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < N / (8 * kParts); ++j)
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    s[r >> 1] += f(m0 + 64 * i + g + 8 * (r >> 1), n0 + 8 * j + 2 * q + (r & 1),
+                                   acc.v[i][j][r]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                s[h] += __shfl_xor_sync(0xffffffffu, s[h], 1);
+                s[h] += __shfl_xor_sync(0xffffffffu, s[h], 2);
+                if (q == 0) out[part * M + m0 + 64 * i + g + 8 * h] = s[h];
+            }
+        }
     }
 };
 

@@ -663,6 +663,22 @@ __device__ __forceinline__ void form_a_p_kda_sep(const float* Ks, const float* Q
     Ops::for_each(ap, [&](int m, int nn, float x) { Pm[m * kLC + nn] = nn <= m ? x : 0.f; });
 }
 
+// The same from operands already scaled in shared memory: A2 = Kp Km^T and
+// P = Qp Km^T (Kp = K o exp G, Qp = Q o exp G, Km = K o exp(-G)).
+template <class Ops, int DK>
+__device__ __forceinline__ void form_a_p_scaled(const float* Kp, const float* Qp, const float* Km,
+                                                const float* bs, float* Am, float* Pm) {
+    constexpr int LK = DK + Ops::kPad, kLC = kC + Ops::kPad;
+    typename Ops::template Acc<64, 64> aa, ap;
+    Ops::zero(aa);
+    Ops::zero(ap);
+    const auto km = [&](int c, int nn) { return Km[nn * LK + c]; };
+    Ops::template mm<64, 64, DK>(aa, [&](int m, int c) { return Kp[m * LK + c]; }, km);
+    Ops::template mm<64, 64, DK>(ap, [&](int m, int c) { return Qp[m * LK + c]; }, km);
+    Ops::for_each(aa, [&](int m, int nn, float x) { Am[m * kLC + nn] = nn < m ? bs[m] * x : 0.f; });
+    Ops::for_each(ap, [&](int m, int nn, float x) { Pm[m * kLC + nn] = nn <= m ? x : 0.f; });
+}
+
 template <int DK, int NV, int PAD>
 struct ChainKdaSmem {
     static constexpr int LK = DK + PAD, LV = NV + PAD, kLC = kC + PAD;
@@ -732,17 +748,33 @@ chunk_bwd_chain_kda_kernel(const T* __restrict__ q, const T* __restrict__ k,
         load_rows<NT, NV, LV, DV>(Ds, d_o, tok0, t0, n, j0);
         if (tid < kC) bs[tid] = tid < n ? to_f32(beta[tok0 + t0 + tid]) : 0.f;
         const bool sep = chunk_decay_kda<NT, DK, LK>(gate, tok0 + t0, n, Gk, GL);
-        if (sep)
-            form_a_p_kda_sep<Ops, DK>(Ks, Qs, Gk, bs, Am, Pm, nullptr);
-        else
+        // Both forms leave K o gamma, Q o gamma and K o f in place of K, Q and G
+        // (the solve's barriers order these writes before the products below).
+        if (sep) {  // K o exp(-G) over G, the products plain, then exp G_L per channel
+            for (int e = tid; e < kC * DK; e += NT) {
+                const int t = e / DK, i = e % DK;
+                const float G = Gk[t * LK + i], kv = Ks[t * LK + i], ga = __expf(G);
+                Ks[t * LK + i] = kv * ga;
+                Qs[t * LK + i] *= ga;
+                Gk[t * LK + i] = kv * __expf(-G);
+            }
+            __syncthreads();
+            form_a_p_scaled<Ops, DK>(Ks, Qs, Gk, bs, Am, Pm);
+            __syncthreads();
+            for (int e = tid; e < kC * DK; e += NT) {
+                const int t = e / DK, i = e % DK;
+                Gk[t * LK + i] *= __expf(GL[i]);
+            }
+        } else {
             form_a_p_kda_exact<DK, LK, kLC>(Ks, Qs, Gk, bs, Am, Pm, nullptr);
-        __syncthreads();
-        for (int e = tid; e < kC * DK; e += NT) {  // K o gamma, Q o gamma, K o f in place
-            const int t = e / DK, i = e % DK;
-            const float G = Gk[t * LK + i], kv = Ks[t * LK + i], ga = __expf(G);
-            Ks[t * LK + i] = kv * ga;
-            Qs[t * LK + i] *= ga;
-            Gk[t * LK + i] = kv * __expf(GL[i] - G);
+            __syncthreads();
+            for (int e = tid; e < kC * DK; e += NT) {
+                const int t = e / DK, i = e % DK;
+                const float G = Gk[t * LK + i], kv = Ks[t * LK + i], ga = __expf(G);
+                Ks[t * LK + i] = kv * ga;
+                Qs[t * LK + i] *= ga;
+                Gk[t * LK + i] = kv * __expf(GL[i] - G);
+            }
         }
         unit_lower_inverse64<NT, kLC>(Am, Xm, Ys);  // ends with a barrier; A is dead
         {   // dU' = P^T dO + (K o f) G, over A's region

@@ -72,6 +72,15 @@ def test_head_widths_and_states(d, states):
     _check(_run(inp, g, d_o, d_S), ref, TOL[torch.float32], f"d={d} states={states}")
 
 
+@pytest.mark.parametrize("regime", ["mild", "extreme"])
+def test_bf16_64_wide_heads(regime):
+    """bf16 with d = 64: the states from the CUDA-core recompute, the chain
+    and gradients on the tf32 instances for 64-wide heads."""
+    inp, g, d_o, d_S = _case(2, 2, 150, 64, "bf16", seed=21, regime=regime)
+    ref = oracle.backward_gated(inp.q, inp.k, inp.v, inp.beta, g, d_o, inp.S0, d_S)
+    _check(_run(inp, g, d_o, d_S), ref, TOL[torch.bfloat16], f"bf16 d=64 {regime}")
+
+
 def test_zero_decay_matches_the_plain_backward():
     """g = 0: every gradient but d_g equals the plain backward's, both within
     fp32 rounding of each other."""

@@ -84,6 +84,16 @@ def test_head_widths_and_states(dk, dv, states):
     _check(_run(inp, g, d_o, d_S), ref, TOL[torch.float32], f"dk={dk} dv={dv} states={states}")
 
 
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128)])
+@pytest.mark.parametrize("regime", ["mild", "extreme"])
+def test_bf16_64_wide_keys(dk, dv, regime):
+    """bf16 with 64-wide keys: the states from the CUDA-core recompute, the
+    chain and gradients on the tf32 instances, in both ratio forms."""
+    inp, g, d_o, d_S = _case(2, 2, 150, dk, dv, "bf16", seed=dk + dv + 23, regime=regime)
+    ref = oracle.backward_kda(inp.q, inp.k, inp.v, inp.beta, g, d_o, inp.S0, d_S)
+    _check(_run(inp, g, d_o, d_S), ref, TOL[torch.bfloat16], f"bf16 dk={dk} dv={dv} {regime}")
+
+
 def test_equal_channels_match_the_gated_backward():
     """One rate on every key channel: the gated backward's gradients, and
     d_g's channels sum to the gated d_g, within fp32 rounding."""

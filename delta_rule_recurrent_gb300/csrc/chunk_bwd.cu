@@ -1155,11 +1155,13 @@ cudaError_t launch_bwd_gated_typed(const void* q, const void* k, const void* v, 
 
 // KDA's backward: its chain and per-chunk gradients, fp32 products on the
 // CUDA cores for fp32 I/O and tf32 tensor-core products for bf16 I/O.
+// chain_done: the tcgen05 chain has already written Gc, d_v and d_S0.
 template <typename T, int DK, int DV>
 cudaError_t launch_bwd_kda_typed(const void* q, const void* k, const void* v, const void* beta,
                                  const float* g, const void* d_o, const float* d_S_T, void* d_q,
                                  void* d_k, void* d_v, void* d_beta, float* d_g, float* d_S0,
-                                 float* Sc, float* Gc, int BH, int Tlen, cudaStream_t stream) {
+                                 float* Sc, float* Gc, int BH, int Tlen, cudaStream_t stream,
+                                 bool chain_done) {
     constexpr int NV = 64;
     using Ops = std::conditional_t<std::is_same_v<T, float>, simt::Fp32Ops, simt::Tf32Ops<8>>;
     using LC = ChainKdaSmem<DK, NV, Ops::kPad>;
@@ -1175,10 +1177,12 @@ cudaError_t launch_bwd_kda_typed(const void* q, const void* k, const void* v, co
         return err;
     const long long g_chain = (long long)BH * (DV / NV), g_grads = (long long)BH * nchunks;
     if (g_chain > 0x7fffffffLL || g_grads > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    chain<<<(unsigned)g_chain, Ops::kThreads, LC::kBytes, stream>>>(
-        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(beta),
-        static_cast<const T*>(d_o), d_S_T, static_cast<T*>(d_v), d_S0, Gc, Tlen, g);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (!chain_done) {
+        chain<<<(unsigned)g_chain, Ops::kThreads, LC::kBytes, stream>>>(
+            static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(beta),
+            static_cast<const T*>(d_o), d_S_T, static_cast<T*>(d_v), d_S0, Gc, Tlen, g);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
     grads<<<(unsigned)g_grads, Ops::kThreads, LG::kBytes, stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
         static_cast<const T*>(beta), static_cast<const T*>(d_o), Sc, Gc, static_cast<T*>(d_q),
@@ -1268,18 +1272,23 @@ cudaError_t launch_chunk_bwd_kda(const void* q, const void* k, const void* v, co
     const size_t per = (size_t)BH * ((T + kC - 1) / kC) * (size_t)dk * dv;
     float* const Sc = static_cast<float*>(workspace);
     float* const Gc = Sc + per;
+    const bool tc = chunk_tc_supports(dk, dv, dt);
     cudaError_t err =
-        chunk_tc_supports(dk, dv, dt)
-            ? launch_chunk_tc_kda(q, k, v, beta, g, S0, nullptr, nullptr, BH, T, dk, dv, dt,
-                                  Gc + per, stream, kNoNorm, Sc)
-            : launch_chunk_simt_kda(q, k, v, beta, g, S0, nullptr, nullptr, BH, T, dk, dv, dt,
-                                    stream, kNoNorm, Sc);
+        tc ? launch_chunk_tc_kda(q, k, v, beta, g, S0, nullptr, nullptr, BH, T, dk, dv, dt,
+                                 Gc + per, stream, kNoNorm, Sc)
+           : launch_chunk_simt_kda(q, k, v, beta, g, S0, nullptr, nullptr, BH, T, dk, dv, dt,
+                                   stream, kNoNorm, Sc);
     if (err != cudaSuccess) return err;
+    if (tc) {  // the chain on tcgen05, from the forward's decayed operands and tiles
+        *stage = "KDA state-gradient chain";
+        err = launch_chunk_bwd_chain_tc_kda(d_o, d_S_T, d_v, d_S0, Gc, Gc + per, BH, T, stream);
+        if (err != cudaSuccess) return err;
+    }
     *stage = "KDA chain and gradients";
 #define DN_KBWD_CASE(T_, DK_, DV_)                                                              \
     if (dk == DK_ && dv == DV_)                                                                 \
         return launch_bwd_kda_typed<T_, DK_, DV_>(q, k, v, beta, g, d_o, d_S_T, d_q, d_k, d_v,  \
-                                                   d_beta, d_g, d_S0, Sc, Gc, BH, T, stream);
+                                                   d_beta, d_g, d_S0, Sc, Gc, BH, T, stream, tc);
     if (dt == 0) {
         DN_KBWD_CASE(float, 128, 128)
         DN_KBWD_CASE(float, 128, 64)

@@ -2169,8 +2169,15 @@ enum : int {
 };
 constexpr int kBars = 28;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * kBars;
-constexpr uint32_t kSmemBytes = OFF_MISC + 16 + 1024;
+// KDA: 2 side slots of the chunk's keep factors exp G_C per key channel
+// (128 fp32, loaded with [PT; Tm]), then the state's copy of them.
+constexpr uint32_t kSideBytes = 512;
+constexpr uint32_t OFF_SIDE = OFF_MISC + 16;
+constexpr uint32_t OFF_DEC = OFF_SIDE + 2 * kSideBytes;
+constexpr uint32_t kSmemBytes = OFF_DEC + kSideBytes + 1024;
 static_assert(kSmemBytes <= 232448, "backward chain shared memory");
+static_assert(2 * (kStageKQ + kTile) <= kStages * kStageKQ, "KDA's two stages in the ring");
+static_assert(OFF_SIDE % 16 == 0 && OFF_DEC % 16 == 0, "bulk copies need 16-byte alignment");
 // TMEM columns: G^T fp32 | G^T bf16 | dV^T fp32 | dV^T bf16 | K^T Tm fp32
 constexpr uint32_t C_GT = 0, C_GB = 128, C_DV = 192, C_VB = 256, C_B2 = 288;
 constexpr uint32_t ID_MM64 = idesc_bf16_f32(128, 64, 1, 1);   // A, B both MN-major, N = 64
@@ -2178,38 +2185,56 @@ constexpr uint32_t ID_TM64 = idesc_bf16_f32(128, 64, 0, 1);   // A from TMEM, B 
 constexpr uint32_t ID_MM128 = idesc_bf16_f32(128, 128, 1, 1); // A, B both MN-major, N = 128
 constexpr uint32_t ID_TM128N = idesc_bf16_f32(128, 128, 0, 1) | (1u << 14);  // B negated
 
+// The [K; Q] ring: kStages stages of kStageKQ, or for KDA two stages that
+// also hold K^ = K o exp(G_C - G) (two 64-column dk halves, 8 KB apart).
 struct Smem {
     uint32_t base;
-    __device__ uint32_t kq(int i) const { return base + OFF_KQ + (uint32_t)(i % kStages) * kStageKQ; }
+    int nst = kStages;
+    uint32_t stage = kStageKQ;
+    __device__ uint32_t kq(int i) const { return base + OFF_KQ + (uint32_t)(i % nst) * stage; }
+    __device__ uint32_t kh(int i) const { return kq(i) + kStageKQ; }
+    __device__ uint32_t side(int g) const { return base + OFF_SIDE + (uint32_t)g * kSideBytes; }
     __device__ uint32_t dO(int i) const { return base + OFF_DO + (uint32_t)(i & 1) * kTile; }
     __device__ uint32_t tp(int i) const { return base + OFF_TP + (uint32_t)(i & 1) * kTile; }
     __device__ uint32_t b2(int i) const { return base + OFF_B2 + (uint32_t)(i & 1) * kTile; }
 };
 
-// Load i is chunk nchunks - 1 - i.
+// Load i is chunk nchunks - 1 - i.  KDA (tm_kh, side): K^ rides with each
+// stage and the chunk's keep factors with [PT; Tm] (side: this head's first
+// chunk's side vectors).
 __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q,
                          const CUtensorMap* tm_k, const CUtensorMap* tm_do,
-                         const CUtensorMap* tm_ws, int bh, int nchunks) {
+                         const CUtensorMap* tm_ws, int bh, int nchunks, const CUtensorMap* tm_kh,
+                         const float* side) {
+    const int ns = sm.nst;
     int nkq = 0, ndo = 0, ntp = 0;
     long long t0 = clock64();
     while ((nkq < nchunks || ndo < nchunks || ntp < nchunks) && !ctl.aborted()) {
         bool progressed = false;
         if (nkq < nchunks &&
-            (nkq < kStages ||
-             mbar_test_wait(ctl.bar(B_KQ_EMPTY + nkq % kStages), (uint32_t)(nkq / kStages - 1) & 1u))) {
+            (nkq < ns ||
+             mbar_test_wait(ctl.bar(B_KQ_EMPTY + nkq % ns), (uint32_t)(nkq / ns - 1) & 1u))) {
             const int y = (nchunks - 1 - nkq) * kC;
             const uint32_t st = sm.kq(nkq), bar = ctl.bar(B_KQ_FULL + nkq % kKQ);
-            mbar_arrive_expect_tx(bar, 4 * 8192);
+            mbar_arrive_expect_tx(bar, (tm_kh ? 6 : 4) * 8192);
             tma_load_3d(st, tm_k, bar, 0, y, bh);
             tma_load_3d(st + kRegKQ, tm_k, bar, 64, y, bh);
             tma_load_3d(st + 8192, tm_q, bar, 0, y, bh);
             tma_load_3d(st + kRegKQ + 8192, tm_q, bar, 64, y, bh);
-            if (nkq + kStages < nchunks) {  // warm L2 for this stage's next tiles
-                const int yn = (nchunks - 1 - nkq - kStages) * kC;
+            if (tm_kh) {
+                tma_load_3d(sm.kh(nkq), tm_kh, bar, 0, y, bh);
+                tma_load_3d(sm.kh(nkq) + 8192, tm_kh, bar, 64, y, bh);
+            }
+            if (nkq + ns < nchunks) {  // warm L2 for this stage's next tiles
+                const int yn = (nchunks - 1 - nkq - ns) * kC;
                 tma_prefetch_l2_3d(tm_k, 0, yn, bh);
                 tma_prefetch_l2_3d(tm_k, 64, yn, bh);
                 tma_prefetch_l2_3d(tm_q, 0, yn, bh);
                 tma_prefetch_l2_3d(tm_q, 64, yn, bh);
+                if (tm_kh) {
+                    tma_prefetch_l2_3d(tm_kh, 0, yn, bh);
+                    tma_prefetch_l2_3d(tm_kh, 64, yn, bh);
+                }
             }
             ++nkq;
             progressed = true;
@@ -2228,8 +2253,11 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
             const int g = ntp & 1, it = ntp >> 1;
             if (it == 0 || mbar_test_wait(ctl.bar(B_FREE + g), (uint32_t)(it - 1) & 1u)) {
                 const uint32_t bar = ctl.bar(B_TP_FULL + g);
-                mbar_arrive_expect_tx(bar, kTile);
+                mbar_arrive_expect_tx(bar, kTile + (side ? kSideBytes : 0u));
                 tma_load_3d(sm.tp(ntp), tm_ws, bar, 0, (nchunks - 1 - ntp) * 128, bh);
+                if (side)
+                    bulk_load(sm.side(g), side + (size_t)(nchunks - 1 - ntp) * kSideFloats,
+                              kSideBytes, bar);
                 ++ntp;
                 progressed = true;
             }
@@ -2253,9 +2281,16 @@ __device__ void producer(const Ctl& ctl, const Smem& sm, const CUtensorMap* tm_q
     }
 }
 
+// kKda: G <- diag(exp G_L) G + (Q o gamma)^T dO - (K o gamma)^T dV, with the
+// stage's q and k the decayed operands: G^T's columns are scaled by the
+// chunk's keep factors (sside slot, copied to sdec before the dV MMAs free
+// it) while the dV MMAs read the bf16 copy, and only then does dO^T Q go in.
+// G is then recorded in fp32 (G_chunks points at fp32 [BH][chunk][dk][dv]).
+template <bool kKda>
 __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                            const float* __restrict__ d_S_T, float* __restrict__ d_S0,
-                           __nv_bfloat16* __restrict__ G_chunks, int bh, int nchunks) {
+                           __nv_bfloat16* __restrict__ G_chunks, int bh, int nchunks,
+                           const float* sside, float* sdec) {
     constexpr int kBar = 1;
     const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
     // d_S_T^T into TMEM: lane t holds dv column t (zeros without d_S_T).
@@ -2272,7 +2307,20 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         const int c = nchunks - 1 - i;
         if (i > 0 && !wg_wait(ctl, B_G_READY, (uint32_t)(i - 1), t, kBar)) return;
         tc_fence_after_sync();
-        {   // G^T -> bf16, and G itself recorded as the gradient at chunk c's end
+        if constexpr (kKda) {  // this chunk's keep factors, before the dV MMAs free their slot
+            bool okk = true;
+            if (t == 0) okk = ctl.wait(B_TP_FULL + (i & 1), (uint32_t)(i >> 1));
+            if (wg_sync_or(kBar, !okk)) return;
+            if (t < 32)
+                reinterpret_cast<float4*>(sdec)[t] =
+                    reinterpret_cast<const float4*>(sside + (i & 1) * (kSideBytes / 4))[t];
+        }
+        if constexpr (kKda) {  // G^T -> bf16, G recorded in fp32 as the gradient at chunk c's end
+            float* const rec32 =
+                reinterpret_cast<float*>(G_chunks) + ((size_t)bh * nchunks + c) * kD * kD + t;
+            scan::tmem_pack64_rec32(lane + C_GT, lane + C_GB, rec32);
+            scan::tmem_pack64_rec32(lane + C_GT + 64u, lane + C_GB + 32u, rec32 + 64 * kD);
+        } else {  // G^T -> bf16, and G recorded as a bf16 hi/lo pair
             __nv_bfloat16* const rec = G_chunks + 2 * ((size_t)bh * nchunks + c) * kD * kD + t;
             scan::tmem_pack64(lane + C_GT, lane + C_GB, rec);
             scan::tmem_pack64(lane + C_GT + 64u, lane + C_GB + 32u, rec + 64 * kD);
@@ -2281,22 +2329,43 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
         tc_fence_before_sync();
         wg_sync(kBar);
         bool ok = true;
+        const uint32_t dO = sm.dO(i), kq = sm.kq(i);
+        // G^T += dO^T Q over the chunk's tokens
+        auto issue_doq = [&] {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + C_GT, sw128_desc(dO + 2048u * kk, 8192, 1024),
+                            sw128_desc(kq + 8192u + 2048u * kk, kRegKQ, 1024), ID_MM128, 1);
+        };
         if (t == 0) {
             ok = ctl.wait(B_B2_READY + (i & 1), (uint32_t)(i >> 1)) &&
                  ctl.wait(B_VP_DONE, (uint32_t)i);
             if (ok) {
                 tc_fence_after_sync();
-                const uint32_t b2 = sm.b2(i), dO = sm.dO(i), kq = sm.kq(i);
+                const uint32_t b2 = sm.b2(i);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // dV^T += G^T (K^T Tm) over dk
                     mma_bf16_ts(tmem + C_DV, tmem + C_GB + 8u * kk,
                                 sw128_desc(b2 + 2048u * kk, 8192, 1024), ID_TM64, 1);
                 mma_commit(ctl.bar(B_DV_FULL));
                 mma_commit(ctl.bar(B_FREE + (i & 1)));
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)  // G^T += dO^T Q over the chunk's tokens
-                    mma_bf16_ss(tmem + C_GT, sw128_desc(dO + 2048u * kk, 8192, 1024),
-                                sw128_desc(kq + 8192u + 2048u * kk, kRegKQ, 1024), ID_MM128, 1);
+                if constexpr (!kKda) {
+                    issue_doq();
+                    ok = ctl.wait(B_DV_FULL, (uint32_t)i);
+                    if (ok) mbar_arrive(ctl.bar(B_DV_READY));
+                }
+            }
+        }
+        if constexpr (kKda) {  // G^T <- G^T diag(exp G_L) while the dV MMAs read the bf16 copy
+            __syncwarp();
+            scan::tmem_scale64_cols(lane + C_GT, sdec);
+            scan::tmem_scale64_cols(lane + C_GT + 64u, sdec + 64);
+            tmem_wait_st();
+            tc_fence_before_sync();
+            if (wg_sync_or(kBar, !ok)) return;
+            if (t == 0) {
+                tc_fence_after_sync();
+                issue_doq();
                 ok = ctl.wait(B_DV_FULL, (uint32_t)i);
                 if (ok) mbar_arrive(ctl.bar(B_DV_READY));
             }
@@ -2315,7 +2384,7 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                 mma_bf16_ts(tmem + C_GT, tmem + C_VB + 8u * kk,
                             sw128_desc(kq + 2048u * kk, kRegKQ, 1024), ID_TM128N, 1);
             mma_commit(ctl.bar(B_G_READY));
-            mma_commit(ctl.bar(B_KQ_EMPTY + i % kStages));
+            mma_commit(ctl.bar(B_KQ_EMPTY + i % sm.nst));
             mma_commit(ctl.bar(B_DO_EMPTY + (i & 1)));
             mbar_arrive(ctl.bar(B_DV_READ));  // the writer may start the next dV^T
         }
@@ -2333,6 +2402,8 @@ __device__ void state_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
     }
 }
 
+// kKda: B2 = K^T Tm with K^ = K o exp(G_C - G) from the stage.
+template <bool kKda>
 __device__ void group_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t, int nchunks) {
     constexpr int kBar = 2;
     const uint32_t lane = tmem + ((uint32_t)(32 * (t >> 5)) << 16);
@@ -2343,10 +2414,11 @@ __device__ void group_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t,
                  ctl.wait(B_TP_FULL + (i & 1), (uint32_t)(i >> 1));
             if (ok) {
                 tc_fence_after_sync();
-                const uint32_t kq = sm.kq(i), tp = sm.tp(i);
+                const uint32_t ka = kKda ? sm.kh(i) : sm.kq(i), tp = sm.tp(i);
+                const uint32_t lbo = kKda ? 8192u : kRegKQ;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // K^T Tm over the chunk's tokens
-                    mma_bf16_ss(tmem + C_B2, sw128_desc(kq + 2048u * kk, kRegKQ, 1024),
+                    mma_bf16_ss(tmem + C_B2, sw128_desc(ka + 2048u * kk, lbo, 1024),
                                 sw128_desc(tp + 8192u + 2048u * kk, 8192, 1024), ID_MM64, kk > 0);
                 mma_commit(ctl.bar(B_B2_DONE));
                 ok = ctl.wait(B_B2_DONE, (uint32_t)i);
@@ -2408,17 +2480,29 @@ __device__ void writer_body(const Ctl& ctl, const Smem& sm, uint32_t tmem, int t
 }
 }  // namespace bchain
 
+// kKda: tm_q, tm_k map the decayed Q o exp G, K o exp G, tm_kh maps
+// K o exp(G_C - G), side holds every chunk's keep factors (kSideFloats per
+// chunk, exp G_C per key channel first), and G_chunks is fp32.
+template <bool kKda>
 __global__ void __launch_bounds__(512, 1)
 chunk_bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_do,
                           const __grid_constant__ CUtensorMap tm_ws, const float* __restrict__ d_S_T,
                           __nv_bfloat16* __restrict__ d_v, float* __restrict__ d_S0,
-                          __nv_bfloat16* __restrict__ G_chunks, int T) {
+                          __nv_bfloat16* __restrict__ G_chunks, int T,
+                          const __grid_constant__ CUtensorMap tm_kh, const float* __restrict__ side) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
-    const bchain::Smem sm{base};
+    bchain::Smem sm{base};
+    if constexpr (kKda) {
+        sm.nst = 2;
+        sm.stage = kStageKQ + kTile;
+    }
+    const float* const sside =
+        reinterpret_cast<const float*>(smem_raw + (base - raw_addr) + bchain::OFF_SIDE);
+    float* const sdec = reinterpret_cast<float*>(smem_raw + (base - raw_addr) + bchain::OFF_DEC);
     int* const misc = reinterpret_cast<int*>(smem_raw + (base - raw_addr) + bchain::OFF_MISC);
     const Ctl ctl{base + bchain::OFF_BAR, reinterpret_cast<volatile int*>(misc)};
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(misc + 1);
@@ -2434,6 +2518,7 @@ chunk_bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_do);
         prefetch_tensormap(&tm_ws);
+        if (kKda) prefetch_tensormap(&tm_kh);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_holder), 512);
@@ -2445,14 +2530,18 @@ chunk_bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t tmem = *tmem_holder;
 
     if (warp == 0) {
-        if (lane == 0) bchain::producer(ctl, sm, &tm_q, &tm_k, &tm_do, &tm_ws, bh, nchunks);
+        if (lane == 0)
+            bchain::producer(ctl, sm, &tm_q, &tm_k, &tm_do, &tm_ws, bh, nchunks,
+                             kKda ? &tm_kh : nullptr,
+                             kKda ? side + (size_t)bh * nchunks * kSideFloats : nullptr);
     } else if (warp >= 4 && warp < 8) {
         const int t = tid - 128;
-        bchain::state_body(ctl, sm, tmem, t, d_S_T, d_S0, G_chunks, bh, nchunks);
+        bchain::state_body<kKda>(ctl, sm, tmem, t, d_S_T, d_S0, G_chunks, bh, nchunks, sside,
+                                 sdec);
         if (t == 0) drain_mmas(ctl, bchain::B_DRAIN + 0);
     } else if (warp >= 8 && warp < 12) {
         const int t = tid - 256;
-        bchain::group_body(ctl, sm, tmem, t, nchunks);
+        bchain::group_body<kKda>(ctl, sm, tmem, t, nchunks);
         if (t == 0) drain_mmas(ctl, bchain::B_DRAIN + 1);
     } else if (warp >= 12) {
         const int t = tid - 384;
@@ -3459,13 +3548,46 @@ cudaError_t launch_chunk_bwd_chain_tc(const void* q, const void* k, const void* 
         !make_ws_map(&mws, const_cast<void*>(tiles), BH, nchunks))
         return cudaErrorInvalidValue;
     cudaError_t err;
-    if ((err = cudaFuncSetAttribute(chunk_bwd_chain_tc_kernel,
+    if ((err = cudaFuncSetAttribute(chunk_bwd_chain_tc_kernel<false>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     bchain::kSmemBytes)) != cudaSuccess)
         return err;
-    chunk_bwd_chain_tc_kernel<<<BH, 512, bchain::kSmemBytes, stream>>>(
+    chunk_bwd_chain_tc_kernel<false><<<BH, 512, bchain::kSmemBytes, stream>>>(
         mq, mk, mdo, mws, d_S_T, static_cast<__nv_bfloat16*>(d_v), d_S0,
-        static_cast<__nv_bfloat16*>(G_chunks), T);
+        static_cast<__nv_bfloat16*>(G_chunks), T, mk, nullptr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_bwd_chain_tc_kda(const void* d_o, const float* d_S_T, void* d_v,
+                                          float* d_S0, float* G_chunks, const void* workspace,
+                                          int BH, int T, cudaStream_t stream) {
+    if (BH <= 0 || T <= 0) return cudaSuccess;
+    const int nchunks = (T + kC - 1) / kC;
+    const long long items = (long long)BH * nchunks;
+    if (items > 0x7fffffffLL || !workspace) return cudaErrorInvalidValue;
+    // the KDA forward's workspace (launch_chunk_tc_kda): tiles, side vectors,
+    // then Q o exp G, K o exp G, K o exp(G_C - G)
+    const uint8_t* const ws = static_cast<const uint8_t*>(workspace);
+    const size_t op = (size_t)BH * (size_t)T * kD * sizeof(__nv_bfloat16);
+    const float* const side = reinterpret_cast<const float*>(ws + (size_t)items * kTile);
+    const uint8_t* const qt = ws + (size_t)items * (kTile + kSideFloats * sizeof(float));
+    const uint8_t* const kt = qt + op;
+    const uint8_t* const kh = kt + op;
+    CUtensorMap mq, mk, mkh, mdo, mws;
+    if (!make_map(&mq, const_cast<uint8_t*>(qt), BH, T) ||
+        !make_map(&mk, const_cast<uint8_t*>(kt), BH, T) ||
+        !make_map(&mkh, const_cast<uint8_t*>(kh), BH, T) ||
+        !make_map(&mdo, const_cast<void*>(d_o), BH, T) ||
+        !make_ws_map(&mws, const_cast<void*>(workspace), BH, nchunks))
+        return cudaErrorInvalidValue;
+    cudaError_t err;
+    if ((err = cudaFuncSetAttribute(chunk_bwd_chain_tc_kernel<true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    bchain::kSmemBytes)) != cudaSuccess)
+        return err;
+    chunk_bwd_chain_tc_kernel<true><<<BH, 512, bchain::kSmemBytes, stream>>>(
+        mq, mk, mdo, mws, d_S_T, static_cast<__nv_bfloat16*>(d_v), d_S0,
+        reinterpret_cast<__nv_bfloat16*>(G_chunks), T, mkh, side);
     return cudaGetLastError();
 }
 

@@ -95,6 +95,14 @@ cudaError_t launch_chunk_bwd_gated(const void* q, const void* k, const void* v, 
                                    int dv, int dt, void* workspace, cudaStream_t stream,
                                    const char** stage);
 
+// KDA's backward chain on tcgen05 (bf16, dk = dv = 128): the state gradient
+// from the last chunk to the first with the decayed operands, tiles and keep
+// factors the tensor-core KDA forward left in its workspace (kda_workspace,
+// as launch_chunk_tc_kda lays it out); writes d_v, d_S0 and G at every chunk
+// end in fp32 (G_chunks, [BH][chunk][dk][dv]).
+cudaError_t launch_chunk_bwd_chain_tc_kda(const void* d_o, const float* d_S_T, void* d_v,
+                                          float* d_S0, float* G_chunks, const void* kda_workspace,
+                                          int BH, int T, cudaStream_t stream);
 // KDA's backward (g, d_g: fp32 [BH][T][dk]): the states recomputed by the
 // KDA forward (on tcgen05 for bf16 with dk = dv = 128, else on the CUDA
 // cores), then its chain and per-chunk gradients with the per-channel decay.

@@ -1122,11 +1122,13 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
 // Gated DeltaNet's backward: the chain and the per-chunk gradients with the
 // decay; fp32 products on the CUDA cores for fp32 I/O, tf32 tensor-core
 // products (fp32 accumulation) for bf16 I/O, as the plain backward.
+// chain_done: the tcgen05 chain has already written Gc, d_v and d_S0.
 template <typename T, int DK, int DV>
 cudaError_t launch_bwd_gated_typed(const void* q, const void* k, const void* v, const void* beta,
                                    const float* g, const void* d_o, const float* d_S_T, void* d_q,
                                    void* d_k, void* d_v, void* d_beta, float* d_g, float* d_S0,
-                                   float* Sc, float* Gc, int BH, int Tlen, cudaStream_t stream) {
+                                   float* Sc, float* Gc, int BH, int Tlen, cudaStream_t stream,
+                                   bool chain_done) {
     constexpr int NV = DV < 64 ? DV : 64;
     using Ops = std::conditional_t<std::is_same_v<T, float>, simt::Fp32Ops, simt::Tf32Ops<8>>;
     using LC = ChainSmem<DK, NV, Ops::kPad>;
@@ -1142,10 +1144,12 @@ cudaError_t launch_bwd_gated_typed(const void* q, const void* k, const void* v, 
         return err;
     const long long g_chain = (long long)BH * (DV / NV), g_grads = (long long)BH * nchunks;
     if (g_chain > 0x7fffffffLL || g_grads > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    chain<<<(unsigned)g_chain, Ops::kThreads, LC::kBytes, stream>>>(
-        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(beta),
-        static_cast<const T*>(d_o), d_S_T, static_cast<T*>(d_v), d_S0, Gc, Tlen, g);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (!chain_done) {
+        chain<<<(unsigned)g_chain, Ops::kThreads, LC::kBytes, stream>>>(
+            static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(beta),
+            static_cast<const T*>(d_o), d_S_T, static_cast<T*>(d_v), d_S0, Gc, Tlen, g);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
     grads<<<(unsigned)g_grads, Ops::kThreads, LG::kBytes, stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
         static_cast<const T*>(beta), static_cast<const T*>(d_o), Sc, Gc, static_cast<T*>(d_q),
@@ -1209,11 +1213,29 @@ cudaError_t launch_bwd_dims(const void* q, const void* k, const void* v, const v
 
 }  // namespace
 
+namespace {
+// Gated DeltaNet's rate on every key channel: gk[bh][t][c] = g[bh][t] (the
+// KDA form with equal channels is Gated DeltaNet).
+__global__ void broadcast_gate_kernel(const float* __restrict__ g, float4* __restrict__ gk,
+                                      size_t n4, int per_tok4) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const float x = g[i / per_tok4];
+        gk[i] = make_float4(x, x, x, x);
+    }
+}
+constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+}  // namespace
+
+// Workspace.  The fp32 S and G of every chunk; for bf16 with d = 128 also the
+// tensor-core KDA forward's scratch and the broadcast rates it reads.
 size_t chunk_bwd_gated_workspace_bytes(int BH, int T, int dk, int dv, int dt) {
     if (BH <= 0 || T <= 0) return 0;
     const size_t items = (size_t)BH * (size_t)((T + kC - 1) / kC);
     const size_t states = 2 * items * (size_t)dk * (size_t)dv * sizeof(float);
-    return states + (chunk_tc_supports(dk, dv, dt) ? chunk_tc_gated_workspace_bytes(BH, T) : 0);
+    if (!chunk_tc_supports(dk, dv, dt)) return states;
+    return states + align256(chunk_tc_kda_workspace_bytes(BH, T)) +
+           (size_t)BH * (size_t)T * (size_t)dk * sizeof(float);
 }
 
 cudaError_t launch_chunk_bwd_gated(const void* q, const void* k, const void* v, const void* beta,
@@ -1227,18 +1249,34 @@ cudaError_t launch_chunk_bwd_gated(const void* q, const void* k, const void* v, 
     const size_t per = (size_t)BH * ((T + kC - 1) / kC) * (size_t)dk * dv;
     float* const Sc = static_cast<float*>(workspace);
     float* const Gc = Sc + per;
-    cudaError_t err =
-        chunk_tc_supports(dk, dv, dt)
-            ? launch_chunk_tc_gated(q, k, v, beta, g, S0, nullptr, nullptr, BH, T, dk, dv, dt,
-                                    Gc + per, stream, kNoNorm, Sc)
-            : launch_chunk_simt(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt, stream,
+    const bool tc = chunk_tc_supports(dk, dv, dt);
+    cudaError_t err;
+    if (tc) {
+        // bf16, d = 128: Gated DeltaNet as KDA with the rate on every key
+        // channel, so the states come from the tcgen05 KDA forward and the
+        // chain runs on tcgen05 from the decayed operands that forward leaves
+        uint8_t* const kws = reinterpret_cast<uint8_t*>(Gc + per);
+        float* const gk = reinterpret_cast<float*>(kws + align256(chunk_tc_kda_workspace_bytes(BH, T)));
+        *stage = "rates on every key channel";
+        const size_t n4 = (size_t)BH * (size_t)T * (size_t)(dk / 4);
+        broadcast_gate_kernel<<<1216, 256, 0, stream>>>(g, reinterpret_cast<float4*>(gk), n4, dk / 4);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        *stage = "state recompute";
+        err = launch_chunk_tc_kda(q, k, v, beta, gk, S0, nullptr, nullptr, BH, T, dk, dv, dt, kws,
+                                  stream, kNoNorm, Sc);
+        if (err != cudaSuccess) return err;
+        *stage = "state-gradient chain";
+        err = launch_chunk_bwd_chain_tc_kda(d_o, d_S_T, d_v, d_S0, Gc, kws, BH, T, stream);
+    } else {
+        err = launch_chunk_simt(q, k, v, beta, S0, nullptr, nullptr, BH, T, dk, dv, dt, stream,
                                 Sc, g);
+    }
     if (err != cudaSuccess) return err;
     *stage = "gated chain and gradients";
 #define DN_GBWD_CASE(T_, DK_, DV_)                                                              \
     if (dk == DK_ && dv == DV_)                                                                 \
         return launch_bwd_gated_typed<T_, DK_, DV_>(q, k, v, beta, g, d_o, d_S_T, d_q, d_k, d_v,\
-                                                     d_beta, d_g, d_S0, Sc, Gc, BH, T, stream);
+                                                     d_beta, d_g, d_S0, Sc, Gc, BH, T, stream, tc);
     if (dt == 0) {
         DN_GBWD_CASE(float, 128, 128)
         DN_GBWD_CASE(float, 128, 64)
@@ -1364,7 +1402,6 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
 // way.  The copies and the launches of one sequence queue on the stream
 // behind the previous sequence's, so one set of scratch buffers serves all.
 namespace {
-constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 struct VarlenBwdScratch {
     size_t ws, q, v, b;  // bytes: the batched backward's workspace, a dk tensor, a dv tensor, beta
 };

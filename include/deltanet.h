@@ -376,9 +376,11 @@ DN_API size_t dn_chunk_fwd_varlen_workspace_bytes(const int *cu_seqlens, int N, 
  * "Hardware-efficient implementation", paperlayer.ai/abs/2406.06484v6).
  *   g, d_g  [B, H, T] fp32 (4-byte aligned); the rest as dn_chunk_bwd.
  *   workspace  device scratch of dn_chunk_bwd_gated_workspace_bytes(...) bytes.
- * The forward's states are recomputed (on tcgen05 for bf16 with dk = dv = 128,
- * else on the CUDA cores) and the gradients formed chunk by chunk on the CUDA
- * cores (fp32 products for fp32 I/O, tf32 tensor-core products with fp32
+ * For bf16 with dk = dv = 128 the states are recomputed and the state
+ * gradient carried on tcgen05, through the KDA form with the rate on every
+ * key channel (Gated DeltaNet is KDA with equal channels); otherwise both run
+ * on the CUDA cores.  The per-chunk gradients are formed on the CUDA cores
+ * (fp32 products for fp32 I/O, tf32 tensor-core products with fp32
  * accumulation for bf16).  d_g is
  * the gradient of each token's log keep rate, through every later ratio
  * exp(G_i - G_j), keep factor and state carried out of its chunk.  Errors and
@@ -391,8 +393,10 @@ DN_API int dn_chunk_bwd_gated(const void *q, const void *k, const void *v, const
                               int dt, void *workspace, size_t workspace_bytes, void *stream);
 /* Its scratch: the fp32 state and state gradient of every chunk,
  * 2 * B * H * ceil(T / 64) * dk * dv * 4 bytes, plus, for bf16 with
- * dk = dv = 128, the tensor-core forward's scratch (as
- * dn_chunk_fwd_gated_workspace_bytes); 0 for invalid arguments.  Host-only. */
+ * dk = dv = 128, the tensor-core KDA forward's scratch (as
+ * dn_chunk_fwd_kda_workspace_bytes, rounded up to 256 bytes) and the rates
+ * broadcast over the key channels (B * H * T * dk * 4 bytes); 0 for invalid
+ * arguments.  Host-only. */
 DN_API size_t dn_chunk_bwd_gated_workspace_bytes(int B, int H, int T, int dk, int dv, int C,
                                                  int dt);
 

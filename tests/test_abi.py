@@ -120,6 +120,19 @@ def test_kda_backward_workspace_bytes(lib):
     assert f(1, 1, 64, 128, 128, 32, 1) == 0
 
 
+def test_gated_backward_workspace_bytes(lib):
+    """The gated backward keeps the fp32 state and state gradient of every
+    chunk; for bf16 with d = 128 also the tensor-core KDA forward's scratch
+    (256-byte aligned) and the rates on every key channel."""
+    f = lib.dn_chunk_bwd_gated_workspace_bytes
+    states = 2 * 8 * 16 * 32 * 128 * 128 * 4
+    kda = lib.dn_chunk_fwd_kda_workspace_bytes(8, 16, 2048, 128, 128, 64, 1)
+    assert f(8, 16, 2048, 128, 128, 64, 1) == states + (kda + 255) // 256 * 256 + 8 * 16 * 2048 * 128 * 4
+    assert f(8, 16, 2048, 128, 128, 64, 0) == states
+    assert f(1, 2, 130, 64, 64, 64, 1) == 2 * 2 * 3 * 64 * 64 * 4
+    assert f(1, 1, 0, 128, 128, 64, 1) == 0
+
+
 def test_kda_backward_rejects_a_short_workspace_before_any_cuda_call(lib):
     need = lib.dn_chunk_bwd_kda_workspace_bytes(1, 2, 130, 64, 64, 64, 0)
     st = lib.dn_chunk_bwd_kda(*([None] * 14), 1, 2, 130, 64, 64, 64, 0,

@@ -1099,6 +1099,9 @@ static_assert(kPrepCtasPerSm * (kPrepSmemBytes + 1024) <= 233472, "prepare kerne
 constexpr uint32_t P_OFF_KB = (P_OFF_MISC + 16 + 1023) & ~1023u;
 constexpr uint32_t kPrepSmemBytesSepB = P_OFF_KB + 16384 + 1024;
 constexpr int kPrepCtasPerSmSepB = 3;
+// Packed sequences: the item lookup's extra live values spill at the
+// four-CTA register budget (128), so that instance runs three CTAs per SM.
+constexpr int kPrepCtasPerSmVarlen = 3;
 static_assert(kPrepCtasPerSmSepB * (kPrepSmemBytesSepB + 1024) <= 233472,
               "prepare kernel occupancy (separate right factor)");
 static_assert(P_OFF_X % 1024 == 0 && kXBytes >= kTile, "[PT; Tm] over the solve array");
@@ -1145,7 +1148,9 @@ __device__ __forceinline__ void decay_row_tmem(uint32_t taddr, const float* Gs, 
 // kDIO = 64: heads of 64 features, loaded into the first column half of the
 // 128-wide tile; the second half stays zero.
 template <int NMAX, bool kGate, bool kSepB = false, int kDIO = kD>
-__global__ void __launch_bounds__(kPrepThreads, kSepB ? kPrepCtasPerSmSepB : kPrepCtasPerSm)
+__global__ void __launch_bounds__(kPrepThreads, kSepB ? kPrepCtasPerSmSepB
+                                                      : (NMAX > 1 ? kPrepCtasPerSmVarlen
+                                                                  : kPrepCtasPerSm))
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_ws, const __nv_bfloat16* __restrict__ beta,
                   int T, int nchunks, int items, const __grid_constant__ SeqTable<NMAX> seqs,
@@ -3228,7 +3233,8 @@ cudaError_t launch_chunk_tc_varlen(const void* q, const void* k, const void* v, 
                                     scan::kSmemBytes)) != cudaSuccess)
         return err;
     if (items > 0) {
-        const int grid = (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSm);
+        const int grid =
+            (int)std::min<long long>(items, (long long)sm_count() * kPrepCtasPerSmVarlen);
         prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(
             mq, mk, mws, static_cast<const __nv_bfloat16*>(beta), T, 0, (int)items, seqs, nullptr,
             side, mws, norm, nullptr);

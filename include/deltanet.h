@@ -22,16 +22,19 @@
  *     NULL means the legacy default stream).  Results are ready when the
  *     stream reaches them.
  *   - q and k are used as given: the caller L2-normalises them and applies
- *     any query scale, or runs dn_qk_prepare first.  beta is used as given
+ *     any query scale, runs dn_qk_prepare first, or calls the *_qk entry
+ *     points, whose kernels prepare them as they load them.  beta is used as given
  *     (0..1, or 0..2 for the negative-eigenvalue variant), with no clamping.
  *   - Arguments are checked on the host before anything is enqueued; a
  *     rejected call enqueues nothing.  Kernels have no device traps and no
  *     unbounded waits.  Launch failures are reported as DN_ERR_CUDA.
  *   - Global state: a thread-local error message (dn_last_error); per device,
  *     one word where a tensor-core kernel records the first of its bounded
- *     waits that ran out (read and cleared by dn_device_error); and the
- *     static scratch array of dn_chunk_fwd_noalloc with its looked-up device
- *     address.  Calls from several threads are safe, except that
+ *     waits that ran out (read and cleared by dn_device_error), and the
+ *     testing hook's limit of the gradient kernel's first wait
+ *     (dn_debug_first_wait_ns); and the static scratch array of
+ *     dn_chunk_fwd_noalloc with its looked-up device address.  Calls from
+ *     several threads are safe, except that
  *     dn_chunk_fwd_noalloc calls whose kernels overlap on one device race on
  *     that array.
  */

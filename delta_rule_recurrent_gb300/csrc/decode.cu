@@ -16,6 +16,11 @@
 // With a dn_qk_norm, q and k are L2-normalised (and q scaled) in fp32 after
 // they are loaded, before any product uses them.
 //
+// Consecutive steps overlap their launches: each is launched with
+// programmatic stream serialization, lets the next launch be scheduled once
+// all of its CTAs have started, and waits (griddepcontrol.wait) for the grid
+// before it in the stream to finish and flush before reading anything.
+//
 // Work split: one CTA per head.  A thread owns one float4 column group of
 // the value channel and DK / RG rows of the key channel, so a warp's loads
 // and stores cover 512 contiguous bytes, and the whole head's state sits in
@@ -49,6 +54,8 @@ recurrent_step_kernel(const T* __restrict__ q, const T* __restrict__ k,
     const int tid = threadIdx.x;
     const int cg = tid % CG, rg = tid / CG;
     float4* Sh = reinterpret_cast<float4*>(S + (size_t)head * DK * DV);
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous step's state is written
 
     // Issue every state load first: RPT independent 16-byte loads per thread.
     float4 s[RPT];
@@ -161,13 +168,24 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
     const T* const vt = static_cast<const T*>(v);
     const T* const bt = static_cast<const T*>(beta);
     T* const ot = static_cast<T*>(o);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)BH);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (!g)
-        recurrent_step_kernel<T, DK, DV, NT, 0><<<BH, NT, 0, stream>>>(qt, kt, vt, bt, g, S, ot, nm);
-    else if (gpc)
-        recurrent_step_kernel<T, DK, DV, NT, 2><<<BH, NT, 0, stream>>>(qt, kt, vt, bt, g, S, ot, nm);
-    else
-        recurrent_step_kernel<T, DK, DV, NT, 1><<<BH, NT, 0, stream>>>(qt, kt, vt, bt, g, S, ot, nm);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<T, DK, DV, NT, 0>, qt, kt, vt, bt, g,
+                                  S, ot, nm);
+    if (gpc)
+        return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<T, DK, DV, NT, 2>, qt, kt, vt, bt, g,
+                                  S, ot, nm);
+    return cudaLaunchKernelEx(&cfg, recurrent_step_kernel<T, DK, DV, NT, 1>, qt, kt, vt, bt, g, S,
+                              ot, nm);
 }
 
 template <typename T>

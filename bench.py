@@ -238,6 +238,24 @@ def timed_loop(fn, steps, stream, world):
     return region_s, [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def timed_region(fn, steps, stream, world):
+    """Runs fn `steps` times back to back between a barrier + synchronize on
+    both sides, with CUDA events only at the region's ends (none between the
+    steps, so launches that overlap their predecessor's tail can); returns
+    the region's seconds."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / 1e3
+
+
 def graph_decode(step, nsteps, stream, world):
     """Captures step(0..nsteps-1) into one CUDA graph, replays it once to
     warm up, then times one replay; returns (seconds, None) or (None, error)."""
@@ -379,8 +397,13 @@ def run_ours(args, rank, world, local):
         for i in range(args.warmup):
             decode_step(nsteps + i)
         torch.cuda.synchronize()
-        dec_region_s, dec_launch = timed_loop(decode_step, nsteps, stream, world)
-        dec_region_s = max_over_ranks(dec_region_s, world)
+        # Consecutive steps overlap their launches (programmatic dependent
+        # launch), which an event between two steps would prevent: the steps
+        # run back to back and the region's time over the steps is the mean
+        # launch duration; the per-step events of timed_loop give the steps in
+        # isolation beside it.
+        dec_region_s = max_over_ranks(timed_region(decode_step, nsteps, stream, world), world)
+        _, dec_launch = timed_loop(decode_step, nsteps, stream, world)
 
         # The same steps captured once into a CUDA graph and replayed as one
         # launch (no per-step host overhead); the state keeps evolving.
@@ -494,7 +517,8 @@ def run_ours(args, rank, world, local):
         for i in range(args.warmup):
             gated_decode_step(nsteps + i)
         torch.cuda.synchronize()
-        gd_region_s, gd_launch = timed_loop(gated_decode_step, nsteps, stream, world)
+        gd_region_s = timed_region(gated_decode_step, nsteps, stream, world)
+        _, gd_launch = timed_loop(gated_decode_step, nsteps, stream, world)
         gd_region_s = max_over_ranks(gd_region_s, world)
         del dgate, Sdg
 
@@ -531,7 +555,8 @@ def run_ours(args, rank, world, local):
         for i in range(args.warmup):
             kda_decode_step(nsteps + i)
         torch.cuda.synchronize()
-        kd_region_s, kd_launch = timed_loop(kda_decode_step, nsteps, stream, world)
+        kd_region_s = timed_region(kda_decode_step, nsteps, stream, world)
+        _, kd_launch = timed_loop(kda_decode_step, nsteps, stream, world)
         kd_region_s = max_over_ranks(kd_region_s, world)
         del dkgate, Sdk
 
@@ -727,7 +752,8 @@ def run_ours(args, rank, world, local):
                    "peak_source": f"{peak_src} (bf16 dense burst)"},
     }
     dbytes = decode_bytes(Bd, Hd, dkd, dvd, 2)
-    dec_launch_s = statistics.mean(dec_launch) / 1e3
+    dec_launch_s = dec_region_s / nsteps  # back to back (see timed_region)
+    dec_iso_s = statistics.mean(dec_launch) / 1e3
     dec_gbs = dbytes / dec_launch_s / 1e9
     decode = {
         "workload": DECODE, "steps": nsteps, "value": world * Bd * nsteps / dec_region_s,
@@ -736,7 +762,10 @@ def run_ours(args, rank, world, local):
                      "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
                      "traffic": kernel_traffic("recurrent_step", "decode.cu"),
                      "peak_source": f"{peak_src} (copy bandwidth)", "bytes_per_launch": dbytes,
-                     "launch_us": dec_launch_s * 1e6},
+                     "launch_us": dec_launch_s * 1e6,
+                     "launch_us_isolated": dec_iso_s * 1e6,
+                     "timing": "steps back to back, events at the region's ends (consecutive "
+                               "launches overlap); launch_us_isolated: events around each step"},
         "graph": ({"value": world * Bd * nsteps / dec_graph[0], "unit": "tokens/s",
                    "ms_per_step": 1e3 * dec_graph[0] / nsteps,
                    "hbm_gbs": dbytes * nsteps / dec_graph[0] / 1e9,
@@ -857,7 +886,7 @@ def run_ours(args, rank, world, local):
                   "unit": "TFLOP/s", "frac": gflops / g_launch_s / 1e12 / alu_peak,
                   "traffic": None, "peak_source": alu_src, "flops_per_launch": gflops,
                   "launch_us": g_launch_s * 1e6}
-    gd_launch_s = statistics.mean(gd_launch) / 1e3
+    gd_launch_s = gd_region_s / nsteps  # back to back, as the plain step
     gdbytes = dbytes + Bd * Hd * 4  # plus the fp32 log keep rate per head
     gated = {
         "chunk": {"workload": HEADLINE, "steps": gsteps,
@@ -885,7 +914,7 @@ def run_ours(args, rank, world, local):
                                 "bytes_per_launch": gdbytes, "launch_us": gd_launch_s * 1e6}},
     }
     k_launch_s = statistics.mean(k_launch) / 1e3
-    kd_launch_s = statistics.mean(kd_launch) / 1e3
+    kd_launch_s = kd_region_s / nsteps  # back to back, as the plain step
     kdbytes = dbytes + Bd * Hd * dkd * 4  # plus the fp32 per-channel log keep rates
     ks_launch_s = statistics.mean(ks_launch) / 1e3
     kbytes = cbytes + B * H * T * dk * 4  # plus the fp32 log keep rate per token, head and channel
@@ -986,13 +1015,14 @@ def run_ours(args, rank, world, local):
         "long_prefill": long_prefill,
         "gpu_launches": (launches_per_call * (args.steps + n_sl * e2e_steps)  # chunk fwd, e2e
                          + (long_launches + launches_per_call) * lsteps  # long prefill: split, plain
-                         + nsteps + (nsteps if dec_graph[0] else 0)     # decode, graph replay
+                         + 2 * nsteps + (nsteps if dec_graph[0] else 0)  # decode (back to back,
+                         # then isolated), graph replay
                          + (4 if bwd_tc else 3) * bwd_steps             # recompute, chain, grads
                          + launches_per_call * vsteps                   # varlen
                          + psteps                                       # q/k preparation
                          + launches_per_call * psteps                   # forward preparing q, k
-                         + (2 if gneed else 1) * gsteps + gsteps + nsteps  # gated: both forms, decode
-                         + (4 if kneed else 1) * gsteps + ksteps + nsteps   # KDA: both forms, decode
+                         + (2 if gneed else 1) * gsteps + gsteps + 2 * nsteps  # gated: both forms, decode
+                         + (4 if kneed else 1) * gsteps + ksteps + 2 * nsteps   # KDA: both forms, decode
                          # decayed backwards: recompute (2 or 4 launches on tcgen05, else 1),
                          # chain, gradients
                          + sum((2 + ((4 if f == "kda" else 2) if dec_tc else 1)) * d[2]

@@ -13,7 +13,10 @@ transposed block or a misplaced decay factor fails:
   [[PT E, -E]; [Tm E, 0]] (E = diag(exp G)), the keep factor exp(G_C) on the
   state and exp(G_C - G_s) on U';
 - the backward chain: dV = PT^T dO + (K^T Tm)^T G, G <- G + Q^T dO - K^T dV,
-  reading the forward's [PT; Tm] transposed;
+  reading the forward's [PT; Tm] transposed; and its KDA form, with the
+  forward's decayed operands (K o f in the chunk group's tile, Q o gamma and
+  K o gamma in the update) and the keep factors exp G_L on G's key rows,
+  which the gated backward also takes with one rate on every channel;
 - KDA on CUDA cores: the per-channel ratio as exp(G_i[d]) exp(-G_j[d]).
 - the per-chunk gradients in feature-lane form (the layout a tcgen05
   gradient kernel takes), dP and dTm as diagonal blocks of one product.
@@ -129,6 +132,44 @@ def test_backward_chain_regrouping():
     ref = oracle.backward(q, k, v, beta, dO, S0, dS_T)
     assert _rel(dV, ref[2][0, 0]) < 1e-9
     assert _rel(G, ref[4][0, 0]) < 1e-9
+
+
+@pytest.mark.parametrize("equal_channels", [False, True], ids=["kda", "gated"])
+def test_kda_backward_chain_regrouping(equal_channels):
+    """The tcgen05 KDA chain: dV = PT^T dO + ((K o f)^T Tm)^T G and
+    G <- diag(exp G_L) G + (Q o gamma)^T dO - (K o gamma)^T dV, with [PT; Tm]
+    carrying the per-channel ratios; the oracle's d_v and d_S0 (KDA, and with
+    one rate on every key channel the gated oracle's)."""
+    q, k, v, beta, S0, g = _case(5, kda=True)
+    if equal_channels:
+        g = np.repeat(g[..., :1], g.shape[-1], axis=-1)
+    r = np.random.default_rng(55)
+    dO = r.standard_normal(v.shape)
+    dS_T = r.standard_normal(S0.shape)
+    K_, Q_, b_, dO_, g_ = k[0, 0], q[0, 0], beta[0, 0], dO[0, 0], g[0, 0]
+    T = K_.shape[0]
+    G = dS_T[0, 0].copy()
+    dV = np.zeros_like(v[0, 0])
+    for t0 in reversed(range(0, T, C)):
+        sl = slice(t0, t0 + C)
+        K, Q, D, bt = K_[sl], Q_[sl], dO_[sl], b_[sl]
+        Gc = np.cumsum(g_[sl], axis=0)                   # per-channel log decay from the chunk start
+        n = K.shape[0]
+        ratio = np.exp(Gc[:, None, :] - Gc[None, :, :])  # exp(G_t[c] - G_s[c])
+        A = np.tril(bt[:, None] * np.einsum("tc,sc,tsc->ts", K, K, ratio), -1)
+        Tm = np.linalg.solve(np.eye(n) + A, np.diag(bt))
+        PT = np.tril(np.einsum("tc,sc,tsc->ts", Q, K, ratio)) @ Tm
+        gam, eL = np.exp(Gc), np.exp(Gc[-1])
+        Kh, Kp, Qp = K * (eL / gam), K * gam, Q * gam    # the forward's decayed operands
+        dVc = PT.T @ D + (Kh.T @ Tm).T @ G               # dV^T = dO^T PT + G^T (K^T Tm)
+        dV[sl] = dVc
+        G = eL[:, None] * G + Qp.T @ D - Kp.T @ dVc      # keep on G's key rows, then the update
+    if equal_channels:
+        ref = oracle.backward_gated(q, k, v, beta, g[..., 0], dO, S0, dS_T)
+    else:
+        ref = oracle.backward_kda(q, k, v, beta, g, dO, S0, dS_T)
+    assert _rel(dV, ref[2][0, 0]) < 1e-9
+    assert _rel(G, ref[5][0, 0]) < 1e-9
 
 
 @pytest.mark.parametrize("scale", [1.0, 40.0], ids=["mild", "strong"])

@@ -412,10 +412,12 @@ DN_API size_t dn_chunk_bwd_gated_workspace_bytes(int B, int H, int T, int dk, in
  * "Hardware-efficient implementation", paperlayer.ai/abs/2406.06484v6).
  *   g, d_g  [B, H, T, dk] fp32 (g 16-byte aligned); the rest as dn_chunk_bwd.
  *   workspace  device scratch of dn_chunk_bwd_kda_workspace_bytes(...) bytes.
- * The states are recomputed by the KDA forward (on tcgen05 for bf16 with
- * dk = dv = 128, else on the CUDA cores) and the gradients formed chunk by
- * chunk on the CUDA cores (fp32 products for fp32 I/O, tf32
- * tensor-core products with fp32 accumulation for bf16).  The decay ratios
+ * For bf16 with dk = dv = 128 the states are recomputed and the state
+ * gradient carried on tcgen05 (the tensor-core KDA forward, then a chain
+ * that reads the decayed operands it leaves); otherwise both run on the CUDA
+ * cores.  The per-chunk gradients are formed on the CUDA cores (fp32
+ * products for fp32 I/O, tf32 tensor-core products with fp32 accumulation
+ * for bf16).  The decay ratios
  * exp(G_t[c] - G_s[c]) sit inside the channel sums: as products of
  * exp(G) and exp(-G) scaled operands while a chunk's decay stays within
  * exp(-60) on every channel, else one exponential per ratio.  d_g[t][c] is
